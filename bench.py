@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""Throughput of the fused LM-head + GMPO forward+backward on GB300.
+
+One step = one call of rlloss_fwd_bwd over one batch of the Qwen-0.5B
+LM-head workload (B=1, T=4096, H=896, V=151936, bf16, GMPO eps 0.4/0.4,
+beta 0): forward logits + streamed log-softmax / entropy, loss, and
+dX, dW through tensor-core kernels.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+build) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused LM-head+GMPO fwd+bwd tokens/s at H896/V151936; % bf16 TC peak"
+UNIT = "tokens/s"
+WORKLOAD_INDEX = 1
+REF_SAMPLE_TOKENS = 512
+CPU_BASELINE_TOKENS = 2048
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons with timestamps."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.t0 = time.time()
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                       "-lms", "100", "-i", str(gpu_index)], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        self.marks = []
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        # rows arrive every ~100 ms from t0; keep those overlapping the timed region
+        n = len(rows)
+        t_end = time.time()
+        dt = (t_end - self.t0) / max(n, 1)
+        ts = [self.t0 + (i + 0.5) * dt for i in range(n)]
+        a, b = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (self.t0, t_end)
+        sel = [r for r, t in zip(rows, ts) if a - 0.15 <= t <= b + 0.15] or rows[-2:]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in sel if num(r[1]) is not None]
+        mx = [num(r[2]) for r in sel if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in sel:
+            for k, name in enumerate(names):
+                if len(r) > 5 + k and r[5 + k].strip().lower() == "active":
+                    reasons.add(name)
+        pw = [num(r[3]) for r in sel if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sel),
+                "power_w_max": max(pw) if pw else None}
+
+
+def make_workload(dev):
+    """Seeded inputs on the device; old_logp = policy logp + N(0, 0.3^2) where
+    the policy logp comes from a plain chunked full-logits pass (cuBLAS bf16
+    matmul, fp32 log-softmax) used only to build this input."""
+    import torch
+    from lm_head_log_tma_gb300.workloads import WORKLOADS, make_inputs
+    spec = WORKLOADS[WORKLOAD_INDEX]
+    inp = make_inputs(spec, device=dev)
+    N = spec.N
+    pol = torch.empty(N, dtype=torch.float32, device=dev)
+    with torch.no_grad():
+        for r0 in range(0, N, 1024):
+            z = (inp.X[r0:r0 + 1024] @ inp.W.T).float()
+            if inp.b is not None:
+                z += inp.b.float()
+            z /= spec.temperature
+            pol[r0:r0 + 1024] = z.gather(1, inp.targets[r0:r0 + 1024, None])[:, 0] - torch.logsumexp(z, 1)
+            del z
+    old = inp.old_logp(pol)
+    ref = inp.ref_logp(pol)
+    torch.cuda.synchronize()
+    return spec, inp, old, ref
+
+
+def cfg_for(R, spec):
+    return R.make_cfg(spec.B, spec.T, spec.H, spec.V, dtype=R.BF16 if spec.dtype == "bf16" else R.FP32,
+                      loss_type=spec.loss_type, eps_low=spec.eps_low, eps_high=spec.eps_high, beta=spec.beta,
+                      temperature=spec.temperature, top_entropy_quantile=spec.top_entropy_quantile,
+                      has_bias=spec.has_bias)
+
+
+def oracle_sample_rate(spec, inp, old, ref, tokens):
+    """Oracle fwd+bwd over the last ``tokens`` rows of the batch taken as one
+    sequence.  Returns (tokens/s, seconds, threads)."""
+    import numpy as np
+    import oracle as O
+    n = spec.N
+    r0 = n - tokens
+    X = inp.X[r0:].cpu()
+    W = inp.W.cpu()
+    b = None if inp.b is None else inp.b.cpu()
+    y = inp.targets[r0:].cpu()
+    oldc = old[r0:].cpu()
+    refc = None if ref is None else ref[r0:].cpu()
+    mask = inp.mask[r0:].cpu()
+    adv = inp.adv[:1].cpu()
+    prob = O.Problem(1, tokens, spec.loss_type, spec.eps_low, spec.eps_high, spec.beta, spec.temperature,
+                     spec.top_entropy_quantile)
+    threads = os.cpu_count() or 1
+    t = time.perf_counter()
+    O.fwd_bwd(prob, X, W, b, y, oldc, refc, adv, mask, threads=threads)
+    dt = time.perf_counter() - t
+    return tokens / dt, dt, threads
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if dev == "cuda":
+        torch.cuda.set_device(local)
+    from lm_head_log_tma_gb300.workloads import WORKLOADS, make_inputs
+    spec = WORKLOADS[WORKLOAD_INDEX]
+    inp = make_inputs(spec, device="cpu")
+    # sampler log-probs: any value near the policy's keeps the clip mix realistic;
+    # the oracle's own timing does not depend on it
+    import oracle as O
+    _, lp, _ = O.row_stats(inp.X[-REF_SAMPLE_TOKENS:], inp.W, inp.b, inp.targets[-REF_SAMPLE_TOKENS:],
+                           spec.temperature)
+    pol = torch.zeros(spec.N)
+    pol[-REF_SAMPLE_TOKENS:] = torch.from_numpy(lp).float()
+    old = inp.old_logp(pol)
+    ref = inp.ref_logp(pol)
+    for _ in range(args.warmup):
+        oracle_sample_rate(spec, inp, old, ref, REF_SAMPLE_TOKENS)
+    t = time.perf_counter()
+    threads = os.cpu_count() or 1
+    for _ in range(args.steps):
+        _, _, threads = oracle_sample_rate(spec, inp, old, ref, REF_SAMPLE_TOKENS)
+    dt = time.perf_counter() - t
+    value = REF_SAMPLE_TOKENS * args.steps / dt
+    sample = (f"last {REF_SAMPLE_TOKENS} tokens of the {spec.name} batch as one sequence, full H and V, "
+              f"fp64 numpy oracle fwd+bwd per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": spec.name, "B": spec.B, "T": spec.T, "H": spec.H,
+                                              "V": spec.V, "loss": "gmpo"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from lm_head_log_tma_gb300 import rlloss as R
+
+    spec, inp, old, ref = make_workload(dev)
+    cfg = cfg_for(R, spec)
+    N, H, V = spec.N, spec.H, spec.V
+    ws = R.alloc_workspace(R.rlloss_workspace_bytes(cfg), dev)
+    outs = None
+
+    def step():
+        nonlocal outs
+        outs = R.fwd_bwd(cfg, inp.X, inp.W, inp.b, inp.targets, old, ref, inp.adv, inp.mask, workspace=ws,
+                         outputs=outs)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = R.rlloss_get_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x}")
+
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    R.rlloss_phase_timing(True)
+    n_launch0 = R.rlloss_kernel_launches()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark()
+    barrier()
+    launches = R.rlloss_kernel_launches() - n_launch0
+    phase_ms, phase_n = R.rlloss_phase_times()
+    R.rlloss_phase_timing(False)
+    time.sleep(0.2)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = N * world * args.steps / (ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    host = {k: v.cpu().pin_memory() for k, v in dict(X=inp.X, W=inp.W, targets=inp.targets, old=old,
+                                                       adv=inp.adv, mask=inp.mask).items()}
+    if inp.b is not None:
+        host["b"] = inp.b.cpu().pin_memory()
+    if ref is not None:
+        host["ref"] = ref.cpu().pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    res_host = torch.empty(1 + R.NMETRICS, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = res_host.numel() * 4
+
+    def e2e_step():
+        nonlocal outs
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        outs = R.fwd_bwd(cfg, dbuf["X"], dbuf["W"], dbuf.get("b"), dbuf["targets"], dbuf["old"], dbuf.get("ref"),
+                         dbuf["adv"], dbuf["mask"], workspace=ws, outputs=outs)
+        res_host[:1].copy_(outs["loss"], non_blocking=True)
+        res_host[1:].copy_(outs["metrics"], non_blocking=True)
+        stream.synchronize()
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t
+    if world > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e_value = N * world * e2e_steps / e2e_s
+
+    # ---- roofline of the dominant tensor-core kernel (phase timing, same timed region)
+    peak, peak_sus, hbm, peak_src = load_peaks()
+    per_step = [m / args.steps for m in phase_ms]
+    gemm_phases = {0: "fwd_gemm", 2: "bwd_dlogits", 3: "bwd_dX", 4: "bwd_dW"}
+    dom = max(gemm_phases, key=lambda k: per_step[k])
+    flops_phase = 2.0 * N * H * V          # each of the four GEMM phases does 2NHV per step
+    launches_per_step = max(1, phase_n[dom] // args.steps)
+    achieved = flops_phase / (per_step[dom] / 1e3) / 1e12
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        traffic = json.load(open(tp)).get(gemm_phases[dom])
+    roofline = {"bound": "tensor", "kernel": gemm_phases[dom], "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst", "frac_of_sustained": achieved / peak_sus,
+                "launches_per_step": launches_per_step}
+    step_tflops = 6.0 * N * H * V / (ms_step / 1e3) / 1e12
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": spec.name, "B": spec.B, "T": spec.T, "H": H, "V": V, "loss": "gmpo",
+                       "eps_low": spec.eps_low, "eps_high": spec.eps_high, "beta": spec.beta,
+                       "l2": "inputs larger than L2 (W is 272 MB, dW 545 MB)",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "tc_peak_frac_6nhv": step_tflops / peak,
+            "tc_tflops_6nhv": step_tflops,
+            "roofline": roofline,
+            "phases_ms_per_step": {R.PHASE_NAMES[i]: per_step[i] for i in range(R.NPHASES)},
+            "clocks": clk,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": launches}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, secs, threads = oracle_sample_rate(spec, inp, old, ref, CPU_BASELINE_TOKENS)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"last {CPU_BASELINE_TOKENS} tokens of the batch as one sequence, full "
+                                          f"H and V, fp64 numpy fwd+bwd ({secs:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

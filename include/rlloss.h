@@ -1,0 +1,185 @@
+/*
+ * rlloss — fused LM-head projection + RL policy loss (GMPO, GSPO-token,
+ * top-entropy-quantile mask) with its gradients, for one NVIDIA GB300 GPU.
+ *
+ * C ABI.  Plain pointers and sizes only.  All tensor pointers are DEVICE
+ * pointers owned by the caller; the library never allocates or frees device
+ * memory and keeps no pointer after a call returns.  Every call is
+ * asynchronous on the given CUDA stream (a cudaStream_t passed as void*; NULL
+ * = legacy default stream).  Gradients are overwritten, not accumulated.
+ *
+ * What is computed (sources: the pages' titles and sections):
+ *   logits l = X W^T (+ b)  — "Add GMPO to fused linear GRPO loss", Summary
+ *       (the fused linear path never materialises [tokens, vocab] logits);
+ *   z = l / temperature; per token the target log-prob logp = z_y - lse(z)
+ *       and the entropy H = lse - sum p z, streamed over the vocabulary with
+ *       running (max, sum e^(z-m), sum e^(z-m) z) — "support
+ *       top_entropy_quantile in fused linear GRPO loss", Details;
+ *   optional entropy mask: keep active tokens with H >= quantile(active H,
+ *       1 - q) over the whole batch — same page, Details;
+ *   GMPO: per-token log ratio clipped one-sided in log space to
+ *       [-eps_low, +eps_high] by the sign of the advantage, per-sequence
+ *       geometric mean r_i = exp(masked_mean(clipped lr)), loss
+ *       mean_i(-A_i r_i ebar_i + beta KL_i) with K3 KL — "Add GMPO ...",
+ *       Summary and Details;
+ *   GSPO-token: s_i = exp(masked_mean(logp - old)), token ratio with s_i's
+ *       value and its own log-prob's gradient, loss
+ *       -sum_t min(s A_t, clip(s, 1-eps_low, 1+eps_high) A_t) — Tinker
+ *       "GSPO", the ratio and objective formulas;
+ *   gradients dX, dW, db of the loss through the LM head.
+ *
+ * Layouts (row-major, contiguous): X [N, H], W [V, H], b [V] with N = B*T
+ * (sequence i owns rows i*T .. i*T+T-1); dtype of X, W, b per cfg.dtype
+ * (bf16 or fp32).  targets int64 [N] in [0, V).  old_logp, ref_logp fp32 [N].
+ * adv fp32 [B] (applied on the sequence's active tokens).  mask uint8 [N],
+ * nonzero = completion token (active).  Outputs fp32 unless noted.
+ *
+ * Errors.  Functions return RLLOSS_OK or a synchronous error code BEFORE any
+ * launch (invalid configuration, null or misaligned pointers, too small a
+ * workspace), or RLLOSS_ECUDA when a launch failed.  Problems only visible on
+ * the device (a bounded wait that ran out, a target id outside [0, V), a GSPO
+ * sequence without active tokens, a non-finite loss) are OR-ed into a status
+ * word inside the workspace; read it with rlloss_get_device_status after the
+ * stream has been synchronised.  No kernel traps.
+ */
+#ifndef RLLOSS_H
+#define RLLOSS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define RLLOSS_OK 0
+#define RLLOSS_EINVAL 1        /* invalid configuration, size or pointer */
+#define RLLOSS_EUNSUPPORTED 2  /* valid request this build does not implement */
+#define RLLOSS_EWORKSPACE 3    /* workspace too small or misaligned */
+#define RLLOSS_ECUDA 4         /* a CUDA call or kernel launch failed */
+
+/* device status bits (rlloss_get_device_status) */
+#define RLLOSS_DEV_ETIMEOUT 0x10    /* a bounded on-device wait ran out; results invalid */
+#define RLLOSS_DEV_ENONFINITE 0x20  /* the loss came out NaN or infinite */
+#define RLLOSS_DEV_EBADTARGET 0x40  /* a target id outside [0, V); its logp is NaN */
+#define RLLOSS_DEV_EEMPTYSEQ 0x80   /* GSPO sequence with no active token; it contributes 0 */
+
+/* cfg.dtype */
+#define RLLOSS_BF16 0
+#define RLLOSS_FP32 1
+/* cfg.loss_type */
+#define RLLOSS_GMPO 0
+#define RLLOSS_GSPO_TOKEN 1
+/* cfg.is_level: importance-sampling level.  GMPO clips at token level before
+ * the sequence aggregation, so GMPO with RLLOSS_IS_SEQUENCE is rejected with
+ * RLLOSS_EINVAL ("Add GMPO ...", Details).  GSPO ignores it. */
+#define RLLOSS_IS_TOKEN 0
+#define RLLOSS_IS_SEQUENCE 1
+/* cfg.flags */
+#define RLLOSS_FLAG_FORCE_ENTROPY_PATH 0x1u  /* run the quantile/mask path even at q = 1 */
+
+#define RLLOSS_NMETRICS 8
+/* out_metrics layout:
+ *  [0] clip fraction: GMPO clipped active tokens / active tokens;
+ *      GSPO sequences whose ratio lies strictly outside the clip range / B
+ *      (Tinker "GSPO", Output diagnostics: gspo_clipped_fraction:mean)
+ *  [1] clip count (tokens for GMPO, sequences for GSPO)
+ *  [2] K3 KL mean over active tokens (0 when beta == 0)
+ *  [3] number of active tokens
+ *  [4] entropy threshold (NaN when the mask is off or no token is active)
+ *  [5] active tokens kept by the entropy mask
+ *  [6] mean over sequences of the sequence log ratio (GMPO: mean clipped lr;
+ *      GSPO: log s_i — gspo_sequence_log_ratio:mean)
+ *  [7] mean over sequences of the sequence ratio (GMPO r_i, GSPO s_i)
+ * GMPO means in [6], [7] run over sequences with at least one active token. */
+
+typedef struct {
+  int32_t B, T, H, V;       /* sequences, tokens per sequence, hidden size, vocabulary */
+  int32_t dtype;            /* RLLOSS_BF16 or RLLOSS_FP32 for X, W, b */
+  int32_t loss_type;        /* RLLOSS_GMPO or RLLOSS_GSPO_TOKEN */
+  int32_t is_level;         /* RLLOSS_IS_TOKEN or RLLOSS_IS_SEQUENCE */
+  float eps_low, eps_high;  /* GMPO: log-space bounds [-eps_low, +eps_high] ("Add GMPO ...",
+                               Details); GSPO: ratio clip [1-eps_low, 1+eps_high] (Tinker
+                               "GSPO", Choosing clipping thresholds: 3e-4, 4e-4) */
+  float beta;               /* K3 KL weight; 0 = off (GMPO only) */
+  float temperature;        /* > 0; logits are divided by it before softmax and entropy */
+  float top_entropy_quantile; /* q in [0, 1]; 1 = mask off ("support top_entropy_quantile",
+                                 Details); GMPO only */
+  int32_t has_bias;         /* b present */
+  uint32_t flags;           /* RLLOSS_FLAG_* */
+  int32_t chunk_rows;       /* rows per backward chunk; 0 = library default */
+} rlloss_cfg;
+
+/* Bytes of device workspace rlloss_fwd_bwd needs for cfg (0 if cfg is
+ * invalid).  Depends on the current device's SM count.  Pure host call. */
+size_t rlloss_workspace_bytes(const rlloss_cfg* cfg);
+
+/* Bytes of device workspace rlloss_loss_from_logp needs (0 if invalid). */
+size_t rlloss_loss_workspace_bytes(const rlloss_cfg* cfg);
+
+/* The whole fused path: forward (LM head + streamed log-softmax, target
+ * log-prob, entropy), entropy mask, loss and metrics, and backward.
+ *   X, W: [N,H], [V,H] of cfg.dtype; b: [V] or NULL when !has_bias.
+ *   targets [N] int64; old_logp [N]; ref_logp [N] (NULL when beta == 0);
+ *   adv [B]; mask [N].
+ *   out_loss [1]; out_metrics [RLLOSS_NMETRICS]; dX [N,H] fp32;
+ *   dW [V,H] fp32; db [V] fp32 (NULL when !has_bias; required otherwise).
+ *   out_logp [N], out_entropy [N] fp32 and out_entropy_mask [N] uint8 are
+ *   optional (NULL = not written).
+ *   workspace: device buffer of at least rlloss_workspace_bytes(cfg) bytes,
+ *   256-byte aligned; it also holds the device status word.
+ * Pointers must be 16-byte aligned.  Returns RLLOSS_* codes as above. */
+int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const void* b,
+                   const int64_t* targets, const float* old_logp, const float* ref_logp,
+                   const float* adv, const uint8_t* mask, float* out_loss, float* out_metrics,
+                   float* dX, float* dW, float* db, float* out_logp, float* out_entropy,
+                   uint8_t* out_entropy_mask, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/* The loss stage alone, from given per-token log-probs (no LM head): entropy
+ * mask (if q < 1), loss, metrics and dL/dlogp.
+ *   logp [N] fp32; entropy [N] fp32 (required when q < 1 or the
+ *   FORCE_ENTROPY_PATH flag is set, else may be NULL); old_logp, ref_logp,
+ *   adv, mask as for rlloss_fwd_bwd.  out_dlogp [N] fp32 = dL/dlogp_n
+ *   (optional); out_entropy_mask [N] uint8 (optional).  cfg.H, cfg.V,
+ *   cfg.dtype, cfg.has_bias and cfg.temperature are ignored. */
+int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float* entropy,
+                          const float* old_logp, const float* ref_logp, const float* adv,
+                          const uint8_t* mask, float* out_loss, float* out_metrics,
+                          float* out_dlogp, uint8_t* out_entropy_mask, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Copy the device status word of ``workspace`` (the one a previous call used)
+ * into *status.  Synchronous; call after the stream has finished.  Returns
+ * RLLOSS_ECUDA if the copy failed. */
+int rlloss_get_device_status(const void* workspace, int32_t* status);
+
+/* Launch a kernel that waits on a barrier nothing will complete, with a limit
+ * of limit_ns nanoseconds, so the bounded-wait path can be exercised: the
+ * status word of ``workspace`` (>= 256 bytes) then carries RLLOSS_DEV_ETIMEOUT.
+ * The library has no other use for it. */
+int rlloss_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* stream);
+
+/* Phase timing for benchmarks.  While enabled, rlloss_fwd_bwd records CUDA
+ * events on the caller's stream around its phases:
+ *   0 forward tensor-core kernel, 1 row merge + entropy mask + loss,
+ *   2 backward G producer (all chunks), 3 dX kernels, 4 dW kernels,
+ *   5 everything else (operand split, bias scaling, db).
+ * rlloss_phase_times synchronises on the recorded events, writes the summed
+ * milliseconds and the launch counts per phase (arrays of nphase <= 6), and
+ * clears the record.  rlloss_phase_timing(0/1) switches it off/on and clears. */
+#define RLLOSS_NPHASES 6
+int rlloss_phase_timing(int enable);
+int rlloss_phase_times(float* ms, int32_t* launches, int nphase);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t rlloss_kernel_launches(void);
+
+/* Static description of a code. */
+const char* rlloss_status_str(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RLLOSS_H */

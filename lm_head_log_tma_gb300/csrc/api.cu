@@ -1,0 +1,661 @@
+// Host side of the C ABI declared in include/rlloss.h: validation, the
+// work plan (tiles, vocabulary segments, backward chunks), the workspace
+// layout, TMA tensor maps and the launch sequence on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <mutex>
+#include <vector>
+#include <cstdint>
+#include <cstring>
+
+#include "kernels.h"
+#include "status.h"
+
+namespace {
+
+using namespace rl;
+
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
+constexpr size_t kPartialCapBytes = size_t(64) << 20;
+constexpr int kDefaultChunk = 8192;
+
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+inline long long rup(long long a, long long b) { return cdiv(a, b) * b; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return sms;
+}
+
+bool finite(float x) { return std::isfinite(x); }
+
+int validate_common(const rlloss_cfg* c) {
+  if (!c) return RLLOSS_EINVAL;
+  if (c->B < 1 || c->T < 1) return RLLOSS_EINVAL;
+  if ((long long)c->B * c->T > (1ll << 31) - 1) return RLLOSS_EINVAL;
+  if (c->loss_type != RLLOSS_GMPO && c->loss_type != RLLOSS_GSPO_TOKEN) return RLLOSS_EINVAL;
+  if (c->is_level != RLLOSS_IS_TOKEN && c->is_level != RLLOSS_IS_SEQUENCE) return RLLOSS_EINVAL;
+  if (c->loss_type == RLLOSS_GMPO && c->is_level == RLLOSS_IS_SEQUENCE) return RLLOSS_EINVAL;
+  if (!finite(c->eps_low) || !finite(c->eps_high) || c->eps_low < 0.f || c->eps_high < 0.f) return RLLOSS_EINVAL;
+  if (!finite(c->beta)) return RLLOSS_EINVAL;
+  const float q = c->top_entropy_quantile;
+  if (!(q >= 0.f && q <= 1.f)) return RLLOSS_EINVAL;
+  if (c->flags & ~RLLOSS_FLAG_FORCE_ENTROPY_PATH) return RLLOSS_EINVAL;
+  if (c->loss_type == RLLOSS_GSPO_TOKEN) {
+    if (c->beta != 0.f) return RLLOSS_EUNSUPPORTED;
+    if (q < 1.f || (c->flags & RLLOSS_FLAG_FORCE_ENTROPY_PATH)) return RLLOSS_EUNSUPPORTED;
+  }
+  return RLLOSS_OK;
+}
+
+int validate_full(const rlloss_cfg* c) {
+  int e = validate_common(c);
+  if (e) return e;
+  if (c->H < 1 || c->V < 1) return RLLOSS_EINVAL;
+  if (c->dtype != RLLOSS_BF16 && c->dtype != RLLOSS_FP32) return RLLOSS_EINVAL;
+  if (!(c->temperature > 0.f) || !finite(c->temperature)) return RLLOSS_EINVAL;
+  if (c->has_bias != 0 && c->has_bias != 1) return RLLOSS_EINVAL;
+  if (c->chunk_rows < 0) return RLLOSS_EINVAL;
+  if (c->dtype == RLLOSS_BF16 && (c->H % 8) != 0) return RLLOSS_EUNSUPPORTED;  // TMA row stride: 16 bytes
+  if (c->H > 65536 || c->V > (1 << 30)) return RLLOSS_EUNSUPPORTED;
+  return RLLOSS_OK;
+}
+
+bool entropy_path(const rlloss_cfg* c) {
+  return c->top_entropy_quantile < 1.f || (c->flags & RLLOSS_FLAG_FORCE_ENTROPY_PATH);
+}
+
+struct Plan {
+  int B, T, N, H, V, sms;
+  bool fp32, bias, ent;
+  int R, Vt, P, Hp, Vp;
+  int kb_fwd, nseg_fwd;     // forward K: nseg_fwd * kb_fwd k-blocks
+  int Kx;                   // row width (elements) of the bf16 X / W operand arrays
+  int Nc, nchunks, ld_dl;
+  // workspace offsets
+  size_t o_status, o_partial, o_lse2, o_logp64, o_ent, o_coef, o_emask, o_k3, o_seq, o_bias2, o_dl, o_x3, o_w3,
+      o_dxpart, o_dbpart, total;
+};
+
+// k splits of the dX GEMM when its tiles alone would leave SMs idle; the
+// partial slices are summed in a fixed order afterwards.  At most one split
+// per k-block, so every slice is written.
+int dx_splits(int H, int nc, int kblocks, int sms) {
+  const long long tiles = cdiv(H, 128) * cdiv(nc, 256);
+  if (tiles >= sms) return 1;
+  int best_s = 1;
+  double best = 1e30;
+  for (int s = 1; s <= std::min(16, kblocks); ++s) {
+    const double t = double(cdiv(tiles * s, sms)) / s;
+    if (t < best - 1e-9) {
+      best = t;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
+int choose_segments(int R, int Vt, int G, long long N) {
+  int best = 1;
+  long long best_t = -1;
+  for (int P = 1; P <= std::min(64, Vt); ++P) {
+    if (P > 1 && size_t(N) * 2 * P * 32 > kPartialCapBytes) break;
+    const long long waves = cdiv((long long)R * P, G);
+    const long long t = waves * cdiv(Vt, P);
+    if (best_t < 0 || t < best_t) {
+      best_t = t;
+      best = P;
+    }
+  }
+  return best;
+}
+
+Plan make_plan(const rlloss_cfg* c, bool loss_only) {
+  Plan p{};
+  p.B = c->B;
+  p.T = c->T;
+  p.N = c->B * c->T;
+  p.sms = device_sms();
+  p.ent = entropy_path(c);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  p.o_status = take(256);
+  if (!loss_only) {
+    p.H = c->H;
+    p.V = c->V;
+    p.fp32 = c->dtype == RLLOSS_FP32;
+    p.bias = c->has_bias != 0;
+    p.R = int(cdiv(p.N, 128));
+    p.Vt = int(cdiv(p.V, 256));
+    p.P = choose_segments(p.R, p.Vt, p.sms, p.N);
+    p.Hp = int(rup(p.H, 64));
+    p.Vp = int(rup(p.V, 64));
+    if (p.fp32) {
+      p.nseg_fwd = 6;
+      p.kb_fwd = p.Hp / 64;
+      p.Kx = 3 * p.Hp;
+    } else {
+      p.nseg_fwd = 1;
+      p.kb_fwd = int(cdiv(p.H, 64));
+      p.Kx = p.H;
+    }
+    const int want = c->chunk_rows > 0 ? int(rup(c->chunk_rows, 128)) : kDefaultChunk;
+    p.Nc = int(std::min<long long>(want, rup(p.N, 128)));
+    p.nchunks = int(cdiv(p.N, p.Nc));
+    p.ld_dl = p.fp32 ? 2 * p.Vp : p.Vp;
+    p.o_partial = take(size_t(p.N) * 2 * p.P * 32);
+    p.o_lse2 = take(size_t(p.N) * 4);
+    p.o_logp64 = take(size_t(p.N) * 8);
+    p.o_ent = take(size_t(p.N) * 4);
+    p.o_coef = take(size_t(p.N) * 4);
+  }
+  p.o_emask = take(size_t(p.N));
+  p.o_k3 = take(kK3Bytes);
+  p.o_seq = take(size_t(p.B) * 64);
+  if (!loss_only) {
+    p.o_bias2 = take(p.bias ? size_t(p.Vt) * 256 * 4 : 0);
+    p.o_dl = take(size_t(p.Nc) * p.ld_dl * 2);
+    p.o_x3 = take(p.fp32 ? size_t(p.N) * 3 * p.Hp * 2 : 0);
+    p.o_w3 = take(p.fp32 ? size_t(p.V) * 3 * p.Hp * 2 : 0);
+    size_t dxp = 0;
+    for (int nc : {p.Nc, p.N - (p.nchunks - 1) * p.Nc}) {
+      const int sp = dx_splits(p.H, nc, (p.fp32 ? 3 : 1) * int(cdiv(p.V, 64)), p.sms);
+      if (sp > 1) dxp = std::max(dxp, size_t(sp) * nc * p.H * 4);
+    }
+    p.o_dxpart = take(dxp);
+    p.o_dbpart = take(p.bias ? size_t(db_part_rows(p.Nc)) * p.V * 4 : 0);
+  }
+  p.total = off;
+  return p;
+}
+
+// ------------------------------------------------------------------ instrumentation
+std::atomic<uint64_t> g_launches{0};
+
+struct PhaseRec {
+  int phase;
+  int launches;
+  cudaEvent_t a, b;
+};
+struct PhaseTimer {
+  std::mutex mu;
+  bool on = false;
+  std::vector<PhaseRec> recs;
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+PhaseTimer g_timer;
+
+// Records an event pair around one phase when timing is on; counts launches.
+struct Phase {
+  cudaStream_t st;
+  int phase;
+  int n = 0;
+  cudaEvent_t a = nullptr;
+  Phase(cudaStream_t s, int ph) : st(s), phase(ph) {
+    std::lock_guard<std::mutex> g(g_timer.mu);
+    if (g_timer.on) {
+      a = g_timer.get();
+      cudaEventRecord(a, st);
+    }
+  }
+  void launched(int k = 1) {
+    n += k;
+    g_launches += uint64_t(k);
+  }
+  ~Phase() {
+    std::lock_guard<std::mutex> g(g_timer.mu);
+    if (a) {
+      cudaEvent_t b = g_timer.get();
+      cudaEventRecord(b, st);
+      g_timer.recs.push_back(PhaseRec{phase, n, a, b});
+    }
+  }
+};
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 map, 128-byte swizzle, box {64, box_outer}; OOB reads return 0.
+bool tmap_bf16(CUtensorMap* m, const void* base, long long inner, long long outer, long long row_elems,
+               int box_outer) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+  const cuuint64_t strides[1] = {cuuint64_t(row_elems) * 2};
+  const cuuint32_t box[2] = {64u, cuuint32_t(box_outer)};
+  const cuuint32_t es[2] = {1u, 1u};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? RLLOSS_OK : RLLOSS_ECUDA; }
+#define RL_TRY(x)                    \
+  do {                               \
+    cudaError_t _e = (x);            \
+    if (_e != cudaSuccess) return RLLOSS_ECUDA; \
+  } while (0)
+
+LossParams loss_params(const rlloss_cfg* c, const Plan& p, char* ws) {
+  LossParams lp{};
+  lp.B = c->B;
+  lp.T = c->T;
+  lp.loss_type = c->loss_type;
+  lp.eps_low = double(c->eps_low);
+  lp.eps_high = double(c->eps_high);
+  lp.clip_lo = double(1.0f - c->eps_low);
+  lp.clip_hi = double(1.0f + c->eps_high);
+  lp.beta = double(c->beta);
+  lp.inv_tau = 1.0 / double(c->temperature > 0.f ? c->temperature : 1.f);
+  lp.seqres = reinterpret_cast<double*>(ws + p.o_seq);
+  lp.ticket = reinterpret_cast<unsigned int*>(ws + p.o_status + 4);
+  lp.status = reinterpret_cast<int*>(ws + p.o_status);
+  lp.k3 = p.ent ? reinterpret_cast<const double*>(ws + p.o_k3) : nullptr;
+  return lp;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t rlloss_workspace_bytes(const rlloss_cfg* cfg) {
+  if (validate_full(cfg) != RLLOSS_OK) return 0;
+  return make_plan(cfg, false).total;
+}
+
+size_t rlloss_loss_workspace_bytes(const rlloss_cfg* cfg) {
+  if (validate_common(cfg) != RLLOSS_OK) return 0;
+  return make_plan(cfg, true).total;
+}
+
+const char* rlloss_status_str(int code) {
+  switch (code) {
+    case RLLOSS_OK: return "ok";
+    case RLLOSS_EINVAL: return "invalid argument";
+    case RLLOSS_EUNSUPPORTED: return "unsupported configuration";
+    case RLLOSS_EWORKSPACE: return "workspace too small or misaligned";
+    case RLLOSS_ECUDA: return "CUDA error";
+    case RLLOSS_DEV_ETIMEOUT: return "device: bounded wait ran out";
+    case RLLOSS_DEV_ENONFINITE: return "device: non-finite loss";
+    case RLLOSS_DEV_EBADTARGET: return "device: target id out of range";
+    case RLLOSS_DEV_EEMPTYSEQ: return "device: sequence without active tokens";
+    default: return "unknown status";
+  }
+}
+
+int rlloss_phase_timing(int enable) {
+  std::lock_guard<std::mutex> g(g_timer.mu);
+  for (PhaseRec& r : g_timer.recs) {
+    g_timer.pool.push_back(r.a);
+    g_timer.pool.push_back(r.b);
+  }
+  g_timer.recs.clear();
+  g_timer.on = enable != 0;
+  return RLLOSS_OK;
+}
+
+int rlloss_phase_times(float* ms, int32_t* launches, int nphase) {
+  if (!ms || nphase < 1 || nphase > RLLOSS_NPHASES) return RLLOSS_EINVAL;
+  std::lock_guard<std::mutex> g(g_timer.mu);
+  for (int i = 0; i < nphase; ++i) {
+    ms[i] = 0.f;
+    if (launches) launches[i] = 0;
+  }
+  int rc = RLLOSS_OK;
+  for (PhaseRec& r : g_timer.recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      rc = RLLOSS_ECUDA;
+    if (r.phase >= 0 && r.phase < nphase) {
+      ms[r.phase] += t;
+      if (launches) launches[r.phase] += r.launches;
+    }
+    g_timer.pool.push_back(r.a);
+    g_timer.pool.push_back(r.b);
+  }
+  g_timer.recs.clear();
+  return rc;
+}
+
+uint64_t rlloss_kernel_launches(void) { return g_launches.load(); }
+
+int rlloss_get_device_status(const void* workspace, int32_t* status) {
+  if (!workspace || !status) return RLLOSS_EINVAL;
+  return cuda_rc(cudaMemcpy(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost));
+}
+
+int rlloss_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* stream) {
+  if (!workspace || !aligned(workspace, 256)) return RLLOSS_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RL_TRY(cudaMemsetAsync(workspace, 0, 256, st));
+  RL_TRY(launch_selftest_wait(static_cast<int*>(workspace), limit_ns, st));
+  g_launches += 1;
+  return RLLOSS_OK;
+}
+
+int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float* entropy, const float* old_logp,
+                          const float* ref_logp, const float* adv, const uint8_t* mask, float* out_loss,
+                          float* out_metrics, float* out_dlogp, uint8_t* out_entropy_mask, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  int e = validate_common(cfg);
+  if (e) return e;
+  if (!logp || !old_logp || !adv || !mask || !out_loss || !out_metrics || !workspace) return RLLOSS_EINVAL;
+  if (cfg->beta != 0.f && !ref_logp) return RLLOSS_EINVAL;
+  const Plan p = make_plan(cfg, true);
+  if (p.ent && !entropy) return RLLOSS_EINVAL;
+  if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, 256, st));
+  uint8_t* emask = reinterpret_cast<uint8_t*>(ws + p.o_emask);
+  if (p.ent) {
+    RL_TRY(launch_entropy_mask(entropy, mask, p.N, double(cfg->top_entropy_quantile), ws + p.o_k3, emask, st));
+    g_launches += 9;
+  }
+  LossParams lp = loss_params(cfg, p, ws);
+  lp.logp = logp;
+  lp.logp_is_f64 = 0;
+  lp.old_logp = old_logp;
+  lp.ref_logp = ref_logp;
+  lp.adv = adv;
+  lp.mask = mask;
+  lp.emask = p.ent ? emask : nullptr;
+  lp.dlogp = out_dlogp;
+  lp.out_loss = out_loss;
+  lp.out_metrics = out_metrics;
+  RL_TRY(launch_loss(lp, st));
+  g_launches += 1;
+  if (out_entropy_mask)
+    RL_TRY(cudaMemcpyAsync(out_entropy_mask, p.ent ? emask : mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
+  return RLLOSS_OK;
+}
+
+int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const void* b, const int64_t* targets,
+                   const float* old_logp, const float* ref_logp, const float* adv, const uint8_t* mask,
+                   float* out_loss, float* out_metrics, float* dX, float* dW, float* db, float* out_logp,
+                   float* out_entropy, uint8_t* out_entropy_mask, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  int e = validate_full(cfg);
+  if (e) return e;
+  if (!X || !W || !targets || !old_logp || !adv || !mask || !out_loss || !out_metrics || !dX || !dW || !workspace)
+    return RLLOSS_EINVAL;
+  if (cfg->has_bias && (!b || !db)) return RLLOSS_EINVAL;
+  if (cfg->beta != 0.f && !ref_logp) return RLLOSS_EINVAL;
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16)) return RLLOSS_EINVAL;
+  const Plan p = make_plan(cfg, false);
+  if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
+  if (!encode_fn()) return RLLOSS_ECUDA;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + p.o_status);
+  const float scale2 = float(1.4426950408889634 / double(cfg->temperature));
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, 256, st));
+
+  // Operand arrays: bf16 inputs are used in place; fp32 inputs are split
+  // into three bf16 terms (hi, mid, lo) so the same bf16 tensor-core kernels
+  // reach fp32-level accuracy (six of the nine term products are kept).
+  const void* Xop = X;
+  const void* Wop = W;
+  if (p.fp32) {
+    __nv_bfloat16* x3 = reinterpret_cast<__nv_bfloat16*>(ws + p.o_x3);
+    __nv_bfloat16* w3 = reinterpret_cast<__nv_bfloat16*>(ws + p.o_w3);
+    Phase ph(st, 5);
+    RL_TRY(launch_split3(static_cast<const float*>(X), p.N, p.H, p.Hp, x3, st));
+    RL_TRY(launch_split3(static_cast<const float*>(W), p.V, p.H, p.Hp, w3, st));
+    ph.launched(2);
+    Xop = x3;
+    Wop = w3;
+  }
+  const float* bias2 = nullptr;
+  if (p.bias) {
+    float* b2 = reinterpret_cast<float*>(ws + p.o_bias2);
+    Phase ph(st, 5);
+    RL_TRY(launch_bias2(b, p.fp32 ? 1 : 0, p.V, p.Vt * 256, scale2, b2, st));
+    ph.launched();
+    bias2 = b2;
+  }
+  // K-segments of the forward / recompute GEMM: products of the split terms.
+  int seg_a[kMaxSeg] = {0, 0, 0, 0, 0, 0}, seg_b[kMaxSeg] = {0, 0, 0, 0, 0, 0};
+  if (p.fp32) {
+    const int hp = p.Hp;
+    const int sa[6] = {0, 0, hp, 0, hp, 2 * hp};   // hi*hi, hi*mid, mid*hi, hi*lo, mid*mid, lo*hi
+    const int sb[6] = {0, hp, 0, 2 * hp, hp, 0};
+    std::memcpy(seg_a, sa, sizeof(sa));
+    std::memcpy(seg_b, sb, sizeof(sb));
+  }
+
+  // ---- forward: tensor-core logits + streamed row state
+  FwdParams fp{};
+  if (!tmap_bf16(&fp.tmA, Xop, p.Kx, p.N, p.Kx, 128)) return RLLOSS_ECUDA;
+  if (!tmap_bf16(&fp.tmB, Wop, p.Kx, p.V, p.Kx, 256)) return RLLOSS_ECUDA;
+  fp.nseg = p.nseg_fwd;
+  fp.kb_per_seg = p.kb_fwd;
+  std::memcpy(fp.seg_a, seg_a, sizeof(seg_a));
+  std::memcpy(fp.seg_b, seg_b, sizeof(seg_b));
+  fp.N = p.N;
+  fp.V = p.V;
+  fp.R = p.R;
+  fp.Vt = p.Vt;
+  fp.P = p.P;
+  fp.scale2 = scale2;
+  fp.bias2 = bias2;
+  fp.targets = targets;
+  fp.partial = reinterpret_cast<float4*>(ws + p.o_partial);
+  fp.status = status;
+  fp.limit_ns = kWaitLimitNs;
+  {
+    Phase ph(st, 0);
+    RL_TRY(launch_fwd(fp, std::min(p.sms, p.R * p.P), st));
+    ph.launched();
+  }
+
+  MergeParams mp{};
+  LossParams lp{};
+  {
+  Phase ph_loss(st, 1);
+  mp.partial = fp.partial;
+  mp.N = p.N;
+  mp.V = p.V;
+  mp.slots = 2 * p.P;
+  mp.targets = targets;
+  mp.lse2 = reinterpret_cast<float*>(ws + p.o_lse2);
+  mp.logp64 = reinterpret_cast<double*>(ws + p.o_logp64);
+  mp.ent32 = reinterpret_cast<float*>(ws + p.o_ent);
+  mp.out_logp = out_logp;
+  mp.out_ent = out_entropy;
+  mp.status = status;
+  RL_TRY(launch_merge(mp, st));
+  ph_loss.launched();
+
+  // ---- entropy mask and loss
+  uint8_t* emask = reinterpret_cast<uint8_t*>(ws + p.o_emask);
+  if (p.ent) {
+    RL_TRY(launch_entropy_mask(mp.ent32, mask, p.N, double(cfg->top_entropy_quantile), ws + p.o_k3, emask, st));
+    ph_loss.launched(9);
+  }
+  lp = loss_params(cfg, p, ws);
+  lp.logp = mp.logp64;
+  lp.logp_is_f64 = 1;
+  lp.old_logp = old_logp;
+  lp.ref_logp = ref_logp;
+  lp.adv = adv;
+  lp.mask = mask;
+  lp.emask = p.ent ? emask : nullptr;
+  lp.coef = reinterpret_cast<float*>(ws + p.o_coef);
+  lp.out_loss = out_loss;
+  lp.out_metrics = out_metrics;
+  RL_TRY(launch_loss(lp, st));
+  ph_loss.launched();
+  if (out_entropy_mask)
+    RL_TRY(cudaMemcpyAsync(out_entropy_mask, p.ent ? emask : mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
+  }
+
+  // ---- backward, one chunk of rows at a time:
+  //      G = (c/tau)(onehot - p) as bf16, dX = G W, dW += G^T X, db += sum G.
+  __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dl);
+  const int lo_off = p.fp32 ? p.Vp : 0;
+  const int Mt = int(cdiv(p.H, 128));
+  for (int ch = 0; ch < p.nchunks; ++ch) {
+    const int n0 = ch * p.Nc;
+    const int nc = std::min(p.Nc, p.N - n0);
+    const int Rc = int(cdiv(nc, 128));
+
+    DlParams dp{};
+    dp.tmA = fp.tmA;
+    dp.tmB = fp.tmB;
+    dp.nseg = fp.nseg;
+    dp.kb_per_seg = fp.kb_per_seg;
+    std::memcpy(dp.seg_a, seg_a, sizeof(seg_a));
+    std::memcpy(dp.seg_b, seg_b, sizeof(seg_b));
+    dp.n0 = n0;
+    dp.Nc = nc;
+    dp.Rc = Rc;
+    dp.V = p.V;
+    dp.Vp = p.Vp;
+    dp.Vt = p.Vt;
+    dp.scale2 = scale2;
+    dp.bias2 = bias2;
+    dp.targets = targets;
+    dp.lse2 = mp.lse2;
+    dp.coef = lp.coef;
+    dp.dl = dl;
+    dp.ld = p.ld_dl;
+    dp.lo_off = lo_off;
+    dp.status = status;
+    dp.limit_ns = kWaitLimitNs;
+    {
+      Phase ph(st, 2);
+      RL_TRY(launch_dl(dp, std::min(p.sms, Rc * p.Vt), st));
+      ph.launched();
+    }
+
+    // dX rows of this chunk: dX^T[h, n] = sum_v W[v, h] G[n, v]
+    {
+      TParams tp{};
+      const long long a_inner = p.fp32 ? 3ll * p.Hp : p.H;
+      if (!tmap_bf16(&tp.tmA, Wop, a_inner, p.V, a_inner, 64)) return RLLOSS_ECUDA;
+      const long long b_inner = p.fp32 ? 2ll * p.Vp : p.V;
+      if (!tmap_bf16(&tp.tmB, dl, b_inner, nc, p.ld_dl, 256)) return RLLOSS_ECUDA;
+      tp.kb_per_seg = int(cdiv(p.V, 64));
+      if (p.fp32) {
+        tp.nseg = 3;   // G_hi*W_hi, G_hi*W_mid, G_lo*W_hi
+        tp.seg_a[0] = 0; tp.seg_b[0] = 0;
+        tp.seg_a[1] = p.Hp; tp.seg_b[1] = 0;
+        tp.seg_a[2] = 0; tp.seg_b[2] = p.Vp;
+      } else {
+        tp.nseg = 1;
+      }
+      tp.Mt = Mt;
+      tp.Nt = int(cdiv(nc, 256));
+      const int tiles = tp.Mt * tp.Nt;
+      const int splits = dx_splits(p.H, nc, tp.nseg * tp.kb_per_seg, p.sms);
+      tp.splits = splits;
+      tp.Hout = p.H;
+      tp.Ncols = nc;
+      tp.ldo = p.H;
+      float* dx_rows = dX + size_t(n0) * p.H;
+      if (splits > 1) {
+        tp.out = reinterpret_cast<float*>(ws + p.o_dxpart);
+        tp.split_stride = (long long)nc * p.H;
+        tp.mode = 2;
+      } else {
+        tp.out = dx_rows;
+        tp.mode = 0;
+      }
+      tp.status = status;
+      tp.limit_ns = kWaitLimitNs;
+      Phase ph(st, 3);
+      RL_TRY(launch_gemmT(tp, 0, std::min(p.sms, tiles * splits), st));
+      ph.launched();
+      if (splits > 1) {
+        RL_TRY(launch_sum_slices(tp.out, splits, (long long)nc * p.H, dx_rows, st));
+        ph.launched();
+      }
+    }
+    // dW (+)= over this chunk: dW^T[h, v] = sum_n X[n, h] G[n, v]
+    {
+      TParams tp{};
+      const long long a_inner = p.fp32 ? 3ll * p.Hp : p.H;
+      if (!tmap_bf16(&tp.tmA, Xop, a_inner, p.N, a_inner, 64)) return RLLOSS_ECUDA;
+      const long long b_inner = p.fp32 ? 2ll * p.Vp : p.V;
+      if (!tmap_bf16(&tp.tmB, dl, b_inner, nc, p.ld_dl, 64)) return RLLOSS_ECUDA;
+      tp.kb_per_seg = int(cdiv(nc, 64));
+      if (p.fp32) {
+        tp.nseg = 3;   // X_hi*G_hi, X_mid*G_hi, X_hi*G_lo
+        tp.seg_a[0] = 0; tp.seg_b[0] = 0;
+        tp.seg_a[1] = p.Hp; tp.seg_b[1] = 0;
+        tp.seg_a[2] = 0; tp.seg_b[2] = p.Vp;
+      } else {
+        tp.nseg = 1;
+      }
+      tp.a_outer0 = n0;
+      tp.b_outer0 = 0;
+      tp.Mt = Mt;
+      tp.Nt = p.Vt;
+      tp.splits = 1;
+      tp.Hout = p.H;
+      tp.Ncols = p.V;
+      tp.out = dW;
+      tp.ldo = p.H;
+      tp.mode = ch == 0 ? 0 : 1;
+      tp.status = status;
+      tp.limit_ns = kWaitLimitNs;
+      Phase ph(st, 4);
+      RL_TRY(launch_gemmT(tp, 1, std::min(p.sms, tp.Mt * tp.Nt), st));
+      ph.launched();
+    }
+    if (p.bias) {
+      Phase ph(st, 5);
+      RL_TRY(launch_db(dl, p.ld_dl, lo_off, nc, p.V, reinterpret_cast<float*>(ws + p.o_dbpart), db, ch > 0, st));
+      ph.launched(2);
+    }
+  }
+  return RLLOSS_OK;
+}
+
+}  // extern "C"

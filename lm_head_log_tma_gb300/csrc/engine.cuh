@@ -1,0 +1,191 @@
+// Persistent, warp-specialised tcgen05 GEMM engine for sm_103a.
+//
+//   warp 0 (one lane)  : TMA producer, fills a ring of shared-memory stages
+//   warp 1 (one lane)  : MMA issuer, tcgen05.mma into one of two TMEM
+//                        accumulators (128 lanes x BN fp32 columns each)
+//   warp 2             : TMEM allocation / release
+//   warps 4..11        : epilogue; warp w reads TMEM lanes 32*(w%4)..+31 and
+//                        column half (w-4)/4 of the accumulator
+//
+// A policy class supplies the tile schedule, the TMA loads of one k-block,
+// the shared-memory descriptors of one K=16 step and the epilogue.  Every
+// wait is bounded (see mbar_wait); when one role gives up, the others stop at
+// their next wait, in-flight copies and MMAs are drained, TMEM is released
+// and the kernel returns with RLLOSS_DEV_ETIMEOUT in the status word.
+#pragma once
+#include "ptx.cuh"
+
+namespace rl {
+
+constexpr int kEngineThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kTmemCols = 512;
+
+struct TileInfo {
+  int m0;        // first row of the 128-row accumulator (A rows)
+  int n0;        // first column of the accumulator (B rows)
+  int kb_begin;  // k-block range
+  int kb_end;
+  int unit;      // policy-defined work-unit id
+  int seg;       // policy-defined segment id
+  bool first;    // first tile of its unit
+  bool last;     // last tile of its unit
+};
+
+// Wait that ignores the abort flag; used only to drain in-flight work.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+template <class P>
+__host__ __device__ constexpr int engine_smem_bytes() {
+  return 1024 /*alignment slack*/ + P::kStages * (P::kABytes + P::kBBytes) + 256 /*barriers*/ +
+         P::kExtraSmem;
+}
+
+template <class P>
+__global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __grid_constant__ typename P::Params prm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int S = P::kStages;
+  constexpr int SB = P::kABytes + P::kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * SB);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = bars + 2 * S + 2;
+  uint64_t* drain = bars + 2 * S + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  int* abort_i = reinterpret_cast<int*>(tmem_slot + 1);
+  uint8_t* extra = smem + S * SB + 256;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_i = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  P::cta_setup(prm, extra);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const AbortCtl ac{abort_i, prm.status, prm.limit_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      P::prefetch(prm);
+      int stage = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      P::for_each_tile(prm, [&](const TileInfo& t) -> bool {
+        for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u, ac)) return ok = false;
+          mbar_expect_tx(&full[stage], SB);
+          P::load(prm, smem + stage * SB, &full[stage], t, kb);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        return true;
+      });
+      if (!ok) {
+        // Let every copy this thread started land before the CTA can exit.
+        for (int j = 0; j < S && j < issued; ++j) {
+          if (--stage < 0) {
+            stage = S - 1;
+            ph ^= 1u;
+          }
+          mbar_wait_drain(&full[stage], ph, 20000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aph = 0;
+      bool ok = true;
+      P::for_each_tile(prm, [&](const TileInfo& t) -> bool {
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, ac)) return ok = false;
+        tc_fence_after();
+        const uint32_t d = tmem + uint32_t(acc * P::kBN);
+        for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
+          if (!mbar_wait(&full[stage], ph, ac)) return ok = false;
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * SB);
+#pragma unroll
+          for (int k = 0; k < P::kK16; ++k) {
+            umma_bf16(d, P::adesc(sa, k), P::bdesc(sa, k), P::kIdesc, (kb > t.kb_begin || k > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1u;
+        }
+        return true;
+      });
+      if (!ok) {
+        umma_commit(drain);
+        mbar_wait_drain(drain, 0, 20000000ull);
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    const int q = warp & 3;
+    const int half = (warp - kEpiWarp0) >> 2;
+    int acc = 0;
+    uint32_t aph = 0;
+    typename P::EpiState st;
+    P::for_each_tile(prm, [&](const TileInfo& t) -> bool {
+      const bool got = mbar_wait(&tfull[acc], aph, ac);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      tc_fence_after();
+      P::epilogue(prm, st, t, tmem + uint32_t(acc * P::kBN) + (uint32_t(q * 32) << 16), q, half, lane, extra);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aph ^= 1u;
+      }
+      return true;
+    });
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace rl

@@ -1,0 +1,528 @@
+// Tensor-core kernels of the fused LM-head path.
+//
+//  fwd   : S = X W^T tile by tile (128 tokens x 256 vocab, K = H), epilogue
+//          folds each tile into per-row streaming log-softmax state
+//          (reference max, sum 2^(t-m), sum 2^(t-m)(t-m), target logit) —
+//          "support top_entropy_quantile in fused linear GRPO loss", Details
+//          (second online accumulator next to the running max and sum).
+//  merge : combines the partial row states of the vocabulary segments into
+//          lse, logp and entropy per token.
+//  dl    : recomputes S for a chunk of rows and writes
+//          G = dL/dl = (c/tau)(onehot(y) - p) as bf16 (p = softmax(S/tau)).
+//  gemmT : C^T[h, col] = sum_k A[k, h] B[col, k] with h on the TMEM lanes;
+//          dX^T = W^T G^T (k = vocab) and dW^T = X^T G (k = tokens).
+#include <cuda_runtime.h>
+
+#include "engine.cuh"
+#include "kernels.h"
+
+namespace rl {
+
+// =============================================================== forward
+struct FwdPolicy {
+  static constexpr int kStages = 4;
+  static constexpr int kBN = 256;
+  static constexpr int kK16 = 4;
+  static constexpr int kABytes = 128 * 64 * 2;
+  static constexpr int kBBytes = 256 * 64 * 2;
+  static constexpr int kExtraSmem = 0;
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, 0, 0);
+  using Params = FwdParams;
+
+  struct EpiState {
+    float mref, s_hi, s_lo, w_hi, w_lo, zy;
+    int found, y;
+  };
+
+  __device__ static void cta_setup(const Params&, uint8_t*) {}
+  __device__ static void prefetch(const Params& p) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+
+  // Units u = seg * R + r (row tile r, vocabulary segment seg), dealt
+  // round-robin to the CTAs so that CTAs running at the same time share the
+  // same W tiles (L2 reuse) while each keeps its own rows.
+  template <class F>
+  __device__ static void for_each_tile(const Params& p, F&& f) {
+    const int units = p.R * p.P;
+    const int kbs = p.nseg * p.kb_per_seg;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int seg = u / p.R;
+      const int r = u - seg * p.R;
+      const int j0 = int((long long)seg * p.Vt / p.P);
+      const int j1 = int((long long)(seg + 1) * p.Vt / p.P);
+      for (int j = j0; j < j1; ++j) {
+        TileInfo t{r * 128, j * 256, 0, kbs, u, seg, j == j0, j == j1 - 1};
+        if (!f(t)) return;
+      }
+    }
+  }
+
+  __device__ static void load(const Params& p, uint8_t* st, uint64_t* bar, const TileInfo& t, int kb) {
+    const int s = kb / p.kb_per_seg;
+    const int kk = (kb - s * p.kb_per_seg) * 64;
+    tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0);
+    tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+  }
+  __device__ static uint64_t adesc(uint32_t sa, int k) { return sdesc_sw128(sa + k * 32, 16, 1024); }
+  __device__ static uint64_t bdesc(uint32_t sa, int k) { return sdesc_sw128(sa + kABytes + k * 32, 16, 1024); }
+
+  __device__ static void epilogue(const Params& p, EpiState& e, const TileInfo& t, uint32_t taddr, int q, int half,
+                                  int lane, uint8_t*) {
+    const int row = t.m0 + q * 32 + lane;
+    if (t.first) {
+      e.mref = -INFINITY;
+      e.s_hi = e.s_lo = e.w_hi = e.w_lo = 0.f;
+      e.zy = 0.f;
+      e.found = 0;
+      e.y = row < p.N ? int(p.targets[row]) : -1;
+    }
+    const float sc = p.scale2;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      const int c0 = t.n0 + half * 128 + ch * 32;
+      if (c0 >= p.V) break;
+      float v[32];
+      tmem_ld32(taddr + uint32_t(half * 128 + ch * 32), v);
+      if (p.bias2) {
+        const float4* b4 = reinterpret_cast<const float4*>(p.bias2 + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 b = __ldg(b4 + i);
+          v[4 * i + 0] = fmaf(v[4 * i + 0], sc, b.x);
+          v[4 * i + 1] = fmaf(v[4 * i + 1], sc, b.y);
+          v[4 * i + 2] = fmaf(v[4 * i + 2], sc, b.z);
+          v[4 * i + 3] = fmaf(v[4 * i + 3], sc, b.w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = v[i] * sc;
+      }
+      if (c0 + 32 > p.V) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c0 + i >= p.V) v[i] = -3.0e38f;
+      }
+      float mx = v[0];
+#pragma unroll
+      for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
+      // Reference max kept on an integer grid in log2 units; move it only
+      // when a logit would exceed it by more than 2^16, so rescaling is rare
+      // and exact (a power of two).
+      if (mx > e.mref + 16.f) {
+        const float nref = ceilf(mx);
+        if (e.mref == -INFINITY) {
+          e.mref = nref;
+        } else {
+          const float dd = e.mref - nref;     // negative integer
+          const int di = int(dd);
+          e.w_hi = ldexpf(e.w_hi + dd * e.s_hi, di);
+          e.w_lo = ldexpf(e.w_lo + dd * e.s_lo, di);
+          e.s_hi = ldexpf(e.s_hi, di);
+          e.s_lo = ldexpf(e.s_lo, di);
+          e.mref = nref;
+        }
+      }
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float d0 = v[i] - e.mref, d1 = v[i + 1] - e.mref, d2 = v[i + 2] - e.mref, d3 = v[i + 3] - e.mref;
+        const float x0 = ex2_approx(d0), x1 = ex2_approx(d1), x2 = ex2_approx(d2), x3 = ex2_approx(d3);
+        s0 += x0; s1 += x1; s2 += x2; s3 += x3;
+        w0 = fmaf(x0, d0, w0); w1 = fmaf(x1, d1, w1); w2 = fmaf(x2, d2, w2); w3 = fmaf(x3, d3, w3);
+      }
+      two_sum_acc(e.s_hi, e.s_lo, (s0 + s1) + (s2 + s3));
+      two_sum_acc(e.w_hi, e.w_lo, (w0 + w1) + (w2 + w3));
+      const unsigned ty = unsigned(e.y - c0);
+      if (ty < 32u) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (unsigned(i) == ty) e.zy = v[i];
+        e.found = 1;
+      }
+    }
+    if (t.last && row < p.N) {
+      float4* dst = p.partial + (size_t(row) * (2 * p.P) + size_t(t.seg) * 2 + half) * 2;
+      dst[0] = make_float4(e.mref, e.s_hi, e.s_lo, e.w_hi);
+      dst[1] = make_float4(e.w_lo, e.zy, e.found ? 1.f : 0.f, 0.f);
+    }
+  }
+};
+
+// Merge the 2P partial states of each row (fp64).  Each partial holds, for
+// one vocabulary segment and column half: reference m (log2 units, integer),
+// s = sum 2^(t-m), w = sum 2^(t-m) (t-m), and the target's t if it fell there.
+__global__ void fwd_merge_kernel(MergeParams p) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= p.N) return;
+  const float4* base = p.partial + size_t(row) * p.slots * 2;
+  double M = -INFINITY;
+  for (int k = 0; k < p.slots; ++k) {
+    const float4 a = base[2 * k];
+    if (a.y + a.z > 0.f) M = fmax(M, double(a.x));
+  }
+  double S = 0.0, Wd = 0.0, zy = 0.0;
+  int found = 0;
+  for (int k = 0; k < p.slots; ++k) {
+    const float4 a = base[2 * k];
+    const float4 b = base[2 * k + 1];
+    const double s = double(a.y) + double(a.z);
+    if (s > 0.0) {
+      const double d = double(a.x) - M;            // integer, <= 0
+      const double f = ldexp(1.0, int(d));
+      S += s * f;
+      Wd += f * ((double(a.w) + double(b.x)) + d * s);
+    }
+    if (b.z != 0.f) {
+      zy = double(b.y);
+      found = 1;
+    }
+  }
+  const long long y = p.targets[row];
+  const double ln2 = 0.6931471805599453;
+  const double l2s = log2(S);
+  const double lse2 = M + l2s;
+  const double ent = ln2 * (l2s - Wd / S);
+  double logp = ln2 * (zy - lse2);
+  if (y < 0 || y >= p.V || !found) {
+    logp = __longlong_as_double(0x7ff8000000000000ll);
+    if (p.status) atomicOr(p.status, RLLOSS_DEV_EBADTARGET);
+  }
+  p.lse2[row] = float(lse2);
+  p.logp64[row] = logp;
+  p.ent32[row] = float(ent);
+  if (p.out_logp) p.out_logp[row] = float(logp);
+  if (p.out_ent) p.out_ent[row] = float(ent);
+}
+
+// =============================================================== dlogits
+struct DlPolicy {
+  static constexpr int kStages = 4;
+  static constexpr int kBN = 256;
+  static constexpr int kK16 = 4;
+  static constexpr int kABytes = 128 * 64 * 2;
+  static constexpr int kBBytes = 256 * 64 * 2;
+  static constexpr int kExtraSmem = 0;
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, 0, 0);
+  using Params = DlParams;
+  struct EpiState {};
+
+  __device__ static void cta_setup(const Params&, uint8_t*) {}
+  __device__ static void prefetch(const Params& p) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+  // Tiles u = j * Rc + r: CTAs running together share the W tile j.
+  template <class F>
+  __device__ static void for_each_tile(const Params& p, F&& f) {
+    const int tiles = p.Rc * p.Vt;
+    const int kbs = p.nseg * p.kb_per_seg;
+    for (int u = blockIdx.x; u < tiles; u += gridDim.x) {
+      const int j = u / p.Rc;
+      const int r = u - j * p.Rc;
+      TileInfo t{r * 128, j * 256, 0, kbs, u, 0, true, true};
+      if (!f(t)) return;
+    }
+  }
+  __device__ static void load(const Params& p, uint8_t* st, uint64_t* bar, const TileInfo& t, int kb) {
+    const int s = kb / p.kb_per_seg;
+    const int kk = (kb - s * p.kb_per_seg) * 64;
+    tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0);
+    tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+  }
+  __device__ static uint64_t adesc(uint32_t sa, int k) { return sdesc_sw128(sa + k * 32, 16, 1024); }
+  __device__ static uint64_t bdesc(uint32_t sa, int k) { return sdesc_sw128(sa + kABytes + k * 32, 16, 1024); }
+
+  __device__ static void epilogue(const Params& p, EpiState&, const TileInfo& t, uint32_t taddr, int q, int half,
+                                  int lane, uint8_t*) {
+    const int rl = t.m0 + q * 32 + lane;   // row within the chunk
+    const bool valid = rl < p.Nc;
+    const int row = p.n0 + rl;
+    const float lse2 = valid ? p.lse2[row] : 0.f;
+    const float cf = valid ? p.coef[row] : 0.f;
+    const int y = valid ? int(p.targets[row]) : -1;
+    const float sc = p.scale2;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      const int c0 = t.n0 + half * 128 + ch * 32;
+      if (c0 >= p.Vp) break;
+      float v[32];
+      tmem_ld32(taddr + uint32_t(half * 128 + ch * 32), v);
+      if (p.bias2) {
+        const float4* b4 = reinterpret_cast<const float4*>(p.bias2 + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 b = __ldg(b4 + i);
+          v[4 * i + 0] = fmaf(v[4 * i + 0], sc, b.x - lse2);
+          v[4 * i + 1] = fmaf(v[4 * i + 1], sc, b.y - lse2);
+          v[4 * i + 2] = fmaf(v[4 * i + 2], sc, b.z - lse2);
+          v[4 * i + 3] = fmaf(v[4 * i + 3], sc, b.w - lse2);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = fmaf(v[i], sc, -lse2);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = -cf * ex2_approx(v[i]);
+      const unsigned ty = unsigned(y - c0);
+      if (ty < 32u) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (unsigned(i) == ty) v[i] += cf;
+      }
+      if (c0 + 32 > p.V) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c0 + i >= p.V) v[i] = 0.f;
+      }
+      if (valid) {
+        __nv_bfloat16* dst = p.dl + size_t(rl) * p.ld + c0;
+        uint32_t hi[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hi[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
+        if (p.lo_off) {
+          uint32_t lo[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&hi[i]);
+            lo[i] = pack_bf16x2(v[2 * i] - __low2float(h2), v[2 * i + 1] - __high2float(h2));
+          }
+          uint4* l4 = reinterpret_cast<uint4*>(dst + p.lo_off);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) l4[i] = make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+        }
+      }
+    }
+  }
+};
+
+// =============================================================== gemmT
+// h-major output: TMEM lane = h (M = 128), columns = output rows (N = 256).
+template <int B_MN>
+struct TPolicy {
+  static constexpr int kStages = 4;
+  static constexpr int kBN = 256;
+  static constexpr int kK16 = 4;
+  static constexpr int kABytes = 128 * 64 * 2;   // two 64(h) x 64(k) boxes
+  static constexpr int kBBytes = 256 * 64 * 2;
+  static constexpr int kExtraSmem = 0;
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, 1, B_MN);
+  using Params = TParams;
+  struct EpiState {};
+
+  __device__ static void cta_setup(const Params&, uint8_t*) {}
+  __device__ static void prefetch(const Params& p) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+  // Units u = (s * Nt + j) * Mt + i: CTAs running together share the B tile
+  // (output columns j) and walk the same k range.
+  template <class F>
+  __device__ static void for_each_tile(const Params& p, F&& f) {
+    const int units = p.Mt * p.Nt * p.splits;
+    const int kbs = p.nseg * p.kb_per_seg;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int i = u % p.Mt;
+      const int j = (u / p.Mt) % p.Nt;
+      const int s = u / (p.Mt * p.Nt);
+      const int kb0 = int((long long)s * kbs / p.splits);
+      const int kb1 = int((long long)(s + 1) * kbs / p.splits);
+      if (kb1 <= kb0) continue;
+      TileInfo t{i * 128, j * 256, kb0, kb1, u, s, true, true};
+      if (!f(t)) return;
+    }
+  }
+  __device__ static void load(const Params& p, uint8_t* st, uint64_t* bar, const TileInfo& t, int kb) {
+    const int s = kb / p.kb_per_seg;
+    const int kk = (kb - s * p.kb_per_seg) * 64;
+    // A: MN-major, inner = h, outer = k
+    tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + t.m0, p.a_outer0 + kk);
+    tma_load_2d(&p.tmA, bar, st + 8192, p.seg_a[s] + t.m0 + 64, p.a_outer0 + kk);
+    if (B_MN) {
+      // B: MN-major, inner = output column, outer = k
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        tma_load_2d(&p.tmB, bar, st + kABytes + b * 8192, p.seg_b[s] + t.n0 + 64 * b, p.b_outer0 + kk);
+    } else {
+      // B: K-major, inner = k, outer = output column
+      tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+    }
+  }
+  __device__ static uint64_t adesc(uint32_t sa, int k) { return sdesc_sw128(sa + k * 2048, 8192, 1024); }
+  __device__ static uint64_t bdesc(uint32_t sa, int k) {
+    return B_MN ? sdesc_sw128(sa + kABytes + k * 2048, 8192, 1024) : sdesc_sw128(sa + kABytes + k * 32, 16, 1024);
+  }
+
+  __device__ static void epilogue(const Params& p, EpiState&, const TileInfo& t, uint32_t taddr, int q, int half,
+                                  int lane, uint8_t*) {
+    const int h = t.m0 + q * 32 + lane;
+    const bool hv = h < p.Hout;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      const int c0 = t.n0 + half * 128 + ch * 32;
+      if (c0 >= p.Ncols) break;
+      float v[32];
+      tmem_ld32(taddr + uint32_t(half * 128 + ch * 32), v);
+      if (!hv) continue;
+      float* o = p.out + (p.mode == 2 ? size_t(t.seg) * size_t(p.split_stride) : size_t(0)) + size_t(c0) * p.ldo + h;
+      const int nc = min(32, p.Ncols - c0);
+      if (p.mode == 1) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c < nc) o[size_t(c) * p.ldo] += v[c];
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c < nc) o[size_t(c) * p.ldo] = v[c];
+      }
+    }
+  }
+};
+
+// =============================================================== small kernels
+__global__ void bias2_kernel(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out) {
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= Vpad) return;
+  float x = 0.f;
+  if (v < V) x = is_fp32 ? static_cast<const float*>(b)[v] : __bfloat162float(static_cast<const __nv_bfloat16*>(b)[v]);
+  out[v] = v < V ? x * scale2 : 0.f;
+}
+
+// fp32 -> three bf16 terms hi + mid + lo (each the rounding of what is left),
+// laid out [rows, 3*Cp] with each term in its own Cp-wide column block.
+__global__ void split3_kernel(const float* src, long long rows, int cols, int Cp, __nv_bfloat16* out) {
+  const long long n = rows * Cp;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long r = idx / Cp;
+    const int c = int(idx - r * Cp);
+    const float x = c < cols ? src[r * cols + c] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    __nv_bfloat16* o = out + r * 3 * Cp + c;
+    o[0] = hi;
+    o[Cp] = mid;
+    o[2 * Cp] = lo;
+  }
+}
+
+// Column sums of G over blocks of kDbRows chunk rows: part[blk][v] (hi + lo
+// terms in fp32 mode).  No atomics, so db is reproducible bit for bit.
+constexpr int kDbRows = 256;
+__global__ void db_part_kernel(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, int V, float* part) {
+  const int v = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
+  if (v >= V) return;
+  const int r0 = blockIdx.y * kDbRows;
+  const int r1 = min(Nc, r0 + kDbRows);
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+  for (int r = r0; r < r1; ++r) {
+    const __nv_bfloat16* p = dl + size_t(r) * ld + v;
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(p);
+    a0 += __low2float(x);
+    a1 += __high2float(x);
+    if (lo_off) {
+      const __nv_bfloat162 l = *reinterpret_cast<const __nv_bfloat162*>(p + lo_off);
+      a0 += __low2float(l);
+      a1 += __high2float(l);
+    }
+  }
+  float* o = part + size_t(blockIdx.y) * V + v;
+  o[0] = a0;
+  if (v + 1 < V) o[1] = a1;
+}
+
+__global__ void db_reduce_kernel(const float* part, int nblk, int V, float* db, int accumulate) {
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= V) return;
+  float a = 0.f;
+  for (int k = 0; k < nblk; ++k) a += part[size_t(k) * V + v];
+  db[v] = accumulate ? db[v] + a : a;
+}
+
+// out[i] = sum over slices s of part[s * n + i], in slice order.
+__global__ void sum_slices_kernel(const float* part, int slices, long long n, float* out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    float a = part[i];
+    for (int s = 1; s < slices; ++s) a += part[s * n + i];
+    out[i] = a;
+  }
+}
+
+__global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const AbortCtl ac{&abort_flag, status, limit_ns};
+    mbar_wait(&bar, 0, ac);   // nothing arrives: runs out after limit_ns
+  }
+}
+
+// =============================================================== launchers
+template <class P>
+static cudaError_t launch_engine(const typename P::Params& prm, int grid, cudaStream_t st) {
+  constexpr int smem = engine_smem_bytes<P>();
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_engine_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  tc_engine_kernel<P><<<grid, kEngineThreads, smem, st>>>(prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t st) { return launch_engine<FwdPolicy>(p, grid, st); }
+cudaError_t launch_dl(const DlParams& p, int grid, cudaStream_t st) { return launch_engine<DlPolicy>(p, grid, st); }
+cudaError_t launch_gemmT(const TParams& p, int b_mn, int grid, cudaStream_t st) {
+  return b_mn ? launch_engine<TPolicy<1>>(p, grid, st) : launch_engine<TPolicy<0>>(p, grid, st);
+}
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
+  fwd_merge_kernel<<<(p.N + 127) / 128, 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st) {
+  bias2_kernel<<<(Vpad + 255) / 256, 256, 0, st>>>(b, is_fp32, V, Vpad, scale2, out);
+  return cudaGetLastError();
+}
+cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __nv_bfloat16* out, cudaStream_t st) {
+  const long long n = rows * Cp;
+  long long nb = (n + 255) / 256;
+  if (nb > 65535LL * 8) nb = 65535LL * 8;
+  const int blocks = int(nb < 1 ? 1 : nb);
+  split3_kernel<<<blocks, 256, 0, st>>>(src, rows, cols, Cp, out);
+  return cudaGetLastError();
+}
+int db_part_rows(int Nc) { return (Nc + kDbRows - 1) / kDbRows; }
+cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, int V, float* part, float* db,
+                      int accumulate, cudaStream_t st) {
+  const int nblk = db_part_rows(Nc);
+  dim3 grid((V / 2 + 1 + 255) / 256, nblk);
+  db_part_kernel<<<grid, 256, 0, st>>>(dl, ld, lo_off, Nc, V, part);
+  db_reduce_kernel<<<(V + 255) / 256, 256, 0, st>>>(part, nblk, V, db, accumulate);
+  return cudaGetLastError();
+}
+cudaError_t launch_sum_slices(const float* part, int slices, long long n, float* out, cudaStream_t st) {
+  long long nb = (n + 255) / 256;
+  if (nb > 152LL * 16) nb = 152LL * 16;
+  sum_slices_kernel<<<int(nb < 1 ? 1 : nb), 256, 0, st>>>(part, slices, n, out);
+  return cudaGetLastError();
+}
+cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace rl

@@ -1,0 +1,114 @@
+// Kernel parameter blocks and launchers shared by the host API and the CUDA
+// translation units of the library.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace rl {
+
+constexpr int kMaxSeg = 6;
+
+struct FwdParams {
+  CUtensorMap tmA;            // X (or its 3-term bf16 split): inner K, outer rows; box 64 x 128
+  CUtensorMap tmB;            // W (or split): inner K, outer vocab; box 64 x 256
+  int nseg, kb_per_seg;       // K = nseg * kb_per_seg * 64
+  int seg_a[kMaxSeg], seg_b[kMaxSeg];  // K offsets of each product term
+  int N, V, R, Vt, P;         // rows, vocab, row tiles, vocab tiles (256), vocab segments
+  float scale2;               // log2(e) / temperature
+  const float* bias2;         // [Vt*256] b * scale2, zero padded; null without bias
+  const int64_t* targets;
+  float4* partial;            // [N][2P][2]
+  int* status;
+  unsigned long long limit_ns;
+};
+
+struct MergeParams {
+  const float4* partial;
+  int N, V, slots;            // slots = 2P
+  const int64_t* targets;
+  float* lse2;                // [N] lse in log2 units
+  double* logp64;             // [N]
+  float* ent32;               // [N]
+  float* out_logp;            // optional
+  float* out_ent;             // optional
+  int* status;
+};
+
+struct DlParams {
+  CUtensorMap tmA, tmB;
+  int nseg, kb_per_seg;
+  int seg_a[kMaxSeg], seg_b[kMaxSeg];
+  int n0, Nc, Rc, V, Vp, Vt;  // chunk start row, rows in chunk, row tiles, vocab, padded vocab, vocab tiles
+  float scale2;
+  const float* bias2;
+  const int64_t* targets;
+  const float* lse2;
+  const float* coef;          // dL/dlogp / temperature
+  __nv_bfloat16* dl;          // [Nc, ld] chunk buffer (hi terms)
+  int ld;                     // row stride in elements
+  int lo_off;                 // element offset of the lo terms (fp32 mode), else 0
+  int* status;
+  unsigned long long limit_ns;
+};
+
+struct TParams {
+  CUtensorMap tmA;            // MN-major: inner h, outer k; box 64 x 64
+  CUtensorMap tmB;            // K-major: inner k, outer col, box 64 x 256; or MN-major: inner col, outer k, box 64 x 64
+  int nseg, kb_per_seg;
+  int seg_a[kMaxSeg], seg_b[kMaxSeg];  // inner-coordinate offsets of each product term
+  int a_outer0, b_outer0;     // outer (k) coordinate origins of A and MN-major B
+  int Mt, Nt, splits;         // h tiles (128), column tiles (256), k splits
+  int Hout, Ncols;            // valid h and output columns
+  float* out;                 // out[col * ldo + h] (+ split * split_stride in mode 2)
+  long long ldo;
+  long long split_stride;     // elements between the slices of a split-k partial output
+  int mode;                   // 0 store, 1 add, 2 store into the slice of the k split
+  int* status;
+  unsigned long long limit_ns;
+};
+
+struct LossParams {
+  int B, T, loss_type;
+  double eps_low, eps_high;   // GMPO log-space bounds, fp32 values widened
+  double clip_lo, clip_hi;    // GSPO ratio bounds, fp32 values of 1-eps_low, 1+eps_high
+  double beta, inv_tau;
+  const void* logp;           // fp64 [N] when logp_is_f64, else fp32
+  int logp_is_f64;
+  const float* old_logp;
+  const float* ref_logp;
+  const float* adv;
+  const uint8_t* mask;
+  const uint8_t* emask;       // entropy mask, or null (= mask)
+  const double* k3;           // K3 state (threshold at k3[0]) or null
+  double* seqres;             // [B][8]
+  unsigned int* ticket;
+  float* coef;                // optional: c / tau
+  float* dlogp;               // optional: c
+  float* out_loss;
+  float* out_metrics;
+  int* status;
+};
+
+cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t st);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
+cudaError_t launch_dl(const DlParams& p, int grid, cudaStream_t st);
+cudaError_t launch_gemmT(const TParams& p, int b_mn, int grid, cudaStream_t st);
+cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st);
+cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __nv_bfloat16* out, cudaStream_t st);
+cudaError_t launch_sum_slices(const float* part, int slices, long long n, float* out, cudaStream_t st);
+// db (+)= column sums of the chunk's G; part is scratch of db_part_rows(Nc) * V floats.
+int db_part_rows(int Nc);
+cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, int V, float* part, float* db,
+                      int accumulate, cudaStream_t st);
+cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
+
+// entropy quantile (K3): a 256-byte state block followed by 4 passes x 2 x 256
+// uint32 histogram bins
+constexpr int kK3Bytes = 256 + 4 * 512 * 4;
+cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long N, double q, void* k3_ws,
+                                uint8_t* emask, cudaStream_t st);
+cudaError_t launch_loss(const LossParams& p, cudaStream_t st);
+
+}  // namespace rl

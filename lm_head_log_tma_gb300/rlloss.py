@@ -1,0 +1,212 @@
+"""ctypes binding of librlloss.so (include/rlloss.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of the library.  torch supplies device memory and streams.  Importing
+this module fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from ctypes import c_float, c_int, c_int32, c_size_t, c_uint32, c_uint64, c_void_p
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librlloss.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "rlloss.h")
+
+OK, EINVAL, EUNSUPPORTED, EWORKSPACE, ECUDA = 0, 1, 2, 3, 4
+DEV_ETIMEOUT, DEV_ENONFINITE, DEV_EBADTARGET, DEV_EEMPTYSEQ = 0x10, 0x20, 0x40, 0x80
+BF16, FP32 = 0, 1
+GMPO, GSPO_TOKEN = 0, 1
+IS_TOKEN, IS_SEQUENCE = 0, 1
+FLAG_FORCE_ENTROPY_PATH = 0x1
+NMETRICS = 8
+
+
+class RllossCfg(ctypes.Structure):
+    _fields_ = [("B", c_int32), ("T", c_int32), ("H", c_int32), ("V", c_int32),
+                ("dtype", c_int32), ("loss_type", c_int32), ("is_level", c_int32),
+                ("eps_low", c_float), ("eps_high", c_float), ("beta", c_float),
+                ("temperature", c_float), ("top_entropy_quantile", c_float),
+                ("has_bias", c_int32), ("flags", c_uint32), ("chunk_rows", c_int32)]
+
+
+def make_cfg(B, T, H=0, V=0, dtype=BF16, loss_type=GMPO, is_level=IS_TOKEN, eps_low=0.4,
+             eps_high=0.4, beta=0.0, temperature=1.0, top_entropy_quantile=1.0, has_bias=False,
+             flags=0, chunk_rows=0) -> RllossCfg:
+    return RllossCfg(B, T, H, V, dtype, loss_type, is_level, eps_low, eps_high, beta, temperature,
+                     top_entropy_quantile, int(bool(has_bias)), flags, chunk_rows)
+
+
+class RllossError(RuntimeError):
+    def __init__(self, code, where=""):
+        super().__init__(f"{where}: {status_str(code)} ({code})")
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"librlloss.so is not built ({LIB_PATH}); run lm_head_log_tma_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = c_void_p
+    cfgp = ctypes.POINTER(RllossCfg)
+    lib.rlloss_workspace_bytes.argtypes = [cfgp]
+    lib.rlloss_workspace_bytes.restype = c_size_t
+    lib.rlloss_loss_workspace_bytes.argtypes = [cfgp]
+    lib.rlloss_loss_workspace_bytes.restype = c_size_t
+    lib.rlloss_fwd_bwd.argtypes = [cfgp] + [P] * 16 + [P, c_size_t, P]
+    lib.rlloss_fwd_bwd.restype = c_int
+    lib.rlloss_loss_from_logp.argtypes = [cfgp] + [P] * 10 + [P, c_size_t, P]
+    lib.rlloss_loss_from_logp.restype = c_int
+    lib.rlloss_get_device_status.argtypes = [P, ctypes.POINTER(c_int32)]
+    lib.rlloss_get_device_status.restype = c_int
+    lib.rlloss_selftest_bounded_wait.argtypes = [P, c_uint64, P]
+    lib.rlloss_selftest_bounded_wait.restype = c_int
+    lib.rlloss_phase_timing.argtypes = [c_int]
+    lib.rlloss_phase_timing.restype = c_int
+    lib.rlloss_phase_times.argtypes = [ctypes.POINTER(c_float), ctypes.POINTER(c_int32), c_int]
+    lib.rlloss_phase_times.restype = c_int
+    lib.rlloss_kernel_launches.argtypes = []
+    lib.rlloss_kernel_launches.restype = c_uint64
+    lib.rlloss_status_str.argtypes = [c_int]
+    lib.rlloss_status_str.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def declared_functions() -> list[str]:
+    """Function names declared in include/rlloss.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:size_t|int|uint64_t|const char\s*\*)\s*(rlloss_\w+)\s*\(", text, re.M)))
+
+
+def status_str(code: int) -> str:
+    return lib.rlloss_status_str(int(code)).decode()
+
+
+def _p(t):
+    if t is None:
+        return None
+    return c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(stream.cuda_stream)
+
+
+# ---------------------------------------------------------------- raw entry points
+def rlloss_workspace_bytes(cfg: RllossCfg) -> int:
+    return int(lib.rlloss_workspace_bytes(ctypes.byref(cfg)))
+
+
+def rlloss_loss_workspace_bytes(cfg: RllossCfg) -> int:
+    return int(lib.rlloss_loss_workspace_bytes(ctypes.byref(cfg)))
+
+
+def rlloss_fwd_bwd(cfg, X, W, b, targets, old_logp, ref_logp, adv, mask, out_loss, out_metrics, dX, dW,
+                   db, out_logp, out_entropy, out_entropy_mask, workspace, stream=None) -> int:
+    return lib.rlloss_fwd_bwd(ctypes.byref(cfg), _p(X), _p(W), _p(b), _p(targets), _p(old_logp),
+                              _p(ref_logp), _p(adv), _p(mask), _p(out_loss), _p(out_metrics), _p(dX),
+                              _p(dW), _p(db), _p(out_logp), _p(out_entropy), _p(out_entropy_mask),
+                              _p(workspace), c_size_t(0 if workspace is None else workspace.numel()),
+                              _stream(stream))
+
+
+def rlloss_loss_from_logp(cfg, logp, entropy, old_logp, ref_logp, adv, mask, out_loss, out_metrics,
+                          out_dlogp, out_entropy_mask, workspace, stream=None) -> int:
+    return lib.rlloss_loss_from_logp(ctypes.byref(cfg), _p(logp), _p(entropy), _p(old_logp),
+                                     _p(ref_logp), _p(adv), _p(mask), _p(out_loss), _p(out_metrics),
+                                     _p(out_dlogp), _p(out_entropy_mask), _p(workspace),
+                                     c_size_t(0 if workspace is None else workspace.numel()),
+                                     _stream(stream))
+
+
+def rlloss_get_device_status(workspace) -> int:
+    st = c_int32(0)
+    rc = lib.rlloss_get_device_status(_p(workspace), ctypes.byref(st))
+    if rc != OK:
+        raise RllossError(rc, "rlloss_get_device_status")
+    return int(st.value)
+
+
+def rlloss_selftest_bounded_wait(workspace, limit_ns: int, stream=None) -> int:
+    return lib.rlloss_selftest_bounded_wait(_p(workspace), c_uint64(limit_ns), _stream(stream))
+
+
+NPHASES = 6
+PHASE_NAMES = ["fwd_gemm", "merge_mask_loss", "bwd_dlogits", "bwd_dX", "bwd_dW", "other"]
+
+
+def rlloss_phase_timing(enable: bool) -> int:
+    return lib.rlloss_phase_timing(int(bool(enable)))
+
+
+def rlloss_phase_times():
+    ms = (c_float * NPHASES)()
+    n = (c_int32 * NPHASES)()
+    rc = lib.rlloss_phase_times(ms, n, NPHASES)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_phase_times")
+    return [float(x) for x in ms], [int(x) for x in n]
+
+
+def rlloss_kernel_launches() -> int:
+    return int(lib.rlloss_kernel_launches())
+
+
+# ---------------------------------------------------------------- convenience
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def fwd_bwd(cfg: RllossCfg, X, W, b, targets, old_logp, ref_logp, adv, mask, workspace=None,
+            outputs=None, stream=None):
+    """Allocate outputs (torch) and run rlloss_fwd_bwd.  Returns a dict of tensors."""
+    dev = X.device
+    N, H, V = cfg.B * cfg.T, cfg.H, cfg.V
+    if outputs is None:
+        outputs = dict(
+            loss=torch.empty(1, dtype=torch.float32, device=dev),
+            metrics=torch.empty(NMETRICS, dtype=torch.float32, device=dev),
+            dX=torch.empty(N, H, dtype=torch.float32, device=dev),
+            dW=torch.empty(V, H, dtype=torch.float32, device=dev),
+            db=torch.empty(V, dtype=torch.float32, device=dev) if cfg.has_bias else None,
+            logp=torch.empty(N, dtype=torch.float32, device=dev),
+            entropy=torch.empty(N, dtype=torch.float32, device=dev),
+            emask=torch.empty(N, dtype=torch.uint8, device=dev),
+        )
+    if workspace is None:
+        workspace = alloc_workspace(rlloss_workspace_bytes(cfg), dev)
+    o = outputs
+    rc = rlloss_fwd_bwd(cfg, X, W, b, targets, old_logp, ref_logp, adv, mask, o["loss"], o["metrics"],
+                        o["dX"], o["dW"], o.get("db"), o.get("logp"), o.get("entropy"), o.get("emask"),
+                        workspace, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_fwd_bwd")
+    o["workspace"] = workspace
+    return o
+
+
+def loss_from_logp(cfg: RllossCfg, logp, entropy, old_logp, ref_logp, adv, mask, workspace=None,
+                   stream=None):
+    dev = logp.device
+    N = cfg.B * cfg.T
+    o = dict(loss=torch.empty(1, dtype=torch.float32, device=dev),
+             metrics=torch.empty(NMETRICS, dtype=torch.float32, device=dev),
+             dlogp=torch.empty(N, dtype=torch.float32, device=dev),
+             emask=torch.empty(N, dtype=torch.uint8, device=dev))
+    if workspace is None:
+        workspace = alloc_workspace(rlloss_loss_workspace_bytes(cfg), dev)
+    rc = rlloss_loss_from_logp(cfg, logp, entropy, old_logp, ref_logp, adv, mask, o["loss"], o["metrics"],
+                               o["dlogp"], o["emask"], workspace, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_loss_from_logp")
+    o["workspace"] = workspace
+    return o

@@ -1,0 +1,101 @@
+"""Host-side tests of the C ABI: the library loads, exports every function the
+header declares, and rejects invalid requests synchronously (no GPU needed:
+validation happens before any CUDA call)."""
+import ctypes
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from lm_head_log_tma_gb300 import build as B
+
+if not os.path.exists(B.LIB):
+    B.build()
+from lm_head_log_tma_gb300 import rlloss as R  # noqa: E402
+
+
+def test_library_exports_every_declared_function():
+    names = R.declared_functions()
+    assert "rlloss_fwd_bwd" in names and "rlloss_loss_from_logp" in names
+    lib = ctypes.CDLL(R.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    for code in (R.OK, R.EINVAL, R.EUNSUPPORTED, R.EWORKSPACE, R.ECUDA, R.DEV_ETIMEOUT):
+        assert R.status_str(code) != "unknown status"
+
+
+def _cfg(**kw):
+    base = dict(B=2, T=16, H=64, V=512, dtype=R.BF16)
+    base.update(kw)
+    return R.make_cfg(**base)
+
+
+def test_workspace_bytes_positive_and_zero_for_invalid():
+    assert R.rlloss_workspace_bytes(_cfg()) > 0
+    assert R.rlloss_workspace_bytes(_cfg(top_entropy_quantile=1.5)) == 0
+    assert R.rlloss_workspace_bytes(_cfg(temperature=0.0)) == 0
+    assert R.rlloss_loss_workspace_bytes(_cfg(H=0, V=0)) > 0
+
+
+def test_workspace_grows_with_fp32_split_and_bias():
+    a = R.rlloss_workspace_bytes(_cfg())
+    assert R.rlloss_workspace_bytes(_cfg(dtype=R.FP32)) > a
+    assert R.rlloss_workspace_bytes(_cfg(has_bias=True)) > a
+
+
+class _Null:
+    def data_ptr(self):
+        return 0
+
+
+def _call(cfg):
+    """fwd_bwd with null tensors: must be rejected before touching the GPU."""
+    return R.lib.rlloss_fwd_bwd(ctypes.byref(cfg), *([None] * 16), None, 0, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(is_level=R.IS_SEQUENCE), R.EINVAL),          # GMPO rejects sequence-level IS
+    (dict(top_entropy_quantile=1.0001), R.EINVAL),     # q outside [0, 1]
+    (dict(top_entropy_quantile=-0.01), R.EINVAL),
+    (dict(top_entropy_quantile=float("nan")), R.EINVAL),
+    (dict(temperature=0.0), R.EINVAL),
+    (dict(temperature=-1.0), R.EINVAL),
+    (dict(eps_low=-0.1), R.EINVAL),
+    (dict(B=0), R.EINVAL),
+    (dict(V=0), R.EINVAL),
+    (dict(loss_type=7), R.EINVAL),
+    (dict(dtype=3), R.EINVAL),
+    (dict(H=60), R.EUNSUPPORTED),                       # bf16 rows must be 16-byte multiples
+    (dict(loss_type=R.GSPO_TOKEN, beta=0.1), R.EUNSUPPORTED),
+    (dict(loss_type=R.GSPO_TOKEN, top_entropy_quantile=0.5), R.EUNSUPPORTED),
+    (dict(), R.EINVAL),                                 # valid cfg, null pointers
+])
+def test_invalid_requests_rejected_synchronously(kw, code):
+    assert _call(_cfg(**kw)) == code
+
+
+def test_gmpo_sequence_is_rejection_matches_page():
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_constants.json")))
+    assert g["gmpo_rejects_sequence_level_is"]["value"] is True
+    assert _call(_cfg(is_level=R.IS_SEQUENCE)) == R.EINVAL
+    # GSPO is a sequence-level ratio by construction and ignores the level
+    assert _call(_cfg(loss_type=R.GSPO_TOKEN, is_level=R.IS_SEQUENCE)) == R.EINVAL  # still null pointers
+    assert R.rlloss_workspace_bytes(_cfg(loss_type=R.GSPO_TOKEN, is_level=R.IS_SEQUENCE)) > 0
+
+
+def test_quantile_range_matches_page():
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_constants.json")))["top_entropy_quantile"]
+    assert R.rlloss_workspace_bytes(_cfg(top_entropy_quantile=g["valid_min"])) > 0
+    assert R.rlloss_workspace_bytes(_cfg(top_entropy_quantile=g["valid_max"])) > 0
+    assert R.rlloss_workspace_bytes(_cfg(top_entropy_quantile=float(np.nextafter(np.float32(g["valid_max"]), np.float32(2))))) == 0
+
+
+def test_loss_from_logp_validation():
+    cfg = _cfg(top_entropy_quantile=0.5)
+    rc = R.lib.rlloss_loss_from_logp(ctypes.byref(cfg), *([None] * 10), None, 0, None)
+    assert rc == R.EINVAL

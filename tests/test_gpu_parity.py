@@ -1,0 +1,236 @@
+"""GPU parity of the fused path against the fp64 oracle, through the C ABI.
+
+Sizes here span several 128-row and 256-column tiles with ragged tails, so
+every tail path of the kernels runs; the oracle finishes each in seconds.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from lm_head_log_tma_gb300.workloads import GMPO, GSPO_TOKEN, WORKLOADS, Workload, make_inputs, random_entropies
+
+from parity import (EDGE, Case, check_grads, check_loss_and_metrics, check_rows, reconcile_loss)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def R():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from lm_head_log_tma_gb300 import rlloss
+    return rlloss
+
+
+MID = [
+    Workload("mid_gmpo_bf16", B=3, T=150, H=192, V=1000, dtype="bf16", prompt_len=20, seed=101),
+    Workload("mid_gmpo_bias_k3kl", B=4, T=130, H=256, V=777, dtype="bf16", has_bias=True, bias_std=0.3,
+             eps_low=0.2, eps_high=0.3, beta=0.04, prompt_len=(5, 40), adv_kind="pm1zero",
+             ref_noise_std=0.1, seed=102),
+    Workload("mid_entropy_q0.2_tau0.7", B=5, T=100, H=128, V=1300, dtype="bf16", temperature=0.7,
+             top_entropy_quantile=0.2, prompt_len=10, seed=103),
+    Workload("mid_gspo_token", B=6, T=97, H=64, V=600, dtype="bf16", loss_type=GSPO_TOKEN, eps_low=3e-4,
+             eps_high=4e-4, prompt_len=8, old_noise_std=0.02, seed=104),
+    Workload("mid_fp32_bias_odd", B=2, T=77, H=100, V=515, dtype="fp32", has_bias=True, bias_std=0.1,
+             temperature=1.3, prompt_len=3, seed=105),
+    Workload("mid_wide_logits", B=2, T=140, H=512, V=2000, dtype="bf16", prompt_len=12, seed=106),
+]
+
+
+def _full_check(R, case, **cfg_kw):
+    out = case.run_gpu(R, **cfg_kw)
+    assert out["status"] == 0, hex(out["status"])
+    check_rows(out, case)
+    res = reconcile_loss(out, case)
+    gl, ol = check_loss_and_metrics(out, case, res)
+    stats = check_grads(out, case, res)
+    return out, res, stats
+
+
+def test_tiny_fp32_workload(R):
+    case = Case(WORKLOADS[0])
+    _full_check(R, case)
+
+
+@pytest.mark.parametrize("spec", MID, ids=[s.name for s in MID])
+def test_mid_workloads(R, spec):
+    case = Case(spec)
+    _full_check(R, case)
+
+
+def test_backward_chunking_is_invariant(R):
+    """Chunks of 128 rows (several dW/db accumulation steps) give the same result."""
+    spec = MID[1]
+    case = Case(spec)
+    a, _, _ = _full_check(R, case)
+    b, _, _ = _full_check(R, case, chunk_rows=128)
+    assert torch.equal(a["loss"], b["loss"])
+    assert torch.allclose(a["dX"], b["dX"], rtol=1e-4, atol=1e-9)
+    assert torch.allclose(a["dW"], b["dW"], rtol=1e-4, atol=1e-9)
+
+
+def test_entropy_mask_non_vacuous_and_forced_path_bit_identical(R):
+    spec = MID[2]
+    case = Case(spec)
+    out, res, _ = _full_check(R, case)
+    m = out["metrics"].cpu().numpy()
+    assert 0 < m[5] < m[3]           # drops some but not all active tokens
+    # q = 1 with the quantile path forced is bit-identical to the path off
+    spec1 = spec.with_(top_entropy_quantile=1.0)
+    case1 = Case(spec1, case.inp)
+    o1 = case1.run_gpu(R)
+    o2 = case1.run_gpu(R, flags=R.FLAG_FORCE_ENTROPY_PATH)
+    for k in ("loss", "dX", "dW"):
+        assert torch.equal(o1[k], o2[k]), k
+    assert torch.equal(o2["emask"], case.inp.mask.cuda())
+
+
+def test_repeated_calls_are_bit_identical(R):
+    """No floating-point atomics anywhere: two calls give the same bits."""
+    case = Case(MID[1])
+    a = case.run_gpu(R)
+    b = case.run_gpu(R)
+    for k in ("loss", "metrics", "dX", "dW", "db", "logp", "entropy"):
+        assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), k
+
+
+def test_uniform_logits_closed_form(R):
+    """W = 0: every logit is 0, so logp = -log V and H = log V on the GPU too."""
+    spec = Workload("zeros", B=2, T=130, H=64, V=700, dtype="bf16", prompt_len=0, seed=7)
+    inp = make_inputs(spec)
+    inp.W.zero_()
+    case = Case(spec, inp)
+    out = case.run_gpu(R)
+    assert out["status"] == 0
+    assert np.allclose(out["logp"].cpu().numpy(), -np.log(700), atol=2e-6)
+    assert np.allclose(out["entropy"].cpu().numpy(), np.log(700), atol=2e-6)
+
+
+def test_bad_target_sets_status(R):
+    spec = Workload("badtarget", B=1, T=128, H=64, V=300, dtype="bf16", seed=8)
+    case = Case(spec)
+    case.inp.targets[5] = 300
+    out = case.run_gpu(R)
+    assert out["status"] & R.DEV_EBADTARGET
+    assert np.isnan(out["logp"][5].item())
+
+
+def test_bounded_wait_times_out_cleanly(R):
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    assert R.rlloss_selftest_bounded_wait(ws, 2_000_000) == R.OK
+    torch.cuda.synchronize()
+    assert R.rlloss_get_device_status(ws) & R.DEV_ETIMEOUT
+    # the context is still usable afterwards
+    assert torch.ones(4, device="cuda").sum().item() == 4
+
+
+# ------------------------------------------------------------------ loss stage only
+def _loss_gpu(R, cfg, logp, old, adv, mask, entropy=None, ref=None):
+    c = lambda x: None if x is None else torch.as_tensor(x).cuda()
+    o = R.loss_from_logp(cfg, c(logp), c(entropy), c(old), c(ref), c(adv), c(mask))
+    torch.cuda.synchronize()
+    o["status"] = R.rlloss_get_device_status(o["workspace"])
+    return o
+
+
+@pytest.mark.parametrize("side", ["high", "low"])
+def test_exact_clip_boundaries_loss_stage(R, side):
+    """lr == bound exactly (Sterbenz: logp = -b, old = -2b) is unclipped with full
+    gradient; the next fp32 value outward clips.  Decisions and gradients are
+    compared exactly, the loss to the oracle's value rounded to fp32."""
+    eps = 0.4
+    ef = np.float32(eps)
+    A = 1.0 if side == "high" else -1.0
+    bound = ef if A > 0 else -ef
+    old = np.float32(-2 * ef) if A > 0 else np.float32(-ef)
+    on = np.float32(old + bound)
+    assert float(on) - float(old) == float(bound)
+    out_v = np.nextafter(on, np.float32(np.inf if A > 0 else -np.inf))
+    in_v = np.nextafter(on, np.float32(-np.inf if A > 0 else np.inf))
+    logp = np.array([on, out_v, in_v, on], np.float32)
+    oldv = np.full(4, old, np.float32)
+    adv = np.array([A], np.float32)
+    mask = np.ones(4, np.uint8)
+    cfg = R.make_cfg(1, 4, eps_low=eps, eps_high=eps)
+    g = _loss_gpu(R, cfg, logp, oldv, adv, mask)
+    o = O.gmpo_loss(logp.astype(np.float64), oldv.astype(np.float64), None, adv.astype(np.float64), mask, 1, 4,
+                    eps, eps)
+    assert g["status"] == 0
+    assert g["metrics"][1].item() == o.metrics[1] == 1
+    gd = g["dlogp"].cpu().numpy()
+    assert np.array_equal(gd == 0, o.c == 0)
+    assert np.allclose(gd, o.c, rtol=1e-6, atol=0)
+    assert g["loss"].item() == pytest.approx(np.float32(o.loss), rel=1e-7)
+
+
+def test_gspo_clip_bounds_loss_stage(R):
+    """GSPO: sequence ratios exactly at, just inside and just outside the bounds."""
+    B, T = 4, 2
+    lo, hi = O.f32(1 - 3e-4), O.f32(1 + 4e-4)
+    rng = np.random.default_rng(3)
+    logp = rng.uniform(-3, -1, B * T).astype(np.float32)
+    shifts = [np.log(hi) + 1e-6, np.log(hi) - 1e-6, np.log(lo) - 1e-6, 0.0]
+    old = (logp.astype(np.float64) - np.repeat(shifts, T)).astype(np.float32)
+    adv = np.array([1.0, 1.0, -1.0, 0.5], np.float32)
+    mask = np.ones(B * T, np.uint8)
+    cfg = R.make_cfg(B, T, loss_type=R.GSPO_TOKEN, eps_low=3e-4, eps_high=4e-4)
+    g = _loss_gpu(R, cfg, logp, old, adv, mask)
+    o = O.gspo_token_loss(logp.astype(np.float64), old.astype(np.float64), adv.astype(np.float64), mask, B, T)
+    assert g["status"] == 0
+    assert g["metrics"][1].item() == o.metrics[1]
+    assert np.array_equal(g["dlogp"].cpu().numpy() == 0, o.c == 0)
+    assert g["loss"].item() == pytest.approx(o.loss, rel=1e-6)
+
+
+def test_quantile_beyond_2_24_elements_exact(R):
+    """2^24 + 1 active entropies (past torch.quantile's cap): threshold and mask
+    against a sort of the same fp32 values ("support top_entropy_quantile",
+    Details: the sort fallback beyond the 2^24-element cap)."""
+    n = (1 << 24) + 1
+    H = random_entropies(n, seed=11)
+    mask = torch.ones(n, dtype=torch.uint8)
+    mask[::7] = 0
+    logp = torch.full((n,), -11.0)
+    old = logp.clone()
+    adv = torch.ones(1)
+    cfg = R.make_cfg(1, n, top_entropy_quantile=0.2)
+    g = _loss_gpu(R, cfg, logp, old, adv, mask, entropy=H)
+    thr, e = O.entropy_threshold(H.double().numpy(), mask.numpy(), 0.2)
+    assert g["status"] == 0
+    assert g["metrics"][4].item() == np.float32(thr)
+    assert np.array_equal(g["emask"].cpu().numpy(), e)
+    assert g["metrics"][5].item() == e.sum()
+
+
+def test_quantile_small_cases_exact(R):
+    rng = np.random.default_rng(12)
+    for n, q in ((1, 0.2), (2, 0.5), (5, 0.0), (5, 1.0), (1000, 0.37), (4097, 0.8)):
+        H = rng.normal(3.0, 1.0, n).astype(np.float32)
+        H[: n // 3] = H[0]                       # ties
+        mask = (rng.uniform(size=n) < 0.9).astype(np.uint8)
+        cfg = R.make_cfg(1, n, top_entropy_quantile=q, flags=R.FLAG_FORCE_ENTROPY_PATH)
+        g = _loss_gpu(R, cfg, np.full(n, -2.0, np.float32), np.full(n, -2.0, np.float32),
+                      np.ones(1, np.float32), mask, entropy=H)
+        thr, e = O.entropy_threshold(H.astype(np.float64), mask, q)
+        assert np.array_equal(g["emask"].cpu().numpy(), e), (n, q)
+        if mask.sum():
+            assert g["metrics"][4].item() == np.float32(thr), (n, q)
+
+
+def test_empty_active_set(R):
+    n = 64
+    cfg = R.make_cfg(2, 32, top_entropy_quantile=0.3)
+    g = _loss_gpu(R, cfg, np.full(n, -2.0, np.float32), np.full(n, -2.0, np.float32), np.ones(2, np.float32),
+                  np.zeros(n, np.uint8), entropy=np.ones(n, np.float32))
+    assert g["status"] == 0
+    assert np.isnan(g["metrics"][4].item())
+    assert g["emask"].sum().item() == 0
+    assert g["loss"].item() == 0.0
+
+
+def test_gspo_empty_sequence_flags_status(R):
+    cfg = R.make_cfg(2, 4, loss_type=R.GSPO_TOKEN, eps_low=3e-4, eps_high=4e-4)
+    mask = np.array([1, 1, 1, 1, 0, 0, 0, 0], np.uint8)
+    g = _loss_gpu(R, cfg, np.full(8, -2.0, np.float32), np.full(8, -2.0, np.float32), np.ones(2, np.float32), mask)
+    assert g["status"] & R.DEV_EEMPTYSEQ
