@@ -150,6 +150,30 @@ int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float*
                           float* out_dlogp, uint8_t* out_entropy_mask, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* The loss stage of rlloss_loss_from_logp for callers that cannot allocate
+ * device memory: code that runs while another component is capturing a CUDA
+ * graph, plugins that are handed only the tensors they read and write, and
+ * runtimes whose memory pool is reserved in full up front.  It takes no
+ * workspace.  The pages have no counterpart of this entry point.
+ *   Scratch: a file-scope device array of 4 MiB inside the library, which
+ *   every GPU that loads the library holds until the process exits.  A
+ *   problem whose rlloss_loss_workspace_bytes exceeds 4 MiB (N = B*T tokens
+ *   plus 64 bytes per sequence, plus about 9 KB: e.g. N > 2^21 with
+ *   B <= 16384) is rejected with RLLOSS_ETOOLARGE before any launch.
+ *   The first call on a device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.
+ *   All calls share the one array, which keeps the last call's contents; each
+ *   call clears what must start at zero.  Calls that overlap on the GPU (for
+ *   example on two streams) race on the array and must not be issued.
+ *   Arguments as for rlloss_loss_from_logp; out_device_status (optional,
+ *   device int32) receives this call's device status word (RLLOSS_DEV_*). */
+#define RLLOSS_ETOOLARGE 5     /* problem larger than a fixed-size internal scratch */
+int rlloss_loss_from_logp_noalloc(const rlloss_cfg* cfg, const float* logp, const float* entropy,
+                                  const float* old_logp, const float* ref_logp, const float* adv,
+                                  const uint8_t* mask, float* out_loss, float* out_metrics,
+                                  float* out_dlogp, uint8_t* out_entropy_mask,
+                                  int32_t* out_device_status, void* stream);
+
 /* Copy the device status word of ``workspace`` (the one a previous call used)
  * into *status.  Synchronous; call after the stream has finished.  Returns
  * RLLOSS_ECUDA if the copy failed. */
