@@ -1,0 +1,59 @@
+"""Run a few fused forward+backward steps of the Qwen-0.5B LM-head workload
+recipe at a chosen token count, for profilers (ncu) to attach to.
+
+  python -m lm_head_log_tma_gb300.profile_step --T 2048 --steps 1 --warmup 2
+
+The inputs follow the workload recipe (H=896, V=151936, bf16, GMPO); the
+sampler log-probs are the policy's plus noise, with the policy log-probs
+taken from the library's own forward output of a first call.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+
+import torch
+
+from lm_head_log_tma_gb300 import rlloss as R
+from lm_head_log_tma_gb300.workloads import WORKLOADS, make_inputs
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--B", type=int, default=None)
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--steps", type=int, default=1)
+    ap.add_argument("--warmup", type=int, default=2)
+    a = ap.parse_args()
+    spec = WORKLOADS[a.workload]
+    kw = {}
+    if a.B:
+        kw["B"] = a.B
+    if a.T:
+        kw["T"] = a.T
+        if not isinstance(spec.prompt_len, tuple):
+            kw["prompt_len"] = min(spec.prompt_len, a.T // 8)
+    spec = dataclasses.replace(spec, **kw)
+    inp = make_inputs(spec, device="cuda")
+    cfg = R.make_cfg(spec.B, spec.T, spec.H, spec.V, dtype=R.BF16 if spec.dtype == "bf16" else R.FP32,
+                     loss_type=spec.loss_type, eps_low=spec.eps_low, eps_high=spec.eps_high, beta=spec.beta,
+                     temperature=spec.temperature, top_entropy_quantile=spec.top_entropy_quantile,
+                     has_bias=spec.has_bias)
+    zeros = torch.zeros(spec.N, device="cuda")
+    first = R.fwd_bwd(cfg, inp.X, inp.W, inp.b, inp.targets, zeros, zeros if spec.beta else None, inp.adv,
+                      inp.mask)
+    pol = first["logp"].clone()
+    old, ref = inp.old_logp(pol), inp.ref_logp(pol)
+    ws, outs = first["workspace"], first
+    for _ in range(a.warmup + a.steps):
+        outs = R.fwd_bwd(cfg, inp.X, inp.W, inp.b, inp.targets, old, ref, inp.adv, inp.mask, workspace=ws,
+                         outputs=outs)
+    torch.cuda.synchronize()
+    st = R.rlloss_get_device_status(ws)
+    print(f"{spec.name} B={spec.B} T={spec.T}: loss {outs['loss'].item():.6g} status {st:#x}")
+    return 0 if st == 0 else 1
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
