@@ -86,6 +86,8 @@ struct Plan {
   int Kx;                   // row width (elements) of the bf16 X / W operand arrays
   int Nc, nchunks, ld_dl;
   // workspace offsets
+  int slices;
+  size_t o_tickets, o_part;
   size_t o_status, o_partial, o_lse2, o_logp64, o_ent, o_coef, o_emask, o_k3, o_seq, o_bias2, o_dl, o_x3, o_w3,
       o_dxpart, o_dbpart, total;
 };
@@ -137,6 +139,9 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
     return o;
   };
   p.o_status = take(256);
+  p.o_tickets = take(size_t(p.B) * 4);
+  p.slices = loss_slices(p.B, p.T, p.sms);
+  p.o_part = take(size_t(p.B) * p.slices * 5 * 8);
   if (!loss_only) {
     p.H = c->H;
     p.V = c->V;
@@ -257,18 +262,24 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map, 128-byte swizzle, box {64, box_outer}; OOB reads return 0.
-bool tmap_bf16(CUtensorMap* m, const void* base, long long inner, long long outer, long long row_elems,
-               int box_outer) {
+// 2-D bf16 map; OOB reads return 0 and OOB parts of stores are dropped.
+bool tmap_bf16_box(CUtensorMap* m, const void* base, long long inner, long long outer, long long row_elems,
+                   int box_inner, int box_outer, CUtensorMapSwizzle swz) {
   EncodeTiledFn f = encode_fn();
   if (!f) return false;
   const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
   const cuuint64_t strides[1] = {cuuint64_t(row_elems) * 2};
-  const cuuint32_t box[2] = {64u, cuuint32_t(box_outer)};
+  const cuuint32_t box[2] = {cuuint32_t(box_inner), cuuint32_t(box_outer)};
   const cuuint32_t es[2] = {1u, 1u};
   return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand map: 128-byte swizzle, box {64, box_outer}.
+bool tmap_bf16(CUtensorMap* m, const void* base, long long inner, long long outer, long long row_elems,
+               int box_outer) {
+  return tmap_bf16_box(m, base, inner, outer, row_elems, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -292,6 +303,9 @@ LossParams loss_params(const rlloss_cfg* c, const Plan& p, char* ws) {
   lp.beta = double(c->beta);
   lp.inv_tau = 1.0 / double(c->temperature > 0.f ? c->temperature : 1.f);
   lp.seqres = reinterpret_cast<double*>(ws + p.o_seq);
+  lp.part = reinterpret_cast<double*>(ws + p.o_part);
+  lp.seq_ticket = reinterpret_cast<unsigned int*>(ws + p.o_tickets);
+  lp.slices = p.slices;
   lp.ticket = reinterpret_cast<unsigned int*>(ws + p.o_status + 4);
   lp.status = reinterpret_cast<int*>(ws + p.o_status);
   lp.k3 = p.ent ? reinterpret_cast<const double*>(ws + p.o_k3) : nullptr;
@@ -390,7 +404,7 @@ int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float*
   if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, 256, st));
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, p.o_tickets + size_t(p.B) * 4 - p.o_status, st));
   uint8_t* emask = reinterpret_cast<uint8_t*>(ws + p.o_emask);
   if (p.ent) {
     RL_TRY(launch_entropy_mask(entropy, mask, p.N, double(cfg->top_entropy_quantile), ws + p.o_k3, emask, st));
@@ -408,7 +422,7 @@ int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float*
   lp.out_loss = out_loss;
   lp.out_metrics = out_metrics;
   RL_TRY(launch_loss(lp, st));
-  g_launches += 1;
+  g_launches += out_dlogp ? 2 : 1;
   if (out_entropy_mask)
     RL_TRY(cudaMemcpyAsync(out_entropy_mask, p.ent ? emask : mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
   return RLLOSS_OK;
@@ -434,7 +448,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + p.o_status);
   const float scale2 = float(1.4426950408889634 / double(cfg->temperature));
-  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, 256, st));
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, p.o_tickets + size_t(p.B) * 4 - p.o_status, st));
 
   // Operand arrays: bf16 inputs are used in place; fp32 inputs are split
   // into three bf16 terms (hi, mid, lo) so the same bf16 tensor-core kernels
@@ -530,7 +544,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   lp.out_loss = out_loss;
   lp.out_metrics = out_metrics;
   RL_TRY(launch_loss(lp, st));
-  ph_loss.launched();
+  ph_loss.launched(2);
   if (out_entropy_mask)
     RL_TRY(cudaMemcpyAsync(out_entropy_mask, p.ent ? emask : mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
   }
@@ -565,6 +579,8 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     dp.coef = lp.coef;
     dp.dl = dl;
     dp.ld = p.ld_dl;
+    if (!tmap_bf16_box(&dp.tmG, dl, p.fp32 ? 2ll * p.Vp : p.V, nc, p.ld_dl, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return RLLOSS_ECUDA;
     dp.lo_off = lo_off;
     dp.status = status;
     dp.limit_ns = kWaitLimitNs;

@@ -44,7 +44,7 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 
 template <class P>
 __host__ __device__ constexpr int engine_smem_bytes() {
-  return 1024 /*alignment slack*/ + P::kStages * (P::kABytes + P::kBBytes) + 256 /*barriers*/ +
+  return 1024 /*alignment slack*/ + P::kStages * (P::kABytes + P::kBBytes) + 1024 /*barriers*/ +
          P::kExtraSmem;
 }
 
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
   uint64_t* drain = bars + 2 * S + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   int* abort_i = reinterpret_cast<int*>(tmem_slot + 1);
-  uint8_t* extra = smem + S * SB + 256;
+  uint8_t* extra = smem + S * SB + 1024;   // 1024-aligned policy scratch
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
       }
       return true;
     });
+    P::epilogue_finish(prm, lane);
   }
 
   tc_fence_before();

@@ -148,23 +148,38 @@ struct FwdPolicy {
       dst[1] = make_float4(e.w_lo, e.zy, e.found ? 1.f : 0.f, 0.f);
     }
   }
+  __device__ static void epilogue_finish(const Params&, int) {}
 };
 
-// Merge the 2P partial states of each row (fp64).  Each partial holds, for
-// one vocabulary segment and column half: reference m (log2 units, integer),
-// s = sum 2^(t-m), w = sum 2^(t-m) (t-m), and the target's t if it fell there.
+// Merge the 2P partial states of each row (fp64), one warp per row.  Each
+// partial holds, for one vocabulary segment and column half: reference m
+// (log2 units, integer), s = sum 2^(t-m), w = sum 2^(t-m) (t-m), and the
+// target's t if it fell there.
+__device__ __forceinline__ double warp_max_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 __global__ void fwd_merge_kernel(MergeParams p) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  const int row = int((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
   if (row >= p.N) return;
   const float4* base = p.partial + size_t(row) * p.slots * 2;
   double M = -INFINITY;
-  for (int k = 0; k < p.slots; ++k) {
+  for (int k = lane; k < p.slots; k += 32) {
     const float4 a = base[2 * k];
     if (a.y + a.z > 0.f) M = fmax(M, double(a.x));
   }
+  M = warp_max_d(M);
   double S = 0.0, Wd = 0.0, zy = 0.0;
   int found = 0;
-  for (int k = 0; k < p.slots; ++k) {
+  for (int k = lane; k < p.slots; k += 32) {
     const float4 a = base[2 * k];
     const float4 b = base[2 * k + 1];
     const double s = double(a.y) + double(a.z);
@@ -179,13 +194,18 @@ __global__ void fwd_merge_kernel(MergeParams p) {
       found = 1;
     }
   }
+  S = warp_sum_d(S);
+  Wd = warp_sum_d(Wd);
+  const unsigned who = __ballot_sync(0xffffffffu, found);
+  zy = __shfl_sync(0xffffffffu, zy, who ? __ffs(who) - 1 : 0);
+  if (lane != 0) return;
   const long long y = p.targets[row];
   const double ln2 = 0.6931471805599453;
   const double l2s = log2(S);
   const double lse2 = M + l2s;
   const double ent = ln2 * (l2s - Wd / S);
   double logp = ln2 * (zy - lse2);
-  if (y < 0 || y >= p.V || !found) {
+  if (y < 0 || y >= p.V || !who) {
     logp = __longlong_as_double(0x7ff8000000000000ll);
     if (p.status) atomicOr(p.status, RLLOSS_DEV_EBADTARGET);
   }
@@ -203,15 +223,19 @@ struct DlPolicy {
   static constexpr int kK16 = 4;
   static constexpr int kABytes = 128 * 64 * 2;
   static constexpr int kBBytes = 256 * 64 * 2;
-  static constexpr int kExtraSmem = 0;
+  static constexpr int kStageBuf = 32 * 64;        // one 32-row x 32-column bf16 box, 64-byte swizzle
+  static constexpr int kExtraSmem = kEpiWarps * 2 * kStageBuf;
   static constexpr uint32_t kIdesc = idesc_bf16(128, 256, 0, 0);
   using Params = DlParams;
-  struct EpiState {};
+  struct EpiState {
+    int nbuf = 0;
+  };
 
   __device__ static void cta_setup(const Params&, uint8_t*) {}
   __device__ static void prefetch(const Params& p) {
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB);
+    tma_prefetch_desc(&p.tmG);
   }
   // Tiles u = j * Rc + r: CTAs running together share the W tile j.
   template <class F>
@@ -234,8 +258,29 @@ struct DlPolicy {
   __device__ static uint64_t adesc(uint32_t sa, int k) { return sdesc_sw128(sa + k * 32, 16, 1024); }
   __device__ static uint64_t bdesc(uint32_t sa, int k) { return sdesc_sw128(sa + kABytes + k * 32, 16, 1024); }
 
-  __device__ static void epilogue(const Params& p, EpiState&, const TileInfo& t, uint32_t taddr, int q, int half,
-                                  int lane, uint8_t*) {
+  // Write one 32x32 bf16 box (this lane's 64-byte row) through shared memory
+  // with a TMA store; two staging buffers per warp alternate.
+  __device__ static void store_box(const Params& p, EpiState& e, uint8_t* wbuf, int lane, const uint32_t (&w)[16],
+                                   int x, int y) {
+    uint8_t* buf = wbuf + (e.nbuf & 1) * kStageBuf;
+    if (lane == 0) tma_store_wait_read<1>();
+    __syncwarp();
+    const int sw = (lane >> 1) & 3;
+    uint4* row = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) row[c ^ sw] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&p.tmG, buf, x, y);
+      tma_store_commit();
+    }
+    ++e.nbuf;
+  }
+
+  __device__ static void epilogue(const Params& p, EpiState& e, const TileInfo& t, uint32_t taddr, int q, int half,
+                                  int lane, uint8_t* extra) {
+    uint8_t* wbuf = extra + (q + 4 * half) * 2 * kStageBuf;
     const int rl = t.m0 + q * 32 + lane;   // row within the chunk
     const bool valid = rl < p.Nc;
     const int row = p.n0 + rl;
@@ -276,27 +321,25 @@ struct DlPolicy {
         for (int i = 0; i < 32; ++i)
           if (c0 + i >= p.V) v[i] = 0.f;
       }
-      if (valid) {
-        __nv_bfloat16* dst = p.dl + size_t(rl) * p.ld + c0;
-        uint32_t hi[16];
+      uint32_t hi[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) hi[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+      for (int i = 0; i < 16; ++i) hi[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+      const int y0 = t.m0 + q * 32;
+      store_box(p, e, wbuf, lane, hi, c0, y0);
+      if (p.lo_off) {
+        uint32_t lo[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
-        if (p.lo_off) {
-          uint32_t lo[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&hi[i]);
-            lo[i] = pack_bf16x2(v[2 * i] - __low2float(h2), v[2 * i + 1] - __high2float(h2));
-          }
-          uint4* l4 = reinterpret_cast<uint4*>(dst + p.lo_off);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) l4[i] = make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+        for (int i = 0; i < 16; ++i) {
+          const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&hi[i]);
+          lo[i] = pack_bf16x2(v[2 * i] - __low2float(h2), v[2 * i + 1] - __high2float(h2));
         }
+        store_box(p, e, wbuf, lane, lo, c0 + p.lo_off, y0);
       }
     }
+  }
+  __device__ static void epilogue_finish(const Params&, int lane) {
+    if (lane == 0) tma_store_wait_all<0>();
+    __syncwarp();
   }
 };
 
@@ -381,6 +424,7 @@ struct TPolicy {
       }
     }
   }
+  __device__ static void epilogue_finish(const Params&, int) {}
 };
 
 // =============================================================== small kernels
@@ -490,7 +534,7 @@ cudaError_t launch_gemmT(const TParams& p, int b_mn, int grid, cudaStream_t st) 
   return b_mn ? launch_engine<TPolicy<1>>(p, grid, st) : launch_engine<TPolicy<0>>(p, grid, st);
 }
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
-  fwd_merge_kernel<<<(p.N + 127) / 128, 128, 0, st>>>(p);
+  fwd_merge_kernel<<<(p.N + 7) / 8, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st) {

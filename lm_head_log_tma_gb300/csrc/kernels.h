@@ -38,6 +38,7 @@ struct MergeParams {
 
 struct DlParams {
   CUtensorMap tmA, tmB;
+  CUtensorMap tmG;            // G chunk buffer: inner columns, outer chunk rows; box 32 x 32, 64-byte swizzle
   int nseg, kb_per_seg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];
   int n0, Nc, Rc, V, Vp, Vt;  // chunk start row, rows in chunk, row tiles, vocab, padded vocab, vocab tiles
@@ -83,7 +84,10 @@ struct LossParams {
   const uint8_t* emask;       // entropy mask, or null (= mask)
   const double* k3;           // K3 state (threshold at k3[0]) or null
   double* seqres;             // [B][8]
-  unsigned int* ticket;
+  double* part;               // [B][slices][5] partial sums
+  unsigned int* seq_ticket;   // [B], zero on entry
+  unsigned int* ticket;       // zero on entry
+  int slices;                 // blocks per sequence
   float* coef;                // optional: c / tau
   float* dlogp;               // optional: c
   float* out_loss;
@@ -110,5 +114,6 @@ constexpr int kK3Bytes = 256 + 4 * 512 * 4;
 cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long N, double q, void* k3_ws,
                                 uint8_t* emask, cudaStream_t st);
 cudaError_t launch_loss(const LossParams& p, cudaStream_t st);
+int loss_slices(int B, int T, int sms);
 
 }  // namespace rl

@@ -131,7 +131,7 @@ cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long
 }
 
 // ----------------------------------------------------------------------- K2
-constexpr int kLossThreads = 512;
+constexpr int kLossThreads = 256;
 
 __device__ __forceinline__ double block_sum(double v, double* sh) {
 #pragma unroll
@@ -150,16 +150,26 @@ __device__ __forceinline__ double logp_at(const LossParams& p, long long n) {
   return p.logp_is_f64 ? static_cast<const double*>(p.logp)[n] : double(static_cast<const float*>(p.logp)[n]);
 }
 
-__global__ void __launch_bounds__(kLossThreads) loss_seq_kernel(LossParams p) {
+// Partial sums of one slice of one sequence; the last slice block of a
+// sequence folds the slices in order into the sequence record, and the last
+// sequence folds the records into the loss and metrics (fixed order, so the
+// result does not depend on block timing).
+//
+// Sequence record: [0] term of the loss, [1] n_i, [2] clip count, [3] sum of
+// KL, [4] tokens kept by the entropy mask, [5] sequence log ratio, [6]
+// sequence ratio, [7] GMPO: kept fraction ebar_i; GSPO: gradient gate.
+__global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p) {
   __shared__ double sh[32];
-  __shared__ double res[8];
   __shared__ int is_last;
-  const int i = blockIdx.x;
+  const int i = blockIdx.y;
+  const int sl = blockIdx.x;
   const long long base = (long long)i * p.T;
+  const int t0 = int((long long)sl * p.T / p.slices);
+  const int t1 = int((long long)(sl + 1) * p.T / p.slices);
   const double A = double(p.adv[i]);
   const bool gmpo = p.loss_type == RLLOSS_GMPO;
   double a_m = 0, a_x = 0, a_e = 0, a_kl = 0, a_clip = 0;
-  for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
+  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
     const long long n = base + t;
     if (!p.mask[n]) continue;
     const double lp = logp_at(p, n);
@@ -183,79 +193,55 @@ __global__ void __launch_bounds__(kLossThreads) loss_seq_kernel(LossParams p) {
   a_e = block_sum(a_e, sh);
   a_kl = block_sum(a_kl, sh);
   a_clip = block_sum(a_clip, sh);
-  // Per-sequence record: [0] term of the loss, [1] n_i, [2] clip count,
-  // [3] sum of KL, [4] tokens kept by the entropy mask, [5] sequence log
-  // ratio, [6] sequence ratio, [7] GMPO: mean mask; GSPO: gradient gate.
   if (threadIdx.x == 0) {
-    const double ni = a_m;
-    double r8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    r8[1] = ni;
-    if (gmpo) {
-      const double mean_x = ni > 0 ? a_x / ni : 0.0;
-      const double r = ni > 0 ? exp(mean_x) : 0.0;
-      const double ebar = ni > 0 ? a_e / ni : 0.0;
-      const double klt = ni > 0 ? a_kl / ni : 0.0;
-      r8[0] = ni > 0 ? -A * r * ebar + p.beta * klt : 0.0;
-      r8[2] = a_clip; r8[3] = a_kl; r8[4] = a_e; r8[5] = mean_x; r8[6] = r; r8[7] = ebar;
-    } else if (ni == 0) {
-      if (p.status) atomicOr(p.status, RLLOSS_DEV_EEMPTYSEQ);
-    } else {
-      const double slr = a_x / ni;
-      const double s = exp(slr);
-      const double sc = fmin(fmax(s, p.clip_lo), p.clip_hi);
-      r8[0] = -ni * fmin(s * A, sc * A);
-      r8[2] = (s < p.clip_lo || s > p.clip_hi) ? 1.0 : 0.0;
-      r8[4] = ni; r8[5] = slr; r8[6] = s;
-      r8[7] = ((A > 0.0 && s > p.clip_hi) || (A < 0.0 && s < p.clip_lo)) ? 0.0 : 1.0;
-    }
-    for (int k = 0; k < 8; ++k) {
-      res[k] = r8[k];
-      p.seqres[size_t(i) * 8 + k] = r8[k];
-    }
+    double* pr = p.part + (size_t(i) * p.slices + sl) * 5;
+    pr[0] = a_m; pr[1] = a_x; pr[2] = a_e; pr[3] = a_kl; pr[4] = a_clip;
+    __threadfence();
+    is_last = atomicAdd(p.seq_ticket + i, 1u) == unsigned(p.slices) - 1u;
   }
-  __syncthreads();
-
-  // Per-token gradient coefficient c_n = dL/dlogp_n.
-  if (p.coef || p.dlogp) {
-    const double ni = res[1];
-    const double inv_bn = ni > 0 ? 1.0 / (double(p.B) * ni) : 0.0;
-    for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
-      const long long n = base + t;
-      double c = 0.0;
-      if (p.mask[n] && ni > 0) {
-        if (gmpo) {
-          const double lp = logp_at(p, n);
-          const double lr = lp - double(p.old_logp[n]);
-          const bool clip = (A > 0.0 && lr > p.eps_high) || (A < 0.0 && lr < -p.eps_low);
-          c = clip ? 0.0 : -A * res[6] * res[7];
-          if (p.beta != 0.0) c += p.beta * (1.0 - exp(double(p.ref_logp[n]) - lp));
-          c *= inv_bn;
-        } else {
-          c = -A * res[6] * res[7];
-        }
-      }
-      if (p.coef) p.coef[n] = float(c * p.inv_tau);
-      if (p.dlogp) p.dlogp[n] = float(c);
-    }
-  }
-
-  // The last block to finish folds the per-sequence records, in index order.
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(p.ticket, 1u) == unsigned(p.B) - 1u);
   __syncthreads();
   if (!is_last || threadIdx.x != 0) return;
+  __threadfence();
+  double s5[5] = {0, 0, 0, 0, 0};
+  for (int k = 0; k < p.slices; ++k) {
+    const double* pr = p.part + (size_t(i) * p.slices + k) * 5;
+    for (int j = 0; j < 5; ++j) s5[j] += __ldcg(pr + j);
+  }
+  const double ni = s5[0];
+  double r8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  r8[1] = ni;
+  if (gmpo) {
+    const double mean_x = ni > 0 ? s5[1] / ni : 0.0;
+    const double r = ni > 0 ? exp(mean_x) : 0.0;
+    const double ebar = ni > 0 ? s5[2] / ni : 0.0;
+    const double klt = ni > 0 ? s5[3] / ni : 0.0;
+    r8[0] = ni > 0 ? -A * r * ebar + p.beta * klt : 0.0;
+    r8[2] = s5[4]; r8[3] = s5[3]; r8[4] = s5[2]; r8[5] = mean_x; r8[6] = r; r8[7] = ebar;
+  } else if (ni == 0) {
+    if (p.status) atomicOr(p.status, RLLOSS_DEV_EEMPTYSEQ);
+  } else {
+    const double slr = s5[1] / ni;
+    const double sv = exp(slr);
+    const double sc = fmin(fmax(sv, p.clip_lo), p.clip_hi);
+    r8[0] = -ni * fmin(sv * A, sc * A);
+    r8[2] = (sv < p.clip_lo || sv > p.clip_hi) ? 1.0 : 0.0;
+    r8[4] = ni; r8[5] = slr; r8[6] = sv;
+    r8[7] = ((A > 0.0 && sv > p.clip_hi) || (A < 0.0 && sv < p.clip_lo)) ? 0.0 : 1.0;
+  }
+  for (int k = 0; k < 8; ++k) p.seqres[size_t(i) * 8 + k] = r8[k];
+  __threadfence();
+  if (atomicAdd(p.ticket, 1u) != unsigned(p.B) - 1u) return;
   __threadfence();
   double loss = 0, n_act = 0, clip = 0, kl = 0, kept = 0, sx = 0, sr = 0, nh = 0;
   for (int j = 0; j < p.B; ++j) {
     const double* r = p.seqres + size_t(j) * 8;
-    const double ni = __ldcg(r + 1);
+    const double nj = __ldcg(r + 1);
     loss += __ldcg(r + 0);
-    n_act += ni;
+    n_act += nj;
     clip += __ldcg(r + 2);
     kl += __ldcg(r + 3);
     kept += __ldcg(r + 4);
-    if (ni > 0) {
+    if (nj > 0) {
       sx += __ldcg(r + 5);
       sr += __ldcg(r + 6);
       nh += 1.0;
@@ -278,11 +264,51 @@ __global__ void __launch_bounds__(kLossThreads) loss_seq_kernel(LossParams p) {
   m[7] = nh > 0 ? float(sr / nh) : 0.f;
   *p.out_loss = float(loss);
   if (!isfinite(loss) && p.status) atomicOr(p.status, RLLOSS_DEV_ENONFINITE);
-  *p.ticket = 0u;
+}
+
+// Per-token gradient coefficient c_n = dL/dlogp_n from the sequence records.
+__global__ void loss_coef_kernel(LossParams p) {
+  const long long N = (long long)p.B * p.T;
+  const bool gmpo = p.loss_type == RLLOSS_GMPO;
+  for (long long n = blockIdx.x * (long long)blockDim.x + threadIdx.x; n < N; n += (long long)gridDim.x * blockDim.x) {
+    const int i = int(n / p.T);
+    const double* r = p.seqres + size_t(i) * 8;
+    const double ni = r[1];
+    double c = 0.0;
+    if (p.mask[n] && ni > 0) {
+      const double A = double(p.adv[i]);
+      if (gmpo) {
+        const double lp = logp_at(p, n);
+        const double lr = lp - double(p.old_logp[n]);
+        const bool clip = (A > 0.0 && lr > p.eps_high) || (A < 0.0 && lr < -p.eps_low);
+        c = clip ? 0.0 : -A * r[6] * r[7];
+        if (p.beta != 0.0) c += p.beta * (1.0 - exp(double(p.ref_logp[n]) - lp));
+        c /= double(p.B) * ni;
+      } else {
+        c = -A * r[6] * r[7];
+      }
+    }
+    if (p.coef) p.coef[n] = float(c * p.inv_tau);
+    if (p.dlogp) p.dlogp[n] = float(c);
+  }
+}
+
+int loss_slices(int B, int T, int sms) {
+  long long s = (4ll * sms + B - 1) / B;
+  const long long smax = (T + 255) / 256;
+  if (s > smax) s = smax;
+  if (s < 1) s = 1;
+  return int(s);
 }
 
 cudaError_t launch_loss(const LossParams& p, cudaStream_t st) {
-  loss_seq_kernel<<<p.B, kLossThreads, 0, st>>>(p);
+  loss_partial_kernel<<<dim3(p.slices, p.B), kLossThreads, 0, st>>>(p);
+  if (p.coef || p.dlogp) {
+    const long long N = (long long)p.B * p.T;
+    long long nb = (N + 255) / 256;
+    if (nb > 4096) nb = 4096;
+    loss_coef_kernel<<<int(nb), 256, 0, st>>>(p);
+  }
   return cudaGetLastError();
 }
 
