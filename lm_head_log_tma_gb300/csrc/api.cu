@@ -53,7 +53,7 @@ int validate_common(const rlloss_cfg* c) {
   if (!finite(c->beta)) return RLLOSS_EINVAL;
   const float q = c->top_entropy_quantile;
   if (!(q >= 0.f && q <= 1.f)) return RLLOSS_EINVAL;
-  if (c->flags & ~RLLOSS_FLAG_FORCE_ENTROPY_PATH) return RLLOSS_EINVAL;
+  if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES)) return RLLOSS_EINVAL;
   if (c->loss_type == RLLOSS_GSPO_TOKEN) {
     if (c->beta != 0.f) return RLLOSS_EUNSUPPORTED;
     if (q < 1.f || (c->flags & RLLOSS_FLAG_FORCE_ENTROPY_PATH)) return RLLOSS_EUNSUPPORTED;
@@ -80,6 +80,7 @@ bool entropy_path(const rlloss_cfg* c) {
 
 struct Plan {
   int B, T, N, H, V, sms;
+  int pair, rows_tile;      // CTAs per LM-head tile (1 or 2) and rows per tile
   bool fp32, bias, ent;
   int R, Vt, P, Hp, Vp;
   int kb_fwd, nseg_fwd;     // forward K: nseg_fwd * kb_fwd k-blocks
@@ -147,9 +148,11 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
     p.V = c->V;
     p.fp32 = c->dtype == RLLOSS_FP32;
     p.bias = c->has_bias != 0;
-    p.R = int(cdiv(p.N, 128));
+    p.pair = (c->flags & RLLOSS_FLAG_SINGLE_CTA_TILES) ? 1 : 2;
+    p.rows_tile = 128 * p.pair;
+    p.R = int(cdiv(p.N, p.rows_tile));
     p.Vt = int(cdiv(p.V, 256));
-    p.P = choose_segments(p.R, p.Vt, p.sms, p.N);
+    p.P = choose_segments(p.R, p.Vt, p.sms / p.pair, p.N);
     p.Hp = int(rup(p.H, 64));
     p.Vp = int(rup(p.V, 64));
     if (p.fp32) {
@@ -486,7 +489,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   // ---- forward: tensor-core logits + streamed row state
   FwdParams fp{};
   if (!tmap_bf16(&fp.tmA, Xop, p.Kx, p.N, p.Kx, 128)) return RLLOSS_ECUDA;
-  if (!tmap_bf16(&fp.tmB, Wop, p.Kx, p.V, p.Kx, 256)) return RLLOSS_ECUDA;
+  if (!tmap_bf16(&fp.tmB, Wop, p.Kx, p.V, p.Kx, 256 / p.pair)) return RLLOSS_ECUDA;
   fp.nseg = p.nseg_fwd;
   fp.kb_per_seg = p.kb_fwd;
   std::memcpy(fp.seg_a, seg_a, sizeof(seg_a));
@@ -504,7 +507,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   fp.limit_ns = kWaitLimitNs;
   {
     Phase ph(st, 0);
-    RL_TRY(launch_fwd(fp, std::min(p.sms, p.R * p.P), st));
+    RL_TRY(launch_fwd(fp, p.pair * std::min(p.sms / p.pair, p.R * p.P), p.pair, st));
     ph.launched();
   }
 
@@ -557,7 +560,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   for (int ch = 0; ch < p.nchunks; ++ch) {
     const int n0 = ch * p.Nc;
     const int nc = std::min(p.Nc, p.N - n0);
-    const int Rc = int(cdiv(nc, 128));
+    const int Rc = int(cdiv(nc, p.rows_tile));
 
     DlParams dp{};
     dp.tmA = fp.tmA;
@@ -586,7 +589,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     dp.limit_ns = kWaitLimitNs;
     {
       Phase ph(st, 2);
-      RL_TRY(launch_dl(dp, std::min(p.sms, Rc * p.Vt), st));
+      RL_TRY(launch_dl(dp, p.pair * std::min(p.sms / p.pair, Rc * p.Vt), p.pair, st));
       ph.launched();
     }
 

@@ -7,6 +7,15 @@
 //   warps 4..11        : epilogue; warp w reads TMEM lanes 32*(w%4)..+31 and
 //                        column half (w-4)/4 of the accumulator
 //
+// Pair mode (P::kPair == 2, launched as clusters of 2 CTAs): one tile is
+// 256 rows; each CTA loads its own 128 rows of A and its half of the B rows
+// into its own shared memory, and holds its 128 rows of the accumulator in
+// its own TMEM.  The leader CTA (rank 0) issues cta_group::2 MMAs over both
+// CTAs' operands.  TMA completions of both CTAs are counted on the leader's
+// "full" barriers; the leader's commits release both CTAs' stages and
+// accumulators (multicast); both CTAs' epilogues report a drained
+// accumulator on the leader's "empty" barrier.
+//
 // A policy class supplies the tile schedule, the TMA loads of one k-block,
 // the shared-memory descriptors of one K=16 step and the epilogue.  Every
 // wait is bounded (see mbar_wait); when one role gives up, the others stop at
@@ -23,7 +32,7 @@ constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 
 struct TileInfo {
-  int m0;        // first row of the 128-row accumulator (A rows)
+  int m0;        // first row of the accumulator tile (A rows; 256 per tile in pair mode)
   int n0;        // first column of the accumulator (B rows)
   int kb_begin;  // k-block range
   int kb_end;
@@ -42,6 +51,12 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   }
 }
 
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
+  }
+}
+
 template <class P>
 __host__ __device__ constexpr int engine_smem_bytes() {
   return 1024 /*alignment slack*/ + P::kStages * (P::kABytes + P::kBBytes) + 1024 /*barriers*/ +
@@ -50,6 +65,7 @@ __host__ __device__ constexpr int engine_smem_bytes() {
 
 template <class P>
 __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __grid_constant__ typename P::Params prm) {
+  constexpr bool kPair = P::kPair == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -67,6 +83,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -75,22 +92,29 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kEpiWarps);
+      mbar_init(&tempty[i], kEpiWarps * (kPair ? 2 : 1));
     }
     mbar_init(drain, 1);
     *abort_i = 0;
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   P::cta_setup(prm, extra);
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const AbortCtl ac{abort_i, prm.status, prm.limit_ns};
+  bool aborted = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -98,12 +122,12 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
       int stage = 0;
       uint32_t ph = 0;
       int issued = 0;
-      bool ok = true;
       P::for_each_tile(prm, [&](const TileInfo& t) -> bool {
         for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-          if (!mbar_wait(&empty[stage], ph ^ 1u, ac)) return ok = false;
-          mbar_expect_tx(&full[stage], SB);
-          P::load(prm, smem + stage * SB, &full[stage], t, kb);
+          if (!mbar_wait(&empty[stage], ph ^ 1u, ac)) { aborted = true; return false; }
+          const uint32_t fb = smem_u32(&full[stage]);
+          if (!kPair || rank == 0) mbar_expect_tx(&full[stage], kPair ? 2 * SB : SB);
+          P::load(prm, smem + stage * SB, kPair ? mapa_shared(fb, 0) : fb, t, kb, rank);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -112,51 +136,67 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
         }
         return true;
       });
-      if (!ok) {
+      if (aborted) {
         // Let every copy this thread started land before the CTA can exit.
-        for (int j = 0; j < S && j < issued; ++j) {
-          if (--stage < 0) {
-            stage = S - 1;
-            ph ^= 1u;
+        if (!kPair || rank == 0) {
+          for (int j = 0; j < S && j < issued; ++j) {
+            if (--stage < 0) {
+              stage = S - 1;
+              ph ^= 1u;
+            }
+            mbar_wait_drain(&full[stage], ph, 20000000ull);
           }
-          mbar_wait_drain(&full[stage], ph, 20000000ull);
+        } else {
+          spin_ns(2000000ull);   // the peer's copies are counted on the leader's barriers
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (!kPair || rank == 0)) {
       int stage = 0;
       uint32_t ph = 0;
       int acc = 0;
       uint32_t aph = 0;
-      bool ok = true;
       P::for_each_tile(prm, [&](const TileInfo& t) -> bool {
-        if (!mbar_wait(&tempty[acc], aph ^ 1u, ac)) return ok = false;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, ac)) { aborted = true; return false; }
         tc_fence_after();
         const uint32_t d = tmem + uint32_t(acc * P::kBN);
         for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-          if (!mbar_wait(&full[stage], ph, ac)) return ok = false;
+          if (!mbar_wait(&full[stage], ph, ac)) { aborted = true; return false; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * SB);
 #pragma unroll
           for (int k = 0; k < P::kK16; ++k) {
-            umma_bf16(d, P::adesc(sa, k), P::bdesc(sa, k), P::kIdesc, (kb > t.kb_begin || k > 0) ? 1u : 0u);
+            const uint32_t accum = (kb > t.kb_begin || k > 0) ? 1u : 0u;
+            if constexpr (kPair)
+              umma_bf16_pair(d, P::adesc(sa, k), P::bdesc(sa, k), P::kIdesc, accum);
+            else
+              umma_bf16(d, P::adesc(sa, k), P::bdesc(sa, k), P::kIdesc, accum);
           }
-          umma_commit(&empty[stage]);
+          if constexpr (kPair)
+            umma_commit_pair_mc(&empty[stage], 0x3);
+          else
+            umma_commit(&empty[stage]);
           if (++stage == S) {
             stage = 0;
             ph ^= 1u;
           }
         }
-        umma_commit(&tfull[acc]);
+        if constexpr (kPair)
+          umma_commit_pair_mc(&tfull[acc], 0x3);
+        else
+          umma_commit(&tfull[acc]);
         if (++acc == 2) {
           acc = 0;
           aph ^= 1u;
         }
         return true;
       });
-      if (!ok) {
-        umma_commit(drain);
+      if (aborted) {
+        if constexpr (kPair)
+          umma_commit_pair(drain);
+        else
+          umma_commit(drain);
         mbar_wait_drain(drain, 0, 20000000ull);
       }
     }
@@ -170,10 +210,15 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
       const bool got = mbar_wait(&tfull[acc], aph, ac);
       if (!__all_sync(0xffffffffu, got)) return false;
       tc_fence_after();
-      P::epilogue(prm, st, t, tmem + uint32_t(acc * P::kBN) + (uint32_t(q * 32) << 16), q, half, lane, extra);
+      P::epilogue(prm, st, t, tmem + uint32_t(acc * P::kBN) + (uint32_t(q * 32) << 16), q, half, lane, extra, rank);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if constexpr (kPair)
+          mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
+        else
+          mbar_arrive(&tempty[acc]);
+      }
       if (++acc == 2) {
         acc = 0;
         aph ^= 1u;
@@ -185,8 +230,14 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 2) {
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 }  // namespace rl

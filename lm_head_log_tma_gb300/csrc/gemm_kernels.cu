@@ -19,14 +19,18 @@
 namespace rl {
 
 // =============================================================== forward
+// PAIR = 2: 256-row tiles over a CTA pair (cta_group::2); PAIR = 1: 128-row tiles.
+template <int PAIR>
 struct FwdPolicy {
-  static constexpr int kStages = 4;
+  static constexpr int kPair = PAIR;
+  static constexpr int kRows = 128 * PAIR;           // accumulator rows per tile (both CTAs)
+  static constexpr int kStages = PAIR == 2 ? 6 : 4;
   static constexpr int kBN = 256;
   static constexpr int kK16 = 4;
   static constexpr int kABytes = 128 * 64 * 2;
-  static constexpr int kBBytes = 256 * 64 * 2;
+  static constexpr int kBBytes = (256 / PAIR) * 64 * 2;   // this CTA's share of the B rows
   static constexpr int kExtraSmem = 0;
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, 0, 0);
+  static constexpr uint32_t kIdesc = idesc_bf16(kRows, 256, 0, 0);
   using Params = FwdParams;
 
   struct EpiState {
@@ -47,30 +51,36 @@ struct FwdPolicy {
   __device__ static void for_each_tile(const Params& p, F&& f) {
     const int units = p.R * p.P;
     const int kbs = p.nseg * p.kb_per_seg;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int g0 = blockIdx.x / PAIR, gn = gridDim.x / PAIR;
+    for (int u = g0; u < units; u += gn) {
       const int seg = u / p.R;
       const int r = u - seg * p.R;
       const int j0 = int((long long)seg * p.Vt / p.P);
       const int j1 = int((long long)(seg + 1) * p.Vt / p.P);
       for (int j = j0; j < j1; ++j) {
-        TileInfo t{r * 128, j * 256, 0, kbs, u, seg, j == j0, j == j1 - 1};
+        TileInfo t{r * kRows, j * 256, 0, kbs, u, seg, j == j0, j == j1 - 1};
         if (!f(t)) return;
       }
     }
   }
 
-  __device__ static void load(const Params& p, uint8_t* st, uint64_t* bar, const TileInfo& t, int kb) {
+  __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int s = kb / p.kb_per_seg;
     const int kk = (kb - s * p.kb_per_seg) * 64;
-    tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0);
-    tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+    if constexpr (PAIR == 2) {
+      tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0 + 128 * int(rank));
+      tma_load_2d_pair(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0 + 128 * int(rank));
+    } else {
+      tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0);
+      tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+    }
   }
   __device__ static uint64_t adesc(uint32_t sa, int k) { return sdesc_sw128(sa + k * 32, 16, 1024); }
   __device__ static uint64_t bdesc(uint32_t sa, int k) { return sdesc_sw128(sa + kABytes + k * 32, 16, 1024); }
 
   __device__ static void epilogue(const Params& p, EpiState& e, const TileInfo& t, uint32_t taddr, int q, int half,
-                                  int lane, uint8_t*) {
-    const int row = t.m0 + q * 32 + lane;
+                                  int lane, uint8_t*, uint32_t rank) {
+    const int row = t.m0 + 128 * int(rank) + q * 32 + lane;
     if (t.first) {
       e.mref = -INFINITY;
       e.s_hi = e.s_lo = e.w_hi = e.w_lo = 0.f;
@@ -217,15 +227,18 @@ __global__ void fwd_merge_kernel(MergeParams p) {
 }
 
 // =============================================================== dlogits
+template <int PAIR>
 struct DlPolicy {
-  static constexpr int kStages = 4;
+  static constexpr int kPair = PAIR;
+  static constexpr int kRows = 128 * PAIR;
+  static constexpr int kStages = PAIR == 2 ? 6 : 4;
   static constexpr int kBN = 256;
   static constexpr int kK16 = 4;
   static constexpr int kABytes = 128 * 64 * 2;
-  static constexpr int kBBytes = 256 * 64 * 2;
+  static constexpr int kBBytes = (256 / PAIR) * 64 * 2;
   static constexpr int kStageBuf = 32 * 64;        // one 32-row x 32-column bf16 box, 64-byte swizzle
   static constexpr int kExtraSmem = kEpiWarps * 2 * kStageBuf;
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, 0, 0);
+  static constexpr uint32_t kIdesc = idesc_bf16(kRows, 256, 0, 0);
   using Params = DlParams;
   struct EpiState {
     int nbuf = 0;
@@ -242,18 +255,24 @@ struct DlPolicy {
   __device__ static void for_each_tile(const Params& p, F&& f) {
     const int tiles = p.Rc * p.Vt;
     const int kbs = p.nseg * p.kb_per_seg;
-    for (int u = blockIdx.x; u < tiles; u += gridDim.x) {
+    const int g0 = blockIdx.x / PAIR, gn = gridDim.x / PAIR;
+    for (int u = g0; u < tiles; u += gn) {
       const int j = u / p.Rc;
       const int r = u - j * p.Rc;
-      TileInfo t{r * 128, j * 256, 0, kbs, u, 0, true, true};
+      TileInfo t{r * kRows, j * 256, 0, kbs, u, 0, true, true};
       if (!f(t)) return;
     }
   }
-  __device__ static void load(const Params& p, uint8_t* st, uint64_t* bar, const TileInfo& t, int kb) {
+  __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int s = kb / p.kb_per_seg;
     const int kk = (kb - s * p.kb_per_seg) * 64;
-    tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0);
-    tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+    if constexpr (PAIR == 2) {
+      tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0 + 128 * int(rank));
+      tma_load_2d_pair(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0 + 128 * int(rank));
+    } else {
+      tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0);
+      tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+    }
   }
   __device__ static uint64_t adesc(uint32_t sa, int k) { return sdesc_sw128(sa + k * 32, 16, 1024); }
   __device__ static uint64_t bdesc(uint32_t sa, int k) { return sdesc_sw128(sa + kABytes + k * 32, 16, 1024); }
@@ -279,9 +298,10 @@ struct DlPolicy {
   }
 
   __device__ static void epilogue(const Params& p, EpiState& e, const TileInfo& t, uint32_t taddr, int q, int half,
-                                  int lane, uint8_t* extra) {
+                                  int lane, uint8_t* extra, uint32_t rank) {
     uint8_t* wbuf = extra + (q + 4 * half) * 2 * kStageBuf;
-    const int rl = t.m0 + q * 32 + lane;   // row within the chunk
+    const int r0 = t.m0 + 128 * int(rank) + q * 32;   // first row of this warp within the chunk
+    const int rl = r0 + lane;
     const bool valid = rl < p.Nc;
     const int row = p.n0 + rl;
     const float lse2 = valid ? p.lse2[row] : 0.f;
@@ -324,7 +344,7 @@ struct DlPolicy {
       uint32_t hi[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) hi[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-      const int y0 = t.m0 + q * 32;
+      const int y0 = r0;
       store_box(p, e, wbuf, lane, hi, c0, y0);
       if (p.lo_off) {
         uint32_t lo[16];
@@ -347,6 +367,7 @@ struct DlPolicy {
 // h-major output: TMEM lane = h (M = 128), columns = output rows (N = 256).
 template <int B_MN>
 struct TPolicy {
+  static constexpr int kPair = 1;
   static constexpr int kStages = 4;
   static constexpr int kBN = 256;
   static constexpr int kK16 = 4;
@@ -379,7 +400,7 @@ struct TPolicy {
       if (!f(t)) return;
     }
   }
-  __device__ static void load(const Params& p, uint8_t* st, uint64_t* bar, const TileInfo& t, int kb) {
+  __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t) {
     const int s = kb / p.kb_per_seg;
     const int kk = (kb - s * p.kb_per_seg) * 64;
     // A: MN-major, inner = h, outer = k
@@ -401,7 +422,7 @@ struct TPolicy {
   }
 
   __device__ static void epilogue(const Params& p, EpiState&, const TileInfo& t, uint32_t taddr, int q, int half,
-                                  int lane, uint8_t*) {
+                                  int lane, uint8_t*, uint32_t) {
     const int h = t.m0 + q * 32 + lane;
     const bool hv = h < p.Hout;
 #pragma unroll 1
@@ -518,18 +539,40 @@ __global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
 template <class P>
 static cudaError_t launch_engine(const typename P::Params& prm, int grid, cudaStream_t st) {
   constexpr int smem = engine_smem_bytes<P>();
-  static bool attr_set = false;
-  if (!attr_set) {
+  static_assert(smem <= 232448, "shared memory budget");
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static unsigned long long attr_set = 0;   // one bit per device
+  if (dev < 64 && !(attr_set >> dev & 1ull)) {
     cudaError_t e = cudaFuncSetAttribute(tc_engine_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set |= 1ull << dev;
   }
-  tc_engine_kernel<P><<<grid, kEngineThreads, smem, st>>>(prm);
-  return cudaGetLastError();
+  if (P::kPair == 1) {
+    tc_engine_kernel<P><<<grid, kEngineThreads, smem, st>>>(prm);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid), 1, 1);
+  cfg.blockDim = dim3(kEngineThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_engine_kernel<P>, prm);
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t st) { return launch_engine<FwdPolicy>(p, grid, st); }
-cudaError_t launch_dl(const DlParams& p, int grid, cudaStream_t st) { return launch_engine<DlPolicy>(p, grid, st); }
+cudaError_t launch_fwd(const FwdParams& p, int grid, int pair, cudaStream_t st) {
+  return pair == 2 ? launch_engine<FwdPolicy<2>>(p, grid, st) : launch_engine<FwdPolicy<1>>(p, grid, st);
+}
+cudaError_t launch_dl(const DlParams& p, int grid, int pair, cudaStream_t st) {
+  return pair == 2 ? launch_engine<DlPolicy<2>>(p, grid, st) : launch_engine<DlPolicy<1>>(p, grid, st);
+}
 cudaError_t launch_gemmT(const TParams& p, int b_mn, int grid, cudaStream_t st) {
   return b_mn ? launch_engine<TPolicy<1>>(p, grid, st) : launch_engine<TPolicy<0>>(p, grid, st);
 }

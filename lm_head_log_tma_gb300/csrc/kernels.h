@@ -15,7 +15,7 @@ struct FwdParams {
   CUtensorMap tmB;            // W (or split): inner K, outer vocab; box 64 x 256
   int nseg, kb_per_seg;       // K = nseg * kb_per_seg * 64
   int seg_a[kMaxSeg], seg_b[kMaxSeg];  // K offsets of each product term
-  int N, V, R, Vt, P;         // rows, vocab, row tiles, vocab tiles (256), vocab segments
+  int N, V, R, Vt, P;         // rows, vocab, row tiles (128 or 256 rows), vocab tiles (256), vocab segments
   float scale2;               // log2(e) / temperature
   const float* bias2;         // [Vt*256] b * scale2, zero padded; null without bias
   const int64_t* targets;
@@ -41,7 +41,7 @@ struct DlParams {
   CUtensorMap tmG;            // G chunk buffer: inner columns, outer chunk rows; box 32 x 32, 64-byte swizzle
   int nseg, kb_per_seg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];
-  int n0, Nc, Rc, V, Vp, Vt;  // chunk start row, rows in chunk, row tiles, vocab, padded vocab, vocab tiles
+  int n0, Nc, Rc, V, Vp, Vt;  // chunk start row, rows in chunk, row tiles (128 or 256 rows), vocab, padded vocab, vocab tiles
   float scale2;
   const float* bias2;
   const int64_t* targets;
@@ -95,9 +95,10 @@ struct LossParams {
   int* status;
 };
 
-cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t st);
+// pair = 2: clusters of two CTAs with 256-row tiles (grid counts CTAs, even)
+cudaError_t launch_fwd(const FwdParams& p, int grid, int pair, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
-cudaError_t launch_dl(const DlParams& p, int grid, cudaStream_t st);
+cudaError_t launch_dl(const DlParams& p, int grid, int pair, cudaStream_t st);
 cudaError_t launch_gemmT(const TParams& p, int b_mn, int grid, cudaStream_t st);
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st);
 cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __nv_bfloat16* out, cudaStream_t st);

@@ -23,6 +23,7 @@ BF16, FP32 = 0, 1
 GMPO, GSPO_TOKEN = 0, 1
 IS_TOKEN, IS_SEQUENCE = 0, 1
 FLAG_FORCE_ENTROPY_PATH = 0x1
+FLAG_SINGLE_CTA_TILES = 0x2
 NMETRICS = 8
 
 
