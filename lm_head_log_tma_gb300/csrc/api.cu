@@ -21,7 +21,6 @@ using namespace rl;
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
 constexpr size_t kPartialCapBytes = size_t(64) << 20;
-constexpr int kDefaultChunk = 8192;
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 inline long long rup(long long a, long long b) { return cdiv(a, b) * b; }
@@ -70,6 +69,7 @@ int validate_full(const rlloss_cfg* c) {
   if (c->has_bias != 0 && c->has_bias != 1) return RLLOSS_EINVAL;
   if (c->chunk_rows < 0) return RLLOSS_EINVAL;
   if (c->dtype == RLLOSS_BF16 && (c->H % 8) != 0) return RLLOSS_EUNSUPPORTED;  // TMA row stride: 16 bytes
+  if ((c->H % 4) != 0) return RLLOSS_EUNSUPPORTED;                            // fp32 dX / dW rows: 16 bytes
   if (c->H > 65536 || c->V > (1 << 30)) return RLLOSS_EUNSUPPORTED;
   return RLLOSS_OK;
 }
@@ -90,26 +90,8 @@ struct Plan {
   int slices;
   size_t o_tickets, o_part;
   size_t o_status, o_partial, o_lse2, o_logp64, o_ent, o_coef, o_emask, o_k3, o_seq, o_bias2, o_dl, o_x3, o_w3,
-      o_dxpart, o_dbpart, total;
+      o_dbpart, total;
 };
-
-// k splits of the dX GEMM when its tiles alone would leave SMs idle; the
-// partial slices are summed in a fixed order afterwards.  At most one split
-// per k-block, so every slice is written.
-int dx_splits(int H, int nc, int kblocks, int sms) {
-  const long long tiles = cdiv(H, 128) * cdiv(nc, 256);
-  if (tiles >= sms) return 1;
-  int best_s = 1;
-  double best = 1e30;
-  for (int s = 1; s <= std::min(16, kblocks); ++s) {
-    const double t = double(cdiv(tiles * s, sms)) / s;
-    if (t < best - 1e-9) {
-      best = t;
-      best_s = s;
-    }
-  }
-  return best_s;
-}
 
 int choose_segments(int R, int Vt, int G, long long N) {
   int best = 1;
@@ -164,7 +146,12 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
       p.kb_fwd = int(cdiv(p.H, 64));
       p.Kx = p.H;
     }
-    const int want = c->chunk_rows > 0 ? int(rup(c->chunk_rows, 128)) : kDefaultChunk;
+    // Default chunk: a whole number of dX pair tiles per pair of SMs (one or
+    // two waves of 256-row x 224-h tiles).
+    const int hts = int(cdiv(p.H, 224));
+    const int per_wave = 256 * std::max(1, (p.sms / 2) / hts);
+    const int base_chunk = p.N > 2 * per_wave ? 2 * per_wave : per_wave;
+    const int want = c->chunk_rows > 0 ? int(rup(c->chunk_rows, 256)) : std::max(base_chunk, 1024);
     p.Nc = int(std::min<long long>(want, rup(p.N, 128)));
     p.nchunks = int(cdiv(p.N, p.Nc));
     p.ld_dl = p.fp32 ? 2 * p.Vp : p.Vp;
@@ -182,12 +169,6 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
     p.o_dl = take(size_t(p.Nc) * p.ld_dl * 2);
     p.o_x3 = take(p.fp32 ? size_t(p.N) * 3 * p.Hp * 2 : 0);
     p.o_w3 = take(p.fp32 ? size_t(p.V) * 3 * p.Hp * 2 : 0);
-    size_t dxp = 0;
-    for (int nc : {p.Nc, p.N - (p.nchunks - 1) * p.Nc}) {
-      const int sp = dx_splits(p.H, nc, (p.fp32 ? 3 : 1) * int(cdiv(p.V, 64)), p.sms);
-      if (sp > 1) dxp = std::max(dxp, size_t(sp) * nc * p.H * 4);
-    }
-    p.o_dxpart = take(dxp);
     p.o_dbpart = take(p.bias ? size_t(db_part_rows(p.Nc)) * p.V * 4 : 0);
   }
   p.total = off;
@@ -285,6 +266,19 @@ bool tmap_bf16(CUtensorMap* m, const void* base, long long inner, long long oute
   return tmap_bf16_box(m, base, inner, outer, row_elems, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// fp32 output map for TMA stores / reduce-adds: box 32 x 32, 128-byte swizzle.
+bool tmap_f32_out(CUtensorMap* m, const float* base, long long inner, long long outer) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+  const cuuint64_t strides[1] = {cuuint64_t(inner) * 4};
+  const cuuint32_t box[2] = {32u, 32u};
+  const cuuint32_t es[2] = {1u, 1u};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? RLLOSS_OK : RLLOSS_ECUDA; }
@@ -293,6 +287,19 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? RLLOSS_OK : RLLOSS_ECUDA;
     cudaError_t _e = (x);            \
     if (_e != cudaSuccess) return RLLOSS_ECUDA; \
   } while (0)
+
+// K-segments of the dX / dW GEMMs.  bf16: one product.  fp32: G = G_hi + G_lo
+// and W (or X) = hi + mid + lo; the products G_hi*hi, G_hi*mid, G_lo*hi.
+void set_bwd_segments(HParams& hp, const Plan& p) {
+  if (p.fp32) {
+    hp.nseg = 3;
+    hp.seg_a[0] = 0;    hp.seg_b[0] = 0;
+    hp.seg_a[1] = 0;    hp.seg_b[1] = p.Hp;
+    hp.seg_a[2] = p.Vp; hp.seg_b[2] = 0;
+  } else {
+    hp.nseg = 1;
+  }
+}
 
 LossParams loss_params(const rlloss_cfg* c, const Plan& p, char* ws) {
   LossParams lp{};
@@ -556,7 +563,6 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   //      G = (c/tau)(onehot - p) as bf16, dX = G W, dW += G^T X, db += sum G.
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dl);
   const int lo_off = p.fp32 ? p.Vp : 0;
-  const int Mt = int(cdiv(p.H, 128));
   for (int ch = 0; ch < p.nchunks; ++ch) {
     const int n0 = ch * p.Nc;
     const int nc = std::min(p.Nc, p.N - n0);
@@ -593,79 +599,48 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       ph.launched();
     }
 
-    // dX rows of this chunk: dX^T[h, n] = sum_v W[v, h] G[n, v]
+    // dX rows of this chunk: dX[n][h] = sum_v G[n][v] W[v][h]
     {
-      TParams tp{};
-      const long long a_inner = p.fp32 ? 3ll * p.Hp : p.H;
-      if (!tmap_bf16(&tp.tmA, Wop, a_inner, p.V, a_inner, 64)) return RLLOSS_ECUDA;
-      const long long b_inner = p.fp32 ? 2ll * p.Vp : p.V;
-      if (!tmap_bf16(&tp.tmB, dl, b_inner, nc, p.ld_dl, 256)) return RLLOSS_ECUDA;
-      tp.kb_per_seg = int(cdiv(p.V, 64));
-      if (p.fp32) {
-        tp.nseg = 3;   // G_hi*W_hi, G_hi*W_mid, G_lo*W_hi
-        tp.seg_a[0] = 0; tp.seg_b[0] = 0;
-        tp.seg_a[1] = p.Hp; tp.seg_b[1] = 0;
-        tp.seg_a[2] = 0; tp.seg_b[2] = p.Vp;
-      } else {
-        tp.nseg = 1;
-      }
-      tp.Mt = Mt;
-      tp.Nt = int(cdiv(nc, 256));
-      const int tiles = tp.Mt * tp.Nt;
-      const int splits = dx_splits(p.H, nc, tp.nseg * tp.kb_per_seg, p.sms);
-      tp.splits = splits;
-      tp.Hout = p.H;
-      tp.Ncols = nc;
-      tp.ldo = p.H;
-      float* dx_rows = dX + size_t(n0) * p.H;
-      if (splits > 1) {
-        tp.out = reinterpret_cast<float*>(ws + p.o_dxpart);
-        tp.split_stride = (long long)nc * p.H;
-        tp.mode = 2;
-      } else {
-        tp.out = dx_rows;
-        tp.mode = 0;
-      }
-      tp.status = status;
-      tp.limit_ns = kWaitLimitNs;
+      HParams hp{};
+      const long long g_inner = p.fp32 ? 2ll * p.Vp : p.V;
+      if (!tmap_bf16(&hp.tmA, dl, g_inner, nc, p.ld_dl, 128)) return RLLOSS_ECUDA;
+      if (!tmap_bf16(&hp.tmB, Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
+      if (!tmap_f32_out(&hp.tmO, dX + size_t(n0) * p.H, p.H, nc)) return RLLOSS_ECUDA;
+      hp.kb_per_seg = int(cdiv(p.V, 64));
+      set_bwd_segments(hp, p);
+      hp.a_outer0 = 0;
+      hp.b_outer0 = 0;
+      hp.Mt = int(cdiv(nc, 256));
+      hp.Ht = int(cdiv(p.H, 224));
+      hp.Hout = p.H;
+      hp.order = 0;
+      hp.reduce = 0;
+      hp.status = status;
+      hp.limit_ns = kWaitLimitNs;
       Phase ph(st, 3);
-      RL_TRY(launch_gemmT(tp, 0, std::min(p.sms, tiles * splits), st));
+      RL_TRY(launch_gemmH(hp, 0, 2 * std::min(p.sms / 2, hp.Mt * hp.Ht), st));
       ph.launched();
-      if (splits > 1) {
-        RL_TRY(launch_sum_slices(tp.out, splits, (long long)nc * p.H, dx_rows, st));
-        ph.launched();
-      }
     }
-    // dW (+)= over this chunk: dW^T[h, v] = sum_n X[n, h] G[n, v]
+    // dW (+)= over this chunk: dW[v][h] = sum_n G[n][v] X[n][h]
     {
-      TParams tp{};
-      const long long a_inner = p.fp32 ? 3ll * p.Hp : p.H;
-      if (!tmap_bf16(&tp.tmA, Xop, a_inner, p.N, a_inner, 64)) return RLLOSS_ECUDA;
-      const long long b_inner = p.fp32 ? 2ll * p.Vp : p.V;
-      if (!tmap_bf16(&tp.tmB, dl, b_inner, nc, p.ld_dl, 64)) return RLLOSS_ECUDA;
-      tp.kb_per_seg = int(cdiv(nc, 64));
-      if (p.fp32) {
-        tp.nseg = 3;   // X_hi*G_hi, X_mid*G_hi, X_hi*G_lo
-        tp.seg_a[0] = 0; tp.seg_b[0] = 0;
-        tp.seg_a[1] = p.Hp; tp.seg_b[1] = 0;
-        tp.seg_a[2] = 0; tp.seg_b[2] = p.Vp;
-      } else {
-        tp.nseg = 1;
-      }
-      tp.a_outer0 = n0;
-      tp.b_outer0 = 0;
-      tp.Mt = Mt;
-      tp.Nt = p.Vt;
-      tp.splits = 1;
-      tp.Hout = p.H;
-      tp.Ncols = p.V;
-      tp.out = dW;
-      tp.ldo = p.H;
-      tp.mode = ch == 0 ? 0 : 1;
-      tp.status = status;
-      tp.limit_ns = kWaitLimitNs;
+      HParams hp{};
+      const long long g_inner = p.fp32 ? 2ll * p.Vp : p.V;
+      if (!tmap_bf16(&hp.tmA, dl, g_inner, nc, p.ld_dl, 64)) return RLLOSS_ECUDA;
+      if (!tmap_bf16(&hp.tmB, Xop, p.Kx, p.N, p.Kx, 64)) return RLLOSS_ECUDA;
+      if (!tmap_f32_out(&hp.tmO, dW, p.H, p.V)) return RLLOSS_ECUDA;
+      hp.kb_per_seg = int(cdiv(nc, 64));
+      set_bwd_segments(hp, p);
+      hp.a_outer0 = 0;
+      hp.b_outer0 = n0;
+      hp.Mt = int(cdiv(p.V, 256));
+      hp.Ht = int(cdiv(p.H, 224));
+      hp.Hout = p.H;
+      hp.order = 1;
+      hp.reduce = ch > 0 ? 1 : 0;
+      hp.status = status;
+      hp.limit_ns = kWaitLimitNs;
       Phase ph(st, 4);
-      RL_TRY(launch_gemmT(tp, 1, std::min(p.sms, tp.Mt * tp.Nt), st));
+      RL_TRY(launch_gemmH(hp, 1, 2 * std::min(p.sms / 2, hp.Mt * hp.Ht), st));
       ph.launched();
     }
     if (p.bias) {

@@ -9,8 +9,8 @@
 //          lse, logp and entropy per token.
 //  dl    : recomputes S for a chunk of rows and writes
 //          G = dL/dl = (c/tau)(onehot(y) - p) as bf16 (p = softmax(S/tau)).
-//  gemmT : C^T[h, col] = sum_k A[k, h] B[col, k] with h on the TMEM lanes;
-//          dX^T = W^T G^T (k = vocab) and dW^T = X^T G (k = tokens).
+//  gemmH : D[row][h] = sum_k A[row][k] B[h][k] on CTA pairs, 256 rows x 224 h
+//          per tile: dX = G W (k = vocab) and dW = G^T X (k = tokens).
 #include <cuda_runtime.h>
 
 #include "engine.cuh"
@@ -363,89 +363,99 @@ struct DlPolicy {
   }
 };
 
-// =============================================================== gemmT
-// h-major output: TMEM lane = h (M = 128), columns = output rows (N = 256).
-template <int B_MN>
-struct TPolicy {
-  static constexpr int kPair = 1;
-  static constexpr int kStages = 4;
-  static constexpr int kBN = 256;
+// =============================================================== gemmH
+// D[row][h] on CTA pairs: TMEM lane = output row (128 per CTA), columns = h
+// (224 per tile).  Output rows leave through shared memory as 32x32 fp32
+// boxes with TMA stores (or TMA reduce-adds when accumulating).
+template <int A_MN>
+struct HPolicy {
+  static constexpr int kPair = 2;
+  static constexpr int kStages = 6;
+  static constexpr int kBN = 256;                 // TMEM column stride of the two accumulators
+  static constexpr int kNH = 224;                 // h per tile (112 per CTA)
   static constexpr int kK16 = 4;
-  static constexpr int kABytes = 128 * 64 * 2;   // two 64(h) x 64(k) boxes
-  static constexpr int kBBytes = 256 * 64 * 2;
-  static constexpr int kExtraSmem = 0;
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, 1, B_MN);
-  using Params = TParams;
+  static constexpr int kABytes = 128 * 64 * 2;    // 128 rows x 64 k
+  static constexpr int kBBytes = 128 * 64 * 2;    // two 64-h runs (112 h used)
+  static constexpr int kBoxBytes = 32 * 32 * 4;
+  static constexpr int kExtraSmem = kEpiWarps * kBoxBytes;
+  static constexpr uint32_t kIdesc = idesc_bf16(256, kNH, A_MN, 1);
+  using Params = HParams;
   struct EpiState {};
 
   __device__ static void cta_setup(const Params&, uint8_t*) {}
   __device__ static void prefetch(const Params& p) {
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB);
+    tma_prefetch_desc(&p.tmO);
   }
-  // Units u = (s * Nt + j) * Mt + i: CTAs running together share the B tile
-  // (output columns j) and walk the same k range.
   template <class F>
   __device__ static void for_each_tile(const Params& p, F&& f) {
-    const int units = p.Mt * p.Nt * p.splits;
+    const int units = p.Mt * p.Ht;
     const int kbs = p.nseg * p.kb_per_seg;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int i = u % p.Mt;
-      const int j = (u / p.Mt) % p.Nt;
-      const int s = u / (p.Mt * p.Nt);
-      const int kb0 = int((long long)s * kbs / p.splits);
-      const int kb1 = int((long long)(s + 1) * kbs / p.splits);
-      if (kb1 <= kb0) continue;
-      TileInfo t{i * 128, j * 256, kb0, kb1, u, s, true, true};
+    const int g0 = blockIdx.x >> 1, gn = gridDim.x >> 1;
+    for (int u = g0; u < units; u += gn) {
+      int i, j;
+      if (p.order == 0) {
+        j = u / p.Mt;
+        i = u - j * p.Mt;
+      } else {
+        i = u / p.Ht;
+        j = u - i * p.Ht;
+      }
+      TileInfo t{i * 256, j * kNH, 0, kbs, u, 0, true, true};
       if (!f(t)) return;
     }
   }
-  __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t) {
+  __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int s = kb / p.kb_per_seg;
     const int kk = (kb - s * p.kb_per_seg) * 64;
-    // A: MN-major, inner = h, outer = k
-    tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + t.m0, p.a_outer0 + kk);
-    tma_load_2d(&p.tmA, bar, st + 8192, p.seg_a[s] + t.m0 + 64, p.a_outer0 + kk);
-    if (B_MN) {
-      // B: MN-major, inner = output column, outer = k
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-        tma_load_2d(&p.tmB, bar, st + kABytes + b * 8192, p.seg_b[s] + t.n0 + 64 * b, p.b_outer0 + kk);
+    const int r = t.m0 + 128 * int(rank);
+    if (A_MN) {
+      tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + r, p.a_outer0 + kk);
+      tma_load_2d_pair(&p.tmA, bar, st + 8192, p.seg_a[s] + r + 64, p.a_outer0 + kk);
     } else {
-      // B: K-major, inner = k, outer = output column
-      tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+      tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + kk, r);
     }
+    const int h = p.seg_b[s] + t.n0 + 112 * int(rank);
+    tma_load_2d_pair(&p.tmB, bar, st + kABytes, h, p.b_outer0 + kk);
+    tma_load_2d_pair(&p.tmB, bar, st + kABytes + 8192, h + 64, p.b_outer0 + kk);
   }
-  __device__ static uint64_t adesc(uint32_t sa, int k) { return sdesc_sw128(sa + k * 2048, 8192, 1024); }
-  __device__ static uint64_t bdesc(uint32_t sa, int k) {
-    return B_MN ? sdesc_sw128(sa + kABytes + k * 2048, 8192, 1024) : sdesc_sw128(sa + kABytes + k * 32, 16, 1024);
+  __device__ static uint64_t adesc(uint32_t sa, int k) {
+    return A_MN ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
   }
+  __device__ static uint64_t bdesc(uint32_t sa, int k) { return sdesc_sw128(sa + kABytes + k * 2048, 8192, 1024); }
 
   __device__ static void epilogue(const Params& p, EpiState&, const TileInfo& t, uint32_t taddr, int q, int half,
-                                  int lane, uint8_t*, uint32_t) {
-    const int h = t.m0 + q * 32 + lane;
-    const bool hv = h < p.Hout;
+                                  int lane, uint8_t* extra, uint32_t rank) {
+    uint8_t* buf = extra + (q + 4 * half) * kBoxBytes;
+    const int y0 = t.m0 + 128 * int(rank) + q * 32;
+    const int c_begin = half ? 4 : 0, c_end = half ? 7 : 4;
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
-      const int c0 = t.n0 + half * 128 + ch * 32;
-      if (c0 >= p.Ncols) break;
+    for (int c = c_begin; c < c_end; ++c) {
+      const int x0 = t.n0 + c * 32;
+      if (x0 >= p.Hout) break;
       float v[32];
-      tmem_ld32(taddr + uint32_t(half * 128 + ch * 32), v);
-      if (!hv) continue;
-      float* o = p.out + (p.mode == 2 ? size_t(t.seg) * size_t(p.split_stride) : size_t(0)) + size_t(c0) * p.ldo + h;
-      const int nc = min(32, p.Ncols - c0);
-      if (p.mode == 1) {
+      tmem_ld32(taddr + uint32_t(c * 32), v);
+      if (lane == 0) tma_store_wait_read<0>();
+      __syncwarp();
+      float4* row = reinterpret_cast<float4*>(buf + lane * 128);
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c < nc) o[size_t(c) * p.ldo] += v[c];
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c < nc) o[size_t(c) * p.ldo] = v[c];
+      for (int k = 0; k < 8; ++k) row[k ^ (lane & 7)] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        if (p.reduce)
+          tma_reduce_add_2d(&p.tmO, buf, x0, y0);
+        else
+          tma_store_2d(&p.tmO, buf, x0, y0);
+        tma_store_commit();
       }
     }
   }
-  __device__ static void epilogue_finish(const Params&, int) {}
+  __device__ static void epilogue_finish(const Params&, int lane) {
+    if (lane == 0) tma_store_wait_all<0>();
+    __syncwarp();
+  }
 };
 
 // =============================================================== small kernels
@@ -511,15 +521,6 @@ __global__ void db_reduce_kernel(const float* part, int nblk, int V, float* db, 
   db[v] = accumulate ? db[v] + a : a;
 }
 
-// out[i] = sum over slices s of part[s * n + i], in slice order.
-__global__ void sum_slices_kernel(const float* part, int slices, long long n, float* out) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    float a = part[i];
-    for (int s = 1; s < slices; ++s) a += part[s * n + i];
-    out[i] = a;
-  }
-}
-
 __global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
@@ -573,8 +574,8 @@ cudaError_t launch_fwd(const FwdParams& p, int grid, int pair, cudaStream_t st) 
 cudaError_t launch_dl(const DlParams& p, int grid, int pair, cudaStream_t st) {
   return pair == 2 ? launch_engine<DlPolicy<2>>(p, grid, st) : launch_engine<DlPolicy<1>>(p, grid, st);
 }
-cudaError_t launch_gemmT(const TParams& p, int b_mn, int grid, cudaStream_t st) {
-  return b_mn ? launch_engine<TPolicy<1>>(p, grid, st) : launch_engine<TPolicy<0>>(p, grid, st);
+cudaError_t launch_gemmH(const HParams& p, int a_mn, int grid, cudaStream_t st) {
+  return a_mn ? launch_engine<HPolicy<1>>(p, grid, st) : launch_engine<HPolicy<0>>(p, grid, st);
 }
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
   fwd_merge_kernel<<<(p.N + 7) / 8, 256, 0, st>>>(p);
@@ -599,12 +600,6 @@ cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, int V
   dim3 grid((V / 2 + 1 + 255) / 256, nblk);
   db_part_kernel<<<grid, 256, 0, st>>>(dl, ld, lo_off, Nc, V, part);
   db_reduce_kernel<<<(V + 255) / 256, 256, 0, st>>>(part, nblk, V, db, accumulate);
-  return cudaGetLastError();
-}
-cudaError_t launch_sum_slices(const float* part, int slices, long long n, float* out, cudaStream_t st) {
-  long long nb = (n + 255) / 256;
-  if (nb > 152LL * 16) nb = 152LL * 16;
-  sum_slices_kernel<<<int(nb < 1 ? 1 : nb), 256, 0, st>>>(part, slices, n, out);
   return cudaGetLastError();
 }
 cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st) {

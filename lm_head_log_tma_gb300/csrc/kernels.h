@@ -54,18 +54,21 @@ struct DlParams {
   unsigned long long limit_ns;
 };
 
-struct TParams {
-  CUtensorMap tmA;            // MN-major: inner h, outer k; box 64 x 64
-  CUtensorMap tmB;            // K-major: inner k, outer col, box 64 x 256; or MN-major: inner col, outer k, box 64 x 64
+// Output D[row][h] = sum_k A[row][k] B[h][k] on CTA pairs: 256 output rows
+// by 224 h per tile.  dX: rows = tokens of the chunk, k = vocabulary,
+// A = G (K-major), B = W.  dW: rows = vocabulary, k = tokens of the chunk,
+// A = G read MN-major, B = X.  B is always read MN-major (h contiguous).
+struct HParams {
+  CUtensorMap tmA;            // dX: G, inner k, box 64 x 128 | dW: G, inner row (vocab), box 64 x 64
+  CUtensorMap tmB;            // W or X: inner h, outer k, box 64 x 64
+  CUtensorMap tmO;            // fp32 output: inner h, outer rows, box 32 x 32, 128-byte swizzle
   int nseg, kb_per_seg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];  // inner-coordinate offsets of each product term
-  int a_outer0, b_outer0;     // outer (k) coordinate origins of A and MN-major B
-  int Mt, Nt, splits;         // h tiles (128), column tiles (256), k splits
-  int Hout, Ncols;            // valid h and output columns
-  float* out;                 // out[col * ldo + h] (+ split * split_stride in mode 2)
-  long long ldo;
-  long long split_stride;     // elements between the slices of a split-k partial output
-  int mode;                   // 0 store, 1 add, 2 store into the slice of the k split
+  int a_outer0, b_outer0;     // outer (k) coordinate origins of MN-major operands
+  int Mt, Ht;                 // 256-row tiles, 224-column h tiles
+  int Hout;                   // valid h
+  int order;                  // 0: tiles sharing an h tile run together; 1: tiles sharing a row tile
+  int reduce;                 // 0: store, 1: add into the output
   int* status;
   unsigned long long limit_ns;
 };
@@ -99,10 +102,10 @@ struct LossParams {
 cudaError_t launch_fwd(const FwdParams& p, int grid, int pair, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 cudaError_t launch_dl(const DlParams& p, int grid, int pair, cudaStream_t st);
-cudaError_t launch_gemmT(const TParams& p, int b_mn, int grid, cudaStream_t st);
+// a_mn = 0: dX form (A K-major), 1: dW form (A MN-major).  grid counts CTAs (even).
+cudaError_t launch_gemmH(const HParams& p, int a_mn, int grid, cudaStream_t st);
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st);
 cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __nv_bfloat16* out, cudaStream_t st);
-cudaError_t launch_sum_slices(const float* part, int slices, long long n, float* out, cudaStream_t st);
 // db (+)= column sums of the chunk's G; part is scratch of db_part_rows(Nc) * V floats.
 int db_part_rows(int Nc);
 cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, int V, float* part, float* db,
