@@ -324,7 +324,7 @@ def run_ours(args):
     launches_per_step = max(1, phase_n[dom] // args.steps)
     achieved = flops_phase / (per_step[dom] / 1e3) / 1e12
     traffic = None
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    tp = os.path.join(ROOT, "profiles", "traffic_qwen05b_t4096.txt")
     if os.path.exists(tp):
         traffic = json.load(open(tp)).get(gemm_phases[dom])
     roofline = {"bound": "tensor", "kernel": gemm_phases[dom], "achieved": achieved, "peak": peak,

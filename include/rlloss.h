@@ -78,8 +78,9 @@ extern "C" {
 #define RLLOSS_IS_SEQUENCE 1
 /* cfg.flags */
 #define RLLOSS_FLAG_FORCE_ENTROPY_PATH 0x1u  /* run the quantile/mask path even at q = 1 */
-#define RLLOSS_FLAG_SINGLE_CTA_TILES 0x2u    /* 128-row single-CTA tiles instead of 256-row CTA-pair
-                                                tiles in the LM-head kernels (same results) */
+#define RLLOSS_FLAG_SINGLE_CTA_TILES 0x2u    /* forward / recompute kernels on 128-row single-CTA
+                                                tiles instead of 256-row CTA-pair tiles (same
+                                                results; for comparison) */
 
 #define RLLOSS_NMETRICS 8
 /* out_metrics layout:

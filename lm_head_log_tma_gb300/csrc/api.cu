@@ -41,6 +41,14 @@ int device_sms() {
 
 bool finite(float x) { return std::isfinite(x); }
 
+// Resident-cluster count from the runtime, or a fallback when no device is
+// usable (host-only sizing).
+int resident_or(int n, int fallback) {
+  if (n > 0) return n;
+  cudaGetLastError();
+  return std::max(1, fallback);
+}
+
 int validate_common(const rlloss_cfg* c) {
   if (!c) return RLLOSS_EINVAL;
   if (c->B < 1 || c->T < 1) return RLLOSS_EINVAL;
@@ -81,6 +89,7 @@ bool entropy_path(const rlloss_cfg* c) {
 struct Plan {
   int B, T, N, H, V, sms;
   int pair, rows_tile;      // CTAs per LM-head tile (1 or 2) and rows per tile
+  int fwd_clusters, h_pairs;  // resident clusters of the forward and dX/dW kernels
   bool fp32, bias, ent;
   int R, Vt, P, Hp, Vp;
   int kb_fwd, nseg_fwd;     // forward K: nseg_fwd * kb_fwd k-blocks
@@ -134,7 +143,9 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
     p.rows_tile = 128 * p.pair;
     p.R = int(cdiv(p.N, p.rows_tile));
     p.Vt = int(cdiv(p.V, 256));
-    p.P = choose_segments(p.R, p.Vt, p.sms / p.pair, p.N);
+    p.fwd_clusters = resident_or(fwd_resident_clusters(p.pair), p.sms / p.pair);
+    p.h_pairs = resident_or(gemmH_resident_clusters(), p.sms / 2);
+    p.P = choose_segments(p.R, p.Vt, p.fwd_clusters, p.N);
     p.Hp = int(rup(p.H, 64));
     p.Vp = int(rup(p.V, 64));
     if (p.fp32) {
@@ -149,7 +160,7 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
     // Default chunk: a whole number of dX pair tiles per pair of SMs (one or
     // two waves of 256-row x 224-h tiles).
     const int hts = int(cdiv(p.H, 224));
-    const int per_wave = 256 * std::max(1, (p.sms / 2) / hts);
+    const int per_wave = 256 * std::max(1, p.h_pairs / hts);
     const int base_chunk = p.N > 2 * per_wave ? 2 * per_wave : per_wave;
     const int want = c->chunk_rows > 0 ? int(rup(c->chunk_rows, 256)) : std::max(base_chunk, 1024);
     p.Nc = int(std::min<long long>(want, rup(p.N, 128)));
@@ -496,7 +507,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   // ---- forward: tensor-core logits + streamed row state
   FwdParams fp{};
   if (!tmap_bf16(&fp.tmA, Xop, p.Kx, p.N, p.Kx, 128)) return RLLOSS_ECUDA;
-  if (!tmap_bf16(&fp.tmB, Wop, p.Kx, p.V, p.Kx, 256 / p.pair)) return RLLOSS_ECUDA;
+  if (!tmap_bf16(&fp.tmB, Wop, p.Kx, p.V, p.Kx, p.pair == 1 ? 256 : 128)) return RLLOSS_ECUDA;
   fp.nseg = p.nseg_fwd;
   fp.kb_per_seg = p.kb_fwd;
   std::memcpy(fp.seg_a, seg_a, sizeof(seg_a));
@@ -514,7 +525,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   fp.limit_ns = kWaitLimitNs;
   {
     Phase ph(st, 0);
-    RL_TRY(launch_fwd(fp, p.pair * std::min(p.sms / p.pair, p.R * p.P), p.pair, st));
+    RL_TRY(launch_fwd(fp, p.R * p.P, p.pair, st));
     ph.launched();
   }
 
@@ -595,7 +606,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     dp.limit_ns = kWaitLimitNs;
     {
       Phase ph(st, 2);
-      RL_TRY(launch_dl(dp, p.pair * std::min(p.sms / p.pair, Rc * p.Vt), p.pair, st));
+      RL_TRY(launch_dl(dp, Rc * p.Vt, p.pair, st));
       ph.launched();
     }
 
@@ -618,7 +629,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       hp.status = status;
       hp.limit_ns = kWaitLimitNs;
       Phase ph(st, 3);
-      RL_TRY(launch_gemmH(hp, 0, 2 * std::min(p.sms / 2, hp.Mt * hp.Ht), st));
+      RL_TRY(launch_gemmH(hp, 0, hp.Mt * hp.Ht, st));
       ph.launched();
     }
     // dW (+)= over this chunk: dW[v][h] = sum_n G[n][v] X[n][h]
@@ -640,7 +651,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       hp.status = status;
       hp.limit_ns = kWaitLimitNs;
       Phase ph(st, 4);
-      RL_TRY(launch_gemmH(hp, 1, 2 * std::min(p.sms / 2, hp.Mt * hp.Ht), st));
+      RL_TRY(launch_gemmH(hp, 1, hp.Mt * hp.Ht, st));
       ph.launched();
     }
     if (p.bias) {

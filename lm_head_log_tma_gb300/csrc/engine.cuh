@@ -65,7 +65,8 @@ __host__ __device__ constexpr int engine_smem_bytes() {
 
 template <class P>
 __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __grid_constant__ typename P::Params prm) {
-  constexpr bool kPair = P::kPair == 2;
+  static_assert(P::kCluster == 1 || P::kCluster == 2, "single CTAs or CTA pairs");
+  constexpr bool kPair = P::kCluster == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -84,6 +85,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const uint32_t leader = rank & ~1u;             // pair leader (issues the MMAs)
+  const bool is_leader = (rank & 1u) == 0u;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -126,8 +129,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
         for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, ac)) { aborted = true; return false; }
           const uint32_t fb = smem_u32(&full[stage]);
-          if (!kPair || rank == 0) mbar_expect_tx(&full[stage], kPair ? 2 * SB : SB);
-          P::load(prm, smem + stage * SB, kPair ? mapa_shared(fb, 0) : fb, t, kb, rank);
+          if (is_leader) mbar_expect_tx(&full[stage], kPair ? 2 * SB : SB);
+          P::load(prm, smem + stage * SB, kPair ? mapa_shared(fb, leader) : fb, t, kb, rank);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
       });
       if (aborted) {
         // Let every copy this thread started land before the CTA can exit.
-        if (!kPair || rank == 0) {
+        if (is_leader) {
           for (int j = 0; j < S && j < issued; ++j) {
             if (--stage < 0) {
               stage = S - 1;
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && (!kPair || rank == 0)) {
+    if (lane == 0 && is_leader) {
       int stage = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
           }
         }
         if constexpr (kPair)
-          umma_commit_pair_mc(&tfull[acc], 0x3);
+          umma_commit_pair_mc(&tfull[acc], uint16_t(0x3u << leader));
         else
           umma_commit(&tfull[acc]);
         if (++acc == 2) {
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
       __syncwarp();
       if (lane == 0) {
         if constexpr (kPair)
-          mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
+          mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), leader));
         else
           mbar_arrive(&tempty[acc]);
       }

@@ -19,11 +19,13 @@
 namespace rl {
 
 // =============================================================== forward
-// PAIR = 2: 256-row tiles over a CTA pair (cta_group::2); PAIR = 1: 128-row tiles.
-template <int PAIR>
+// CL = 1: 128-row tiles on one CTA; CL = 2: 256-row tiles over a CTA pair
+// (cta_group::2).
+template <int CL>
 struct FwdPolicy {
-  static constexpr int kPair = PAIR;
-  static constexpr int kRows = 128 * PAIR;           // accumulator rows per tile (both CTAs)
+  static constexpr int kCluster = CL;
+  static constexpr int PAIR = CL >= 2 ? 2 : 1;
+  static constexpr int kRows = 128 * CL;             // accumulator rows per tile (whole cluster)
   static constexpr int kStages = PAIR == 2 ? 6 : 4;
   static constexpr int kBN = 256;
   static constexpr int kK16 = 4;
@@ -51,7 +53,7 @@ struct FwdPolicy {
   __device__ static void for_each_tile(const Params& p, F&& f) {
     const int units = p.R * p.P;
     const int kbs = p.nseg * p.kb_per_seg;
-    const int g0 = blockIdx.x / PAIR, gn = gridDim.x / PAIR;
+    const int g0 = blockIdx.x / CL, gn = gridDim.x / CL;
     for (int u = g0; u < units; u += gn) {
       const int seg = u / p.R;
       const int r = u - seg * p.R;
@@ -67,7 +69,7 @@ struct FwdPolicy {
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int s = kb / p.kb_per_seg;
     const int kk = (kb - s * p.kb_per_seg) * 64;
-    if constexpr (PAIR == 2) {
+    if constexpr (CL == 2) {
       tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0 + 128 * int(rank));
       tma_load_2d_pair(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0 + 128 * int(rank));
     } else {
@@ -227,10 +229,11 @@ __global__ void fwd_merge_kernel(MergeParams p) {
 }
 
 // =============================================================== dlogits
-template <int PAIR>
+template <int CL>
 struct DlPolicy {
-  static constexpr int kPair = PAIR;
-  static constexpr int kRows = 128 * PAIR;
+  static constexpr int kCluster = CL;
+  static constexpr int PAIR = CL >= 2 ? 2 : 1;
+  static constexpr int kRows = 128 * CL;
   static constexpr int kStages = PAIR == 2 ? 6 : 4;
   static constexpr int kBN = 256;
   static constexpr int kK16 = 4;
@@ -255,7 +258,7 @@ struct DlPolicy {
   __device__ static void for_each_tile(const Params& p, F&& f) {
     const int tiles = p.Rc * p.Vt;
     const int kbs = p.nseg * p.kb_per_seg;
-    const int g0 = blockIdx.x / PAIR, gn = gridDim.x / PAIR;
+    const int g0 = blockIdx.x / CL, gn = gridDim.x / CL;
     for (int u = g0; u < tiles; u += gn) {
       const int j = u / p.Rc;
       const int r = u - j * p.Rc;
@@ -266,7 +269,7 @@ struct DlPolicy {
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int s = kb / p.kb_per_seg;
     const int kk = (kb - s * p.kb_per_seg) * 64;
-    if constexpr (PAIR == 2) {
+    if constexpr (CL == 2) {
       tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0 + 128 * int(rank));
       tma_load_2d_pair(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0 + 128 * int(rank));
     } else {
@@ -369,7 +372,7 @@ struct DlPolicy {
 // boxes with TMA stores (or TMA reduce-adds when accumulating).
 template <int A_MN>
 struct HPolicy {
-  static constexpr int kPair = 2;
+  static constexpr int kCluster = 2;
   static constexpr int kStages = 6;
   static constexpr int kBN = 256;                 // TMEM column stride of the two accumulators
   static constexpr int kNH = 224;                 // h per tile (112 per CTA)
@@ -537,19 +540,57 @@ __global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
 }
 
 // =============================================================== launchers
+// Per device: set the shared-memory attribute once and find how many
+// clusters (CTAs for kCluster == 1) of this kernel can be resident at once.
 template <class P>
-static cudaError_t launch_engine(const typename P::Params& prm, int grid, cudaStream_t st) {
+static int engine_resident(cudaError_t* err) {
   constexpr int smem = engine_smem_bytes<P>();
   static_assert(smem <= 232448, "shared memory budget");
+  static int cached[64] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  static unsigned long long attr_set = 0;   // one bit per device
-  if (dev < 64 && !(attr_set >> dev & 1ull)) {
-    cudaError_t e = cudaFuncSetAttribute(tc_engine_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set |= 1ull << dev;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return 0;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  *err = cudaFuncSetAttribute(tc_engine_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (*err != cudaSuccess) return 0;
+  int n = 0;
+  if (P::kCluster == 1) {
+    int per_sm = 0, sms = 0;
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_engine_kernel<P>, kEngineThreads, smem);
+    if (*err == cudaSuccess) *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    n = per_sm * sms;
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(P::kCluster), 1, 1);
+    cfg.blockDim = dim3(kEngineThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = P::kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    *err = cudaOccupancyMaxActiveClusters(&n, tc_engine_kernel<P>, &cfg);
   }
-  if (P::kPair == 1) {
+  if (*err != cudaSuccess) return 0;
+  if (n < 1) {
+    *err = cudaErrorInvalidConfiguration;
+    return 0;
+  }
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+// Launch ``units`` independent work units' worth of persistent clusters.
+template <class P>
+static cudaError_t launch_engine(const typename P::Params& prm, int units, cudaStream_t st) {
+  constexpr int smem = engine_smem_bytes<P>();
+  cudaError_t err = cudaSuccess;
+  const int resident = engine_resident<P>(&err);
+  if (err != cudaSuccess) return err;
+  const int grid = P::kCluster * (units < resident ? (units < 1 ? 1 : units) : resident);
+  if (P::kCluster == 1) {
     tc_engine_kernel<P><<<grid, kEngineThreads, smem, st>>>(prm);
     return cudaGetLastError();
   }
@@ -560,7 +601,7 @@ static cudaError_t launch_engine(const typename P::Params& prm, int grid, cudaSt
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = P::kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -568,14 +609,26 @@ static cudaError_t launch_engine(const typename P::Params& prm, int grid, cudaSt
   return cudaLaunchKernelEx(&cfg, tc_engine_kernel<P>, prm);
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int grid, int pair, cudaStream_t st) {
-  return pair == 2 ? launch_engine<FwdPolicy<2>>(p, grid, st) : launch_engine<FwdPolicy<1>>(p, grid, st);
+int fwd_resident_clusters(int cluster) {
+  cudaError_t e;
+  return cluster == 2 ? engine_resident<FwdPolicy<2>>(&e) : engine_resident<FwdPolicy<1>>(&e);
 }
-cudaError_t launch_dl(const DlParams& p, int grid, int pair, cudaStream_t st) {
-  return pair == 2 ? launch_engine<DlPolicy<2>>(p, grid, st) : launch_engine<DlPolicy<1>>(p, grid, st);
+int dl_resident_clusters(int cluster) {
+  cudaError_t e;
+  return cluster == 2 ? engine_resident<DlPolicy<2>>(&e) : engine_resident<DlPolicy<1>>(&e);
 }
-cudaError_t launch_gemmH(const HParams& p, int a_mn, int grid, cudaStream_t st) {
-  return a_mn ? launch_engine<HPolicy<1>>(p, grid, st) : launch_engine<HPolicy<0>>(p, grid, st);
+int gemmH_resident_clusters() {
+  cudaError_t e;
+  return engine_resident<HPolicy<0>>(&e);
+}
+cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, cudaStream_t st) {
+  return cluster == 2 ? launch_engine<FwdPolicy<2>>(p, units, st) : launch_engine<FwdPolicy<1>>(p, units, st);
+}
+cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st) {
+  return cluster == 2 ? launch_engine<DlPolicy<2>>(p, units, st) : launch_engine<DlPolicy<1>>(p, units, st);
+}
+cudaError_t launch_gemmH(const HParams& p, int a_mn, int units, cudaStream_t st) {
+  return a_mn ? launch_engine<HPolicy<1>>(p, units, st) : launch_engine<HPolicy<0>>(p, units, st);
 }
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
   fwd_merge_kernel<<<(p.N + 7) / 8, 256, 0, st>>>(p);

@@ -98,12 +98,17 @@ struct LossParams {
   int* status;
 };
 
-// pair = 2: clusters of two CTAs with 256-row tiles (grid counts CTAs, even)
-cudaError_t launch_fwd(const FwdParams& p, int grid, int pair, cudaStream_t st);
+// Persistent launches: ``units`` = independent work units; the grid is the
+// number of clusters that can be resident at once (or fewer).  cluster = 1
+// or 2 CTAs per 128 * cluster-row tile.
+int fwd_resident_clusters(int cluster);
+int dl_resident_clusters(int cluster);
+int gemmH_resident_clusters();
+cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
-cudaError_t launch_dl(const DlParams& p, int grid, int pair, cudaStream_t st);
-// a_mn = 0: dX form (A K-major), 1: dW form (A MN-major).  grid counts CTAs (even).
-cudaError_t launch_gemmH(const HParams& p, int a_mn, int grid, cudaStream_t st);
+cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st);
+// a_mn = 0: dX form (A K-major), 1: dW form (A MN-major).
+cudaError_t launch_gemmH(const HParams& p, int a_mn, int units, cudaStream_t st);
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st);
 cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __nv_bfloat16* out, cudaStream_t st);
 // db (+)= column sums of the chunk's G; part is scratch of db_part_rows(Nc) * V floats.

@@ -86,9 +86,10 @@ def test_entropy_mask_non_vacuous_and_forced_path_bit_identical(R):
     assert torch.equal(o2["emask"], case.inp.mask.cuda())
 
 
-@pytest.mark.parametrize("spec", [MID[1], MID[4]], ids=["bf16_bias_k3kl", "fp32_bias_odd"])
-def test_pair_tiles_match_single_cta_tiles(R, spec):
-    """256-row CTA-pair tiles and 128-row single-CTA tiles give the same results."""
+@pytest.mark.parametrize("spec", [MID[1], MID[4], MID[5]], ids=["bf16_bias_k3kl", "fp32_bias_odd", "wide"])
+def test_tile_shapes_agree(R, spec):
+    """256-row CTA-pair tiles (default) and 128-row single-CTA tiles give the
+    same results."""
     case = Case(spec)
     a, _, _ = _full_check(R, case)
     b, _, _ = _full_check(R, case, flags=R.FLAG_SINGLE_CTA_TILES)
