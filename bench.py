@@ -318,16 +318,17 @@ def run_ours(args):
     # ---- roofline of the dominant tensor-core kernel (phase timing, same timed region)
     peak, peak_sus, hbm, peak_src = load_peaks()
     per_step = [m / args.steps for m in phase_ms]
-    gemm_phases = {0: "fwd_gemm", 2: "bwd_dlogits", 3: "bwd_dX", 4: "bwd_dW"}
+    # tensor-core phases and their algorithmic flop per step (units of N*H*V)
+    gemm_phases = {0: ("fwd_gemm", 2.0), 2: ("bwd_dlogits", 2.0), 3: ("bwd_dX_dW", 4.0)}
     dom = max(gemm_phases, key=lambda k: per_step[k])
-    flops_phase = 2.0 * N * H * V          # each of the four GEMM phases does 2NHV per step
+    flops_phase = gemm_phases[dom][1] * N * H * V
     launches_per_step = max(1, phase_n[dom] // args.steps)
     achieved = flops_phase / (per_step[dom] / 1e3) / 1e12
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic_qwen05b_t4096.txt")
     if os.path.exists(tp):
-        traffic = json.load(open(tp)).get(gemm_phases[dom])
-    roofline = {"bound": "tensor", "kernel": gemm_phases[dom], "achieved": achieved, "peak": peak,
+        traffic = json.load(open(tp)).get(gemm_phases[dom][0])
+    roofline = {"bound": "tensor", "kernel": gemm_phases[dom][0], "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 burst", "frac_of_sustained": achieved / peak_sus,
                 "launches_per_step": launches_per_step}

@@ -191,8 +191,8 @@ int rlloss_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* strea
 /* Phase timing for benchmarks.  While enabled, rlloss_fwd_bwd records CUDA
  * events on the caller's stream around its phases:
  *   0 forward tensor-core kernel, 1 row merge + entropy mask + loss,
- *   2 backward G producer (all chunks), 3 dX kernels, 4 dW kernels,
- *   5 everything else (operand split, bias scaling, db).
+ *   2 backward G producer (all chunks), 3 grouped dX + dW kernels,
+ *   4 (unused), 5 everything else (operand split, bias scaling, db).
  * rlloss_phase_times synchronises on the recorded events, writes the summed
  * milliseconds and the launch counts per phase (arrays of nphase <= 6), and
  * clears the record.  rlloss_phase_timing(0/1) switches it off/on and clears. */

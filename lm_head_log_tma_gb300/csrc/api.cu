@@ -610,48 +610,45 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       ph.launched();
     }
 
-    // dX rows of this chunk: dX[n][h] = sum_v G[n][v] W[v][h]
+    // One grouped launch: problem 0 = dX rows of this chunk,
+    //   dX[n][h] = sum_v G[n][v] W[v][h];  problem 1 = dW (+)= over this chunk,
+    //   dW[v][h] = sum_n G[n][v] X[n][h].
     {
       HParams hp{};
       const long long g_inner = p.fp32 ? 2ll * p.Vp : p.V;
-      if (!tmap_bf16(&hp.tmA, dl, g_inner, nc, p.ld_dl, 128)) return RLLOSS_ECUDA;
-      if (!tmap_bf16(&hp.tmB, Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
-      if (!tmap_f32_out(&hp.tmO, dX + size_t(n0) * p.H, p.H, nc)) return RLLOSS_ECUDA;
-      hp.kb_per_seg = int(cdiv(p.V, 64));
+      if (!tmap_bf16(&hp.tmA[0], dl, g_inner, nc, p.ld_dl, 128)) return RLLOSS_ECUDA;
+      if (!tmap_bf16(&hp.tmB[0], Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
+      if (!tmap_f32_out(&hp.tmO[0], dX + size_t(n0) * p.H, p.H, nc)) return RLLOSS_ECUDA;
+      if (!tmap_bf16(&hp.tmA[1], dl, g_inner, nc, p.ld_dl, 64)) return RLLOSS_ECUDA;
+      if (!tmap_bf16(&hp.tmB[1], Xop, p.Kx, p.N, p.Kx, 64)) return RLLOSS_ECUDA;
+      if (!tmap_f32_out(&hp.tmO[1], dW, p.H, p.V)) return RLLOSS_ECUDA;
+      HProblem& px = hp.pr[0];
+      px.kb_per_seg = int(cdiv(p.V, 64));
+      px.a_outer0 = 0;
+      px.b_outer0 = 0;
+      px.Mt = int(cdiv(nc, 256));
+      px.Ht = int(cdiv(p.H, 224));
+      px.Hout = p.H;
+      px.order = 0;
+      px.a_mn = 0;
+      px.reduce = 0;
+      HProblem& pw = hp.pr[1];
+      pw.kb_per_seg = int(cdiv(nc, 64));
+      pw.a_outer0 = 0;
+      pw.b_outer0 = n0;
+      pw.Mt = int(cdiv(p.V, 256));
+      pw.Ht = int(cdiv(p.H, 224));
+      pw.Hout = p.H;
+      pw.order = 1;
+      pw.a_mn = 1;
+      pw.reduce = ch > 0 ? 1 : 0;
+      hp.nprob = 2;
+      hp.d_tiles = int((px.kb_per_seg + pw.kb_per_seg / 2) / pw.kb_per_seg);
       set_bwd_segments(hp, p);
-      hp.a_outer0 = 0;
-      hp.b_outer0 = 0;
-      hp.Mt = int(cdiv(nc, 256));
-      hp.Ht = int(cdiv(p.H, 224));
-      hp.Hout = p.H;
-      hp.order = 0;
-      hp.reduce = 0;
       hp.status = status;
       hp.limit_ns = kWaitLimitNs;
       Phase ph(st, 3);
-      RL_TRY(launch_gemmH(hp, 0, hp.Mt * hp.Ht, st));
-      ph.launched();
-    }
-    // dW (+)= over this chunk: dW[v][h] = sum_n G[n][v] X[n][h]
-    {
-      HParams hp{};
-      const long long g_inner = p.fp32 ? 2ll * p.Vp : p.V;
-      if (!tmap_bf16(&hp.tmA, dl, g_inner, nc, p.ld_dl, 64)) return RLLOSS_ECUDA;
-      if (!tmap_bf16(&hp.tmB, Xop, p.Kx, p.N, p.Kx, 64)) return RLLOSS_ECUDA;
-      if (!tmap_f32_out(&hp.tmO, dW, p.H, p.V)) return RLLOSS_ECUDA;
-      hp.kb_per_seg = int(cdiv(nc, 64));
-      set_bwd_segments(hp, p);
-      hp.a_outer0 = 0;
-      hp.b_outer0 = n0;
-      hp.Mt = int(cdiv(p.V, 256));
-      hp.Ht = int(cdiv(p.H, 224));
-      hp.Hout = p.H;
-      hp.order = 1;
-      hp.reduce = ch > 0 ? 1 : 0;
-      hp.status = status;
-      hp.limit_ns = kWaitLimitNs;
-      Phase ph(st, 4);
-      RL_TRY(launch_gemmH(hp, 1, hp.Mt * hp.Ht, st));
+      RL_TRY(launch_gemmH(hp, px.Mt * px.Ht + pw.Mt * pw.Ht, st));
       ph.launched();
     }
     if (p.bias) {

@@ -172,9 +172,9 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
           for (int k = 0; k < P::kK16; ++k) {
             const uint32_t accum = (kb > t.kb_begin || k > 0) ? 1u : 0u;
             if constexpr (kPair)
-              umma_bf16_pair(d, P::adesc(sa, k), P::bdesc(sa, k), P::kIdesc, accum);
+              umma_bf16_pair(d, P::adesc(sa, k, t), P::bdesc(sa, k, t), P::idesc(t), accum);
             else
-              umma_bf16(d, P::adesc(sa, k), P::bdesc(sa, k), P::kIdesc, accum);
+              umma_bf16(d, P::adesc(sa, k, t), P::bdesc(sa, k, t), P::idesc(t), accum);
           }
           if constexpr (kPair)
             umma_commit_pair_mc(&empty[stage], 0x3);

@@ -77,8 +77,11 @@ struct FwdPolicy {
       tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
     }
   }
-  __device__ static uint64_t adesc(uint32_t sa, int k) { return sdesc_sw128(sa + k * 32, 16, 1024); }
-  __device__ static uint64_t bdesc(uint32_t sa, int k) { return sdesc_sw128(sa + kABytes + k * 32, 16, 1024); }
+  __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo&) { return sdesc_sw128(sa + k * 32, 16, 1024); }
+  __device__ static uint64_t bdesc(uint32_t sa, int k, const TileInfo&) {
+    return sdesc_sw128(sa + kABytes + k * 32, 16, 1024);
+  }
+  __device__ static uint32_t idesc(const TileInfo&) { return kIdesc; }
 
   __device__ static void epilogue(const Params& p, EpiState& e, const TileInfo& t, uint32_t taddr, int q, int half,
                                   int lane, uint8_t*, uint32_t rank) {
@@ -277,8 +280,11 @@ struct DlPolicy {
       tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
     }
   }
-  __device__ static uint64_t adesc(uint32_t sa, int k) { return sdesc_sw128(sa + k * 32, 16, 1024); }
-  __device__ static uint64_t bdesc(uint32_t sa, int k) { return sdesc_sw128(sa + kABytes + k * 32, 16, 1024); }
+  __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo&) { return sdesc_sw128(sa + k * 32, 16, 1024); }
+  __device__ static uint64_t bdesc(uint32_t sa, int k, const TileInfo&) {
+    return sdesc_sw128(sa + kABytes + k * 32, 16, 1024);
+  }
+  __device__ static uint32_t idesc(const TileInfo&) { return kIdesc; }
 
   // Write one 32x32 bf16 box (this lane's 64-byte row) through shared memory
   // with a TMA store; two staging buffers per warp alternate.
@@ -369,8 +375,9 @@ struct DlPolicy {
 // =============================================================== gemmH
 // D[row][h] on CTA pairs: TMEM lane = output row (128 per CTA), columns = h
 // (224 per tile).  Output rows leave through shared memory as 32x32 fp32
-// boxes with TMA stores (or TMA reduce-adds when accumulating).
-template <int A_MN>
+// boxes with TMA stores (or TMA reduce-adds when accumulating).  One launch
+// runs up to two such problems (dX and dW of a chunk) with a balanced static
+// schedule; see for_each_tile.
 struct HPolicy {
   static constexpr int kCluster = 2;
   static constexpr int kStages = 6;
@@ -381,62 +388,88 @@ struct HPolicy {
   static constexpr int kBBytes = 128 * 64 * 2;    // two 64-h runs (112 h used)
   static constexpr int kBoxBytes = 32 * 32 * 4;
   static constexpr int kExtraSmem = kEpiWarps * kBoxBytes;
-  static constexpr uint32_t kIdesc = idesc_bf16(256, kNH, A_MN, 1);
   using Params = HParams;
   struct EpiState {};
 
   __device__ static void cta_setup(const Params&, uint8_t*) {}
   __device__ static void prefetch(const Params& p) {
-    tma_prefetch_desc(&p.tmA);
-    tma_prefetch_desc(&p.tmB);
-    tma_prefetch_desc(&p.tmO);
+    for (int q = 0; q < p.nprob; ++q) {
+      tma_prefetch_desc(&p.tmA[q]);
+      tma_prefetch_desc(&p.tmB[q]);
+      tma_prefetch_desc(&p.tmO[q]);
+    }
   }
+  __device__ static TileInfo tile_of(const Params& p, int q, int u) {
+    const HProblem& pr = p.pr[q];
+    int i, j;
+    if (pr.order == 0) {
+      j = u / pr.Mt;
+      i = u - j * pr.Mt;
+    } else {
+      i = u / pr.Ht;
+      j = u - i * pr.Ht;
+    }
+    return TileInfo{i * 256, j * kNH, 0, p.nseg * pr.kb_per_seg, u, q, true, true};
+  }
+  // Pair g of gn: problem 0 tiles g, g+gn, ...; then problem 1 tiles.  Pairs
+  // that got fewer problem-0 tiles ("early" pairs) first take problem-1 tiles
+  // [0, F*d) round-robin among themselves, d = problem-0 tile length in
+  // problem-1 tiles; the rest go round-robin over all pairs.  Consecutive
+  // tiles run at the same time, so operand tiles they share stay in L2.
   template <class F>
   __device__ static void for_each_tile(const Params& p, F&& f) {
-    const int units = p.Mt * p.Ht;
-    const int kbs = p.nseg * p.kb_per_seg;
-    const int g0 = blockIdx.x >> 1, gn = gridDim.x >> 1;
-    for (int u = g0; u < units; u += gn) {
-      int i, j;
-      if (p.order == 0) {
-        j = u / p.Mt;
-        i = u - j * p.Mt;
-      } else {
-        i = u / p.Ht;
-        j = u - i * p.Ht;
-      }
-      TileInfo t{i * 256, j * kNH, 0, kbs, u, 0, true, true};
-      if (!f(t)) return;
-    }
+    const int g = blockIdx.x >> 1, gn = gridDim.x >> 1;
+    const int T0 = p.pr[0].Mt * p.pr[0].Ht;
+    for (int u = g; u < T0; u += gn)
+      if (!f(tile_of(p, 0, u))) return;
+    if (p.nprob < 2) return;
+    const int T1 = p.pr[1].Mt * p.pr[1].Ht;
+    const int r = T0 % gn;
+    const int early = (r == 0) ? 0 : gn - r;
+    const int ph1 = min(T1, early * p.d_tiles);
+    if (early > 0 && g >= r)
+      for (int u = g - r; u < ph1; u += early)
+        if (!f(tile_of(p, 1, u))) return;
+    for (int u = ph1 + g; u < T1; u += gn)
+      if (!f(tile_of(p, 1, u))) return;
   }
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
-    const int s = kb / p.kb_per_seg;
-    const int kk = (kb - s * p.kb_per_seg) * 64;
+    const int q = t.seg;
+    const HProblem& pr = p.pr[q];
+    const int s = kb / pr.kb_per_seg;
+    const int kk = (kb - s * pr.kb_per_seg) * 64;
     const int r = t.m0 + 128 * int(rank);
-    if (A_MN) {
-      tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + r, p.a_outer0 + kk);
-      tma_load_2d_pair(&p.tmA, bar, st + 8192, p.seg_a[s] + r + 64, p.a_outer0 + kk);
+    if (pr.a_mn) {
+      tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + r, pr.a_outer0 + kk);
+      tma_load_2d_pair(&p.tmA[q], bar, st + 8192, p.seg_a[s] + r + 64, pr.a_outer0 + kk);
     } else {
-      tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + kk, r);
+      tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + kk, r);
     }
     const int h = p.seg_b[s] + t.n0 + 112 * int(rank);
-    tma_load_2d_pair(&p.tmB, bar, st + kABytes, h, p.b_outer0 + kk);
-    tma_load_2d_pair(&p.tmB, bar, st + kABytes + 8192, h + 64, p.b_outer0 + kk);
+    tma_load_2d_pair(&p.tmB[q], bar, st + kABytes, h, pr.b_outer0 + kk);
+    tma_load_2d_pair(&p.tmB[q], bar, st + kABytes + 8192, h + 64, pr.b_outer0 + kk);
   }
-  __device__ static uint64_t adesc(uint32_t sa, int k) {
-    return A_MN ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
+  __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo& t) {
+    return t.seg == 1 ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
   }
-  __device__ static uint64_t bdesc(uint32_t sa, int k) { return sdesc_sw128(sa + kABytes + k * 2048, 8192, 1024); }
+  __device__ static uint64_t bdesc(uint32_t sa, int k, const TileInfo&) {
+    return sdesc_sw128(sa + kABytes + k * 2048, 8192, 1024);
+  }
+  __device__ static uint32_t idesc(const TileInfo& t) {
+    return t.seg == 1 ? idesc_bf16(256, kNH, 1, 1) : idesc_bf16(256, kNH, 0, 1);
+  }
 
   __device__ static void epilogue(const Params& p, EpiState&, const TileInfo& t, uint32_t taddr, int q, int half,
                                   int lane, uint8_t* extra, uint32_t rank) {
+    const HProblem& pr = p.pr[t.seg];
+    const CUtensorMap* om = &p.tmO[t.seg];
     uint8_t* buf = extra + (q + 4 * half) * kBoxBytes;
     const int y0 = t.m0 + 128 * int(rank) + q * 32;
     const int c_begin = half ? 4 : 0, c_end = half ? 7 : 4;
 #pragma unroll 1
     for (int c = c_begin; c < c_end; ++c) {
       const int x0 = t.n0 + c * 32;
-      if (x0 >= p.Hout) break;
+      if (x0 >= pr.Hout) break;
       float v[32];
       tmem_ld32(taddr + uint32_t(c * 32), v);
       if (lane == 0) tma_store_wait_read<0>();
@@ -447,10 +480,10 @@ struct HPolicy {
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
-        if (p.reduce)
-          tma_reduce_add_2d(&p.tmO, buf, x0, y0);
+        if (pr.reduce)
+          tma_reduce_add_2d(om, buf, x0, y0);
         else
-          tma_store_2d(&p.tmO, buf, x0, y0);
+          tma_store_2d(om, buf, x0, y0);
         tma_store_commit();
       }
     }
@@ -619,7 +652,7 @@ int dl_resident_clusters(int cluster) {
 }
 int gemmH_resident_clusters() {
   cudaError_t e;
-  return engine_resident<HPolicy<0>>(&e);
+  return engine_resident<HPolicy>(&e);
 }
 cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, cudaStream_t st) {
   return cluster == 2 ? launch_engine<FwdPolicy<2>>(p, units, st) : launch_engine<FwdPolicy<1>>(p, units, st);
@@ -627,9 +660,7 @@ cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, cudaStream_t 
 cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st) {
   return cluster == 2 ? launch_engine<DlPolicy<2>>(p, units, st) : launch_engine<DlPolicy<1>>(p, units, st);
 }
-cudaError_t launch_gemmH(const HParams& p, int a_mn, int units, cudaStream_t st) {
-  return a_mn ? launch_engine<HPolicy<1>>(p, units, st) : launch_engine<HPolicy<0>>(p, units, st);
-}
+cudaError_t launch_gemmH(const HParams& p, int units, cudaStream_t st) { return launch_engine<HPolicy>(p, units, st); }
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
   fwd_merge_kernel<<<(p.N + 7) / 8, 256, 0, st>>>(p);
   return cudaGetLastError();

@@ -58,17 +58,24 @@ struct DlParams {
 // by 224 h per tile.  dX: rows = tokens of the chunk, k = vocabulary,
 // A = G (K-major), B = W.  dW: rows = vocabulary, k = tokens of the chunk,
 // A = G read MN-major, B = X.  B is always read MN-major (h contiguous).
-struct HParams {
-  CUtensorMap tmA;            // dX: G, inner k, box 64 x 128 | dW: G, inner row (vocab), box 64 x 64
-  CUtensorMap tmB;            // W or X: inner h, outer k, box 64 x 64
-  CUtensorMap tmO;            // fp32 output: inner h, outer rows, box 32 x 32, 128-byte swizzle
-  int nseg, kb_per_seg;
-  int seg_a[kMaxSeg], seg_b[kMaxSeg];  // inner-coordinate offsets of each product term
+struct HProblem {
+  int kb_per_seg;             // k-blocks per product term
   int a_outer0, b_outer0;     // outer (k) coordinate origins of MN-major operands
   int Mt, Ht;                 // 256-row tiles, 224-column h tiles
   int Hout;                   // valid h
-  int order;                  // 0: tiles sharing an h tile run together; 1: tiles sharing a row tile
+  int order;                  // tile numbering: 0 = h tile major, 1 = row tile major
+  int a_mn;                   // A operand: 0 = K-major (dX form), 1 = MN-major (dW form)
   int reduce;                 // 0: store, 1: add into the output
+};
+struct HParams {
+  CUtensorMap tmA[2];         // K-major: inner k, box 64 x 128 | MN-major: inner row, box 64 x 64
+  CUtensorMap tmB[2];         // inner h, outer k, box 64 x 64
+  CUtensorMap tmO[2];         // fp32 output: inner h, outer rows, box 32 x 32, 128-byte swizzle
+  HProblem pr[2];             // problem 0 must be the K-major one (a_mn = 0) when both run
+  int nprob;                  // 1 or 2
+  int d_tiles;                // problem-0 tile length in problem-1 tiles (scheduling)
+  int nseg;
+  int seg_a[kMaxSeg], seg_b[kMaxSeg];  // inner-coordinate offsets of each product term
   int* status;
   unsigned long long limit_ns;
 };
@@ -107,8 +114,7 @@ int gemmH_resident_clusters();
 cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st);
-// a_mn = 0: dX form (A K-major), 1: dW form (A MN-major).
-cudaError_t launch_gemmH(const HParams& p, int a_mn, int units, cudaStream_t st);
+cudaError_t launch_gemmH(const HParams& p, int units, cudaStream_t st);
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st);
 cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __nv_bfloat16* out, cudaStream_t st);
 // db (+)= column sums of the chunk's G; part is scratch of db_part_rows(Nc) * V floats.

@@ -142,7 +142,7 @@ def rlloss_selftest_bounded_wait(workspace, limit_ns: int, stream=None) -> int:
 
 
 NPHASES = 6
-PHASE_NAMES = ["fwd_gemm", "merge_mask_loss", "bwd_dlogits", "bwd_dX", "bwd_dW", "other"]
+PHASE_NAMES = ["fwd_gemm", "merge_mask_loss", "bwd_dlogits", "bwd_dX_dW", "unused", "other"]
 
 
 def rlloss_phase_timing(enable: bool) -> int:
