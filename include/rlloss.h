@@ -31,7 +31,8 @@
  * Layouts (row-major, contiguous): X [N, H], W [V, H], b [V] with N = B*T
  * (sequence i owns rows i*T .. i*T+T-1); dtype of X, W, b per cfg.dtype
  * (bf16 or fp32).  targets int64 [N] in [0, V).  old_logp, ref_logp fp32 [N].
- * adv fp32 [B] (applied on the sequence's active tokens).  mask uint8 [N],
+ * adv fp32 [B] (applied on the sequence's active tokens), or [N] with
+ * RLLOSS_FLAG_ADV_PER_TOKEN.  mask uint8 [N],
  * nonzero = completion token (active).  Outputs fp32 unless noted.
  *
  * Errors.  Functions return RLLOSS_OK or a synchronous error code BEFORE any
@@ -78,6 +79,10 @@ extern "C" {
 #define RLLOSS_IS_SEQUENCE 1
 /* cfg.flags */
 #define RLLOSS_FLAG_FORCE_ENTROPY_PATH 0x1u  /* run the quantile/mask path even at q = 1 */
+#define RLLOSS_FLAG_ADV_PER_TOKEN 0x4u       /* adv holds N per-token advantages (GSPO only; Tinker
+                                                "GSPO", Input tensors: advantages (N,)); each token's
+                                                objective uses its own A_n, tokens outside the mask
+                                                included */
 #define RLLOSS_FLAG_SINGLE_CTA_TILES 0x2u    /* forward / recompute kernels on 128-row single-CTA
                                                 tiles instead of 256-row CTA-pair tiles (same
                                                 results; for comparison) */
@@ -139,6 +144,19 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
                    float* dX, float* dW, float* db, float* out_logp, float* out_entropy,
                    uint8_t* out_entropy_mask, void* workspace, size_t workspace_bytes,
                    void* stream);
+
+/* Forward only (scoring): per-token target log-prob, entropy and log-sum-exp
+ * of the temperature-scaled logits, streamed over the vocabulary without
+ * writing logits (Tinker "GSPO", Output tensors: logprobs; "support
+ * top_entropy_quantile in fused linear GRPO loss", Details: entropy from the
+ * streamed accumulators).  Uses cfg.B, T, H, V, dtype, temperature,
+ * has_bias, flags; the loss fields are ignored.  out_logp, out_entropy,
+ * out_lse: fp32 [N], each optional.  workspace: at least
+ * rlloss_forward_workspace_bytes(cfg) bytes, 256-byte aligned. */
+size_t rlloss_forward_workspace_bytes(const rlloss_cfg* cfg);
+int rlloss_forward(const rlloss_cfg* cfg, const void* X, const void* W, const void* b,
+                   const int64_t* targets, float* out_logp, float* out_entropy, float* out_lse,
+                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* The loss stage alone, from given per-token log-probs (no LM head): entropy
  * mask (if q < 1), loss, metrics and dL/dlogp.

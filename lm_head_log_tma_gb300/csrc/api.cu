@@ -60,7 +60,9 @@ int validate_common(const rlloss_cfg* c) {
   if (!finite(c->beta)) return RLLOSS_EINVAL;
   const float q = c->top_entropy_quantile;
   if (!(q >= 0.f && q <= 1.f)) return RLLOSS_EINVAL;
-  if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES)) return RLLOSS_EINVAL;
+  if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN))
+    return RLLOSS_EINVAL;
+  if ((c->flags & RLLOSS_FLAG_ADV_PER_TOKEN) && c->loss_type != RLLOSS_GSPO_TOKEN) return RLLOSS_EUNSUPPORTED;
   if (c->loss_type == RLLOSS_GSPO_TOKEN) {
     if (c->beta != 0.f) return RLLOSS_EUNSUPPORTED;
     if (q < 1.f || (c->flags & RLLOSS_FLAG_FORCE_ENTROPY_PATH)) return RLLOSS_EUNSUPPORTED;
@@ -68,9 +70,13 @@ int validate_common(const rlloss_cfg* c) {
   return RLLOSS_OK;
 }
 
-int validate_full(const rlloss_cfg* c) {
-  int e = validate_common(c);
-  if (e) return e;
+// LM-head part of a configuration (shapes, dtype, temperature, bias).
+int validate_head(const rlloss_cfg* c) {
+  if (!c) return RLLOSS_EINVAL;
+  if (c->B < 1 || c->T < 1) return RLLOSS_EINVAL;
+  if ((long long)c->B * c->T > (1ll << 31) - 1) return RLLOSS_EINVAL;
+  if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN))
+    return RLLOSS_EINVAL;
   if (c->H < 1 || c->V < 1) return RLLOSS_EINVAL;
   if (c->dtype != RLLOSS_BF16 && c->dtype != RLLOSS_FP32) return RLLOSS_EINVAL;
   if (!(c->temperature > 0.f) || !finite(c->temperature)) return RLLOSS_EINVAL;
@@ -80,6 +86,12 @@ int validate_full(const rlloss_cfg* c) {
   if ((c->H % 4) != 0) return RLLOSS_EUNSUPPORTED;                            // fp32 dX / dW rows: 16 bytes
   if (c->H > 65536 || c->V > (1 << 30)) return RLLOSS_EUNSUPPORTED;
   return RLLOSS_OK;
+}
+
+int validate_full(const rlloss_cfg* c) {
+  int e = validate_common(c);
+  if (e) return e;
+  return validate_head(c);
 }
 
 bool entropy_path(const rlloss_cfg* c) {
@@ -117,7 +129,12 @@ int choose_segments(int R, int Vt, int G, long long N) {
   return best;
 }
 
-Plan make_plan(const rlloss_cfg* c, bool loss_only) {
+enum PlanMode { kFull, kLossOnly, kForwardOnly };
+
+Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
+  const bool head = mode != kLossOnly;      // LM-head forward kernels
+  const bool loss = mode != kForwardOnly;   // loss stage
+  const bool bwd = mode == kFull;           // backward chunks
   Plan p{};
   p.B = c->B;
   p.T = c->T;
@@ -131,10 +148,12 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
     return o;
   };
   p.o_status = take(256);
-  p.o_tickets = take(size_t(p.B) * 4);
-  p.slices = loss_slices(p.B, p.T, p.sms);
-  p.o_part = take(size_t(p.B) * p.slices * 5 * 8);
-  if (!loss_only) {
+  if (loss) {
+    p.o_tickets = take(size_t(p.B) * 4);
+    p.slices = loss_slices(p.B, p.T, p.sms);
+    p.o_part = take(size_t(p.B) * p.slices * 5 * 8);
+  }
+  if (head) {
     p.H = c->H;
     p.V = c->V;
     p.fp32 = c->dtype == RLLOSS_FP32;
@@ -144,7 +163,6 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
     p.R = int(cdiv(p.N, p.rows_tile));
     p.Vt = int(cdiv(p.V, 256));
     p.fwd_clusters = resident_or(fwd_resident_clusters(p.pair), p.sms / p.pair);
-    p.h_pairs = resident_or(gemmH_resident_clusters(), p.sms / 2);
     p.P = choose_segments(p.R, p.Vt, p.fwd_clusters, p.N);
     p.Hp = int(rup(p.H, 64));
     p.Vp = int(rup(p.V, 64));
@@ -157,6 +175,21 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
       p.kb_fwd = int(cdiv(p.H, 64));
       p.Kx = p.H;
     }
+    p.o_partial = take(size_t(p.N) * 2 * p.P * 32);
+    p.o_lse2 = take(size_t(p.N) * 4);
+    p.o_logp64 = take(size_t(p.N) * 8);
+    p.o_ent = take(size_t(p.N) * 4);
+    p.o_bias2 = take(p.bias ? size_t(p.Vt) * 256 * 4 : 0);
+    p.o_x3 = take(p.fp32 ? size_t(p.N) * 3 * p.Hp * 2 : 0);
+    p.o_w3 = take(p.fp32 ? size_t(p.V) * 3 * p.Hp * 2 : 0);
+  }
+  if (loss) {
+    p.o_emask = take(size_t(p.N));
+    p.o_k3 = take(kK3Bytes);
+    p.o_seq = take(size_t(p.B) * 64);
+  }
+  if (bwd) {
+    p.h_pairs = resident_or(gemmH_resident_clusters(), p.sms / 2);
     // Default chunk: a whole number of dX pair tiles per pair of SMs (one or
     // two waves of 256-row x 224-h tiles).
     const int hts = int(cdiv(p.H, 224));
@@ -166,20 +199,8 @@ Plan make_plan(const rlloss_cfg* c, bool loss_only) {
     p.Nc = int(std::min<long long>(want, rup(p.N, 128)));
     p.nchunks = int(cdiv(p.N, p.Nc));
     p.ld_dl = p.fp32 ? 2 * p.Vp : p.Vp;
-    p.o_partial = take(size_t(p.N) * 2 * p.P * 32);
-    p.o_lse2 = take(size_t(p.N) * 4);
-    p.o_logp64 = take(size_t(p.N) * 8);
-    p.o_ent = take(size_t(p.N) * 4);
     p.o_coef = take(size_t(p.N) * 4);
-  }
-  p.o_emask = take(size_t(p.N));
-  p.o_k3 = take(kK3Bytes);
-  p.o_seq = take(size_t(p.B) * 64);
-  if (!loss_only) {
-    p.o_bias2 = take(p.bias ? size_t(p.Vt) * 256 * 4 : 0);
     p.o_dl = take(size_t(p.Nc) * p.ld_dl * 2);
-    p.o_x3 = take(p.fp32 ? size_t(p.N) * 3 * p.Hp * 2 : 0);
-    p.o_w3 = take(p.fp32 ? size_t(p.V) * 3 * p.Hp * 2 : 0);
     p.o_dbpart = take(p.bias ? size_t(db_part_rows(p.Nc)) * p.V * 4 : 0);
   }
   p.total = off;
@@ -330,7 +351,108 @@ LossParams loss_params(const rlloss_cfg* c, const Plan& p, char* ws) {
   lp.ticket = reinterpret_cast<unsigned int*>(ws + p.o_status + 4);
   lp.status = reinterpret_cast<int*>(ws + p.o_status);
   lp.k3 = p.ent ? reinterpret_cast<const double*>(ws + p.o_k3) : nullptr;
+  lp.adv_per_token = (c->flags & RLLOSS_FLAG_ADV_PER_TOKEN) ? 1 : 0;
   return lp;
+}
+
+// The LM-head forward shared by rlloss_fwd_bwd and rlloss_forward: operand
+// preparation (fp32 split, scaled bias), the tensor-core forward, and the
+// row merge into lse, logp and entropy.
+struct Head {
+  const void* Xop = nullptr;
+  const void* Wop = nullptr;
+  const float* bias2 = nullptr;
+  int seg_a[kMaxSeg] = {0, 0, 0, 0, 0, 0};
+  int seg_b[kMaxSeg] = {0, 0, 0, 0, 0, 0};
+  FwdParams fp{};
+  MergeParams mp{};
+};
+
+#define RL_TRY_RC(x)             \
+  do {                           \
+    const int _rc = (x);         \
+    if (_rc != RLLOSS_OK) return _rc; \
+  } while (0)
+
+int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W, const void* b,
+             const int64_t* targets, float* out_logp, float* out_entropy, float* out_lse, char* ws,
+             cudaStream_t st, Head& h) {
+  int* status = reinterpret_cast<int*>(ws + p.o_status);
+  const float scale2 = float(1.4426950408889634 / double(cfg->temperature));
+  // Operand arrays: bf16 inputs are used in place; fp32 inputs are split
+  // into three bf16 terms (hi, mid, lo) so the same bf16 tensor-core kernels
+  // reach fp32-level accuracy (six of the nine term products are kept).
+  h.Xop = X;
+  h.Wop = W;
+  if (p.fp32) {
+    __nv_bfloat16* x3 = reinterpret_cast<__nv_bfloat16*>(ws + p.o_x3);
+    __nv_bfloat16* w3 = reinterpret_cast<__nv_bfloat16*>(ws + p.o_w3);
+    Phase ph(st, 5);
+    RL_TRY(launch_split3(static_cast<const float*>(X), p.N, p.H, p.Hp, x3, st));
+    RL_TRY(launch_split3(static_cast<const float*>(W), p.V, p.H, p.Hp, w3, st));
+    ph.launched(2);
+    h.Xop = x3;
+    h.Wop = w3;
+  }
+  if (p.bias) {
+    float* b2 = reinterpret_cast<float*>(ws + p.o_bias2);
+    Phase ph(st, 5);
+    RL_TRY(launch_bias2(b, p.fp32 ? 1 : 0, p.V, p.Vt * 256, scale2, b2, st));
+    ph.launched();
+    h.bias2 = b2;
+  }
+  // K-segments of the forward / recompute GEMM: products of the split terms.
+  if (p.fp32) {
+    const int hp = p.Hp;
+    const int sa[6] = {0, 0, hp, 0, hp, 2 * hp};   // hi*hi, hi*mid, mid*hi, hi*lo, mid*mid, lo*hi
+    const int sb[6] = {0, hp, 0, 2 * hp, hp, 0};
+    std::memcpy(h.seg_a, sa, sizeof(sa));
+    std::memcpy(h.seg_b, sb, sizeof(sb));
+  }
+
+  // ---- forward: tensor-core logits + streamed row state
+  FwdParams& fp = h.fp;
+  if (!tmap_bf16(&fp.tmA, h.Xop, p.Kx, p.N, p.Kx, 128)) return RLLOSS_ECUDA;
+  if (!tmap_bf16(&fp.tmB, h.Wop, p.Kx, p.V, p.Kx, p.pair == 1 ? 256 : 128)) return RLLOSS_ECUDA;
+  fp.nseg = p.nseg_fwd;
+  fp.kb_per_seg = p.kb_fwd;
+  std::memcpy(fp.seg_a, h.seg_a, sizeof(h.seg_a));
+  std::memcpy(fp.seg_b, h.seg_b, sizeof(h.seg_b));
+  fp.N = p.N;
+  fp.V = p.V;
+  fp.R = p.R;
+  fp.Vt = p.Vt;
+  fp.P = p.P;
+  fp.scale2 = scale2;
+  fp.bias2 = h.bias2;
+  fp.targets = targets;
+  fp.partial = reinterpret_cast<float4*>(ws + p.o_partial);
+  fp.status = status;
+  fp.limit_ns = kWaitLimitNs;
+  {
+    Phase ph(st, 0);
+    RL_TRY(launch_fwd(fp, p.R * p.P, p.pair, st));
+    ph.launched();
+  }
+  MergeParams& mp = h.mp;
+  mp.partial = fp.partial;
+  mp.N = p.N;
+  mp.V = p.V;
+  mp.slots = 2 * p.P;
+  mp.targets = targets;
+  mp.lse2 = reinterpret_cast<float*>(ws + p.o_lse2);
+  mp.logp64 = reinterpret_cast<double*>(ws + p.o_logp64);
+  mp.ent32 = reinterpret_cast<float*>(ws + p.o_ent);
+  mp.out_logp = out_logp;
+  mp.out_ent = out_entropy;
+  mp.out_lse = out_lse;
+  mp.status = status;
+  {
+    Phase ph(st, 1);
+    RL_TRY(launch_merge(mp, st));
+    ph.launched();
+  }
+  return RLLOSS_OK;
 }
 
 }  // namespace
@@ -339,12 +461,12 @@ extern "C" {
 
 size_t rlloss_workspace_bytes(const rlloss_cfg* cfg) {
   if (validate_full(cfg) != RLLOSS_OK) return 0;
-  return make_plan(cfg, false).total;
+  return make_plan(cfg, kFull).total;
 }
 
 size_t rlloss_loss_workspace_bytes(const rlloss_cfg* cfg) {
   if (validate_common(cfg) != RLLOSS_OK) return 0;
-  return make_plan(cfg, true).total;
+  return make_plan(cfg, kLossOnly).total;
 }
 
 const char* rlloss_status_str(int code) {
@@ -412,6 +534,29 @@ int rlloss_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* strea
   return RLLOSS_OK;
 }
 
+size_t rlloss_forward_workspace_bytes(const rlloss_cfg* cfg) {
+  if (validate_head(cfg) != RLLOSS_OK) return 0;
+  return make_plan(cfg, kForwardOnly).total;
+}
+
+int rlloss_forward(const rlloss_cfg* cfg, const void* X, const void* W, const void* b, const int64_t* targets,
+                   float* out_logp, float* out_entropy, float* out_lse, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  int e = validate_head(cfg);
+  if (e) return e;
+  if (!X || !W || !targets || !workspace) return RLLOSS_EINVAL;
+  if (cfg->has_bias && !b) return RLLOSS_EINVAL;
+  if (!aligned(X, 16) || !aligned(W, 16)) return RLLOSS_EINVAL;
+  const Plan p = make_plan(cfg, kForwardOnly);
+  if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
+  if (!encode_fn()) return RLLOSS_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, 256, st));
+  Head hd;
+  return run_head(cfg, p, X, W, b, targets, out_logp, out_entropy, out_lse, ws, st, hd);
+}
+
 int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float* entropy, const float* old_logp,
                           const float* ref_logp, const float* adv, const uint8_t* mask, float* out_loss,
                           float* out_metrics, float* out_dlogp, uint8_t* out_entropy_mask, void* workspace,
@@ -420,7 +565,7 @@ int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float*
   if (e) return e;
   if (!logp || !old_logp || !adv || !mask || !out_loss || !out_metrics || !workspace) return RLLOSS_EINVAL;
   if (cfg->beta != 0.f && !ref_logp) return RLLOSS_EINVAL;
-  const Plan p = make_plan(cfg, true);
+  const Plan p = make_plan(cfg, kLossOnly);
   if (p.ent && !entropy) return RLLOSS_EINVAL;
   if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -461,7 +606,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   if (cfg->has_bias && (!b || !db)) return RLLOSS_EINVAL;
   if (cfg->beta != 0.f && !ref_logp) return RLLOSS_EINVAL;
   if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16)) return RLLOSS_EINVAL;
-  const Plan p = make_plan(cfg, false);
+  const Plan p = make_plan(cfg, kFull);
   if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
   if (!encode_fn()) return RLLOSS_ECUDA;
 
@@ -471,82 +616,16 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   const float scale2 = float(1.4426950408889634 / double(cfg->temperature));
   RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, p.o_tickets + size_t(p.B) * 4 - p.o_status, st));
 
-  // Operand arrays: bf16 inputs are used in place; fp32 inputs are split
-  // into three bf16 terms (hi, mid, lo) so the same bf16 tensor-core kernels
-  // reach fp32-level accuracy (six of the nine term products are kept).
-  const void* Xop = X;
-  const void* Wop = W;
-  if (p.fp32) {
-    __nv_bfloat16* x3 = reinterpret_cast<__nv_bfloat16*>(ws + p.o_x3);
-    __nv_bfloat16* w3 = reinterpret_cast<__nv_bfloat16*>(ws + p.o_w3);
-    Phase ph(st, 5);
-    RL_TRY(launch_split3(static_cast<const float*>(X), p.N, p.H, p.Hp, x3, st));
-    RL_TRY(launch_split3(static_cast<const float*>(W), p.V, p.H, p.Hp, w3, st));
-    ph.launched(2);
-    Xop = x3;
-    Wop = w3;
-  }
-  const float* bias2 = nullptr;
-  if (p.bias) {
-    float* b2 = reinterpret_cast<float*>(ws + p.o_bias2);
-    Phase ph(st, 5);
-    RL_TRY(launch_bias2(b, p.fp32 ? 1 : 0, p.V, p.Vt * 256, scale2, b2, st));
-    ph.launched();
-    bias2 = b2;
-  }
-  // K-segments of the forward / recompute GEMM: products of the split terms.
-  int seg_a[kMaxSeg] = {0, 0, 0, 0, 0, 0}, seg_b[kMaxSeg] = {0, 0, 0, 0, 0, 0};
-  if (p.fp32) {
-    const int hp = p.Hp;
-    const int sa[6] = {0, 0, hp, 0, hp, 2 * hp};   // hi*hi, hi*mid, mid*hi, hi*lo, mid*mid, lo*hi
-    const int sb[6] = {0, hp, 0, 2 * hp, hp, 0};
-    std::memcpy(seg_a, sa, sizeof(sa));
-    std::memcpy(seg_b, sb, sizeof(sb));
-  }
-
-  // ---- forward: tensor-core logits + streamed row state
-  FwdParams fp{};
-  if (!tmap_bf16(&fp.tmA, Xop, p.Kx, p.N, p.Kx, 128)) return RLLOSS_ECUDA;
-  if (!tmap_bf16(&fp.tmB, Wop, p.Kx, p.V, p.Kx, p.pair == 1 ? 256 : 128)) return RLLOSS_ECUDA;
-  fp.nseg = p.nseg_fwd;
-  fp.kb_per_seg = p.kb_fwd;
-  std::memcpy(fp.seg_a, seg_a, sizeof(seg_a));
-  std::memcpy(fp.seg_b, seg_b, sizeof(seg_b));
-  fp.N = p.N;
-  fp.V = p.V;
-  fp.R = p.R;
-  fp.Vt = p.Vt;
-  fp.P = p.P;
-  fp.scale2 = scale2;
-  fp.bias2 = bias2;
-  fp.targets = targets;
-  fp.partial = reinterpret_cast<float4*>(ws + p.o_partial);
-  fp.status = status;
-  fp.limit_ns = kWaitLimitNs;
-  {
-    Phase ph(st, 0);
-    RL_TRY(launch_fwd(fp, p.R * p.P, p.pair, st));
-    ph.launched();
-  }
-
-  MergeParams mp{};
+  Head hd;
+  RL_TRY_RC(run_head(cfg, p, X, W, b, targets, out_logp, out_entropy, nullptr, ws, st, hd));
+  const void* Xop = hd.Xop;
+  const void* Wop = hd.Wop;
+  const float* bias2 = hd.bias2;
+  const FwdParams& fp = hd.fp;
+  const MergeParams& mp = hd.mp;
   LossParams lp{};
   {
   Phase ph_loss(st, 1);
-  mp.partial = fp.partial;
-  mp.N = p.N;
-  mp.V = p.V;
-  mp.slots = 2 * p.P;
-  mp.targets = targets;
-  mp.lse2 = reinterpret_cast<float*>(ws + p.o_lse2);
-  mp.logp64 = reinterpret_cast<double*>(ws + p.o_logp64);
-  mp.ent32 = reinterpret_cast<float*>(ws + p.o_ent);
-  mp.out_logp = out_logp;
-  mp.out_ent = out_entropy;
-  mp.status = status;
-  RL_TRY(launch_merge(mp, st));
-  ph_loss.launched();
-
   // ---- entropy mask and loss
   uint8_t* emask = reinterpret_cast<uint8_t*>(ws + p.o_emask);
   if (p.ent) {
@@ -584,8 +663,8 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     dp.tmB = fp.tmB;
     dp.nseg = fp.nseg;
     dp.kb_per_seg = fp.kb_per_seg;
-    std::memcpy(dp.seg_a, seg_a, sizeof(seg_a));
-    std::memcpy(dp.seg_b, seg_b, sizeof(seg_b));
+    std::memcpy(dp.seg_a, hd.seg_a, sizeof(hd.seg_a));
+    std::memcpy(dp.seg_b, hd.seg_b, sizeof(hd.seg_b));
     dp.n0 = n0;
     dp.Nc = nc;
     dp.Rc = Rc;

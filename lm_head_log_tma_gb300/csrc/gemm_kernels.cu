@@ -229,6 +229,7 @@ __global__ void fwd_merge_kernel(MergeParams p) {
   p.ent32[row] = float(ent);
   if (p.out_logp) p.out_logp[row] = float(logp);
   if (p.out_ent) p.out_ent[row] = float(ent);
+  if (p.out_lse) p.out_lse[row] = float(ln2 * lse2);
 }
 
 // =============================================================== dlogits

@@ -33,6 +33,7 @@ struct MergeParams {
   float* ent32;               // [N]
   float* out_logp;            // optional
   float* out_ent;             // optional
+  float* out_lse;             // optional, natural-log units
   int* status;
 };
 
@@ -89,7 +90,8 @@ struct LossParams {
   int logp_is_f64;
   const float* old_logp;
   const float* ref_logp;
-  const float* adv;
+  const float* adv;           // [B], or [N] when adv_per_token
+  int adv_per_token;
   const uint8_t* mask;
   const uint8_t* emask;       // entropy mask, or null (= mask)
   const double* k3;           // K3 state (threshold at k3[0]) or null

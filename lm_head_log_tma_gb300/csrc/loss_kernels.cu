@@ -166,16 +166,19 @@ __global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p
   const long long base = (long long)i * p.T;
   const int t0 = int((long long)sl * p.T / p.slices);
   const int t1 = int((long long)(sl + 1) * p.T / p.slices);
-  const double A = double(p.adv[i]);
+  const double A = p.adv_per_token ? 0.0 : double(p.adv[i]);
   const bool gmpo = p.loss_type == RLLOSS_GMPO;
+  // GMPO: a_e = tokens kept by the entropy mask, a_kl = sum of K3 KL.
+  // GSPO: a_e / a_kl = sums of the positive / negative token advantages.
   double a_m = 0, a_x = 0, a_e = 0, a_kl = 0, a_clip = 0;
   for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
     const long long n = base + t;
-    if (!p.mask[n]) continue;
-    const double lp = logp_at(p, n);
-    const double lr = lp - double(p.old_logp[n]);
-    a_m += 1.0;
+    const bool m = p.mask[n] != 0;
     if (gmpo) {
+      if (!m) continue;
+      const double lp = logp_at(p, n);
+      const double lr = lp - double(p.old_logp[n]);
+      a_m += 1.0;
       const bool clip = (A > 0.0 && lr > p.eps_high) || (A < 0.0 && lr < -p.eps_low);
       a_x += clip ? (A > 0.0 ? p.eps_high : -p.eps_low) : lr;
       a_clip += clip ? 1.0 : 0.0;
@@ -185,7 +188,12 @@ __global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p
         a_kl += exp(d) - d - 1.0;
       }
     } else {
-      a_x += lr;
+      if (m) {
+        a_m += 1.0;
+        a_x += logp_at(p, n) - double(p.old_logp[n]);
+      }
+      const double An = p.adv_per_token ? double(p.adv[n]) : (m ? A : 0.0);
+      if (An > 0.0) a_e += An; else a_kl += An;
     }
   }
   a_m = block_sum(a_m, sh);
@@ -220,13 +228,13 @@ __global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p
   } else if (ni == 0) {
     if (p.status) atomicOr(p.status, RLLOSS_DEV_EEMPTYSEQ);
   } else {
+    // min(s A, clip(s) A) = A min(s, clip(s)) for A > 0 and A max(s, clip(s)) for A < 0
     const double slr = s5[1] / ni;
     const double sv = exp(slr);
     const double sc = fmin(fmax(sv, p.clip_lo), p.clip_hi);
-    r8[0] = -ni * fmin(sv * A, sc * A);
+    r8[0] = -(fmin(sv, sc) * s5[2] + fmax(sv, sc) * s5[3]);
     r8[2] = (sv < p.clip_lo || sv > p.clip_hi) ? 1.0 : 0.0;
     r8[4] = ni; r8[5] = slr; r8[6] = sv;
-    r8[7] = ((A > 0.0 && sv > p.clip_hi) || (A < 0.0 && sv < p.clip_lo)) ? 0.0 : 1.0;
   }
   for (int k = 0; k < 8; ++k) p.seqres[size_t(i) * 8 + k] = r8[k];
   __threadfence();
@@ -275,18 +283,19 @@ __global__ void loss_coef_kernel(LossParams p) {
     const double* r = p.seqres + size_t(i) * 8;
     const double ni = r[1];
     double c = 0.0;
-    if (p.mask[n] && ni > 0) {
+    if (!gmpo && ni > 0) {
+      const double An = p.adv_per_token ? double(p.adv[n]) : (p.mask[n] ? double(p.adv[i]) : 0.0);
+      const double sv = r[6];
+      const bool flat = (An > 0.0 && sv > p.clip_hi) || (An < 0.0 && sv < p.clip_lo);
+      c = flat ? 0.0 : -An * sv;
+    } else if (gmpo && p.mask[n] && ni > 0) {
       const double A = double(p.adv[i]);
-      if (gmpo) {
-        const double lp = logp_at(p, n);
-        const double lr = lp - double(p.old_logp[n]);
-        const bool clip = (A > 0.0 && lr > p.eps_high) || (A < 0.0 && lr < -p.eps_low);
-        c = clip ? 0.0 : -A * r[6] * r[7];
-        if (p.beta != 0.0) c += p.beta * (1.0 - exp(double(p.ref_logp[n]) - lp));
-        c /= double(p.B) * ni;
-      } else {
-        c = -A * r[6] * r[7];
-      }
+      const double lp = logp_at(p, n);
+      const double lr = lp - double(p.old_logp[n]);
+      const bool clip = (A > 0.0 && lr > p.eps_high) || (A < 0.0 && lr < -p.eps_low);
+      c = clip ? 0.0 : -A * r[6] * r[7];
+      if (p.beta != 0.0) c += p.beta * (1.0 - exp(double(p.ref_logp[n]) - lp));
+      c /= double(p.B) * ni;
     }
     if (p.coef) p.coef[n] = float(c * p.inv_tau);
     if (p.dlogp) p.dlogp[n] = float(c);

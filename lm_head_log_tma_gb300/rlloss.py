@@ -24,6 +24,7 @@ GMPO, GSPO_TOKEN = 0, 1
 IS_TOKEN, IS_SEQUENCE = 0, 1
 FLAG_FORCE_ENTROPY_PATH = 0x1
 FLAG_SINGLE_CTA_TILES = 0x2
+FLAG_ADV_PER_TOKEN = 0x4
 NMETRICS = 8
 
 
@@ -60,6 +61,10 @@ def _load():
     lib.rlloss_loss_workspace_bytes.restype = c_size_t
     lib.rlloss_fwd_bwd.argtypes = [cfgp] + [P] * 16 + [P, c_size_t, P]
     lib.rlloss_fwd_bwd.restype = c_int
+    lib.rlloss_forward_workspace_bytes.argtypes = [cfgp]
+    lib.rlloss_forward_workspace_bytes.restype = c_size_t
+    lib.rlloss_forward.argtypes = [cfgp] + [P] * 7 + [P, c_size_t, P]
+    lib.rlloss_forward.restype = c_int
     lib.rlloss_loss_from_logp.argtypes = [cfgp] + [P] * 10 + [P, c_size_t, P]
     lib.rlloss_loss_from_logp.restype = c_int
     lib.rlloss_get_device_status.argtypes = [P, ctypes.POINTER(c_int32)]
@@ -118,6 +123,16 @@ def rlloss_fwd_bwd(cfg, X, W, b, targets, old_logp, ref_logp, adv, mask, out_los
                               _p(dW), _p(db), _p(out_logp), _p(out_entropy), _p(out_entropy_mask),
                               _p(workspace), c_size_t(0 if workspace is None else workspace.numel()),
                               _stream(stream))
+
+
+def rlloss_forward_workspace_bytes(cfg: RllossCfg) -> int:
+    return int(lib.rlloss_forward_workspace_bytes(ctypes.byref(cfg)))
+
+
+def rlloss_forward(cfg, X, W, b, targets, out_logp, out_entropy, out_lse, workspace, stream=None) -> int:
+    return lib.rlloss_forward(ctypes.byref(cfg), _p(X), _p(W), _p(b), _p(targets), _p(out_logp),
+                              _p(out_entropy), _p(out_lse), _p(workspace),
+                              c_size_t(0 if workspace is None else workspace.numel()), _stream(stream))
 
 
 def rlloss_loss_from_logp(cfg, logp, entropy, old_logp, ref_logp, adv, mask, out_loss, out_metrics,
@@ -191,6 +206,20 @@ def fwd_bwd(cfg: RllossCfg, X, W, b, targets, old_logp, ref_logp, adv, mask, wor
                         workspace, stream)
     if rc != OK:
         raise RllossError(rc, "rlloss_fwd_bwd")
+    o["workspace"] = workspace
+    return o
+
+
+def forward(cfg: RllossCfg, X, W, b, targets, workspace=None, stream=None):
+    """Scoring pass: per-token logp, entropy and lse (fp32 [N] each)."""
+    dev = X.device
+    N = cfg.B * cfg.T
+    o = {k: torch.empty(N, dtype=torch.float32, device=dev) for k in ("logp", "entropy", "lse")}
+    if workspace is None:
+        workspace = alloc_workspace(rlloss_forward_workspace_bytes(cfg), dev)
+    rc = rlloss_forward(cfg, X, W, b, targets, o["logp"], o["entropy"], o["lse"], workspace, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_forward")
     o["workspace"] = workspace
     return o
 

@@ -273,28 +273,33 @@ def gmpo_loss(logp, old_logp, ref_logp, adv, mask, B, T, eps_low, eps_high, beta
 
 
 def gspo_token_loss(logp, old_logp, adv, mask, B, T, eps_low=3e-4, eps_high=4e-4,
-                    clip_override=None):
+                    clip_override=None, per_token_adv=False):
     """GSPO-token objective (Tinker "GSPO").
 
     s_i = exp(sum_t m (logp - old) / n_i) (taken on detached log-probs); each
     token's ratio s_t has s_i's value and the gradient of its own logp, so
-    ds_t/dlogp_t = s_i.  A_n = A_i m_n.  obj_n = min(s A_n, clip(s, lo, hi) A_n),
-    L = -sum_n obj_n.  c_n = -A_n s_i g_i, where g_i = 0 exactly when the clipped
-    branch is the strictly smaller one with a flat clamp:
+    ds_t/dlogp_t = s_i.  Advantages: per sequence ([B]) gives A_n = A_i m_n
+    (reading R8); with ``per_token_adv`` ([N]) A_n is given directly (the
+    page's per-token advantages input).  obj_n = min(s A_n, clip(s, lo, hi) A_n),
+    L = -sum_n obj_n.  c_n = -A_n s_i g_n, where g_n = 0 exactly when the
+    clipped branch is the strictly smaller one with a flat clamp:
     (A_n > 0 and s_i > hi) or (A_n < 0 and s_i < lo).  At s_i == lo or hi the
     clamp is inclusive and the minimum ties, so the gradient passes in full.
     """
     lp = np.asarray(logp, np.float64).reshape(B, T)
     old = np.asarray(old_logp, np.float64).reshape(B, T)
     m = (np.asarray(mask).reshape(B, T) != 0)
-    A = np.asarray(adv, np.float64).reshape(B)
+    A = np.asarray(adv, np.float64)
     lo, hi = f32(1.0 - eps_low), f32(1.0 + eps_high)
     n_i = m.sum(axis=1).astype(np.float64)
     if np.any(n_i == 0):
         raise ValueError("sequence_ratio_mask must mark at least one token per sequence")
     slr = (m * (lp - old)).sum(axis=1) / n_i
     s = np.exp(slr)
-    An = A[:, None] * m
+    if per_token_adv:
+        An = A.reshape(B, T)
+    else:
+        An = A.reshape(B)[:, None] * m
     sc = np.clip(s, lo, hi)
     obj = np.minimum(s[:, None] * An, sc[:, None] * An)
     loss = -obj.sum()
@@ -399,6 +404,7 @@ class Problem:
     temperature: float = 1.0
     top_entropy_quantile: float = 1.0
     is_level_sequence: bool = False
+    per_token_adv: bool = False
 
 
 def loss_stage(prob: Problem, logp, entropy, old_logp, ref_logp, adv, mask,
@@ -411,7 +417,9 @@ def loss_stage(prob: Problem, logp, entropy, old_logp, ref_logp, adv, mask,
                          emask_override, clip_override)
     if prob.loss_type == GSPO_TOKEN:
         return gspo_token_loss(logp, old_logp, adv, mask, prob.B, prob.T, prob.eps_low,
-                               prob.eps_high, clip_override)
+                               prob.eps_high, clip_override, prob.per_token_adv)
+    if prob.per_token_adv:
+        raise ValueError("per-token advantages are defined for GSPO-token only")
     raise ValueError("unknown loss type")
 
 

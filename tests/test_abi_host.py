@@ -73,6 +73,8 @@ def _call(cfg):
     (dict(H=60), R.EUNSUPPORTED),                       # bf16 rows must be 16-byte multiples
     (dict(loss_type=R.GSPO_TOKEN, beta=0.1), R.EUNSUPPORTED),
     (dict(loss_type=R.GSPO_TOKEN, top_entropy_quantile=0.5), R.EUNSUPPORTED),
+    (dict(flags=R.FLAG_ADV_PER_TOKEN), R.EUNSUPPORTED),  # per-token advantages: GSPO only
+    (dict(flags=0x80), R.EINVAL),                       # unknown flag
     (dict(), R.EINVAL),                                 # valid cfg, null pointers
 ])
 def test_invalid_requests_rejected_synchronously(kw, code):
@@ -93,6 +95,17 @@ def test_quantile_range_matches_page():
     assert R.rlloss_workspace_bytes(_cfg(top_entropy_quantile=g["valid_min"])) > 0
     assert R.rlloss_workspace_bytes(_cfg(top_entropy_quantile=g["valid_max"])) > 0
     assert R.rlloss_workspace_bytes(_cfg(top_entropy_quantile=float(np.nextafter(np.float32(g["valid_max"]), np.float32(2))))) == 0
+
+
+def test_forward_only_workspace_is_smaller_and_validated():
+    full = R.rlloss_workspace_bytes(_cfg())
+    fwd = R.rlloss_forward_workspace_bytes(_cfg())
+    assert 0 < fwd < full
+    assert R.rlloss_forward_workspace_bytes(_cfg(temperature=0.0)) == 0
+    # loss fields do not matter for the scoring pass
+    assert R.rlloss_forward_workspace_bytes(_cfg(top_entropy_quantile=7.0)) == fwd
+    cfg = _cfg()
+    assert R.lib.rlloss_forward(ctypes.byref(cfg), *([None] * 7), None, 0, None) == R.EINVAL
 
 
 def test_loss_from_logp_validation():

@@ -138,6 +138,51 @@ def test_bounded_wait_times_out_cleanly(R):
     assert torch.ones(4, device="cuda").sum().item() == 4
 
 
+def test_forward_only_scoring_matches_oracle_and_full_call(R):
+    """rlloss_forward: per-token logp, entropy and lse against the oracle, and
+    bit-identical logp / entropy to the full call."""
+    spec = MID[1]
+    case = Case(spec)
+    i = case.inp
+    cfg = R.make_cfg(spec.B, spec.T, spec.H, spec.V, dtype=R.BF16, temperature=0.7, has_bias=True)
+    f = R.forward(cfg, i.X.cuda(), i.W.cuda(), i.b.cuda(), i.targets.cuda())
+    torch.cuda.synchronize()
+    assert R.rlloss_get_device_status(f["workspace"]) == 0
+    lse, logp, ent = O.row_stats(i.X, i.W, i.b, i.targets, 0.7)
+    for k, ref in (("logp", logp), ("entropy", ent), ("lse", lse)):
+        g = f[k].double().cpu().numpy()
+        assert np.all(np.abs(g - ref) <= 2e-5 + 2e-6 * np.abs(ref)), k
+    case07 = Case(spec.with_(temperature=0.7), i)
+    full = case07.run_gpu(R)
+    assert torch.equal(full["logp"], f["logp"]) and torch.equal(full["entropy"], f["entropy"])
+
+
+def test_gspo_per_token_advantages_full_path(R):
+    """GSPO with per-token advantages (nonzero also outside the ratio mask)
+    through the fused path, against the oracle."""
+    spec = MID[3]
+    case = Case(spec)
+    i = case.inp
+    g = torch.Generator().manual_seed(77)
+    An = torch.randn(spec.N, generator=g)
+    cfg = R.make_cfg(spec.B, spec.T, spec.H, spec.V, dtype=R.BF16, loss_type=R.GSPO_TOKEN, eps_low=spec.eps_low,
+                     eps_high=spec.eps_high, flags=R.FLAG_ADV_PER_TOKEN)
+    c = lambda x: x.cuda()
+    out = R.fwd_bwd(cfg, c(i.X), c(i.W), None, c(i.targets), c(case.old), None, c(An), c(i.mask))
+    torch.cuda.synchronize()
+    assert R.rlloss_get_device_status(out["workspace"]) == 0
+    prob = O.Problem(spec.B, spec.T, O.GSPO_TOKEN, spec.eps_low, spec.eps_high, per_token_adv=True)
+    res = O.loss_stage(prob, case.logp, case.ent, case.old64, None, An.double().numpy(), case.mask)
+    gl = out["loss"].item()
+    assert abs(gl - res.loss) <= 1e-5 * abs(res.loss), (gl, res.loss)
+    assert out["metrics"][1].item() == res.metrics[1]
+    dX, dW, _ = O.grads(i.X, i.W, None, i.targets, spec.temperature, case.lse, res.c)
+    from parity import rel_l2, cosine
+    for name, gx, ox in (("dX", out["dX"], dX), ("dW", out["dW"], dW)):
+        gx = gx.double().cpu().numpy()
+        assert rel_l2(gx, ox) <= 5e-3 and cosine(gx, ox) >= 0.9999, name
+
+
 # ------------------------------------------------------------------ loss stage only
 def _loss_gpu(R, cfg, logp, old, adv, mask, entropy=None, ref=None):
     c = lambda x: None if x is None else torch.as_tensor(x).cuda()

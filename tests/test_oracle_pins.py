@@ -278,12 +278,12 @@ def test_gspo_default_clip_range_matches_page():
     assert 1 + sig.parameters["eps_high"].default == pytest.approx(hi, abs=1e-15)
 
 
-def _torch_gspo(logp, old, adv, mask, B, T, lo, hi):
+def _torch_gspo(logp, old, adv, mask, B, T, lo, hi, per_token=False):
     """Independent autograd statement of GSPO-token: stop-gradient via detach."""
     lp = logp.reshape(B, T); m = mask.reshape(B, T)
     seq = ((lp.detach() - old.reshape(B, T)) * m).sum(1) / m.sum(1)
     ratio = torch.exp(seq[:, None] + lp - lp.detach())
-    An = adv[:, None] * m
+    An = adv.reshape(B, T) if per_token else adv[:, None] * m
     obj = torch.minimum(ratio * An, torch.clamp(ratio, lo, hi) * An)
     return -obj.sum()
 
@@ -305,6 +305,28 @@ def test_gspo_gradient_matches_autograd():
     assert r.loss == pytest.approx(L.item(), rel=1e-14)
     assert np.allclose(r.c, lp_t.grad.numpy(), rtol=1e-14, atol=0)
     assert r.metrics[1] == 3
+
+
+def test_gspo_per_token_advantages_match_autograd_and_reduce_to_per_sequence():
+    rng = np.random.default_rng(14)
+    B, T = 3, 8
+    logp = rng.uniform(-3, -1, B * T)
+    mask = np.ones(B * T, np.uint8); mask[[0, 1, 8]] = 0
+    old = logp - np.repeat([3e-3, -3e-3, 1e-5], T)
+    An = rng.normal(size=B * T)                 # per-token, including some outside the ratio mask
+    r = O.gspo_token_loss(logp, old, An, mask, B, T, per_token_adv=True)
+    lp_t = torch.tensor(logp, requires_grad=True)
+    L = _torch_gspo(lp_t, torch.tensor(old), torch.tensor(An), torch.tensor(mask, dtype=torch.float64), B, T,
+                    O.f32(1 - 3e-4), O.f32(1 + 4e-4), per_token=True)
+    L.backward()
+    assert r.loss == pytest.approx(L.item(), rel=1e-14)
+    assert np.allclose(r.c, lp_t.grad.numpy(), rtol=1e-14, atol=0)
+    # per-sequence advantages broadcast on the mask are the special case A_n = A_i m_n
+    adv = rng.normal(size=B)
+    a = O.gspo_token_loss(logp, old, adv, mask, B, T)
+    b_ = O.gspo_token_loss(logp, old, (adv[:, None] * mask.reshape(B, T)).reshape(-1), mask, B, T,
+                           per_token_adv=True)
+    assert a.loss == b_.loss and np.array_equal(a.c, b_.c)
 
 
 def test_gspo_requires_active_token_per_sequence():
