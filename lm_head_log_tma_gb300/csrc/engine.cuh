@@ -1,7 +1,7 @@
 // Persistent, warp-specialised tcgen05 GEMM engine for sm_103a.
 //
 //   warp 0 (one lane)  : TMA producer, fills a ring of shared-memory stages
-//   warp 1 (one lane)  : MMA issuer, tcgen05.mma into one of two TMEM
+//   warp 1 (one lane)  : MMA issuer, tcgen05.mma into one of P::kAccBufs TMEM
 //                        accumulators (128 lanes x BN fp32 columns each)
 //   warp 2             : TMEM allocation / release
 //   warps 4..11        : epilogue; warp w reads TMEM lanes 32*(w%4)..+31 and
@@ -65,6 +65,7 @@ __host__ __device__ constexpr int engine_smem_bytes() {
 
 template <class P>
 __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __grid_constant__ typename P::Params prm) {
+  static_assert(P::kAccBufs * P::kBN <= int(kTmemCols), "accumulators exceed TMEM");
   static_assert(P::kCluster == 1 || P::kCluster == 2, "single CTAs or CTA pairs");
   constexpr bool kPair = P::kCluster == 2;
   extern __shared__ uint8_t smem_raw[];
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
         for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, ac)) { aborted = true; return false; }
           const uint32_t fb = smem_u32(&full[stage]);
-          if (is_leader) mbar_expect_tx(&full[stage], kPair ? 2 * SB : SB);
+          if (is_leader) mbar_expect_tx(&full[stage], (kPair ? 2 : 1) * P::tx_bytes(prm, t));
           P::load(prm, smem + stage * SB, kPair ? mapa_shared(fb, leader) : fb, t, kb, rank);
           ++issued;
           if (++stage == S) {
@@ -169,13 +170,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * SB);
 #pragma unroll
-          for (int k = 0; k < P::kK16; ++k) {
-            const uint32_t accum = (kb > t.kb_begin || k > 0) ? 1u : 0u;
-            if constexpr (kPair)
-              umma_bf16_pair(d, P::adesc(sa, k, t), P::bdesc(sa, k, t), P::idesc(t), accum);
-            else
-              umma_bf16(d, P::adesc(sa, k, t), P::bdesc(sa, k, t), P::idesc(t), accum);
-          }
+          for (int k = 0; k < P::kK16; ++k) P::mma(prm, d, sa, k, t, (kb > t.kb_begin || k > 0) ? 1u : 0u);
           if constexpr (kPair)
             umma_commit_pair_mc(&empty[stage], 0x3);
           else
@@ -189,7 +184,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
           umma_commit_pair_mc(&tfull[acc], uint16_t(0x3u << leader));
         else
           umma_commit(&tfull[acc]);
-        if (++acc == 2) {
+        if (++acc == P::kAccBufs) {
           acc = 0;
           aph ^= 1u;
         }
@@ -222,7 +217,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
         else
           mbar_arrive(&tempty[acc]);
       }
-      if (++acc == 2) {
+      if (++acc == P::kAccBufs) {
         acc = 0;
         aph ^= 1u;
       }

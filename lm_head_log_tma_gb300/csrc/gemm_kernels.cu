@@ -82,6 +82,14 @@ struct FwdPolicy {
     return sdesc_sw128(sa + kABytes + k * 32, 16, 1024);
   }
   __device__ static uint32_t idesc(const TileInfo&) { return kIdesc; }
+  static constexpr int kAccBufs = 2;
+  __device__ static uint32_t tx_bytes(const Params&, const TileInfo&) { return kABytes + kBBytes; }
+  __device__ static void mma(const Params&, uint32_t d, uint32_t sa, int k, const TileInfo& t, uint32_t accum) {
+    if constexpr (PAIR == 2)
+      umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, t), kIdesc, accum);
+    else
+      umma_bf16(d, adesc(sa, k, t), bdesc(sa, k, t), kIdesc, accum);
+  }
 
   __device__ static void epilogue(const Params& p, EpiState& e, const TileInfo& t, uint32_t taddr, int q, int half,
                                   int lane, uint8_t*, uint32_t rank) {
@@ -286,6 +294,14 @@ struct DlPolicy {
     return sdesc_sw128(sa + kABytes + k * 32, 16, 1024);
   }
   __device__ static uint32_t idesc(const TileInfo&) { return kIdesc; }
+  static constexpr int kAccBufs = 2;
+  __device__ static uint32_t tx_bytes(const Params&, const TileInfo&) { return kABytes + kBBytes; }
+  __device__ static void mma(const Params&, uint32_t d, uint32_t sa, int k, const TileInfo& t, uint32_t accum) {
+    if constexpr (PAIR == 2)
+      umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, t), kIdesc, accum);
+    else
+      umma_bf16(d, adesc(sa, k, t), bdesc(sa, k, t), kIdesc, accum);
+  }
 
   // Write one 32x32 bf16 box (this lane's 64-byte row) through shared memory
   // with a TMA store; two staging buffers per warp alternate.
@@ -383,6 +399,7 @@ struct HPolicy {
   static constexpr int kCluster = 2;
   static constexpr int kStages = 6;
   static constexpr int kBN = 256;                 // TMEM column stride of the two accumulators
+  static constexpr int kAccBufs = 2;
   static constexpr int kNH = 224;                 // h per tile (112 per CTA)
   static constexpr int kK16 = 4;
   static constexpr int kABytes = 128 * 64 * 2;    // 128 rows x 64 k
@@ -458,6 +475,10 @@ struct HPolicy {
   }
   __device__ static uint32_t idesc(const TileInfo& t) {
     return t.seg == 1 ? idesc_bf16(256, kNH, 1, 1) : idesc_bf16(256, kNH, 0, 1);
+  }
+  __device__ static uint32_t tx_bytes(const Params&, const TileInfo&) { return kABytes + kBBytes; }
+  __device__ static void mma(const Params&, uint32_t d, uint32_t sa, int k, const TileInfo& t, uint32_t accum) {
+    umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, t), idesc(t), accum);
   }
 
   __device__ static void epilogue(const Params& p, EpiState&, const TileInfo& t, uint32_t taddr, int q, int half,
