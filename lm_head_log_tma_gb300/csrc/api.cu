@@ -190,10 +190,10 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
   }
   if (bwd) {
     p.h_pairs = resident_or(gemmH_resident_clusters(), p.sms / 2);
-    // Default chunk: a whole number of dX pair tiles per pair of SMs (one or
-    // two waves of 256-row x 224-h tiles).
-    const int hts = int(cdiv(p.H, 224));
-    const int per_wave = 256 * std::max(1, p.h_pairs / hts);
+    // Default chunk: a whole number of dX units per pair of SMs (one or two
+    // waves of 256-row x 448-h tiles, each in two k halves).
+    const int hts = int(cdiv(p.H, 448));
+    const int per_wave = 256 * std::max(1, p.h_pairs / (2 * hts));
     const int base_chunk = p.N > 2 * per_wave ? 2 * per_wave : per_wave;
     const int want = c->chunk_rows > 0 ? int(rup(c->chunk_rows, 256)) : std::max(base_chunk, 1024);
     p.Nc = int(std::min<long long>(want, rup(p.N, 128)));
@@ -694,6 +694,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     //   dW[v][h] = sum_n G[n][v] X[n][h].
     {
       HParams hp{};
+      set_bwd_segments(hp, p);
       const long long g_inner = p.fp32 ? 2ll * p.Vp : p.V;
       if (!tmap_bf16(&hp.tmA[0], dl, g_inner, nc, p.ld_dl, 128)) return RLLOSS_ECUDA;
       if (!tmap_bf16(&hp.tmB[0], Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
@@ -706,28 +707,31 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       px.a_outer0 = 0;
       px.b_outer0 = 0;
       px.Mt = int(cdiv(nc, 256));
-      px.Ht = int(cdiv(p.H, 224));
+      px.Ht = int(cdiv(p.H, 448));
       px.Hout = p.H;
       px.order = 0;
       px.a_mn = 0;
-      px.reduce = 0;
+      px.ksplit = hp.nseg * px.kb_per_seg >= 2 ? 2 : 1;
+      px.reduce = px.ksplit == 2 ? 1 : 0;
       HProblem& pw = hp.pr[1];
       pw.kb_per_seg = int(cdiv(nc, 64));
       pw.a_outer0 = 0;
       pw.b_outer0 = n0;
       pw.Mt = int(cdiv(p.V, 256));
-      pw.Ht = int(cdiv(p.H, 224));
+      pw.Ht = int(cdiv(p.H, 448));
       pw.Hout = p.H;
       pw.order = 1;
       pw.a_mn = 1;
       pw.reduce = ch > 0 ? 1 : 0;
+      pw.ksplit = 1;
       hp.nprob = 2;
-      hp.d_tiles = int((px.kb_per_seg + pw.kb_per_seg / 2) / pw.kb_per_seg);
-      set_bwd_segments(hp, p);
+      const int kx = hp.nseg * px.kb_per_seg / px.ksplit, kw = hp.nseg * pw.kb_per_seg;
+      hp.d_tiles = std::max(1, (kx + kw / 2) / kw);
       hp.status = status;
       hp.limit_ns = kWaitLimitNs;
       Phase ph(st, 3);
-      RL_TRY(launch_gemmH(hp, px.Mt * px.Ht + pw.Mt * pw.Ht, st));
+      if (px.reduce) RL_TRY(cudaMemsetAsync(dX + size_t(n0) * p.H, 0, size_t(nc) * p.H * 4, st));
+      RL_TRY(launch_gemmH(hp, px.Mt * px.Ht * px.ksplit + pw.Mt * pw.Ht, st));
       ph.launched();
     }
     if (p.bias) {

@@ -2,7 +2,9 @@
 //
 //   warp 0 (one lane)  : TMA producer, fills a ring of shared-memory stages
 //   warp 1 (one lane)  : MMA issuer, tcgen05.mma into one of P::kAccBufs TMEM
-//                        accumulators (128 lanes x BN fp32 columns each)
+//                        accumulators (128 lanes x BN fp32 columns each), or,
+//                        with P::kSubs == 2, into one accumulator made of two
+//                        column halves ("subs") that share the A operand
 //   warp 2             : TMEM allocation / release
 //   warps 4..11        : epilogue; warp w reads TMEM lanes 32*(w%4)..+31 and
 //                        column half (w-4)/4 of the accumulator
@@ -15,6 +17,13 @@
 // "full" barriers; the leader's commits release both CTAs' stages and
 // accumulators (multicast); both CTAs' epilogues report a drained
 // accumulator on the leader's "empty" barrier.
+//
+// Split accumulator (P::kSubs == 2): the epilogue drains sub 0, releases
+// it, then drains sub 1.  The MMA issuer starts the next tile on sub 0 as soon
+// as sub 0 is free and holds back sub 1's MMAs, keeping their stages, until
+// sub 1 is free too (at most kStages k-blocks behind); so the tensor pipe
+// idles only while half of the accumulator is read out, and one A tile feeds
+// twice the columns of a double-buffered accumulator of the same TMEM size.
 //
 // A policy class supplies the tile schedule, the TMA loads of one k-block,
 // the shared-memory descriptors of one K=16 step and the epilogue.  Every
@@ -63,9 +72,93 @@ __host__ __device__ constexpr int engine_smem_bytes() {
          P::kExtraSmem;
 }
 
+// MMA issuer for a split accumulator (see the header).  Sub s lives at TMEM
+// column s * P::kBN.  Returns false if a wait gave up.
+template <class P>
+__device__ bool mma_split_subs(const typename P::Params& prm, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                               uint64_t* tfull, uint64_t* tempty, uint32_t tmem, const AbortCtl& ac) {
+  constexpr bool kPair = P::kCluster == 2;
+  constexpr int S = P::kStages;
+  constexpr int SB = P::kABytes + P::kBBytes;
+  int stage = 0;
+  uint32_t ph = 0;
+  uint32_t aph = 0;
+  auto release = [&](int s) {
+    if constexpr (kPair)
+      umma_commit_pair_mc(&empty[s], 0x3);
+    else
+      umma_commit(&empty[s]);
+  };
+  // Sub-1 MMAs of k-blocks j0..j1-1 of the tile, held in stages from s0.
+  auto catch_up = [&](const TileInfo& t, int s0, int j0, int j1) {
+    int s = s0;
+    for (int j = j0; j < j1; ++j) {
+      const uint32_t sa = smem_u32(smem + s * SB);
+#pragma unroll
+      for (int k = 0; k < P::kK16; ++k) P::mma(prm, tmem + uint32_t(P::kBN), sa, k, t, 1, (j > 0 || k > 0) ? 1u : 0u);
+      release(s);
+      if (++s == S) s = 0;
+    }
+  };
+  bool ok = true;
+  P::for_each_tile(prm, [&](const TileInfo& t) -> bool {
+    if (!mbar_wait(&tempty[0], aph ^ 1u, ac)) { ok = false; return false; }
+    tc_fence_after();
+    bool ready1 = false;
+    int lag = 0;
+    const int s0 = stage;
+    for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
+      if (!mbar_wait(&full[stage], ph, ac)) { ok = false; return false; }
+      tc_fence_after();
+      const uint32_t sa = smem_u32(smem + stage * SB);
+      const int j = kb - t.kb_begin;
+#pragma unroll
+      for (int k = 0; k < P::kK16; ++k) P::mma(prm, tmem, sa, k, t, 0, (j > 0 || k > 0) ? 1u : 0u);
+      if (!ready1) {
+        if (lag + 1 == S) {
+          // Every stage is held for sub 1: wait for it to be drained.
+          if (!mbar_wait(&tempty[1], aph ^ 1u, ac)) { ok = false; return false; }
+          ready1 = true;
+        } else {
+          ready1 = mbar_try_wait(smem_u32(&tempty[1]), aph ^ 1u);
+        }
+        if (ready1) {
+          tc_fence_after();
+          catch_up(t, s0, 0, lag);
+          lag = 0;
+        }
+      }
+      if (ready1) {
+#pragma unroll
+        for (int k = 0; k < P::kK16; ++k) P::mma(prm, tmem + uint32_t(P::kBN), sa, k, t, 1, (j > 0 || k > 0) ? 1u : 0u);
+        release(stage);
+      } else {
+        ++lag;
+      }
+      if (++stage == S) {
+        stage = 0;
+        ph ^= 1u;
+      }
+    }
+    if (!ready1) {
+      if (!mbar_wait(&tempty[1], aph ^ 1u, ac)) { ok = false; return false; }
+      tc_fence_after();
+      catch_up(t, s0, 0, lag);
+    }
+    if constexpr (kPair)
+      umma_commit_pair_mc(&tfull[0], uint16_t(0x3u << (cluster_ctarank() & ~1u)));
+    else
+      umma_commit(&tfull[0]);
+    aph ^= 1u;
+    return true;
+  });
+  return ok;
+}
+
 template <class P>
 __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __grid_constant__ typename P::Params prm) {
   static_assert(P::kAccBufs * P::kBN <= int(kTmemCols), "accumulators exceed TMEM");
+  static_assert(P::kSubs == 1 || (P::kSubs == 2 && P::kAccBufs == 1), "a split accumulator is single-buffered");
   static_assert(P::kCluster == 1 || P::kCluster == 2, "single CTAs or CTA pairs");
   constexpr bool kPair = P::kCluster == 2;
   extern __shared__ uint8_t smem_raw[];
@@ -156,7 +249,16 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && is_leader) {
+    if constexpr (P::kSubs == 2) {
+      if (lane == 0 && is_leader) aborted = !mma_split_subs<P>(prm, smem, full, empty, tfull, tempty, tmem, ac);
+      if (aborted) {
+        if constexpr (kPair)
+          umma_commit_pair(drain);
+        else
+          umma_commit(drain);
+        mbar_wait_drain(drain, 0, 20000000ull);
+      }
+    } else if (lane == 0 && is_leader) {
       int stage = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -204,6 +306,28 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
     int acc = 0;
     uint32_t aph = 0;
     typename P::EpiState st;
+    if constexpr (P::kSubs == 2) {
+      P::for_each_tile(prm, [&](const TileInfo& t) -> bool {
+        const bool got = mbar_wait(&tfull[0], aph, ac);
+        if (!__all_sync(0xffffffffu, got)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int sub = 0; sub < 2; ++sub) {
+          P::epilogue(prm, st, t, tmem + uint32_t(sub * P::kBN) + (uint32_t(q * 32) << 16), q, half, lane, extra,
+                      rank, sub);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (kPair)
+              mbar_arrive_remote(mapa_shared(smem_u32(&tempty[sub]), leader));
+            else
+              mbar_arrive(&tempty[sub]);
+          }
+        }
+        aph ^= 1u;
+        return true;
+      });
+    } else
     P::for_each_tile(prm, [&](const TileInfo& t) -> bool {
       const bool got = mbar_wait(&tfull[acc], aph, ac);
       if (!__all_sync(0xffffffffu, got)) return false;

@@ -27,6 +27,7 @@ struct FwdPolicy {
   static constexpr int PAIR = CL >= 2 ? 2 : 1;
   static constexpr int kRows = 128 * CL;             // accumulator rows per tile (whole cluster)
   static constexpr int kStages = PAIR == 2 ? 6 : 4;
+  static constexpr int kSubs = 1;
   static constexpr int kBN = 256;
   static constexpr int kK16 = 4;
   static constexpr int kABytes = 128 * 64 * 2;
@@ -247,6 +248,7 @@ struct DlPolicy {
   static constexpr int PAIR = CL >= 2 ? 2 : 1;
   static constexpr int kRows = 128 * CL;
   static constexpr int kStages = PAIR == 2 ? 6 : 4;
+  static constexpr int kSubs = 1;
   static constexpr int kBN = 256;
   static constexpr int kK16 = 4;
   static constexpr int kABytes = 128 * 64 * 2;
@@ -390,20 +392,25 @@ struct DlPolicy {
 };
 
 // =============================================================== gemmH
-// D[row][h] on CTA pairs: TMEM lane = output row (128 per CTA), columns = h
-// (224 per tile).  Output rows leave through shared memory as 32x32 fp32
-// boxes with TMA stores (or TMA reduce-adds when accumulating).  One launch
-// runs up to two such problems (dX and dW of a chunk) with a balanced static
-// schedule; see for_each_tile.
+// D[row][h] on CTA pairs: TMEM lane = output row (128 per CTA), columns = h.
+// A tile is 256 rows x 448 h, held as one split accumulator of two 224-h
+// subs (TMEM columns 0.. and 256..): each k-block's A tile (G rows) feeds
+// both, so an A byte carries 448 columns of work.  Output rows leave through
+// shared memory as 32x32 fp32 boxes with TMA stores (or TMA reduce-adds when
+// accumulating).  One launch runs up to two such problems (dX and dW of a
+// chunk) with a balanced static schedule; see for_each_tile.
 struct HPolicy {
   static constexpr int kCluster = 2;
-  static constexpr int kStages = 6;
-  static constexpr int kBN = 256;                 // TMEM column stride of the two accumulators
-  static constexpr int kAccBufs = 2;
-  static constexpr int kNH = 224;                 // h per tile (112 per CTA)
+  static constexpr int kStages = 4;
+  static constexpr int kSubs = 2;
+  static constexpr int kBN = 256;                 // TMEM column offset of sub 1
+  static constexpr int kAccBufs = 1;
+  static constexpr int kNS = 224;                 // h per sub (112 per CTA)
+  static constexpr int kNH = 2 * kNS;             // h per tile
   static constexpr int kK16 = 4;
   static constexpr int kABytes = 128 * 64 * 2;    // 128 rows x 64 k
-  static constexpr int kBBytes = 128 * 64 * 2;    // two 64-h runs (112 h used)
+  static constexpr int kBSub = 128 * 64 * 2;      // per sub: two 64-h runs (112 h used)
+  static constexpr int kBBytes = 2 * kBSub;
   static constexpr int kBoxBytes = 32 * 32 * 4;
   static constexpr int kExtraSmem = kEpiWarps * kBoxBytes;
   using Params = HParams;
@@ -417,31 +424,40 @@ struct HPolicy {
       tma_prefetch_desc(&p.tmO[q]);
     }
   }
+  // Unit u of problem q: order 0 numbers (k part, h tile, row tile) with the
+  // row tile fastest; order 1 numbers (row tile, h tile) with h fastest.
+  // A problem with ksplit 2 cuts the k range in two halves, one unit each.
   __device__ static TileInfo tile_of(const Params& p, int q, int u) {
     const HProblem& pr = p.pr[q];
+    const int per = pr.Mt * pr.Ht;
+    const int part = u / per;
+    const int v = u - part * per;
     int i, j;
     if (pr.order == 0) {
-      j = u / pr.Mt;
-      i = u - j * pr.Mt;
+      j = v / pr.Mt;
+      i = v - j * pr.Mt;
     } else {
-      i = u / pr.Ht;
-      j = u - i * pr.Ht;
+      i = v / pr.Ht;
+      j = v - i * pr.Ht;
     }
-    return TileInfo{i * 256, j * kNH, 0, p.nseg * pr.kb_per_seg, u, q, true, true};
+    const int kbt = p.nseg * pr.kb_per_seg;
+    const int cut = pr.ksplit == 2 ? kbt / 2 : kbt;
+    return TileInfo{i * 256, j * kNH, part == 0 ? 0 : cut, part == 0 ? cut : kbt, u, q, true, true};
   }
-  // Pair g of gn: problem 0 tiles g, g+gn, ...; then problem 1 tiles.  Pairs
-  // that got fewer problem-0 tiles ("early" pairs) first take problem-1 tiles
-  // [0, F*d) round-robin among themselves, d = problem-0 tile length in
-  // problem-1 tiles; the rest go round-robin over all pairs.  Consecutive
-  // tiles run at the same time, so operand tiles they share stay in L2.
+  __device__ static int units(const Params& p, int q) { return p.pr[q].Mt * p.pr[q].Ht * p.pr[q].ksplit; }
+  // Pair g of gn: problem 0 units g, g+gn, ...; then problem 1 units.  Pairs
+  // that got fewer problem-0 units ("early" pairs) first take problem-1 units
+  // [0, F*d) round-robin among themselves, d = problem-0 unit length in
+  // problem-1 units; the rest go round-robin over all pairs.  Consecutive
+  // units run at the same time, so operand tiles they share stay in L2.
   template <class F>
   __device__ static void for_each_tile(const Params& p, F&& f) {
     const int g = blockIdx.x >> 1, gn = gridDim.x >> 1;
-    const int T0 = p.pr[0].Mt * p.pr[0].Ht;
+    const int T0 = units(p, 0);
     for (int u = g; u < T0; u += gn)
       if (!f(tile_of(p, 0, u))) return;
     if (p.nprob < 2) return;
-    const int T1 = p.pr[1].Mt * p.pr[1].Ht;
+    const int T1 = units(p, 1);
     const int r = T0 % gn;
     const int early = (r == 0) ? 0 : gn - r;
     const int ph1 = min(T1, early * p.d_tiles);
@@ -451,6 +467,8 @@ struct HPolicy {
     for (int u = ph1 + g; u < T1; u += gn)
       if (!f(tile_of(p, 1, u))) return;
   }
+  // One k-block: this CTA's 128 A rows and, for each sub, its 112 B rows
+  // (two 64-h runs, rows beyond 112 unused).
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int q = t.seg;
     const HProblem& pr = p.pr[q];
@@ -463,26 +481,33 @@ struct HPolicy {
     } else {
       tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + kk, r);
     }
-    const int h = p.seg_b[s] + t.n0 + 112 * int(rank);
-    tma_load_2d_pair(&p.tmB[q], bar, st + kABytes, h, pr.b_outer0 + kk);
-    tma_load_2d_pair(&p.tmB[q], bar, st + kABytes + 8192, h + 64, pr.b_outer0 + kk);
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+      const int h = p.seg_b[s] + t.n0 + kNS * sub + 112 * int(rank);
+      uint8_t* b = st + kABytes + sub * kBSub;
+      tma_load_2d_pair(&p.tmB[q], bar, b, h, pr.b_outer0 + kk);
+      tma_load_2d_pair(&p.tmB[q], bar, b + 8192, h + 64, pr.b_outer0 + kk);
+    }
   }
   __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo& t) {
     return t.seg == 1 ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
   }
-  __device__ static uint64_t bdesc(uint32_t sa, int k, const TileInfo&) {
-    return sdesc_sw128(sa + kABytes + k * 2048, 8192, 1024);
+  __device__ static uint64_t bdesc(uint32_t sa, int k, int sub) {
+    return sdesc_sw128(sa + kABytes + sub * kBSub + k * 2048, 8192, 1024);
   }
   __device__ static uint32_t idesc(const TileInfo& t) {
-    return t.seg == 1 ? idesc_bf16(256, kNH, 1, 1) : idesc_bf16(256, kNH, 0, 1);
+    return t.seg == 1 ? idesc_bf16(256, kNS, 1, 1) : idesc_bf16(256, kNS, 0, 1);
   }
   __device__ static uint32_t tx_bytes(const Params&, const TileInfo&) { return kABytes + kBBytes; }
-  __device__ static void mma(const Params&, uint32_t d, uint32_t sa, int k, const TileInfo& t, uint32_t accum) {
-    umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, t), idesc(t), accum);
+  __device__ static void mma(const Params&, uint32_t d, uint32_t sa, int k, const TileInfo& t, int sub,
+                             uint32_t accum) {
+    umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, sub), idesc(t), accum);
   }
 
+  // Sub `sub` of the accumulator: warp (q, half) writes TMEM lanes 32q..+31,
+  // 32-column chunks 0-3 (half 0) or 4-6 (half 1).
   __device__ static void epilogue(const Params& p, EpiState&, const TileInfo& t, uint32_t taddr, int q, int half,
-                                  int lane, uint8_t* extra, uint32_t rank) {
+                                  int lane, uint8_t* extra, uint32_t rank, int sub) {
     const HProblem& pr = p.pr[t.seg];
     const CUtensorMap* om = &p.tmO[t.seg];
     uint8_t* buf = extra + (q + 4 * half) * kBoxBytes;
@@ -490,7 +515,7 @@ struct HPolicy {
     const int c_begin = half ? 4 : 0, c_end = half ? 7 : 4;
 #pragma unroll 1
     for (int c = c_begin; c < c_end; ++c) {
-      const int x0 = t.n0 + c * 32;
+      const int x0 = t.n0 + sub * kNS + c * 32;
       if (x0 >= pr.Hout) break;
       float v[32];
       tmem_ld32(taddr + uint32_t(c * 32), v);

@@ -62,11 +62,13 @@ struct DlParams {
 struct HProblem {
   int kb_per_seg;             // k-blocks per product term
   int a_outer0, b_outer0;     // outer (k) coordinate origins of MN-major operands
-  int Mt, Ht;                 // 256-row tiles, 224-column h tiles
+  int Mt, Ht;                 // 256-row tiles, 448-column h tiles
   int Hout;                   // valid h
   int order;                  // tile numbering: 0 = h tile major, 1 = row tile major
   int a_mn;                   // A operand: 0 = K-major (dX form), 1 = MN-major (dW form)
   int reduce;                 // 0: store, 1: add into the output
+  int ksplit;                 // 1, or 2: each tile's k range in two units that both add
+                              // into a zeroed output (two addends: the sum is order-free)
 };
 struct HParams {
   CUtensorMap tmA[2];         // K-major: inner k, box 64 x 128 | MN-major: inner row, box 64 x 64
