@@ -40,6 +40,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunk-rows", type=int, default=0,
+                    help="backward chunk (rows of G kept in HBM); 0 = the library's default")
+    ap.add_argument("--no-naive-memory", action="store_true",
+                    help="skip the full-logits torch path run for the memory comparison")
     return ap.parse_args()
 
 
@@ -144,11 +148,46 @@ def make_workload(dev):
     return spec, inp, old, ref
 
 
-def cfg_for(R, spec):
+def cfg_for(R, spec, chunk_rows=0):
     return R.make_cfg(spec.B, spec.T, spec.H, spec.V, dtype=R.BF16 if spec.dtype == "bf16" else R.FP32,
                       loss_type=spec.loss_type, eps_low=spec.eps_low, eps_high=spec.eps_high, beta=spec.beta,
                       temperature=spec.temperature, top_entropy_quantile=spec.top_entropy_quantile,
-                      has_bias=spec.has_bias)
+                      has_bias=spec.has_bias, chunk_rows=chunk_rows)
+
+
+def naive_peak_extra_bytes(spec, inp, old, dev):
+    """Peak device memory above the inputs of a plain full-logits autograd
+    path over the same batch (fp32 logits, log-softmax, target gather,
+    entropy, the GMPO sequence term, backward to X and W) -- the comparison
+    point for the fused path's workspace.  None if it does not fit."""
+    import torch
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    try:
+        X = inp.X.detach().clone().requires_grad_(True)
+        W = inp.W.detach().clone().requires_grad_(True)
+        z = (X @ W.T).float()
+        if inp.b is not None:
+            z = z + inp.b.float()
+        lp = torch.log_softmax(z / spec.temperature, dim=-1)
+        logp = lp.gather(1, inp.targets[:, None])[:, 0]
+        ent = -(lp.exp() * lp).sum(-1)
+        m = inp.mask.float().view(spec.B, spec.T)
+        lr = (logp - old).view(spec.B, spec.T)
+        adv = inp.adv.view(spec.B, 1)
+        clr = torch.where(adv > 0, lr.clamp(max=spec.eps_high), lr.clamp(min=-spec.eps_low))
+        r = torch.exp((clr * m).sum(1) / m.sum(1).clamp(min=1))
+        loss = -(inp.adv * r).mean() + 0.0 * ent.sum()
+        loss.backward()
+        torch.cuda.synchronize(dev)
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        del X, W, z, lp, logp, ent, lr, clr, r, loss
+    except torch.OutOfMemoryError:
+        peak = None
+    torch.cuda.empty_cache()
+    return peak
 
 
 def oracle_sample_rate(spec, inp, old, ref, tokens):
@@ -227,9 +266,11 @@ def run_ours(args):
     from lm_head_log_tma_gb300 import rlloss as R
 
     spec, inp, old, ref = make_workload(dev)
-    cfg = cfg_for(R, spec)
+    cfg = cfg_for(R, spec, args.chunk_rows)
     N, H, V = spec.N, spec.H, spec.V
-    ws = R.alloc_workspace(R.rlloss_workspace_bytes(cfg), dev)
+    ws_bytes = R.rlloss_workspace_bytes(cfg)
+    naive_bytes = None if args.no_naive_memory else naive_peak_extra_bytes(spec, inp, old, dev)
+    ws = R.alloc_workspace(ws_bytes, dev)
     outs = None
 
     def step():
@@ -241,9 +282,14 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    for _ in range(max(3, args.warmup)):
+    step()   # outputs allocated here; later calls reuse them
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem0 = torch.cuda.memory_allocated(dev)
+    for _ in range(max(3, args.warmup) - 1):
         step()
     torch.cuda.synchronize()
+    call_alloc = torch.cuda.max_memory_allocated(dev) - mem0
     status = R.rlloss_get_device_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {status:#x}")
@@ -277,36 +323,55 @@ def run_ours(args):
     ms_step = ms / args.steps
     value = N * world * args.steps / (ms / 1e3)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step
+    # copies its inputs from pinned host memory and reads its loss and
+    # metrics back.  The copies of step k+1 run on a copy stream while step k
+    # computes (two device buffer sets), as a training loop's input pipeline
+    # would; each step's result is read back before the next step is issued.
     host = {k: v.cpu().pin_memory() for k, v in dict(X=inp.X, W=inp.W, targets=inp.targets, old=old,
                                                        adv=inp.adv, mask=inp.mask).items()}
     if inp.b is not None:
         host["b"] = inp.b.cpu().pin_memory()
     if ref is not None:
         host["ref"] = ref.cpu().pin_memory()
-    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    dbufs = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
     res_host = torch.empty(1 + R.NMETRICS, dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = res_host.numel() * 4
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    consumed = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def e2e_step():
+    def issue_copy(k):
+        slot = k % 2
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(consumed[slot])
+            for name in host:
+                dbufs[slot][name].copy_(host[name], non_blocking=True)
+            copied[slot].record(copy_stream)
+
+    def e2e_run(n):
         nonlocal outs
-        for k in host:
-            dbuf[k].copy_(host[k], non_blocking=True)
-        outs = R.fwd_bwd(cfg, dbuf["X"], dbuf["W"], dbuf.get("b"), dbuf["targets"], dbuf["old"], dbuf.get("ref"),
-                         dbuf["adv"], dbuf["mask"], workspace=ws, outputs=outs)
-        res_host[:1].copy_(outs["loss"], non_blocking=True)
-        res_host[1:].copy_(outs["metrics"], non_blocking=True)
-        stream.synchronize()
+        issue_copy(0)
+        for k in range(n):
+            slot = k % 2
+            if k + 1 < n:
+                issue_copy(k + 1)
+            stream.wait_event(copied[slot])
+            d = dbufs[slot]
+            outs = R.fwd_bwd(cfg, d["X"], d["W"], d.get("b"), d["targets"], d["old"], d.get("ref"), d["adv"],
+                             d["mask"], workspace=ws, outputs=outs)
+            consumed[slot].record(stream)
+            res_host[:1].copy_(outs["loss"], non_blocking=True)
+            res_host[1:].copy_(outs["metrics"], non_blocking=True)
+            stream.synchronize()
 
     e2e_steps = max(3, min(args.steps, 50))
-    for _ in range(3):
-        e2e_step()
+    e2e_run(3)
     barrier()
     torch.cuda.synchronize()
     t = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t
     if world > 1:
@@ -347,8 +412,12 @@ def run_ours(args):
             "phases_ms_per_step": {R.PHASE_NAMES[i]: per_step[i] for i in range(R.NPHASES)},
             "clocks": clk,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps},
-            "gpu_launches": launches}
+                    "steps": e2e_steps, "pipeline": "step k+1's H2D copies overlap step k on a copy stream"},
+            "gpu_launches": launches,
+            "memory": {"library_workspace_bytes": ws_bytes, "allocated_during_call_bytes": call_alloc,
+                       "naive_full_logits_peak_extra_bytes": naive_bytes,
+                       "naive_fits": naive_bytes is not None,
+                       "chunk_rows": args.chunk_rows or "default"}}
 
     if rank == 0 and not args.no_cpu_baseline:
         rate, secs, threads = oracle_sample_rate(spec, inp, old, ref, CPU_BASELINE_TOKENS)
