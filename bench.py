@@ -64,22 +64,32 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons with timestamps."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of SM clock, power and throttle reasons, each with
+    nvidia-smi's own timestamp, so that the samples taken inside the timed
+    region can be picked out exactly."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-        self.t0 = time.time()
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                       "-lms", "100", "-i", str(gpu_index)], stdout=self.f,
+                                       "-lms", str(self.PERIOD_MS), "-i", str(gpu_index)], stdout=self.f,
                                       stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
         self.marks = []
+
+    def wait_first_sample(self, timeout=10.0):
+        t = time.time()
+        while self.p is not None and time.time() - t < timeout:
+            self.f.flush()
+            if os.path.getsize(self.f.name) > 0:
+                return
+            time.sleep(0.05)
 
     def mark(self):
         self.marks.append(time.time())
@@ -93,35 +103,62 @@ class ClockSampler:
         except Exception:
             self.p.kill()
         self.f.flush()
-        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        rows = [[c.strip() for c in r.split(",")] for r in open(self.f.name).read().strip().splitlines()
+                if r.strip()]
         os.unlink(self.f.name)
         if not rows:
             return None
-        # rows arrive every ~100 ms from t0; keep those overlapping the timed region
-        n = len(rows)
-        t_end = time.time()
-        dt = (t_end - self.t0) / max(n, 1)
-        ts = [self.t0 + (i + 0.5) * dt for i in range(n)]
-        a, b = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (self.t0, t_end)
-        sel = [r for r, t in zip(rows, ts) if a - 0.15 <= t <= b + 0.15] or rows[-2:]
+
+        def stamp(x):
+            # "YYYY/MM/DD hh:mm:ss.mmm" in local time -> seconds since the epoch
+            whole, _, frac = x.partition(".")
+            try:
+                return time.mktime(time.strptime(whole, "%Y/%m/%d %H:%M:%S")) + (float("0." + frac) if frac else 0.0)
+            except ValueError:
+                return None
+        a, b = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (None, None)
+        sel = [r for r in rows if a is not None and (stamp(r[0]) or 0) >= a and (stamp(r[0]) or 0) <= b]
+        aligned = bool(sel)
+        if not sel:
+            sel = rows[-3:]
 
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[1]) for r in sel if num(r[1]) is not None]
-        mx = [num(r[2]) for r in sel if num(r[2]) is not None]
+        sm = [num(r[2]) for r in sel if num(r[2]) is not None]
+        mx = [num(r[3]) for r in sel if num(r[3]) is not None]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in sel:
             for k, name in enumerate(names):
-                if len(r) > 5 + k and r[5 + k].strip().lower() == "active":
+                if len(r) > 6 + k and r[6 + k].lower() == "active":
                     reasons.add(name)
-        pw = [num(r[3]) for r in sel if num(r[3]) is not None]
+        pw = [num(r[4]) for r in sel if num(r[4]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sel),
-                "power_w_max": max(pw) if pw else None}
+                "sm_mhz_min": min(sm) if sm else None, "reasons": sorted(reasons), "samples": len(sel),
+                "power_w_max": max(pw) if pw else None, "power_w_median": statistics.median(pw) if pw else None,
+                "aligned_to_timed_region": aligned}
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest of each rank's ``x`` (time-like values: the slowest rank
+    sets the whole job's time).  Works with nccl (device tensors) and gloo
+    (CPU tensors); a single process returns ``x``."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, steps: int, seconds: float) -> float:
+    """Units per second over all ranks: every rank processes the same
+    ``units_per_rank`` per step (weak scaling)."""
+    return units_per_rank * world * steps / seconds
 
 
 def make_workload(dev):
@@ -296,7 +333,8 @@ def run_ours(args):
 
     stream = torch.cuda.current_stream()
     clocks = ClockSampler(local)
-    time.sleep(0.3)
+    clocks.wait_first_sample()
+    time.sleep(0.1)
     R.rlloss_phase_timing(True)
     n_launch0 = R.rlloss_kernel_launches()
     barrier()
@@ -315,13 +353,9 @@ def run_ours(args):
     R.rlloss_phase_timing(False)
     time.sleep(0.2)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
     ms_step = ms / args.steps
-    value = N * world * args.steps / (ms / 1e3)
+    value = whole_job_rate(N, world, args.steps, ms / 1e3)
 
     # ---- end to end through the public API with host buffers: every step
     # copies its inputs from pinned host memory and reads its loss and
@@ -373,12 +407,8 @@ def run_ours(args):
     t = time.perf_counter()
     e2e_run(e2e_steps)
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
-    e2e_value = N * world * e2e_steps / e2e_s
+    e2e_s = max_over_ranks(time.perf_counter() - t, dev)
+    e2e_value = whole_job_rate(N, world, e2e_steps, e2e_s)
 
     # ---- roofline of the dominant tensor-core kernel (phase timing, same timed region)
     peak, peak_sus, hbm, peak_src = load_peaks()

@@ -103,6 +103,7 @@ struct Plan {
   int pair, rows_tile;      // CTAs per LM-head tile (1 or 2) and rows per tile
   int fwd_clusters, h_pairs;  // resident clusters of the forward and dX/dW kernels
   bool fp32, bias, ent;
+  bool fused_loss;          // row merge and loss stage in one launch (no entropy mask)
   int R, Vt, P, Hp, Vp;
   int kb_fwd, nseg_fwd;     // forward K: nseg_fwd * kb_fwd k-blocks
   int Kx;                   // row width (elements) of the bf16 X / W operand arrays
@@ -141,6 +142,7 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
   p.N = c->B * c->T;
   p.sms = device_sms();
   p.ent = entropy_path(c);
+  p.fused_loss = mode == kFull && !p.ent;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -150,7 +152,7 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
   p.o_status = take(256);
   if (loss) {
     p.o_tickets = take(size_t(p.B) * 4);
-    p.slices = loss_slices(p.B, p.T, p.sms);
+    p.slices = p.fused_loss ? fused_loss_slices(p.T) : loss_slices(p.B, p.T, p.sms);
     p.o_part = take(size_t(p.B) * p.slices * 5 * 8);
   }
   if (head) {
@@ -186,7 +188,7 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
   if (loss) {
     p.o_emask = take(size_t(p.N));
     p.o_k3 = take(kK3Bytes);
-    p.o_seq = take(size_t(p.B) * 64);
+    p.o_seq = take(size_t(p.B) * 10 * 8);   // sequence records, 10 doubles each
   }
   if (bwd) {
     p.h_pairs = resident_or(gemmH_resident_clusters(), p.sms / 2);
@@ -374,9 +376,11 @@ struct Head {
     if (_rc != RLLOSS_OK) return _rc; \
   } while (0)
 
+// With merge == false the row merge is left to the caller (the fused merge +
+// loss launch); h.mp is filled either way.
 int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W, const void* b,
              const int64_t* targets, float* out_logp, float* out_entropy, float* out_lse, char* ws,
-             cudaStream_t st, Head& h) {
+             cudaStream_t st, Head& h, bool merge = true) {
   int* status = reinterpret_cast<int*>(ws + p.o_status);
   const float scale2 = float(1.4426950408889634 / double(cfg->temperature));
   // Operand arrays: bf16 inputs are used in place; fp32 inputs are split
@@ -447,7 +451,7 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
   mp.out_ent = out_entropy;
   mp.out_lse = out_lse;
   mp.status = status;
-  {
+  if (merge) {
     Phase ph(st, 1);
     RL_TRY(launch_merge(mp, st));
     ph.launched();
@@ -617,7 +621,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, p.o_tickets + size_t(p.B) * 4 - p.o_status, st));
 
   Head hd;
-  RL_TRY_RC(run_head(cfg, p, X, W, b, targets, out_logp, out_entropy, nullptr, ws, st, hd));
+  RL_TRY_RC(run_head(cfg, p, X, W, b, targets, out_logp, out_entropy, nullptr, ws, st, hd, !p.fused_loss));
   const void* Xop = hd.Xop;
   const void* Wop = hd.Wop;
   const float* bias2 = hd.bias2;
@@ -643,8 +647,13 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   lp.coef = reinterpret_cast<float*>(ws + p.o_coef);
   lp.out_loss = out_loss;
   lp.out_metrics = out_metrics;
-  RL_TRY(launch_loss(lp, st));
-  ph_loss.launched(2);
+  if (p.fused_loss) {
+    RL_TRY(launch_merge_loss(mp, lp, st));
+    ph_loss.launched(2);
+  } else {
+    RL_TRY(launch_loss(lp, st));
+    ph_loss.launched(2);
+  }
   if (out_entropy_mask)
     RL_TRY(cudaMemcpyAsync(out_entropy_mask, p.ent ? emask : mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
   }

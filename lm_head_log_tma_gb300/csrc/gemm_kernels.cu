@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "engine.cuh"
+#include "merge_row.cuh"
 #include "kernels.h"
 
 namespace rl {
@@ -175,86 +176,11 @@ struct FwdPolicy {
   __device__ static void epilogue_finish(const Params&, int) {}
 };
 
-// Merge the 2P partial states of each row, one warp per row.  Each partial
-// holds, for one vocabulary segment and column half: reference m (log2
-// units, integer), s = sum 2^(t-m) and w = sum 2^(t-m) (t-m) as hi + lo
-// pairs, and the target's t if it fell there.  With M the largest m,
-//   S = sum_k 2^(m_k-M) s_k,   W = sum_k 2^(m_k-M) (w_k + (m_k-M) s_k).
-// Scaling by 2^(m_k-M) is exact in fp32, the sums are carried as
-// double-float (hi + lo) pairs, and only the final row values use fp64
-// (fp64 is a narrow unit on this GPU; conversions and adds per slot cost
-// more than the whole fp32 path).
-__device__ __forceinline__ float pow2_int(int d) {
-  // 2^d for an integer d <= 0; 0 below 2^-126 (such a slot weighs less than
-  // 2^-90 of the row sum: the forward keeps every s of the maximal slot >= 1/2)
-  return d < -126 ? 0.f : __int_as_float((127 + d) << 23);
-}
-__device__ __forceinline__ void df_warp_sum(float& hi, float& lo) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
-    const float ol = __shfl_xor_sync(0xffffffffu, lo, o);
-    two_sum_acc(hi, lo, oh);
-    lo += ol;
-  }
-}
-
+// One warp per row: see merge_row.cuh.
 __global__ void fwd_merge_kernel(MergeParams p) {
   const int row = int((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
   if (row >= p.N) return;
-  const float4* base = p.partial + size_t(row) * p.slots * 2;
-  float M = -INFINITY;
-  for (int k = lane; k < p.slots; k += 32) {
-    const float4 a = base[2 * k];
-    if (a.y + a.z > 0.f) M = fmaxf(M, a.x);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float shi = 0.f, slo = 0.f, whi = 0.f, wlo = 0.f, zy = 0.f;
-  int found = 0;
-  for (int k = lane; k < p.slots; k += 32) {
-    const float4 a = base[2 * k];
-    const float4 b = base[2 * k + 1];
-    if (a.y + a.z > 0.f) {
-      const float d = a.x - M;                   // integer, <= 0, exact
-      const float f = pow2_int(int(d));
-      two_sum_acc(shi, slo, a.y * f);
-      slo += a.z * f;
-      const float ds = d * a.y;                  // d * s_hi = ds + dse exactly
-      const float dse = fmaf(d, a.y, -ds);
-      two_sum_acc(whi, wlo, a.w * f);
-      two_sum_acc(whi, wlo, ds * f);
-      wlo += ((b.x + dse) + d * a.z) * f;
-    }
-    if (b.z != 0.f) {
-      zy = b.y;
-      found = 1;
-    }
-  }
-  df_warp_sum(shi, slo);
-  df_warp_sum(whi, wlo);
-  const unsigned who = __ballot_sync(0xffffffffu, found);
-  zy = __shfl_sync(0xffffffffu, zy, who ? __ffs(who) - 1 : 0);
-  if (lane != 0) return;
-  const double S = double(shi) + double(slo);
-  const double Wd = double(whi) + double(wlo);
-  const long long y = p.targets[row];
-  const double ln2 = 0.6931471805599453;
-  const double l2s = log2(S);
-  const double lse2 = double(M) + l2s;
-  const double ent = ln2 * (l2s - Wd / S);
-  double logp = ln2 * (double(zy) - lse2);
-  if (y < 0 || y >= p.V || !who) {
-    logp = __longlong_as_double(0x7ff8000000000000ll);
-    if (p.status) atomicOr(p.status, RLLOSS_DEV_EBADTARGET);
-  }
-  p.lse2[row] = float(lse2);
-  p.logp64[row] = logp;
-  p.ent32[row] = float(ent);
-  if (p.out_logp) p.out_logp[row] = float(logp);
-  if (p.out_ent) p.out_ent[row] = float(ent);
-  if (p.out_lse) p.out_lse[row] = float(ln2 * lse2);
+  merge_row(p, row, threadIdx.x & 31);
 }
 
 // =============================================================== dlogits

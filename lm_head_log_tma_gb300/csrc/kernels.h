@@ -134,5 +134,7 @@ cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long
                                 uint8_t* emask, cudaStream_t st);
 cudaError_t launch_loss(const LossParams& p, cudaStream_t st);
 int loss_slices(int B, int T, int sms);
+int fused_loss_slices(int T);
+cudaError_t launch_merge_loss(const MergeParams& mp, const LossParams& p, cudaStream_t st);
 
 }  // namespace rl

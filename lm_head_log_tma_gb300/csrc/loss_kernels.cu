@@ -14,6 +14,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "merge_row.cuh"
 #include "status.h"
 
 namespace rl {
@@ -132,91 +133,80 @@ cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long
 
 // ----------------------------------------------------------------------- K2
 constexpr int kLossThreads = 256;
+constexpr int kFusedRows = 8;      // rows per block of the fused merge + loss kernel (one per warp)
+constexpr int kRec = 10;           // doubles per sequence record
 
-__device__ __forceinline__ double block_sum(double v, double* sh) {
+template <int K>
+__device__ __forceinline__ void warp_sum_k(double (&v)[K]) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+  for (int k = 0; k < K; ++k)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_down_sync(0xffffffffu, v[k], o);
+}
+
+// K sums over the block, in a fixed order; the result is valid in thread 0.
+// With lane0_only, each warp's values are already summed into its lane 0.
+template <int K>
+__device__ __forceinline__ void block_sum_k(double (&v)[K], double (*sh)[32], bool lane0_only = false) {
+  if (!lane0_only) warp_sum_k(v);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0)
+#pragma unroll
+    for (int k = 0; k < K; ++k) sh[k][w] = v[k];
   __syncthreads();
-  if (l == 0) sh[w] = v;
-  __syncthreads();
-  double r = 0.0;
-  if (threadIdx.x == 0)
-    for (int i = 0; i < int(blockDim.x >> 5); ++i) r += sh[i];
-  return r;   // valid in thread 0
+  if (w == 0) {
+    const int nw = int(blockDim.x >> 5);
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = l < nw ? sh[k][l] : 0.0;
+    warp_sum_k(v);
+  }
 }
 
 __device__ __forceinline__ double logp_at(const LossParams& p, long long n) {
-  return p.logp_is_f64 ? static_cast<const double*>(p.logp)[n] : double(static_cast<const float*>(p.logp)[n]);
+  return p.logp_is_f64 ? __ldcg(static_cast<const double*>(p.logp) + n)
+                       : double(static_cast<const float*>(p.logp)[n]);
+}
+__device__ __forceinline__ double seq_adv(const LossParams& p, int i) {
+  return p.adv_per_token ? 0.0 : double(p.adv[i]);
 }
 
-// Partial sums of one slice of one sequence; the last slice block of a
-// sequence folds the slices in order into the sequence record, and the last
-// sequence folds the records into the loss and metrics (fixed order, so the
-// result does not depend on block timing).
-//
-// Sequence record: [0] term of the loss, [1] n_i, [2] clip count, [3] sum of
-// KL, [4] tokens kept by the entropy mask, [5] sequence log ratio, [6]
-// sequence ratio, [7] GMPO: kept fraction ebar_i; GSPO: gradient gate.
-__global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p) {
-  __shared__ double sh[32];
-  __shared__ int is_last;
-  const int i = blockIdx.y;
-  const int sl = blockIdx.x;
-  const long long base = (long long)i * p.T;
-  const int t0 = int((long long)sl * p.T / p.slices);
-  const int t1 = int((long long)(sl + 1) * p.T / p.slices);
-  const double A = p.adv_per_token ? 0.0 : double(p.adv[i]);
-  const bool gmpo = p.loss_type == RLLOSS_GMPO;
-  // GMPO: a_e = tokens kept by the entropy mask, a_kl = sum of K3 KL.
-  // GSPO: a_e / a_kl = sums of the positive / negative token advantages.
-  double a_m = 0, a_x = 0, a_e = 0, a_kl = 0, a_clip = 0;
-  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
-    const long long n = base + t;
-    const bool m = p.mask[n] != 0;
-    if (gmpo) {
-      if (!m) continue;
-      const double lp = logp_at(p, n);
-      const double lr = lp - double(p.old_logp[n]);
-      a_m += 1.0;
-      const bool clip = (A > 0.0 && lr > p.eps_high) || (A < 0.0 && lr < -p.eps_low);
-      a_x += clip ? (A > 0.0 ? p.eps_high : -p.eps_low) : lr;
-      a_clip += clip ? 1.0 : 0.0;
-      a_e += p.emask ? (p.emask[n] ? 1.0 : 0.0) : 1.0;
-      if (p.beta != 0.0) {
-        const double d = double(p.ref_logp[n]) - lp;
-        a_kl += exp(d) - d - 1.0;
-      }
-    } else {
-      if (m) {
-        a_m += 1.0;
-        a_x += logp_at(p, n) - double(p.old_logp[n]);
-      }
-      const double An = p.adv_per_token ? double(p.adv[n]) : (m ? A : 0.0);
-      if (An > 0.0) a_e += An; else a_kl += An;
+// Token n's share of its sequence's sums (lp = its logp):
+//   [0] active tokens, [1] sum of (clipped) log ratios, [4] clip count;
+//   GMPO: [2] tokens kept by the entropy mask, [3] sum of K3 KL;
+//   GSPO: [2] / [3] sums of the positive / negative token advantages.
+__device__ __forceinline__ void token_terms(const LossParams& p, long long n, double lp, double A, bool gmpo,
+                                            double (&a)[5]) {
+  const bool m = p.mask[n] != 0;
+  if (gmpo) {
+    if (!m) return;
+    const double lr = lp - double(p.old_logp[n]);
+    a[0] += 1.0;
+    const bool clip = (A > 0.0 && lr > p.eps_high) || (A < 0.0 && lr < -p.eps_low);
+    a[1] += clip ? (A > 0.0 ? p.eps_high : -p.eps_low) : lr;
+    a[4] += clip ? 1.0 : 0.0;
+    a[2] += p.emask ? (p.emask[n] ? 1.0 : 0.0) : 1.0;
+    if (p.beta != 0.0) {
+      const double d = double(p.ref_logp[n]) - lp;
+      a[3] += exp(d) - d - 1.0;
     }
+  } else {
+    if (m) {
+      a[0] += 1.0;
+      a[1] += lp - double(p.old_logp[n]);
+    }
+    const double An = p.adv_per_token ? double(p.adv[n]) : (m ? A : 0.0);
+    if (An > 0.0) a[2] += An; else a[3] += An;
   }
-  a_m = block_sum(a_m, sh);
-  a_x = block_sum(a_x, sh);
-  a_e = block_sum(a_e, sh);
-  a_kl = block_sum(a_kl, sh);
-  a_clip = block_sum(a_clip, sh);
-  if (threadIdx.x == 0) {
-    double* pr = p.part + (size_t(i) * p.slices + sl) * 5;
-    pr[0] = a_m; pr[1] = a_x; pr[2] = a_e; pr[3] = a_kl; pr[4] = a_clip;
-    __threadfence();
-    is_last = atomicAdd(p.seq_ticket + i, 1u) == unsigned(p.slices) - 1u;
-  }
-  __syncthreads();
-  if (!is_last || threadIdx.x != 0) return;
-  __threadfence();
-  double s5[5] = {0, 0, 0, 0, 0};
-  for (int k = 0; k < p.slices; ++k) {
-    const double* pr = p.part + (size_t(i) * p.slices + k) * 5;
-    for (int j = 0; j < 5; ++j) s5[j] += __ldcg(pr + j);
-  }
+}
+
+// Sequence record from the sequence's sums: [0] term of the loss, [1] n_i,
+// [2] clip count, [3] sum of KL, [4] tokens kept by the entropy mask, [5]
+// sequence log ratio, [6] sequence ratio, [7] GMPO: kept fraction ebar_i;
+// GMPO coefficient factors [8] 1/(B n_i) and [9] -A_i r_i ebar_i/(B n_i).
+__device__ __forceinline__ void seq_record(const LossParams& p, const double (&s5)[5], double A, bool gmpo,
+                                           double (&r8)[kRec]) {
   const double ni = s5[0];
-  double r8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int k = 0; k < kRec; ++k) r8[k] = 0.0;
   r8[1] = ni;
   if (gmpo) {
     const double mean_x = ni > 0 ? s5[1] / ni : 0.0;
@@ -225,6 +215,10 @@ __global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p
     const double klt = ni > 0 ? s5[3] / ni : 0.0;
     r8[0] = ni > 0 ? -A * r * ebar + p.beta * klt : 0.0;
     r8[2] = s5[4]; r8[3] = s5[3]; r8[4] = s5[2]; r8[5] = mean_x; r8[6] = r; r8[7] = ebar;
+    if (ni > 0) {
+      r8[8] = 1.0 / (double(p.B) * ni);
+      r8[9] = -A * r * ebar * r8[8];
+    }
   } else if (ni == 0) {
     if (p.status) atomicOr(p.status, RLLOSS_DEV_EEMPTYSEQ);
   } else {
@@ -236,25 +230,72 @@ __global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p
     r8[2] = (sv < p.clip_lo || sv > p.clip_hi) ? 1.0 : 0.0;
     r8[4] = ni; r8[5] = slr; r8[6] = sv;
   }
-  for (int k = 0; k < 8; ++k) p.seqres[size_t(i) * 8 + k] = r8[k];
-  __threadfence();
-  if (atomicAdd(p.ticket, 1u) != unsigned(p.B) - 1u) return;
-  __threadfence();
-  double loss = 0, n_act = 0, clip = 0, kl = 0, kept = 0, sx = 0, sr = 0, nh = 0;
-  for (int j = 0; j < p.B; ++j) {
-    const double* r = p.seqres + size_t(j) * 8;
+}
+
+// Token n's gradient coefficient c_n = dL/dlogp_n (r = its sequence record).
+__device__ __forceinline__ double token_coef(const LossParams& p, long long n, int i, const double* r, bool gmpo) {
+  const double ni = r[1];
+  double c = 0.0;
+  if (!gmpo && ni > 0) {
+    const double An = p.adv_per_token ? double(p.adv[n]) : (p.mask[n] ? double(p.adv[i]) : 0.0);
+    const double sv = r[6];
+    const bool flat = (An > 0.0 && sv > p.clip_hi) || (An < 0.0 && sv < p.clip_lo);
+    c = flat ? 0.0 : -An * sv;
+  } else if (gmpo && p.mask[n] && ni > 0) {
+    const double A = double(p.adv[i]);
+    const double lp = logp_at(p, n);
+    const double lr = lp - double(p.old_logp[n]);
+    const bool clip = (A > 0.0 && lr > p.eps_high) || (A < 0.0 && lr < -p.eps_low);
+    c = clip ? 0.0 : r[9];
+    if (p.beta != 0.0) c += p.beta * (1.0 - exp(double(p.ref_logp[n]) - lp)) * r[8];
+  }
+  return c;
+}
+__device__ __forceinline__ void store_coef(const LossParams& p, long long n, double c) {
+  if (p.coef) p.coef[n] = float(c * p.inv_tau);
+  if (p.dlogp) p.dlogp[n] = float(c);
+}
+
+// The slices of sequence i folded by warp 0 of the block that finished last
+// (lane k takes slices k, k+32, ...; then a fixed shuffle tree).  Writes the
+// sequence record; returns it on lane 0.
+__device__ __forceinline__ void fold_sequence(const LossParams& p, int i, int lane, bool gmpo, double (&r8)[kRec]) {
+  double s5[5] = {0, 0, 0, 0, 0};
+  for (int k = lane; k < p.slices; k += 32) {
+    const double* pr = p.part + (size_t(i) * p.slices + k) * 5;
+#pragma unroll
+    for (int j = 0; j < 5; ++j) s5[j] += __ldcg(pr + j);
+  }
+  warp_sum_k(s5);
+  if (lane == 0) {
+    seq_record(p, s5, seq_adv(p, i), gmpo, r8);
+    for (int k = 0; k < kRec; ++k) p.seqres[size_t(i) * kRec + k] = r8[k];
+  }
+}
+
+// Loss and metrics from all sequence records, by one warp, in a fixed order.
+__device__ __forceinline__ void fold_batch(const LossParams& p, int lane, bool gmpo) {
+  // [0] loss, [1] n_act, [2] clips, [3] KL, [4] kept, [5] sum of log ratios,
+  // [6] sum of ratios, [7] sequences with tokens.
+  double f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int j = lane; j < p.B; j += 32) {
+    const double* r = p.seqres + size_t(j) * kRec;
     const double nj = __ldcg(r + 1);
-    loss += __ldcg(r + 0);
-    n_act += nj;
-    clip += __ldcg(r + 2);
-    kl += __ldcg(r + 3);
-    kept += __ldcg(r + 4);
+    f[0] += __ldcg(r + 0);
+    f[1] += nj;
+    f[2] += __ldcg(r + 2);
+    f[3] += __ldcg(r + 3);
+    f[4] += __ldcg(r + 4);
     if (nj > 0) {
-      sx += __ldcg(r + 5);
-      sr += __ldcg(r + 6);
-      nh += 1.0;
+      f[5] += __ldcg(r + 5);
+      f[6] += __ldcg(r + 6);
+      f[7] += 1.0;
     }
   }
+  warp_sum_k(f);
+  if (lane != 0) return;
+  double loss = f[0];
+  const double n_act = f[1], clip = f[2], kl = f[3], kept = f[4], sx = f[5], sr = f[6], nh = f[7];
   float* m = p.out_metrics;
   if (gmpo) {
     loss /= double(p.B);
@@ -274,32 +315,102 @@ __global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p
   if (!isfinite(loss) && p.status) atomicOr(p.status, RLLOSS_DEV_ENONFINITE);
 }
 
+// Thread 0: publish this block's slice sums and take a ticket; true (for the
+// whole block) if this was the sequence's last slice.
+__device__ __forceinline__ bool publish_slice(const LossParams& p, int i, int sl, const double (&a)[5], int* flag) {
+  if (threadIdx.x == 0) {
+    double* pr = p.part + (size_t(i) * p.slices + sl) * 5;
+#pragma unroll
+    for (int j = 0; j < 5; ++j) pr[j] = a[j];
+    __threadfence();
+    const bool last = atomicAdd(p.seq_ticket + i, 1u) == unsigned(p.slices) - 1u;
+    if (last) __threadfence();
+    *flag = last ? 1 : 0;
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
+// Lane 0: take the batch ticket after writing a sequence record; true (for
+// the whole warp) if this was the last sequence.
+__device__ __forceinline__ bool take_batch_ticket(const LossParams& p, int lane) {
+  unsigned last = 0;
+  if (lane == 0) {
+    __threadfence();
+    last = atomicAdd(p.ticket, 1u) == unsigned(p.B) - 1u;
+    if (last) __threadfence();
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  __syncwarp();
+  return last != 0;
+}
+
+// Partial sums of one slice of one sequence; the last slice block of a
+// sequence folds the slices in order into the sequence record, and the last
+// sequence folds the records into the loss and metrics (fixed order, so the
+// result does not depend on block timing).
+__global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p) {
+  __shared__ double sh[5][32];
+  __shared__ int is_last;
+  const int i = blockIdx.y;
+  const int sl = blockIdx.x;
+  const long long base = (long long)i * p.T;
+  const int t0 = int((long long)sl * p.T / p.slices);
+  const int t1 = int((long long)(sl + 1) * p.T / p.slices);
+  const double A = seq_adv(p, i);
+  const bool gmpo = p.loss_type == RLLOSS_GMPO;
+  double a[5] = {0, 0, 0, 0, 0};
+  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+    const long long n = base + t;
+    token_terms(p, n, logp_at(p, n), A, gmpo, a);
+  }
+  block_sum_k(a, sh);
+  if (!publish_slice(p, i, sl, a, &is_last) || threadIdx.x >= 32) return;
+  double r8[kRec];
+  fold_sequence(p, i, threadIdx.x, gmpo, r8);
+  if (take_batch_ticket(p, threadIdx.x)) fold_batch(p, threadIdx.x, gmpo);
+}
+
 // Per-token gradient coefficient c_n = dL/dlogp_n from the sequence records.
 __global__ void loss_coef_kernel(LossParams p) {
   const long long N = (long long)p.B * p.T;
   const bool gmpo = p.loss_type == RLLOSS_GMPO;
   for (long long n = blockIdx.x * (long long)blockDim.x + threadIdx.x; n < N; n += (long long)gridDim.x * blockDim.x) {
     const int i = int(n / p.T);
-    const double* r = p.seqres + size_t(i) * 8;
-    const double ni = r[1];
-    double c = 0.0;
-    if (!gmpo && ni > 0) {
-      const double An = p.adv_per_token ? double(p.adv[n]) : (p.mask[n] ? double(p.adv[i]) : 0.0);
-      const double sv = r[6];
-      const bool flat = (An > 0.0 && sv > p.clip_hi) || (An < 0.0 && sv < p.clip_lo);
-      c = flat ? 0.0 : -An * sv;
-    } else if (gmpo && p.mask[n] && ni > 0) {
-      const double A = double(p.adv[i]);
-      const double lp = logp_at(p, n);
-      const double lr = lp - double(p.old_logp[n]);
-      const bool clip = (A > 0.0 && lr > p.eps_high) || (A < 0.0 && lr < -p.eps_low);
-      c = clip ? 0.0 : -A * r[6] * r[7];
-      if (p.beta != 0.0) c += p.beta * (1.0 - exp(double(p.ref_logp[n]) - lp));
-      c /= double(p.B) * ni;
-    }
-    if (p.coef) p.coef[n] = float(c * p.inv_tau);
-    if (p.dlogp) p.dlogp[n] = float(c);
+    store_coef(p, n, token_coef(p, n, i, p.seqres + size_t(i) * kRec, gmpo));
   }
+}
+
+// Row merge and loss sums in one launch, for batches without the entropy
+// mask (no batch-global threshold sits between the two): block (sl, i)
+// merges rows [16 sl, 16 sl + 16) of sequence i (a warp per row) and sums
+// their loss terms; the sequence's last block folds the slices into the
+// sequence record and the last sequence folds the batch.  The coefficients
+// follow in loss_coef_kernel (one sequence's tokens are too many for the
+// one block that holds its record).
+__global__ void __launch_bounds__(kLossThreads) merge_loss_kernel(MergeParams mp, LossParams p) {
+  __shared__ double sh[5][32];
+  __shared__ int is_last;
+  const int i = blockIdx.y;
+  const int sl = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long base = (long long)i * p.T;
+  const int t0 = sl * kFusedRows;
+  const int t1 = min(p.T, t0 + kFusedRows);
+  const double A = seq_adv(p, i);
+  const bool gmpo = p.loss_type == RLLOSS_GMPO;
+  double a[5] = {0, 0, 0, 0, 0};
+  for (int t = t0 + warp; t < t1; t += kLossThreads / 32) {
+    const long long n = base + t;
+    const double lp = merge_row(mp, int(n), lane);
+    if (lane == 0) token_terms(p, n, lp, A, gmpo, a);
+  }
+  if (lane == 0) __threadfence();   // this warp's row outputs before the slice ticket
+  block_sum_k(a, sh, true);         // only lane 0 of each warp holds terms
+  if (!publish_slice(p, i, sl, a, &is_last) || warp != 0) return;
+  double r8[kRec];
+  fold_sequence(p, i, lane, gmpo, r8);
+  if (take_batch_ticket(p, lane)) fold_batch(p, lane, gmpo);
 }
 
 int loss_slices(int B, int T, int sms) {
@@ -310,14 +421,25 @@ int loss_slices(int B, int T, int sms) {
   return int(s);
 }
 
+int fused_loss_slices(int T) { return (T + kFusedRows - 1) / kFusedRows; }
+
+static cudaError_t launch_coef(const LossParams& p, cudaStream_t st) {
+  const long long N = (long long)p.B * p.T;
+  long long nb = (N + 127) / 128;
+  if (nb > 8192) nb = 8192;
+  loss_coef_kernel<<<int(nb), 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_loss(const MergeParams& mp, const LossParams& p, cudaStream_t st) {
+  merge_loss_kernel<<<dim3(p.slices, p.B), kLossThreads, 0, st>>>(mp, p);
+  if (p.coef || p.dlogp) return launch_coef(p, st);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_loss(const LossParams& p, cudaStream_t st) {
   loss_partial_kernel<<<dim3(p.slices, p.B), kLossThreads, 0, st>>>(p);
-  if (p.coef || p.dlogp) {
-    const long long N = (long long)p.B * p.T;
-    long long nb = (N + 255) / 256;
-    if (nb > 4096) nb = 4096;
-    loss_coef_kernel<<<int(nb), 256, 0, st>>>(p);
-  }
+  if (p.coef || p.dlogp) return launch_coef(p, st);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,111 @@
+// Row merge of the forward's partial softmax states, shared by the merge
+// kernel and the fused merge + loss kernel.
+#pragma once
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "status.h"
+
+namespace rl {
+
+// Merge the 2P partial states of each row, one warp per row.  Each partial
+// holds, for one vocabulary segment and column half: reference m (log2
+// units, integer), s = sum 2^(t-m) and w = sum 2^(t-m) (t-m) as hi + lo
+// pairs, and the target's t if it fell there.  With M the largest m,
+//   S = sum_k 2^(m_k-M) s_k,   W = sum_k 2^(m_k-M) (w_k + (m_k-M) s_k).
+// Scaling by 2^(m_k-M) is exact in fp32, the sums are carried as
+// double-float (hi + lo) pairs, and only the final row values use fp64
+// (fp64 is a narrow unit on this GPU; conversions and adds per slot cost
+// more than the whole fp32 path).
+__device__ __forceinline__ float pow2_int(int d) {
+  // 2^d for an integer d <= 0; 0 below 2^-126 (such a slot weighs less than
+  // 2^-90 of the row sum: the forward keeps every s of the maximal slot >= 1/2)
+  return d < -126 ? 0.f : __int_as_float((127 + d) << 23);
+}
+__device__ __forceinline__ void df_warp_sum(float& hi, float& lo) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float ol = __shfl_xor_sync(0xffffffffu, lo, o);
+    two_sum_acc(hi, lo, oh);
+    lo += ol;
+  }
+}
+
+// Merges row `row` (all 32 lanes of the warp take part) and writes its lse,
+// logp and entropy; returns the row's logp on lane 0 (NaN for a bad target).
+__device__ __forceinline__ double merge_row(const MergeParams& p, int row, int lane) {
+  const long long y = lane == 0 ? p.targets[row] : 0;   // issued early, used at the end
+  const float4* base = p.partial + size_t(row) * p.slots * 2;
+  float M = -INFINITY;
+  for (int k = lane; k < p.slots; k += 32) {
+    const float4 a = base[2 * k];
+    if (a.y + a.z > 0.f) M = fmaxf(M, a.x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float shi = 0.f, slo = 0.f, whi = 0.f, wlo = 0.f, zy = 0.f;
+  int found = 0;
+  for (int k = lane; k < p.slots; k += 32) {
+    const float4 a = base[2 * k];
+    const float4 b = base[2 * k + 1];
+    if (a.y + a.z > 0.f) {
+      const float d = a.x - M;                   // integer, <= 0, exact
+      const float f = pow2_int(int(d));
+      two_sum_acc(shi, slo, a.y * f);
+      slo += a.z * f;
+      const float ds = d * a.y;                  // d * s_hi = ds + dse exactly
+      const float dse = fmaf(d, a.y, -ds);
+      two_sum_acc(whi, wlo, a.w * f);
+      two_sum_acc(whi, wlo, ds * f);
+      wlo += ((b.x + dse) + d * a.z) * f;
+    }
+    if (b.z != 0.f) {
+      zy = b.y;
+      found = 1;
+    }
+  }
+  df_warp_sum(shi, slo);
+  df_warp_sum(whi, wlo);
+  const unsigned who = __ballot_sync(0xffffffffu, found);
+  zy = __shfl_sync(0xffffffffu, zy, who ? __ffs(who) - 1 : 0);
+  if (lane != 0) return 0.0;
+  // log2 S = e + log2(mh) + log2(1 + slo/shi), with shi = 2^e mh, mh in
+  // [1, 2) (S >= 1/2, so shi is a normal number): log2f on [1, 2) is within
+  // an ulp of [0, 1); the last term is slo/shi/ln2 to first order
+  // (|slo/shi| < 2^-23).  W/S = q + q_lo with q = whi/shi and the exact
+  // division residual.  Both log2 S and log2 S - W/S are formed as fp32
+  // hi + lo pairs; fp64 (a narrow unit here) only joins and scales them.
+  const uint32_t sb = __float_as_uint(shi);
+  const float e = float(int(sb >> 23) - 127);
+  const float l2m = log2f(__uint_as_float((sb & 0x7fffffu) | 0x3f800000u));
+  const float corr = (slo / shi) * 1.44269504f;
+  const float q = whi / shi;
+  const float q_lo = (fmaf(-q, shi, whi) + fmaf(-q, slo, wlo)) / shi;
+  float yh = e, yl = 0.f;                  // log2 S
+  two_sum_acc(yh, yl, l2m);
+  yl += corr;
+  float xh = yh, xl = yl;                  // log2 S - W/S
+  two_sum_acc(xh, xl, -q);
+  xl -= q_lo;
+  const double ln2 = 0.6931471805599453;
+  const double l2s = double(yh) + double(yl);
+  const double lse2 = double(M) + l2s;
+  const double ent = ln2 * (double(xh) + double(xl));
+  double logp = ln2 * (double(zy) - lse2);
+  if (y < 0 || y >= p.V || !who) {
+    logp = __longlong_as_double(0x7ff8000000000000ll);
+    if (p.status) atomicOr(p.status, RLLOSS_DEV_EBADTARGET);
+  }
+  p.lse2[row] = float(lse2);
+  p.logp64[row] = logp;
+  p.ent32[row] = float(ent);
+  if (p.out_logp) p.out_logp[row] = float(logp);
+  if (p.out_ent) p.out_ent[row] = float(ent);
+  if (p.out_lse) p.out_lse[row] = float(ln2 * lse2);
+  return logp;
+}
+
+}  // namespace rl
