@@ -328,6 +328,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     call_alloc = torch.cuda.max_memory_allocated(dev) - mem0
     status = R.rlloss_get_device_status(ws)
+    bwd_rows = R.rlloss_get_backward_rows(ws)   # rows with c_n != 0: the backward runs over these
     if status != 0:
         raise RuntimeError(f"device status {status:#x}")
 
@@ -413,10 +414,11 @@ def run_ours(args):
     # ---- roofline of the dominant tensor-core kernel (phase timing, same timed region)
     peak, peak_sus, hbm, peak_src = load_peaks()
     per_step = [m / args.steps for m in phase_ms]
-    # tensor-core phases and their algorithmic flop per step (units of N*H*V)
-    gemm_phases = {0: ("fwd_gemm", 2.0), 2: ("bwd_dlogits", 2.0), 3: ("bwd_dX_dW", 4.0)}
+    # tensor-core phases and the flop they execute per step: the forward over
+    # all N rows, the recompute and dX/dW over the backward's rows
+    gemm_phases = {0: ("fwd_gemm", 2.0 * N), 2: ("bwd_dlogits", 2.0 * bwd_rows), 3: ("bwd_dX_dW", 4.0 * bwd_rows)}
     dom = max(gemm_phases, key=lambda k: per_step[k])
-    flops_phase = gemm_phases[dom][1] * N * H * V
+    flops_phase = gemm_phases[dom][1] * H * V
     launches_per_step = max(1, phase_n[dom] // args.steps)
     achieved = flops_phase / (per_step[dom] / 1e3) / 1e12
     traffic = None
@@ -428,6 +430,7 @@ def run_ours(args):
                 "peak_source": f"{peak_src} bf16 burst", "frac_of_sustained": achieved / peak_sus,
                 "launches_per_step": launches_per_step}
     step_tflops = 6.0 * N * H * V / (ms_step / 1e3) / 1e12
+    executed_tflops = (2.0 * N + 6.0 * bwd_rows) * H * V / (ms_step / 1e3) / 1e12
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -438,6 +441,9 @@ def run_ours(args):
                        "parallelism": "replicas" if world > 1 else "single"},
             "tc_peak_frac_6nhv": step_tflops / peak,
             "tc_tflops_6nhv": step_tflops,
+            "backward_rows": bwd_rows,
+            "executed_tflops": executed_tflops,
+            "executed_peak_frac": executed_tflops / peak,
             "roofline": roofline,
             "phases_ms_per_step": {R.PHASE_NAMES[i]: per_step[i] for i in range(R.NPHASES)},
             "clocks": clk,

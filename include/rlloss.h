@@ -86,6 +86,14 @@ extern "C" {
 #define RLLOSS_FLAG_SINGLE_CTA_TILES 0x2u    /* forward / recompute kernels on 128-row single-CTA
                                                 tiles instead of 256-row CTA-pair tiles (same
                                                 results; for comparison) */
+#define RLLOSS_FLAG_DENSE_BACKWARD 0x8u      /* run the backward over every row.  By default rows
+                                                whose coefficient c_n = dL/dlogp_n is zero (tokens
+                                                outside the mask, clipped tokens without KL, clipped
+                                                GSPO sequences) are dropped before the backward:
+                                                they add exactly nothing to dX, dW, db ("Add GMPO
+                                                ...", Details: the gradients are sums over tokens
+                                                of c_n times per-token terms).  Same results up to
+                                                fp32 summation order; for comparison */
 
 #define RLLOSS_NMETRICS 8
 /* out_metrics layout:
@@ -199,6 +207,13 @@ int rlloss_loss_from_logp_noalloc(const rlloss_cfg* cfg, const float* logp, cons
  * into *status.  Synchronous; call after the stream has finished.  Returns
  * RLLOSS_ECUDA if the copy failed. */
 int rlloss_get_device_status(const void* workspace, int32_t* status);
+
+/* Copy into *rows the number of rows the last rlloss_fwd_bwd on ``workspace``
+ * ran its backward over: the rows with c_n != 0, or every row under
+ * RLLOSS_FLAG_DENSE_BACKWARD (see there).  Synchronous; call after the stream
+ * has finished.  Returns RLLOSS_ECUDA if the copy failed.  (Our addition, for
+ * reporting executed work; the pages have no counterpart.) */
+int rlloss_get_backward_rows(const void* workspace, int32_t* rows);
 
 /* Launch a kernel that waits on a barrier nothing will complete, with a limit
  * of limit_ns nanoseconds, so the bounded-wait path can be exercised: the

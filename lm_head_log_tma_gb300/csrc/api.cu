@@ -20,6 +20,9 @@ namespace {
 using namespace rl;
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
+// Status region (first 256 bytes of every workspace): [0] device status word,
+// [4] loss-stage batch ticket, [8] compaction ticket, [12] backward rows.
+constexpr size_t kBackwardRowsOffset = 12;
 constexpr size_t kPartialCapBytes = size_t(64) << 20;
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
@@ -60,7 +63,8 @@ int validate_common(const rlloss_cfg* c) {
   if (!finite(c->beta)) return RLLOSS_EINVAL;
   const float q = c->top_entropy_quantile;
   if (!(q >= 0.f && q <= 1.f)) return RLLOSS_EINVAL;
-  if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN))
+  if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN |
+                   RLLOSS_FLAG_DENSE_BACKWARD))
     return RLLOSS_EINVAL;
   if ((c->flags & RLLOSS_FLAG_ADV_PER_TOKEN) && c->loss_type != RLLOSS_GSPO_TOKEN) return RLLOSS_EUNSUPPORTED;
   if (c->loss_type == RLLOSS_GSPO_TOKEN) {
@@ -75,7 +79,8 @@ int validate_head(const rlloss_cfg* c) {
   if (!c) return RLLOSS_EINVAL;
   if (c->B < 1 || c->T < 1) return RLLOSS_EINVAL;
   if ((long long)c->B * c->T > (1ll << 31) - 1) return RLLOSS_EINVAL;
-  if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN))
+  if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN |
+                   RLLOSS_FLAG_DENSE_BACKWARD))
     return RLLOSS_EINVAL;
   if (c->H < 1 || c->V < 1) return RLLOSS_EINVAL;
   if (c->dtype != RLLOSS_BF16 && c->dtype != RLLOSS_FP32) return RLLOSS_EINVAL;
@@ -104,6 +109,7 @@ struct Plan {
   int fwd_clusters, h_pairs;  // resident clusters of the forward and dX/dW kernels
   bool fp32, bias, ent;
   bool fused_loss;          // row merge and loss stage in one launch (no entropy mask)
+  bool compact;             // backward over the rows with c_n != 0 only
   int R, Vt, P, Hp, Vp;
   int kb_fwd, nseg_fwd;     // forward K: nseg_fwd * kb_fwd k-blocks
   int Kx;                   // row width (elements) of the bf16 X / W operand arrays
@@ -112,7 +118,8 @@ struct Plan {
   int slices;
   size_t o_tickets, o_part;
   size_t o_status, o_partial, o_lse2, o_logp64, o_ent, o_coef, o_emask, o_k3, o_seq, o_bias2, o_dl, o_x3, o_w3,
-      o_dbpart, total;
+      o_dbpart, o_blk, o_cidx, o_xc, o_coefc, o_lse2c, o_tgtc, o_dxc, total;
+  int Ncap;                 // rows of the compacted arrays (N rounded up to 256)
 };
 
 int choose_segments(int R, int Vt, int G, long long N) {
@@ -204,6 +211,17 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.o_coef = take(size_t(p.N) * 4);
     p.o_dl = take(size_t(p.Nc) * p.ld_dl * 2);
     p.o_dbpart = take(p.bias ? size_t(db_part_rows(p.Nc)) * p.V * 4 : 0);
+    p.compact = !(c->flags & RLLOSS_FLAG_DENSE_BACKWARD);
+    if (p.compact) {
+      p.Ncap = int(rup(p.N, 256));
+      p.o_blk = take(size_t(compact_groups(p.N)) * 2 * 4);
+      p.o_cidx = take(size_t(p.Ncap) * 4);
+      p.o_coefc = take(size_t(p.Ncap) * 4);
+      p.o_lse2c = take(size_t(p.Ncap) * 4);
+      p.o_tgtc = take(size_t(p.Ncap) * 8);
+      p.o_xc = take(size_t(p.Ncap) * p.Kx * 2);
+      p.o_dxc = take(size_t(p.Nc) * p.H * 4);
+    }
   }
   p.total = off;
   return p;
@@ -529,6 +547,12 @@ int rlloss_get_device_status(const void* workspace, int32_t* status) {
   return cuda_rc(cudaMemcpy(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost));
 }
 
+int rlloss_get_backward_rows(const void* workspace, int32_t* rows) {
+  if (!workspace || !rows) return RLLOSS_EINVAL;
+  return cuda_rc(cudaMemcpy(rows, static_cast<const char*>(workspace) + kBackwardRowsOffset, sizeof(int32_t),
+                            cudaMemcpyDeviceToHost));
+}
+
 int rlloss_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* stream) {
   if (!workspace || !aligned(workspace, 256)) return RLLOSS_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -660,15 +684,65 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
 
   // ---- backward, one chunk of rows at a time:
   //      G = (c/tau)(onehot - p) as bf16, dX = G W, dW += G^T X, db += sum G.
+  // Rows with c_n = 0 add nothing to any of the three; unless the caller asks
+  // for the dense backward they are dropped first (ordered compaction), the
+  // chunks run over the kept rows, and dX rows are scattered back (the rest
+  // of dX is zero).  The kept-row count stays on the device: every backward
+  // kernel reads it, and chunks past it do no work.
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dl);
   const int lo_off = p.fp32 ? p.Vp : 0;
+  int* rows_total = reinterpret_cast<int*>(ws + p.o_status + kBackwardRowsOffset);
+  const void* Xb = Xop;              // X operand rows of the backward
+  const int64_t* tg_b = targets;
+  const float* lse2_b = mp.lse2;
+  const float* coef_b = lp.coef;
+  const int* cidx = nullptr;
+  float* dxc = nullptr;
+  long long xb_rows = p.N;
+  {
+    Phase ph(st, 5);
+    if (p.compact) {
+      CompactParams cp{};
+      cp.N = p.N;
+      cp.Kx = p.Kx;
+      cp.Ncap = p.Ncap;
+      cp.coef = lp.coef;
+      cp.lse2 = mp.lse2;
+      cp.targets = targets;
+      cp.x = static_cast<const __nv_bfloat16*>(Xop);
+      cp.blk_cnt = reinterpret_cast<int*>(ws + p.o_blk);
+      cp.blk_off = cp.blk_cnt + compact_groups(p.N);
+      cp.ticket = reinterpret_cast<unsigned int*>(ws + p.o_status + 8);
+      cp.total = rows_total;
+      cp.idx = reinterpret_cast<int*>(ws + p.o_cidx);
+      cp.coefc = reinterpret_cast<float*>(ws + p.o_coefc);
+      cp.lse2c = reinterpret_cast<float*>(ws + p.o_lse2c);
+      cp.tgtc = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
+      cp.xc = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
+      RL_TRY(launch_compact(cp, st));
+      RL_TRY(cudaMemsetAsync(dX, 0, size_t(p.N) * p.H * 4, st));
+      ph.launched(2);
+      Xb = cp.xc;
+      tg_b = cp.tgtc;
+      lse2_b = cp.lse2c;
+      coef_b = cp.coefc;
+      cidx = cp.idx;
+      dxc = reinterpret_cast<float*>(ws + p.o_dxc);
+      xb_rows = p.Ncap;
+    } else {
+      RL_TRY(launch_set_total(rows_total, p.N, st));
+      ph.launched();
+    }
+  }
+  CUtensorMap tm_xb;
+  if (!tmap_bf16(&tm_xb, Xb, p.Kx, xb_rows, p.Kx, 128)) return RLLOSS_ECUDA;
   for (int ch = 0; ch < p.nchunks; ++ch) {
     const int n0 = ch * p.Nc;
-    const int nc = std::min(p.Nc, p.N - n0);
+    const int nc = std::min(p.Nc, p.N - n0);   // upper bound; the kernels clamp to the kept rows
     const int Rc = int(cdiv(nc, p.rows_tile));
 
     DlParams dp{};
-    dp.tmA = fp.tmA;
+    dp.tmA = tm_xb;
     dp.tmB = fp.tmB;
     dp.nseg = fp.nseg;
     dp.kb_per_seg = fp.kb_per_seg;
@@ -677,14 +751,15 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     dp.n0 = n0;
     dp.Nc = nc;
     dp.Rc = Rc;
+    dp.rows_total = rows_total;
     dp.V = p.V;
     dp.Vp = p.Vp;
     dp.Vt = p.Vt;
     dp.scale2 = scale2;
     dp.bias2 = bias2;
-    dp.targets = targets;
-    dp.lse2 = mp.lse2;
-    dp.coef = lp.coef;
+    dp.targets = tg_b;
+    dp.lse2 = lse2_b;
+    dp.coef = coef_b;
     dp.dl = dl;
     dp.ld = p.ld_dl;
     if (!tmap_bf16_box(&dp.tmG, dl, p.fp32 ? 2ll * p.Vp : p.V, nc, p.ld_dl, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
@@ -704,12 +779,13 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     {
       HParams hp{};
       set_bwd_segments(hp, p);
+      float* dx_out = p.compact ? dxc : dX + size_t(n0) * p.H;
       const long long g_inner = p.fp32 ? 2ll * p.Vp : p.V;
       if (!tmap_bf16(&hp.tmA[0], dl, g_inner, nc, p.ld_dl, 128)) return RLLOSS_ECUDA;
       if (!tmap_bf16(&hp.tmB[0], Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
-      if (!tmap_f32_out(&hp.tmO[0], dX + size_t(n0) * p.H, p.H, nc)) return RLLOSS_ECUDA;
+      if (!tmap_f32_out(&hp.tmO[0], dx_out, p.H, nc)) return RLLOSS_ECUDA;
       if (!tmap_bf16(&hp.tmA[1], dl, g_inner, nc, p.ld_dl, 64)) return RLLOSS_ECUDA;
-      if (!tmap_bf16(&hp.tmB[1], Xop, p.Kx, p.N, p.Kx, 64)) return RLLOSS_ECUDA;
+      if (!tmap_bf16(&hp.tmB[1], Xb, p.Kx, xb_rows, p.Kx, 64)) return RLLOSS_ECUDA;
       if (!tmap_f32_out(&hp.tmO[1], dW, p.H, p.V)) return RLLOSS_ECUDA;
       HProblem& px = hp.pr[0];
       px.kb_per_seg = int(cdiv(p.V, 64));
@@ -736,16 +812,24 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       hp.nprob = 2;
       const int kx = hp.nseg * px.kb_per_seg / px.ksplit, kw = hp.nseg * pw.kb_per_seg;
       hp.d_tiles = std::max(1, (kx + kw / 2) / kw);
+      hp.rows_total = rows_total;
+      hp.n0 = n0;
+      hp.nc_max = nc;
       hp.status = status;
       hp.limit_ns = kWaitLimitNs;
       Phase ph(st, 3);
-      if (px.reduce) RL_TRY(cudaMemsetAsync(dX + size_t(n0) * p.H, 0, size_t(nc) * p.H * 4, st));
+      if (px.reduce) RL_TRY(cudaMemsetAsync(dx_out, 0, size_t(nc) * p.H * 4, st));
       RL_TRY(launch_gemmH(hp, px.Mt * px.Ht * px.ksplit + pw.Mt * pw.Ht, st));
       ph.launched();
+      if (p.compact) {
+        RL_TRY(launch_scatter_rows(dxc, cidx, rows_total, n0, nc, p.H, dX, st));
+        ph.launched();
+      }
     }
     if (p.bias) {
       Phase ph(st, 5);
-      RL_TRY(launch_db(dl, p.ld_dl, lo_off, nc, p.V, reinterpret_cast<float*>(ws + p.o_dbpart), db, ch > 0, st));
+      RL_TRY(launch_db(dl, p.ld_dl, lo_off, nc, rows_total, n0, p.V, reinterpret_cast<float*>(ws + p.o_dbpart), db,
+                       ch > 0, st));
       ph.launched(2);
     }
   }

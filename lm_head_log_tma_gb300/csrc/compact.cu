@@ -1,0 +1,151 @@
+// Backward row compaction.
+//
+// The backward's per-row factor is the gradient coefficient c_n (GMPO page,
+// Details: the input/weight/bias gradients are sums over tokens of
+// c_n (onehot - p_n) against W or X).  A row with c_n = 0 -- a prompt or
+// padding token, a token whose log ratio is clipped (no KL term), every token
+// of a clipped GSPO sequence -- adds exactly nothing to dX, dW or db, so the
+// recompute and both GEMMs run over the other rows only.  The compaction is
+// ordered (a prefix sum over 32-row groups, ranks within a group by a warp
+// ballot), so repeated calls see the same row order and give the same bits.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace rl {
+
+constexpr int kCompactBlock = 256;
+constexpr int kGroup = 32;        // rows per compaction group (one warp's ballot)
+
+// Per 32-row group: rows with c != 0.  The block that finishes last turns
+// the counts into exclusive offsets (fixed order), writes the total and
+// zero-fills the compacted arrays from the total up to the next multiple of
+// 256 rows (the backward reads whole 256-row tiles).
+__global__ void __launch_bounds__(kCompactBlock) compact_count_kernel(CompactParams p) {
+  __shared__ int is_last;
+  __shared__ int part[kCompactBlock];
+  const int n = blockIdx.x * kCompactBlock + threadIdx.x;
+  const unsigned bal = __ballot_sync(0xffffffffu, n < p.N && p.coef[n] != 0.f);
+  const int ngroups = (p.N + kGroup - 1) / kGroup;
+  const int grp = n / kGroup;
+  if ((threadIdx.x & 31) == 0 && grp < ngroups) p.blk_cnt[grp] = __popc(bal);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    is_last = atomicAdd(p.ticket, 1u) == gridDim.x - 1;
+    if (is_last) __threadfence();
+  }
+  __syncthreads();
+  if (!is_last) return;
+  const int per = (ngroups + kCompactBlock - 1) / kCompactBlock;   // consecutive groups per thread
+  int s = 0;
+  for (int k = 0; k < per; ++k) {
+    const int i = threadIdx.x * per + k;
+    if (i < ngroups) s += __ldcg(p.blk_cnt + i);
+  }
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 1; o < kCompactBlock; o <<= 1) {   // inclusive scan of part[]
+    const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int base = threadIdx.x ? part[threadIdx.x - 1] : 0;
+  for (int k = 0; k < per; ++k) {
+    const int i = threadIdx.x * per + k;
+    if (i < ngroups) {
+      p.blk_off[i] = base;
+      base += __ldcg(p.blk_cnt + i);
+    }
+  }
+  const int total = part[kCompactBlock - 1];
+  if (threadIdx.x == 0) *p.total = total;
+  const int tail_end = min((total + 255) / 256 * 256, p.Ncap);
+  for (int r = total + threadIdx.x; r < tail_end; r += kCompactBlock) {
+    p.idx[r] = 0;
+    p.coefc[r] = 0.f;
+    p.lse2c[r] = 0.f;
+    p.tgtc[r] = -1;
+  }
+  const int words = p.Kx / 8;   // 16-byte words per row
+  const long long tail_words = (long long)(tail_end - total) * words;
+  for (long long w = threadIdx.x; w < tail_words; w += kCompactBlock) {
+    const long long r = total + w / words;
+    reinterpret_cast<uint4*>(p.xc + r * p.Kx)[w % words] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Block b handles the 32 rows of group b: each kept row goes to its group's
+// offset plus its rank in the group, with its index, coefficient, lse and
+// target; then the block copies the kept X rows (16-byte words spread over
+// all threads).
+__global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactParams p) {
+  __shared__ int rows[kGroup];
+  __shared__ int cnt;
+  const int g = blockIdx.x;
+  if (threadIdx.x < 32) {
+    const int n = g * kGroup + threadIdx.x;
+    const bool keep = n < p.N && p.coef[n] != 0.f;
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    const int rank = __popc(bal & ((1u << threadIdx.x) - 1u));
+    if (keep) {
+      const int pos = p.blk_off[g] + rank;
+      p.idx[pos] = n;
+      p.coefc[pos] = p.coef[n];
+      p.lse2c[pos] = p.lse2[n];
+      p.tgtc[pos] = p.targets[n];
+      rows[rank] = n;
+    }
+    if (threadIdx.x == 0) cnt = __popc(bal);
+  }
+  __syncthreads();
+  const int base = p.blk_off[g];
+  const int words = p.Kx / 8;
+  const int total_words = cnt * words;
+  for (int w = threadIdx.x; w < total_words; w += kCompactBlock) {
+    const int r = w / words, c = w - r * words;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + size_t(rows[r]) * p.Kx) + c);
+    reinterpret_cast<uint4*>(p.xc + size_t(base + r) * p.Kx)[c] = v;
+  }
+}
+
+__global__ void set_total_kernel(int* total, int N) { *total = N; }
+
+__global__ void scatter_rows_kernel(const float4* src, const int* idx, const int* total, int n0, int nc_max, int H4,
+                                    float4* dst) {
+  const int nc = min(max(*total - n0, 0), nc_max);
+  const long long n = (long long)nc * H4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long j = i / H4;
+    const int c = int(i - j * H4);
+    dst[(long long)idx[n0 + j] * H4 + c] = src[i];
+  }
+}
+
+int compact_groups(int N) { return (N + kGroup - 1) / kGroup; }
+
+cudaError_t launch_compact(const CompactParams& p, cudaStream_t st) {
+  compact_count_kernel<<<(p.N + kCompactBlock - 1) / kCompactBlock, kCompactBlock, 0, st>>>(p);
+  compact_gather_kernel<<<compact_groups(p.N), kCompactBlock, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_set_total(int* total, int N, cudaStream_t st) {
+  set_total_kernel<<<1, 1, 0, st>>>(total, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_rows(const float* src, const int* idx, const int* total, int n0, int nc_max, int H,
+                                float* dst, cudaStream_t st) {
+  const long long n = (long long)nc_max * (H / 4);
+  long long blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  scatter_rows_kernel<<<int(blocks), 256, 0, st>>>(reinterpret_cast<const float4*>(src), idx, total, n0, nc_max,
+                                                   H / 4, reinterpret_cast<float4*>(dst));
+  return cudaGetLastError();
+}
+
+}  // namespace rl

@@ -201,7 +201,9 @@ struct DlPolicy {
   using Params = DlParams;
   struct EpiState {
     int nbuf = 0;
+    int nc = -1;   // rows of this chunk (read from the device on the first tile)
   };
+  __device__ static int chunk_rows(const Params& p) { return min(max(*p.rows_total - p.n0, 0), p.Nc); }
 
   __device__ static void cta_setup(const Params&, uint8_t*) {}
   __device__ static void prefetch(const Params& p) {
@@ -212,12 +214,13 @@ struct DlPolicy {
   // Tiles u = j * Rc + r: CTAs running together share the W tile j.
   template <class F>
   __device__ static void for_each_tile(const Params& p, F&& f) {
-    const int tiles = p.Rc * p.Vt;
+    const int Rc = (chunk_rows(p) + kRows - 1) / kRows;
+    const int tiles = Rc * p.Vt;
     const int kbs = p.nseg * p.kb_per_seg;
     const int g0 = blockIdx.x / CL, gn = gridDim.x / CL;
     for (int u = g0; u < tiles; u += gn) {
-      const int j = u / p.Rc;
-      const int r = u - j * p.Rc;
+      const int j = u / Rc;
+      const int r = u - j * Rc;
       TileInfo t{r * kRows, j * 256, 0, kbs, u, 0, true, true};
       if (!f(t)) return;
     }
@@ -272,7 +275,8 @@ struct DlPolicy {
     uint8_t* wbuf = extra + (q + 4 * half) * 2 * kStageBuf;
     const int r0 = t.m0 + 128 * int(rank) + q * 32;   // first row of this warp within the chunk
     const int rl = r0 + lane;
-    const bool valid = rl < p.Nc;
+    if (e.nc < 0) e.nc = chunk_rows(p);
+    const bool valid = rl < e.nc;
     const int row = p.n0 + rl;
     const float lse2 = valid ? p.lse2[row] : 0.f;
     const float cf = valid ? p.coef[row] : 0.f;
@@ -366,11 +370,22 @@ struct HPolicy {
       tma_prefetch_desc(&p.tmO[q]);
     }
   }
+  // The chunk's row count is read on the device: problem 0 (dX) gets its
+  // row tiles from it, problem 1 (dW) its k-blocks per term.
+  __device__ static void chunk_problems(const Params& p, HProblem (&pr)[2]) {
+    const int nc = min(max(*p.rows_total - p.n0, 0), p.nc_max);
+    pr[0] = p.pr[0];
+    pr[1] = p.pr[1];
+    pr[0].Mt = (nc + 255) / 256;
+    if (p.nprob > 1) {
+      pr[1].kb_per_seg = (nc + 63) / 64;
+      if (nc == 0 && pr[1].reduce) pr[1].Mt = 0;   // nothing to add
+    }
+  }
   // Unit u of problem q: order 0 numbers (k part, h tile, row tile) with the
   // row tile fastest; order 1 numbers (row tile, h tile) with h fastest.
   // A problem with ksplit 2 cuts the k range in two halves, one unit each.
-  __device__ static TileInfo tile_of(const Params& p, int q, int u) {
-    const HProblem& pr = p.pr[q];
+  __device__ static TileInfo tile_of(const Params& p, const HProblem& pr, int q, int u) {
     const int per = pr.Mt * pr.Ht;
     const int part = u / per;
     const int v = u - part * per;
@@ -384,9 +399,9 @@ struct HPolicy {
     }
     const int kbt = p.nseg * pr.kb_per_seg;
     const int cut = pr.ksplit == 2 ? kbt / 2 : kbt;
-    return TileInfo{i * 256, j * kNH, part == 0 ? 0 : cut, part == 0 ? cut : kbt, u, q, true, true};
+    return TileInfo{i * 256, j * kNH, part == 0 ? 0 : cut, part == 0 ? cut : kbt, u, q, true, true, pr.kb_per_seg};
   }
-  __device__ static int units(const Params& p, int q) { return p.pr[q].Mt * p.pr[q].Ht * p.pr[q].ksplit; }
+  __device__ static int units(const HProblem& pr) { return pr.Mt * pr.Ht * pr.ksplit; }
   // Pair g of gn: problem 0 units g, g+gn, ...; then problem 1 units.  Pairs
   // that got fewer problem-0 units ("early" pairs) first take problem-1 units
   // [0, F*d) round-robin among themselves, d = problem-0 unit length in
@@ -394,28 +409,32 @@ struct HPolicy {
   // units run at the same time, so operand tiles they share stay in L2.
   template <class F>
   __device__ static void for_each_tile(const Params& p, F&& f) {
+    HProblem pr[2];
+    chunk_problems(p, pr);
     const int g = blockIdx.x >> 1, gn = gridDim.x >> 1;
-    const int T0 = units(p, 0);
+    const int T0 = units(pr[0]);
     for (int u = g; u < T0; u += gn)
-      if (!f(tile_of(p, 0, u))) return;
+      if (!f(tile_of(p, pr[0], 0, u))) return;
     if (p.nprob < 2) return;
-    const int T1 = units(p, 1);
+    const int T1 = units(pr[1]);
+    const int kx = p.nseg * pr[0].kb_per_seg / pr[0].ksplit, kw = p.nseg * pr[1].kb_per_seg;
+    const int d_tiles = kw > 0 ? max(1, (kx + kw / 2) / kw) : 1;
     const int r = T0 % gn;
     const int early = (r == 0) ? 0 : gn - r;
-    const int ph1 = min(T1, early * p.d_tiles);
+    const int ph1 = min(T1, early * d_tiles);
     if (early > 0 && g >= r)
       for (int u = g - r; u < ph1; u += early)
-        if (!f(tile_of(p, 1, u))) return;
+        if (!f(tile_of(p, pr[1], 1, u))) return;
     for (int u = ph1 + g; u < T1; u += gn)
-      if (!f(tile_of(p, 1, u))) return;
+      if (!f(tile_of(p, pr[1], 1, u))) return;
   }
   // One k-block: this CTA's 128 A rows and, for each sub, its 112 B rows
   // (two 64-h runs, rows beyond 112 unused).
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int q = t.seg;
     const HProblem& pr = p.pr[q];
-    const int s = kb / pr.kb_per_seg;
-    const int kk = (kb - s * pr.kb_per_seg) * 64;
+    const int s = kb / t.kbps;
+    const int kk = (kb - s * t.kbps) * 64;
     const int r = t.m0 + 128 * int(rank);
     if (pr.a_mn) {
       tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + r, pr.a_outer0 + kk);
@@ -455,12 +474,18 @@ struct HPolicy {
     uint8_t* buf = extra + (q + 4 * half) * kBoxBytes;
     const int y0 = t.m0 + 128 * int(rank) + q * 32;
     const int c_begin = half ? 4 : 0, c_end = half ? 7 : 4;
+    const bool no_k = t.kb_end <= t.kb_begin;   // empty sum (a chunk without rows): store zeros
 #pragma unroll 1
     for (int c = c_begin; c < c_end; ++c) {
       const int x0 = t.n0 + sub * kNS + c * 32;
       if (x0 >= pr.Hout) break;
       float v[32];
-      tmem_ld32(taddr + uint32_t(c * 32), v);
+      if (no_k) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      } else {
+        tmem_ld32(taddr + uint32_t(c * 32), v);
+      }
       if (lane == 0) tma_store_wait_read<0>();
       __syncwarp();
       float4* row = reinterpret_cast<float4*>(buf + lane * 128);
@@ -515,9 +540,11 @@ __global__ void split3_kernel(const float* src, long long rows, int cols, int Cp
 // Column sums of G over blocks of kDbRows chunk rows: part[blk][v] (hi + lo
 // terms in fp32 mode).  No atomics, so db is reproducible bit for bit.
 constexpr int kDbRows = 256;
-__global__ void db_part_kernel(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, int V, float* part) {
+__global__ void db_part_kernel(const __nv_bfloat16* dl, int ld, int lo_off, int Ncap, const int* rows_total, int n0,
+                               int V, float* part) {
   const int v = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
   if (v >= V) return;
+  const int Nc = min(max(*rows_total - n0, 0), Ncap);
   const int r0 = blockIdx.y * kDbRows;
   const int r1 = min(Nc, r0 + kDbRows);
   float a0 = 0.f, a1 = 0.f;
@@ -667,11 +694,11 @@ cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __
   return cudaGetLastError();
 }
 int db_part_rows(int Nc) { return (Nc + kDbRows - 1) / kDbRows; }
-cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, int V, float* part, float* db,
-                      int accumulate, cudaStream_t st) {
+cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, const int* rows_total, int n0, int V,
+                      float* part, float* db, int accumulate, cudaStream_t st) {
   const int nblk = db_part_rows(Nc);
   dim3 grid((V / 2 + 1 + 255) / 256, nblk);
-  db_part_kernel<<<grid, 256, 0, st>>>(dl, ld, lo_off, Nc, V, part);
+  db_part_kernel<<<grid, 256, 0, st>>>(dl, ld, lo_off, Nc, rows_total, n0, V, part);
   db_reduce_kernel<<<(V + 255) / 256, 256, 0, st>>>(part, nblk, V, db, accumulate);
   return cudaGetLastError();
 }

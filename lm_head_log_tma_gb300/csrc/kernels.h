@@ -42,7 +42,8 @@ struct DlParams {
   CUtensorMap tmG;            // G chunk buffer: inner columns, outer chunk rows; box 32 x 32, 64-byte swizzle
   int nseg, kb_per_seg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];
-  int n0, Nc, Rc, V, Vp, Vt;  // chunk start row, rows in chunk, row tiles (128 or 256 rows), vocab, padded vocab, vocab tiles
+  int n0, Nc, Rc, V, Vp, Vt;  // chunk start row, rows in chunk (upper bound), row tiles (128 or 256 rows), vocab, padded vocab, vocab tiles
+  const int* rows_total;      // device: rows of the backward operands (chunk rows = clamp(*rows_total - n0, 0, Nc))
   float scale2;
   const float* bias2;
   const int64_t* targets;
@@ -76,7 +77,11 @@ struct HParams {
   CUtensorMap tmO[2];         // fp32 output: inner h, outer rows, box 32 x 32, 128-byte swizzle
   HProblem pr[2];             // problem 0 must be the K-major one (a_mn = 0) when both run
   int nprob;                  // 1 or 2
-  int d_tiles;                // problem-0 tile length in problem-1 tiles (scheduling)
+  int d_tiles;                // problem-0 tile length in problem-1 tiles (host estimate; the kernel recomputes it)
+  // Rows of the chunk, read on the device: nc = clamp(*rows_total - n0, 0, nc_max).
+  // Problem 0 (dX) has ceil(nc/256) row tiles; problem 1 (dW) ceil(nc/64) k-blocks per term.
+  const int* rows_total;
+  int n0, nc_max;
   int nseg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];  // inner-coordinate offsets of each product term
   int* status;
@@ -121,9 +126,37 @@ cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st
 cudaError_t launch_gemmH(const HParams& p, int units, cudaStream_t st);
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st);
 cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __nv_bfloat16* out, cudaStream_t st);
-// db (+)= column sums of the chunk's G; part is scratch of db_part_rows(Nc) * V floats.
+// Backward row compaction (rows whose coefficient c_n is 0 add nothing to
+// dX, dW, db).  Arrays are indexed by compacted row; rows from the total up
+// to the next multiple of 256 are zero-filled (target -1).
+struct CompactParams {
+  int N, Kx, Ncap;            // rows, bf16 row width of X operand, rows allocated (multiple of 256)
+  const float* coef;          // [N] c_n / temperature
+  const float* lse2;          // [N]
+  const int64_t* targets;     // [N]
+  const __nv_bfloat16* x;     // [N, Kx] X operand (bf16, or the fp32 split terms)
+  int* blk_cnt;               // [compact_groups(N)] scratch
+  int* blk_off;               // [compact_groups(N)] scratch
+  unsigned int* ticket;       // zeroed before the launch
+  int* total;                 // out: compacted rows
+  int* idx;                   // [Ncap] compacted row -> original row
+  float* coefc;               // [Ncap]
+  float* lse2c;               // [Ncap]
+  int64_t* tgtc;              // [Ncap]
+  __nv_bfloat16* xc;          // [Ncap, Kx]
+};
+int compact_groups(int N);   // 32-row groups
+cudaError_t launch_compact(const CompactParams& p, cudaStream_t st);
+cudaError_t launch_set_total(int* total, int N, cudaStream_t st);
+// dst[idx[n0 + j]][:] = src[j][:] for j < clamp(*total - n0, 0, nc_max); H % 4 == 0.
+cudaError_t launch_scatter_rows(const float* src, const int* idx, const int* total, int n0, int nc_max, int H,
+                                float* dst, cudaStream_t st);
+
+// db (+)= column sums of the chunk's G rows (clamp(*rows_total - n0, 0, Nc) of them);
+// part is scratch of db_part_rows(Nc) * V floats.
 int db_part_rows(int Nc);
-cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, int V, float* part, float* db,
+cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, const int* rows_total, int n0, int V,
+                      float* part, float* db,
                       int accumulate, cudaStream_t st);
 cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
 

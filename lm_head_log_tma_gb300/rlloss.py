@@ -25,6 +25,7 @@ IS_TOKEN, IS_SEQUENCE = 0, 1
 FLAG_FORCE_ENTROPY_PATH = 0x1
 FLAG_SINGLE_CTA_TILES = 0x2
 FLAG_ADV_PER_TOKEN = 0x4
+FLAG_DENSE_BACKWARD = 0x8
 NMETRICS = 8
 
 
@@ -69,6 +70,8 @@ def _load():
     lib.rlloss_loss_from_logp.restype = c_int
     lib.rlloss_get_device_status.argtypes = [P, ctypes.POINTER(c_int32)]
     lib.rlloss_get_device_status.restype = c_int
+    lib.rlloss_get_backward_rows.argtypes = [P, ctypes.POINTER(c_int32)]
+    lib.rlloss_get_backward_rows.restype = c_int
     lib.rlloss_selftest_bounded_wait.argtypes = [P, c_uint64, P]
     lib.rlloss_selftest_bounded_wait.restype = c_int
     lib.rlloss_phase_timing.argtypes = [c_int]
@@ -150,6 +153,14 @@ def rlloss_get_device_status(workspace) -> int:
     if rc != OK:
         raise RllossError(rc, "rlloss_get_device_status")
     return int(st.value)
+
+
+def rlloss_get_backward_rows(workspace) -> int:
+    rows = c_int32(0)
+    rc = lib.rlloss_get_backward_rows(_p(workspace), ctypes.byref(rows))
+    if rc != OK:
+        raise RllossError(rc, "rlloss_get_backward_rows")
+    return int(rows.value)
 
 
 def rlloss_selftest_bounded_wait(workspace, limit_ns: int, stream=None) -> int:

@@ -183,6 +183,59 @@ def test_gspo_per_token_advantages_full_path(R):
         assert rel_l2(gx, ox) <= 5e-3 and cosine(gx, ox) >= 0.9999, name
 
 
+# ------------------------------------------------------------------ backward row compaction
+def _grads_close(a, b):
+    for k in ("dX", "dW", "db"):
+        if a.get(k) is None:
+            continue
+        x, y = a[k], b[k]
+        tol = 1e-5 * float(y.abs().max()) + 1e-12
+        assert torch.allclose(x, y, rtol=1e-4, atol=tol), k
+
+
+@pytest.mark.parametrize("spec", [MID[0], MID[1], MID[3], MID[4]], ids=["gmpo", "bias_k3kl", "gspo", "fp32_bias_odd"])
+def test_compacted_backward_matches_dense(R, spec):
+    """By default rows with c_n = 0 are dropped before the backward; the dense
+    backward over every row gives the same gradients up to fp32 summation
+    order, the same forward and loss bits, and both pass the oracle."""
+    case = Case(spec)
+    a, res, _ = _full_check(R, case)
+    b, _, _ = _full_check(R, case, flags=R.FLAG_DENSE_BACKWARD)
+    keep = res.c != 0
+    assert 0 < keep.sum() < spec.N, "the workload must both keep and drop rows"
+    assert R.rlloss_get_backward_rows(a["workspace"]) == int(keep.sum())
+    assert R.rlloss_get_backward_rows(b["workspace"]) == spec.N
+    for k in ("loss", "metrics", "logp", "entropy"):
+        assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), k
+    assert torch.count_nonzero(a["dX"][torch.from_numpy(~keep).cuda()]) == 0
+    _grads_close(a, b)
+
+
+def test_backward_without_gradient_rows(R):
+    """All advantages 0 and no KL: every c_n is 0, nothing is kept, and dX,
+    dW, db come out exactly zero, in one chunk and in several."""
+    spec = MID[1].with_(beta=0.0)
+    case = Case(spec)
+    case.inp.adv.zero_()
+    for chunk in (0, 128):
+        out = case.run_gpu(R, chunk_rows=chunk)
+        assert out["status"] == 0, hex(out["status"])
+        assert out["loss"].item() == 0.0
+        for k in ("dX", "dW", "db"):
+            assert torch.count_nonzero(out[k]) == 0, (chunk, k)
+
+
+def test_compaction_with_empty_later_chunks(R):
+    """Most rows are prompt: the kept rows fit in the first 256-row chunk and
+    the later chunks have none.  Matches the dense backward and the oracle."""
+    spec = Workload("mostly_prompt", B=2, T=640, H=128, V=900, dtype="bf16", prompt_len=560, seed=109)
+    case = Case(spec)
+    a, res, _ = _full_check(R, case, chunk_rows=256)
+    assert 0 < (res.c != 0).sum() <= 160
+    b, _, _ = _full_check(R, case, chunk_rows=256, flags=R.FLAG_DENSE_BACKWARD)
+    _grads_close(a, b)
+
+
 # ------------------------------------------------------------------ loss stage only
 def _loss_gpu(R, cfg, logp, old, adv, mask, entropy=None, ref=None):
     c = lambda x: None if x is None else torch.as_tensor(x).cuda()
