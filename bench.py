@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunk-rows", type=int, default=0,
                     help="backward chunk (rows of G kept in HBM); 0 = the library's default")
+    ap.add_argument("--dense-backward", action="store_true",
+                    help="run the backward over every row (RLLOSS_FLAG_DENSE_BACKWARD), for comparison")
     ap.add_argument("--no-naive-memory", action="store_true",
                     help="skip the full-logits torch path run for the memory comparison")
     return ap.parse_args()
@@ -185,11 +187,11 @@ def make_workload(dev):
     return spec, inp, old, ref
 
 
-def cfg_for(R, spec, chunk_rows=0):
+def cfg_for(R, spec, chunk_rows=0, flags=0):
     return R.make_cfg(spec.B, spec.T, spec.H, spec.V, dtype=R.BF16 if spec.dtype == "bf16" else R.FP32,
                       loss_type=spec.loss_type, eps_low=spec.eps_low, eps_high=spec.eps_high, beta=spec.beta,
                       temperature=spec.temperature, top_entropy_quantile=spec.top_entropy_quantile,
-                      has_bias=spec.has_bias, chunk_rows=chunk_rows)
+                      has_bias=spec.has_bias, chunk_rows=chunk_rows, flags=flags)
 
 
 def naive_peak_extra_bytes(spec, inp, old, dev):
@@ -303,7 +305,7 @@ def run_ours(args):
     from lm_head_log_tma_gb300 import rlloss as R
 
     spec, inp, old, ref = make_workload(dev)
-    cfg = cfg_for(R, spec, args.chunk_rows)
+    cfg = cfg_for(R, spec, args.chunk_rows, R.FLAG_DENSE_BACKWARD if args.dense_backward else 0)
     N, H, V = spec.N, spec.H, spec.V
     ws_bytes = R.rlloss_workspace_bytes(cfg)
     naive_bytes = None if args.no_naive_memory else naive_peak_extra_bytes(spec, inp, old, dev)
@@ -453,7 +455,8 @@ def run_ours(args):
             "memory": {"library_workspace_bytes": ws_bytes, "allocated_during_call_bytes": call_alloc,
                        "naive_full_logits_peak_extra_bytes": naive_bytes,
                        "naive_fits": naive_bytes is not None,
-                       "chunk_rows": args.chunk_rows or "default"}}
+                       "chunk_rows": args.chunk_rows or "default",
+                       "backward": "dense" if args.dense_backward else "rows with c_n != 0"}}
 
     if rank == 0 and not args.no_cpu_baseline:
         rate, secs, threads = oracle_sample_rate(spec, inp, old, ref, CPU_BASELINE_TOKENS)
