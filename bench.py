@@ -42,6 +42,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunk-rows", type=int, default=0,
                     help="backward chunk (rows of G kept in HBM); 0 = the library's default")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
+                    help="index into the workload list (default: the B=1 T=4096 Qwen-0.5B LM-head shape)")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="one JSON line per workload (0-4) with the oracle timed on config 0 and on a "
+                         "1-sequence slice of the others; not the single-line default")
     ap.add_argument("--dense-backward", action="store_true",
                     help="run the backward over every row (RLLOSS_FLAG_DENSE_BACKWARD), for comparison")
     ap.add_argument("--no-naive-memory", action="store_true",
@@ -163,13 +168,14 @@ def whole_job_rate(units_per_rank: int, world: int, steps: int, seconds: float) 
     return units_per_rank * world * steps / seconds
 
 
-def make_workload(dev):
-    """Seeded inputs on the device; old_logp = policy logp + N(0, 0.3^2) where
-    the policy logp comes from a plain chunked full-logits pass (cuBLAS bf16
-    matmul, fp32 log-softmax) used only to build this input."""
+def make_workload(dev, index=WORKLOAD_INDEX):
+    """Seeded inputs on the device; the sampler (and reference) log-probs are
+    the policy's plus noise, where the policy logp comes from a plain chunked
+    full-logits pass (cuBLAS matmul, fp32 log-softmax) used only to build
+    this input."""
     import torch
     from lm_head_log_tma_gb300.workloads import WORKLOADS, make_inputs
-    spec = WORKLOADS[WORKLOAD_INDEX]
+    spec = WORKLOADS[index]
     inp = make_inputs(spec, device=dev)
     N = spec.N
     pol = torch.empty(N, dtype=torch.float32, device=dev)
@@ -194,14 +200,22 @@ def cfg_for(R, spec, chunk_rows=0, flags=0):
                       has_bias=spec.has_bias, chunk_rows=chunk_rows, flags=flags)
 
 
+NAIVE_BYTES_PER_LOGIT = 24.5   # measured peak of the path below at B=1, T=4096
+
+
 def naive_peak_extra_bytes(spec, inp, old, dev):
     """Peak device memory above the inputs of a plain full-logits autograd
     path over the same batch (fp32 logits, log-softmax, target gather,
     entropy, the GMPO sequence term, backward to X and W) -- the comparison
-    point for the fused path's workspace.  None if it does not fit."""
+    point for the fused path's workspace.  Returns (bytes or None, note):
+    not run when its estimate exceeds 70% of the free device memory."""
     import torch
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
+    free, _ = torch.cuda.mem_get_info(dev)
+    est = NAIVE_BYTES_PER_LOGIT * spec.N * spec.V
+    if est > 0.7 * free:
+        return None, f"not run: needs about {est / 2**30:.0f} GiB, {free / 2**30:.0f} GiB free"
     torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
     try:
@@ -223,18 +237,30 @@ def naive_peak_extra_bytes(spec, inp, old, dev):
         torch.cuda.synchronize(dev)
         peak = torch.cuda.max_memory_allocated(dev) - base
         del X, W, z, lp, logp, ent, lr, clr, r, loss
+        note = "measured"
     except torch.OutOfMemoryError:
-        peak = None
+        peak, note = None, "out of memory"
     torch.cuda.empty_cache()
-    return peak
+    return peak, note
 
 
 def oracle_sample_rate(spec, inp, old, ref, tokens):
-    """Oracle fwd+bwd over the last ``tokens`` rows of the batch taken as one
-    sequence.  Returns (tokens/s, seconds, threads)."""
+    """Oracle fwd+bwd over the last ``tokens`` rows of the batch (within the
+    last sequence) taken as one sequence, or over the whole batch when
+    ``tokens`` is N.  Returns (tokens/s, seconds, threads)."""
     import numpy as np
     import oracle as O
     n = spec.N
+    if tokens == n:
+        prob = O.Problem(spec.B, spec.T, spec.loss_type, spec.eps_low, spec.eps_high, spec.beta, spec.temperature,
+                         spec.top_entropy_quantile)
+        threads = os.cpu_count() or 1
+        c = lambda x: None if x is None else x.cpu()
+        t = time.perf_counter()
+        O.fwd_bwd(prob, c(inp.X), c(inp.W), c(inp.b), c(inp.targets), c(old), c(ref), c(inp.adv), c(inp.mask),
+                  threads=threads)
+        dt = time.perf_counter() - t
+        return tokens / dt, dt, threads
     r0 = n - tokens
     X = inp.X[r0:].cpu()
     W = inp.W.cpu()
@@ -243,7 +269,7 @@ def oracle_sample_rate(spec, inp, old, ref, tokens):
     oldc = old[r0:].cpu()
     refc = None if ref is None else ref[r0:].cpu()
     mask = inp.mask[r0:].cpu()
-    adv = inp.adv[:1].cpu()
+    adv = inp.adv[-1:].cpu()
     prob = O.Problem(1, tokens, spec.loss_type, spec.eps_low, spec.eps_high, spec.beta, spec.temperature,
                      spec.top_entropy_quantile)
     threads = os.cpu_count() or 1
@@ -302,13 +328,29 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    indices = range(5) if args.all_configs else [args.workload]
+    for k in indices:
+        line = measure(args, k, dev, world, rank, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure(args, index, dev, world, rank, local):
+    """One bench line for workload ``index``."""
+    import torch
+    import torch.distributed as dist
     from lm_head_log_tma_gb300 import rlloss as R
 
-    spec, inp, old, ref = make_workload(dev)
+    spec, inp, old, ref = make_workload(dev, index)
     cfg = cfg_for(R, spec, args.chunk_rows, R.FLAG_DENSE_BACKWARD if args.dense_backward else 0)
     N, H, V = spec.N, spec.H, spec.V
     ws_bytes = R.rlloss_workspace_bytes(cfg)
-    naive_bytes = None if args.no_naive_memory else naive_peak_extra_bytes(spec, inp, old, dev)
+    naive_bytes, naive_note = (None, "skipped") if args.no_naive_memory else naive_peak_extra_bytes(
+        spec, inp, old, dev)
     ws = R.alloc_workspace(ws_bytes, dev)
     outs = None
 
@@ -437,9 +479,14 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": spec.name, "B": spec.B, "T": spec.T, "H": H, "V": V, "loss": "gmpo",
+            "config": {"workload": spec.name, "B": spec.B, "T": spec.T, "H": H, "V": V,
+                       "loss": "gmpo" if spec.loss_type == R.GMPO else "gspo_token", "dtype_in": spec.dtype,
                        "eps_low": spec.eps_low, "eps_high": spec.eps_high, "beta": spec.beta,
-                       "l2": "inputs larger than L2 (W is 272 MB, dW 545 MB)",
+                       "temperature": spec.temperature, "top_entropy_quantile": spec.top_entropy_quantile,
+                       "bias": spec.has_bias,
+                       "l2": (f"inputs larger than L2 (W is {inp.W.numel() * inp.W.element_size() / 1e6:.0f} MB, "
+                              f"dW {V * H * 4 / 1e6:.0f} MB)") if V * H * 2 > 129e6 else
+                             "inputs fit in L2 (not flushed between steps)",
                        "parallelism": "replicas" if world > 1 else "single"},
             "tc_peak_frac_6nhv": step_tflops / peak,
             "tc_tflops_6nhv": step_tflops,
@@ -454,20 +501,20 @@ def run_ours(args):
             "gpu_launches": launches,
             "memory": {"library_workspace_bytes": ws_bytes, "allocated_during_call_bytes": call_alloc,
                        "naive_full_logits_peak_extra_bytes": naive_bytes,
-                       "naive_fits": naive_bytes is not None,
+                       "naive_fits": naive_bytes is not None, "naive_note": naive_note,
                        "chunk_rows": args.chunk_rows or "default",
                        "backward": "dense" if args.dense_backward else "rows with c_n != 0"}}
 
     if rank == 0 and not args.no_cpu_baseline:
-        rate, secs, threads = oracle_sample_rate(spec, inp, old, ref, CPU_BASELINE_TOKENS)
+        if args.all_configs:   # config 0 whole, the others one sequence
+            tokens = N if index == 0 else spec.T
+            what = "the whole batch" if index == 0 else f"the last sequence ({spec.T} tokens)"
+        else:
+            tokens, what = CPU_BASELINE_TOKENS, f"last {CPU_BASELINE_TOKENS} tokens of the batch as one sequence"
+        rate, secs, threads = oracle_sample_rate(spec, inp, old, ref, tokens)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                "sample": f"last {CPU_BASELINE_TOKENS} tokens of the batch as one sequence, full "
-                                          f"H and V, fp64 numpy fwd+bwd ({secs:.1f} s)"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
-    return 0
+                                "sample": f"{what}, full H and V, fp64 numpy fwd+bwd ({secs:.1f} s)"}
+    return line
 
 
 def main():
