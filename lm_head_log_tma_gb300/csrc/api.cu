@@ -765,6 +765,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     if (!tmap_bf16_box(&dp.tmG, dl, p.fp32 ? 2ll * p.Vp : p.V, nc, p.ld_dl, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
       return RLLOSS_ECUDA;
     dp.lo_off = lo_off;
+    dp.dbp = p.bias ? reinterpret_cast<float*>(ws + p.o_dbpart) : nullptr;
     dp.status = status;
     dp.limit_ns = kWaitLimitNs;
     {
@@ -828,9 +829,8 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     }
     if (p.bias) {
       Phase ph(st, 5);
-      RL_TRY(launch_db(dl, p.ld_dl, lo_off, nc, rows_total, n0, p.V, reinterpret_cast<float*>(ws + p.o_dbpart), db,
-                       ch > 0, st));
-      ph.launched(2);
+      RL_TRY(launch_db_reduce(reinterpret_cast<float*>(ws + p.o_dbpart), rows_total, n0, nc, p.V, db, ch > 0, st));
+      ph.launched();
     }
   }
   return RLLOSS_OK;

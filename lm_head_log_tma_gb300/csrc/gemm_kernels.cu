@@ -184,6 +184,28 @@ __global__ void fwd_merge_kernel(MergeParams p) {
 }
 
 // =============================================================== dlogits
+// Column sums of a 32 x 32 block held one row per lane (v[j] = column j):
+// a butterfly in which each step halves the columns a lane keeps and adds the
+// partner's half, so lane l ends with column l's sum in v[0] (fixed order).
+template <int OFF>
+__device__ __forceinline__ void colsum_step(float (&v)[32], int lane) {
+  const bool upper = (lane & OFF) != 0;
+#pragma unroll
+  for (int i = 0; i < OFF; ++i) {
+    const float send = upper ? v[i] : v[i + OFF];
+    const float keep = upper ? v[i + OFF] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+  }
+}
+__device__ __forceinline__ float warp_column_sum(float (&v)[32], int lane) {
+  colsum_step<16>(v, lane);
+  colsum_step<8>(v, lane);
+  colsum_step<4>(v, lane);
+  colsum_step<2>(v, lane);
+  colsum_step<1>(v, lane);
+  return v[0];
+}
+
 template <int CL>
 struct DlPolicy {
   static constexpr int kCluster = CL;
@@ -328,6 +350,12 @@ struct DlPolicy {
           lo[i] = pack_bf16x2(v[2 * i] - __low2float(h2), v[2 * i + 1] - __high2float(h2));
         }
         store_box(p, e, wbuf, lane, lo, c0 + p.lo_off, y0);
+      }
+      if (p.dbp) {
+        // db partial: this warp's 32 rows summed per column (fp32 G, before
+        // the bf16 rounding), one row of the [rows/32][V] partial buffer
+        const float cs = warp_column_sum(v, lane);
+        if (c0 + lane < p.V) p.dbp[size_t(r0 >> 5) * p.V + c0 + lane] = cs;
       }
     }
   }
@@ -537,37 +565,14 @@ __global__ void split3_kernel(const float* src, long long rows, int cols, int Cp
   }
 }
 
-// Column sums of G over blocks of kDbRows chunk rows: part[blk][v] (hi + lo
-// terms in fp32 mode).  No atomics, so db is reproducible bit for bit.
-constexpr int kDbRows = 256;
-__global__ void db_part_kernel(const __nv_bfloat16* dl, int ld, int lo_off, int Ncap, const int* rows_total, int n0,
-                               int V, float* part) {
-  const int v = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
-  if (v >= V) return;
-  const int Nc = min(max(*rows_total - n0, 0), Ncap);
-  const int r0 = blockIdx.y * kDbRows;
-  const int r1 = min(Nc, r0 + kDbRows);
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll 4
-  for (int r = r0; r < r1; ++r) {
-    const __nv_bfloat16* p = dl + size_t(r) * ld + v;
-    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(p);
-    a0 += __low2float(x);
-    a1 += __high2float(x);
-    if (lo_off) {
-      const __nv_bfloat162 l = *reinterpret_cast<const __nv_bfloat162*>(p + lo_off);
-      a0 += __low2float(l);
-      a1 += __high2float(l);
-    }
-  }
-  float* o = part + size_t(blockIdx.y) * V + v;
-  o[0] = a0;
-  if (v + 1 < V) o[1] = a1;
-}
-
-__global__ void db_reduce_kernel(const float* part, int nblk, int V, float* db, int accumulate) {
+// db (+)= the sum, in row-block order, of the recompute's per-32-row column
+// partials over the chunk's rows.
+__global__ void db_reduce_kernel(const float* part, const int* rows_total, int n0, int Nc, int V, float* db,
+                                 int accumulate) {
   const int v = blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= V) return;
+  const int nc = min(max(*rows_total - n0, 0), Nc);
+  const int nblk = (nc + 31) / 32;
   float a = 0.f;
   for (int k = 0; k < nblk; ++k) a += part[size_t(k) * V + v];
   db[v] = accumulate ? db[v] + a : a;
@@ -693,13 +698,12 @@ cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __
   split3_kernel<<<blocks, 256, 0, st>>>(src, rows, cols, Cp, out);
   return cudaGetLastError();
 }
-int db_part_rows(int Nc) { return (Nc + kDbRows - 1) / kDbRows; }
-cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, const int* rows_total, int n0, int V,
-                      float* part, float* db, int accumulate, cudaStream_t st) {
-  const int nblk = db_part_rows(Nc);
-  dim3 grid((V / 2 + 1 + 255) / 256, nblk);
-  db_part_kernel<<<grid, 256, 0, st>>>(dl, ld, lo_off, Nc, rows_total, n0, V, part);
-  db_reduce_kernel<<<(V + 255) / 256, 256, 0, st>>>(part, nblk, V, db, accumulate);
+// Rows of the partial buffer: the recompute's tiles cover the chunk in whole
+// 256-row tiles, and each 32 rows of a tile write one partial row.
+int db_part_rows(int Nc) { return (Nc + 255) / 256 * 8; }
+cudaError_t launch_db_reduce(const float* part, const int* rows_total, int n0, int Nc, int V, float* db, int accumulate,
+                             cudaStream_t st) {
+  db_reduce_kernel<<<(V + 255) / 256, 256, 0, st>>>(part, rows_total, n0, Nc, V, db, accumulate);
   return cudaGetLastError();
 }
 cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st) {

@@ -52,6 +52,7 @@ struct DlParams {
   __nv_bfloat16* dl;          // [Nc, ld] chunk buffer (hi terms)
   int ld;                     // row stride in elements
   int lo_off;                 // element offset of the lo terms (fp32 mode), else 0
+  float* dbp;                 // bias: [rows/32][V] column sums of G per 32 chunk rows, else null
   int* status;
   unsigned long long limit_ns;
 };
@@ -152,12 +153,11 @@ cudaError_t launch_set_total(int* total, int N, cudaStream_t st);
 cudaError_t launch_scatter_rows(const float* src, const int* idx, const int* total, int n0, int nc_max, int H,
                                 float* dst, cudaStream_t st);
 
-// db (+)= column sums of the chunk's G rows (clamp(*rows_total - n0, 0, Nc) of them);
-// part is scratch of db_part_rows(Nc) * V floats.
+// db (+)= the recompute's per-32-row column partials of the chunk (DlParams::dbp,
+// db_part_rows(Nc) rows of V floats), summed over clamp(*rows_total - n0, 0, Nc) rows.
 int db_part_rows(int Nc);
-cudaError_t launch_db(const __nv_bfloat16* dl, int ld, int lo_off, int Nc, const int* rows_total, int n0, int V,
-                      float* part, float* db,
-                      int accumulate, cudaStream_t st);
+cudaError_t launch_db_reduce(const float* part, const int* rows_total, int n0, int Nc, int V, float* db, int accumulate,
+                             cudaStream_t st);
 cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
 
 // entropy quantile (K3): a 256-byte state block followed by 4 passes x 2 x 256
