@@ -183,6 +183,44 @@ def test_gspo_per_token_advantages_full_path(R):
         assert rel_l2(gx, ox) <= 5e-3 and cosine(gx, ox) >= 0.9999, name
 
 
+@pytest.mark.parametrize("q", [0.5, 0.8])
+def test_entropy_mask_other_quantiles_full_path(R, q):
+    """The batch-global mask at q = 0.5 and 0.8 through the fused path: it
+    drops some but not all active tokens, and everything matches the oracle."""
+    case = Case(MID[2].with_(top_entropy_quantile=q))
+    out, _, _ = _full_check(R, case)
+    m = out["metrics"].cpu().numpy()
+    assert 0 < m[5] < m[3]
+
+
+@pytest.mark.parametrize("spec", [MID[0], MID[3]], ids=["gmpo", "gspo"])
+def test_extreme_log_ratios_full_path(R, spec):
+    """Sampler log-probs 30 nats away from the policy's (alternating sign by
+    sequence): GMPO's log-space clip keeps every ratio finite, GSPO's
+    sequence ratios are e^(+-30)-sized and clipped; loss and gradients stay
+    finite and match the oracle."""
+    case = Case(spec)
+    sign = torch.tensor([(-1.0) ** i for i in range(spec.B)]).repeat_interleave(spec.T)
+    case.old = (case.old.double() + 30.0 * sign).float()
+    case.old64 = case.old.double().numpy()
+    out, _, _ = _full_check(R, case)
+    assert np.isfinite(out["loss"].item())
+    for k in ("dX", "dW"):
+        assert torch.isfinite(out[k]).all(), k
+
+
+def test_nonfinite_logp_sets_status(R):
+    """A NaN log-prob on an active token makes the loss NaN and sets the
+    non-finite bit in the device status word (no trap)."""
+    n = 64
+    logp = np.full(n, -2.0, np.float32)
+    logp[5] = np.nan
+    g = _loss_gpu(R, R.make_cfg(1, n), logp, np.full(n, -2.0, np.float32), np.ones(1, np.float32),
+                  np.ones(n, np.uint8))
+    assert g["status"] & R.DEV_ENONFINITE
+    assert np.isnan(g["loss"].item())
+
+
 # ------------------------------------------------------------------ backward row compaction
 def _grads_close(a, b):
     for k in ("dX", "dW", "db"):
