@@ -69,6 +69,8 @@ extern "C" {
 /* cfg.dtype */
 #define RLLOSS_BF16 0
 #define RLLOSS_FP32 1
+#define RLLOSS_FP8_E4M3 2   /* forward-only scoring (rlloss_forward_e4m3): X, W as e4m3 bytes with
+                               per-row fp32 scales; the pages name no fp8 path, this is ours */
 /* cfg.loss_type */
 #define RLLOSS_GMPO 0
 #define RLLOSS_GSPO_TOKEN 1
@@ -112,7 +114,8 @@ extern "C" {
 
 typedef struct {
   int32_t B, T, H, V;       /* sequences, tokens per sequence, hidden size, vocabulary */
-  int32_t dtype;            /* RLLOSS_BF16 or RLLOSS_FP32 for X, W, b */
+  int32_t dtype;            /* RLLOSS_BF16 or RLLOSS_FP32 for X, W, b; RLLOSS_FP8_E4M3 for
+                               rlloss_forward_e4m3 only */
   int32_t loss_type;        /* RLLOSS_GMPO or RLLOSS_GSPO_TOKEN */
   int32_t is_level;         /* RLLOSS_IS_TOKEN or RLLOSS_IS_SEQUENCE */
   float eps_low, eps_high;  /* GMPO: log-space bounds [-eps_low, +eps_high] ("Add GMPO ...",
@@ -165,6 +168,22 @@ size_t rlloss_forward_workspace_bytes(const rlloss_cfg* cfg);
 int rlloss_forward(const rlloss_cfg* cfg, const void* X, const void* W, const void* b,
                    const int64_t* targets, float* out_logp, float* out_entropy, float* out_lse,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* rlloss_forward with e4m3 operands (cfg.dtype = RLLOSS_FP8_E4M3): the
+ * tensor cores take X and W as 8-bit floats (OCP e4m3, finite-only) and the
+ * logit of token n and vocabulary row v is
+ *     (sum_h X8[n][h] * W8[v][h]) * x_scale[n] * w_scale[v] (+ b[v]),
+ * then scaled by 1/temperature as in rlloss_forward.  X8 [N,H] and W8 [V,H]
+ * are row-major bytes (H a multiple of 16); x_scale [N], w_scale [V] and b
+ * [V] (NULL when !has_bias) are fp32.  The products and their fp32 sums are
+ * exact up to fp32 rounding, so the results equal those of the dequantized
+ * inputs X8*x_scale, W8*w_scale to fp32 accuracy; how the caller quantizes
+ * is its own choice.  Workspace: rlloss_forward_workspace_bytes(cfg).
+ * RLLOSS_FLAG_SINGLE_CTA_TILES is not supported here (RLLOSS_EUNSUPPORTED). */
+int rlloss_forward_e4m3(const rlloss_cfg* cfg, const void* X8, const float* x_scale, const void* W8,
+                        const float* w_scale, const float* b, const int64_t* targets, float* out_logp,
+                        float* out_entropy, float* out_lse, void* workspace, size_t workspace_bytes,
+                        void* stream);
 
 /* The loss stage alone, from given per-token log-probs (no LM head): entropy
  * mask (if q < 1), loss, metrics and dL/dlogp.

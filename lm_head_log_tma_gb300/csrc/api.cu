@@ -83,11 +83,15 @@ int validate_head(const rlloss_cfg* c) {
                    RLLOSS_FLAG_DENSE_BACKWARD))
     return RLLOSS_EINVAL;
   if (c->H < 1 || c->V < 1) return RLLOSS_EINVAL;
-  if (c->dtype != RLLOSS_BF16 && c->dtype != RLLOSS_FP32) return RLLOSS_EINVAL;
+  if (c->dtype != RLLOSS_BF16 && c->dtype != RLLOSS_FP32 && c->dtype != RLLOSS_FP8_E4M3) return RLLOSS_EINVAL;
   if (!(c->temperature > 0.f) || !finite(c->temperature)) return RLLOSS_EINVAL;
   if (c->has_bias != 0 && c->has_bias != 1) return RLLOSS_EINVAL;
   if (c->chunk_rows < 0) return RLLOSS_EINVAL;
   if (c->dtype == RLLOSS_BF16 && (c->H % 8) != 0) return RLLOSS_EUNSUPPORTED;  // TMA row stride: 16 bytes
+  if (c->dtype == RLLOSS_FP8_E4M3) {
+    if ((c->H % 16) != 0) return RLLOSS_EUNSUPPORTED;                          // TMA row stride: 16 bytes
+    if (c->flags & RLLOSS_FLAG_SINGLE_CTA_TILES) return RLLOSS_EUNSUPPORTED;
+  }
   if ((c->H % 4) != 0) return RLLOSS_EUNSUPPORTED;                            // fp32 dX / dW rows: 16 bytes
   if (c->H > 65536 || c->V > (1 << 30)) return RLLOSS_EUNSUPPORTED;
   return RLLOSS_OK;
@@ -96,7 +100,10 @@ int validate_head(const rlloss_cfg* c) {
 int validate_full(const rlloss_cfg* c) {
   int e = validate_common(c);
   if (e) return e;
-  return validate_head(c);
+  e = validate_head(c);
+  if (e) return e;
+  if (c->dtype == RLLOSS_FP8_E4M3) return RLLOSS_EUNSUPPORTED;   // e4m3: forward-only scoring
+  return RLLOSS_OK;
 }
 
 bool entropy_path(const rlloss_cfg* c) {
@@ -107,7 +114,7 @@ struct Plan {
   int B, T, N, H, V, sms;
   int pair, rows_tile;      // CTAs per LM-head tile (1 or 2) and rows per tile
   int fwd_clusters, h_pairs;  // resident clusters of the forward and dX/dW kernels
-  bool fp32, bias, ent;
+  bool fp32, f8, bias, ent;
   bool fused_loss;          // row merge and loss stage in one launch (no entropy mask)
   bool compact;             // backward over the rows with c_n != 0 only
   int R, Vt, P, Hp, Vp;
@@ -118,7 +125,7 @@ struct Plan {
   int slices;
   size_t o_tickets, o_part;
   size_t o_status, o_partial, o_lse2, o_logp64, o_ent, o_coef, o_emask, o_k3, o_seq, o_bias2, o_dl, o_x3, o_w3,
-      o_dbpart, o_blk, o_cidx, o_xc, o_coefc, o_lse2c, o_tgtc, o_dxc, total;
+      o_dbpart, o_ws2, o_blk, o_cidx, o_xc, o_coefc, o_lse2c, o_tgtc, o_dxc, total;
   int Ncap;                 // rows of the compacted arrays (N rounded up to 256)
 };
 
@@ -166,6 +173,7 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.H = c->H;
     p.V = c->V;
     p.fp32 = c->dtype == RLLOSS_FP32;
+    p.f8 = c->dtype == RLLOSS_FP8_E4M3;
     p.bias = c->has_bias != 0;
     p.pair = (c->flags & RLLOSS_FLAG_SINGLE_CTA_TILES) ? 1 : 2;
     p.rows_tile = 128 * p.pair;
@@ -179,6 +187,10 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
       p.nseg_fwd = 6;
       p.kb_fwd = p.Hp / 64;
       p.Kx = 3 * p.Hp;
+    } else if (p.f8) {
+      p.nseg_fwd = 1;
+      p.kb_fwd = int(cdiv(p.H, 128));   // 128 e4m3 elements = 128 bytes per k-block row
+      p.Kx = p.H;
     } else {
       p.nseg_fwd = 1;
       p.kb_fwd = int(cdiv(p.H, 64));
@@ -189,6 +201,7 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.o_logp64 = take(size_t(p.N) * 8);
     p.o_ent = take(size_t(p.N) * 4);
     p.o_bias2 = take(p.bias ? size_t(p.Vt) * 256 * 4 : 0);
+    p.o_ws2 = take(p.f8 ? size_t(p.Vt) * 256 * 4 : 0);
     p.o_x3 = take(p.fp32 ? size_t(p.N) * 3 * p.Hp * 2 : 0);
     p.o_w3 = take(p.fp32 ? size_t(p.V) * 3 * p.Hp * 2 : 0);
   }
@@ -318,6 +331,20 @@ bool tmap_bf16(CUtensorMap* m, const void* base, long long inner, long long oute
   return tmap_bf16_box(m, base, inner, outer, row_elems, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// 2-D byte (e4m3) operand map: rows of `inner` bytes, box 128 bytes x box_outer,
+// 128-byte swizzle (the same shared-memory layout as a 64-wide bf16 box).
+bool tmap_u8(CUtensorMap* m, const void* base, long long inner, long long outer, int box_outer) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+  const cuuint64_t strides[1] = {cuuint64_t(inner)};
+  const cuuint32_t box[2] = {128u, cuuint32_t(box_outer)};
+  const cuuint32_t es[2] = {1u, 1u};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 output map for TMA stores / reduce-adds: box 32 x 32, 128-byte swizzle.
 bool tmap_f32_out(CUtensorMap* m, const float* base, long long inner, long long outer) {
   EncodeTiledFn f = encode_fn();
@@ -382,6 +409,8 @@ struct Head {
   const void* Xop = nullptr;
   const void* Wop = nullptr;
   const float* bias2 = nullptr;
+  const float* x_scale = nullptr;   // e4m3 operands: per-row scales (set by the caller of run_head)
+  const float* w_scale = nullptr;
   int seg_a[kMaxSeg] = {0, 0, 0, 0, 0, 0};
   int seg_b[kMaxSeg] = {0, 0, 0, 0, 0, 0};
   FwdParams fp{};
@@ -419,9 +448,16 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
   if (p.bias) {
     float* b2 = reinterpret_cast<float*>(ws + p.o_bias2);
     Phase ph(st, 5);
-    RL_TRY(launch_bias2(b, p.fp32 ? 1 : 0, p.V, p.Vt * 256, scale2, b2, st));
+    RL_TRY(launch_bias2(b, (p.fp32 || p.f8) ? 1 : 0, p.V, p.Vt * 256, scale2, b2, st));
     ph.launched();
     h.bias2 = b2;
+  }
+  float* ws2 = nullptr;
+  if (p.f8) {   // w_scale * log2(e) / tau, zero padded (same layout as the scaled bias)
+    ws2 = reinterpret_cast<float*>(ws + p.o_ws2);
+    Phase ph(st, 5);
+    RL_TRY(launch_bias2(h.w_scale, 1, p.V, p.Vt * 256, scale2, ws2, st));
+    ph.launched();
   }
   // K-segments of the forward / recompute GEMM: products of the split terms.
   if (p.fp32) {
@@ -434,8 +470,15 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
 
   // ---- forward: tensor-core logits + streamed row state
   FwdParams& fp = h.fp;
-  if (!tmap_bf16(&fp.tmA, h.Xop, p.Kx, p.N, p.Kx, 128)) return RLLOSS_ECUDA;
-  if (!tmap_bf16(&fp.tmB, h.Wop, p.Kx, p.V, p.Kx, p.pair == 1 ? 256 : 128)) return RLLOSS_ECUDA;
+  if (p.f8) {
+    if (!tmap_u8(&fp.tmA, h.Xop, p.Kx, p.N, 128)) return RLLOSS_ECUDA;
+    if (!tmap_u8(&fp.tmB, h.Wop, p.Kx, p.V, 128)) return RLLOSS_ECUDA;
+    fp.xs = h.x_scale;
+    fp.ws2 = ws2;
+  } else {
+    if (!tmap_bf16(&fp.tmA, h.Xop, p.Kx, p.N, p.Kx, 128)) return RLLOSS_ECUDA;
+    if (!tmap_bf16(&fp.tmB, h.Wop, p.Kx, p.V, p.Kx, p.pair == 1 ? 256 : 128)) return RLLOSS_ECUDA;
+  }
   fp.nseg = p.nseg_fwd;
   fp.kb_per_seg = p.kb_fwd;
   std::memcpy(fp.seg_a, h.seg_a, sizeof(h.seg_a));
@@ -572,6 +615,7 @@ int rlloss_forward(const rlloss_cfg* cfg, const void* X, const void* W, const vo
                    void* stream) {
   int e = validate_head(cfg);
   if (e) return e;
+  if (cfg->dtype == RLLOSS_FP8_E4M3) return RLLOSS_EINVAL;   // needs the scales: rlloss_forward_e4m3
   if (!X || !W || !targets || !workspace) return RLLOSS_EINVAL;
   if (cfg->has_bias && !b) return RLLOSS_EINVAL;
   if (!aligned(X, 16) || !aligned(W, 16)) return RLLOSS_EINVAL;
@@ -583,6 +627,28 @@ int rlloss_forward(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, 256, st));
   Head hd;
   return run_head(cfg, p, X, W, b, targets, out_logp, out_entropy, out_lse, ws, st, hd);
+}
+
+int rlloss_forward_e4m3(const rlloss_cfg* cfg, const void* X8, const float* x_scale, const void* W8,
+                        const float* w_scale, const float* b, const int64_t* targets, float* out_logp,
+                        float* out_entropy, float* out_lse, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  int e = validate_head(cfg);
+  if (e) return e;
+  if (cfg->dtype != RLLOSS_FP8_E4M3) return RLLOSS_EINVAL;
+  if (!X8 || !W8 || !x_scale || !w_scale || !targets || !workspace) return RLLOSS_EINVAL;
+  if (cfg->has_bias && !b) return RLLOSS_EINVAL;
+  if (!aligned(X8, 16) || !aligned(W8, 16)) return RLLOSS_EINVAL;
+  const Plan p = make_plan(cfg, kForwardOnly);
+  if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
+  if (!encode_fn()) return RLLOSS_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, 256, st));
+  Head hd;
+  hd.x_scale = x_scale;
+  hd.w_scale = w_scale;
+  return run_head(cfg, p, X8, W8, b, targets, out_logp, out_entropy, out_lse, ws, st, hd);
 }
 
 int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float* entropy, const float* old_logp,

@@ -21,8 +21,10 @@ namespace rl {
 
 // =============================================================== forward
 // CL = 1: 128-row tiles on one CTA; CL = 2: 256-row tiles over a CTA pair
-// (cta_group::2).
-template <int CL>
+// (cta_group::2).  F8: e4m3 operands (forward-only scoring) with per-row
+// scales of X and W applied in the epilogue; a k-block is then 128 elements
+// (the same 128 bytes per row) and each MMA step covers K = 32.
+template <int CL, bool F8 = false>
 struct FwdPolicy {
   static constexpr int kCluster = CL;
   static constexpr int PAIR = CL >= 2 ? 2 : 1;
@@ -34,12 +36,14 @@ struct FwdPolicy {
   static constexpr int kABytes = 128 * 64 * 2;
   static constexpr int kBBytes = (256 / PAIR) * 64 * 2;   // this CTA's share of the B rows
   static constexpr int kExtraSmem = 0;
-  static constexpr uint32_t kIdesc = idesc_bf16(kRows, 256, 0, 0);
+  static constexpr uint32_t kIdesc = F8 ? idesc_e4m3(kRows, 256) : idesc_bf16(kRows, 256, 0, 0);
+  static constexpr int kKB = F8 ? 128 : 64;           // K elements per k-block (128 bytes per row)
   using Params = FwdParams;
 
   struct EpiState {
     float mref, s_hi, s_lo, w_hi, w_lo, zy;
     int found, y;
+    float xs;     // F8: this row's X scale
   };
 
   __device__ static void cta_setup(const Params&, uint8_t*) {}
@@ -70,7 +74,7 @@ struct FwdPolicy {
 
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int s = kb / p.kb_per_seg;
-    const int kk = (kb - s * p.kb_per_seg) * 64;
+    const int kk = (kb - s * p.kb_per_seg) * kKB;
     if constexpr (CL == 2) {
       tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0 + 128 * int(rank));
       tma_load_2d_pair(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0 + 128 * int(rank));
@@ -87,10 +91,16 @@ struct FwdPolicy {
   static constexpr int kAccBufs = 2;
   __device__ static uint32_t tx_bytes(const Params&, const TileInfo&) { return kABytes + kBBytes; }
   __device__ static void mma(const Params&, uint32_t d, uint32_t sa, int k, const TileInfo& t, uint32_t accum) {
-    if constexpr (PAIR == 2)
+    if constexpr (F8) {
+      if constexpr (PAIR == 2)
+        umma_e4m3_pair(d, adesc(sa, k, t), bdesc(sa, k, t), kIdesc, accum);
+      else
+        umma_e4m3(d, adesc(sa, k, t), bdesc(sa, k, t), kIdesc, accum);
+    } else if constexpr (PAIR == 2) {
       umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, t), kIdesc, accum);
-    else
+    } else {
       umma_bf16(d, adesc(sa, k, t), bdesc(sa, k, t), kIdesc, accum);
+    }
   }
 
   __device__ static void epilogue(const Params& p, EpiState& e, const TileInfo& t, uint32_t taddr, int q, int half,
@@ -102,6 +112,7 @@ struct FwdPolicy {
       e.zy = 0.f;
       e.found = 0;
       e.y = row < p.N ? int(p.targets[row]) : -1;
+      if constexpr (F8) e.xs = row < p.N ? p.xs[row] : 0.f;
     }
     const float sc = p.scale2;
 #pragma unroll 1
@@ -110,7 +121,20 @@ struct FwdPolicy {
       if (c0 >= p.V) break;
       float v[32];
       tmem_ld32(taddr + uint32_t(half * 128 + ch * 32), v);
-      if (p.bias2) {
+      if constexpr (F8) {
+        // logit * log2(e)/tau = acc * xs[row] * (ws[col] * log2(e)/tau) (+ b * log2(e)/tau)
+        const float4* w4 = reinterpret_cast<const float4*>(p.ws2 + c0);
+        const float4* b4 = reinterpret_cast<const float4*>(p.bias2 + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 w = __ldg(w4 + i);
+          const float4 b = p.bias2 ? __ldg(b4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[4 * i + 0] = fmaf(v[4 * i + 0] * e.xs, w.x, b.x);
+          v[4 * i + 1] = fmaf(v[4 * i + 1] * e.xs, w.y, b.y);
+          v[4 * i + 2] = fmaf(v[4 * i + 2] * e.xs, w.z, b.z);
+          v[4 * i + 3] = fmaf(v[4 * i + 3] * e.xs, w.w, b.w);
+        }
+      } else if (p.bias2) {
         const float4* b4 = reinterpret_cast<const float4*>(p.bias2 + c0);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -676,6 +700,7 @@ int gemmH_resident_clusters() {
   return engine_resident<HPolicy>(&e);
 }
 cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, cudaStream_t st) {
+  if (p.xs) return launch_engine<FwdPolicy<2, true>>(p, units, st);   // e4m3 operands: CTA pairs only
   return cluster == 2 ? launch_engine<FwdPolicy<2>>(p, units, st) : launch_engine<FwdPolicy<1>>(p, units, st);
 }
 cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st) {

@@ -11,13 +11,15 @@ namespace rl {
 constexpr int kMaxSeg = 6;
 
 struct FwdParams {
-  CUtensorMap tmA;            // X (or its 3-term bf16 split): inner K, outer rows; box 64 x 128
-  CUtensorMap tmB;            // W (or split): inner K, outer vocab; box 64 x 256
-  int nseg, kb_per_seg;       // K = nseg * kb_per_seg * 64
+  CUtensorMap tmA;            // X (or its 3-term bf16 split, or e4m3): inner K, outer rows; box 128 B x 128
+  CUtensorMap tmB;            // W (or split, or e4m3): inner K, outer vocab; box 128 B x 256 (128 per CTA of a pair)
+  int nseg, kb_per_seg;       // K = nseg * kb_per_seg * (64 bf16 or 128 e4m3 elements)
   int seg_a[kMaxSeg], seg_b[kMaxSeg];  // K offsets of each product term
   int N, V, R, Vt, P;         // rows, vocab, row tiles (128 or 256 rows), vocab tiles (256), vocab segments
   float scale2;               // log2(e) / temperature
   const float* bias2;         // [Vt*256] b * scale2, zero padded; null without bias
+  const float* xs;            // e4m3 operands: [N] per-row X scales, else null
+  const float* ws2;           // e4m3 operands: [Vt*256] per-row W scales * scale2, zero padded
   const int64_t* targets;
   float4* partial;            // [N][2P][2]
   int* status;

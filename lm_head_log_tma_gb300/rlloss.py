@@ -19,7 +19,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "rlloss.h")
 
 OK, EINVAL, EUNSUPPORTED, EWORKSPACE, ECUDA = 0, 1, 2, 3, 4
 DEV_ETIMEOUT, DEV_ENONFINITE, DEV_EBADTARGET, DEV_EEMPTYSEQ = 0x10, 0x20, 0x40, 0x80
-BF16, FP32 = 0, 1
+BF16, FP32, FP8_E4M3 = 0, 1, 2
 GMPO, GSPO_TOKEN = 0, 1
 IS_TOKEN, IS_SEQUENCE = 0, 1
 FLAG_FORCE_ENTROPY_PATH = 0x1
@@ -66,6 +66,8 @@ def _load():
     lib.rlloss_forward_workspace_bytes.restype = c_size_t
     lib.rlloss_forward.argtypes = [cfgp] + [P] * 7 + [P, c_size_t, P]
     lib.rlloss_forward.restype = c_int
+    lib.rlloss_forward_e4m3.argtypes = [cfgp] + [P] * 9 + [P, c_size_t, P]
+    lib.rlloss_forward_e4m3.restype = c_int
     lib.rlloss_loss_from_logp.argtypes = [cfgp] + [P] * 10 + [P, c_size_t, P]
     lib.rlloss_loss_from_logp.restype = c_int
     lib.rlloss_get_device_status.argtypes = [P, ctypes.POINTER(c_int32)]
@@ -136,6 +138,13 @@ def rlloss_forward(cfg, X, W, b, targets, out_logp, out_entropy, out_lse, worksp
     return lib.rlloss_forward(ctypes.byref(cfg), _p(X), _p(W), _p(b), _p(targets), _p(out_logp),
                               _p(out_entropy), _p(out_lse), _p(workspace),
                               c_size_t(0 if workspace is None else workspace.numel()), _stream(stream))
+
+
+def rlloss_forward_e4m3(cfg, X8, x_scale, W8, w_scale, b, targets, out_logp, out_entropy, out_lse, workspace,
+                        stream=None) -> int:
+    return lib.rlloss_forward_e4m3(ctypes.byref(cfg), _p(X8), _p(x_scale), _p(W8), _p(w_scale), _p(b), _p(targets),
+                                   _p(out_logp), _p(out_entropy), _p(out_lse), _p(workspace),
+                                   c_size_t(0 if workspace is None else workspace.numel()), _stream(stream))
 
 
 def rlloss_loss_from_logp(cfg, logp, entropy, old_logp, ref_logp, adv, mask, out_loss, out_metrics,
@@ -231,6 +240,22 @@ def forward(cfg: RllossCfg, X, W, b, targets, workspace=None, stream=None):
     rc = rlloss_forward(cfg, X, W, b, targets, o["logp"], o["entropy"], o["lse"], workspace, stream)
     if rc != OK:
         raise RllossError(rc, "rlloss_forward")
+    o["workspace"] = workspace
+    return o
+
+
+def forward_e4m3(cfg: RllossCfg, X8, x_scale, W8, w_scale, b, targets, workspace=None, stream=None):
+    """Scoring pass with e4m3 operands (torch.float8_e4m3fn or uint8 tensors)
+    and fp32 per-row scales: per-token logp, entropy and lse."""
+    dev = X8.device
+    N = cfg.B * cfg.T
+    o = {k: torch.empty(N, dtype=torch.float32, device=dev) for k in ("logp", "entropy", "lse")}
+    if workspace is None:
+        workspace = alloc_workspace(rlloss_forward_workspace_bytes(cfg), dev)
+    rc = rlloss_forward_e4m3(cfg, X8, x_scale, W8, w_scale, b, targets, o["logp"], o["entropy"], o["lse"],
+                             workspace, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_forward_e4m3")
     o["workspace"] = workspace
     return o
 

@@ -75,6 +75,7 @@ def _call(cfg):
     (dict(loss_type=R.GSPO_TOKEN, top_entropy_quantile=0.5), R.EUNSUPPORTED),
     (dict(flags=R.FLAG_ADV_PER_TOKEN), R.EUNSUPPORTED),  # per-token advantages: GSPO only
     (dict(flags=0x80), R.EINVAL),                       # unknown flag
+    (dict(dtype=R.FP8_E4M3), R.EUNSUPPORTED),            # e4m3 operands: forward-only scoring
     (dict(), R.EINVAL),                                 # valid cfg, null pointers
 ])
 def test_invalid_requests_rejected_synchronously(kw, code):
@@ -112,3 +113,17 @@ def test_loss_from_logp_validation():
     cfg = _cfg(top_entropy_quantile=0.5)
     rc = R.lib.rlloss_loss_from_logp(ctypes.byref(cfg), *([None] * 10), None, 0, None)
     assert rc == R.EINVAL
+
+
+def test_e4m3_scoring_validation():
+    """e4m3 operands: only through rlloss_forward_e4m3, rows of 16-byte
+    multiples, CTA-pair tiles only; the plain forward refuses them."""
+    ok = _cfg(dtype=R.FP8_E4M3, H=896)
+    assert R.rlloss_forward_workspace_bytes(ok) > 0
+    assert R.rlloss_workspace_bytes(ok) == 0                       # no fwd+bwd with e4m3
+    assert R.rlloss_forward_workspace_bytes(_cfg(dtype=R.FP8_E4M3, H=904)) == 0   # 904 % 16 != 0
+    assert R.rlloss_forward_workspace_bytes(_cfg(dtype=R.FP8_E4M3, H=896, flags=R.FLAG_SINGLE_CTA_TILES)) == 0
+    assert R.lib.rlloss_forward(ctypes.byref(ok), *([None] * 7), None, 0, None) == R.EINVAL
+    assert R.lib.rlloss_forward_e4m3(ctypes.byref(ok), *([None] * 9), None, 0, None) == R.EINVAL
+    bf = _cfg()
+    assert R.lib.rlloss_forward_e4m3(ctypes.byref(bf), *([None] * 9), None, 0, None) == R.EINVAL

@@ -157,6 +157,42 @@ def test_forward_only_scoring_matches_oracle_and_full_call(R):
     assert torch.equal(full["logp"], f["logp"]) and torch.equal(full["entropy"], f["entropy"])
 
 
+def _e4m3_rows(x):
+    """Per-row absmax scaling into e4m3 (the caller's quantizer; any would do):
+    returns (e4m3 tensor, fp32 scales, fp64 dequantized values)."""
+    x = x.float()
+    scale = (x.abs().amax(dim=1) / 448.0).clamp(min=1e-30)
+    q = (x / scale[:, None]).to(torch.float8_e4m3fn)
+    return q, scale, q.to(torch.float64) * scale.double()[:, None]
+
+
+@pytest.mark.parametrize("shape", [(2, 150, 192, 1000, True, 0.7), (3, 77, 64, 515, False, 1.0),
+                                   (1, 300, 896, 2000, False, 1.0)], ids=["h192_bias", "h64", "h896"])
+def test_e4m3_scoring_matches_oracle(R, shape):
+    """Forward-only scoring with e4m3 operands and per-row scales: logp,
+    entropy and lse equal the oracle's on the dequantized inputs to the same
+    bar as the bf16 path (the e4m3 products and their fp32 sums are exact up
+    to fp32 rounding)."""
+    B, T, H, V, bias, tau = shape
+    g = torch.Generator().manual_seed(H + V)
+    X = torch.randn(B * T, H, generator=g)
+    W = torch.randn(V, H, generator=g) * 0.02
+    b = torch.randn(V, generator=g) * 0.05 if bias else None
+    y = torch.randint(0, V, (B * T,), generator=g)
+    X8, xs, Xd = _e4m3_rows(X)
+    W8, ws, Wd = _e4m3_rows(W)
+    cfg = R.make_cfg(B, T, H, V, dtype=R.FP8_E4M3, temperature=tau, has_bias=bias)
+    c = lambda t: None if t is None else t.cuda()
+    f = R.forward_e4m3(cfg, c(X8), c(xs), c(W8), c(ws), c(b), c(y))
+    torch.cuda.synchronize()
+    assert R.rlloss_get_device_status(f["workspace"]) == 0
+    lse, logp, ent = O.row_stats(Xd, Wd, None if b is None else b.double(), y, tau)
+    for k, ref in (("logp", logp), ("entropy", ent), ("lse", lse)):
+        gk = f[k].double().cpu().numpy()
+        err = np.abs(gk - ref)
+        assert np.all(err <= 2e-5 + 2e-6 * np.abs(ref)), (k, float(err.max()))
+
+
 def test_gspo_per_token_advantages_full_path(R):
     """GSPO with per-token advantages (nonzero also outside the ratio mask)
     through the fused path, against the oracle."""
