@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true",
                     help="one JSON line per workload (0-4) with the oracle timed on config 0 and on a "
                          "1-sequence slice of the others; not the single-line default")
+    ap.add_argument("--scoring", choices=["bf16", "e4m3"], default=None,
+                    help="time the forward-only scoring entry instead (per-token logp/entropy/lse, no "
+                         "gradients); e4m3 quantizes X and W per row first (outside the timed region)")
     ap.add_argument("--dense-backward", action="store_true",
                     help="run the backward over every row (RLLOSS_FLAG_DENSE_BACKWARD), for comparison")
     ap.add_argument("--no-naive-memory", action="store_true",
@@ -330,13 +333,70 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     indices = range(5) if args.all_configs else [args.workload]
     for k in indices:
-        line = measure(args, k, dev, world, rank, local)
+        line = measure_scoring(args, k, dev, world) if args.scoring else measure(args, k, dev, world, rank, local)
         if rank == 0:
             print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def measure_scoring(args, index, dev, world):
+    """Forward-only scoring throughput (rlloss_forward / rlloss_forward_e4m3)
+    on workload ``index``: tokens/s and 2*N*H*V flop per step."""
+    import torch
+    from lm_head_log_tma_gb300 import rlloss as R
+    from lm_head_log_tma_gb300.workloads import WORKLOADS, make_inputs
+    spec = WORKLOADS[index]
+    inp = make_inputs(spec, device=dev)
+    N, H, V = spec.N, spec.H, spec.V
+    peak, peak_sus, _, peak_src = load_peaks()
+    if args.scoring == "e4m3":
+        def q(x):
+            x = x.float()
+            sc = (x.abs().amax(dim=1) / 448.0).clamp(min=1e-30)
+            return (x / sc[:, None]).to(torch.float8_e4m3fn), sc.contiguous()
+        X8, xs = q(inp.X)
+        W8, wsc = q(inp.W)
+        b = None if inp.b is None else inp.b.float()
+        cfg = R.make_cfg(spec.B, spec.T, H, V, dtype=R.FP8_E4M3, temperature=spec.temperature,
+                         has_bias=spec.has_bias)
+        call = lambda ws: R.forward_e4m3(cfg, X8, xs, W8, wsc, b, inp.targets, workspace=ws)
+        dtype, bf16_equiv_peak = "e4m3", 2 * peak
+    else:
+        cfg = cfg_for(R, spec)
+        call = lambda ws: R.forward(cfg, inp.X, inp.W, inp.b, inp.targets, workspace=ws)
+        dtype, bf16_equiv_peak = spec.dtype, peak
+    ws = R.alloc_workspace(R.rlloss_forward_workspace_bytes(cfg), dev)
+    for _ in range(max(3, args.warmup)):
+        call(ws)
+    torch.cuda.synchronize()
+    assert R.rlloss_get_device_status(ws) == 0
+    clocks = ClockSampler(dev.index or 0)
+    clocks.wait_first_sample()
+    time.sleep(0.1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark()
+    e0.record()
+    for _ in range(args.steps):
+        call(ws)
+    e1.record()
+    torch.cuda.synchronize()
+    clocks.mark()
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
+    tflops = 2.0 * N * H * V / (ms / 1e3) / 1e12
+    return {"metric": "LM-head forward-only scoring tokens/s (logp, entropy, lse) at H896/V151936",
+            "value": whole_job_rate(N, world, args.steps, ms * args.steps / 1e3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": {"workload": spec.name, "B": spec.B, "T": spec.T, "H": H, "V": V, "mode": "scoring"},
+            "tflops_2nhv": tflops,
+            "peak_frac": tflops / bf16_equiv_peak,
+            "peak_note": (f"{peak_src} bf16 burst x 2 (the nominal e4m3:bf16 ratio)" if dtype == "e4m3"
+                          else f"{peak_src} bf16 burst"),
+            "clocks": clk}
 
 
 def measure(args, index, dev, world, rank, local):
