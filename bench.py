@@ -50,8 +50,8 @@ def parse_args():
     ap.add_argument("--scoring", choices=["bf16", "e4m3"], default=None,
                     help="time the forward-only scoring entry instead (per-token logp/entropy/lse, no "
                          "gradients); e4m3 quantizes X and W per row first (outside the timed region)")
-    ap.add_argument("--dense-backward", action="store_true",
-                    help="run the backward over every row (RLLOSS_FLAG_DENSE_BACKWARD), for comparison")
+    ap.add_argument("--all-rows", action="store_true",
+                    help="run the backward over every row (RLLOSS_FLAG_ALL_ROWS), for comparison")
     ap.add_argument("--no-naive-memory", action="store_true",
                     help="skip the full-logits torch path run for the memory comparison")
     return ap.parse_args()
@@ -406,7 +406,7 @@ def measure(args, index, dev, world, rank, local):
     from lm_head_log_tma_gb300 import rlloss as R
 
     spec, inp, old, ref = make_workload(dev, index)
-    cfg = cfg_for(R, spec, args.chunk_rows, R.FLAG_DENSE_BACKWARD if args.dense_backward else 0)
+    cfg = cfg_for(R, spec, args.chunk_rows, R.FLAG_ALL_ROWS if args.all_rows else 0)
     N, H, V = spec.N, spec.H, spec.V
     ws_bytes = R.rlloss_workspace_bytes(cfg)
     naive_bytes, naive_note = (None, "skipped") if args.no_naive_memory else naive_peak_extra_bytes(
@@ -417,7 +417,7 @@ def measure(args, index, dev, world, rank, local):
     def step():
         nonlocal outs
         outs = R.fwd_bwd(cfg, inp.X, inp.W, inp.b, inp.targets, old, ref, inp.adv, inp.mask, workspace=ws,
-                         outputs=outs)
+                         outputs=outs, per_token=False)
 
     def barrier():
         if world > 1:
@@ -433,6 +433,8 @@ def measure(args, index, dev, world, rank, local):
     call_alloc = torch.cuda.max_memory_allocated(dev) - mem0
     status = R.rlloss_get_device_status(ws)
     bwd_rows = R.rlloss_get_backward_rows(ws)   # rows with c_n != 0: the backward runs over these
+    # rows the forward computed: whole row tiles holding an unmasked row
+    fwd_rows = min(N, R.rlloss_get_forward_tiles(ws) * (128 if (cfg.flags & R.FLAG_SINGLE_CTA_TILES) else 256))
     if status != 0:
         raise RuntimeError(f"device status {status:#x}")
 
@@ -499,7 +501,7 @@ def measure(args, index, dev, world, rank, local):
             stream.wait_event(copied[slot])
             d = dbufs[slot]
             outs = R.fwd_bwd(cfg, d["X"], d["W"], d.get("b"), d["targets"], d["old"], d.get("ref"), d["adv"],
-                             d["mask"], workspace=ws, outputs=outs)
+                             d["mask"], workspace=ws, outputs=outs, per_token=False)
             consumed[slot].record(stream)
             res_host[:1].copy_(outs["loss"], non_blocking=True)
             res_host[1:].copy_(outs["metrics"], non_blocking=True)
@@ -520,7 +522,8 @@ def measure(args, index, dev, world, rank, local):
     per_step = [m / args.steps for m in phase_ms]
     # tensor-core phases and the flop they execute per step: the forward over
     # all N rows, the recompute and dX/dW over the backward's rows
-    gemm_phases = {0: ("fwd_gemm", 2.0 * N), 2: ("bwd_dlogits", 2.0 * bwd_rows), 3: ("bwd_dX_dW", 4.0 * bwd_rows)}
+    gemm_phases = {0: ("fwd_gemm", 2.0 * fwd_rows), 2: ("bwd_dlogits", 2.0 * bwd_rows),
+                   3: ("bwd_dX_dW", 4.0 * bwd_rows)}
     dom = max(gemm_phases, key=lambda k: per_step[k])
     flops_phase = gemm_phases[dom][1] * H * V
     launches_per_step = max(1, phase_n[dom] // args.steps)
@@ -534,7 +537,7 @@ def measure(args, index, dev, world, rank, local):
                 "peak_source": f"{peak_src} bf16 burst", "frac_of_sustained": achieved / peak_sus,
                 "launches_per_step": launches_per_step}
     step_tflops = 6.0 * N * H * V / (ms_step / 1e3) / 1e12
-    executed_tflops = (2.0 * N + 6.0 * bwd_rows) * H * V / (ms_step / 1e3) / 1e12
+    executed_tflops = (2.0 * fwd_rows + 6.0 * bwd_rows) * H * V / (ms_step / 1e3) / 1e12
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -550,6 +553,7 @@ def measure(args, index, dev, world, rank, local):
                        "parallelism": "replicas" if world > 1 else "single"},
             "tc_peak_frac_6nhv": step_tflops / peak,
             "tc_tflops_6nhv": step_tflops,
+            "forward_rows": fwd_rows,
             "backward_rows": bwd_rows,
             "executed_tflops": executed_tflops,
             "executed_peak_frac": executed_tflops / peak,
@@ -563,7 +567,7 @@ def measure(args, index, dev, world, rank, local):
                        "naive_full_logits_peak_extra_bytes": naive_bytes,
                        "naive_fits": naive_bytes is not None, "naive_note": naive_note,
                        "chunk_rows": args.chunk_rows or "default",
-                       "backward": "dense" if args.dense_backward else "rows with c_n != 0"}}
+                       "backward": "dense" if args.all_rows else "rows with c_n != 0"}}
 
     if rank == 0 and not args.no_cpu_baseline:
         if args.all_configs:   # config 0 whole, the others one sequence

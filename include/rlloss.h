@@ -88,10 +88,15 @@ extern "C" {
 #define RLLOSS_FLAG_SINGLE_CTA_TILES 0x2u    /* forward / recompute kernels on 128-row single-CTA
                                                 tiles instead of 256-row CTA-pair tiles (same
                                                 results; for comparison) */
-#define RLLOSS_FLAG_DENSE_BACKWARD 0x8u      /* run the backward over every row.  By default rows
-                                                whose coefficient c_n = dL/dlogp_n is zero (tokens
-                                                outside the mask, clipped tokens without KL, clipped
-                                                GSPO sequences) are dropped before the backward:
+#define RLLOSS_FLAG_ALL_ROWS 0x8u            /* run the forward and the backward over every row.
+                                                By default rlloss_fwd_bwd (1) skips the forward of
+                                                row tiles in which every row is masked, when no
+                                                per-token logp / entropy output is requested and
+                                                advantages are per sequence: such rows enter
+                                                neither the loss nor the gradients; and (2) drops
+                                                before the backward the rows whose coefficient
+                                                c_n = dL/dlogp_n is zero (tokens outside the mask,
+                                                clipped tokens without KL, clipped GSPO sequences):
                                                 they add exactly nothing to dX, dW, db ("Add GMPO
                                                 ...", Details: the gradients are sums over tokens
                                                 of c_n times per-token terms).  Same results up to
@@ -229,10 +234,17 @@ int rlloss_get_device_status(const void* workspace, int32_t* status);
 
 /* Copy into *rows the number of rows the last rlloss_fwd_bwd on ``workspace``
  * ran its backward over: the rows with c_n != 0, or every row under
- * RLLOSS_FLAG_DENSE_BACKWARD (see there).  Synchronous; call after the stream
+ * RLLOSS_FLAG_ALL_ROWS (see there).  Synchronous; call after the stream
  * has finished.  Returns RLLOSS_ECUDA if the copy failed.  (Our addition, for
  * reporting executed work; the pages have no counterpart.) */
 int rlloss_get_backward_rows(const void* workspace, int32_t* rows);
+
+/* Copy into *tiles the number of row tiles (256 rows each, 128 with
+ * RLLOSS_FLAG_SINGLE_CTA_TILES) the last forward on ``workspace`` computed:
+ * all of them, or under rlloss_fwd_bwd's tile skipping (see
+ * RLLOSS_FLAG_ALL_ROWS) those holding a row with mask != 0.  Synchronous;
+ * call after the stream has finished.  (Ours, for reporting executed work.) */
+int rlloss_get_forward_tiles(const void* workspace, int32_t* tiles);
 
 /* Launch a kernel that waits on a barrier nothing will complete, with a limit
  * of limit_ns nanoseconds, so the bounded-wait path can be exercised: the

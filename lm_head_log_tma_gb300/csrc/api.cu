@@ -21,8 +21,10 @@ using namespace rl;
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
 // Status region (first 256 bytes of every workspace): [0] device status word,
-// [4] loss-stage batch ticket, [8] compaction ticket, [12] backward rows.
+// [4] loss-stage batch ticket, [8] compaction ticket, [12] backward rows,
+// [16] tile-scan ticket, [20] forward row tiles, [24] forward vocabulary segments.
 constexpr size_t kBackwardRowsOffset = 12;
+constexpr size_t kTileTicketOffset = 16, kFwdTilesOffset = 20, kFwdSegmentsOffset = 24;
 constexpr size_t kPartialCapBytes = size_t(64) << 20;
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
@@ -64,7 +66,7 @@ int validate_common(const rlloss_cfg* c) {
   const float q = c->top_entropy_quantile;
   if (!(q >= 0.f && q <= 1.f)) return RLLOSS_EINVAL;
   if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN |
-                   RLLOSS_FLAG_DENSE_BACKWARD))
+                   RLLOSS_FLAG_ALL_ROWS))
     return RLLOSS_EINVAL;
   if ((c->flags & RLLOSS_FLAG_ADV_PER_TOKEN) && c->loss_type != RLLOSS_GSPO_TOKEN) return RLLOSS_EUNSUPPORTED;
   if (c->loss_type == RLLOSS_GSPO_TOKEN) {
@@ -80,7 +82,7 @@ int validate_head(const rlloss_cfg* c) {
   if (c->B < 1 || c->T < 1) return RLLOSS_EINVAL;
   if ((long long)c->B * c->T > (1ll << 31) - 1) return RLLOSS_EINVAL;
   if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN |
-                   RLLOSS_FLAG_DENSE_BACKWARD))
+                   RLLOSS_FLAG_ALL_ROWS))
     return RLLOSS_EINVAL;
   if (c->H < 1 || c->V < 1) return RLLOSS_EINVAL;
   if (c->dtype != RLLOSS_BF16 && c->dtype != RLLOSS_FP32 && c->dtype != RLLOSS_FP8_E4M3) return RLLOSS_EINVAL;
@@ -117,7 +119,7 @@ struct Plan {
   bool fp32, f8, bias, ent;
   bool fused_loss;          // row merge and loss stage in one launch (no entropy mask)
   bool compact;             // backward over the rows with c_n != 0 only
-  int R, Vt, P, Hp, Vp;
+  int R, Vt, P, pcap, Hp, Vp;
   int kb_fwd, nseg_fwd;     // forward K: nseg_fwd * kb_fwd k-blocks
   int Kx;                   // row width (elements) of the bf16 X / W operand arrays
   int Nc, nchunks, ld_dl;
@@ -125,23 +127,15 @@ struct Plan {
   int slices;
   size_t o_tickets, o_part;
   size_t o_status, o_partial, o_lse2, o_logp64, o_ent, o_coef, o_emask, o_k3, o_seq, o_bias2, o_dl, o_x3, o_w3,
-      o_dbpart, o_ws2, o_blk, o_cidx, o_xc, o_coefc, o_lse2c, o_tgtc, o_dxc, total;
+      o_dbpart, o_ws2, o_tflags, o_tlist, o_blk, o_cidx, o_xc, o_coefc, o_lse2c, o_tgtc, o_dxc, total;
   int Ncap;                 // rows of the compacted arrays (N rounded up to 256)
 };
 
-int choose_segments(int R, int Vt, int G, long long N) {
-  int best = 1;
-  long long best_t = -1;
-  for (int P = 1; P <= std::min(64, Vt); ++P) {
-    if (P > 1 && size_t(N) * 2 * P * 32 > kPartialCapBytes) break;
-    const long long waves = cdiv((long long)R * P, G);
-    const long long t = waves * cdiv(Vt, P);
-    if (best_t < 0 || t < best_t) {
-      best_t = t;
-      best = P;
-    }
-  }
-  return best;
+// Largest vocabulary-segment count whose partial states fit the cap (<= 64).
+int segment_cap(long long N) {
+  long long c = (long long)(kPartialCapBytes / (size_t(N) * 2 * 32));
+  if (c > 64) c = 64;
+  return c < 1 ? 1 : int(c);
 }
 
 enum PlanMode { kFull, kLossOnly, kForwardOnly };
@@ -180,7 +174,8 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.R = int(cdiv(p.N, p.rows_tile));
     p.Vt = int(cdiv(p.V, 256));
     p.fwd_clusters = resident_or(fwd_resident_clusters(p.pair), p.sms / p.pair);
-    p.P = choose_segments(p.R, p.Vt, p.fwd_clusters, p.N);
+    p.pcap = segment_cap(p.N);
+    p.P = choose_segments(p.R, p.Vt, p.fwd_clusters, p.pcap);
     p.Hp = int(rup(p.H, 64));
     p.Vp = int(rup(p.V, 64));
     if (p.fp32) {
@@ -196,7 +191,7 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
       p.kb_fwd = int(cdiv(p.H, 64));
       p.Kx = p.H;
     }
-    p.o_partial = take(size_t(p.N) * 2 * p.P * 32);
+    p.o_partial = take(size_t(p.N) * 2 * p.pcap * 32);   // room for a segment count chosen on the device
     p.o_lse2 = take(size_t(p.N) * 4);
     p.o_logp64 = take(size_t(p.N) * 8);
     p.o_ent = take(size_t(p.N) * 4);
@@ -224,7 +219,9 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.o_coef = take(size_t(p.N) * 4);
     p.o_dl = take(size_t(p.Nc) * p.ld_dl * 2);
     p.o_dbpart = take(p.bias ? size_t(db_part_rows(p.Nc)) * p.V * 4 : 0);
-    p.compact = !(c->flags & RLLOSS_FLAG_DENSE_BACKWARD);
+    p.compact = !(c->flags & RLLOSS_FLAG_ALL_ROWS);
+    p.o_tflags = take(size_t(p.R));
+    p.o_tlist = take(size_t(p.R) * 4);
     if (p.compact) {
       p.Ncap = int(rup(p.N, 256));
       p.o_blk = take(size_t(compact_groups(p.N)) * 2 * 4);
@@ -425,9 +422,11 @@ struct Head {
 
 // With merge == false the row merge is left to the caller (the fused merge +
 // loss launch); h.mp is filled either way.
+// With skip_mask set, the forward runs only over row tiles that hold a row
+// with skip_mask != 0 (the rows of the other tiles get no outputs).
 int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W, const void* b,
              const int64_t* targets, float* out_logp, float* out_entropy, float* out_lse, char* ws,
-             cudaStream_t st, Head& h, bool merge = true) {
+             cudaStream_t st, Head& h, bool merge = true, const uint8_t* skip_mask = nullptr) {
   int* status = reinterpret_cast<int*>(ws + p.o_status);
   const float scale2 = float(1.4426950408889634 / double(cfg->temperature));
   // Operand arrays: bf16 inputs are used in place; fp32 inputs are split
@@ -492,6 +491,23 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
   fp.bias2 = h.bias2;
   fp.targets = targets;
   fp.partial = reinterpret_cast<float4*>(ws + p.o_partial);
+  fp.pcap = p.pcap;
+  const uint8_t* tflags = nullptr;
+  if (skip_mask) {
+    tflags = reinterpret_cast<uint8_t*>(ws + p.o_tflags);
+    int* tlist = reinterpret_cast<int*>(ws + p.o_tlist);
+    int* ntiles = reinterpret_cast<int*>(ws + p.o_status + kFwdTilesOffset);
+    Phase ph(st, 5);
+    RL_TRY(launch_tile_scan(skip_mask, p.N, p.rows_tile, const_cast<uint8_t*>(tflags), tlist, ntiles,
+                            reinterpret_cast<unsigned int*>(ws + p.o_status + kTileTicketOffset), st));
+    ph.launched();
+    fp.tiles = tlist;
+    fp.ntiles = ntiles;
+    fp.P_out = reinterpret_cast<int*>(ws + p.o_status + kFwdSegmentsOffset);
+  } else {
+    RL_TRY(launch_set_total(reinterpret_cast<int*>(ws + p.o_status + kFwdTilesOffset), p.R, st));
+    g_launches += 1;
+  }
   fp.status = status;
   fp.limit_ns = kWaitLimitNs;
   {
@@ -504,6 +520,11 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
   mp.N = p.N;
   mp.V = p.V;
   mp.slots = 2 * p.P;
+  if (skip_mask) {
+    mp.P_dev = fp.P_out;
+    mp.tile_active = tflags;
+    mp.tile_shift = p.rows_tile == 256 ? 8 : 7;
+  }
   mp.targets = targets;
   mp.lse2 = reinterpret_cast<float*>(ws + p.o_lse2);
   mp.logp64 = reinterpret_cast<double*>(ws + p.o_logp64);
@@ -588,6 +609,12 @@ uint64_t rlloss_kernel_launches(void) { return g_launches.load(); }
 int rlloss_get_device_status(const void* workspace, int32_t* status) {
   if (!workspace || !status) return RLLOSS_EINVAL;
   return cuda_rc(cudaMemcpy(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost));
+}
+
+int rlloss_get_forward_tiles(const void* workspace, int32_t* tiles) {
+  if (!workspace || !tiles) return RLLOSS_EINVAL;
+  return cuda_rc(cudaMemcpy(tiles, static_cast<const char*>(workspace) + kFwdTilesOffset, sizeof(int32_t),
+                            cudaMemcpyDeviceToHost));
 }
 
 int rlloss_get_backward_rows(const void* workspace, int32_t* rows) {
@@ -711,7 +738,13 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, p.o_tickets + size_t(p.B) * 4 - p.o_status, st));
 
   Head hd;
-  RL_TRY_RC(run_head(cfg, p, X, W, b, targets, out_logp, out_entropy, nullptr, ws, st, hd, !p.fused_loss));
+  // Row tiles whose rows are all masked enter neither the loss nor the
+  // gradients; their forward is skipped unless per-token outputs are wanted
+  // or advantages are per token (tokens outside the mask then count).
+  const bool skip_tiles = !(cfg->flags & (RLLOSS_FLAG_ALL_ROWS | RLLOSS_FLAG_ADV_PER_TOKEN)) && !out_logp &&
+                          !out_entropy;
+  RL_TRY_RC(run_head(cfg, p, X, W, b, targets, out_logp, out_entropy, nullptr, ws, st, hd, !p.fused_loss,
+                     skip_tiles ? mask : nullptr));
   const void* Xop = hd.Xop;
   const void* Wop = hd.Wop;
   const float* bias2 = hd.bias2;

@@ -111,6 +111,53 @@ __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactPa
   }
 }
 
+// Block b: does row tile b hold a row with mask != 0?  The last block to
+// finish lists the flagged tiles in ascending order.
+__global__ void __launch_bounds__(kCompactBlock) tile_scan_kernel(const uint8_t* mask, int N, int tile_rows,
+                                                                   uint8_t* flags, int* list, int* count,
+                                                                   unsigned int* ticket) {
+  __shared__ int is_last;
+  __shared__ int part[kCompactBlock];
+  const int r = blockIdx.x * tile_rows + threadIdx.x;
+  const int any = __syncthreads_or(threadIdx.x < tile_rows && r < N && mask[r] != 0);
+  if (threadIdx.x == 0) {
+    flags[blockIdx.x] = any ? 1 : 0;
+    __threadfence();
+    is_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    if (is_last) __threadfence();
+  }
+  __syncthreads();
+  if (!is_last) return;
+  const int nt = int(gridDim.x);
+  const int per = (nt + kCompactBlock - 1) / kCompactBlock;   // consecutive tiles per thread
+  int s = 0;
+  for (int k = 0; k < per; ++k) {
+    const int i = threadIdx.x * per + k;
+    if (i < nt) s += __ldcg(flags + i);
+  }
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 1; o < kCompactBlock; o <<= 1) {   // inclusive scan of part[]
+    const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int pos = threadIdx.x ? part[threadIdx.x - 1] : 0;
+  for (int k = 0; k < per; ++k) {
+    const int i = threadIdx.x * per + k;
+    if (i < nt && __ldcg(flags + i)) list[pos++] = i;
+  }
+  if (threadIdx.x == 0) *count = part[kCompactBlock - 1];
+}
+
+cudaError_t launch_tile_scan(const uint8_t* mask, int N, int tile_rows, uint8_t* flags, int* list, int* count,
+                             unsigned int* ticket, cudaStream_t st) {
+  tile_scan_kernel<<<(N + tile_rows - 1) / tile_rows, kCompactBlock, 0, st>>>(mask, N, tile_rows, flags, list, count,
+                                                                             ticket);
+  return cudaGetLastError();
+}
+
 __global__ void set_total_kernel(int* total, int N) { *total = N; }
 
 __global__ void scatter_rows_kernel(const float4* src, const int* idx, const int* total, int n0, int nc_max, int H4,

@@ -49,7 +49,7 @@ struct TileInfo {
   int seg;       // policy-defined segment id
   bool first;    // first tile of its unit
   bool last;     // last tile of its unit
-  int kbps = 0;  // policy-defined: k-blocks per product term
+  int aux = 0;   // policy-defined (dX/dW: k-blocks per product term; forward: vocabulary segments)
 };
 
 // Wait that ignores the abort flag; used only to drain in-flight work.

@@ -46,7 +46,24 @@ struct FwdPolicy {
     float xs;     // F8: this row's X scale
   };
 
-  __device__ static void cta_setup(const Params&, uint8_t*) {}
+  // Row tiles and vocabulary segments of this launch: all R tiles with the
+  // host's P, or the listed tiles with P chosen here for their count.
+  __device__ static void shape(const Params& p, int& R, int& P) {
+    if (p.tiles) {
+      R = *p.ntiles;
+      P = choose_segments(R, p.Vt, int(gridDim.x) / CL, p.pcap);
+    } else {
+      R = p.R;
+      P = p.P;
+    }
+  }
+  __device__ static void cta_setup(const Params& p, uint8_t*) {
+    if (p.P_out && blockIdx.x == 0 && threadIdx.x == 0) {
+      int R, P;
+      shape(p, R, P);
+      *p.P_out = P;
+    }
+  }
   __device__ static void prefetch(const Params& p) {
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB);
@@ -57,16 +74,19 @@ struct FwdPolicy {
   // same W tiles (L2 reuse) while each keeps its own rows.
   template <class F>
   __device__ static void for_each_tile(const Params& p, F&& f) {
-    const int units = p.R * p.P;
+    int R, P;
+    shape(p, R, P);
+    const int units = R * P;
     const int kbs = p.nseg * p.kb_per_seg;
     const int g0 = blockIdx.x / CL, gn = gridDim.x / CL;
     for (int u = g0; u < units; u += gn) {
-      const int seg = u / p.R;
-      const int r = u - seg * p.R;
-      const int j0 = int((long long)seg * p.Vt / p.P);
-      const int j1 = int((long long)(seg + 1) * p.Vt / p.P);
+      const int seg = u / R;
+      const int ri = u - seg * R;
+      const int r = p.tiles ? p.tiles[ri] : ri;
+      const int j0 = int((long long)seg * p.Vt / P);
+      const int j1 = int((long long)(seg + 1) * p.Vt / P);
       for (int j = j0; j < j1; ++j) {
-        TileInfo t{r * kRows, j * 256, 0, kbs, u, seg, j == j0, j == j1 - 1};
+        TileInfo t{r * kRows, j * 256, 0, kbs, u, seg, j == j0, j == j1 - 1, P};
         if (!f(t)) return;
       }
     }
@@ -192,7 +212,7 @@ struct FwdPolicy {
       }
     }
     if (t.last && row < p.N) {
-      float4* dst = p.partial + (size_t(row) * (2 * p.P) + size_t(t.seg) * 2 + half) * 2;
+      float4* dst = p.partial + (size_t(row) * (2 * t.aux) + size_t(t.seg) * 2 + half) * 2;
       dst[0] = make_float4(e.mref, e.s_hi, e.s_lo, e.w_hi);
       dst[1] = make_float4(e.w_lo, e.zy, e.found ? 1.f : 0.f, 0.f);
     }
@@ -203,7 +223,7 @@ struct FwdPolicy {
 // One warp per row: see merge_row.cuh.
 __global__ void fwd_merge_kernel(MergeParams p) {
   const int row = int((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5);
-  if (row >= p.N) return;
+  if (row >= p.N || !row_has_forward(p, row)) return;
   merge_row(p, row, threadIdx.x & 31);
 }
 
@@ -485,8 +505,8 @@ struct HPolicy {
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int q = t.seg;
     const HProblem& pr = p.pr[q];
-    const int s = kb / t.kbps;
-    const int kk = (kb - s * t.kbps) * 64;
+    const int s = kb / t.aux;
+    const int kk = (kb - s * t.aux) * 64;
     const int r = t.m0 + 128 * int(rank);
     if (pr.a_mn) {
       tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + r, pr.a_outer0 + kk);

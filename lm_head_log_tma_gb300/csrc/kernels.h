@@ -10,12 +10,36 @@ namespace rl {
 
 constexpr int kMaxSeg = 6;
 
+// Vocabulary segments of the forward: for R row tiles, Vt vocabulary tiles and
+// G clusters, the P <= pcap that minimises (waves of R*P units) x (tiles per
+// segment).  The host plan and the forward kernel (for a row count known only
+// on the device) use this same rule.
+__host__ __device__ inline int choose_segments(int R, int Vt, int G, int pcap) {
+  int best = 1;
+  long long best_t = -1;
+  for (int P = 1; P <= pcap && P <= Vt; ++P) {
+    const long long waves = ((long long)R * P + G - 1) / G;
+    const long long t = waves * ((Vt + P - 1) / P);
+    if (best_t < 0 || t < best_t) {
+      best_t = t;
+      best = P;
+    }
+  }
+  return best;
+}
+
 struct FwdParams {
   CUtensorMap tmA;            // X (or its 3-term bf16 split, or e4m3): inner K, outer rows; box 128 B x 128
   CUtensorMap tmB;            // W (or split, or e4m3): inner K, outer vocab; box 128 B x 256 (128 per CTA of a pair)
   int nseg, kb_per_seg;       // K = nseg * kb_per_seg * (64 bf16 or 128 e4m3 elements)
   int seg_a[kMaxSeg], seg_b[kMaxSeg];  // K offsets of each product term
   int N, V, R, Vt, P;         // rows, vocab, row tiles (128 or 256 rows), vocab tiles (256), vocab segments
+  // Optional: only the row tiles in tiles[0 .. *ntiles) (ascending) are computed, and
+  // the segment count is chosen on the device for them (<= pcap; written to *P_out).
+  const int* tiles;
+  const int* ntiles;
+  int pcap;
+  int* P_out;
   float scale2;               // log2(e) / temperature
   const float* bias2;         // [Vt*256] b * scale2, zero padded; null without bias
   const float* xs;            // e4m3 operands: [N] per-row X scales, else null
@@ -29,6 +53,9 @@ struct FwdParams {
 struct MergeParams {
   const float4* partial;
   int N, V, slots;            // slots = 2P
+  const int* P_dev;           // if set, slots = 2 * *P_dev (segments chosen on the device)
+  const uint8_t* tile_active; // if set, rows of row tiles (1 << tile_shift rows) with a 0 flag
+  int tile_shift;             //   had no forward: they are skipped (all their rows are masked)
   const int64_t* targets;
   float* lse2;                // [N] lse in log2 units
   double* logp64;             // [N]
@@ -149,6 +176,10 @@ struct CompactParams {
   __nv_bfloat16* xc;          // [Ncap, Kx]
 };
 int compact_groups(int N);   // 32-row groups
+// Row tiles of tile_rows rows holding a row with mask != 0: flags[R], their
+// ascending list and count (ticket zeroed before the launch).
+cudaError_t launch_tile_scan(const uint8_t* mask, int N, int tile_rows, uint8_t* flags, int* list, int* count,
+                             unsigned int* ticket, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t st);
 cudaError_t launch_set_total(int* total, int N, cudaStream_t st);
 // dst[idx[n0 + j]][:] = src[j][:] for j < clamp(*total - n0, 0, nc_max); H % 4 == 0.

@@ -402,6 +402,7 @@ __global__ void __launch_bounds__(kLossThreads) merge_loss_kernel(MergeParams mp
   double a[5] = {0, 0, 0, 0, 0};
   for (int t = t0 + warp; t < t1; t += kLossThreads / 32) {
     const long long n = base + t;
+    if (!row_has_forward(mp, int(n))) continue;   // skipped tile: every row masked, no terms
     const double lp = merge_row(mp, int(n), lane);
     if (lane == 0) token_terms(p, n, lp, A, gmpo, a);
   }

@@ -34,13 +34,19 @@ __device__ __forceinline__ void df_warp_sum(float& hi, float& lo) {
   }
 }
 
+// False for rows of row tiles the forward skipped (every row there is masked).
+__device__ __forceinline__ bool row_has_forward(const MergeParams& p, int row) {
+  return !p.tile_active || p.tile_active[row >> p.tile_shift];
+}
+
 // Merges row `row` (all 32 lanes of the warp take part) and writes its lse,
 // logp and entropy; returns the row's logp on lane 0 (NaN for a bad target).
 __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int lane) {
   const long long y = lane == 0 ? p.targets[row] : 0;   // issued early, used at the end
-  const float4* base = p.partial + size_t(row) * p.slots * 2;
+  const int slots = p.P_dev ? 2 * *p.P_dev : p.slots;
+  const float4* base = p.partial + size_t(row) * slots * 2;
   float M = -INFINITY;
-  for (int k = lane; k < p.slots; k += 32) {
+  for (int k = lane; k < slots; k += 32) {
     const float4 a = base[2 * k];
     if (a.y + a.z > 0.f) M = fmaxf(M, a.x);
   }
@@ -48,7 +54,7 @@ __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int l
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float shi = 0.f, slo = 0.f, whi = 0.f, wlo = 0.f, zy = 0.f;
   int found = 0;
-  for (int k = lane; k < p.slots; k += 32) {
+  for (int k = lane; k < slots; k += 32) {
     const float4 a = base[2 * k];
     const float4 b = base[2 * k + 1];
     if (a.y + a.z > 0.f) {

@@ -45,10 +45,10 @@ def main():
                       inp.mask)
     pol = first["logp"].clone()
     old, ref = inp.old_logp(pol), inp.ref_logp(pol)
-    ws, outs = first["workspace"], first
-    for _ in range(a.warmup + a.steps):
+    ws, outs = first["workspace"], None
+    for _ in range(a.warmup + a.steps):   # a training step: no per-token outputs
         outs = R.fwd_bwd(cfg, inp.X, inp.W, inp.b, inp.targets, old, ref, inp.adv, inp.mask, workspace=ws,
-                         outputs=outs)
+                         outputs=outs, per_token=False)
     torch.cuda.synchronize()
     st = R.rlloss_get_device_status(ws)
     print(f"{spec.name} B={spec.B} T={spec.T}: loss {outs['loss'].item():.6g} status {st:#x}")

@@ -25,7 +25,7 @@ IS_TOKEN, IS_SEQUENCE = 0, 1
 FLAG_FORCE_ENTROPY_PATH = 0x1
 FLAG_SINGLE_CTA_TILES = 0x2
 FLAG_ADV_PER_TOKEN = 0x4
-FLAG_DENSE_BACKWARD = 0x8
+FLAG_ALL_ROWS = 0x8
 NMETRICS = 8
 
 
@@ -74,6 +74,8 @@ def _load():
     lib.rlloss_get_device_status.restype = c_int
     lib.rlloss_get_backward_rows.argtypes = [P, ctypes.POINTER(c_int32)]
     lib.rlloss_get_backward_rows.restype = c_int
+    lib.rlloss_get_forward_tiles.argtypes = [P, ctypes.POINTER(c_int32)]
+    lib.rlloss_get_forward_tiles.restype = c_int
     lib.rlloss_selftest_bounded_wait.argtypes = [P, c_uint64, P]
     lib.rlloss_selftest_bounded_wait.restype = c_int
     lib.rlloss_phase_timing.argtypes = [c_int]
@@ -164,6 +166,14 @@ def rlloss_get_device_status(workspace) -> int:
     return int(st.value)
 
 
+def rlloss_get_forward_tiles(workspace) -> int:
+    tiles = c_int32(0)
+    rc = lib.rlloss_get_forward_tiles(_p(workspace), ctypes.byref(tiles))
+    if rc != OK:
+        raise RllossError(rc, "rlloss_get_forward_tiles")
+    return int(tiles.value)
+
+
 def rlloss_get_backward_rows(workspace) -> int:
     rows = c_int32(0)
     rc = lib.rlloss_get_backward_rows(_p(workspace), ctypes.byref(rows))
@@ -203,8 +213,11 @@ def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
 
 
 def fwd_bwd(cfg: RllossCfg, X, W, b, targets, old_logp, ref_logp, adv, mask, workspace=None,
-            outputs=None, stream=None):
-    """Allocate outputs (torch) and run rlloss_fwd_bwd.  Returns a dict of tensors."""
+            outputs=None, stream=None, per_token=True):
+    """Allocate outputs (torch) and run rlloss_fwd_bwd.  Returns a dict of tensors.
+    per_token=False leaves out the per-token logp / entropy outputs (a
+    training step needs only loss, metrics and gradients), which lets the
+    library skip the forward of row tiles whose rows are all masked."""
     dev = X.device
     N, H, V = cfg.B * cfg.T, cfg.H, cfg.V
     if outputs is None:
@@ -214,8 +227,8 @@ def fwd_bwd(cfg: RllossCfg, X, W, b, targets, old_logp, ref_logp, adv, mask, wor
             dX=torch.empty(N, H, dtype=torch.float32, device=dev),
             dW=torch.empty(V, H, dtype=torch.float32, device=dev),
             db=torch.empty(V, dtype=torch.float32, device=dev) if cfg.has_bias else None,
-            logp=torch.empty(N, dtype=torch.float32, device=dev),
-            entropy=torch.empty(N, dtype=torch.float32, device=dev),
+            logp=torch.empty(N, dtype=torch.float32, device=dev) if per_token else None,
+            entropy=torch.empty(N, dtype=torch.float32, device=dev) if per_token else None,
             emask=torch.empty(N, dtype=torch.uint8, device=dev),
         )
     if workspace is None:

@@ -72,12 +72,12 @@ class Case:
         return O.loss_stage(self.prob, self.logp, self.ent, self.old64, self.ref64, self.adv64,
                             self.mask, emask_override=emask_override, clip_override=clip_override)
 
-    def run_gpu(self, R, dev="cuda", **cfg_kw):
+    def run_gpu(self, R, dev="cuda", per_token=True, **cfg_kw):
         i = self.inp
         cfg = cfg_of(R, self.spec, **cfg_kw)
         t = lambda x: None if x is None else x.to(dev)
         out = R.fwd_bwd(cfg, t(i.X), t(i.W), t(i.b), t(i.targets), t(self.old), t(self.ref), t(i.adv),
-                        t(i.mask))
+                        t(i.mask), per_token=per_token)
         torch.cuda.synchronize()
         out["status"] = R.rlloss_get_device_status(out["workspace"])
         return out

@@ -44,3 +44,14 @@ def test_full_size_workload(R, idx):
     stats = check_grads(out, case, res, dx_rows=rows, dw_rows=vs)
     print(f"{spec.name}: loss {gl:.9g} vs {ol:.9g} (rel {abs(gl - ol) / abs(ol):.2e}); "
           f"logp max err {el:.2e}, entropy max err {ee:.2e}; grads {stats}")
+    # the training-step call the bench times (no per-token outputs: fully masked
+    # row tiles skip the forward) meets the same bar on the same samples
+    del out
+    step = case.run_gpu(R, per_token=False)
+    assert step["status"] == 0, hex(step["status"])
+    res2 = reconcile_loss(step, case)
+    check_loss_and_metrics(step, case, res2)
+    stats2 = check_grads(step, case, res2, dx_rows=rows, dw_rows=vs)
+    print(f"  training-step call: loss {step['loss'].item():.9g}; forward tiles "
+          f"{R.rlloss_get_forward_tiles(step['workspace'])}, backward rows "
+          f"{R.rlloss_get_backward_rows(step['workspace'])}; grads {stats2}")

@@ -274,7 +274,7 @@ def test_compacted_backward_matches_dense(R, spec):
     order, the same forward and loss bits, and both pass the oracle."""
     case = Case(spec)
     a, res, _ = _full_check(R, case)
-    b, _, _ = _full_check(R, case, flags=R.FLAG_DENSE_BACKWARD)
+    b, _, _ = _full_check(R, case, flags=R.FLAG_ALL_ROWS)
     keep = res.c != 0
     assert 0 < keep.sum() < spec.N, "the workload must both keep and drop rows"
     assert R.rlloss_get_backward_rows(a["workspace"]) == int(keep.sum())
@@ -306,7 +306,37 @@ def test_compaction_with_empty_later_chunks(R):
     case = Case(spec)
     a, res, _ = _full_check(R, case, chunk_rows=256)
     assert 0 < (res.c != 0).sum() <= 160
-    b, _, _ = _full_check(R, case, chunk_rows=256, flags=R.FLAG_DENSE_BACKWARD)
+    b, _, _ = _full_check(R, case, chunk_rows=256, flags=R.FLAG_ALL_ROWS)
+    _grads_close(a, b)
+
+
+SKIP = [
+    Workload("long_prompt_gmpo", B=2, T=640, H=128, V=900, dtype="bf16", prompt_len=560, seed=111),
+    Workload("long_prompt_entropy", B=3, T=512, H=128, V=700, dtype="bf16", prompt_len=300, temperature=0.7,
+             top_entropy_quantile=0.3, seed=112),
+    Workload("long_prompt_gspo", B=4, T=512, H=64, V=600, dtype="bf16", loss_type=GSPO_TOKEN, eps_low=3e-4,
+             eps_high=4e-4, prompt_len=280, old_noise_std=0.02, seed=113),
+    Workload("long_prompt_fp32_bias", B=2, T=600, H=100, V=515, dtype="fp32", has_bias=True, bias_std=0.1,
+             prompt_len=520, seed=114),
+]
+
+
+@pytest.mark.parametrize("spec", SKIP, ids=[s.name for s in SKIP])
+def test_forward_skips_fully_masked_tiles(R, spec):
+    """Without per-token outputs the forward runs only over row tiles that
+    hold an unmasked row; loss, metrics and gradients match the oracle and the
+    run with per-token outputs (which computes every tile)."""
+    case = Case(spec)
+    a = case.run_gpu(R, per_token=False)
+    assert a["status"] == 0, hex(a["status"])
+    tiles = -(-spec.N // 256)
+    assert R.rlloss_get_forward_tiles(a["workspace"]) < tiles
+    res = reconcile_loss(a, case)
+    check_loss_and_metrics(a, case, res)
+    check_grads(a, case, res)
+    b, _, _ = _full_check(R, case)
+    assert R.rlloss_get_forward_tiles(b["workspace"]) == tiles
+    assert abs(a["loss"].item() - b["loss"].item()) <= 1e-6 * abs(b["loss"].item()) + 1e-9
     _grads_close(a, b)
 
 
