@@ -220,11 +220,11 @@ struct FwdPolicy {
   __device__ static void epilogue_finish(const Params&, int) {}
 };
 
-// One warp per row: see merge_row.cuh.
+// Four lanes per row: see merge_row.cuh.
 __global__ void fwd_merge_kernel(MergeParams p) {
-  const int row = int((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5);
-  if (row >= p.N || !row_has_forward(p, row)) return;
-  merge_row(p, row, threadIdx.x & 31);
+  const int r = int((blockIdx.x * (long long)blockDim.x + threadIdx.x) / kMergeLanes);
+  const bool live = r < p.N && row_has_forward(p, r);
+  merge_row(p, live ? r : -1, threadIdx.x % kMergeLanes);
 }
 
 // =============================================================== dlogits
@@ -728,7 +728,7 @@ cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st
 }
 cudaError_t launch_gemmH(const HParams& p, int units, cudaStream_t st) { return launch_engine<HPolicy>(p, units, st); }
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
-  fwd_merge_kernel<<<(p.N + 7) / 8, 256, 0, st>>>(p);
+  fwd_merge_kernel<<<(p.N + 63) / 64, 256, 0, st>>>(p);   // 64 rows per block
   return cudaGetLastError();
 }
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st) {

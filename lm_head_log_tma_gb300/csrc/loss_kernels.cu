@@ -133,7 +133,7 @@ cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long
 
 // ----------------------------------------------------------------------- K2
 constexpr int kLossThreads = 256;
-constexpr int kFusedRows = 8;      // rows per block of the fused merge + loss kernel (one per warp)
+constexpr int kFusedRows = 64;     // rows per block of the fused merge + loss kernel (8 per warp, 4 lanes each)
 constexpr int kRec = 10;           // doubles per sequence record
 
 template <int K>
@@ -145,10 +145,9 @@ __device__ __forceinline__ void warp_sum_k(double (&v)[K]) {
 }
 
 // K sums over the block, in a fixed order; the result is valid in thread 0.
-// With lane0_only, each warp's values are already summed into its lane 0.
 template <int K>
-__device__ __forceinline__ void block_sum_k(double (&v)[K], double (*sh)[32], bool lane0_only = false) {
-  if (!lane0_only) warp_sum_k(v);
+__device__ __forceinline__ void block_sum_k(double (&v)[K], double (*sh)[32]) {
+  warp_sum_k(v);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0)
 #pragma unroll
@@ -400,14 +399,15 @@ __global__ void __launch_bounds__(kLossThreads) merge_loss_kernel(MergeParams mp
   const double A = seq_adv(p, i);
   const bool gmpo = p.loss_type == RLLOSS_GMPO;
   double a[5] = {0, 0, 0, 0, 0};
-  for (int t = t0 + warp; t < t1; t += kLossThreads / 32) {
+  {
+    const int t = t0 + warp * kMergeRowsPerWarp + (lane / kMergeLanes);   // this lane group's row
     const long long n = base + t;
-    if (!row_has_forward(mp, int(n))) continue;   // skipped tile: every row masked, no terms
-    const double lp = merge_row(mp, int(n), lane);
-    if (lane == 0) token_terms(p, n, lp, A, gmpo, a);
+    const bool live = t < t1 && row_has_forward(mp, int(n));   // skipped tiles: every row masked, no terms
+    const double lp = merge_row(mp, live ? int(n) : -1, lane % kMergeLanes);
+    if (live && lane % kMergeLanes == 0) token_terms(p, n, lp, A, gmpo, a);
+    if (lane % kMergeLanes == 0) __threadfence();   // this row's outputs before the slice ticket
   }
-  if (lane == 0) __threadfence();   // this warp's row outputs before the slice ticket
-  block_sum_k(a, sh, true);         // only lane 0 of each warp holds terms
+  block_sum_k(a, sh);
   if (!publish_slice(p, i, sl, a, &is_last) || warp != 0) return;
   double r8[kRec];
   fold_sequence(p, i, lane, gmpo, r8);

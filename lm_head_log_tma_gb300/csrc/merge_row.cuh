@@ -10,23 +10,32 @@
 
 namespace rl {
 
-// Merge the 2P partial states of each row, one warp per row.  Each partial
-// holds, for one vocabulary segment and column half: reference m (log2
-// units, integer), s = sum 2^(t-m) and w = sum 2^(t-m) (t-m) as hi + lo
-// pairs, and the target's t if it fell there.  With M the largest m,
+// Merge the 2P partial states of each row.  Each partial holds, for one
+// vocabulary segment and column half: reference m (log2 units, integer),
+// s = sum 2^(t-m) and w = sum 2^(t-m) (t-m) as hi + lo pairs, and the
+// target's t if it fell there.  With M the largest m,
 //   S = sum_k 2^(m_k-M) s_k,   W = sum_k 2^(m_k-M) (w_k + (m_k-M) s_k).
 // Scaling by 2^(m_k-M) is exact in fp32, the sums are carried as
-// double-float (hi + lo) pairs, and only the final row values use fp64
-// (fp64 is a narrow unit on this GPU; conversions and adds per slot cost
-// more than the whole fp32 path).
+// double-float (hi + lo) pairs, and only the final row values use fp64.
+//
+// Four lanes merge one row (a warp holds 8 rows): each lane takes every
+// fourth slot, the group combines with two shuffle steps, and the group's
+// first lane finishes the row, so the per-row fp64 work runs for 8 rows at
+// once (fp64 is a narrow unit on this GPU; a warp instruction costs the same
+// with one active lane as with eight).
+constexpr int kMergeLanes = 4;
+constexpr int kMergeRowsPerWarp = 32 / kMergeLanes;
+
 __device__ __forceinline__ float pow2_int(int d) {
   // 2^d for an integer d <= 0; 0 below 2^-126 (such a slot weighs less than
   // 2^-90 of the row sum: the forward keeps every s of the maximal slot >= 1/2)
   return d < -126 ? 0.f : __int_as_float((127 + d) << 23);
 }
-__device__ __forceinline__ void df_warp_sum(float& hi, float& lo) {
+// Sum of a double-float pair over the 4 lanes of a group (every lane of the
+// group gets a sum; the group's first lane's is the one used).
+__device__ __forceinline__ void df_group_sum(float& hi, float& lo) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
+  for (int o = 1; o < kMergeLanes; o <<= 1) {
     const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
     const float ol = __shfl_xor_sync(0xffffffffu, lo, o);
     two_sum_acc(hi, lo, oh);
@@ -39,22 +48,26 @@ __device__ __forceinline__ bool row_has_forward(const MergeParams& p, int row) {
   return !p.tile_active || p.tile_active[row >> p.tile_shift];
 }
 
-// Merges row `row` (all 32 lanes of the warp take part) and writes its lse,
-// logp and entropy; returns the row's logp on lane 0 (NaN for a bad target).
-__device__ __forceinline__ double merge_row(const MergeParams& p, int row, int lane) {
-  const long long y = lane == 0 ? p.targets[row] : 0;   // issued early, used at the end
+// Merges `row` with the 4 lanes of this lane's group (sub = lane % 4; all 32
+// lanes of the warp must call it, with `row` < 0 for groups without a row)
+// and writes the row's lse, logp and entropy.  Returns the row's logp on the
+// group's first lane (NaN for a bad target), 0 elsewhere.
+__device__ __forceinline__ double merge_row(const MergeParams& p, int row, int sub) {
+  const bool live = row >= 0;
+  const long long y = (live && sub == 0) ? p.targets[row] : 0;   // issued early, used at the end
   const int slots = p.P_dev ? 2 * *p.P_dev : p.slots;
-  const float4* base = p.partial + size_t(row) * slots * 2;
+  const float4* base = p.partial + size_t(live ? row : 0) * slots * 2;
+  const int nk = live ? slots : 0;
   float M = -INFINITY;
-  for (int k = lane; k < slots; k += 32) {
+  for (int k = sub; k < nk; k += kMergeLanes) {
     const float4 a = base[2 * k];
     if (a.y + a.z > 0.f) M = fmaxf(M, a.x);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  for (int o = 1; o < kMergeLanes; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float shi = 0.f, slo = 0.f, whi = 0.f, wlo = 0.f, zy = 0.f;
   int found = 0;
-  for (int k = lane; k < slots; k += 32) {
+  for (int k = sub; k < nk; k += kMergeLanes) {
     const float4 a = base[2 * k];
     const float4 b = base[2 * k + 1];
     if (a.y + a.z > 0.f) {
@@ -73,17 +86,19 @@ __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int l
       found = 1;
     }
   }
-  df_warp_sum(shi, slo);
-  df_warp_sum(whi, wlo);
-  const unsigned who = __ballot_sync(0xffffffffu, found);
-  zy = __shfl_sync(0xffffffffu, zy, who ? __ffs(who) - 1 : 0);
-  if (lane != 0) return 0.0;
+  df_group_sum(shi, slo);
+  df_group_sum(whi, wlo);
+  const int lane = threadIdx.x & 31;
+  const unsigned gmask = 0xfu << (lane & ~3);
+  const unsigned who = __ballot_sync(0xffffffffu, found) & gmask;
+  zy = __shfl_sync(0xffffffffu, zy, who ? __ffs(who) - 1 : (lane & ~3));
+  if (!live || sub != 0) return 0.0;
   // log2 S = e + log2(mh) + log2(1 + slo/shi), with shi = 2^e mh, mh in
   // [1, 2) (S >= 1/2, so shi is a normal number): log2f on [1, 2) is within
   // an ulp of [0, 1); the last term is slo/shi/ln2 to first order
   // (|slo/shi| < 2^-23).  W/S = q + q_lo with q = whi/shi and the exact
   // division residual.  Both log2 S and log2 S - W/S are formed as fp32
-  // hi + lo pairs; fp64 (a narrow unit here) only joins and scales them.
+  // hi + lo pairs; fp64 only joins and scales them.
   const uint32_t sb = __float_as_uint(shi);
   const float e = float(int(sb >> 23) - 127);
   const float l2m = log2f(__uint_as_float((sb & 0x7fffffu) | 0x3f800000u));
