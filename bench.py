@@ -152,6 +152,20 @@ class ClockSampler:
                 "aligned_to_timed_region": aligned}
 
 
+def config_of(spec, world: int) -> dict:
+    """The workload description both arms print (synthetic inputs of this shape)."""
+    H, V = spec.H, spec.V
+    w_bytes = V * H * (4 if spec.dtype == "fp32" else 2)
+    return {"workload": spec.name, "B": spec.B, "T": spec.T, "H": H, "V": V,
+            "loss": "gmpo" if spec.loss_type == 0 else "gspo_token", "dtype_in": spec.dtype,
+            "eps_low": spec.eps_low, "eps_high": spec.eps_high, "beta": spec.beta,
+            "temperature": spec.temperature, "top_entropy_quantile": spec.top_entropy_quantile,
+            "bias": spec.has_bias,
+            "l2": (f"inputs larger than L2 (W is {w_bytes / 1e6:.0f} MB, dW {V * H * 4 / 1e6:.0f} MB)"
+                   if w_bytes > 129e6 else "inputs fit in L2 (not flushed between steps)"),
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest of each rank's ``x`` (time-like values: the slowest rank
     sets the whole job's time).  Works with nccl (device tensors) and gloo
@@ -315,8 +329,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": spec.name, "B": spec.B, "T": spec.T, "H": spec.H,
-                                              "V": spec.V, "loss": "gmpo"},
+            "data": "synthetic", "config": config_of(spec, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -542,15 +555,7 @@ def measure(args, index, dev, world, rank, local):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": spec.name, "B": spec.B, "T": spec.T, "H": H, "V": V,
-                       "loss": "gmpo" if spec.loss_type == R.GMPO else "gspo_token", "dtype_in": spec.dtype,
-                       "eps_low": spec.eps_low, "eps_high": spec.eps_high, "beta": spec.beta,
-                       "temperature": spec.temperature, "top_entropy_quantile": spec.top_entropy_quantile,
-                       "bias": spec.has_bias,
-                       "l2": (f"inputs larger than L2 (W is {inp.W.numel() * inp.W.element_size() / 1e6:.0f} MB, "
-                              f"dW {V * H * 4 / 1e6:.0f} MB)") if V * H * 2 > 129e6 else
-                             "inputs fit in L2 (not flushed between steps)",
-                       "parallelism": "replicas" if world > 1 else "single"},
+            "config": config_of(spec, world),
             "tc_peak_frac_6nhv": step_tflops / peak,
             "tc_tflops_6nhv": step_tflops,
             "forward_rows": fwd_rows,
