@@ -48,6 +48,25 @@ def _full_check(R, case, **cfg_kw):
     return out, res, stats
 
 
+EDGE_SHAPES = [
+    Workload("wide_h_2048", B=2, T=300, H=2048, V=3000, dtype="bf16", prompt_len=10, seed=121),
+    Workload("ragged_h_1040_bias", B=3, T=100, H=1040, V=1500, dtype="bf16", has_bias=True, bias_std=0.2,
+             prompt_len=5, seed=122),
+    Workload("many_short_sequences", B=300, T=3, H=64, V=500, dtype="bf16", prompt_len=1, seed=123),
+    Workload("many_short_gspo", B=257, T=4, H=64, V=300, dtype="bf16", loss_type=GSPO_TOKEN, eps_low=0.05,
+             eps_high=0.05, prompt_len=1, old_noise_std=0.05, seed=124),
+    Workload("one_token_sequence", B=1, T=1, H=64, V=257, dtype="bf16", prompt_len=0, seed=125),
+]
+
+
+@pytest.mark.parametrize("spec", EDGE_SHAPES, ids=[s.name for s in EDGE_SHAPES])
+def test_edge_shapes(R, spec):
+    """Hidden sizes that span several 448-wide dX/dW tiles (one ragged), many
+    sequences of a few tokens, and a single one-token sequence."""
+    case = Case(spec)
+    _full_check(R, case)
+
+
 def test_tiny_fp32_workload(R):
     case = Case(WORKLOADS[0])
     _full_check(R, case)
