@@ -52,6 +52,7 @@ def parse_args():
                          "gradients); e4m3 quantizes X and W per row first (outside the timed region)")
     ap.add_argument("--all-rows", action="store_true",
                     help="run the backward over every row (RLLOSS_FLAG_ALL_ROWS), for comparison")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
     ap.add_argument("--no-naive-memory", action="store_true",
                     help="skip the full-logits torch path run for the memory comparison")
     return ap.parse_args()
@@ -477,6 +478,32 @@ def measure(args, index, dev, world, rank, local):
     ms_step = ms / args.steps
     value = whole_job_rate(N, world, args.steps, ms / 1e3)
 
+    # ---- the same step captured once in a CUDA graph and replayed (every
+    # operation of a call is stream-ordered and allocation-free)
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        gms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
+        graph = {"ms_per_step": gms, "value": whole_job_rate(N, world, args.steps, gms * args.steps / 1e3),
+                 "unit": UNIT, "note": "one captured call replayed per step; kernels identical to the eager call"}
+        del g
+
     # ---- end to end through the public API with host buffers: every step
     # copies its inputs from pinned host memory and reads its loss and
     # metrics back.  The copies of step k+1 run on a copy stream while step k
@@ -568,6 +595,7 @@ def measure(args, index, dev, world, rank, local):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "pipeline": "step k+1's H2D copies overlap step k on a copy stream"},
             "gpu_launches": launches,
+            "cuda_graph": graph,
             "memory": {"library_workspace_bytes": ws_bytes, "allocated_during_call_bytes": call_alloc,
                        "naive_full_logits_peak_extra_bytes": naive_bytes,
                        "naive_fits": naive_bytes is not None, "naive_note": naive_note,

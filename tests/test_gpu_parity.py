@@ -10,7 +10,8 @@ import torch
 import oracle as O
 from lm_head_log_tma_gb300.workloads import GMPO, GSPO_TOKEN, WORKLOADS, Workload, make_inputs, random_entropies
 
-from parity import (EDGE, Case, check_grads, check_loss_and_metrics, check_rows, reconcile_loss)
+from parity import (EDGE, Case, cfg_of as parity_cfg, check_grads, check_loss_and_metrics, check_rows,
+                    reconcile_loss)
 
 pytestmark = pytest.mark.gpu
 
@@ -357,6 +358,45 @@ def test_forward_skips_fully_masked_tiles(R, spec):
     assert R.rlloss_get_forward_tiles(b["workspace"]) == tiles
     assert abs(a["loss"].item() - b["loss"].item()) <= 1e-6 * abs(b["loss"].item()) + 1e-9
     _grads_close(a, b)
+
+
+@pytest.mark.parametrize("spec", [MID[1], MID[2]], ids=["bias_k3kl", "entropy_mask"])
+def test_cuda_graph_capture_and_replay(R, spec):
+    """A fwd_bwd call captured in a CUDA graph (every operation of the call is
+    stream-ordered and allocation-free) replays to the eager call's bits, and
+    picks up new input values written in place between replays."""
+    case = Case(spec)
+    i = case.inp
+    c = lambda x: None if x is None else x.cuda()
+    X, W, b, y, old, ref, adv, mask = map(c, (i.X, i.W, i.b, i.targets, case.old, case.ref, i.adv, i.mask))
+    cfg = parity_cfg(R, spec)
+    ws = R.alloc_workspace(R.rlloss_workspace_bytes(cfg), "cuda")
+    eager = R.fwd_bwd(cfg, X, W, b, y, old, ref, adv, mask, workspace=ws, per_token=False)
+    ref_out = {k: v.clone() for k, v in eager.items() if k != "workspace" and v is not None}
+    outs = {k: v for k, v in eager.items() if k != "workspace"}
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        R.fwd_bwd(cfg, X, W, b, y, old, ref, adv, mask, workspace=ws, outputs=outs, per_token=False)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        R.fwd_bwd(cfg, X, W, b, y, old, ref, adv, mask, workspace=ws, outputs=outs, per_token=False)
+    for v in outs.values():
+        if v is not None:
+            v.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert R.rlloss_get_device_status(ws) == 0
+    for k, v in ref_out.items():
+        assert torch.equal(outs[k].view(torch.int32) if outs[k].dtype == torch.float32 else outs[k],
+                           v.view(torch.int32) if v.dtype == torch.float32 else v), k
+    adv.neg_()                                   # new advantages, same buffers
+    g.replay()
+    torch.cuda.synchronize()
+    fresh = R.fwd_bwd(cfg, X, W, b, y, old, ref, adv, mask, per_token=False)
+    for k in ("loss", "dX", "dW"):
+        assert torch.equal(outs[k], fresh[k]), k
 
 
 # ------------------------------------------------------------------ loss stage only
