@@ -35,7 +35,8 @@ struct FwdPolicy {
   static constexpr int kK16 = 4;
   static constexpr int kABytes = 128 * 64 * 2;
   static constexpr int kBBytes = (256 / PAIR) * 64 * 2;   // this CTA's share of the B rows
-  static constexpr int kExtraSmem = 0;
+  static constexpr int kColBytes = 2 * 128 * 4;   // per epilogue warp: its 128 columns' W scales and biases
+  static constexpr int kExtraSmem = kEpiWarps * kColBytes;
   static constexpr uint32_t kIdesc = F8 ? idesc_e4m3(kRows, 256) : idesc_bf16(kRows, 256, 0, 0);
   static constexpr int kKB = F8 ? 128 : 64;           // K elements per k-block (128 bytes per row)
   using Params = FwdParams;
@@ -44,6 +45,11 @@ struct FwdPolicy {
     float mref, s_hi, s_lo, w_hi, w_lo, zy;
     int found, y;
     float xs;     // F8: this row's X scale
+    // Per-column vectors (W scales, bias) of this warp's 128 columns, loaded
+    // one tile ahead so their L2 latency hides behind the current tile.
+    float4 pw, pb;
+    int pre_n0 = -1;       // tile whose columns pw / pb hold
+    int R = -1, P = 0;     // launch shape (for the next tile's columns)
   };
 
   // Row tiles and vocabulary segments of this launch: all R tiles with the
@@ -123,9 +129,35 @@ struct FwdPolicy {
     }
   }
 
+  // First column of the tile this CTA's epilogue handles after t (-1: none).
+  __device__ static int next_tile_n0(const Params& p, EpiState& e, const TileInfo& t) {
+    if (!t.last) return t.n0 + 256;
+    if (e.R < 0) shape(p, e.R, e.P);
+    const int u = t.unit + int(gridDim.x) / CL;
+    if (u >= e.R * e.P) return -1;
+    return int((long long)(u / e.R) * p.Vt / e.P) * 256;
+  }
+  // This lane's 4 of the warp's 128 column scales / biases of the tile at n0
+  // (the vectors are padded to whole 256-column tiles).
+  __device__ static void fetch_cols(const Params& p, EpiState& e, int n0, int half, int lane) {
+    const int c = n0 + half * 128 + 4 * lane;
+    if constexpr (F8) e.pw = __ldg(reinterpret_cast<const float4*>(p.ws2 + c));
+    if (p.bias2) e.pb = __ldg(reinterpret_cast<const float4*>(p.bias2 + c));
+  }
+
   __device__ static void epilogue(const Params& p, EpiState& e, const TileInfo& t, uint32_t taddr, int q, int half,
-                                  int lane, uint8_t*, uint32_t rank) {
+                                  int lane, uint8_t* extra, uint32_t rank) {
     const int row = t.m0 + 128 * int(rank) + q * 32 + lane;
+    float* cols = reinterpret_cast<float*>(extra + (q + 4 * half) * kColBytes);   // [128 scales][128 biases]
+    if (F8 || p.bias2) {
+      if (e.pre_n0 != t.n0) fetch_cols(p, e, t.n0, half, lane);
+      __syncwarp();
+      if constexpr (F8) reinterpret_cast<float4*>(cols)[lane] = e.pw;
+      if (p.bias2) reinterpret_cast<float4*>(cols + 128)[lane] = e.pb;
+      __syncwarp();
+      e.pre_n0 = next_tile_n0(p, e, t);
+      if (e.pre_n0 >= 0) fetch_cols(p, e, e.pre_n0, half, lane);
+    }
     if (t.first) {
       e.mref = -INFINITY;
       e.s_hi = e.s_lo = e.w_hi = e.w_lo = 0.f;
@@ -143,22 +175,22 @@ struct FwdPolicy {
       tmem_ld32(taddr + uint32_t(half * 128 + ch * 32), v);
       if constexpr (F8) {
         // logit * log2(e)/tau = acc * xs[row] * (ws[col] * log2(e)/tau) (+ b * log2(e)/tau)
-        const float4* w4 = reinterpret_cast<const float4*>(p.ws2 + c0);
-        const float4* b4 = reinterpret_cast<const float4*>(p.bias2 + c0);
+        const float4* w4 = reinterpret_cast<const float4*>(cols + ch * 32);
+        const float4* b4 = reinterpret_cast<const float4*>(cols + 128 + ch * 32);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 w = __ldg(w4 + i);
-          const float4 b = p.bias2 ? __ldg(b4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 w = w4[i];
+          const float4 b = p.bias2 ? b4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
           v[4 * i + 0] = fmaf(v[4 * i + 0] * e.xs, w.x, b.x);
           v[4 * i + 1] = fmaf(v[4 * i + 1] * e.xs, w.y, b.y);
           v[4 * i + 2] = fmaf(v[4 * i + 2] * e.xs, w.z, b.z);
           v[4 * i + 3] = fmaf(v[4 * i + 3] * e.xs, w.w, b.w);
         }
       } else if (p.bias2) {
-        const float4* b4 = reinterpret_cast<const float4*>(p.bias2 + c0);
+        const float4* b4 = reinterpret_cast<const float4*>(cols + 128 + ch * 32);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 b = __ldg(b4 + i);
+          const float4 b = b4[i];
           v[4 * i + 0] = fmaf(v[4 * i + 0], sc, b.x);
           v[4 * i + 1] = fmaf(v[4 * i + 1], sc, b.y);
           v[4 * i + 2] = fmaf(v[4 * i + 2], sc, b.z);

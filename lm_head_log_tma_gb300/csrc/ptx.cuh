@@ -210,8 +210,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Arrive on an mbarrier of a CTA of this cluster.  Used only to report a
+// drained TMEM accumulator: the arriving warp's tcgen05.ld already completed
+// (tcgen05.wait::ld) and was fenced (tcgen05.fence::before_thread_sync), and
+// no memory the waiter reads is published through it, so the default
+// CTA-scope release is enough (a cluster-scope release costs a memory
+// barrier per epilogue warp per tile).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA of the pair.
