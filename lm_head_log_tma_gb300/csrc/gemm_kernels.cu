@@ -252,7 +252,7 @@ struct FwdPolicy {
   __device__ static void epilogue_finish(const Params&, int) {}
 };
 
-// Four lanes per row: see merge_row.cuh.
+// kMergeLanes lanes per row: see merge_row.cuh.
 __global__ void fwd_merge_kernel(MergeParams p) {
   const int r = int((blockIdx.x * (long long)blockDim.x + threadIdx.x) / kMergeLanes);
   const bool live = r < p.N && row_has_forward(p, r);
@@ -760,7 +760,8 @@ cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st
 }
 cudaError_t launch_gemmH(const HParams& p, int units, cudaStream_t st) { return launch_engine<HPolicy>(p, units, st); }
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
-  fwd_merge_kernel<<<(p.N + 63) / 64, 256, 0, st>>>(p);   // 64 rows per block
+  constexpr int rows = 256 / kMergeLanes;   // rows per 256-thread block
+  fwd_merge_kernel<<<(p.N + rows - 1) / rows, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st) {

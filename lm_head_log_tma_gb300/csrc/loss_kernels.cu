@@ -133,7 +133,7 @@ cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long
 
 // ----------------------------------------------------------------------- K2
 constexpr int kLossThreads = 256;
-constexpr int kFusedRows = 64;     // rows per block of the fused merge + loss kernel (8 per warp, 4 lanes each)
+constexpr int kFusedRows = 256 / kMergeLanes;   // rows per block of the fused merge + loss kernel
 constexpr int kRec = 10;           // doubles per sequence record
 
 template <int K>

@@ -18,12 +18,13 @@ namespace rl {
 // Scaling by 2^(m_k-M) is exact in fp32, the sums are carried as
 // double-float (hi + lo) pairs, and only the final row values use fp64.
 //
-// Four lanes merge one row (a warp holds 8 rows): each lane takes every
-// fourth slot, the group combines with two shuffle steps, and the group's
-// first lane finishes the row, so the per-row fp64 work runs for 8 rows at
-// once (fp64 is a narrow unit on this GPU; a warp instruction costs the same
-// with one active lane as with eight).
-constexpr int kMergeLanes = 4;
+// Eight lanes merge one row (a warp holds 4 rows): each lane takes every
+// eighth slot, with the slot loops unrolled so a lane's loads are in flight
+// together (the merge is bound by load latency), the group combines with
+// three shuffle steps, and the group's first lane finishes the row, so the
+// per-row fp64 work runs for 4 rows at once (fp64 is a narrow unit on this
+// GPU; a warp instruction costs the same with one active lane as with four).
+constexpr int kMergeLanes = 8;
 constexpr int kMergeRowsPerWarp = 32 / kMergeLanes;
 
 __device__ __forceinline__ float pow2_int(int d) {
@@ -31,7 +32,7 @@ __device__ __forceinline__ float pow2_int(int d) {
   // 2^-90 of the row sum: the forward keeps every s of the maximal slot >= 1/2)
   return d < -126 ? 0.f : __int_as_float((127 + d) << 23);
 }
-// Sum of a double-float pair over the 4 lanes of a group (every lane of the
+// Sum of a double-float pair over the lanes of a group (every lane of the
 // group gets a sum; the group's first lane's is the one used).
 __device__ __forceinline__ void df_group_sum(float& hi, float& lo) {
 #pragma unroll
@@ -48,7 +49,7 @@ __device__ __forceinline__ bool row_has_forward(const MergeParams& p, int row) {
   return !p.tile_active || p.tile_active[row >> p.tile_shift];
 }
 
-// Merges `row` with the 4 lanes of this lane's group (sub = lane % 4; all 32
+// Merges `row` with the lanes of this lane's group (sub = lane % kMergeLanes; all 32
 // lanes of the warp must call it, with `row` < 0 for groups without a row)
 // and writes the row's lse, logp and entropy.  Returns the row's logp on the
 // group's first lane (NaN for a bad target), 0 elsewhere.
@@ -59,6 +60,7 @@ __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int s
   const float4* base = p.partial + size_t(live ? row : 0) * slots * 2;
   const int nk = live ? slots : 0;
   float M = -INFINITY;
+#pragma unroll 4
   for (int k = sub; k < nk; k += kMergeLanes) {
     const float4 a = base[2 * k];
     if (a.y + a.z > 0.f) M = fmaxf(M, a.x);
@@ -67,6 +69,7 @@ __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int s
   for (int o = 1; o < kMergeLanes; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float shi = 0.f, slo = 0.f, whi = 0.f, wlo = 0.f, zy = 0.f;
   int found = 0;
+#pragma unroll 4
   for (int k = sub; k < nk; k += kMergeLanes) {
     const float4 a = base[2 * k];
     const float4 b = base[2 * k + 1];
@@ -89,9 +92,10 @@ __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int s
   df_group_sum(shi, slo);
   df_group_sum(whi, wlo);
   const int lane = threadIdx.x & 31;
-  const unsigned gmask = 0xfu << (lane & ~3);
+  const int g0 = lane & ~(kMergeLanes - 1);   // first lane of this group
+  const unsigned gmask = ((1u << kMergeLanes) - 1u) << g0;
   const unsigned who = __ballot_sync(0xffffffffu, found) & gmask;
-  zy = __shfl_sync(0xffffffffu, zy, who ? __ffs(who) - 1 : (lane & ~3));
+  zy = __shfl_sync(0xffffffffu, zy, who ? __ffs(who) - 1 : g0);
   if (!live || sub != 0) return 0.0;
   // log2 S = e + log2(mh) + log2(1 + slo/shi), with shi = 2^e mh, mh in
   // [1, 2) (S >= 1/2, so shi is a normal number): log2f on [1, 2) is within
