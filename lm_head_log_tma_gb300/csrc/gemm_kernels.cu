@@ -167,12 +167,22 @@ struct FwdPolicy {
       if constexpr (F8) e.xs = row < p.N ? p.xs[row] : 0.f;
     }
     const float sc = p.scale2;
+    // This warp's 32-column chunks that hold vocabulary columns; the TMEM load
+    // of chunk ch+1 is in flight while chunk ch is processed.
+    const int cbase = t.n0 + half * 128;
+    const int nch = min(4, max(0, (p.V - cbase + 31) / 32));
+    uint32_t r[32];
+    if (nch > 0) {
+      tmem_ld32_issue(taddr + uint32_t(half * 128), r);
+      tmem_ld32_wait(r);
+    }
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
-      const int c0 = t.n0 + half * 128 + ch * 32;
-      if (c0 >= p.V) break;
+    for (int ch = 0; ch < nch; ++ch) {
+      const int c0 = cbase + ch * 32;
       float v[32];
-      tmem_ld32(taddr + uint32_t(half * 128 + ch * 32), v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      if (ch + 1 < nch) tmem_ld32_issue(taddr + uint32_t(half * 128 + (ch + 1) * 32), r);
       if constexpr (F8) {
         // logit * log2(e)/tau = acc * xs[row] * (ws[col] * log2(e)/tau) (+ b * log2(e)/tau)
         const float4* w4 = reinterpret_cast<const float4*>(cols + ch * 32);
@@ -196,18 +206,20 @@ struct FwdPolicy {
           v[4 * i + 2] = fmaf(v[4 * i + 2], sc, b.z);
           v[4 * i + 3] = fmaf(v[4 * i + 3], sc, b.w);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = v[i] * sc;
       }
-      if (c0 + 32 > p.V) {
+      // Without bias or e4m3 scales v is still the raw logit; its scale to
+      // log2 units folds into the FFMA that forms t - m below (mul = sc).
+      const float mul = (F8 || p.bias2) ? 1.f : sc;
+      const bool tail = c0 + 32 > p.V;   // columns past V: out of the max, weight 0
+      if (tail) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (c0 + i >= p.V) v[i] = -3.0e38f;
+          if (c0 + i >= p.V) v[i] = -INFINITY;
       }
       float mx = v[0];
 #pragma unroll
       for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
+      mx *= mul;   // mul > 0
       // Reference max kept on an integer grid in log2 units; move it only
       // when a logit would exceed it by more than 2^16, so rescaling is rare
       // and exact (a power of two).
@@ -228,7 +240,12 @@ struct FwdPolicy {
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
-        const float d0 = v[i] - e.mref, d1 = v[i + 1] - e.mref, d2 = v[i + 2] - e.mref, d3 = v[i + 3] - e.mref;
+        const float nm = -e.mref;
+        float d0 = fmaf(v[i], mul, nm), d1 = fmaf(v[i + 1], mul, nm), d2 = fmaf(v[i + 2], mul, nm),
+              d3 = fmaf(v[i + 3], mul, nm);
+        if (tail) {   // -inf -> a finite large negative: 2^d = 0 and 0 * d = 0
+          d0 = fmaxf(d0, -1.0e30f); d1 = fmaxf(d1, -1.0e30f); d2 = fmaxf(d2, -1.0e30f); d3 = fmaxf(d3, -1.0e30f);
+        }
         const float x0 = ex2_approx(d0), x1 = ex2_approx(d1), x2 = ex2_approx(d2), x3 = ex2_approx(d3);
         s0 += x0; s1 += x1; s2 += x2; s3 += x3;
         w0 = fmaf(x0, d0, w0); w1 = fmaf(x1, d1, w1); w2 = fmaf(x2, d2, w2); w3 = fmaf(x3, d3, w3);
@@ -239,9 +256,10 @@ struct FwdPolicy {
       if (ty < 32u) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (unsigned(i) == ty) e.zy = v[i];
+          if (unsigned(i) == ty) e.zy = v[i] * mul;
         e.found = 1;
       }
+      if (ch + 1 < nch) tmem_ld32_wait(r);
     }
     if (t.last && row < p.N) {
       float4* dst = p.partial + (size_t(row) * (2 * t.aux) + size_t(t.seg) * 2 + half) * 2;
