@@ -57,6 +57,8 @@ EDGE_SHAPES = [
     Workload("many_short_gspo", B=257, T=4, H=64, V=300, dtype="bf16", loss_type=GSPO_TOKEN, eps_low=0.05,
              eps_high=0.05, prompt_len=1, old_noise_std=0.05, seed=124),
     Workload("one_token_sequence", B=1, T=1, H=64, V=257, dtype="bf16", prompt_len=0, seed=125),
+    Workload("narrow_h_8", B=2, T=90, H=8, V=700, dtype="bf16", prompt_len=5, seed=126),
+    Workload("large_vocab_70001", B=1, T=300, H=128, V=70001, dtype="bf16", prompt_len=20, seed=127),
 ]
 
 
