@@ -121,6 +121,8 @@ struct Plan {
   bool compact;             // backward over the rows with c_n != 0 only
   int R, Vt, P, pcap, Hp, Vp;
   int kb_fwd, nseg_fwd;     // forward K: nseg_fwd * kb_fwd k-blocks
+  int kbx;                  // 128-byte boxes per operand per stage of the forward and recompute
+  int kb_dl;                // recompute K-blocks per product term
   int Kx;                   // row width (elements) of the bf16 X / W operand arrays
   int Nc, nchunks, ld_dl;
   // workspace offsets
@@ -178,19 +180,24 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.P = choose_segments(p.R, p.Vt, p.fwd_clusters, p.pcap);
     p.Hp = int(rup(p.H, 64));
     p.Vp = int(rup(p.V, 64));
+    // Stages hold two 128-byte boxes per operand with CTA pairs and one K
+    // segment (bf16, e4m3), one box otherwise (fp32 split terms: K segments
+    // of Hp elements; single-CTA tiles).
+    p.kbx = (p.pair == 2 && !p.fp32) ? 2 : 1;
     if (p.fp32) {
       p.nseg_fwd = 6;
       p.kb_fwd = p.Hp / 64;
       p.Kx = 3 * p.Hp;
     } else if (p.f8) {
       p.nseg_fwd = 1;
-      p.kb_fwd = int(cdiv(p.H, 128));   // 128 e4m3 elements = 128 bytes per k-block row
+      p.kb_fwd = int(cdiv(p.H, 128 * p.kbx));   // 128 e4m3 elements per 128-byte box row
       p.Kx = p.H;
     } else {
       p.nseg_fwd = 1;
-      p.kb_fwd = int(cdiv(p.H, 64));
+      p.kb_fwd = int(cdiv(p.H, 64 * p.kbx));
       p.Kx = p.H;
     }
+    p.kb_dl = p.fp32 ? p.Hp / 64 : int(cdiv(p.H, 64 * p.kbx));
     p.o_partial = take(size_t(p.N) * 2 * p.pcap * 32);   // room for a segment count chosen on the device
     p.o_lse2 = take(size_t(p.N) * 4);
     p.o_logp64 = take(size_t(p.N) * 8);
@@ -512,7 +519,7 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
   fp.limit_ns = kWaitLimitNs;
   {
     Phase ph(st, 0);
-    RL_TRY(launch_fwd(fp, p.R * p.P, p.pair, st));
+    RL_TRY(launch_fwd(fp, p.R * p.P, p.pair, p.kbx, st));
     ph.launched();
   }
   MergeParams& mp = h.mp;
@@ -844,7 +851,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     dp.tmA = tm_xb;
     dp.tmB = fp.tmB;
     dp.nseg = fp.nseg;
-    dp.kb_per_seg = fp.kb_per_seg;
+    dp.kb_per_seg = p.kb_dl;
     std::memcpy(dp.seg_a, hd.seg_a, sizeof(hd.seg_a));
     std::memcpy(dp.seg_b, hd.seg_b, sizeof(hd.seg_b));
     dp.n0 = n0;
@@ -869,7 +876,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     dp.limit_ns = kWaitLimitNs;
     {
       Phase ph(st, 2);
-      RL_TRY(launch_dl(dp, Rc * p.Vt, p.pair, st));
+      RL_TRY(launch_dl(dp, Rc * p.Vt, p.pair, p.kbx, st));
       ph.launched();
     }
 

@@ -22,23 +22,27 @@ namespace rl {
 // =============================================================== forward
 // CL = 1: 128-row tiles on one CTA; CL = 2: 256-row tiles over a CTA pair
 // (cta_group::2).  F8: e4m3 operands (forward-only scoring) with per-row
-// scales of X and W applied in the epilogue; a k-block is then 128 elements
-// (the same 128 bytes per row) and each MMA step covers K = 32.
-template <int CL, bool F8 = false>
+// scales of X and W applied in the epilogue; a 128-byte box row is then 128
+// elements and each MMA step covers K = 32.  KBX: 128-byte boxes per operand
+// in a pipeline stage (2 for pair tiles with one K segment: half as many,
+// twice as deep stages, which halves the per-stage barrier round trips the
+// MMA issuer waits on — measured 9% on the bf16 forward).
+template <int CL, bool F8 = false, int KBX = 1>
 struct FwdPolicy {
   static constexpr int kCluster = CL;
   static constexpr int PAIR = CL >= 2 ? 2 : 1;
   static constexpr int kRows = 128 * CL;             // accumulator rows per tile (whole cluster)
-  static constexpr int kStages = PAIR == 2 ? 6 : 4;
+  static constexpr int kStages = (PAIR == 2 ? 6 : 4) / KBX;
   static constexpr int kSubs = 1;
   static constexpr int kBN = 256;
-  static constexpr int kK16 = 4;
-  static constexpr int kABytes = 128 * 64 * 2;
-  static constexpr int kBBytes = (256 / PAIR) * 64 * 2;   // this CTA's share of the B rows
+  static constexpr int kK16 = 4 * KBX;
+  static constexpr int kBox = 128 * 128;                    // one 128-row x 128-byte operand box
+  static constexpr int kABytes = kBox * KBX;
+  static constexpr int kBBytes = (256 / PAIR) * 128 * KBX;   // this CTA's share of the B rows
   static constexpr int kColBytes = 2 * 128 * 4;   // per epilogue warp: its 128 columns' W scales and biases
   static constexpr int kExtraSmem = kEpiWarps * kColBytes;
   static constexpr uint32_t kIdesc = F8 ? idesc_e4m3(kRows, 256) : idesc_bf16(kRows, 256, 0, 0);
-  static constexpr int kKB = F8 ? 128 : 64;           // K elements per k-block (128 bytes per row)
+  static constexpr int kKB = (F8 ? 128 : 64) * KBX;   // K elements per k-block
   using Params = FwdParams;
 
   struct EpiState {
@@ -102,16 +106,24 @@ struct FwdPolicy {
     const int s = kb / p.kb_per_seg;
     const int kk = (kb - s * p.kb_per_seg) * kKB;
     if constexpr (CL == 2) {
-      tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0 + 128 * int(rank));
-      tma_load_2d_pair(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0 + 128 * int(rank));
+      constexpr int kBoxK = kKB / KBX;   // K elements of one 128-byte box row
+#pragma unroll
+      for (int x = 0; x < KBX; ++x) {
+        tma_load_2d_pair(&p.tmA, bar, st + x * kBox, p.seg_a[s] + kk + kBoxK * x, t.m0 + 128 * int(rank));
+        tma_load_2d_pair(&p.tmB, bar, st + kABytes + x * kBox, p.seg_b[s] + kk + kBoxK * x, t.n0 + 128 * int(rank));
+      }
     } else {
+      static_assert(KBX == 1, "single-CTA tiles keep one box per operand");
       tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0);
       tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
     }
   }
-  __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo&) { return sdesc_sw128(sa + k * 32, 16, 1024); }
+  // MMA step k (32 bytes of K each) of the stage: box k / 4, byte offset 32 (k % 4).
+  __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo&) {
+    return sdesc_sw128(sa + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
+  }
   __device__ static uint64_t bdesc(uint32_t sa, int k, const TileInfo&) {
-    return sdesc_sw128(sa + kABytes + k * 32, 16, 1024);
+    return sdesc_sw128(sa + kABytes + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
   }
   __device__ static uint32_t idesc(const TileInfo&) { return kIdesc; }
   static constexpr int kAccBufs = 2;
@@ -300,17 +312,18 @@ __device__ __forceinline__ float warp_column_sum(float (&v)[32], int lane) {
   return v[0];
 }
 
-template <int CL>
+template <int CL, int KBX = 1>   // KBX: as for FwdPolicy
 struct DlPolicy {
   static constexpr int kCluster = CL;
   static constexpr int PAIR = CL >= 2 ? 2 : 1;
   static constexpr int kRows = 128 * CL;
-  static constexpr int kStages = PAIR == 2 ? 6 : 4;
+  static constexpr int kStages = (PAIR == 2 ? 6 : 4) / KBX;
   static constexpr int kSubs = 1;
   static constexpr int kBN = 256;
-  static constexpr int kK16 = 4;
-  static constexpr int kABytes = 128 * 64 * 2;
-  static constexpr int kBBytes = (256 / PAIR) * 64 * 2;
+  static constexpr int kK16 = 4 * KBX;
+  static constexpr int kBox = 128 * 128;                    // one 128-row x 128-byte operand box
+  static constexpr int kABytes = kBox * KBX;
+  static constexpr int kBBytes = (256 / PAIR) * 128 * KBX;
   static constexpr int kStageBuf = 32 * 64;        // one 32-row x 32-column bf16 box, 64-byte swizzle
   static constexpr int kExtraSmem = kEpiWarps * 2 * kStageBuf;
   static constexpr uint32_t kIdesc = idesc_bf16(kRows, 256, 0, 0);
@@ -343,18 +356,24 @@ struct DlPolicy {
   }
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int s = kb / p.kb_per_seg;
-    const int kk = (kb - s * p.kb_per_seg) * 64;
+    const int kk = (kb - s * p.kb_per_seg) * 64 * KBX;
     if constexpr (CL == 2) {
-      tma_load_2d_pair(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0 + 128 * int(rank));
-      tma_load_2d_pair(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0 + 128 * int(rank));
+#pragma unroll
+      for (int x = 0; x < KBX; ++x) {
+        tma_load_2d_pair(&p.tmA, bar, st + x * kBox, p.seg_a[s] + kk + 64 * x, p.n0 + t.m0 + 128 * int(rank));
+        tma_load_2d_pair(&p.tmB, bar, st + kABytes + x * kBox, p.seg_b[s] + kk + 64 * x, t.n0 + 128 * int(rank));
+      }
     } else {
+      static_assert(KBX == 1, "single-CTA tiles keep one box per operand");
       tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0);
       tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
     }
   }
-  __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo&) { return sdesc_sw128(sa + k * 32, 16, 1024); }
+  __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo&) {
+    return sdesc_sw128(sa + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
+  }
   __device__ static uint64_t bdesc(uint32_t sa, int k, const TileInfo&) {
-    return sdesc_sw128(sa + kABytes + k * 32, 16, 1024);
+    return sdesc_sw128(sa + kABytes + (k >> 2) * kBox + (k & 3) * 32, 16, 1024);
   }
   __device__ static uint32_t idesc(const TileInfo&) { return kIdesc; }
   static constexpr int kAccBufs = 2;
@@ -759,22 +778,24 @@ static cudaError_t launch_engine(const typename P::Params& prm, int units, cudaS
 
 int fwd_resident_clusters(int cluster) {
   cudaError_t e;
-  return cluster == 2 ? engine_resident<FwdPolicy<2>>(&e) : engine_resident<FwdPolicy<1>>(&e);
+  return cluster == 2 ? engine_resident<FwdPolicy<2, false, 2>>(&e) : engine_resident<FwdPolicy<1>>(&e);
 }
 int dl_resident_clusters(int cluster) {
   cudaError_t e;
-  return cluster == 2 ? engine_resident<DlPolicy<2>>(&e) : engine_resident<DlPolicy<1>>(&e);
+  return cluster == 2 ? engine_resident<DlPolicy<2, 2>>(&e) : engine_resident<DlPolicy<1>>(&e);
 }
 int gemmH_resident_clusters() {
   cudaError_t e;
   return engine_resident<HPolicy>(&e);
 }
-cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, cudaStream_t st) {
-  if (p.xs) return launch_engine<FwdPolicy<2, true>>(p, units, st);   // e4m3 operands: CTA pairs only
-  return cluster == 2 ? launch_engine<FwdPolicy<2>>(p, units, st) : launch_engine<FwdPolicy<1>>(p, units, st);
+cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, int kbx, cudaStream_t st) {
+  if (p.xs) return launch_engine<FwdPolicy<2, true, 2>>(p, units, st);   // e4m3 operands: CTA pairs only
+  if (cluster == 1) return launch_engine<FwdPolicy<1>>(p, units, st);
+  return kbx == 2 ? launch_engine<FwdPolicy<2, false, 2>>(p, units, st) : launch_engine<FwdPolicy<2>>(p, units, st);
 }
-cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st) {
-  return cluster == 2 ? launch_engine<DlPolicy<2>>(p, units, st) : launch_engine<DlPolicy<1>>(p, units, st);
+cudaError_t launch_dl(const DlParams& p, int units, int cluster, int kbx, cudaStream_t st) {
+  if (cluster == 1) return launch_engine<DlPolicy<1>>(p, units, st);
+  return kbx == 2 ? launch_engine<DlPolicy<2, 2>>(p, units, st) : launch_engine<DlPolicy<2>>(p, units, st);
 }
 cudaError_t launch_gemmH(const HParams& p, int units, cudaStream_t st) { return launch_engine<HPolicy>(p, units, st); }
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {

@@ -150,9 +150,10 @@ struct LossParams {
 int fwd_resident_clusters(int cluster);
 int dl_resident_clusters(int cluster);
 int gemmH_resident_clusters();
-cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, cudaStream_t st);
+// kbx: 128-byte boxes per operand per pipeline stage (2: pair tiles with one K segment)
+cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, int kbx, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
-cudaError_t launch_dl(const DlParams& p, int units, int cluster, cudaStream_t st);
+cudaError_t launch_dl(const DlParams& p, int units, int cluster, int kbx, cudaStream_t st);
 cudaError_t launch_gemmH(const HParams& p, int units, cudaStream_t st);
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st);
 cudaError_t launch_split3(const float* src, long long rows, int cols, int Cp, __nv_bfloat16* out, cudaStream_t st);
