@@ -101,6 +101,13 @@ extern "C" {
                                                 ...", Details: the gradients are sums over tokens
                                                 of c_n times per-token terms).  Same results up to
                                                 fp32 summation order; for comparison */
+#define RLLOSS_FLAG_ACCUMULATE 0x10u         /* rlloss_fwd_bwd adds its gradients to the values
+                                                already in dX, dW and db instead of overwriting
+                                                them (gradient accumulation over micro-batches).
+                                                Each element receives the call's contribution in a
+                                                fixed order, so repeated calls from the same
+                                                initial values give the same bits.  Ignored by the
+                                                forward-only entries */
 
 #define RLLOSS_NMETRICS 8
 /* out_metrics layout:
@@ -144,6 +151,7 @@ size_t rlloss_loss_workspace_bytes(const rlloss_cfg* cfg);
 
 /* The whole fused path: forward (LM head + streamed log-softmax, target
  * log-prob, entropy), entropy mask, loss and metrics, and backward.
+ * dX, dW and db are overwritten, or added to with RLLOSS_FLAG_ACCUMULATE.
  *   X, W: [N,H], [V,H] of cfg.dtype; b: [V] or NULL when !has_bias.
  *   targets [N] int64; old_logp [N]; ref_logp [N] (NULL when beta == 0);
  *   adv [B]; mask [N].

@@ -66,7 +66,7 @@ int validate_common(const rlloss_cfg* c) {
   const float q = c->top_entropy_quantile;
   if (!(q >= 0.f && q <= 1.f)) return RLLOSS_EINVAL;
   if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN |
-                   RLLOSS_FLAG_ALL_ROWS))
+                   RLLOSS_FLAG_ALL_ROWS | RLLOSS_FLAG_ACCUMULATE))
     return RLLOSS_EINVAL;
   if ((c->flags & RLLOSS_FLAG_ADV_PER_TOKEN) && c->loss_type != RLLOSS_GSPO_TOKEN) return RLLOSS_EUNSUPPORTED;
   if (c->loss_type == RLLOSS_GSPO_TOKEN) {
@@ -82,7 +82,7 @@ int validate_head(const rlloss_cfg* c) {
   if (c->B < 1 || c->T < 1) return RLLOSS_EINVAL;
   if ((long long)c->B * c->T > (1ll << 31) - 1) return RLLOSS_EINVAL;
   if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN |
-                   RLLOSS_FLAG_ALL_ROWS))
+                   RLLOSS_FLAG_ALL_ROWS | RLLOSS_FLAG_ACCUMULATE))
     return RLLOSS_EINVAL;
   if (c->H < 1 || c->V < 1) return RLLOSS_EINVAL;
   if (c->dtype != RLLOSS_BF16 && c->dtype != RLLOSS_FP32 && c->dtype != RLLOSS_FP8_E4M3) return RLLOSS_EINVAL;
@@ -794,7 +794,10 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   // for the dense backward they are dropped first (ordered compaction), the
   // chunks run over the kept rows, and dX rows are scattered back (the rest
   // of dX is zero).  The kept-row count stays on the device: every backward
-  // kernel reads it, and chunks past it do no work.
+  // kernel reads it, and chunks past it do no work.  With ACCUMULATE every
+  // output element still receives one addition per chunk (dX rows: one per
+  // call), so the sums keep a fixed order.
+  const bool acc = (cfg->flags & RLLOSS_FLAG_ACCUMULATE) != 0;
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dl);
   const int lo_off = p.fp32 ? p.Vp : 0;
   int* rows_total = reinterpret_cast<int*>(ws + p.o_status + kBackwardRowsOffset);
@@ -826,7 +829,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       cp.tgtc = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
       cp.xc = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
       RL_TRY(launch_compact(cp, st));
-      RL_TRY(cudaMemsetAsync(dX, 0, size_t(p.N) * p.H * 4, st));
+      if (!acc) RL_TRY(cudaMemsetAsync(dX, 0, size_t(p.N) * p.H * 4, st));
       ph.launched(2);
       Xb = cp.xc;
       tg_b = cp.tgtc;
@@ -903,8 +906,13 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       px.Hout = p.H;
       px.order = 0;
       px.a_mn = 0;
-      px.ksplit = hp.nseg * px.kb_per_seg >= 2 ? 2 : 1;
-      px.reduce = px.ksplit == 2 ? 1 : 0;
+      // Two k halves reduce-added onto a zeroed buffer (two addends: the same
+      // sum in either order); accumulating straight into dX takes one
+      // unsplit reduce-add instead, since a third addend would make the
+      // result depend on the order of the halves.
+      const bool dx_in_place_acc = acc && !p.compact;
+      px.ksplit = (hp.nseg * px.kb_per_seg >= 2 && !dx_in_place_acc) ? 2 : 1;
+      px.reduce = (px.ksplit == 2 || dx_in_place_acc) ? 1 : 0;
       HProblem& pw = hp.pr[1];
       pw.kb_per_seg = int(cdiv(nc, 64));
       pw.a_outer0 = 0;
@@ -914,7 +922,7 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       pw.Hout = p.H;
       pw.order = 1;
       pw.a_mn = 1;
-      pw.reduce = ch > 0 ? 1 : 0;
+      pw.reduce = (ch > 0 || acc) ? 1 : 0;
       pw.ksplit = 1;
       hp.nprob = 2;
       const int kx = hp.nseg * px.kb_per_seg / px.ksplit, kw = hp.nseg * pw.kb_per_seg;
@@ -925,17 +933,17 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
       hp.status = status;
       hp.limit_ns = kWaitLimitNs;
       Phase ph(st, 3);
-      if (px.reduce) RL_TRY(cudaMemsetAsync(dx_out, 0, size_t(nc) * p.H * 4, st));
+      if (px.reduce && !dx_in_place_acc) RL_TRY(cudaMemsetAsync(dx_out, 0, size_t(nc) * p.H * 4, st));
       RL_TRY(launch_gemmH(hp, px.Mt * px.Ht * px.ksplit + pw.Mt * pw.Ht, st));
       ph.launched();
       if (p.compact) {
-        RL_TRY(launch_scatter_rows(dxc, cidx, rows_total, n0, nc, p.H, dX, st));
+        RL_TRY(launch_scatter_rows(dxc, cidx, rows_total, n0, nc, p.H, dX, acc, st));
         ph.launched();
       }
     }
     if (p.bias) {
       Phase ph(st, 5);
-      RL_TRY(launch_db_reduce(reinterpret_cast<float*>(ws + p.o_dbpart), rows_total, n0, nc, p.V, db, ch > 0, st));
+      RL_TRY(launch_db_reduce(reinterpret_cast<float*>(ws + p.o_dbpart), rows_total, n0, nc, p.V, db, ch > 0 || acc, st));
       ph.launched();
     }
   }

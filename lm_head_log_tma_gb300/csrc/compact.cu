@@ -161,13 +161,19 @@ cudaError_t launch_tile_scan(const uint8_t* mask, int N, int tile_rows, uint8_t*
 __global__ void set_total_kernel(int* total, int N) { *total = N; }
 
 __global__ void scatter_rows_kernel(const float4* src, const int* idx, const int* total, int n0, int nc_max, int H4,
-                                    float4* dst) {
+                                    float4* dst, int accumulate) {
   const int nc = min(max(*total - n0, 0), nc_max);
   const long long n = (long long)nc * H4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const long long j = i / H4;
     const int c = int(i - j * H4);
-    dst[(long long)idx[n0 + j] * H4 + c] = src[i];
+    float4* d = dst + (long long)idx[n0 + j] * H4 + c;
+    float4 v = src[i];
+    if (accumulate) {   // each kept row appears once: a plain read-modify-write
+      const float4 o = *d;
+      v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+    }
+    *d = v;
   }
 }
 
@@ -185,13 +191,13 @@ cudaError_t launch_set_total(int* total, int N, cudaStream_t st) {
 }
 
 cudaError_t launch_scatter_rows(const float* src, const int* idx, const int* total, int n0, int nc_max, int H,
-                                float* dst, cudaStream_t st) {
+                                float* dst, bool accumulate, cudaStream_t st) {
   const long long n = (long long)nc_max * (H / 4);
   long long blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
   scatter_rows_kernel<<<int(blocks), 256, 0, st>>>(reinterpret_cast<const float4*>(src), idx, total, n0, nc_max,
-                                                   H / 4, reinterpret_cast<float4*>(dst));
+                                                   H / 4, reinterpret_cast<float4*>(dst), accumulate ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -183,9 +183,9 @@ cudaError_t launch_tile_scan(const uint8_t* mask, int N, int tile_rows, uint8_t*
                              unsigned int* ticket, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t st);
 cudaError_t launch_set_total(int* total, int N, cudaStream_t st);
-// dst[idx[n0 + j]][:] = src[j][:] for j < clamp(*total - n0, 0, nc_max); H % 4 == 0.
+// dst[idx[n0 + j]][:] (+)= src[j][:] for j < clamp(*total - n0, 0, nc_max); H % 4 == 0.
 cudaError_t launch_scatter_rows(const float* src, const int* idx, const int* total, int n0, int nc_max, int H,
-                                float* dst, cudaStream_t st);
+                                float* dst, bool accumulate, cudaStream_t st);
 
 // db (+)= the recompute's per-32-row column partials of the chunk (DlParams::dbp,
 // db_part_rows(Nc) rows of V floats), summed over clamp(*rows_total - n0, 0, Nc) rows.

@@ -26,6 +26,7 @@ FLAG_FORCE_ENTROPY_PATH = 0x1
 FLAG_SINGLE_CTA_TILES = 0x2
 FLAG_ADV_PER_TOKEN = 0x4
 FLAG_ALL_ROWS = 0x8
+FLAG_ACCUMULATE = 0x10
 NMETRICS = 8
 
 

@@ -82,6 +82,12 @@ def test_invalid_requests_rejected_synchronously(kw, code):
     assert _call(_cfg(**kw)) == code
 
 
+def test_accumulate_flag_is_accepted_and_needs_no_extra_workspace():
+    assert R.rlloss_workspace_bytes(_cfg(flags=R.FLAG_ACCUMULATE)) == R.rlloss_workspace_bytes(_cfg())
+    assert R.rlloss_workspace_bytes(_cfg(flags=R.FLAG_ACCUMULATE | R.FLAG_ALL_ROWS)) > 0
+    assert R.rlloss_workspace_bytes(_cfg(flags=0x20)) == 0
+
+
 def test_gmpo_sequence_is_rejection_matches_page():
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_constants.json")))
     assert g["gmpo_rejects_sequence_level_is"]["value"] is True

@@ -332,6 +332,62 @@ def test_compaction_with_empty_later_chunks(R):
     _grads_close(a, b)
 
 
+def _run_into(R, case, outs, **cfg_kw):
+    i = case.inp
+    cfg = parity_cfg(R, case.spec, **cfg_kw)
+    t = lambda x: None if x is None else x.cuda()
+    out = R.fwd_bwd(cfg, t(i.X), t(i.W), t(i.b), t(i.targets), t(case.old), t(case.ref), t(i.adv), t(i.mask),
+                    outputs=outs)
+    torch.cuda.synchronize()
+    assert R.rlloss_get_device_status(out["workspace"]) == 0
+    return out
+
+
+@pytest.mark.parametrize("spec,all_rows,chunk", [(MID[1], False, 0), (MID[1], False, 128), (MID[1], True, 0),
+                                                 (MID[4], False, 0), (MID[4], True, 128), (MID[3], False, 0)],
+                         ids=["bias_k3kl", "bias_k3kl_chunks", "bias_k3kl_all_rows", "fp32_bias",
+                              "fp32_bias_all_rows_chunks", "gspo"])
+def test_accumulate_adds_gradients(R, spec, all_rows, chunk):
+    """FLAG_ACCUMULATE adds the call's gradients to what dX, dW, db hold.
+    The result is the initial values plus the overwriting call's gradients:
+    bit for bit where each element gets a single addition (kept dX rows of
+    the compacted backward; dW and db with one chunk), within fp32 rounding
+    otherwise.  Rows without gradient keep their initial bits, and the same
+    initial values give the same bits on every call."""
+    case = Case(spec)
+    base, res, _ = _full_check(R, case, chunk_rows=chunk, flags=R.FLAG_ALL_ROWS if all_rows else 0)
+    g = torch.Generator().manual_seed(7)
+    init = {k: torch.randn(base[k].shape, generator=g).cuda() for k in ("dX", "dW", "db") if base.get(k) is not None}
+    flags = R.FLAG_ACCUMULATE | (R.FLAG_ALL_ROWS if all_rows else 0)
+    runs = []
+    for _ in range(2):
+        outs = {k: v.clone() for k, v in base.items() if isinstance(v, torch.Tensor)}
+        outs.update({k: v.clone() for k, v in init.items()})
+        runs.append(_run_into(R, case, outs, chunk_rows=chunk, flags=flags))
+    a, b = runs
+    for k in init:
+        assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), k
+    for k in ("loss", "metrics"):
+        assert torch.equal(a[k].view(torch.int32), base[k].view(torch.int32)), k
+    one_chunk = chunk == 0
+    exact = {"dX": not all_rows, "dW": one_chunk, "db": one_chunk}
+    for k, v0 in init.items():
+        want = v0 + base[k]
+        if exact[k]:
+            assert torch.equal(a[k].view(torch.int32), want.view(torch.int32)), k
+        else:
+            tol = 1e-6 * float(want.abs().max())
+            assert torch.allclose(a[k], want, rtol=1e-5, atol=tol), k
+    dropped = torch.from_numpy(res.c == 0).cuda()
+    assert dropped.any()
+    assert torch.equal(a["dX"][dropped], init["dX"][dropped])
+    # the added part against the oracle
+    added = dict(a)
+    for k, v0 in init.items():
+        added[k] = (a[k].double() - v0.double()).float()
+    check_grads(added, case, res)
+
+
 SKIP = [
     Workload("long_prompt_gmpo", B=2, T=640, H=128, V=900, dtype="bf16", prompt_len=560, seed=111),
     Workload("long_prompt_entropy", B=3, T=512, H=128, V=700, dtype="bf16", prompt_len=300, temperature=0.7,
