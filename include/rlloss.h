@@ -235,6 +235,66 @@ int rlloss_loss_from_logp_noalloc(const rlloss_cfg* cfg, const float* logp, cons
                                   float* out_dlogp, uint8_t* out_entropy_mask,
                                   int32_t* out_device_status, void* stream);
 
+/* ---- Vocabulary-parallel form (W split by vocabulary rows over shards).
+ * The streamed softmax accumulators of a row are mergeable ("support
+ * top_entropy_quantile in fused linear GRPO loss", Details: log-sum-exp and
+ * entropy from two online accumulators), so a shard holding W rows
+ * [v_begin, v_begin + cfg.V) needs only X, its W rows and the targets:
+ *   1. rlloss_forward_shard on every shard -> one row state per token;
+ *   2. the caller gathers the states of all shards (an all-gather of
+ *      32 B per token and shard) and calls rlloss_loss_from_shards, which
+ *      gives lse, logp, entropy, loss, metrics and dL/dlogp for the whole
+ *      vocabulary (every shard may run it; the results are the same bits);
+ *   3. rlloss_backward_shard on every shard -> its rows of dW and db and its
+ *      part of dX; dX is the sum of the parts (an all-reduce).
+ * The library makes no collective call: the exchanges are the caller's. */
+#define RLLOSS_MAX_SHARDS 4096
+#define RLLOSS_STATE_FLOATS 8   /* floats per token in a shard row state */
+
+/* Step 1.  cfg describes the shard: cfg.V = rows of this W shard; b = its
+ * bias rows; targets [N] are ids of the whole vocabulary (v_begin >= 0 is
+ * the id of the shard's first row).  out_state: [N][RLLOSS_STATE_FLOATS]
+ * fp32, 16-byte aligned; its contents are opaque (a softmax reference,
+ * sums against it, and the target's logit if the shard holds the target).
+ * bf16 or fp32 operands; workspace as for rlloss_forward
+ * (rlloss_forward_workspace_bytes of the shard's cfg). */
+int rlloss_forward_shard(const rlloss_cfg* cfg, const void* X, const void* W, const void* b,
+                         const int64_t* targets, int64_t v_begin, float* out_state, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace rlloss_loss_from_shards needs (0 if cfg is invalid). */
+size_t rlloss_shard_loss_workspace_bytes(const rlloss_cfg* cfg);
+
+/* Step 2.  cfg describes the whole problem (cfg.V = the whole vocabulary;
+ * the loss fields as for rlloss_fwd_bwd; H and dtype are not used).
+ * states: [nshards][N][RLLOSS_STATE_FLOATS], the shards' outputs of step 1
+ * in any fixed order, 16-byte aligned; 1 <= nshards <= RLLOSS_MAX_SHARDS.
+ * Outputs: out_loss [1], out_metrics [RLLOSS_NMETRICS], and, each optional,
+ * out_lse [N] (natural log; needed by step 3), out_dlogp [N] = dL/dlogp_n
+ * (needed by step 3), out_logp, out_entropy [N] fp32, out_entropy_mask [N].
+ * A target that no shard holds sets RLLOSS_DEV_EBADTARGET. */
+int rlloss_loss_from_shards(const rlloss_cfg* cfg, int32_t nshards, const float* states,
+                            const int64_t* targets, const float* old_logp, const float* ref_logp,
+                            const float* adv, const uint8_t* mask, float* out_loss, float* out_metrics,
+                            float* out_lse, float* out_dlogp, float* out_logp, float* out_entropy,
+                            uint8_t* out_entropy_mask, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* Bytes of workspace rlloss_backward_shard needs (0 if cfg is invalid). */
+size_t rlloss_backward_shard_workspace_bytes(const rlloss_cfg* cfg);
+
+/* Step 3.  cfg, X, W, b, targets, v_begin as in step 1 (the loss fields of
+ * cfg are not used; flags RLLOSS_FLAG_ALL_ROWS and RLLOSS_FLAG_ACCUMULATE
+ * apply); lse, dlogp [N] from step 2.  Writes (or adds into) dW [cfg.V, H]
+ * and db [cfg.V] of this shard and dX [N, H], this shard's part:
+ *   G = (dlogp / temperature)(onehot(target) - softmax) over the shard's
+ *   columns, dX_shard = G W_shard, dW_shard = G^T X, db_shard = sum_n G.
+ * Rows with dlogp = 0 are skipped as in rlloss_fwd_bwd. */
+int rlloss_backward_shard(const rlloss_cfg* cfg, const void* X, const void* W, const void* b,
+                          const int64_t* targets, int64_t v_begin, const float* lse, const float* dlogp,
+                          float* dX, float* dW, float* db, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
 /* Copy the device status word of ``workspace`` (the one a previous call used)
  * into *status.  Synchronous; call after the stream has finished.  Returns
  * RLLOSS_ECUDA if the copy failed. */

@@ -140,12 +140,16 @@ int segment_cap(long long N) {
   return c < 1 ? 1 : int(c);
 }
 
-enum PlanMode { kFull, kLossOnly, kForwardOnly };
+// kShardLoss: loss stage over row states gathered from vocabulary shards (row
+// buffers, no LM head); kBackwardOnly: the backward of one vocabulary shard
+// from given lse and dL/dlogp (LM-head operands and backward buffers only).
+enum PlanMode { kFull, kLossOnly, kForwardOnly, kShardLoss, kBackwardOnly };
 
 Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
-  const bool head = mode != kLossOnly;      // LM-head forward kernels
-  const bool loss = mode != kForwardOnly;   // loss stage
-  const bool bwd = mode == kFull;           // backward chunks
+  const bool head = mode != kLossOnly && mode != kShardLoss;        // LM-head operands
+  const bool fwd = head && mode != kBackwardOnly;                   // LM-head forward kernels
+  const bool loss = mode != kForwardOnly && mode != kBackwardOnly;  // loss stage
+  const bool bwd = mode == kFull || mode == kBackwardOnly;          // backward chunks
   Plan p{};
   p.B = c->B;
   p.T = c->T;
@@ -198,14 +202,22 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
       p.Kx = p.H;
     }
     p.kb_dl = p.fp32 ? p.Hp / 64 : int(cdiv(p.H, 64 * p.kbx));
-    p.o_partial = take(size_t(p.N) * 2 * p.pcap * 32);   // room for a segment count chosen on the device
+    if (fwd) {
+      p.o_partial = take(size_t(p.N) * 2 * p.pcap * 32);   // room for a segment count chosen on the device
+      p.o_logp64 = take(size_t(p.N) * 8);
+      p.o_ent = take(size_t(p.N) * 4);
+    }
     p.o_lse2 = take(size_t(p.N) * 4);
-    p.o_logp64 = take(size_t(p.N) * 8);
-    p.o_ent = take(size_t(p.N) * 4);
     p.o_bias2 = take(p.bias ? size_t(p.Vt) * 256 * 4 : 0);
     p.o_ws2 = take(p.f8 ? size_t(p.Vt) * 256 * 4 : 0);
     p.o_x3 = take(p.fp32 ? size_t(p.N) * 3 * p.Hp * 2 : 0);
     p.o_w3 = take(p.fp32 ? size_t(p.V) * 3 * p.Hp * 2 : 0);
+  }
+  if (mode == kShardLoss) {
+    p.V = c->V;
+    p.o_lse2 = take(size_t(p.N) * 4);
+    p.o_logp64 = take(size_t(p.N) * 8);
+    p.o_ent = take(size_t(p.N) * 4);
   }
   if (loss) {
     p.o_emask = take(size_t(p.N));
@@ -427,14 +439,10 @@ struct Head {
     if (_rc != RLLOSS_OK) return _rc; \
   } while (0)
 
-// With merge == false the row merge is left to the caller (the fused merge +
-// loss launch); h.mp is filled either way.
-// With skip_mask set, the forward runs only over row tiles that hold a row
-// with skip_mask != 0 (the rows of the other tiles get no outputs).
-int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W, const void* b,
-             const int64_t* targets, float* out_logp, float* out_entropy, float* out_lse, char* ws,
-             cudaStream_t st, Head& h, bool merge = true, const uint8_t* skip_mask = nullptr) {
-  int* status = reinterpret_cast<int*>(ws + p.o_status);
+// Operand preparation of the LM head (fp32 split, scaled bias, e4m3 column
+// scales), the K-segments and the forward's tensor maps; launches no GEMM.
+int prepare_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W, const void* b, char* ws,
+                 cudaStream_t st, Head& h) {
   const float scale2 = float(1.4426950408889634 / double(cfg->temperature));
   // Operand arrays: bf16 inputs are used in place; fp32 inputs are split
   // into three bf16 terms (hi, mid, lo) so the same bf16 tensor-core kernels
@@ -474,13 +482,12 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
     std::memcpy(h.seg_b, sb, sizeof(sb));
   }
 
-  // ---- forward: tensor-core logits + streamed row state
   FwdParams& fp = h.fp;
+  fp.ws2 = ws2;
   if (p.f8) {
     if (!tmap_u8(&fp.tmA, h.Xop, p.Kx, p.N, 128)) return RLLOSS_ECUDA;
     if (!tmap_u8(&fp.tmB, h.Wop, p.Kx, p.V, 128)) return RLLOSS_ECUDA;
     fp.xs = h.x_scale;
-    fp.ws2 = ws2;
   } else {
     if (!tmap_bf16(&fp.tmA, h.Xop, p.Kx, p.N, p.Kx, 128)) return RLLOSS_ECUDA;
     if (!tmap_bf16(&fp.tmB, h.Wop, p.Kx, p.V, p.Kx, p.pair == 1 ? 256 : 128)) return RLLOSS_ECUDA;
@@ -496,9 +503,29 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
   fp.P = p.P;
   fp.scale2 = scale2;
   fp.bias2 = h.bias2;
-  fp.targets = targets;
   fp.partial = reinterpret_cast<float4*>(ws + p.o_partial);
   fp.pcap = p.pcap;
+  fp.status = reinterpret_cast<int*>(ws + p.o_status);
+  fp.limit_ns = kWaitLimitNs;
+  return RLLOSS_OK;
+}
+
+// With merge == false the row merge is left to the caller (the fused merge +
+// loss launch); h.mp is filled either way.
+// With skip_mask set, the forward runs only over row tiles that hold a row
+// with skip_mask != 0 (the rows of the other tiles get no outputs).
+// v_begin: vocabulary id of W's first row when W is a shard of a larger
+// vocabulary (targets outside the shard match no column).
+int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W, const void* b,
+             const int64_t* targets, float* out_logp, float* out_entropy, float* out_lse, char* ws,
+             cudaStream_t st, Head& h, bool merge = true, const uint8_t* skip_mask = nullptr,
+             long long v_begin = 0) {
+  int* status = reinterpret_cast<int*>(ws + p.o_status);
+  RL_TRY_RC(prepare_head(cfg, p, X, W, b, ws, st, h));
+  // ---- forward: tensor-core logits + streamed row state
+  FwdParams& fp = h.fp;
+  fp.targets = targets;
+  fp.v_begin = v_begin;
   const uint8_t* tflags = nullptr;
   if (skip_mask) {
     tflags = reinterpret_cast<uint8_t*>(ws + p.o_tflags);
@@ -515,8 +542,6 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
     RL_TRY(launch_set_total(reinterpret_cast<int*>(ws + p.o_status + kFwdTilesOffset), p.R, st));
     g_launches += 1;
   }
-  fp.status = status;
-  fp.limit_ns = kWaitLimitNs;
   {
     Phase ph(st, 0);
     RL_TRY(launch_fwd(fp, p.R * p.P, p.pair, p.kbx, st));
@@ -544,6 +569,175 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
     Phase ph(st, 1);
     RL_TRY(launch_merge(mp, st));
     ph.launched();
+  }
+  return RLLOSS_OK;
+}
+
+// The backward from per-row lse (log2 units) and coefficients c_n (G = (c/tau)
+// (onehot(y) - p)): row compaction, then per chunk the G recompute and the
+// grouped dX / dW GEMMs, and db.  hd holds the prepared operands.
+int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int64_t* targets, long long v_begin,
+                 const float* lse2, const float* coef, float* dX, float* dW, float* db, char* ws, cudaStream_t st) {
+  int* status = reinterpret_cast<int*>(ws + p.o_status);
+  // ---- backward, one chunk of rows at a time:
+  //      G = (c/tau)(onehot - p) as bf16, dX = G W, dW += G^T X, db += sum G.
+  // Rows with c_n = 0 add nothing to any of the three; unless the caller asks
+  // for the dense backward they are dropped first (ordered compaction), the
+  // chunks run over the kept rows, and dX rows are scattered back (the rest
+  // of dX is zero).  The kept-row count stays on the device: every backward
+  // kernel reads it, and chunks past it do no work.  With ACCUMULATE every
+  // output element still receives one addition per chunk (dX rows: one per
+  // call), so the sums keep a fixed order.
+  const bool acc = (cfg->flags & RLLOSS_FLAG_ACCUMULATE) != 0;
+  __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dl);
+  const int lo_off = p.fp32 ? p.Vp : 0;
+  int* rows_total = reinterpret_cast<int*>(ws + p.o_status + kBackwardRowsOffset);
+  const void* Xb = hd.Xop;           // X operand rows of the backward
+  const int64_t* tg_b = targets;
+  const float* lse2_b = lse2;
+  const float* coef_b = coef;
+  const int* cidx = nullptr;
+  float* dxc = nullptr;
+  long long xb_rows = p.N;
+  {
+    Phase ph(st, 5);
+    if (p.compact) {
+      CompactParams cp{};
+      cp.N = p.N;
+      cp.Kx = p.Kx;
+      cp.Ncap = p.Ncap;
+      cp.coef = coef;
+      cp.lse2 = lse2;
+      cp.targets = targets;
+      cp.x = static_cast<const __nv_bfloat16*>(hd.Xop);
+      cp.blk_cnt = reinterpret_cast<int*>(ws + p.o_blk);
+      cp.blk_off = cp.blk_cnt + compact_groups(p.N);
+      cp.ticket = reinterpret_cast<unsigned int*>(ws + p.o_status + 8);
+      cp.total = rows_total;
+      cp.idx = reinterpret_cast<int*>(ws + p.o_cidx);
+      cp.coefc = reinterpret_cast<float*>(ws + p.o_coefc);
+      cp.lse2c = reinterpret_cast<float*>(ws + p.o_lse2c);
+      cp.tgtc = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
+      cp.xc = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
+      RL_TRY(launch_compact(cp, st));
+      if (!acc) RL_TRY(cudaMemsetAsync(dX, 0, size_t(p.N) * p.H * 4, st));
+      ph.launched(2);
+      Xb = cp.xc;
+      tg_b = cp.tgtc;
+      lse2_b = cp.lse2c;
+      coef_b = cp.coefc;
+      cidx = cp.idx;
+      dxc = reinterpret_cast<float*>(ws + p.o_dxc);
+      xb_rows = p.Ncap;
+    } else {
+      RL_TRY(launch_set_total(rows_total, p.N, st));
+      ph.launched();
+    }
+  }
+  CUtensorMap tm_xb;
+  if (!tmap_bf16(&tm_xb, Xb, p.Kx, xb_rows, p.Kx, 128)) return RLLOSS_ECUDA;
+  for (int ch = 0; ch < p.nchunks; ++ch) {
+    const int n0 = ch * p.Nc;
+    const int nc = std::min(p.Nc, p.N - n0);   // upper bound; the kernels clamp to the kept rows
+    const int Rc = int(cdiv(nc, p.rows_tile));
+
+    DlParams dp{};
+    dp.tmA = tm_xb;
+    dp.tmB = hd.fp.tmB;
+    dp.nseg = hd.fp.nseg;
+    dp.kb_per_seg = p.kb_dl;
+    std::memcpy(dp.seg_a, hd.seg_a, sizeof(hd.seg_a));
+    std::memcpy(dp.seg_b, hd.seg_b, sizeof(hd.seg_b));
+    dp.n0 = n0;
+    dp.Nc = nc;
+    dp.Rc = Rc;
+    dp.rows_total = rows_total;
+    dp.V = p.V;
+    dp.Vp = p.Vp;
+    dp.Vt = p.Vt;
+    dp.scale2 = hd.fp.scale2;
+    dp.bias2 = hd.bias2;
+    dp.targets = tg_b;
+    dp.v_begin = v_begin;
+    dp.lse2 = lse2_b;
+    dp.coef = coef_b;
+    dp.dl = dl;
+    dp.ld = p.ld_dl;
+    if (!tmap_bf16_box(&dp.tmG, dl, p.fp32 ? 2ll * p.Vp : p.V, nc, p.ld_dl, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return RLLOSS_ECUDA;
+    dp.lo_off = lo_off;
+    dp.dbp = p.bias ? reinterpret_cast<float*>(ws + p.o_dbpart) : nullptr;
+    dp.status = status;
+    dp.limit_ns = kWaitLimitNs;
+    {
+      Phase ph(st, 2);
+      RL_TRY(launch_dl(dp, Rc * p.Vt, p.pair, p.kbx, st));
+      ph.launched();
+    }
+
+    // One grouped launch: problem 0 = dX rows of this chunk,
+    //   dX[n][h] = sum_v G[n][v] W[v][h];  problem 1 = dW (+)= over this chunk,
+    //   dW[v][h] = sum_n G[n][v] X[n][h].
+    {
+      HParams hp{};
+      set_bwd_segments(hp, p);
+      float* dx_out = p.compact ? dxc : dX + size_t(n0) * p.H;
+      const long long g_inner = p.fp32 ? 2ll * p.Vp : p.V;
+      if (!tmap_bf16(&hp.tmA[0], dl, g_inner, nc, p.ld_dl, 128)) return RLLOSS_ECUDA;
+      if (!tmap_bf16(&hp.tmB[0], hd.Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
+      if (!tmap_f32_out(&hp.tmO[0], dx_out, p.H, nc)) return RLLOSS_ECUDA;
+      if (!tmap_bf16(&hp.tmA[1], dl, g_inner, nc, p.ld_dl, 64)) return RLLOSS_ECUDA;
+      if (!tmap_bf16(&hp.tmB[1], Xb, p.Kx, xb_rows, p.Kx, 64)) return RLLOSS_ECUDA;
+      if (!tmap_f32_out(&hp.tmO[1], dW, p.H, p.V)) return RLLOSS_ECUDA;
+      HProblem& px = hp.pr[0];
+      px.kb_per_seg = int(cdiv(p.V, 64));
+      px.a_outer0 = 0;
+      px.b_outer0 = 0;
+      px.Mt = int(cdiv(nc, 256));
+      px.Ht = int(cdiv(p.H, 448));
+      px.Hout = p.H;
+      px.order = 0;
+      px.a_mn = 0;
+      // Two k halves reduce-added onto a zeroed buffer (two addends: the same
+      // sum in either order); accumulating straight into dX takes one
+      // unsplit reduce-add instead, since a third addend would make the
+      // result depend on the order of the halves.
+      const bool dx_in_place_acc = acc && !p.compact;
+      px.ksplit = (hp.nseg * px.kb_per_seg >= 2 && !dx_in_place_acc) ? 2 : 1;
+      px.reduce = (px.ksplit == 2 || dx_in_place_acc) ? 1 : 0;
+      HProblem& pw = hp.pr[1];
+      pw.kb_per_seg = int(cdiv(nc, 64));
+      pw.a_outer0 = 0;
+      pw.b_outer0 = n0;
+      pw.Mt = int(cdiv(p.V, 256));
+      pw.Ht = int(cdiv(p.H, 448));
+      pw.Hout = p.H;
+      pw.order = 1;
+      pw.a_mn = 1;
+      pw.reduce = (ch > 0 || acc) ? 1 : 0;
+      pw.ksplit = 1;
+      hp.nprob = 2;
+      const int kx = hp.nseg * px.kb_per_seg / px.ksplit, kw = hp.nseg * pw.kb_per_seg;
+      hp.d_tiles = std::max(1, (kx + kw / 2) / kw);
+      hp.rows_total = rows_total;
+      hp.n0 = n0;
+      hp.nc_max = nc;
+      hp.status = status;
+      hp.limit_ns = kWaitLimitNs;
+      Phase ph(st, 3);
+      if (px.reduce && !dx_in_place_acc) RL_TRY(cudaMemsetAsync(dx_out, 0, size_t(nc) * p.H * 4, st));
+      RL_TRY(launch_gemmH(hp, px.Mt * px.Ht * px.ksplit + pw.Mt * pw.Ht, st));
+      ph.launched();
+      if (p.compact) {
+        RL_TRY(launch_scatter_rows(dxc, cidx, rows_total, n0, nc, p.H, dX, acc, st));
+        ph.launched();
+      }
+    }
+    if (p.bias) {
+      Phase ph(st, 5);
+      RL_TRY(launch_db_reduce(reinterpret_cast<float*>(ws + p.o_dbpart), rows_total, n0, nc, p.V, db, ch > 0 || acc, st));
+      ph.launched();
+    }
   }
   return RLLOSS_OK;
 }
@@ -740,8 +934,6 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  int* status = reinterpret_cast<int*>(ws + p.o_status);
-  const float scale2 = float(1.4426950408889634 / double(cfg->temperature));
   RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, p.o_tickets + size_t(p.B) * 4 - p.o_status, st));
 
   Head hd;
@@ -752,10 +944,6 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
                           !out_entropy;
   RL_TRY_RC(run_head(cfg, p, X, W, b, targets, out_logp, out_entropy, nullptr, ws, st, hd, !p.fused_loss,
                      skip_tiles ? mask : nullptr));
-  const void* Xop = hd.Xop;
-  const void* Wop = hd.Wop;
-  const float* bias2 = hd.bias2;
-  const FwdParams& fp = hd.fp;
   const MergeParams& mp = hd.mp;
   LossParams lp{};
   {
@@ -788,166 +976,132 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     RL_TRY(cudaMemcpyAsync(out_entropy_mask, p.ent ? emask : mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
   }
 
-  // ---- backward, one chunk of rows at a time:
-  //      G = (c/tau)(onehot - p) as bf16, dX = G W, dW += G^T X, db += sum G.
-  // Rows with c_n = 0 add nothing to any of the three; unless the caller asks
-  // for the dense backward they are dropped first (ordered compaction), the
-  // chunks run over the kept rows, and dX rows are scattered back (the rest
-  // of dX is zero).  The kept-row count stays on the device: every backward
-  // kernel reads it, and chunks past it do no work.  With ACCUMULATE every
-  // output element still receives one addition per chunk (dX rows: one per
-  // call), so the sums keep a fixed order.
-  const bool acc = (cfg->flags & RLLOSS_FLAG_ACCUMULATE) != 0;
-  __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dl);
-  const int lo_off = p.fp32 ? p.Vp : 0;
-  int* rows_total = reinterpret_cast<int*>(ws + p.o_status + kBackwardRowsOffset);
-  const void* Xb = Xop;              // X operand rows of the backward
-  const int64_t* tg_b = targets;
-  const float* lse2_b = mp.lse2;
-  const float* coef_b = lp.coef;
-  const int* cidx = nullptr;
-  float* dxc = nullptr;
-  long long xb_rows = p.N;
+  return run_backward(cfg, p, hd, targets, 0, mp.lse2, lp.coef, dX, dW, db, ws, st);
+}
+
+// ---------------------------------------------------------------- vocabulary shards
+// The vocabulary-parallel form of the path: each shard of W (a contiguous
+// range of vocabulary rows) yields a mergeable per-row softmax state; the
+// states of all shards give lse, logp, entropy, loss and dL/dlogp; each shard
+// then computes its own dW and db rows and its part of dX (the parts sum to
+// dX).  The streamed accumulators are mergeable ("support
+// top_entropy_quantile in fused linear GRPO loss", Details: the entropy from
+// a second online accumulator beside the log-sum-exp one).
+
+int rlloss_forward_shard(const rlloss_cfg* cfg, const void* X, const void* W, const void* b, const int64_t* targets,
+                         int64_t v_begin, float* out_state, void* workspace, size_t workspace_bytes, void* stream) {
+  int e = validate_head(cfg);
+  if (e) return e;
+  if (cfg->dtype == RLLOSS_FP8_E4M3) return RLLOSS_EUNSUPPORTED;
+  if (!X || !W || !targets || !out_state || !workspace || v_begin < 0) return RLLOSS_EINVAL;
+  if (cfg->has_bias && !b) return RLLOSS_EINVAL;
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(out_state, 16)) return RLLOSS_EINVAL;
+  const Plan p = make_plan(cfg, kForwardOnly);
+  if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
+  if (!encode_fn()) return RLLOSS_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, 256, st));
+  Head hd;
+  RL_TRY_RC(run_head(cfg, p, X, W, b, targets, nullptr, nullptr, nullptr, ws, st, hd, false, nullptr, v_begin));
+  Phase ph(st, 1);
+  RL_TRY(launch_shard_state(hd.mp, reinterpret_cast<float4*>(out_state), st));
+  ph.launched();
+  return RLLOSS_OK;
+}
+
+size_t rlloss_shard_loss_workspace_bytes(const rlloss_cfg* cfg) {
+  if (validate_common(cfg) != RLLOSS_OK || cfg->V < 1) return 0;
+  return make_plan(cfg, kShardLoss).total;
+}
+
+int rlloss_loss_from_shards(const rlloss_cfg* cfg, int32_t nshards, const float* states, const int64_t* targets,
+                            const float* old_logp, const float* ref_logp, const float* adv, const uint8_t* mask,
+                            float* out_loss, float* out_metrics, float* out_lse, float* out_dlogp, float* out_logp,
+                            float* out_entropy, uint8_t* out_entropy_mask, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  int e = validate_common(cfg);
+  if (e) return e;
+  if (cfg->V < 1 || nshards < 1 || nshards > RLLOSS_MAX_SHARDS) return RLLOSS_EINVAL;
+  if (!states || !targets || !old_logp || !adv || !mask || !out_loss || !out_metrics || !workspace)
+    return RLLOSS_EINVAL;
+  if (cfg->beta != 0.f && !ref_logp) return RLLOSS_EINVAL;
+  if (!aligned(states, 16)) return RLLOSS_EINVAL;
+  const Plan p = make_plan(cfg, kShardLoss);
+  if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + p.o_status);
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, p.o_tickets + size_t(p.B) * 4 - p.o_status, st));
+  MergeParams mp{};
+  mp.partial = reinterpret_cast<const float4*>(states);
+  mp.N = p.N;
+  mp.V = cfg->V;
+  mp.slots = nshards;
+  mp.slot_stride = p.N;
+  mp.targets = targets;
+  mp.lse2 = reinterpret_cast<float*>(ws + p.o_lse2);
+  mp.logp64 = reinterpret_cast<double*>(ws + p.o_logp64);
+  mp.ent32 = reinterpret_cast<float*>(ws + p.o_ent);
+  mp.out_logp = out_logp;
+  mp.out_ent = out_entropy;
+  mp.out_lse = out_lse;
+  mp.status = status;
+  Phase ph(st, 1);
+  RL_TRY(launch_merge(mp, st));
+  ph.launched();
+  uint8_t* emask = reinterpret_cast<uint8_t*>(ws + p.o_emask);
+  if (p.ent) {
+    RL_TRY(launch_entropy_mask(mp.ent32, mask, p.N, double(cfg->top_entropy_quantile), ws + p.o_k3, emask, st));
+    ph.launched(9);
+  }
+  LossParams lp = loss_params(cfg, p, ws);
+  lp.logp = mp.logp64;
+  lp.logp_is_f64 = 1;
+  lp.old_logp = old_logp;
+  lp.ref_logp = ref_logp;
+  lp.adv = adv;
+  lp.mask = mask;
+  lp.emask = p.ent ? emask : nullptr;
+  lp.dlogp = out_dlogp;
+  lp.out_loss = out_loss;
+  lp.out_metrics = out_metrics;
+  RL_TRY(launch_loss(lp, st));
+  ph.launched(out_dlogp ? 2 : 1);
+  if (out_entropy_mask)
+    RL_TRY(cudaMemcpyAsync(out_entropy_mask, p.ent ? emask : mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
+  return RLLOSS_OK;
+}
+
+size_t rlloss_backward_shard_workspace_bytes(const rlloss_cfg* cfg) {
+  if (validate_full(cfg) != RLLOSS_OK) return 0;
+  return make_plan(cfg, kBackwardOnly).total;
+}
+
+int rlloss_backward_shard(const rlloss_cfg* cfg, const void* X, const void* W, const void* b, const int64_t* targets,
+                          int64_t v_begin, const float* lse, const float* dlogp, float* dX, float* dW, float* db,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  int e = validate_full(cfg);
+  if (e) return e;
+  if (!X || !W || !targets || !lse || !dlogp || !dX || !dW || !workspace || v_begin < 0) return RLLOSS_EINVAL;
+  if (cfg->has_bias && (!b || !db)) return RLLOSS_EINVAL;
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16)) return RLLOSS_EINVAL;
+  const Plan p = make_plan(cfg, kBackwardOnly);
+  if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
+  if (!encode_fn()) return RLLOSS_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, 256, st));
+  Head hd;
+  RL_TRY_RC(prepare_head(cfg, p, X, W, b, ws, st, hd));
+  float* lse2 = reinterpret_cast<float*>(ws + p.o_lse2);
+  float* coef = reinterpret_cast<float*>(ws + p.o_coef);
   {
     Phase ph(st, 5);
-    if (p.compact) {
-      CompactParams cp{};
-      cp.N = p.N;
-      cp.Kx = p.Kx;
-      cp.Ncap = p.Ncap;
-      cp.coef = lp.coef;
-      cp.lse2 = mp.lse2;
-      cp.targets = targets;
-      cp.x = static_cast<const __nv_bfloat16*>(Xop);
-      cp.blk_cnt = reinterpret_cast<int*>(ws + p.o_blk);
-      cp.blk_off = cp.blk_cnt + compact_groups(p.N);
-      cp.ticket = reinterpret_cast<unsigned int*>(ws + p.o_status + 8);
-      cp.total = rows_total;
-      cp.idx = reinterpret_cast<int*>(ws + p.o_cidx);
-      cp.coefc = reinterpret_cast<float*>(ws + p.o_coefc);
-      cp.lse2c = reinterpret_cast<float*>(ws + p.o_lse2c);
-      cp.tgtc = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
-      cp.xc = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
-      RL_TRY(launch_compact(cp, st));
-      if (!acc) RL_TRY(cudaMemsetAsync(dX, 0, size_t(p.N) * p.H * 4, st));
-      ph.launched(2);
-      Xb = cp.xc;
-      tg_b = cp.tgtc;
-      lse2_b = cp.lse2c;
-      coef_b = cp.coefc;
-      cidx = cp.idx;
-      dxc = reinterpret_cast<float*>(ws + p.o_dxc);
-      xb_rows = p.Ncap;
-    } else {
-      RL_TRY(launch_set_total(rows_total, p.N, st));
-      ph.launched();
-    }
+    RL_TRY(launch_backward_rows_in(lse, dlogp, p.N, 1.0 / double(cfg->temperature), lse2, coef, st));
+    ph.launched();
   }
-  CUtensorMap tm_xb;
-  if (!tmap_bf16(&tm_xb, Xb, p.Kx, xb_rows, p.Kx, 128)) return RLLOSS_ECUDA;
-  for (int ch = 0; ch < p.nchunks; ++ch) {
-    const int n0 = ch * p.Nc;
-    const int nc = std::min(p.Nc, p.N - n0);   // upper bound; the kernels clamp to the kept rows
-    const int Rc = int(cdiv(nc, p.rows_tile));
-
-    DlParams dp{};
-    dp.tmA = tm_xb;
-    dp.tmB = fp.tmB;
-    dp.nseg = fp.nseg;
-    dp.kb_per_seg = p.kb_dl;
-    std::memcpy(dp.seg_a, hd.seg_a, sizeof(hd.seg_a));
-    std::memcpy(dp.seg_b, hd.seg_b, sizeof(hd.seg_b));
-    dp.n0 = n0;
-    dp.Nc = nc;
-    dp.Rc = Rc;
-    dp.rows_total = rows_total;
-    dp.V = p.V;
-    dp.Vp = p.Vp;
-    dp.Vt = p.Vt;
-    dp.scale2 = scale2;
-    dp.bias2 = bias2;
-    dp.targets = tg_b;
-    dp.lse2 = lse2_b;
-    dp.coef = coef_b;
-    dp.dl = dl;
-    dp.ld = p.ld_dl;
-    if (!tmap_bf16_box(&dp.tmG, dl, p.fp32 ? 2ll * p.Vp : p.V, nc, p.ld_dl, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-      return RLLOSS_ECUDA;
-    dp.lo_off = lo_off;
-    dp.dbp = p.bias ? reinterpret_cast<float*>(ws + p.o_dbpart) : nullptr;
-    dp.status = status;
-    dp.limit_ns = kWaitLimitNs;
-    {
-      Phase ph(st, 2);
-      RL_TRY(launch_dl(dp, Rc * p.Vt, p.pair, p.kbx, st));
-      ph.launched();
-    }
-
-    // One grouped launch: problem 0 = dX rows of this chunk,
-    //   dX[n][h] = sum_v G[n][v] W[v][h];  problem 1 = dW (+)= over this chunk,
-    //   dW[v][h] = sum_n G[n][v] X[n][h].
-    {
-      HParams hp{};
-      set_bwd_segments(hp, p);
-      float* dx_out = p.compact ? dxc : dX + size_t(n0) * p.H;
-      const long long g_inner = p.fp32 ? 2ll * p.Vp : p.V;
-      if (!tmap_bf16(&hp.tmA[0], dl, g_inner, nc, p.ld_dl, 128)) return RLLOSS_ECUDA;
-      if (!tmap_bf16(&hp.tmB[0], Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
-      if (!tmap_f32_out(&hp.tmO[0], dx_out, p.H, nc)) return RLLOSS_ECUDA;
-      if (!tmap_bf16(&hp.tmA[1], dl, g_inner, nc, p.ld_dl, 64)) return RLLOSS_ECUDA;
-      if (!tmap_bf16(&hp.tmB[1], Xb, p.Kx, xb_rows, p.Kx, 64)) return RLLOSS_ECUDA;
-      if (!tmap_f32_out(&hp.tmO[1], dW, p.H, p.V)) return RLLOSS_ECUDA;
-      HProblem& px = hp.pr[0];
-      px.kb_per_seg = int(cdiv(p.V, 64));
-      px.a_outer0 = 0;
-      px.b_outer0 = 0;
-      px.Mt = int(cdiv(nc, 256));
-      px.Ht = int(cdiv(p.H, 448));
-      px.Hout = p.H;
-      px.order = 0;
-      px.a_mn = 0;
-      // Two k halves reduce-added onto a zeroed buffer (two addends: the same
-      // sum in either order); accumulating straight into dX takes one
-      // unsplit reduce-add instead, since a third addend would make the
-      // result depend on the order of the halves.
-      const bool dx_in_place_acc = acc && !p.compact;
-      px.ksplit = (hp.nseg * px.kb_per_seg >= 2 && !dx_in_place_acc) ? 2 : 1;
-      px.reduce = (px.ksplit == 2 || dx_in_place_acc) ? 1 : 0;
-      HProblem& pw = hp.pr[1];
-      pw.kb_per_seg = int(cdiv(nc, 64));
-      pw.a_outer0 = 0;
-      pw.b_outer0 = n0;
-      pw.Mt = int(cdiv(p.V, 256));
-      pw.Ht = int(cdiv(p.H, 448));
-      pw.Hout = p.H;
-      pw.order = 1;
-      pw.a_mn = 1;
-      pw.reduce = (ch > 0 || acc) ? 1 : 0;
-      pw.ksplit = 1;
-      hp.nprob = 2;
-      const int kx = hp.nseg * px.kb_per_seg / px.ksplit, kw = hp.nseg * pw.kb_per_seg;
-      hp.d_tiles = std::max(1, (kx + kw / 2) / kw);
-      hp.rows_total = rows_total;
-      hp.n0 = n0;
-      hp.nc_max = nc;
-      hp.status = status;
-      hp.limit_ns = kWaitLimitNs;
-      Phase ph(st, 3);
-      if (px.reduce && !dx_in_place_acc) RL_TRY(cudaMemsetAsync(dx_out, 0, size_t(nc) * p.H * 4, st));
-      RL_TRY(launch_gemmH(hp, px.Mt * px.Ht * px.ksplit + pw.Mt * pw.Ht, st));
-      ph.launched();
-      if (p.compact) {
-        RL_TRY(launch_scatter_rows(dxc, cidx, rows_total, n0, nc, p.H, dX, acc, st));
-        ph.launched();
-      }
-    }
-    if (p.bias) {
-      Phase ph(st, 5);
-      RL_TRY(launch_db_reduce(reinterpret_cast<float*>(ws + p.o_dbpart), rows_total, n0, nc, p.V, db, ch > 0 || acc, st));
-      ph.launched();
-    }
-  }
-  return RLLOSS_OK;
+  return run_backward(cfg, p, hd, targets, v_begin, lse2, coef, dX, dW, db, ws, st);
 }
 
 }  // extern "C"

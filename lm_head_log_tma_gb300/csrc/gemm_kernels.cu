@@ -175,7 +175,9 @@ struct FwdPolicy {
       e.s_hi = e.s_lo = e.w_hi = e.w_lo = 0.f;
       e.zy = 0.f;
       e.found = 0;
-      e.y = row < p.N ? int(p.targets[row]) : -1;
+      // target column within this vocabulary (shard); -1 when it lies outside
+      const long long yl = row < p.N ? p.targets[row] - p.v_begin : -1;
+      e.y = (yl >= 0 && yl < p.V) ? int(yl) : -1;
       if constexpr (F8) e.xs = row < p.N ? p.xs[row] : 0.f;
     }
     const float sc = p.scale2;
@@ -287,6 +289,26 @@ __global__ void fwd_merge_kernel(MergeParams p) {
   const int r = int((blockIdx.x * (long long)blockDim.x + threadIdx.x) / kMergeLanes);
   const bool live = r < p.N && row_has_forward(p, r);
   merge_row(p, live ? r : -1, threadIdx.x % kMergeLanes);
+}
+
+// One merged state slot per row, written in the partial-slot format
+// (M, s_hi, s_lo, w_hi), (w_lo, t_target, found, 0).
+__global__ void shard_state_kernel(MergeParams p, float4* state) {
+  const int r = int((blockIdx.x * (long long)blockDim.x + threadIdx.x) / kMergeLanes);
+  const int sub = threadIdx.x % kMergeLanes;
+  const bool live = r < p.N;
+  const RowSums m = merge_slots(p, live ? r : -1, sub);
+  if (!live || sub != 0) return;
+  state[2 * size_t(r)] = make_float4(m.M, m.shi, m.slo, m.whi);
+  state[2 * size_t(r) + 1] = make_float4(m.wlo, m.who ? m.zy : 0.f, m.who ? 1.f : 0.f, 0.f);
+}
+
+__global__ void backward_rows_in_kernel(const float* lse, const float* dlogp, int N, double inv_tau, float* lse2,
+                                        float* coef) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  lse2[n] = float(double(lse[n]) * 1.4426950408889634);
+  coef[n] = float(double(dlogp[n]) * inv_tau);
 }
 
 // =============================================================== dlogits
@@ -415,7 +437,8 @@ struct DlPolicy {
     const int row = p.n0 + rl;
     const float lse2 = valid ? p.lse2[row] : 0.f;
     const float cf = valid ? p.coef[row] : 0.f;
-    const int y = valid ? int(p.targets[row]) : -1;
+    const long long yl = valid ? p.targets[row] - p.v_begin : -1;
+    const int y = (yl >= 0 && yl < p.V) ? int(yl) : -1;   // target column within this vocabulary (shard)
     const float sc = p.scale2;
 #pragma unroll 1
     for (int ch = 0; ch < 4; ++ch) {
@@ -801,6 +824,16 @@ cudaError_t launch_gemmH(const HParams& p, int units, cudaStream_t st) { return 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
   constexpr int rows = 256 / kMergeLanes;   // rows per 256-thread block
   fwd_merge_kernel<<<(p.N + rows - 1) / rows, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_shard_state(const MergeParams& p, float4* state, cudaStream_t st) {
+  constexpr int rows = 256 / kMergeLanes;
+  shard_state_kernel<<<(p.N + rows - 1) / rows, 256, 0, st>>>(p, state);
+  return cudaGetLastError();
+}
+cudaError_t launch_backward_rows_in(const float* lse, const float* dlogp, int N, double inv_tau, float* lse2,
+                                   float* coef, cudaStream_t st) {
+  backward_rows_in_kernel<<<(N + 255) / 256, 256, 0, st>>>(lse, dlogp, N, inv_tau, lse2, coef);
   return cudaGetLastError();
 }
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st) {

@@ -45,6 +45,7 @@ struct FwdParams {
   const float* xs;            // e4m3 operands: [N] per-row X scales, else null
   const float* ws2;           // e4m3 operands: [Vt*256] per-row W scales * scale2, zero padded
   const int64_t* targets;
+  long long v_begin;          // vocabulary id of column 0 (a shard of a larger vocabulary), else 0
   float4* partial;            // [N][2P][2]
   int* status;
   unsigned long long limit_ns;
@@ -53,6 +54,7 @@ struct FwdParams {
 struct MergeParams {
   const float4* partial;
   int N, V, slots;            // slots = 2P
+  int slot_stride;            // 0: partial is [N][slots][2]; else [slots][slot_stride][2] (gathered shard states)
   const int* P_dev;           // if set, slots = 2 * *P_dev (segments chosen on the device)
   const uint8_t* tile_active; // if set, rows of row tiles (1 << tile_shift rows) with a 0 flag
   int tile_shift;             //   had no forward: they are skipped (all their rows are masked)
@@ -76,6 +78,7 @@ struct DlParams {
   float scale2;
   const float* bias2;
   const int64_t* targets;
+  long long v_begin;          // as in FwdParams
   const float* lse2;
   const float* coef;          // dL/dlogp / temperature
   __nv_bfloat16* dl;          // [Nc, ld] chunk buffer (hi terms)
@@ -153,6 +156,14 @@ int gemmH_resident_clusters();
 // kbx: 128-byte boxes per operand per pipeline stage (2: pair tiles with one K segment)
 cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, int kbx, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
+// One state slot per row ([N][2] float4, the partial-slot layout) from the
+// forward's 2P partial slots of each row: the vocabulary shard's mergeable
+// softmax state.
+cudaError_t launch_shard_state(const MergeParams& p, float4* state, cudaStream_t st);
+// Backward row inputs from the caller's units: lse2[n] = lse[n] log2(e) (the
+// kernels' log2 units) and coef[n] = dlogp[n] / temperature.
+cudaError_t launch_backward_rows_in(const float* lse, const float* dlogp, int N, double inv_tau, float* lse2,
+                                   float* coef, cudaStream_t st);
 cudaError_t launch_dl(const DlParams& p, int units, int cluster, int kbx, cudaStream_t st);
 cudaError_t launch_gemmH(const HParams& p, int units, cudaStream_t st);
 cudaError_t launch_bias2(const void* b, int is_fp32, int V, int Vpad, float scale2, float* out, cudaStream_t st);

@@ -49,20 +49,36 @@ __device__ __forceinline__ bool row_has_forward(const MergeParams& p, int row) {
   return !p.tile_active || p.tile_active[row >> p.tile_shift];
 }
 
-// Merges `row` with the lanes of this lane's group (sub = lane % kMergeLanes; all 32
-// lanes of the warp must call it, with `row` < 0 for groups without a row)
-// and writes the row's lse, logp and entropy.  Returns the row's logp on the
-// group's first lane (NaN for a bad target), 0 elsewhere.
-__device__ __forceinline__ double merge_row(const MergeParams& p, int row, int sub) {
+// A row's merged softmax state, valid on the first lane of its group: the
+// reference M, S and W as hi + lo pairs against M, the target's t and the
+// group lanes whose slot held it (who), and the row's target id (y).
+struct RowSums {
+  float M, shi, slo, whi, wlo, zy;
+  unsigned who;
+  long long y;
+};
+
+// Slot k of `row`: layout [N][slots][2] float4 (slot_stride == 0), or
+// [slots][slot_stride][2] float4 (states gathered from vocabulary shards).
+__device__ __forceinline__ const float4* slot_ptr(const MergeParams& p, int row, int slots, int k) {
+  return p.slot_stride ? p.partial + (size_t(k) * p.slot_stride + row) * 2
+                       : p.partial + (size_t(row) * slots + k) * 2;
+}
+
+// Merges the slots of `row` over the lanes of this lane's group (sub = lane %
+// kMergeLanes; all 32 lanes of the warp must call it, with `row` < 0 for
+// groups without a row).
+__device__ __forceinline__ RowSums merge_slots(const MergeParams& p, int row, int sub) {
   const bool live = row >= 0;
-  const long long y = (live && sub == 0) ? p.targets[row] : 0;   // issued early, used at the end
+  RowSums r;
+  r.y = (live && sub == 0) ? p.targets[row] : 0;   // issued early, used at the end
   const int slots = p.P_dev ? 2 * *p.P_dev : p.slots;
-  const float4* base = p.partial + size_t(live ? row : 0) * slots * 2;
   const int nk = live ? slots : 0;
+  const int rr = live ? row : 0;
   float M = -INFINITY;
 #pragma unroll 4
   for (int k = sub; k < nk; k += kMergeLanes) {
-    const float4 a = base[2 * k];
+    const float4 a = slot_ptr(p, rr, slots, k)[0];
     if (a.y + a.z > 0.f) M = fmaxf(M, a.x);
   }
 #pragma unroll
@@ -71,8 +87,9 @@ __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int s
   int found = 0;
 #pragma unroll 4
   for (int k = sub; k < nk; k += kMergeLanes) {
-    const float4 a = base[2 * k];
-    const float4 b = base[2 * k + 1];
+    const float4* sp = slot_ptr(p, rr, slots, k);
+    const float4 a = sp[0];
+    const float4 b = sp[1];
     if (a.y + a.z > 0.f) {
       const float d = a.x - M;                   // integer, <= 0, exact
       const float f = pow2_int(int(d));
@@ -94,9 +111,20 @@ __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int s
   const int lane = threadIdx.x & 31;
   const int g0 = lane & ~(kMergeLanes - 1);   // first lane of this group
   const unsigned gmask = ((1u << kMergeLanes) - 1u) << g0;
-  const unsigned who = __ballot_sync(0xffffffffu, found) & gmask;
-  zy = __shfl_sync(0xffffffffu, zy, who ? __ffs(who) - 1 : g0);
-  if (!live || sub != 0) return 0.0;
+  r.who = __ballot_sync(0xffffffffu, found) & gmask;
+  r.zy = __shfl_sync(0xffffffffu, zy, r.who ? __ffs(r.who) - 1 : g0);
+  r.M = M;
+  r.shi = shi;
+  r.slo = slo;
+  r.whi = whi;
+  r.wlo = wlo;
+  return r;
+}
+
+// Writes the row's lse, logp and entropy from its merged state (first lane
+// of the group only) and returns the logp (NaN for a bad target).
+__device__ __forceinline__ double finish_row(const MergeParams& p, int row, const RowSums& r) {
+  const float M = r.M, shi = r.shi, slo = r.slo, whi = r.whi, wlo = r.wlo;
   // log2 S = e + log2(mh) + log2(1 + slo/shi), with shi = 2^e mh, mh in
   // [1, 2) (S >= 1/2, so shi is a normal number): log2f on [1, 2) is within
   // an ulp of [0, 1); the last term is slo/shi/ln2 to first order
@@ -119,8 +147,8 @@ __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int s
   const double l2s = double(yh) + double(yl);
   const double lse2 = double(M) + l2s;
   const double ent = ln2 * (double(xh) + double(xl));
-  double logp = ln2 * (double(zy) - lse2);
-  if (y < 0 || y >= p.V || !who) {
+  double logp = ln2 * (double(r.zy) - lse2);
+  if (r.y < 0 || r.y >= p.V || !r.who) {
     logp = __longlong_as_double(0x7ff8000000000000ll);
     if (p.status) atomicOr(p.status, RLLOSS_DEV_EBADTARGET);
   }
@@ -131,6 +159,15 @@ __device__ __forceinline__ double merge_row(const MergeParams& p, int row, int s
   if (p.out_ent) p.out_ent[row] = float(ent);
   if (p.out_lse) p.out_lse[row] = float(ln2 * lse2);
   return logp;
+}
+
+// Merges `row` (see merge_slots) and writes its lse, logp and entropy.
+// Returns the row's logp on the group's first lane (NaN for a bad target),
+// 0 elsewhere.
+__device__ __forceinline__ double merge_row(const MergeParams& p, int row, int sub) {
+  const RowSums r = merge_slots(p, row, sub);
+  if (row < 0 || sub != 0) return 0.0;
+  return finish_row(p, row, r);
 }
 
 }  // namespace rl

@@ -28,6 +28,8 @@ FLAG_ADV_PER_TOKEN = 0x4
 FLAG_ALL_ROWS = 0x8
 FLAG_ACCUMULATE = 0x10
 NMETRICS = 8
+STATE_FLOATS = 8        # floats per token of a vocabulary shard's row state
+MAX_SHARDS = 4096
 
 
 class RllossCfg(ctypes.Structure):
@@ -71,6 +73,16 @@ def _load():
     lib.rlloss_forward_e4m3.restype = c_int
     lib.rlloss_loss_from_logp.argtypes = [cfgp] + [P] * 10 + [P, c_size_t, P]
     lib.rlloss_loss_from_logp.restype = c_int
+    lib.rlloss_forward_shard.argtypes = [cfgp, P, P, P, P, ctypes.c_int64, P, P, c_size_t, P]
+    lib.rlloss_forward_shard.restype = c_int
+    lib.rlloss_shard_loss_workspace_bytes.argtypes = [cfgp]
+    lib.rlloss_shard_loss_workspace_bytes.restype = c_size_t
+    lib.rlloss_loss_from_shards.argtypes = [cfgp, c_int32] + [P] * 13 + [P, c_size_t, P]
+    lib.rlloss_loss_from_shards.restype = c_int
+    lib.rlloss_backward_shard_workspace_bytes.argtypes = [cfgp]
+    lib.rlloss_backward_shard_workspace_bytes.restype = c_size_t
+    lib.rlloss_backward_shard.argtypes = [cfgp, P, P, P, P, ctypes.c_int64, P, P, P, P, P, P, c_size_t, P]
+    lib.rlloss_backward_shard.restype = c_int
     lib.rlloss_get_device_status.argtypes = [P, ctypes.POINTER(c_int32)]
     lib.rlloss_get_device_status.restype = c_int
     lib.rlloss_get_backward_rows.argtypes = [P, ctypes.POINTER(c_int32)]
@@ -157,6 +169,36 @@ def rlloss_loss_from_logp(cfg, logp, entropy, old_logp, ref_logp, adv, mask, out
                                      _p(out_dlogp), _p(out_entropy_mask), _p(workspace),
                                      c_size_t(0 if workspace is None else workspace.numel()),
                                      _stream(stream))
+
+
+def rlloss_forward_shard(cfg, X, W, b, targets, v_begin, out_state, workspace, stream=None) -> int:
+    return lib.rlloss_forward_shard(ctypes.byref(cfg), _p(X), _p(W), _p(b), _p(targets), ctypes.c_int64(v_begin),
+                                    _p(out_state), _p(workspace),
+                                    c_size_t(0 if workspace is None else workspace.numel()), _stream(stream))
+
+
+def rlloss_shard_loss_workspace_bytes(cfg: RllossCfg) -> int:
+    return int(lib.rlloss_shard_loss_workspace_bytes(ctypes.byref(cfg)))
+
+
+def rlloss_loss_from_shards(cfg, nshards, states, targets, old_logp, ref_logp, adv, mask, out_loss, out_metrics,
+                            out_lse, out_dlogp, out_logp, out_entropy, out_entropy_mask, workspace,
+                            stream=None) -> int:
+    return lib.rlloss_loss_from_shards(ctypes.byref(cfg), c_int32(nshards), _p(states), _p(targets), _p(old_logp),
+                                       _p(ref_logp), _p(adv), _p(mask), _p(out_loss), _p(out_metrics), _p(out_lse),
+                                       _p(out_dlogp), _p(out_logp), _p(out_entropy), _p(out_entropy_mask),
+                                       _p(workspace), c_size_t(0 if workspace is None else workspace.numel()),
+                                       _stream(stream))
+
+
+def rlloss_backward_shard_workspace_bytes(cfg: RllossCfg) -> int:
+    return int(lib.rlloss_backward_shard_workspace_bytes(ctypes.byref(cfg)))
+
+
+def rlloss_backward_shard(cfg, X, W, b, targets, v_begin, lse, dlogp, dX, dW, db, workspace, stream=None) -> int:
+    return lib.rlloss_backward_shard(ctypes.byref(cfg), _p(X), _p(W), _p(b), _p(targets), ctypes.c_int64(v_begin),
+                                     _p(lse), _p(dlogp), _p(dX), _p(dW), _p(db), _p(workspace),
+                                     c_size_t(0 if workspace is None else workspace.numel()), _stream(stream))
 
 
 def rlloss_get_device_status(workspace) -> int:
@@ -288,5 +330,60 @@ def loss_from_logp(cfg: RllossCfg, logp, entropy, old_logp, ref_logp, adv, mask,
                                o["dlogp"], o["emask"], workspace, stream)
     if rc != OK:
         raise RllossError(rc, "rlloss_loss_from_logp")
+    o["workspace"] = workspace
+    return o
+
+
+# ---------------------------------------------------------------- vocabulary shards
+def forward_shard(cfg: RllossCfg, X, W, b, targets, v_begin: int, workspace=None, stream=None):
+    """Row states [N, STATE_FLOATS] of the vocabulary shard W (rows
+    [v_begin, v_begin + cfg.V) of the whole vocabulary)."""
+    dev = X.device
+    state = torch.empty(cfg.B * cfg.T, STATE_FLOATS, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(rlloss_forward_workspace_bytes(cfg), dev)
+    rc = rlloss_forward_shard(cfg, X, W, b, targets, v_begin, state, workspace, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_forward_shard")
+    return state, workspace
+
+
+def loss_from_shards(cfg: RllossCfg, states, targets, old_logp, ref_logp, adv, mask, workspace=None, stream=None):
+    """Loss, metrics, lse, dL/dlogp, logp, entropy and entropy mask from the
+    row states of all shards (states: [nshards, N, STATE_FLOATS]; cfg.V is
+    the whole vocabulary)."""
+    dev = states.device
+    N = cfg.B * cfg.T
+    f = lambda: torch.empty(N, dtype=torch.float32, device=dev)
+    o = dict(loss=torch.empty(1, dtype=torch.float32, device=dev),
+             metrics=torch.empty(NMETRICS, dtype=torch.float32, device=dev),
+             lse=f(), dlogp=f(), logp=f(), entropy=f(), emask=torch.empty(N, dtype=torch.uint8, device=dev))
+    if workspace is None:
+        workspace = alloc_workspace(rlloss_shard_loss_workspace_bytes(cfg), dev)
+    rc = rlloss_loss_from_shards(cfg, states.shape[0], states, targets, old_logp, ref_logp, adv, mask, o["loss"],
+                                 o["metrics"], o["lse"], o["dlogp"], o["logp"], o["entropy"], o["emask"],
+                                 workspace, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_loss_from_shards")
+    o["workspace"] = workspace
+    return o
+
+
+def backward_shard(cfg: RllossCfg, X, W, b, targets, v_begin: int, lse, dlogp, outputs=None, workspace=None,
+                   stream=None):
+    """This shard's dW rows, db rows and part of dX (cfg.V = the shard's rows)."""
+    dev = X.device
+    N = cfg.B * cfg.T
+    if outputs is None:
+        outputs = dict(dX=torch.empty(N, cfg.H, dtype=torch.float32, device=dev),
+                       dW=torch.empty(cfg.V, cfg.H, dtype=torch.float32, device=dev),
+                       db=torch.empty(cfg.V, dtype=torch.float32, device=dev) if cfg.has_bias else None)
+    if workspace is None:
+        workspace = alloc_workspace(rlloss_backward_shard_workspace_bytes(cfg), dev)
+    o = outputs
+    rc = rlloss_backward_shard(cfg, X, W, b, targets, v_begin, lse, dlogp, o["dX"], o["dW"], o.get("db"),
+                               workspace, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_backward_shard")
     o["workspace"] = workspace
     return o

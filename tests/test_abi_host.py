@@ -88,6 +88,24 @@ def test_accumulate_flag_is_accepted_and_needs_no_extra_workspace():
     assert R.rlloss_workspace_bytes(_cfg(flags=0x20)) == 0
 
 
+def test_vocab_shard_entries_validate_before_any_launch():
+    cfg = _cfg()
+    full = R.rlloss_workspace_bytes(cfg)
+    assert 0 < R.rlloss_shard_loss_workspace_bytes(cfg) < full
+    assert 0 < R.rlloss_backward_shard_workspace_bytes(cfg) <= full
+    assert R.rlloss_shard_loss_workspace_bytes(_cfg(V=0)) == 0
+    assert R.rlloss_backward_shard_workspace_bytes(_cfg(temperature=0.0)) == 0
+    P = [None] * 13
+    assert R.lib.rlloss_loss_from_shards(ctypes.byref(cfg), 0, *P, None, 0, None) == R.EINVAL
+    assert R.lib.rlloss_loss_from_shards(ctypes.byref(cfg), R.MAX_SHARDS + 1, *P, None, 0, None) == R.EINVAL
+    assert R.lib.rlloss_loss_from_shards(ctypes.byref(cfg), 2, *P, None, 0, None) == R.EINVAL
+    assert R.lib.rlloss_forward_shard(ctypes.byref(cfg), None, None, None, None, 0, None, None, 0, None) == R.EINVAL
+    assert R.lib.rlloss_backward_shard(ctypes.byref(cfg), *([None] * 4), 0, *([None] * 6), 0, None) == R.EINVAL
+    e4 = _cfg(dtype=R.FP8_E4M3, H=896)
+    assert R.lib.rlloss_forward_shard(ctypes.byref(e4), None, None, None, None, 0, None, None, 0, None) == \
+        R.EUNSUPPORTED
+
+
 def test_gmpo_sequence_is_rejection_matches_page():
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_constants.json")))
     assert g["gmpo_rejects_sequence_level_is"]["value"] is True
