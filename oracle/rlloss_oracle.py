@@ -390,6 +390,81 @@ def grads(X, W, b, targets, tau, lse, c, dx_rows=None, dw_rows=None, want_db=Tru
 
 
 # ---------------------------------------------------------------------------
+# Vocabulary shards.  The streamed accumulators of "support
+# top_entropy_quantile ...", Details (the log-sum-exp accumulator and a second
+# online accumulator for the entropy) combine over disjoint vocabulary
+# ranges: for a shard with reference m, s = sum e^(z-m), w = sum e^(z-m)(z-m),
+# and with M = max_k m_k over the shards,
+#   S = sum_k e^(m_k-M) s_k,   Wt = sum_k e^(m_k-M) (w_k + (m_k-M) s_k),
+#   lse = M + log S,           H = lse - E_p[z] = log S - Wt / S.
+# The gradient terms restrict to the shard's columns: G_shard = G[:, shard],
+# dX = sum over shards of G_shard W_shard, dW and db are the shard's rows.
+# ---------------------------------------------------------------------------
+
+def shard_state(X, W_shard, b_shard, targets, tau, v_begin):
+    """fp64 per-row state of the vocabulary rows [v_begin, v_begin + len(W_shard))."""
+    X = as_f64(X); Ws = as_f64(W_shard); bs = as_f64(b_shard); y = as_i64(targets)
+    N, Vs = X.shape[0], Ws.shape[0]
+    m = np.empty(N); s = np.empty(N); w = np.empty(N); zy = np.full(N, np.nan)
+    for k0 in range(0, N, ROW_BLOCK):
+        r = np.arange(k0, min(N, k0 + ROW_BLOCK))
+        z = logits_rows(X, Ws, bs, tau, r)
+        mm = z.max(axis=1)
+        e = np.exp(z - mm[:, None])
+        m[r] = mm
+        s[r] = e.sum(axis=1)
+        w[r] = (e * (z - mm[:, None])).sum(axis=1)
+        yl = y[r] - v_begin
+        inside = (yl >= 0) & (yl < Vs)
+        zy[r[inside]] = z[np.nonzero(inside)[0], yl[inside]]
+    return dict(m=m, s=s, w=w, zy=zy)
+
+
+def merge_states(states, targets=None, V=None):
+    """(lse, logp, entropy) fp64 from the states of disjoint shards.  logp is
+    NaN where no shard holds the target (or the target lies outside [0, V))."""
+    M = np.max([st["m"] for st in states], axis=0)
+    S = np.zeros_like(M); Wt = np.zeros_like(M)
+    zy = np.full_like(M, np.nan)
+    for st in states:
+        f = np.exp(st["m"] - M)
+        S += f * st["s"]
+        Wt += f * (st["w"] + (st["m"] - M) * st["s"])
+        have = ~np.isnan(st["zy"])
+        zy[have] = st["zy"][have]
+    lse = M + np.log(S)
+    ent = np.log(S) - Wt / S
+    logp = zy - lse
+    if targets is not None and V is not None:
+        y = as_i64(targets)
+        logp[(y < 0) | (y >= V)] = np.nan
+    return lse, logp, ent
+
+
+def shard_grads(X, W_shard, b_shard, targets, tau, v_begin, lse, c):
+    """This shard's part of dX, its dW rows and its db rows (fp64), from the
+    whole vocabulary's lse and c = dL/dlogp."""
+    X = as_f64(X); Ws = as_f64(W_shard); bs = as_f64(b_shard); y = as_i64(targets)
+    N, Vs = X.shape[0], Ws.shape[0]
+    lse = np.asarray(lse, np.float64); c = np.asarray(c, np.float64)
+    dX = np.zeros((N, X.shape[1])); dW = np.zeros((Vs, X.shape[1]))
+    db = np.zeros(Vs) if bs is not None else None
+    for k0 in range(0, N, ROW_BLOCK):
+        r = np.arange(k0, min(N, k0 + ROW_BLOCK))
+        z = logits_rows(X, Ws, bs, tau, r)
+        G = -np.exp(z - lse[r][:, None])
+        yl = y[r] - v_begin
+        inside = np.nonzero((yl >= 0) & (yl < Vs))[0]
+        G[inside, yl[inside]] += 1.0
+        G *= (c[r] / tau)[:, None]
+        dX[r] = G @ Ws
+        dW += G.T @ X[r]
+        if db is not None:
+            db += G.sum(axis=0)
+    return dX, dW, db
+
+
+# ---------------------------------------------------------------------------
 # Whole pipeline.
 # ---------------------------------------------------------------------------
 

@@ -422,3 +422,63 @@ def test_db_sums_to_zero_and_sampled_rows_agree():
     assert np.allclose(dX, out["dX"][rows], rtol=1e-13, atol=1e-15)
     assert np.allclose(dW, out["dW"][vs], rtol=1e-13, atol=1e-15)
     assert np.allclose(db, out["db"], rtol=1e-13, atol=1e-15)
+
+
+# --- vocabulary shards ------------------------------------------------------
+
+def _shard_bounds(sizes):
+    cut = np.concatenate([[0], np.cumsum(sizes)]).astype(int)
+    return [(int(cut[k]), int(cut[k + 1])) for k in range(len(sizes))]
+
+
+def test_shard_states_merge_to_library_logsumexp_and_entropy():
+    """States of uneven shards (one of a single row, one whose logits sit 60
+    above the rest) merge, in any order, to scipy's logsumexp, the entropy
+    -sum p log p of scipy's softmax, and the target log-prob."""
+    from scipy.special import logsumexp, softmax
+    rng = np.random.default_rng(41)
+    X, W, b, y = _rand_problem(rng, 40, 16, 300)
+    b[150:151] += 60.0
+    tau = 0.8
+    sizes = [37, 113, 1, 149]
+    states = [O.shard_state(X, W[v0:v1], b[v0:v1], y, tau, v0) for v0, v1 in _shard_bounds(sizes)]
+    z = (X @ W.T + b) / tau
+    lse_ref = logsumexp(z, axis=1)
+    p = softmax(z, axis=1)
+    ent_ref = -(p * np.log(p, where=p > 0, out=np.zeros_like(p))).sum(axis=1)
+    for order in (states, states[::-1], [states[2], states[0], states[3], states[1]]):
+        lse, logp, ent = O.merge_states(order, y, 300)
+        assert np.allclose(lse, lse_ref, rtol=0, atol=1e-12)
+        assert np.allclose(logp, z[np.arange(40), y] - lse_ref, rtol=0, atol=1e-12)
+        assert np.allclose(ent, ent_ref, rtol=0, atol=1e-10)
+
+
+def test_missing_shard_leaves_its_targets_without_logp():
+    rng = np.random.default_rng(42)
+    X, W, b, y = _rand_problem(rng, 30, 8, 90)
+    bounds = _shard_bounds([30, 30, 30])
+    states = [O.shard_state(X, W[v0:v1], b[v0:v1], y, 1.0, v0) for v0, v1 in bounds]
+    _, logp, _ = O.merge_states([states[0], states[2]], y, 90)
+    missing = (y >= 30) & (y < 60)
+    assert missing.any() and (~missing).any()
+    assert np.all(np.isnan(logp[missing])) and np.all(np.isfinite(logp[~missing]))
+    y_bad = y.copy(); y_bad[0] = 90
+    _, logp, _ = O.merge_states(states, y_bad, 90)
+    assert np.isnan(logp[0]) and np.all(np.isfinite(logp[1:]))
+
+
+def test_shard_gradients_sum_to_the_full_vocabulary_gradients():
+    """dX is the sum of the shards' parts; dW and db are the shards' rows
+    stacked (the full gradients are pinned to autograd above)."""
+    B, T, X, W, b, y, tau, old, ref, mask, adv = _small_gmpo_case(14)
+    prob = O.Problem(B, T, O.GMPO, 0.2, 0.3, 0.04, tau)
+    out = O.fwd_bwd(prob, X, W, b, y, old, ref, adv, mask)
+    V = W.shape[0]
+    sizes = [V // 3, 1, V - V // 3 - 1]
+    dX = np.zeros_like(out["dX"]); dWs = []; dbs = []
+    for v0, v1 in _shard_bounds(sizes):
+        px, pw, pb = O.shard_grads(X, W[v0:v1], b[v0:v1], y, tau, v0, out["lse"], out["c"])
+        dX += px; dWs.append(pw); dbs.append(pb)
+    assert np.allclose(dX, out["dX"], rtol=1e-11, atol=1e-15)
+    assert np.allclose(np.concatenate(dWs), out["dW"], rtol=1e-11, atol=1e-15)
+    assert np.allclose(np.concatenate(dbs), out["db"], rtol=1e-11, atol=1e-15)
