@@ -589,6 +589,12 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
   // output element still receives one addition per chunk (dX rows: one per
   // call), so the sums keep a fixed order.
   const bool acc = (cfg->flags & RLLOSS_FLAG_ACCUMULATE) != 0;
+  // Compacted backward without ACCUMULATE: the dX rows of each chunk are added
+  // straight into the zeroed dX at their original rows (two k halves, two
+  // addends); with ACCUMULATE they go through the chunk buffer and a
+  // read-add-write scatter, so each dX element gets one addition per call.
+  const bool dx_direct = p.compact && !acc;
+  const bool dx_vec = p.H % 4 == 0 && (reinterpret_cast<uintptr_t>(dX) & 15u) == 0;
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dl);
   const int lo_off = p.fp32 ? p.Vp : 0;
   int* rows_total = reinterpret_cast<int*>(ws + p.o_status + kBackwardRowsOffset);
@@ -619,8 +625,12 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       cp.lse2c = reinterpret_cast<float*>(ws + p.o_lse2c);
       cp.tgtc = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
       cp.xc = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
+      if (!acc) {   // the gather zeroes dX; the dX/dW launch adds the kept rows into it
+        cp.dx_zero = dX;
+        cp.H = p.H;
+        cp.dx_vec = dx_vec ? 1 : 0;
+      }
       RL_TRY(launch_compact(cp, st));
-      if (!acc) RL_TRY(cudaMemsetAsync(dX, 0, size_t(p.N) * p.H * 4, st));
       ph.launched(2);
       Xb = cp.xc;
       tg_b = cp.tgtc;
@@ -724,11 +734,18 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       hp.nc_max = nc;
       hp.status = status;
       hp.limit_ns = kWaitLimitNs;
+      if (dx_direct) {
+        hp.dx_idx = cidx;
+        hp.dx_out = dX;
+        hp.dx_ld = p.H;
+        hp.dx_vec = dx_vec ? 1 : 0;
+      }
       Phase ph(st, 3);
-      if (px.reduce && !dx_in_place_acc) RL_TRY(cudaMemsetAsync(dx_out, 0, size_t(nc) * p.H * 4, st));
+      if (px.reduce && !dx_in_place_acc && !dx_direct)
+        RL_TRY(cudaMemsetAsync(dx_out, 0, size_t(nc) * p.H * 4, st));
       RL_TRY(launch_gemmH(hp, px.Mt * px.Ht * px.ksplit + pw.Mt * pw.Ht, st));
       ph.launched();
-      if (p.compact) {
+      if (p.compact && !dx_direct) {
         RL_TRY(launch_scatter_rows(dxc, cidx, rows_total, n0, nc, p.H, dX, acc, st));
         ph.launched();
       }

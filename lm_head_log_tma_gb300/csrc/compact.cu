@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kCompactBlock) compact_count_kernel(CompactPar
 // Block b handles the 32 rows of group b: each kept row goes to its group's
 // offset plus its rank in the group, with its index, coefficient, lse and
 // target; then the block copies the kept X rows (16-byte words spread over
-// all threads).
+// all threads) and, with dx_zero set, zeroes the group's gradient rows.
 __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactParams p) {
   __shared__ int rows[kGroup];
   __shared__ int cnt;
@@ -108,6 +108,19 @@ __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactPa
     const int r = w / words, c = w - r * words;
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + size_t(rows[r]) * p.Kx) + c);
     reinterpret_cast<uint4*>(p.xc + size_t(base + r) * p.Kx)[c] = v;
+  }
+  if (p.dx_zero) {
+    const int r0 = g * kGroup;
+    const int nr = min(kGroup, p.N - r0);
+    float* d = p.dx_zero + size_t(r0) * p.H;
+    if (p.dx_vec) {
+      const int n4 = nr * (p.H / 4);
+      for (int i = threadIdx.x; i < n4; i += kCompactBlock)
+        reinterpret_cast<float4*>(d)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      const int n1 = nr * p.H;
+      for (int i = threadIdx.x; i < n1; i += kCompactBlock) d[i] = 0.f;
+    }
   }
 }
 

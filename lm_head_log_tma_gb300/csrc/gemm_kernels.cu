@@ -639,6 +639,31 @@ struct HPolicy {
     const int y0 = t.m0 + 128 * int(rank) + q * 32;
     const int c_begin = half ? 4 : 0, c_end = half ? 7 : 4;
     const bool no_k = t.kb_end <= t.kb_begin;   // empty sum (a chunk without rows): store zeros
+    if (t.seg == 0 && p.dx_idx) {
+      // dX rows of the compacted backward, added at their original rows.
+      const int nc = min(max(*p.rows_total - p.n0, 0), p.nc_max);
+      const int y = y0 + lane;
+      float* dst = (y < nc && !no_k) ? p.dx_out + size_t(p.dx_idx[p.n0 + y]) * p.dx_ld : nullptr;
+#pragma unroll 1
+      for (int c = c_begin; c < c_end; ++c) {
+        const int x0 = t.n0 + sub * kNS + c * 32;
+        if (x0 >= pr.Hout) break;
+        float v[32];
+        tmem_ld32(taddr + uint32_t(c * 32), v);   // warp-collective: every lane loads
+        if (!dst) continue;
+        if (p.dx_vec && x0 + 32 <= pr.Hout) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            atomicAdd(reinterpret_cast<float4*>(dst + x0 + 4 * k),
+                      make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (x0 + i < pr.Hout) atomicAdd(dst + x0 + i, v[i]);
+        }
+      }
+      return;
+    }
 #pragma unroll 1
     for (int c = c_begin; c < c_end; ++c) {
       const int x0 = t.n0 + sub * kNS + c * 32;

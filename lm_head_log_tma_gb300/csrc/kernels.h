@@ -117,6 +117,15 @@ struct HParams {
   int n0, nc_max;
   int nseg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];  // inner-coordinate offsets of each product term
+  // Optional (problem 0 of the compacted backward): output row r of the chunk
+  // is added straight into dx_out[dx_idx[n0 + r]][...] (row stride dx_ld),
+  // with float4 atomic adds when dx_vec, else scalar ones, instead of going
+  // through tmO[0].  dx_out must hold zeros there, and at most two additions
+  // reach an element (ksplit <= 2), so the sum does not depend on their order.
+  const int* dx_idx;
+  float* dx_out;
+  int dx_ld;
+  int dx_vec;
   int* status;
   unsigned long long limit_ns;
 };
@@ -186,6 +195,9 @@ struct CompactParams {
   float* lse2c;               // [Ncap]
   int64_t* tgtc;              // [Ncap]
   __nv_bfloat16* xc;          // [Ncap, Kx]
+  float* dx_zero;             // optional: [N, H] gradient buffer the gather sets to zero
+  int H;
+  int dx_vec;                 // dx_zero is 16-byte aligned and H % 4 == 0
 };
 int compact_groups(int N);   // 32-row groups
 // Row tiles of tile_rows rows holding a row with mask != 0: flags[R], their
