@@ -507,8 +507,10 @@ struct DlPolicy {
 // subs (TMEM columns 0.. and 256..): each k-block's A tile (G rows) feeds
 // both, so an A byte carries 448 columns of work.  Output rows leave through
 // shared memory as 32x32 fp32 boxes with TMA stores (or TMA reduce-adds when
-// accumulating).  One launch runs up to two such problems (dX and dW of a
-// chunk) with a balanced static schedule; see for_each_tile.
+// accumulating); the dX rows of the compacted backward are instead added from
+// registers straight into dX at their original rows (HParams::dx_idx).  One
+// launch runs up to two such problems (dX and dW of a chunk) with a balanced
+// static schedule; see for_each_tile.
 struct HPolicy {
   static constexpr int kCluster = 2;
   static constexpr int kStages = 4;
@@ -827,10 +829,6 @@ static cudaError_t launch_engine(const typename P::Params& prm, int units, cudaS
 int fwd_resident_clusters(int cluster) {
   cudaError_t e;
   return cluster == 2 ? engine_resident<FwdPolicy<2, false, 2>>(&e) : engine_resident<FwdPolicy<1>>(&e);
-}
-int dl_resident_clusters(int cluster) {
-  cudaError_t e;
-  return cluster == 2 ? engine_resident<DlPolicy<2, 2>>(&e) : engine_resident<DlPolicy<1>>(&e);
 }
 int gemmH_resident_clusters() {
   cudaError_t e;

@@ -160,7 +160,6 @@ struct LossParams {
 // number of clusters that can be resident at once (or fewer).  cluster = 1
 // or 2 CTAs per 128 * cluster-row tile.
 int fwd_resident_clusters(int cluster);
-int dl_resident_clusters(int cluster);
 int gemmH_resident_clusters();
 // kbx: 128-byte boxes per operand per pipeline stage (2: pair tiles with one K segment)
 cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, int kbx, cudaStream_t st);

@@ -307,6 +307,31 @@ def test_compacted_backward_matches_dense(R, spec):
     _grads_close(a, b)
 
 
+def test_misaligned_gradient_buffer_is_rejected(R):
+    """dX must start on a 16-byte boundary (its rows leave through TMA maps
+    and float4 adds): a dX one float past such a boundary is rejected before
+    any launch, and the buffer is left as it was."""
+    spec = MID[1]
+    case = Case(spec)
+    a = case.run_gpu(R, per_token=False)
+    assert a["status"] == 0, hex(a["status"])
+    i = case.inp
+    N, H = spec.N, spec.H
+    buf = torch.full((N * H + 8,), float("nan"), device="cuda")
+    dX = buf[1:1 + N * H].view(N, H)
+    assert dX.data_ptr() % 16 == 4
+    outs = dict(a)
+    outs["dX"] = dX
+    cfg = parity_cfg(R, spec)
+    t = lambda x: None if x is None else x.cuda()
+    with pytest.raises(R.RllossError) as e:
+        R.fwd_bwd(cfg, t(i.X), t(i.W), t(i.b), t(i.targets), t(case.old), t(case.ref), t(i.adv), t(i.mask),
+                  workspace=a["workspace"], outputs=outs, per_token=False)
+    assert e.value.code == R.EINVAL
+    torch.cuda.synchronize()
+    assert torch.isnan(buf).all()
+
+
 def test_backward_without_gradient_rows(R):
     """All advantages 0 and no KL: every c_n is 0, nothing is kept, and dX,
     dW, db come out exactly zero, in one chunk and in several."""
