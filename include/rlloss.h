@@ -295,6 +295,84 @@ int rlloss_backward_shard(const rlloss_cfg* cfg, const void* X, const void* W, c
                           float* dX, float* dW, float* db, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* ---- Batch split over ranks by whole sequences (data parallel).
+ * Each rank holds some whole sequences of one batch of B_global sequences.
+ * Every per-sequence quantity is then local; what couples the ranks is the
+ * batch-global entropy threshold ("support top_entropy_quantile in fused
+ * linear GRPO loss", Details: the quantile is taken over the active tokens
+ * of the whole batch, not per chunk), the batch size of GMPO's mean over
+ * sequences ("Add GMPO to fused linear GRPO loss", Details: per-sample
+ * reduction), and sums (metrics, dW, db).  Per step, on every rank:
+ *   1. rlloss_forward (its rows) -> logp, entropy, lse;
+ *   2. only when top_entropy_quantile < 1: for pass = 0 .. RLLOSS_SELECT_PASSES-1,
+ *      rlloss_entropy_hist (this rank's counts), an all-reduce (sum) of the
+ *      RLLOSS_SELECT_COUNTS counts over ranks, rlloss_entropy_select (the
+ *      summed counts); every rank's select state then holds the same
+ *      threshold, bit for bit the one a single device computes for the
+ *      whole batch (exact order statistics by radix selection);
+ *   3. rlloss_loss_from_logp_dp -> dL/dlogp of its tokens for the whole
+ *      batch's loss, the entropy mask of its tokens, and its 8 batch sums;
+ *      an all-reduce (sum) of the sums; rlloss_metrics_from_sums -> loss and
+ *      metrics of the whole batch;
+ *   4. rlloss_backward_shard with the whole vocabulary (v_begin = 0) ->
+ *      dX of its rows, and its dW, db parts; dW and db are sums over ranks.
+ * The library makes no collective call: the exchanges are the caller's. */
+#define RLLOSS_SELECT_PASSES 4
+#define RLLOSS_SELECT_COUNTS 512   /* uint32 counts per pass */
+#define RLLOSS_NSUMS 8             /* doubles of batch sums */
+
+/* Bytes of device memory a select state needs (256).  The state is opaque;
+ * one state per rank, 16-byte aligned, kept across the passes of one step. */
+size_t rlloss_select_state_bytes(void);
+
+/* Pass `pass` (0 .. RLLOSS_SELECT_PASSES-1) of the distributed entropy
+ * quantile: writes into counts (device, RLLOSS_SELECT_COUNTS uint32, zeroed
+ * by the call) this rank's histogram of its active tokens (mask != 0) under
+ * the selection prefixes in select_state (not read at pass 0).  entropy,
+ * mask: [N] device (N may be 0).  RLLOSS_EINVAL for a bad pass or pointer. */
+int rlloss_entropy_hist(const float* entropy, const uint8_t* mask, int64_t N, int32_t pass,
+                        const void* select_state, uint32_t* counts, void* stream);
+
+/* The select step of pass `pass` from counts summed over every rank (device,
+ * RLLOSS_SELECT_COUNTS uint32), q = top_entropy_quantile in [0, 1]: updates
+ * select_state.  Pass 0 initialises the state (the active-token count is the
+ * sum of the counts).  After the last pass the state holds the threshold:
+ * linear interpolation between the order statistics at (1-q)(n_act-1) of
+ * the batch's active entropies, NaN if no token is active. */
+int rlloss_entropy_select(int32_t pass, const uint32_t* counts, float q, void* select_state, void* stream);
+
+/* Copy the threshold held by select_state into *threshold (host).
+ * Synchronous; call after the stream has finished the last select step. */
+int rlloss_select_threshold(const void* select_state, double* threshold);
+
+/* The loss stage of one rank.  cfg describes this rank's sequences (cfg.B of
+ * them, T tokens each); B_global >= cfg.B is the whole batch's sequence
+ * count.  select_state: the finished state of step 2 when the entropy mask
+ * is on (top_entropy_quantile < 1 or RLLOSS_FLAG_FORCE_ENTROPY_PATH), else
+ * NULL; entropy [N] is then required.  Other inputs as for
+ * rlloss_loss_from_logp.  Writes out_sums (device, RLLOSS_NSUMS doubles, this
+ * rank's share; each entry adds over ranks):
+ *   [0] sum of the sequence terms (GMPO: -A_i r_i ebar_i + beta KL_i, before
+ *       the 1/B_global of the mean; GSPO: minus the summed objective),
+ *   [1] active tokens, [2] clipped tokens (GSPO: clipped sequences),
+ *   [3] sum of K3 KL over active tokens, [4] tokens kept by the entropy mask
+ *   (GSPO: active tokens), [5] sum of the sequence log ratios and [6] of the
+ *   sequence ratios over sequences with tokens, [7] sequences with tokens;
+ * and, each optional, out_dlogp [N] = dL/dlogp_n of the whole batch's loss,
+ * out_entropy_mask [N].  Workspace: rlloss_loss_workspace_bytes(cfg). */
+int rlloss_loss_from_logp_dp(const rlloss_cfg* cfg, int32_t B_global, const void* select_state,
+                             const float* logp, const float* entropy, const float* old_logp,
+                             const float* ref_logp, const float* adv, const uint8_t* mask,
+                             double* out_sums, float* out_dlogp, uint8_t* out_entropy_mask,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Host only, no device access: the whole batch's loss (*out_loss) and
+ * metrics (out_metrics [RLLOSS_NMETRICS], the layout of rlloss_fwd_bwd) from
+ * the batch sums added over ranks (sums: host, RLLOSS_NSUMS doubles) and the
+ * threshold of step 2 (NaN without the entropy mask). */
+int rlloss_metrics_from_sums(const rlloss_cfg* cfg, int32_t B_global, const double* sums, double threshold,
+                             float* out_loss, float* out_metrics);
+
 /* Copy the device status word of ``workspace`` (the one a previous call used)
  * into *status.  Synchronous; call after the stream has finished.  Returns
  * RLLOSS_ECUDA if the copy failed. */

@@ -415,6 +415,7 @@ LossParams loss_params(const rlloss_cfg* c, const Plan& p, char* ws) {
   lp.status = reinterpret_cast<int*>(ws + p.o_status);
   lp.k3 = p.ent ? reinterpret_cast<const double*>(ws + p.o_k3) : nullptr;
   lp.adv_per_token = (c->flags & RLLOSS_FLAG_ADV_PER_TOKEN) ? 1 : 0;
+  lp.Bg = double(c->B);
   return lp;
 }
 
@@ -930,6 +931,102 @@ int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float*
   g_launches += out_dlogp ? 2 : 1;
   if (out_entropy_mask)
     RL_TRY(cudaMemcpyAsync(out_entropy_mask, p.ent ? emask : mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
+  return RLLOSS_OK;
+}
+
+// ---- Batch split over ranks by whole sequences (see rlloss.h).
+
+size_t rlloss_select_state_bytes(void) { return size_t(kSelectStateBytes); }
+
+int rlloss_entropy_hist(const float* entropy, const uint8_t* mask, int64_t N, int32_t pass, const void* select_state,
+                        uint32_t* counts, void* stream) {
+  if (N < 0 || pass < 0 || pass >= kSelectPasses || !counts) return RLLOSS_EINVAL;
+  if (N > 0 && (!entropy || !mask)) return RLLOSS_EINVAL;
+  if (pass > 0 && !select_state) return RLLOSS_EINVAL;
+  if (select_state && !aligned(select_state, 16)) return RLLOSS_EINVAL;
+  RL_TRY(launch_entropy_hist(entropy, mask, N, pass, select_state, counts, static_cast<cudaStream_t>(stream)));
+  g_launches += N > 0 ? 1 : 0;
+  return RLLOSS_OK;
+}
+
+int rlloss_entropy_select(int32_t pass, const uint32_t* counts, float q, void* select_state, void* stream) {
+  if (pass < 0 || pass >= kSelectPasses || !counts || !select_state || !aligned(select_state, 16)) return RLLOSS_EINVAL;
+  if (!(q >= 0.f && q <= 1.f)) return RLLOSS_EINVAL;
+  RL_TRY(launch_entropy_select(pass, counts, double(q), select_state, static_cast<cudaStream_t>(stream)));
+  g_launches += 1;
+  return RLLOSS_OK;
+}
+
+int rlloss_select_threshold(const void* select_state, double* threshold) {
+  if (!select_state || !threshold) return RLLOSS_EINVAL;
+  return cuda_rc(cudaMemcpy(threshold, select_state, sizeof(double), cudaMemcpyDeviceToHost));
+}
+
+int rlloss_loss_from_logp_dp(const rlloss_cfg* cfg, int32_t B_global, const void* select_state, const float* logp,
+                             const float* entropy, const float* old_logp, const float* ref_logp, const float* adv,
+                             const uint8_t* mask, double* out_sums, float* out_dlogp, uint8_t* out_entropy_mask,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  int e = validate_common(cfg);
+  if (e) return e;
+  if (B_global < cfg->B) return RLLOSS_EINVAL;
+  if (!logp || !old_logp || !adv || !mask || !out_sums || !workspace) return RLLOSS_EINVAL;
+  if (cfg->beta != 0.f && !ref_logp) return RLLOSS_EINVAL;
+  const Plan p = make_plan(cfg, kLossOnly);
+  if (p.ent && (!entropy || !select_state || !aligned(select_state, 16))) return RLLOSS_EINVAL;
+  if (!aligned(workspace, 256) || workspace_bytes < p.total) return RLLOSS_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  RL_TRY(cudaMemsetAsync(ws + p.o_status, 0, p.o_tickets + size_t(p.B) * 4 - p.o_status, st));
+  uint8_t* emask = reinterpret_cast<uint8_t*>(ws + p.o_emask);
+  if (p.ent) {   // the batch-global threshold comes from the ranks' joint selection
+    RL_TRY(launch_entropy_apply(entropy, mask, p.N, select_state, emask, st));
+    g_launches += 1;
+  }
+  LossParams lp = loss_params(cfg, p, ws);
+  lp.k3 = p.ent ? static_cast<const double*>(select_state) : nullptr;
+  lp.Bg = double(B_global);
+  lp.logp = logp;
+  lp.logp_is_f64 = 0;
+  lp.old_logp = old_logp;
+  lp.ref_logp = ref_logp;
+  lp.adv = adv;
+  lp.mask = mask;
+  lp.emask = p.ent ? emask : nullptr;
+  lp.dlogp = out_dlogp;
+  lp.out_loss = nullptr;
+  lp.out_metrics = nullptr;
+  lp.out_sums = out_sums;
+  RL_TRY(launch_loss(lp, st));
+  g_launches += out_dlogp ? 2 : 1;
+  if (out_entropy_mask)
+    RL_TRY(cudaMemcpyAsync(out_entropy_mask, p.ent ? emask : mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
+  return RLLOSS_OK;
+}
+
+int rlloss_metrics_from_sums(const rlloss_cfg* cfg, int32_t B_global, const double* sums, double threshold,
+                             float* out_loss, float* out_metrics) {
+  if (!cfg || !sums || !out_loss || !out_metrics || B_global < 1) return RLLOSS_EINVAL;
+  if (cfg->loss_type != RLLOSS_GMPO && cfg->loss_type != RLLOSS_GSPO_TOKEN) return RLLOSS_EINVAL;
+  const bool gmpo = cfg->loss_type == RLLOSS_GMPO;
+  const double Bg = double(B_global);
+  const double n_act = sums[1], clip = sums[2], kl = sums[3], kept = sums[4], sx = sums[5], sr = sums[6],
+               nh = sums[7];
+  const double loss = gmpo ? sums[0] / Bg : sums[0];
+  float* m = out_metrics;
+  if (gmpo) {
+    m[0] = n_act > 0 ? float(clip / n_act) : 0.f;
+    m[2] = (cfg->beta != 0.f && n_act > 0) ? float(kl / n_act) : 0.f;
+  } else {
+    m[0] = float(clip / Bg);
+    m[2] = 0.f;
+  }
+  m[1] = float(clip);
+  m[3] = float(n_act);
+  m[4] = float(threshold);
+  m[5] = float(kept);
+  m[6] = nh > 0 ? float(sx / nh) : 0.f;
+  m[7] = nh > 0 ? float(sr / nh) : 0.f;
+  *out_loss = float(loss);
   return RLLOSS_OK;
 }
 

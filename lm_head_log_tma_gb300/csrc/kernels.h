@@ -151,8 +151,12 @@ struct LossParams {
   int slices;                 // blocks per sequence
   float* coef;                // optional: c / tau
   float* dlogp;               // optional: c
-  float* out_loss;
+  float* out_loss;            // null: write out_sums only
   float* out_metrics;
+  // Batch size of the GMPO mean and the GSPO clip fraction: B on one device,
+  // every rank's sequences together when the batch is split over ranks.
+  double Bg;
+  double* out_sums;           // optional: the 8 additive batch sums (see fold_batch)
   int* status;
 };
 
@@ -222,6 +226,18 @@ constexpr int kK3Bytes = 256 + 4 * 512 * 4;
 cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long N, double q, void* k3_ws,
                                 uint8_t* emask, cudaStream_t st);
 cudaError_t launch_loss(const LossParams& p, cudaStream_t st);
+// The entropy quantile split into its passes, for batches whose tokens are
+// spread over ranks: pass `pass` histogram of the active keys under the
+// state's prefixes (counts [kSelectCounts], zeroed here first); the select
+// step from (all ranks' summed) counts; the mask from the final state.
+constexpr int kSelectPasses = 4;
+constexpr int kSelectCounts = 512;
+constexpr int kSelectStateBytes = 256;
+cudaError_t launch_entropy_hist(const float* ent, const uint8_t* mask, long long N, int pass, const void* state,
+                                uint32_t* counts, cudaStream_t st);
+cudaError_t launch_entropy_select(int pass, const uint32_t* counts, double q, void* state, cudaStream_t st);
+cudaError_t launch_entropy_apply(const float* ent, const uint8_t* mask, long long N, const void* state,
+                                 uint8_t* emask, cudaStream_t st);
 int loss_slices(int B, int T, int sms);
 int fused_loss_slices(int T);
 cudaError_t launch_merge_loss(const MergeParams& mp, const LossParams& p, cudaStream_t st);

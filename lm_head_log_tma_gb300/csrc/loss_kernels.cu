@@ -131,6 +131,37 @@ cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long
   return cudaGetLastError();
 }
 
+static_assert(sizeof(K3State) <= kSelectStateBytes, "select state");
+static_assert(kK3HistOff == kSelectStateBytes, "state then histograms");
+
+static int k3_blocks(long long N) {
+  long long blocks = (N + 256 * 8 - 1) / (256 * 8);
+  if (blocks < 1) blocks = 1;
+  if (blocks > 2048) blocks = 2048;
+  return int(blocks);
+}
+
+cudaError_t launch_entropy_hist(const float* ent, const uint8_t* mask, long long N, int pass, const void* state,
+                                uint32_t* counts, cudaStream_t st) {
+  cudaError_t err = cudaMemsetAsync(counts, 0, kSelectCounts * sizeof(uint32_t), st);
+  if (err != cudaSuccess) return err;
+  if (N > 0)
+    k3_hist_kernel<<<k3_blocks(N), 256, 0, st>>>(ent, mask, N, pass, static_cast<const K3State*>(state), counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_entropy_select(int pass, const uint32_t* counts, double q, void* state, cudaStream_t st) {
+  k3_select_kernel<<<1, 32, 0, st>>>(pass, static_cast<K3State*>(state), counts, q);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_entropy_apply(const float* ent, const uint8_t* mask, long long N, const void* state,
+                                 uint8_t* emask, cudaStream_t st) {
+  if (N > 0)
+    k3_mask_kernel<<<k3_blocks(N), 256, 0, st>>>(ent, mask, N, static_cast<const K3State*>(state), emask);
+  return cudaGetLastError();
+}
+
 // ----------------------------------------------------------------------- K2
 constexpr int kLossThreads = 256;
 constexpr int kFusedRows = 256 / kMergeLanes;   // rows per block of the fused merge + loss kernel
@@ -215,7 +246,7 @@ __device__ __forceinline__ void seq_record(const LossParams& p, const double (&s
     r8[0] = ni > 0 ? -A * r * ebar + p.beta * klt : 0.0;
     r8[2] = s5[4]; r8[3] = s5[3]; r8[4] = s5[2]; r8[5] = mean_x; r8[6] = r; r8[7] = ebar;
     if (ni > 0) {
-      r8[8] = 1.0 / (double(p.B) * ni);
+      r8[8] = 1.0 / (p.Bg * ni);
       r8[9] = -A * r * ebar * r8[8];
     }
   } else if (ni == 0) {
@@ -273,9 +304,13 @@ __device__ __forceinline__ void fold_sequence(const LossParams& p, int i, int la
 }
 
 // Loss and metrics from all sequence records, by one warp, in a fixed order.
+// The eight batch sums (written to out_sums when set; each adds over ranks
+// that hold different sequences of one batch): [0] sum of the sequence terms
+// (GMPO: before the 1/B of the mean), [1] active tokens, [2] clipped tokens
+// (GSPO: clipped sequences), [3] sum of K3 KL, [4] tokens kept by the entropy
+// mask (GSPO: active tokens), [5] sum of sequence log ratios, [6] sum of
+// sequence ratios (both over sequences with tokens), [7] sequences with tokens.
 __device__ __forceinline__ void fold_batch(const LossParams& p, int lane, bool gmpo) {
-  // [0] loss, [1] n_act, [2] clips, [3] KL, [4] kept, [5] sum of log ratios,
-  // [6] sum of ratios, [7] sequences with tokens.
   double f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int j = lane; j < p.B; j += 32) {
     const double* r = p.seqres + size_t(j) * kRec;
@@ -293,15 +328,23 @@ __device__ __forceinline__ void fold_batch(const LossParams& p, int lane, bool g
   }
   warp_sum_k(f);
   if (lane != 0) return;
+  if (p.out_sums) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) p.out_sums[k] = f[k];
+  }
+  if (!p.out_loss) {
+    if (!isfinite(f[0]) && p.status) atomicOr(p.status, RLLOSS_DEV_ENONFINITE);
+    return;
+  }
   double loss = f[0];
   const double n_act = f[1], clip = f[2], kl = f[3], kept = f[4], sx = f[5], sr = f[6], nh = f[7];
   float* m = p.out_metrics;
   if (gmpo) {
-    loss /= double(p.B);
+    loss /= p.Bg;
     m[0] = n_act > 0 ? float(clip / n_act) : 0.f;
     m[2] = (p.beta != 0.0 && n_act > 0) ? float(kl / n_act) : 0.f;
   } else {
-    m[0] = float(clip / double(p.B));
+    m[0] = float(clip / p.Bg);
     m[2] = 0.f;
   }
   m[1] = float(clip);

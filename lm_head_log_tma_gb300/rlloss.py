@@ -30,6 +30,9 @@ FLAG_ACCUMULATE = 0x10
 NMETRICS = 8
 STATE_FLOATS = 8        # floats per token of a vocabulary shard's row state
 MAX_SHARDS = 4096
+SELECT_PASSES = 4       # passes of the distributed entropy quantile
+SELECT_COUNTS = 512     # uint32 counts per pass
+NSUMS = 8               # doubles of batch sums (sequence-split batches)
 
 
 class RllossCfg(ctypes.Structure):
@@ -83,6 +86,19 @@ def _load():
     lib.rlloss_backward_shard_workspace_bytes.restype = c_size_t
     lib.rlloss_backward_shard.argtypes = [cfgp, P, P, P, P, ctypes.c_int64, P, P, P, P, P, P, c_size_t, P]
     lib.rlloss_backward_shard.restype = c_int
+    lib.rlloss_select_state_bytes.argtypes = []
+    lib.rlloss_select_state_bytes.restype = c_size_t
+    lib.rlloss_entropy_hist.argtypes = [P, P, ctypes.c_int64, c_int32, P, P, P]
+    lib.rlloss_entropy_hist.restype = c_int
+    lib.rlloss_entropy_select.argtypes = [c_int32, P, c_float, P, P]
+    lib.rlloss_entropy_select.restype = c_int
+    lib.rlloss_select_threshold.argtypes = [P, ctypes.POINTER(ctypes.c_double)]
+    lib.rlloss_select_threshold.restype = c_int
+    lib.rlloss_loss_from_logp_dp.argtypes = [cfgp, c_int32] + [P] * 10 + [P, c_size_t, P]
+    lib.rlloss_loss_from_logp_dp.restype = c_int
+    lib.rlloss_metrics_from_sums.argtypes = [cfgp, c_int32, ctypes.POINTER(ctypes.c_double), ctypes.c_double,
+                                             ctypes.POINTER(c_float), ctypes.POINTER(c_float)]
+    lib.rlloss_metrics_from_sums.restype = c_int
     lib.rlloss_get_device_status.argtypes = [P, ctypes.POINTER(c_int32)]
     lib.rlloss_get_device_status.restype = c_int
     lib.rlloss_get_backward_rows.argtypes = [P, ctypes.POINTER(c_int32)]
@@ -199,6 +215,48 @@ def rlloss_backward_shard(cfg, X, W, b, targets, v_begin, lse, dlogp, dX, dW, db
     return lib.rlloss_backward_shard(ctypes.byref(cfg), _p(X), _p(W), _p(b), _p(targets), ctypes.c_int64(v_begin),
                                      _p(lse), _p(dlogp), _p(dX), _p(dW), _p(db), _p(workspace),
                                      c_size_t(0 if workspace is None else workspace.numel()), _stream(stream))
+
+
+def rlloss_select_state_bytes() -> int:
+    return int(lib.rlloss_select_state_bytes())
+
+
+def rlloss_entropy_hist(entropy, mask, N, pass_, select_state, counts, stream=None) -> int:
+    return lib.rlloss_entropy_hist(_p(entropy), _p(mask), ctypes.c_int64(N), c_int32(pass_), _p(select_state),
+                                   _p(counts), _stream(stream))
+
+
+def rlloss_entropy_select(pass_, counts, q, select_state, stream=None) -> int:
+    return lib.rlloss_entropy_select(c_int32(pass_), _p(counts), c_float(q), _p(select_state), _stream(stream))
+
+
+def rlloss_select_threshold(select_state) -> float:
+    thr = ctypes.c_double(0.0)
+    rc = lib.rlloss_select_threshold(_p(select_state), ctypes.byref(thr))
+    if rc != OK:
+        raise RllossError(rc, "rlloss_select_threshold")
+    return float(thr.value)
+
+
+def rlloss_loss_from_logp_dp(cfg, B_global, select_state, logp, entropy, old_logp, ref_logp, adv, mask, out_sums,
+                             out_dlogp, out_entropy_mask, workspace, stream=None) -> int:
+    return lib.rlloss_loss_from_logp_dp(ctypes.byref(cfg), c_int32(B_global), _p(select_state), _p(logp),
+                                        _p(entropy), _p(old_logp), _p(ref_logp), _p(adv), _p(mask), _p(out_sums),
+                                        _p(out_dlogp), _p(out_entropy_mask), _p(workspace),
+                                        c_size_t(0 if workspace is None else workspace.numel()), _stream(stream))
+
+
+def rlloss_metrics_from_sums(cfg, B_global, sums, threshold):
+    """Host only: (loss, metrics list) of the whole batch from the batch sums
+    added over ranks (a sequence of NSUMS numbers)."""
+    s = (ctypes.c_double * NSUMS)(*[float(x) for x in sums])
+    loss = c_float(0.0)
+    m = (c_float * NMETRICS)()
+    rc = lib.rlloss_metrics_from_sums(ctypes.byref(cfg), c_int32(B_global), s, ctypes.c_double(threshold),
+                                      ctypes.byref(loss), m)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_metrics_from_sums")
+    return float(loss.value), [float(x) for x in m]
 
 
 def rlloss_get_device_status(workspace) -> int:
@@ -385,5 +443,45 @@ def backward_shard(cfg: RllossCfg, X, W, b, targets, v_begin: int, lse, dlogp, o
                                workspace, stream)
     if rc != OK:
         raise RllossError(rc, "rlloss_backward_shard")
+    o["workspace"] = workspace
+    return o
+
+
+# ---------------------------------------------------------------- batch split over ranks by sequences
+def alloc_select_state(device="cuda") -> torch.Tensor:
+    return torch.zeros(rlloss_select_state_bytes(), dtype=torch.uint8, device=device)
+
+
+def entropy_hist(entropy, mask, pass_: int, select_state, counts=None, stream=None):
+    """This rank's counts [SELECT_COUNTS] (uint32 as int32) for pass ``pass_``."""
+    if counts is None:
+        counts = torch.empty(SELECT_COUNTS, dtype=torch.int32, device=entropy.device)
+    rc = rlloss_entropy_hist(entropy, mask, entropy.numel(), pass_, select_state, counts, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_entropy_hist")
+    return counts
+
+
+def entropy_select(pass_: int, counts, q: float, select_state, stream=None):
+    rc = rlloss_entropy_select(pass_, counts, q, select_state, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_entropy_select")
+
+
+def loss_from_logp_dp(cfg: RllossCfg, B_global: int, select_state, logp, entropy, old_logp, ref_logp, adv, mask,
+                      workspace=None, stream=None):
+    """One rank's loss stage: its batch sums [NSUMS] (fp64), dL/dlogp of the
+    whole batch's loss for its tokens, and its entropy mask."""
+    dev = logp.device
+    N = cfg.B * cfg.T
+    o = dict(sums=torch.empty(NSUMS, dtype=torch.float64, device=dev),
+             dlogp=torch.empty(N, dtype=torch.float32, device=dev),
+             emask=torch.empty(N, dtype=torch.uint8, device=dev))
+    if workspace is None:
+        workspace = alloc_workspace(rlloss_loss_workspace_bytes(cfg), dev)
+    rc = rlloss_loss_from_logp_dp(cfg, B_global, select_state, logp, entropy, old_logp, ref_logp, adv, mask,
+                                  o["sums"], o["dlogp"], o["emask"], workspace, stream)
+    if rc != OK:
+        raise RllossError(rc, "rlloss_loss_from_logp_dp")
     o["workspace"] = workspace
     return o

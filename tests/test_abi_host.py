@@ -151,3 +151,60 @@ def test_e4m3_scoring_validation():
     assert R.lib.rlloss_forward_e4m3(ctypes.byref(ok), *([None] * 9), None, 0, None) == R.EINVAL
     bf = _cfg()
     assert R.lib.rlloss_forward_e4m3(ctypes.byref(bf), *([None] * 9), None, 0, None) == R.EINVAL
+
+
+def test_sequence_split_entries_validate_before_any_launch():
+    cfg = _cfg(top_entropy_quantile=0.2)
+    assert R.rlloss_select_state_bytes() == 256
+    c = ctypes.c_void_p
+    # bad pass, missing counts, missing state after pass 0, negative N, bad q
+    assert R.lib.rlloss_entropy_hist(None, None, 0, 4, None, c(256), None) == R.EINVAL
+    assert R.lib.rlloss_entropy_hist(None, None, 0, 0, None, None, None) == R.EINVAL
+    assert R.lib.rlloss_entropy_hist(None, None, 0, 1, None, c(256), None) == R.EINVAL
+    assert R.lib.rlloss_entropy_hist(None, None, -1, 0, None, c(256), None) == R.EINVAL
+    assert R.lib.rlloss_entropy_hist(None, None, 10, 0, None, c(256), None) == R.EINVAL
+    assert R.lib.rlloss_entropy_select(0, c(256), 1.5, c(256), None) == R.EINVAL
+    assert R.lib.rlloss_entropy_select(-1, c(256), 0.2, c(256), None) == R.EINVAL
+    assert R.lib.rlloss_entropy_select(0, None, 0.2, c(256), None) == R.EINVAL
+    assert R.lib.rlloss_entropy_select(0, c(256), 0.2, c(264), None) == R.EINVAL   # state not 16-byte aligned
+    P = [None] * 10
+    assert R.lib.rlloss_loss_from_logp_dp(ctypes.byref(cfg), cfg.B - 1, *P, None, 0, None) == R.EINVAL
+    assert R.lib.rlloss_loss_from_logp_dp(ctypes.byref(cfg), cfg.B, *P, None, 0, None) == R.EINVAL
+    gs = _cfg(loss_type=R.GSPO_TOKEN, beta=0.1)
+    assert R.lib.rlloss_loss_from_logp_dp(ctypes.byref(gs), gs.B, *P, None, 0, None) == R.EUNSUPPORTED
+    with pytest.raises(R.RllossError):
+        R.rlloss_metrics_from_sums(cfg, 0, [0.0] * R.NSUMS, 0.0)
+
+
+def test_metrics_from_sums_follow_the_oracle_definitions():
+    """The host finisher turns the batch sums into the loss and the metric
+    vector exactly as the oracle defines them (GMPO with K3 KL and the
+    entropy mask, and GSPO-token)."""
+    import oracle as O
+    rng = np.random.default_rng(21)
+    B, T = 4, 30
+    N = B * T
+    mask = (rng.random(N) > 0.3).astype(np.uint8)
+    mask[2 * T:3 * T] = 0                                       # a sequence without active tokens
+    logp = rng.normal(-3.0, 1.0, N)
+    old = logp + rng.normal(0, 0.3, N)
+    ref = logp + rng.normal(0, 0.1, N)
+    ent = rng.normal(4.0, 1.0, N)
+    adv = np.array([1.0, -0.5, 0.8, -1.2])
+    r = O.gmpo_loss(logp, old, ref, adv, mask, B, T, 0.2, 0.3, beta=0.04, entropy=ent, q=0.3)
+    nh = float(((mask.reshape(B, T) != 0).sum(axis=1) > 0).sum())
+    n_act = r.metrics[3]
+    sums = [r.loss * B, n_act, r.metrics[1], r.metrics[2] * n_act, r.metrics[5], r.metrics[6] * nh,
+            r.metrics[7] * nh, nh]
+    cfg = _cfg(B=B, T=T, eps_low=0.2, eps_high=0.3, beta=0.04, top_entropy_quantile=0.3)
+    loss, m = R.rlloss_metrics_from_sums(cfg, B, sums, r.metrics[4])
+    assert np.float32(loss) == np.float32(r.loss)
+    assert np.allclose(m, np.float32(r.metrics), rtol=1e-6)
+    # GSPO: the loss is a sum, the clip fraction is over sequences
+    mask[2 * T] = 1
+    g = O.gspo_token_loss(logp, old, adv, mask, B, T, 0.05, 0.05)
+    gs = [g.loss, g.metrics[3], g.metrics[1], 0.0, g.metrics[5], g.metrics[6] * B, g.metrics[7] * B, float(B)]
+    gcfg = _cfg(B=B, T=T, loss_type=R.GSPO_TOKEN, eps_low=0.05, eps_high=0.05)
+    loss, m = R.rlloss_metrics_from_sums(gcfg, B, gs, float("nan"))
+    assert np.float32(loss) == np.float32(g.loss)
+    assert np.allclose(m, np.float32(g.metrics), rtol=1e-6, equal_nan=True)
