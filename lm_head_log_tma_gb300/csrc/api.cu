@@ -129,7 +129,7 @@ struct Plan {
   int slices;
   size_t o_tickets, o_part;
   size_t o_status, o_partial, o_lse2, o_logp64, o_ent, o_coef, o_emask, o_k3, o_seq, o_bias2, o_dl, o_x3, o_w3,
-      o_dbpart, o_ws2, o_tflags, o_tlist, o_blk, o_cidx, o_xc, o_coefc, o_lse2c, o_tgtc, o_dxc, total;
+      o_dbpart, o_ws2, o_tflags, o_tlist, o_blk, o_cidx, o_xc, o_coefc, o_lse2c, o_tgtc, o_dxc, o_err, total;
   int Ncap;                 // rows of the compacted arrays (N rounded up to 256)
 };
 
@@ -239,6 +239,9 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.o_dl = take(size_t(p.Nc) * p.ld_dl * 2);
     p.o_dbpart = take(p.bias ? size_t(db_part_rows(p.Nc)) * p.V * 4 : 0);
     p.compact = !(c->flags & RLLOSS_FLAG_ALL_ROWS);
+    // bf16 G: each backward row's target-entry rounding error (rows or
+    // compacted rows, N rounded up to whole 256-row tiles)
+    p.o_err = take(p.fp32 ? 0 : size_t(rup(p.N, 256)) * 4);
     p.o_tflags = take(size_t(p.R));
     p.o_tlist = take(size_t(p.R) * 4);
     if (p.compact) {
@@ -596,6 +599,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
   // read-add-write scatter, so each dX element gets one addition per call.
   const bool dx_direct = p.compact && !acc;
   const bool dx_vec = p.H % 4 == 0 && (reinterpret_cast<uintptr_t>(dX) & 15u) == 0;
+  float* err = p.fp32 ? nullptr : reinterpret_cast<float*>(ws + p.o_err);
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dl);
   const int lo_off = p.fp32 ? p.Vp : 0;
   int* rows_total = reinterpret_cast<int*>(ws + p.o_status + kBackwardRowsOffset);
@@ -626,6 +630,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       cp.lse2c = reinterpret_cast<float*>(ws + p.o_lse2c);
       cp.tgtc = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
       cp.xc = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
+      cp.errc = err;
       if (!acc) {   // the gather zeroes dX; the dX/dW launch adds the kept rows into it
         cp.dx_zero = dX;
         cp.H = p.H;
@@ -643,6 +648,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     } else {
       RL_TRY(launch_set_total(rows_total, p.N, st));
       ph.launched();
+      if (err) RL_TRY(cudaMemsetAsync(err, 0, size_t(p.N) * 4, st));
     }
   }
   CUtensorMap tm_xb;
@@ -678,6 +684,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       return RLLOSS_ECUDA;
     dp.lo_off = lo_off;
     dp.dbp = p.bias ? reinterpret_cast<float*>(ws + p.o_dbpart) : nullptr;
+    dp.err = err;
     dp.status = status;
     dp.limit_ns = kWaitLimitNs;
     {
@@ -735,6 +742,14 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       hp.nc_max = nc;
       hp.status = status;
       hp.limit_ns = kWaitLimitNs;
+      if (err) {
+        hp.dx_err = err;
+        hp.dx_tgt = tg_b;
+        hp.dx_w = static_cast<const __nv_bfloat16*>(hd.Wop);
+        hp.dx_wbegin = v_begin;
+        hp.dx_wrows = p.V;
+        hp.dx_wld = p.Kx;
+      }
       if (dx_direct) {
         hp.dx_idx = cidx;
         hp.dx_out = dX;

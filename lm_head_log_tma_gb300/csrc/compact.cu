@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kCompactBlock) compact_count_kernel(CompactPar
     p.coefc[r] = 0.f;
     p.lse2c[r] = 0.f;
     p.tgtc[r] = -1;
+    if (p.errc) p.errc[r] = 0.f;
   }
   const int words = p.Kx / 8;   // 16-byte words per row
   const long long tail_words = (long long)(tail_end - total) * words;
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactPa
       p.coefc[pos] = p.coef[n];
       p.lse2c[pos] = p.lse2[n];
       p.tgtc[pos] = p.targets[n];
+      if (p.errc) p.errc[pos] = 0.f;
       rows[rank] = n;
     }
     if (threadIdx.x == 0) cnt = __popc(bal);

@@ -473,6 +473,16 @@ struct DlPolicy {
         for (int i = 0; i < 32; ++i)
           if (c0 + i >= p.V) v[i] = 0.f;
       }
+      if (p.err && ty < 32u) {
+        // The target entry c (1 - p_y) / tau carries a row's dX; its bf16
+        // rounding error (one relative error for every row of a sequence
+        // with the same c) is kept in fp32 and added back in the dX epilogue.
+        float vt = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (unsigned(i) == ty) vt = v[i];
+        p.err[row] = vt - __bfloat162float(__float2bfloat16_rn(vt));
+      }
       uint32_t hi[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) hi[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -631,6 +641,28 @@ struct HPolicy {
     umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, sub), idesc(t), accum);
   }
 
+  // v[i] += err * W[target][x0 + i] for the valid columns (bf16 W row, 16-byte aligned).
+  __device__ static void add_target_row(float (&v)[32], const __nv_bfloat16* wrow, float err, int x0, int Hout) {
+    if (x0 + 32 <= Hout) {
+      const uint4* w4 = reinterpret_cast<const uint4*>(wrow + x0);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 u = __ldg(w4 + k);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+          v[8 * k + 2 * j] = fmaf(err, __low2float(b2), v[8 * k + 2 * j]);
+          v[8 * k + 2 * j + 1] = fmaf(err, __high2float(b2), v[8 * k + 2 * j + 1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (x0 + i < Hout) v[i] = fmaf(err, __bfloat162float(wrow[x0 + i]), v[i]);
+    }
+  }
+
   // Sub `sub` of the accumulator: warp (q, half) writes TMEM lanes 32q..+31,
   // 32-column chunks 0-3 (half 0) or 4-6 (half 1).
   __device__ static void epilogue(const Params& p, EpiState&, const TileInfo& t, uint32_t taddr, int q, int half,
@@ -641,6 +673,18 @@ struct HPolicy {
     const int y0 = t.m0 + 128 * int(rank) + q * 32;
     const int c_begin = half ? 4 : 0, c_end = half ? 7 : 4;
     const bool no_k = t.kb_end <= t.kb_begin;   // empty sum (a chunk without rows): store zeros
+    // dX rows: the target-entry correction err * W[target] on the first k part
+    const __nv_bfloat16* wrow = nullptr;
+    float ferr = 0.f;
+    if (t.seg == 0 && p.dx_err && t.kb_begin == 0 && !no_k) {
+      const int nc = min(max(*p.rows_total - p.n0, 0), p.nc_max);
+      const int y = y0 + lane;
+      if (y < nc) {
+        ferr = p.dx_err[p.n0 + y];
+        const long long tr = p.dx_tgt[p.n0 + y] - p.dx_wbegin;
+        if (ferr != 0.f && tr >= 0 && tr < p.dx_wrows) wrow = p.dx_w + size_t(tr) * p.dx_wld;
+      }
+    }
     if (t.seg == 0 && p.dx_idx) {
       // dX rows of the compacted backward, added at their original rows.
       const int nc = min(max(*p.rows_total - p.n0, 0), p.nc_max);
@@ -653,6 +697,7 @@ struct HPolicy {
         float v[32];
         tmem_ld32(taddr + uint32_t(c * 32), v);   // warp-collective: every lane loads
         if (!dst) continue;
+        if (wrow) add_target_row(v, wrow, ferr, x0, pr.Hout);
         if (p.dx_vec && x0 + 32 <= pr.Hout) {
 #pragma unroll
           for (int k = 0; k < 8; ++k)
@@ -677,6 +722,7 @@ struct HPolicy {
       } else {
         tmem_ld32(taddr + uint32_t(c * 32), v);
       }
+      if (wrow) add_target_row(v, wrow, ferr, x0, pr.Hout);
       if (lane == 0) tma_store_wait_read<0>();
       __syncwarp();
       float4* row = reinterpret_cast<float4*>(buf + lane * 128);

@@ -85,6 +85,10 @@ struct DlParams {
   int ld;                     // row stride in elements
   int lo_off;                 // element offset of the lo terms (fp32 mode), else 0
   float* dbp;                 // bias: [rows/32][V] column sums of G per 32 chunk rows, else null
+  // Optional (bf16 G): per row (same index as coef) the fp32 value of the
+  // row's target entry of G minus its bf16 rounding.  Rows without a target
+  // among these columns are not written (the caller zeroes them).
+  float* err;
   int* status;
   unsigned long long limit_ns;
 };
@@ -126,6 +130,15 @@ struct HParams {
   float* dx_out;
   int dx_ld;
   int dx_vec;
+  // Optional (problem 0): the recompute's target-entry rounding errors
+  // (dx_err, indexed like the chunk's rows, n0 + row) are added back in fp32
+  // as err * W[target - w_begin] on the first k part, so the dominant
+  // c (onehot - p) W term of each dX row carries no bf16 rounding.
+  const float* dx_err;
+  const int64_t* dx_tgt;
+  const __nv_bfloat16* dx_w;  // bf16 W [dx_wrows, dx_wld]
+  long long dx_wbegin;
+  int dx_wrows, dx_wld;
   int* status;
   unsigned long long limit_ns;
 };
@@ -198,6 +211,7 @@ struct CompactParams {
   float* lse2c;               // [Ncap]
   int64_t* tgtc;              // [Ncap]
   __nv_bfloat16* xc;          // [Ncap, Kx]
+  float* errc;                // optional: [Ncap] zeroed for kept rows and the tile tail
   float* dx_zero;             // optional: [N, H] gradient buffer the gather sets to zero
   int H;
   int dx_vec;                 // dx_zero is 16-byte aligned and H % 4 == 0
