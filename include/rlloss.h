@@ -316,6 +316,8 @@ int rlloss_backward_shard(const rlloss_cfg* cfg, const void* X, const void* W, c
  *      metrics of the whole batch;
  *   4. rlloss_backward_shard with the whole vocabulary (v_begin = 0) ->
  *      dX of its rows, and its dW, db parts; dW and db are sums over ranks.
+ * A rank that holds no sequence in a step contributes zero counts
+ * (rlloss_entropy_hist with N = 0) and zero sums, and skips steps 1, 3, 4.
  * The library makes no collective call: the exchanges are the caller's. */
 #define RLLOSS_SELECT_PASSES 4
 #define RLLOSS_SELECT_COUNTS 512   /* uint32 counts per pass */
