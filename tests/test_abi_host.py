@@ -208,3 +208,24 @@ def test_metrics_from_sums_follow_the_oracle_definitions():
     loss, m = R.rlloss_metrics_from_sums(gcfg, B, gs, float("nan"))
     assert np.float32(loss) == np.float32(g.loss)
     assert np.allclose(m, np.float32(g.metrics), rtol=1e-6, equal_nan=True)
+
+
+def test_header_is_plain_c():
+    """include/rlloss.h compiles as strict C99 (no C++ in the ABI), and every
+    declared function is referenced from C."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    names = R.declared_functions()
+    body = "\n".join(f"  (void)&{n};" for n in names)
+    src = f'#include <stddef.h>\n#include "rlloss.h"\nint main(void) {{\n{body}\n  return 0;\n}}\n'
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "abi.c")
+        open(path, "w").write(src)
+        r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                            "-I", inc, path], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
