@@ -482,3 +482,74 @@ def test_shard_gradients_sum_to_the_full_vocabulary_gradients():
     assert np.allclose(dX, out["dX"], rtol=1e-11, atol=1e-15)
     assert np.allclose(np.concatenate(dWs), out["dW"], rtol=1e-11, atol=1e-15)
     assert np.allclose(np.concatenate(dbs), out["db"], rtol=1e-11, atol=1e-15)
+
+
+# --- invariances the definitions imply -------------------------------------------
+
+def test_row_stats_shift_invariance():
+    """Softmax is unchanged when a constant is added to every logit of a row:
+    lse moves by exactly that constant, logp and entropy do not move."""
+    rng = np.random.default_rng(41)
+    X, W, b, y = _rand_problem(rng, 12, 9, 70)
+    tau = 0.8
+    lse0, lp0, h0 = O.row_stats(X, W, b, y, tau)
+    lse1, lp1, h1 = O.row_stats(X, W, b + 3.0 * tau, y, tau)
+    np.testing.assert_allclose(lse1 - lse0, 3.0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lp1, lp0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(h1, h0, rtol=0, atol=1e-12)
+
+
+def test_temperature_folds_into_the_weights():
+    """z = (X W^T + b) / tau: scaling W and b by 1/tau at tau = 1 gives the
+    same row statistics and the same gradient coefficients' G (the 1/tau of
+    dlogits included)."""
+    rng = np.random.default_rng(42)
+    X, W, b, y = _rand_problem(rng, 10, 7, 50)
+    tau = 0.55
+    a = O.row_stats(X, W, b, y, tau)
+    c = O.row_stats(X, W / tau, b / tau, y, 1.0)
+    for u, v in zip(a, c):
+        np.testing.assert_allclose(u, v, rtol=1e-12, atol=1e-12)
+    cn = rng.standard_normal(10)
+    g_a = O.dlogits_rows(X, W, b, y, tau, a[0], cn, np.arange(10))
+    g_c = O.dlogits_rows(X, W / tau, b / tau, y, 1.0, c[0], cn / tau, np.arange(10))
+    np.testing.assert_allclose(g_a, g_c, rtol=1e-12, atol=1e-15)
+
+
+def test_gmpo_common_shift_of_logp_and_old_changes_nothing():
+    """The log ratio lr = logp - old is all GMPO (beta = 0) sees: shifting both
+    by the same amount leaves loss, clip decisions and dL/dlogp unchanged."""
+    rng = np.random.default_rng(43)
+    B, T = 3, 9
+    lp = rng.normal(-4, 1, B * T)
+    old = lp + rng.normal(0, 0.4, B * T)
+    m = (rng.random(B * T) > 0.2).astype(np.uint8)
+    A = np.array([0.9, -1.3, 0.4])
+    r0 = O.gmpo_loss(lp, old, None, A, m, B, T, 0.2, 0.3)
+    r1 = O.gmpo_loss(lp + 1.75, old + 1.75, None, A, m, B, T, 0.2, 0.3)
+    assert r1.loss == pytest.approx(r0.loss, rel=1e-13)
+    assert np.array_equal(r0.clipped, r1.clipped)
+    np.testing.assert_allclose(r1.c, r0.c, rtol=1e-12, atol=1e-18)
+
+
+def test_batch_duplication_pins_the_reductions():
+    """Stacking the batch on itself: GMPO's loss is a mean over sequences, so
+    it stays and each token's dL/dlogp halves; GSPO-token's loss is a sum over
+    tokens, so it doubles and dL/dlogp stays (readings R6 and R8)."""
+    rng = np.random.default_rng(44)
+    B, T = 3, 8
+    lp = rng.normal(-4, 1, B * T)
+    old = lp + rng.normal(0, 0.3, B * T)
+    ref = lp + rng.normal(0, 0.1, B * T)
+    m = (rng.random(B * T) > 0.2).astype(np.uint8)
+    m[::T] = 1
+    A = np.array([1.0, -0.6, 0.3])
+    d = lambda x: np.concatenate([x, x])
+    g1 = O.gmpo_loss(lp, old, ref, A, m, B, T, 0.2, 0.3, beta=0.04)
+    g2 = O.gmpo_loss(d(lp), d(old), d(ref), d(A), d(m), 2 * B, T, 0.2, 0.3, beta=0.04)
+    assert g2.loss == pytest.approx(g1.loss, rel=1e-13)
+    np.testing.assert_allclose(g2.c, d(g1.c) / 2, rtol=1e-12, atol=1e-18)
+    s1 = O.gspo_token_loss(lp, old, A, m, B, T, 0.05, 0.05)
+    s2 = O.gspo_token_loss(d(lp), d(old), d(A), d(m), 2 * B, T, 0.05, 0.05)
+    assert s2.loss == pytest.approx(2 * s1.loss, rel=1e-13)
+    np.testing.assert_allclose(s2.c, d(s1.c), rtol=1e-12, atol=1e-18)
