@@ -65,6 +65,8 @@ extern "C" {
 #define RLLOSS_DEV_ENONFINITE 0x20  /* the loss came out NaN or infinite */
 #define RLLOSS_DEV_EBADTARGET 0x40  /* a target id outside [0, V); its logp is NaN */
 #define RLLOSS_DEV_EEMPTYSEQ 0x80   /* GSPO sequence with no active token; it contributes 0 */
+#define RLLOSS_DEV_EBOUNDS 0x100    /* builds with -DRLLOSS_DEBUG only: an index or TMA coordinate
+                                       check failed and that access was skipped; results invalid */
 
 /* cfg.dtype */
 #define RLLOSS_BF16 0

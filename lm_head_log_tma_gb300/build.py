@@ -33,13 +33,19 @@ def sources() -> list[str]:
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_info: bool = False, debug: bool = False, out: str | None = None) -> str:
+    """Compile every .cu file and link librlloss.so (in place, or at ``out``).
+    debug=True adds -DRLLOSS_DEBUG: device-side index and TMA-coordinate
+    checks that record RLLOSS_DEV_EBOUNDS and skip the access."""
+    obj_dir = BUILD + ("_debug" if debug else "")
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug:
+        extra = extra + ["-DRLLOSS_DEBUG"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -51,14 +57,15 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     srcs = sources()
     with ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    lib = out or LIB
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, ptxas_info="--ptxas" in sys.argv))
+    print(build(verbose="-v" in sys.argv, ptxas_info="--ptxas" in sys.argv, debug="--debug" in sys.argv))

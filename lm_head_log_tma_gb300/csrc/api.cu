@@ -631,6 +631,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       cp.tgtc = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
       cp.xc = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
       cp.errc = err;
+      cp.status = status;
       if (!acc) {   // the gather zeroes dX; the dX/dW launch adds the kept rows into it
         cp.dx_zero = dX;
         cp.H = p.H;
@@ -753,6 +754,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       if (dx_direct) {
         hp.dx_idx = cidx;
         hp.dx_out = dX;
+        hp.dx_nrows = p.N;
         hp.dx_ld = p.H;
         hp.dx_vec = dx_vec ? 1 : 0;
       }

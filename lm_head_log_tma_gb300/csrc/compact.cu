@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace rl {
 
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactPa
     const bool keep = n < p.N && p.coef[n] != 0.f;
     const unsigned bal = __ballot_sync(0xffffffffu, keep);
     const int rank = __popc(bal & ((1u << threadIdx.x) - 1u));
-    if (keep) {
+    if (keep && RL_DCHECK(p.blk_off[g] + rank < p.Ncap, p.status)) {
       const int pos = p.blk_off[g] + rank;
       p.idx[pos] = n;
       p.coefc[pos] = p.coef[n];

@@ -109,13 +109,16 @@ struct FwdPolicy {
       constexpr int kBoxK = kKB / KBX;   // K elements of one 128-byte box row
 #pragma unroll
       for (int x = 0; x < KBX; ++x) {
-        tma_load_2d_pair(&p.tmA, bar, st + x * kBox, p.seg_a[s] + kk + kBoxK * x, t.m0 + 128 * int(rank));
-        tma_load_2d_pair(&p.tmB, bar, st + kABytes + x * kBox, p.seg_b[s] + kk + kBoxK * x, t.n0 + 128 * int(rank));
+        constexpr int EB = F8 ? 1 : 2;
+        if (tma_x_ok<EB>(p.seg_a[s] + kk + kBoxK * x, p.status))
+          tma_load_2d_pair(&p.tmA, bar, st + x * kBox, p.seg_a[s] + kk + kBoxK * x, t.m0 + 128 * int(rank));
+        if (tma_x_ok<EB>(p.seg_b[s] + kk + kBoxK * x, p.status))
+          tma_load_2d_pair(&p.tmB, bar, st + kABytes + x * kBox, p.seg_b[s] + kk + kBoxK * x, t.n0 + 128 * int(rank));
       }
     } else {
       static_assert(KBX == 1, "single-CTA tiles keep one box per operand");
-      tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0);
-      tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+      if (tma_x_ok<F8 ? 1 : 2>(p.seg_a[s] + kk, p.status)) tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, t.m0);
+      if (tma_x_ok<F8 ? 1 : 2>(p.seg_b[s] + kk, p.status)) tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
     }
   }
   // MMA step k (32 bytes of K each) of the stage: box k / 4, byte offset 32 (k % 4).
@@ -275,7 +278,7 @@ struct FwdPolicy {
       }
       if (ch + 1 < nch) tmem_ld32_wait(r);
     }
-    if (t.last && row < p.N) {
+    if (t.last && row < p.N && RL_DCHECK(t.seg < t.aux && t.aux <= p.pcap, p.status)) {
       float4* dst = p.partial + (size_t(row) * (2 * t.aux) + size_t(t.seg) * 2 + half) * 2;
       dst[0] = make_float4(e.mref, e.s_hi, e.s_lo, e.w_hi);
       dst[1] = make_float4(e.w_lo, e.zy, e.found ? 1.f : 0.f, 0.f);
@@ -382,13 +385,15 @@ struct DlPolicy {
     if constexpr (CL == 2) {
 #pragma unroll
       for (int x = 0; x < KBX; ++x) {
-        tma_load_2d_pair(&p.tmA, bar, st + x * kBox, p.seg_a[s] + kk + 64 * x, p.n0 + t.m0 + 128 * int(rank));
-        tma_load_2d_pair(&p.tmB, bar, st + kABytes + x * kBox, p.seg_b[s] + kk + 64 * x, t.n0 + 128 * int(rank));
+        if (tma_x_ok<2>(p.seg_a[s] + kk + 64 * x, p.status))
+          tma_load_2d_pair(&p.tmA, bar, st + x * kBox, p.seg_a[s] + kk + 64 * x, p.n0 + t.m0 + 128 * int(rank));
+        if (tma_x_ok<2>(p.seg_b[s] + kk + 64 * x, p.status))
+          tma_load_2d_pair(&p.tmB, bar, st + kABytes + x * kBox, p.seg_b[s] + kk + 64 * x, t.n0 + 128 * int(rank));
       }
     } else {
       static_assert(KBX == 1, "single-CTA tiles keep one box per operand");
-      tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0);
-      tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
+      if (tma_x_ok<2>(p.seg_a[s] + kk, p.status)) tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0);
+      if (tma_x_ok<2>(p.seg_b[s] + kk, p.status)) tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
     }
   }
   __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo&) {
@@ -421,7 +426,7 @@ struct DlPolicy {
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(&p.tmG, buf, x, y);
+      if (tma_x_ok<2>(x, p.status)) tma_store_2d(&p.tmG, buf, x, y);
       tma_store_commit();
     }
     ++e.nbuf;
@@ -501,7 +506,8 @@ struct DlPolicy {
         // db partial: this warp's 32 rows summed per column (fp32 G, before
         // the bf16 rounding), one row of the [rows/32][V] partial buffer
         const float cs = warp_column_sum(v, lane);
-        if (c0 + lane < p.V) p.dbp[size_t(r0 >> 5) * p.V + c0 + lane] = cs;
+        if (c0 + lane < p.V && RL_DCHECK((r0 >> 5) < (p.Nc + 255) / 256 * 8, p.status))
+          p.dbp[size_t(r0 >> 5) * p.V + c0 + lane] = cs;
       }
     }
   }
@@ -613,17 +619,19 @@ struct HPolicy {
     const int kk = (kb - s * t.aux) * 64;
     const int r = t.m0 + 128 * int(rank);
     if (pr.a_mn) {
-      tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + r, pr.a_outer0 + kk);
-      tma_load_2d_pair(&p.tmA[q], bar, st + 8192, p.seg_a[s] + r + 64, pr.a_outer0 + kk);
+      if (tma_x_ok<2>(p.seg_a[s] + r, p.status))
+        tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + r, pr.a_outer0 + kk);
+      if (tma_x_ok<2>(p.seg_a[s] + r + 64, p.status))
+        tma_load_2d_pair(&p.tmA[q], bar, st + 8192, p.seg_a[s] + r + 64, pr.a_outer0 + kk);
     } else {
-      tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + kk, r);
+      if (tma_x_ok<2>(p.seg_a[s] + kk, p.status)) tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + kk, r);
     }
 #pragma unroll
     for (int sub = 0; sub < 2; ++sub) {
       const int h = p.seg_b[s] + t.n0 + kNS * sub + 112 * int(rank);
       uint8_t* b = st + kABytes + sub * kBSub;
-      tma_load_2d_pair(&p.tmB[q], bar, b, h, pr.b_outer0 + kk);
-      tma_load_2d_pair(&p.tmB[q], bar, b + 8192, h + 64, pr.b_outer0 + kk);
+      if (tma_x_ok<2>(h, p.status)) tma_load_2d_pair(&p.tmB[q], bar, b, h, pr.b_outer0 + kk);
+      if (tma_x_ok<2>(h + 64, p.status)) tma_load_2d_pair(&p.tmB[q], bar, b + 8192, h + 64, pr.b_outer0 + kk);
     }
   }
   __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo& t) {
@@ -689,7 +697,9 @@ struct HPolicy {
       // dX rows of the compacted backward, added at their original rows.
       const int nc = min(max(*p.rows_total - p.n0, 0), p.nc_max);
       const int y = y0 + lane;
-      float* dst = (y < nc && !no_k) ? p.dx_out + size_t(p.dx_idx[p.n0 + y]) * p.dx_ld : nullptr;
+      const int drow = (y < nc && !no_k) ? p.dx_idx[p.n0 + y] : -1;
+      float* dst = (drow >= 0 && RL_DCHECK(drow < p.dx_nrows, p.status)) ? p.dx_out + size_t(drow) * p.dx_ld
+                                                                          : nullptr;
 #pragma unroll 1
       for (int c = c_begin; c < c_end; ++c) {
         const int x0 = t.n0 + sub * kNS + c * 32;
@@ -731,10 +741,12 @@ struct HPolicy {
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
-        if (pr.reduce)
+        if (!tma_x_ok<4>(x0, p.status)) {
+        } else if (pr.reduce) {
           tma_reduce_add_2d(om, buf, x0, y0);
-        else
+        } else {
           tma_store_2d(om, buf, x0, y0);
+        }
         tma_store_commit();
       }
     }

@@ -128,6 +128,7 @@ struct HParams {
   // reach an element (ksplit <= 2), so the sum does not depend on their order.
   const int* dx_idx;
   float* dx_out;
+  int dx_nrows;               // rows of dx_out (checked in debug builds)
   int dx_ld;
   int dx_vec;
   // Optional (problem 0): the recompute's target-entry rounding errors
@@ -212,6 +213,7 @@ struct CompactParams {
   int64_t* tgtc;              // [Ncap]
   __nv_bfloat16* xc;          // [Ncap, Kx]
   float* errc;                // optional: [Ncap] zeroed for kept rows and the tile tail
+  int* status;                // device status word (index checks of debug builds)
   float* dx_zero;             // optional: [N, H] gradient buffer the gather sets to zero
   int H;
   int dx_vec;                 // dx_zero is 16-byte aligned and H % 4 == 0

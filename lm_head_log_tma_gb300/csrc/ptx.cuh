@@ -44,6 +44,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Checks of a debug build (-DRLLOSS_DEBUG): a failed check records
+// RLLOSS_DEV_EBOUNDS in the status word and the caller skips the access
+// (a skipped TMA load then lets its bounded wait run out).  In other builds
+// every check is the constant true and compiles away.
+__device__ __forceinline__ bool rl_dcheck(bool ok, int* status) {
+#ifdef RLLOSS_DEBUG
+  if (!ok && status) atomicOr(status, RLLOSS_DEV_EBOUNDS);
+  return ok;
+#else
+  (void)status;
+  return true;
+#endif
+}
+#ifdef RLLOSS_DEBUG
+#define RL_DCHECK(cond, status) ::rl::rl_dcheck((cond), (status))
+#else
+#define RL_DCHECK(cond, status) true
+#endif
+// A tiled TMA copy's inner coordinate times the element size must be a
+// multiple of 16 bytes.
+template <int EB>
+__device__ __forceinline__ bool tma_x_ok(int x, int* status) {
+  return RL_DCHECK(((x * EB) & 15) == 0, status);
+}
+
 // Shared abort state of one CTA: a flag in shared memory that any role raises
 // when one of its waits ran out, plus the global status word.
 struct AbortCtl {

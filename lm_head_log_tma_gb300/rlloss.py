@@ -19,6 +19,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "rlloss.h")
 
 OK, EINVAL, EUNSUPPORTED, EWORKSPACE, ECUDA = 0, 1, 2, 3, 4
 DEV_ETIMEOUT, DEV_ENONFINITE, DEV_EBADTARGET, DEV_EEMPTYSEQ = 0x10, 0x20, 0x40, 0x80
+DEV_EBOUNDS = 0x100     # builds with -DRLLOSS_DEBUG only
 BF16, FP32, FP8_E4M3 = 0, 1, 2
 GMPO, GSPO_TOKEN = 0, 1
 IS_TOKEN, IS_SEQUENCE = 0, 1

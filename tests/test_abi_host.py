@@ -229,3 +229,25 @@ def test_header_is_plain_c():
         r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
                             "-I", inc, path], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_debug_build_compiles_and_exports_the_same_functions(tmp_path):
+    """The -DRLLOSS_DEBUG variant (device index and TMA-coordinate checks that
+    record RLLOSS_DEV_EBOUNDS instead of faulting) builds for sm_103a and
+    exports every declared function.  nvcc cross-compiles without a GPU."""
+    import shutil
+    import subprocess
+    from lm_head_log_tma_gb300 import build as B
+    try:
+        B.nvcc()
+    except RuntimeError:
+        pytest.skip("no nvcc")
+    lib = B.build(debug=True, out=str(tmp_path / "librlloss_debug.so"))
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("no nm")
+    out = subprocess.run([nm, "-D", "--defined-only", lib], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in R.declared_functions() if n not in exported]
+    assert not missing, missing
+    assert R.DEV_EBOUNDS == 0x100
