@@ -1,16 +1,22 @@
 // Tensor-core kernels of the fused LM-head path.
 //
-//  fwd   : S = X W^T tile by tile (128 tokens x 256 vocab, K = H), epilogue
-//          folds each tile into per-row streaming log-softmax state
-//          (reference max, sum 2^(t-m), sum 2^(t-m)(t-m), target logit) —
-//          "support top_entropy_quantile in fused linear GRPO loss", Details
-//          (second online accumulator next to the running max and sum).
+//  fwd   : S = X W^T tile by tile (256 tokens x 256 vocab on a CTA pair, or
+//          128 x 256 on one CTA; K = H), epilogue folds each tile into
+//          per-row streaming log-softmax state (reference max,
+//          sum 2^(t-m), sum 2^(t-m)(t-m), target logit) — "support
+//          top_entropy_quantile in fused linear GRPO loss", Details (second
+//          online accumulator next to the running max and sum).
 //  merge : combines the partial row states of the vocabulary segments into
 //          lse, logp and entropy per token.
 //  dl    : recomputes S for a chunk of rows and writes
-//          G = dL/dl = (c/tau)(onehot(y) - p) as bf16 (p = softmax(S/tau)).
-//  gemmH : D[row][h] = sum_k A[row][k] B[h][k] on CTA pairs, 256 rows x 224 h
-//          per tile: dX = G W (k = vocab) and dW = G^T X (k = tokens).
+//          G = dL/dl = (c/tau)(onehot(y) - p) as bf16 (p = softmax(S/tau)),
+//          keeping each row's target-entry rounding error in fp32, the
+//          db column partials when there is a bias.
+//  gemmH : D[row][h] = sum_k A[row][k] B[h][k] on CTA pairs, 256 rows x 448 h
+//          per tile (two 224-h halves sharing each A tile): dX = G W
+//          (k = vocab; the target-entry error times W[target] added back,
+//          rows of the compacted backward added in place into dX) and
+//          dW = G^T X (k = tokens) in one grouped launch.
 #include <cuda_runtime.h>
 
 #include "engine.cuh"
