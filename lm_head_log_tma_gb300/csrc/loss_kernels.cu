@@ -5,11 +5,15 @@
 //     keys, then linear interpolation at position (1-q)(n_act-1) and the mask
 //     H >= threshold — "support top_entropy_quantile in fused linear GRPO
 //     loss", Details (batch-global quantile of active entropies at 1 - q).
-//  K2 per-sequence reduction: one block per sequence, fp64 sums, then the
-//     per-token gradient coefficient c_n = dL/dlogp_n; the last block to
-//     finish folds the per-sequence terms into the loss and metrics in a
-//     fixed order.  GMPO: "Add GMPO to fused linear GRPO loss", Summary and
-//     Details.  GSPO-token: Tinker "GSPO", ratio and objective formulas.
+//     The passes are also exported one by one (histogram, then select from
+//     counts summed over ranks) for batches split over ranks.
+//  K2 per-sequence reduction: blocks over slices of each sequence form fp64
+//     partial sums; the last slice of a sequence folds them into its record,
+//     the last sequence folds the records into the loss and metrics (or into
+//     eight batch sums that add over ranks), both in a fixed order; then the
+//     per-token gradient coefficient c_n = dL/dlogp_n.  GMPO: "Add GMPO to
+//     fused linear GRPO loss", Summary and Details.  GSPO-token: Tinker
+//     "GSPO", ratio and objective formulas.
 #include <cuda_runtime.h>
 #include <math.h>
 
