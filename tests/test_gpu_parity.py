@@ -122,7 +122,11 @@ def test_tile_shapes_agree(R, spec):
 
 
 def test_repeated_calls_are_bit_identical(R):
-    """No floating-point atomics anywhere: two calls give the same bits."""
+    """Two calls give the same bits.  Every floating-point reduction has a fixed
+    order, with one exception that is still order-free: the compacted backward
+    adds each kept row's two dX halves (one per vocabulary half) into a zeroed
+    dX with atomic adds, and two addends onto zero give the same fp32 sum in
+    either order."""
     case = Case(MID[1])
     a = case.run_gpu(R)
     b = case.run_gpu(R)
@@ -522,22 +526,38 @@ def test_exact_clip_boundaries_loss_stage(R, side):
 
 
 def test_gspo_clip_bounds_loss_stage(R):
-    """GSPO: sequence ratios exactly at, just inside and just outside the bounds."""
-    B, T = 4, 2
+    """GSPO: sequence ratios exactly on each fp32 clip bound and one fp64 ulp
+    either side, under both advantage signs (Tinker "GSPO", objective formula
+    and "Choosing clipping thresholds").  The log ratios are fp32 pieces whose
+    masked mean is, exactly, the fp64 preimage of the target ratio.  Clip
+    decisions, the zero pattern of dL/dlogp and its values must equal the
+    oracle's; the oracle's ratios are asserted to sit on the targets."""
+    from exact_bounds import gspo_sequences_on_bounds
     lo, hi = O.f32(1 - 3e-4), O.f32(1 + 4e-4)
-    rng = np.random.default_rng(3)
-    logp = rng.uniform(-3, -1, B * T).astype(np.float32)
-    shifts = [np.log(hi) + 1e-6, np.log(hi) - 1e-6, np.log(lo) - 1e-6, 0.0]
-    old = (logp.astype(np.float64) - np.repeat(shifts, T)).astype(np.float32)
-    adv = np.array([1.0, 1.0, -1.0, 0.5], np.float32)
-    mask = np.ones(B * T, np.uint8)
+    targets, lp1, old1, m1 = gspo_sequences_on_bounds(lo, hi)
+    k, T = lp1.shape
+    B = 2 * k
+    logp = np.concatenate([lp1, lp1]).reshape(-1)
+    old = np.concatenate([old1, old1]).reshape(-1)
+    mask = np.concatenate([m1, m1]).reshape(-1)
+    adv = np.concatenate([np.full(k, 1.0), np.full(k, -1.0)]).astype(np.float32)
+    o = O.gspo_token_loss(logp.astype(np.float64), old.astype(np.float64), adv.astype(np.float64), mask, B, T)
+    assert np.array_equal(np.exp(o.seq_log_ratio), np.concatenate([targets, targets]))
+    assert o.metrics[1] == 4
     cfg = R.make_cfg(B, T, loss_type=R.GSPO_TOKEN, eps_low=3e-4, eps_high=4e-4)
     g = _loss_gpu(R, cfg, logp, old, adv, mask)
-    o = O.gspo_token_loss(logp.astype(np.float64), old.astype(np.float64), adv.astype(np.float64), mask, B, T)
     assert g["status"] == 0
     assert g["metrics"][1].item() == o.metrics[1]
-    assert np.array_equal(g["dlogp"].cpu().numpy() == 0, o.c == 0)
+    gd = g["dlogp"].cpu().numpy()
+    assert np.array_equal(gd == 0, o.c == 0)
+    assert np.array_equal(gd, o.c.astype(np.float32))
     assert g["loss"].item() == pytest.approx(o.loss, rel=1e-6)
+    # one sequence at a time: the ratio the GPU formed is the target itself
+    for i in (1, 4):
+        sl = slice(i * T, (i + 1) * T)
+        g1 = _loss_gpu(R, R.make_cfg(1, T, loss_type=R.GSPO_TOKEN, eps_low=3e-4, eps_high=4e-4),
+                       logp[sl], old[sl], adv[i:i + 1], mask[sl])
+        assert g1["metrics"][7].item() == np.float32(targets[i]) and g1["metrics"][1].item() == 0
 
 
 def test_quantile_beyond_2_24_elements_exact(R):

@@ -329,6 +329,50 @@ def test_gspo_per_token_advantages_match_autograd_and_reduce_to_per_sequence():
     assert a.loss == b_.loss and np.array_equal(a.c, b_.c)
 
 
+def test_gspo_exact_bounds_and_neighbours_match_autograd():
+    """Sequence ratios exactly on the fp32 clip bounds and one fp64 ulp either side.
+
+    Tinker "GSPO", objective formula and "Choosing clipping thresholds": the
+    objective is min(s A, clip(s, lo, hi) A).  Autograd of that formula decides
+    the gradient at the bound itself: the clamp's gradient is inclusive and the
+    minimum ties, so the gradient passes in full (reading R12).  The clip
+    diagnostic counts ratios strictly outside the range (reading R17)."""
+    from exact_bounds import gspo_sequences_on_bounds
+    lo, hi = O.f32(1 - 3e-4), O.f32(1 + 4e-4)
+    targets, lp1, old1, m1 = gspo_sequences_on_bounds(lo, hi)
+    k, T = lp1.shape
+    # every ratio under both advantage signs: sequences 0..k-1 with A = +1, k..2k-1 with A = -1
+    logp = np.concatenate([lp1, lp1]).astype(np.float64).reshape(-1)
+    old = np.concatenate([old1, old1]).astype(np.float64).reshape(-1)
+    mask = np.concatenate([m1, m1]).reshape(-1)
+    B = 2 * k
+    adv = np.concatenate([np.ones(k), -np.ones(k)])
+    r = O.gspo_token_loss(logp, old, adv, mask, B, T)
+    s = np.exp(r.seq_log_ratio)
+    assert np.array_equal(s, np.concatenate([targets, targets]))        # on the bound, exactly
+    lp_t = torch.tensor(logp, requires_grad=True)
+    L = _torch_gspo(lp_t, torch.tensor(old), torch.tensor(adv), torch.tensor(mask, dtype=torch.float64),
+                    B, T, lo, hi)
+    L.backward()
+    seq_t = ((torch.tensor(logp) - torch.tensor(old)).reshape(B, T) * torch.tensor(m1.astype(np.float64)).repeat(2, 1)
+             ).sum(1) / 4.0
+    assert np.array_equal(torch.exp(seq_t).numpy(), s)                  # autograd sees the same ratios
+    g = lp_t.grad.numpy()
+    assert r.loss == pytest.approx(L.item(), rel=1e-15)
+    assert np.array_equal(r.c == 0, g == 0)
+    assert np.allclose(r.c, g, rtol=1e-15, atol=0)
+    # the gradient stops only on the flat side of the clamp, strictly past the bound
+    flat = np.zeros(B, bool)
+    flat[5] = True          # A > 0, s = next(hi)
+    flat[k + 0] = True      # A < 0, s = prev(lo)
+    active = mask.reshape(B, T) != 0
+    assert np.array_equal((g.reshape(B, T) == 0) & active, flat[:, None] & active)
+    # strict "outside": prev(lo) and next(hi) count, the bounds themselves do not
+    out = (s < lo) | (s > hi)
+    assert out.sum() == 4 and not out[[1, 4, k + 1, k + 4]].any()
+    assert r.metrics[1] == 4 and np.array_equal(r.clipped, out)
+
+
 def test_gspo_requires_active_token_per_sequence():
     with pytest.raises(ValueError):
         O.gspo_token_loss(np.ones(4), np.ones(4), np.ones(2), np.array([1, 1, 0, 0]), 2, 2)
@@ -336,8 +380,10 @@ def test_gspo_requires_active_token_per_sequence():
 
 # --- gradients ------------------------------------------------------------------
 
-def _torch_gmpo_full(X, W, b, y, old, ref, adv, mask, B, T, tau, el, eh, beta):
-    """Independent full-logits autograd statement of GMPO (q = 1)."""
+def _torch_gmpo_full(X, W, b, y, old, ref, adv, mask, B, T, tau, el, eh, beta, keep=None):
+    """Independent full-logits autograd statement of GMPO.  ``keep`` is a fixed
+    0/1 entropy-mask vector (no gradient flows through a threshold decision);
+    it scales each sequence's policy term by its kept fraction."""
     z = (X @ W.T + b) / tau
     logp = torch.log_softmax(z, -1).gather(1, y[:, None])[:, 0].reshape(B, T)
     m = mask.reshape(B, T)
@@ -346,9 +392,10 @@ def _torch_gmpo_full(X, W, b, y, old, ref, adv, mask, B, T, tau, el, eh, beta):
     clr = torch.where(A > 0, torch.clamp(lr, max=eh), torch.where(A < 0, torch.clamp(lr, min=-el), lr))
     n = m.sum(1)
     r = torch.exp((clr * m).sum(1) / n)
+    ebar = torch.ones_like(n) if keep is None else (keep.reshape(B, T) * m).sum(1) / n
     d = ref.reshape(B, T) - logp
     kl = torch.exp(d) - d - 1
-    return (-adv * r + beta * (kl * m).sum(1) / n).mean()
+    return (-adv * r * ebar + beta * (kl * m).sum(1) / n).mean()
 
 
 def _small_gmpo_case(seed):
@@ -397,6 +444,109 @@ def test_gradients_match_central_finite_differences(loss_type):
     def L(X_, W_, b_):
         _, lp, ent = O.row_stats(X_, W_, b_, y, tau)
         return O.loss_stage(prob, lp, ent, old, ref, adv, mask).loss
+
+    h = 1e-6
+    for name, arr, g in (("X", X, out["dX"]), ("W", W, out["dW"]), ("b", b, out["db"])):
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            save = arr[idx]
+            arr[idx] = save + h; up = L(X, W, b)
+            arr[idx] = save - h; dn = L(X, W, b)
+            arr[idx] = save
+            fd[idx] = (up - dn) / (2 * h)
+        assert np.allclose(g, fd, rtol=1e-6, atol=1e-9), name
+
+
+def _masked_gmpo_case():
+    """B=2, T=8, seven active tokens a sequence, q = 0.2 keeps 2 and 1 of them;
+    every active entropy lies at least 7e-3 from the threshold and from its
+    neighbours, and every log ratio at least 0.05 from a clip bound."""
+    rng = np.random.default_rng(0)
+    B, T, H, V = 2, 8, 6, 11
+    X, W, b, y = _rand_problem(rng, B * T, H, V)
+    tau = 0.7
+    _, logp, _ = O.row_stats(X, W, b, y, tau)
+    lr = np.random.default_rng(100).choice([-0.6, -0.1, 0.05, 0.15, 0.7], size=B * T)
+    old = logp - lr
+    ref = logp + np.random.default_rng(101).normal(0, 0.1, B * T)
+    mask = np.ones(B * T, np.uint8); mask[[0, T]] = 0
+    adv = np.array([1.0, -0.5])
+    return B, T, X, W, b, y, tau, old, ref, mask, adv
+
+
+def _torch_entropy_mask(X, W, b, tau, mask, q):
+    """The entropy mask from torch alone: Categorical entropy of the logits and
+    torch.quantile (linear) of the active entropies at 1 - q; keep H >= thr."""
+    z = (torch.tensor(X) @ torch.tensor(W).T + torch.tensor(b)) / tau
+    Hs = torch.distributions.Categorical(logits=z).entropy()
+    act = torch.tensor(mask) != 0
+    thr = torch.quantile(Hs[act], 1 - q, interpolation="linear")
+    return (act & (Hs >= thr)).to(torch.float64), Hs.numpy(), thr.item()
+
+
+def test_entropy_masked_gradients_match_autograd():
+    """GMPO with the entropy mask at q = 0.2 and beta != 0 ("support
+    top_entropy_quantile ...", Details: the mask multiplies the policy term
+    after the loss-type branch, before the KL penalty).  Every entry of dX, dW,
+    db and of c = dL/dlogp against autograd, with the mask taken from torch."""
+    B, T, X, W, b, y, tau, old, ref, mask, adv = _masked_gmpo_case()
+    q = 0.2
+    keep, Hs, thr = _torch_entropy_mask(X, W, b, tau, mask, q)
+    kept = keep.numpy().reshape(B, T).sum(1)
+    assert kept.tolist() == [2, 1]                                  # the kept fractions differ
+    act = np.sort(Hs[mask != 0])
+    assert np.abs(act - thr).min() > 5e-3 and np.diff(act).min() > 5e-3
+    prob = O.Problem(B, T, O.GMPO, 0.2, 0.3, 0.04, tau, q)
+    out = O.fwd_bwd(prob, X, W, b, y, old, ref, adv, mask)
+    assert np.array_equal(out["emask"], keep.numpy().astype(np.uint8))
+    assert out["metrics"][4] == pytest.approx(thr, abs=1e-12)
+    Xt, Wt, bt = (torch.tensor(a, requires_grad=True) for a in (X, W, b))
+    z = (Xt @ Wt.T + bt) / tau
+    lp_t = torch.log_softmax(z, -1).gather(1, torch.tensor(y)[:, None])[:, 0]
+    lp_t.retain_grad()
+    L = _torch_gmpo_full(Xt, Wt, bt, torch.tensor(y), torch.tensor(old), torch.tensor(ref),
+                         torch.tensor(adv), torch.tensor(mask, dtype=torch.float64), B, T, tau,
+                         O.f32(0.2), O.f32(0.3), 0.04, keep=keep)
+    L.backward()
+    assert out["loss"] == pytest.approx(L.item(), rel=1e-13)
+    assert np.allclose(out["dX"], Xt.grad.numpy(), rtol=1e-10, atol=1e-14)
+    assert np.allclose(out["dW"], Wt.grad.numpy(), rtol=1e-10, atol=1e-14)
+    assert np.allclose(out["db"], bt.grad.numpy(), rtol=1e-10, atol=1e-14)
+    # c itself: the gradient of the same statement with logp as the leaf
+    lp_leaf = torch.tensor(out["logp"], requires_grad=True)
+    m = torch.tensor(mask, dtype=torch.float64).reshape(B, T)
+    lr = lp_leaf.reshape(B, T) - torch.tensor(old).reshape(B, T)
+    A = torch.tensor(adv)[:, None]
+    clr = torch.where(A > 0, torch.clamp(lr, max=O.f32(0.3)), torch.clamp(lr, min=-O.f32(0.2)))
+    n = m.sum(1)
+    r = torch.exp((clr * m).sum(1) / n)
+    ebar = (keep.reshape(B, T) * m).sum(1) / n
+    d = torch.tensor(ref).reshape(B, T) - lp_leaf.reshape(B, T)
+    Lc = (-torch.tensor(adv) * r * ebar + 0.04 * ((torch.exp(d) - d - 1) * m).sum(1) / n).mean()
+    Lc.backward()
+    assert np.allclose(out["c"], lp_leaf.grad.numpy(), rtol=1e-12, atol=1e-16)
+    # non-vacuous: the masked coefficient differs from the unmasked one on every unclipped active token
+    nomask = O.gmpo_loss(out["logp"], old, ref, adv, mask, B, T, 0.2, 0.3, 0.04)
+    live = (mask != 0) & (out["c"] != nomask.c)
+    assert live.sum() == (mask != 0).sum() - out["clipped"].sum()
+
+
+def test_entropy_masked_gradients_match_central_finite_differences():
+    """The same masked case against central differences of the whole oracle
+    (h = 1e-6; the mask is recomputed at every point and does not change,
+    since no entropy lies within 5e-3 of the threshold or of another)."""
+    B, T, X, W, b, y, tau, old, ref, mask, adv = _masked_gmpo_case()
+    prob = O.Problem(B, T, O.GMPO, 0.2, 0.3, 0.04, tau, 0.2)
+    out = O.fwd_bwd(prob, X, W, b, y, old, ref, adv, mask)
+    base_mask = out["emask"].copy()
+
+    def L(X_, W_, b_):
+        _, lp, ent = O.row_stats(X_, W_, b_, y, tau)
+        res = O.loss_stage(prob, lp, ent, old, ref, adv, mask)
+        assert np.array_equal(res.emask, base_mask)
+        return res.loss
 
     h = 1e-6
     for name, arr, g in (("X", X, out["dX"]), ("W", W, out["dW"]), ("b", b, out["db"])):
