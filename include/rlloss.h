@@ -218,19 +218,32 @@ int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float*
  * graph, plugins that are handed only the tensors they read and write, and
  * runtimes whose memory pool is reserved in full up front.  It takes no
  * workspace.  The pages have no counterpart of this entry point.
- *   Scratch: a file-scope device array of 4 MiB inside the library, which
- *   every GPU that loads the library holds until the process exits.  A
- *   problem whose rlloss_loss_workspace_bytes exceeds 4 MiB (N = B*T tokens
- *   plus 64 bytes per sequence, plus about 9 KB: e.g. N > 2^21 with
- *   B <= 16384) is rejected with RLLOSS_ETOOLARGE before any launch.
+ *   Scratch: a file-scope device array of RLLOSS_NOALLOC_SCRATCH_BYTES
+ *   (4 MiB) inside the library, which every GPU that loads the library holds
+ *   until the process exits.  A problem fits when
+ *   rlloss_loss_workspace_bytes(cfg) <= RLLOSS_NOALLOC_SCRATCH_BYTES; callers
+ *   should size problems with that comparison.  The loss workspace is about
+ *   N + B*(84 + 40*S) + 9.5 KB bytes, each region rounded up to 256 bytes,
+ *   with N = B*T and S = min(ceil(4*SMs/B), ceil(T/256)) slices per sequence
+ *   (at least 1; SMs of the current device): on a 152-SM GPU, N up to about
+ *   4.1e6 tokens when B is small (at most ~25 KB of per-sequence sums), while
+ *   many short sequences fill it sooner (B = 34000 with T = 1 does not fit,
+ *   each sequence taking at least 124 + T bytes).  A larger problem is
+ *   rejected with RLLOSS_ETOOLARGE before any launch; a configuration the
+ *   workspace entry rejects gets the same code here (RLLOSS_EINVAL or
+ *   RLLOSS_EUNSUPPORTED).
  *   The first call on a device looks up the array's device address with that
- *   device current; make that first call before any stream capture.
+ *   device current and caches it; make that first call before any stream
+ *   capture.  A device reset (cudaDeviceReset) invalidates the cached
+ *   address: a call that meets a CUDA error drops it, so the call after the
+ *   error looks it up again.
  *   All calls share the one array, which keeps the last call's contents; each
  *   call clears what must start at zero.  Calls that overlap on the GPU (for
  *   example on two streams) race on the array and must not be issued.
  *   Arguments as for rlloss_loss_from_logp; out_device_status (optional,
  *   device int32) receives this call's device status word (RLLOSS_DEV_*). */
 #define RLLOSS_ETOOLARGE 5     /* problem larger than a fixed-size internal scratch */
+#define RLLOSS_NOALLOC_SCRATCH_BYTES (4u << 20)   /* size of that scratch */
 int rlloss_loss_from_logp_noalloc(const rlloss_cfg* cfg, const float* logp, const float* entropy,
                                   const float* old_logp, const float* ref_logp, const float* adv,
                                   const uint8_t* mask, float* out_loss, float* out_metrics,

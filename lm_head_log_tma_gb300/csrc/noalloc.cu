@@ -15,7 +15,8 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(4) << 20;   // 4 MiB, held by every GPU that loads the library
+constexpr size_t kScratchBytes = RLLOSS_NOALLOC_SCRATCH_BYTES;   // 4 MiB, held by every GPU that loads the library
+static_assert(kScratchBytes == (size_t(4) << 20), "scratch size is part of the ABI");
 
 static __device__ __align__(256) unsigned char g_loss_scratch[kScratchBytes];
 
@@ -41,6 +42,15 @@ int scratch_address(void** out) {
   return RLLOSS_OK;
 }
 
+// Forget the cached address of the current device, so that the next call looks
+// it up again (after a CUDA error, which a device reset would also produce).
+void forget_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+  std::lock_guard<std::mutex> g(g_mu);
+  g_scratch_ptr[dev] = nullptr;
+}
+
 }  // namespace
 
 extern "C" int rlloss_loss_from_logp_noalloc(const rlloss_cfg* cfg, const float* logp, const float* entropy,
@@ -49,19 +59,29 @@ extern "C" int rlloss_loss_from_logp_noalloc(const rlloss_cfg* cfg, const float*
                                              float* out_dlogp, uint8_t* out_entropy_mask,
                                              int32_t* out_device_status, void* stream) {
   const size_t need = rlloss_loss_workspace_bytes(cfg);
-  if (need == 0) return RLLOSS_EINVAL;
+  if (need == 0) {
+    // The configuration failed validation: let the workspace entry, which
+    // validates before anything else, name the reason, so both entries return
+    // the same code for the same cfg.  No workspace is passed, so nothing runs.
+    const int v = rlloss_loss_from_logp(cfg, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                        nullptr, nullptr, nullptr, nullptr, 0, stream);
+    return v != RLLOSS_OK ? v : RLLOSS_EINVAL;
+  }
   if (need > kScratchBytes) return RLLOSS_ETOOLARGE;
   void* scratch = nullptr;
   const int e = scratch_address(&scratch);
   if (e != RLLOSS_OK) return e;
   const int rc = rlloss_loss_from_logp(cfg, logp, entropy, old_logp, ref_logp, adv, mask, out_loss, out_metrics,
                                        out_dlogp, out_entropy_mask, scratch, kScratchBytes, stream);
+  if (rc == RLLOSS_ECUDA) forget_scratch_address();
   if (rc != RLLOSS_OK) return rc;
   if (out_device_status) {
     // the status word sits at the start of the scratch
     if (cudaMemcpyAsync(out_device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+      forget_scratch_address();
       return RLLOSS_ECUDA;
+    }
   }
   return RLLOSS_OK;
 }

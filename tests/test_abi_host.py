@@ -139,6 +139,32 @@ def test_loss_from_logp_validation():
     assert rc == R.EINVAL
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(loss_type=R.GSPO_TOKEN, beta=0.1), R.EUNSUPPORTED),
+    (dict(loss_type=R.GSPO_TOKEN, top_entropy_quantile=0.5), R.EUNSUPPORTED),
+    (dict(flags=R.FLAG_ADV_PER_TOKEN), R.EUNSUPPORTED),
+    (dict(top_entropy_quantile=1.5), R.EINVAL),
+    (dict(is_level=R.IS_SEQUENCE), R.EINVAL),
+    (dict(B=0), R.EINVAL),
+])
+def test_noalloc_and_workspace_loss_entries_agree_on_rejections(kw, code):
+    """The allocation-free loss entry returns the workspace entry's code for a
+    configuration that entry rejects (validation runs before any CUDA call)."""
+    cfg = _cfg(**kw)
+    ws = R.lib.rlloss_loss_from_logp(ctypes.byref(cfg), *([None] * 10), None, 0, None)
+    f = R.lib.rlloss_loss_from_logp_noalloc
+    f.argtypes = [ctypes.POINTER(R.RllossCfg)] + [ctypes.c_void_p] * 12
+    f.restype = ctypes.c_int
+    na = f(ctypes.byref(cfg), *([None] * 12))
+    assert ws == na == code
+
+
+def test_noalloc_scratch_limit_is_exported():
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "include", "rlloss.h")).read()
+    assert "#define RLLOSS_NOALLOC_SCRATCH_BYTES (4u << 20)" in text
+
+
 def test_e4m3_scoring_validation():
     """e4m3 operands: only through rlloss_forward_e4m3, rows of 16-byte
     multiples, CTA-pair tiles only; the plain forward refuses them."""

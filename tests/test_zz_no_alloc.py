@@ -6,14 +6,19 @@ handed only the tensors they read and write, runtimes whose memory pool is
 reserved in full up front.  Its scratch is a fixed 4 MiB array inside the
 library instead of a caller workspace.  Here it is called through the C ABI
 twice in a row (different problem shapes, so stale contents of the shared
-array would show) and checked against rlloss_loss_from_logp on the same inputs.
+array would show) and checked against rlloss_loss_from_logp on the same inputs,
+and once against the fp64 oracle, so that a fault the two entries share would
+not go unseen.
 
 The file name makes pytest collect it last.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
+
+import oracle as O
 
 from lm_head_log_tma_gb300.workloads import random_entropies
 
@@ -88,3 +93,26 @@ def test_noalloc_rejects_problems_beyond_its_scratch(R):
     cfg = R.make_cfg(1, 1 << 22)          # 4 Mi tokens: needs more than the 4 MiB scratch
     rc = f(ctypes.byref(cfg), *([None] * 12))
     assert rc == 5                         # RLLOSS_ETOOLARGE
+
+
+def test_noalloc_matches_the_oracle(R):
+    """GMPO with K3 KL and the entropy mask at q = 0.2 against the fp64 oracle
+    on the same fp32 inputs: the mask bit for bit, the loss within 1e-5."""
+    f = _entry(R)
+    B, T = 5, 600
+    cfg = R.make_cfg(B, T, eps_low=0.2, eps_high=0.3, beta=0.04, top_entropy_quantile=0.2)
+    t = _inputs(B, T, 23)
+    rc, a = _call_noalloc(R, f, cfg, t)
+    assert rc == R.OK
+    torch.cuda.synchronize()
+    assert a["status"].item() == 0
+    h = {k: v.cpu().double().numpy() for k, v in t.items()}
+    o = O.gmpo_loss(h["logp"], h["old"], h["ref"], h["adv"], h["mask"].astype(np.uint8), B, T, 0.2, 0.3,
+                    beta=0.04, entropy=h["ent"], q=0.2)
+    assert np.array_equal(a["emask"].cpu().numpy(), o.emask)
+    assert abs(a["loss"].item() - o.loss) <= LOSS_RTOL * abs(o.loss)
+    g = a["dlogp"].cpu().double().numpy()
+    assert np.array_equal(g == 0, o.c == 0)
+    assert np.allclose(g, o.c, rtol=1e-5, atol=1e-12)
+    m = a["metrics"].cpu().double().numpy()
+    assert m[1] == o.metrics[1] and m[3] == o.metrics[3] and m[5] == o.metrics[5]
