@@ -1,7 +1,7 @@
 """Run a few fused forward+backward steps of the Qwen-0.5B LM-head workload
 recipe at a chosen token count, for profilers (ncu) to attach to.
 
-  python -m lm_head_log_tma_gb300.profile_step --T 2048 --steps 1 --warmup 2
+  python profile_step.py --T 2048 --steps 1 --warmup 2
 
 The inputs follow the workload recipe (H=896, V=151936, bf16, GMPO); the
 sampler log-probs are the policy's plus noise, with the policy log-probs
