@@ -30,7 +30,6 @@ METRIC = "fused LM-head+GMPO fwd+bwd tokens/s at H896/V151936; % bf16 TC peak"
 UNIT = "tokens/s"
 WORKLOAD_INDEX = 1
 REF_SAMPLE_TOKENS = 512
-CPU_BASELINE_TOKENS = 2048
 
 
 def parse_args():
@@ -52,9 +51,15 @@ def parse_args():
                          "gradients); e4m3 quantizes X and W per row first (outside the timed region)")
     ap.add_argument("--all-rows", action="store_true",
                     help="run the backward over every row (RLLOSS_FLAG_ALL_ROWS), for comparison")
+    ap.add_argument("--recompute", action="store_true",
+                    help="recompute every backward row's logits (RLLOSS_FLAG_RECOMPUTE), for comparison")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
     ap.add_argument("--no-naive-memory", action="store_true",
                     help="skip the full-logits torch path run for the memory comparison")
+    # internal: time the oracle on workload INDEX in a child process whose BLAS
+    # thread count was fixed before numpy loaded
+    ap.add_argument("--cpu-oracle-child", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-threads", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -297,6 +302,61 @@ def oracle_sample_rate(spec, inp, old, ref, tokens):
     return tokens / dt, dt, threads
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_child(index, threads):
+    """Body of --cpu-oracle-child: the oracle's fwd+bwd of the whole batch of
+    workload ``index`` (CPU inputs from the same seeds; sampler log-probs from
+    a CPU full-logits pass), repeated for at least 2 s.  Prints one JSON line."""
+    import torch
+    import oracle as O
+    from lm_head_log_tma_gb300.workloads import WORKLOADS, make_inputs
+    spec = WORKLOADS[index]
+    inp = make_inputs(spec, device="cpu")
+    z = (inp.X.double() @ inp.W.double().T)
+    if inp.b is not None:
+        z += inp.b.double()
+    z /= spec.temperature
+    pol = (z.gather(1, inp.targets[:, None])[:, 0] - torch.logsumexp(z, 1)).float()
+    old, ref = inp.old_logp(pol), inp.ref_logp(pol)
+    prob = O.Problem(spec.B, spec.T, spec.loss_type, spec.eps_low, spec.eps_high, spec.beta, spec.temperature,
+                     spec.top_entropy_quantile)
+    nt = threads or os.cpu_count() or 1
+    run = lambda: O.fwd_bwd(prob, inp.X, inp.W, inp.b, inp.targets, old, ref, inp.adv, inp.mask, threads=nt)
+    run()
+    reps, t = 0, time.perf_counter()
+    while reps < 3 or time.perf_counter() - t < 2.0:
+        run()
+        reps += 1
+    dt = (time.perf_counter() - t) / reps
+    print(json.dumps({"value": spec.N / dt, "unit": UNIT, "seconds_per_batch": dt, "threads": nt,
+                      "reps": reps}), flush=True)
+    return 0
+
+
+def oracle_child_rate(index, threads):
+    """Runs oracle_child in a fresh process: with threads == 1 every BLAS and
+    OpenMP pool is held to one thread as well."""
+    env = dict(os.environ)
+    if threads == 1:
+        env.update(OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1", BLIS_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-child", str(index),
+                        "--oracle-threads", str(threads)], env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle child failed: " + r.stderr[-500:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def run_reference(args):
     world, rank, local = dist_env()
     if rank != 0:
@@ -420,7 +480,8 @@ def measure(args, index, dev, world, rank, local):
     from lm_head_log_tma_gb300 import rlloss as R
 
     spec, inp, old, ref = make_workload(dev, index)
-    cfg = cfg_for(R, spec, args.chunk_rows, R.FLAG_ALL_ROWS if args.all_rows else 0)
+    cfg = cfg_for(R, spec, args.chunk_rows, (R.FLAG_ALL_ROWS if args.all_rows else 0) |
+                  (R.FLAG_RECOMPUTE if args.recompute else 0))
     N, H, V = spec.N, spec.H, spec.V
     ws_bytes = R.rlloss_workspace_bytes(cfg)
     naive_bytes, naive_note = (None, "skipped") if args.no_naive_memory else naive_peak_extra_bytes(
@@ -446,7 +507,8 @@ def measure(args, index, dev, world, rank, local):
     torch.cuda.synchronize()
     call_alloc = torch.cuda.max_memory_allocated(dev) - mem0
     status = R.rlloss_get_device_status(ws)
-    bwd_rows = R.rlloss_get_backward_rows(ws)   # rows with c_n != 0: the backward runs over these
+    bwd_rows = R.rlloss_get_backward_rows(ws)   # recomputed rows with c_n != 0
+    st_rows = R.rlloss_get_stored_rows(ws)      # rows whose dX, dW came from the stored probabilities
     # rows the forward computed: whole row tiles holding an unmasked row
     fwd_rows = min(N, R.rlloss_get_forward_tiles(ws) * (128 if (cfg.flags & R.FLAG_SINGLE_CTA_TILES) else 256))
     if status != 0:
@@ -583,23 +645,26 @@ def measure(args, index, dev, world, rank, local):
     peak, peak_sus, hbm, peak_src = load_peaks()
     per_step = [m / args.steps for m in phase_ms]
     # tensor-core phases and the flop they execute per step: the forward over
-    # all N rows, the recompute and dX/dW over the backward's rows
+    # its rows, the recompute over the recomputed rows, dX/dW over those and
+    # the stored rows
     gemm_phases = {0: ("fwd_gemm", 2.0 * fwd_rows), 2: ("bwd_dlogits", 2.0 * bwd_rows),
-                   3: ("bwd_dX_dW", 4.0 * bwd_rows)}
+                   3: ("bwd_dX_dW", 4.0 * (bwd_rows + st_rows))}
     dom = max(gemm_phases, key=lambda k: per_step[k])
     flops_phase = gemm_phases[dom][1] * H * V
     launches_per_step = max(1, phase_n[dom] // args.steps)
     achieved = flops_phase / (per_step[dom] / 1e3) / 1e12
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic_qwen05b_t4096.txt")
-    if os.path.exists(tp):
-        traffic = json.load(open(tp)).get(gemm_phases[dom][0])
+    if os.path.exists(tp):   # counters taken for this backward form only
+        tr = json.load(open(tp))
+        if tr.get("backward") == ("stored" if st_rows > 0 else "recompute"):
+            traffic = tr.get(gemm_phases[dom][0])
     roofline = {"bound": "tensor", "kernel": gemm_phases[dom][0], "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 burst", "frac_of_sustained": achieved / peak_sus,
                 "launches_per_step": launches_per_step}
     step_tflops = 6.0 * N * H * V / (ms_step / 1e3) / 1e12
-    executed_tflops = (2.0 * fwd_rows + 6.0 * bwd_rows) * H * V / (ms_step / 1e3) / 1e12
+    executed_tflops = (2.0 * fwd_rows + 4.0 * st_rows + 6.0 * bwd_rows) * H * V / (ms_step / 1e3) / 1e12
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -609,6 +674,7 @@ def measure(args, index, dev, world, rank, local):
             "tc_tflops_6nhv": step_tflops,
             "forward_rows": fwd_rows,
             "backward_rows": bwd_rows,
+            "stored_rows": st_rows,
             "executed_tflops": executed_tflops,
             "executed_peak_frac": executed_tflops / peak,
             "roofline": roofline,
@@ -625,22 +691,32 @@ def measure(args, index, dev, world, rank, local):
                        "naive_full_logits_peak_extra_bytes": naive_bytes,
                        "naive_fits": naive_bytes is not None, "naive_note": naive_note,
                        "chunk_rows": args.chunk_rows or "default",
-                       "backward": "dense" if args.all_rows else "rows with c_n != 0"}}
+                       "backward": ("dense" if args.all_rows else "rows with c_n != 0") +
+                                   ("; dX, dW of the stored rows from the forward's stored probabilities"
+                                    if st_rows > 0 else "; every row recomputed")}}
 
     if rank == 0 and not args.no_cpu_baseline:
-        if args.all_configs:   # config 0 whole, the others one sequence
-            tokens = N if index == 0 else spec.T
-            what = "the whole batch" if index == 0 else f"the last sequence ({spec.T} tokens)"
+        # config 0 whole (1 thread and all threads), the others one whole sequence
+        tokens = N if index == 0 else spec.T
+        what = "the whole batch" if index == 0 else f"the last sequence ({spec.T} tokens)"
+        if index == 0:
+            one, every = oracle_child_rate(0, 1), oracle_child_rate(0, 0)
+            rate, secs, threads = every["value"], every["seconds_per_batch"] * every["reps"], every["threads"]
         else:
-            tokens, what = CPU_BASELINE_TOKENS, f"last {CPU_BASELINE_TOKENS} tokens of the batch as one sequence"
-        rate, secs, threads = oracle_sample_rate(spec, inp, old, ref, tokens)
+            rate, secs, threads = oracle_sample_rate(spec, inp, old, ref, tokens)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "cpu_model": cpu_model(),
                                 "sample": f"{what}, full H and V, fp64 numpy fwd+bwd ({secs:.1f} s)"}
+        if index == 0:
+            line["cpu_baseline"]["threads_1"] = one
+            line["cpu_baseline"]["threads_all"] = every
     return line
 
 
 def main():
     args = parse_args()
+    if args.cpu_oracle_child is not None:
+        return oracle_child(args.cpu_oracle_child, args.oracle_threads)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

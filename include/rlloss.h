@@ -110,6 +110,17 @@ extern "C" {
                                                 fixed order, so repeated calls from the same
                                                 initial values give the same bits.  Ignored by the
                                                 forward-only entries */
+#define RLLOSS_FLAG_RECOMPUTE 0x20u          /* recompute the logits of every backward row.  By
+                                                default, with bf16 operands, no bias and without
+                                                ACCUMULATE, rlloss_fwd_bwd has the forward also
+                                                write each logit's unnormalised probability 2^t
+                                                (bf16) for the row tiles that fit the chunk buffer
+                                                (the memory the recompute's dlogits chunk would
+                                                use), and forms dX and dW of those rows from them
+                                                with no second logits GEMM; rows outside those
+                                                tiles, or whose log-sum-exp lies outside about
+                                                [-55, 66] nats, are recomputed.  Same results up
+                                                to bf16 rounding of the dlogits; for comparison */
 
 #define RLLOSS_NMETRICS 8
 /* out_metrics layout:
@@ -401,6 +412,16 @@ int rlloss_get_device_status(const void* workspace, int32_t* status);
  * has finished.  Returns RLLOSS_ECUDA if the copy failed.  (Our addition, for
  * reporting executed work; the pages have no counterpart.) */
 int rlloss_get_backward_rows(const void* workspace, int32_t* rows);
+
+/* Copy into *rows the number of rows the last rlloss_fwd_bwd on ``workspace``
+ * formed dX and dW for from the forward's stored probabilities (whole
+ * 256-row tiles, rows with c_n = 0 included; 0 under RLLOSS_FLAG_RECOMPUTE,
+ * with a bias, fp32 operands or ACCUMULATE).  The rows counted by
+ * rlloss_get_backward_rows are the others, recomputed.  Synchronous; call
+ * after the stream has finished.  Returns RLLOSS_ECUDA if the copy failed.
+ * (Our addition, for reporting executed work; the pages have no
+ * counterpart.) */
+int rlloss_get_stored_rows(const void* workspace, int32_t* rows);
 
 /* Copy into *tiles the number of row tiles (256 rows each, 128 with
  * RLLOSS_FLAG_SINGLE_CTA_TILES) the last forward on ``workspace`` computed:

@@ -25,6 +25,7 @@ constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
 // [16] tile-scan ticket, [20] forward row tiles, [24] forward vocabulary segments.
 constexpr size_t kBackwardRowsOffset = 12;
 constexpr size_t kTileTicketOffset = 16, kFwdTilesOffset = 20, kFwdSegmentsOffset = 24;
+constexpr size_t kStoredRowsOffset = 28;   // rows the stored-probability backward ran over
 constexpr size_t kPartialCapBytes = size_t(64) << 20;
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
@@ -66,7 +67,7 @@ int validate_common(const rlloss_cfg* c) {
   const float q = c->top_entropy_quantile;
   if (!(q >= 0.f && q <= 1.f)) return RLLOSS_EINVAL;
   if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN |
-                   RLLOSS_FLAG_ALL_ROWS | RLLOSS_FLAG_ACCUMULATE))
+                   RLLOSS_FLAG_ALL_ROWS | RLLOSS_FLAG_ACCUMULATE | RLLOSS_FLAG_RECOMPUTE))
     return RLLOSS_EINVAL;
   if ((c->flags & RLLOSS_FLAG_ADV_PER_TOKEN) && c->loss_type != RLLOSS_GSPO_TOKEN) return RLLOSS_EUNSUPPORTED;
   if (c->loss_type == RLLOSS_GSPO_TOKEN) {
@@ -82,7 +83,7 @@ int validate_head(const rlloss_cfg* c) {
   if (c->B < 1 || c->T < 1) return RLLOSS_EINVAL;
   if ((long long)c->B * c->T > (1ll << 31) - 1) return RLLOSS_EINVAL;
   if (c->flags & ~(RLLOSS_FLAG_FORCE_ENTROPY_PATH | RLLOSS_FLAG_SINGLE_CTA_TILES | RLLOSS_FLAG_ADV_PER_TOKEN |
-                   RLLOSS_FLAG_ALL_ROWS | RLLOSS_FLAG_ACCUMULATE))
+                   RLLOSS_FLAG_ALL_ROWS | RLLOSS_FLAG_ACCUMULATE | RLLOSS_FLAG_RECOMPUTE))
     return RLLOSS_EINVAL;
   if (c->H < 1 || c->V < 1) return RLLOSS_EINVAL;
   if (c->dtype != RLLOSS_BF16 && c->dtype != RLLOSS_FP32 && c->dtype != RLLOSS_FP8_E4M3) return RLLOSS_EINVAL;
@@ -131,6 +132,12 @@ struct Plan {
   size_t o_status, o_partial, o_lse2, o_logp64, o_ent, o_coef, o_emask, o_k3, o_seq, o_bias2, o_dl, o_x3, o_w3,
       o_dbpart, o_ws2, o_tflags, o_tlist, o_blk, o_cidx, o_xc, o_coefc, o_lse2c, o_tgtc, o_dxc, o_err, total;
   int Ncap;                 // rows of the compacted arrays (N rounded up to 256)
+  // Stored probabilities: the forward writes 2^t for the row tiles of its
+  // first pu_tiles slots into the chunk buffer, and the backward of their
+  // rows needs no recompute (bf16 CTA pairs, no bias, no ACCUMULATE).
+  bool stored;
+  int pu_tiles;
+  size_t o_done;
 };
 
 // Largest vocabulary-segment count whose partial states fit the cap (<= 64).
@@ -235,10 +242,14 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.Nc = int(std::min<long long>(want, rup(p.N, 128)));
     p.nchunks = int(cdiv(p.N, p.Nc));
     p.ld_dl = p.fp32 ? 2 * p.Vp : p.Vp;
-    p.o_coef = take(size_t(p.N) * 4);
-    p.o_dl = take(size_t(p.Nc) * p.ld_dl * 2);
-    p.o_dbpart = take(p.bias ? size_t(db_part_rows(p.Nc)) * p.V * 4 : 0);
     p.compact = !(c->flags & RLLOSS_FLAG_ALL_ROWS);
+    p.stored = mode == kFull && !p.fp32 && !p.f8 && !p.bias && p.pair == 2 && p.kbx == 2 && p.compact &&
+               !(c->flags & (RLLOSS_FLAG_ACCUMULATE | RLLOSS_FLAG_RECOMPUTE));
+    p.pu_tiles = p.stored ? int(cdiv(p.Nc, 256)) : 0;
+    p.o_coef = take(size_t(p.N) * 4);
+    p.o_dl = take(size_t(std::max(p.Nc, p.pu_tiles * 256)) * p.ld_dl * 2);
+    p.o_dbpart = take(p.bias ? size_t(db_part_rows(p.Nc)) * p.V * 4 : 0);
+    p.o_done = take(p.stored ? size_t(p.N) : 0);
     // bf16 G: each backward row's target-entry rounding error (rows or
     // compacted rows, N rounded up to whole 256-row tiles)
     p.o_err = take(p.fp32 ? 0 : size_t(rup(p.N, 256)) * 4);
@@ -520,6 +531,8 @@ int prepare_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void
 // with skip_mask != 0 (the rows of the other tiles get no outputs).
 // v_begin: vocabulary id of W's first row when W is a shard of a larger
 // vocabulary (targets outside the shard match no column).
+// With p.stored the forward also writes the stored probabilities of its first
+// p.pu_tiles row-tile slots into the chunk buffer.
 int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W, const void* b,
              const int64_t* targets, float* out_logp, float* out_entropy, float* out_lse, char* ws,
              cudaStream_t st, Head& h, bool merge = true, const uint8_t* skip_mask = nullptr,
@@ -530,6 +543,12 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
   FwdParams& fp = h.fp;
   fp.targets = targets;
   fp.v_begin = v_begin;
+  if (p.stored) {
+    if (!tmap_bf16_box(&fp.tmPu, ws + p.o_dl, p.V, (long long)p.pu_tiles * 256, p.ld_dl, 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B))
+      return RLLOSS_ECUDA;
+    fp.pu_tiles = p.pu_tiles;
+  }
   const uint8_t* tflags = nullptr;
   if (skip_mask) {
     tflags = reinterpret_cast<uint8_t*>(ws + p.o_tflags);
@@ -610,6 +629,96 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
   const int* cidx = nullptr;
   float* dxc = nullptr;
   long long xb_rows = p.N;
+  uint8_t* done = nullptr;
+  if (p.stored) {
+    // ---- rows whose probabilities the forward stored: no recompute.
+    //   G = k2 pu off the target and k1 at it (StoredParams), so
+    //   dX = k2 (pu W) + err W[target] with pu's target entry bf16(k1 / k2),
+    //   dW = pu^T (k2 X), both in one grouped launch over the stored rows.
+    done = reinterpret_cast<uint8_t*>(ws + p.o_done);
+    int* srows = reinterpret_cast<int*>(ws + p.o_status + kStoredRowsOffset);
+    __nv_bfloat16* pu = reinterpret_cast<__nv_bfloat16*>(ws + p.o_dl);
+    const int pu_rows = p.pu_tiles * 256;
+    StoredParams sp{};
+    sp.N = p.N;
+    sp.H = p.H;
+    sp.V = p.V;
+    sp.rows_cap = pu_rows;
+    sp.R = p.R;
+    sp.tiles = hd.fp.tiles;
+    sp.ntiles = hd.fp.ntiles;
+    sp.pu_tiles = p.pu_tiles;
+    sp.coef = coef;
+    sp.lse2 = lse2;
+    sp.logp64 = reinterpret_cast<const double*>(ws + p.o_logp64);
+    sp.targets = targets;
+    sp.x = static_cast<const __nv_bfloat16*>(hd.Xop);
+    sp.pu = pu;
+    sp.pu_ld = p.ld_dl;
+    sp.xs = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
+    sp.idx = reinterpret_cast<int*>(ws + p.o_cidx);
+    sp.k2 = reinterpret_cast<float*>(ws + p.o_coefc);
+    sp.err = err;
+    sp.tgt = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
+    sp.done = done;
+    sp.rows_total = srows;
+    {
+      Phase ph(st, 5);
+      RL_TRY(cudaMemsetAsync(dX, 0, size_t(p.N) * p.H * 4, st));
+      RL_TRY(cudaMemsetAsync(done, 0, size_t(p.N), st));
+      RL_TRY(launch_stored_rows(sp, st));
+      ph.launched(1);
+    }
+    HParams hp{};
+    set_bwd_segments(hp, p);
+    if (!tmap_bf16(&hp.tmA[0], pu, p.V, pu_rows, p.ld_dl, 128)) return RLLOSS_ECUDA;
+    if (!tmap_bf16(&hp.tmB[0], hd.Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
+    if (!tmap_f32_out(&hp.tmO[0], dX, p.H, p.N)) return RLLOSS_ECUDA;   // unused: rows go through dx_idx
+    if (!tmap_bf16(&hp.tmA[1], pu, p.V, pu_rows, p.ld_dl, 64)) return RLLOSS_ECUDA;
+    if (!tmap_bf16(&hp.tmB[1], sp.xs, p.Kx, pu_rows, p.Kx, 64)) return RLLOSS_ECUDA;
+    if (!tmap_f32_out(&hp.tmO[1], dW, p.H, p.V)) return RLLOSS_ECUDA;
+    HProblem& px = hp.pr[0];
+    px.kb_per_seg = int(cdiv(p.V, 64));
+    px.Mt = p.pu_tiles;
+    px.Ht = int(cdiv(p.H, 448));
+    px.Hout = p.H;
+    px.order = 0;
+    px.a_mn = 0;
+    px.ksplit = px.kb_per_seg >= 2 ? 2 : 1;   // two halves: two addends onto the zeroed dX
+    px.reduce = 1;
+    HProblem& pw = hp.pr[1];
+    pw.kb_per_seg = int(cdiv(pu_rows, 64));
+    pw.Mt = int(cdiv(p.V, 256));
+    pw.Ht = int(cdiv(p.H, 448));
+    pw.Hout = p.H;
+    pw.order = 1;
+    pw.a_mn = 1;
+    pw.reduce = 0;
+    pw.ksplit = 1;
+    hp.nprob = 2;
+    const int kx = px.kb_per_seg / px.ksplit, kw = pw.kb_per_seg;
+    hp.d_tiles = std::max(1, (kx + kw / 2) / kw);
+    hp.rows_total = srows;
+    hp.n0 = 0;
+    hp.nc_max = pu_rows;
+    hp.status = status;
+    hp.limit_ns = kWaitLimitNs;
+    hp.dx_idx = sp.idx;
+    hp.dx_out = dX;
+    hp.dx_nrows = p.N;
+    hp.dx_ld = p.H;
+    hp.dx_vec = dx_vec ? 1 : 0;
+    hp.dx_scale = sp.k2;
+    hp.dx_err = err;
+    hp.dx_tgt = sp.tgt;
+    hp.dx_w = static_cast<const __nv_bfloat16*>(hd.Wop);
+    hp.dx_wbegin = 0;
+    hp.dx_wrows = p.V;
+    hp.dx_wld = p.Kx;
+    Phase ph(st, 3);
+    RL_TRY(launch_gemmH(hp, px.Mt * px.Ht * px.ksplit + pw.Mt * pw.Ht, st));
+    ph.launched();
+  }
   {
     Phase ph(st, 5);
     if (p.compact) {
@@ -632,7 +741,8 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       cp.xc = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
       cp.errc = err;
       cp.status = status;
-      if (!acc) {   // the gather zeroes dX; the dX/dW launch adds the kept rows into it
+      cp.done = done;
+      if (!acc && !p.stored) {   // the gather zeroes dX; the dX/dW launch adds the kept rows into it
         cp.dx_zero = dX;
         cp.H = p.H;
         cp.dx_vec = dx_vec ? 1 : 0;
@@ -733,7 +843,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       pw.Hout = p.H;
       pw.order = 1;
       pw.a_mn = 1;
-      pw.reduce = (ch > 0 || acc) ? 1 : 0;
+      pw.reduce = (ch > 0 || acc || p.stored) ? 1 : 0;
       pw.ksplit = 1;
       hp.nprob = 2;
       const int kx = hp.nseg * px.kb_per_seg / px.ksplit, kw = hp.nseg * pw.kb_per_seg;
@@ -856,6 +966,12 @@ int rlloss_get_forward_tiles(const void* workspace, int32_t* tiles) {
 int rlloss_get_backward_rows(const void* workspace, int32_t* rows) {
   if (!workspace || !rows) return RLLOSS_EINVAL;
   return cuda_rc(cudaMemcpy(rows, static_cast<const char*>(workspace) + kBackwardRowsOffset, sizeof(int32_t),
+                            cudaMemcpyDeviceToHost));
+}
+
+int rlloss_get_stored_rows(const void* workspace, int32_t* rows) {
+  if (!workspace || !rows) return RLLOSS_EINVAL;
+  return cuda_rc(cudaMemcpy(rows, static_cast<const char*>(workspace) + kStoredRowsOffset, sizeof(int32_t),
                             cudaMemcpyDeviceToHost));
 }
 

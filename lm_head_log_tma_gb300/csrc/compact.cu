@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(kCompactBlock) compact_count_kernel(CompactPar
   __shared__ int is_last;
   __shared__ int part[kCompactBlock];
   const int n = blockIdx.x * kCompactBlock + threadIdx.x;
-  const unsigned bal = __ballot_sync(0xffffffffu, n < p.N && p.coef[n] != 0.f);
+  const unsigned bal = __ballot_sync(0xffffffffu, n < p.N && p.coef[n] != 0.f && !(p.done && p.done[n]));
   const int ngroups = (p.N + kGroup - 1) / kGroup;
   const int grp = n / kGroup;
   if ((threadIdx.x & 31) == 0 && grp < ngroups) p.blk_cnt[grp] = __popc(bal);
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactPa
   const int g = blockIdx.x;
   if (threadIdx.x < 32) {
     const int n = g * kGroup + threadIdx.x;
-    const bool keep = n < p.N && p.coef[n] != 0.f;
+    const bool keep = n < p.N && p.coef[n] != 0.f && !(p.done && p.done[n]);
     const unsigned bal = __ballot_sync(0xffffffffu, keep);
     const int rank = __popc(bal & ((1u << threadIdx.x) - 1u));
     if (keep && RL_DCHECK(p.blk_off[g] + rank < p.Ncap, p.status)) {
@@ -191,6 +191,75 @@ __global__ void scatter_rows_kernel(const float4* src, const int* idx, const int
     }
     *d = v;
   }
+}
+
+// One warp per row of the stored-probability buffer (see StoredParams): lane
+// 0 forms the row's factors and writes its target entry into the buffer, the
+// warp writes the scaled X row.
+__global__ void __launch_bounds__(kCompactBlock) stored_rows_kernel(StoredParams p) {
+  const int lane = threadIdx.x & 31;
+  const int nt = p.tiles ? *p.ntiles : p.R;
+  const int rows = min(nt, p.pu_tiles) * 256;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.rows_total = rows;
+  const int wstep = int(gridDim.x) * (kCompactBlock / 32);
+  for (int j = int(blockIdx.x) * (kCompactBlock / 32) + (threadIdx.x >> 5); j < rows; j += wstep) {
+    const int slot = j >> 8;
+    const int n = (p.tiles ? p.tiles[slot] : slot) * 256 + (j & 255);
+    int ok = 0;
+    float k2 = 0.f, er = 0.f;
+    long long y = -1;
+    if (lane == 0 && n < p.N) {
+      const float cf = p.coef[n];
+      const float l2 = p.lse2[n];
+      y = p.targets[n];
+      if (cf != 0.f && l2 >= kStoredLse2Min && l2 <= kStoredLse2Max && y >= 0 && y < p.V) {
+        // G = (c/tau)(onehot - p) with p = pu 2^-lse2: off the target G = k2 pu,
+        // at the target k1 = (c/tau)(1 - p_y), 1 - p_y = -expm1(logp)
+        const double k2d = -double(cf) * exp2(-double(l2));
+        const double k1d = double(cf) * -expm1(p.logp64[n]);
+        const __nv_bfloat16 tv = __float2bfloat16_rn(float(k1d / k2d));
+        k2 = float(k2d);
+        er = float(k1d - k2d * double(__bfloat162float(tv)));
+        p.pu[size_t(j) * p.pu_ld + size_t(y)] = tv;
+        ok = 1;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    k2 = __shfl_sync(0xffffffffu, k2, 0);
+    const int words = p.H / 8;   // 16-byte words per row
+    uint4* dst = reinterpret_cast<uint4*>(p.xs + size_t(j) * p.H);
+    if (ok) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(n) * p.H);
+      for (int w = lane; w < words; w += 32) {
+        const uint4 u = __ldg(src + w);
+        uint32_t in[4] = {u.x, u.y, u.z, u.w}, out[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&in[k]);
+          const __nv_bfloat162 r2 = __floats2bfloat162_rn(k2 * __low2float(b2), k2 * __high2float(b2));
+          out[k] = *reinterpret_cast<const uint32_t*>(&r2);
+        }
+        dst[w] = make_uint4(out[0], out[1], out[2], out[3]);
+      }
+    } else {
+      for (int w = lane; w < words; w += 32) dst[w] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (lane == 0) {
+      p.idx[j] = ok ? n : -1;
+      p.k2[j] = k2;
+      p.err[j] = er;
+      p.tgt[j] = ok ? y : -1;
+      if (ok) p.done[n] = 1;
+    }
+  }
+}
+
+cudaError_t launch_stored_rows(const StoredParams& p, cudaStream_t st) {
+  long long blocks = (p.rows_cap + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  stored_rows_kernel<<<int(blocks), kCompactBlock, 0, st>>>(p);
+  return cudaGetLastError();
 }
 
 int compact_groups(int N) { return (N + kGroup - 1) / kGroup; }

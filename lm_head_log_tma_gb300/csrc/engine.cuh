@@ -50,6 +50,7 @@ struct TileInfo {
   bool first;    // first tile of its unit
   bool last;     // last tile of its unit
   int aux = 0;   // policy-defined (dX/dW: k-blocks per product term; forward: vocabulary segments)
+  int slot = 0;  // forward: slot of the row tile in the launch's tile order
 };
 
 // Wait that ignores the abort flag; used only to drain in-flight work.

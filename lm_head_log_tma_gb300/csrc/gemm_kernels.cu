@@ -25,6 +25,32 @@
 
 namespace rl {
 
+// One 32-row x 32-column bf16 box (this lane's 64-byte row w) leaves through
+// a per-warp staging buffer (two alternate, 64-byte swizzle) and a TMA store
+// to columns x.., rows y.. of map m.
+constexpr int kBf16BoxBytes = 32 * 64;
+// zero_col in [0, 32): that element of this lane's row is written as 0.
+__device__ __forceinline__ void store_bf16_box(const CUtensorMap* m, int* status, uint8_t* wbuf, int& nbuf,
+                                               int lane, const uint32_t (&w)[16], int x, int y,
+                                               unsigned zero_col = ~0u) {
+  uint8_t* buf = wbuf + (nbuf & 1) * kBf16BoxBytes;
+  if (lane == 0) tma_store_wait_read<1>();
+  __syncwarp();
+  const int sw = (lane >> 1) & 3;
+  uint4* row = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) row[c ^ sw] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  if (zero_col < 32u)
+    *reinterpret_cast<uint16_t*>(buf + lane * 64 + ((int(zero_col >> 3) ^ sw) << 4) + (zero_col & 7u) * 2) = 0;
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    if (tma_x_ok<2>(x, status)) tma_store_2d(m, buf, x, y);
+    tma_store_commit();
+  }
+  ++nbuf;
+}
+
 // =============================================================== forward
 // CL = 1: 128-row tiles on one CTA; CL = 2: 256-row tiles over a CTA pair
 // (cta_group::2).  F8: e4m3 operands (forward-only scoring) with per-row
@@ -32,8 +58,11 @@ namespace rl {
 // elements and each MMA step covers K = 32.  KBX: 128-byte boxes per operand
 // in a pipeline stage (2 for pair tiles with one K segment: half as many,
 // twice as deep stages, which halves the per-stage barrier round trips the
-// MMA issuer waits on — measured 9% on the bf16 forward).
-template <int CL, bool F8 = false, int KBX = 1>
+// MMA issuer waits on — measured 9% on the bf16 forward).  ST: the tiles of
+// the first FwdParams::pu_tiles row-tile slots also write every logit's
+// unnormalised probability 2^t as bf16 (stored probabilities, for a backward
+// that needs no recompute; bf16 CTA pairs without bias).
+template <int CL, bool F8 = false, int KBX = 1, bool ST = false>
 struct FwdPolicy {
   static constexpr int kCluster = CL;
   static constexpr int PAIR = CL >= 2 ? 2 : 1;
@@ -46,7 +75,9 @@ struct FwdPolicy {
   static constexpr int kABytes = kBox * KBX;
   static constexpr int kBBytes = (256 / PAIR) * 128 * KBX;   // this CTA's share of the B rows
   static constexpr int kColBytes = 2 * 128 * 4;   // per epilogue warp: its 128 columns' W scales and biases
-  static constexpr int kExtraSmem = kEpiWarps * kColBytes;
+  // ST: two staging boxes per epilogue warp instead (no bias, no scales)
+  static constexpr int kExtraSmem = ST ? kEpiWarps * 2 * kBf16BoxBytes : kEpiWarps * kColBytes;
+  static_assert(!ST || (CL == 2 && !F8), "stored probabilities: bf16 CTA-pair forward");
   static constexpr uint32_t kIdesc = F8 ? idesc_e4m3(kRows, 256) : idesc_bf16(kRows, 256, 0, 0);
   static constexpr int kKB = (F8 ? 128 : 64) * KBX;   // K elements per k-block
   using Params = FwdParams;
@@ -60,6 +91,7 @@ struct FwdPolicy {
     float4 pw, pb;
     int pre_n0 = -1;       // tile whose columns pw / pb hold
     int R = -1, P = 0;     // launch shape (for the next tile's columns)
+    int nbuf = 0;          // ST: staging buffer alternation
   };
 
   // Row tiles and vocabulary segments of this launch: all R tiles with the
@@ -83,6 +115,7 @@ struct FwdPolicy {
   __device__ static void prefetch(const Params& p) {
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB);
+    if constexpr (ST) tma_prefetch_desc(&p.tmPu);
   }
 
   // Units u = seg * R + r (row tile r, vocabulary segment seg), dealt
@@ -103,6 +136,7 @@ struct FwdPolicy {
       const int j1 = int((long long)(seg + 1) * p.Vt / P);
       for (int j = j0; j < j1; ++j) {
         TileInfo t{r * kRows, j * 256, 0, kbs, u, seg, j == j0, j == j1 - 1, P};
+        t.slot = ri;
         if (!f(t)) return;
       }
     }
@@ -170,7 +204,11 @@ struct FwdPolicy {
                                   int lane, uint8_t* extra, uint32_t rank) {
     const int row = t.m0 + 128 * int(rank) + q * 32 + lane;
     float* cols = reinterpret_cast<float*>(extra + (q + 4 * half) * kColBytes);   // [128 scales][128 biases]
-    if (F8 || p.bias2) {
+    // ST: this warp's staging boxes; the tile's rows go to rows slot * 256 + .. of the buffer
+    uint8_t* wbuf = extra + (q + 4 * half) * 2 * kBf16BoxBytes;
+    const bool st_tile = ST && t.slot < p.pu_tiles;
+    const int pu_y0 = t.slot * kRows + 128 * int(rank) + q * 32;
+    if (!ST && (F8 || p.bias2)) {
       if (e.pre_n0 != t.n0) fetch_cols(p, e, t.n0, half, lane);
       __syncwarp();
       if constexpr (F8) reinterpret_cast<float4*>(cols)[lane] = e.pw;
@@ -219,7 +257,7 @@ struct FwdPolicy {
           v[4 * i + 2] = fmaf(v[4 * i + 2] * e.xs, w.z, b.z);
           v[4 * i + 3] = fmaf(v[4 * i + 3] * e.xs, w.w, b.w);
         }
-      } else if (p.bias2) {
+      } else if (!ST && p.bias2) {
         const float4* b4 = reinterpret_cast<const float4*>(cols + 128 + ch * 32);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -232,7 +270,7 @@ struct FwdPolicy {
       }
       // Without bias or e4m3 scales v is still the raw logit; its scale to
       // log2 units folds into the FFMA that forms t - m below (mul = sc).
-      const float mul = (F8 || p.bias2) ? 1.f : sc;
+      const float mul = (F8 || (!ST && p.bias2)) ? 1.f : sc;
       const bool tail = c0 + 32 > p.V;   // columns past V: out of the max, weight 0
       if (tail) {
 #pragma unroll
@@ -260,6 +298,16 @@ struct FwdPolicy {
           e.mref = nref;
         }
       }
+      // ST: 2^t = 2^(t - m) 2^m exactly (m an integer); m is capped at 100, past
+      // which the backward recomputes the row anyway, and 2^m below 2^-126
+      // is taken as 0 (such a column's p is below 2^-46 in any row the
+      // stored path keeps)
+      float psc = 0.f;
+      if constexpr (ST) {
+        const float mr = fminf(e.mref, 100.f);
+        psc = mr >= -126.f ? __int_as_float((int(mr) + 127) << 23) : 0.f;
+      }
+      uint32_t pk[ST ? 16 : 1];
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
@@ -272,6 +320,10 @@ struct FwdPolicy {
         const float x0 = ex2_approx(d0), x1 = ex2_approx(d1), x2 = ex2_approx(d2), x3 = ex2_approx(d3);
         s0 += x0; s1 += x1; s2 += x2; s3 += x3;
         w0 = fmaf(x0, d0, w0); w1 = fmaf(x1, d1, w1); w2 = fmaf(x2, d2, w2); w3 = fmaf(x3, d3, w3);
+        if constexpr (ST) {
+          pk[i / 2] = pack_bf16x2(x0 * psc, x1 * psc);
+          pk[i / 2 + 1] = pack_bf16x2(x2 * psc, x3 * psc);
+        }
       }
       two_sum_acc(e.s_hi, e.s_lo, (s0 + s1) + (s2 + s3));
       two_sum_acc(e.w_hi, e.w_lo, (w0 + w1) + (w2 + w3));
@@ -282,6 +334,10 @@ struct FwdPolicy {
           if (unsigned(i) == ty) e.zy = v[i] * mul;
         e.found = 1;
       }
+      if constexpr (ST) {
+        // warp-uniform; the target entry is written as 0 (the backward sets it)
+        if (st_tile) store_bf16_box(&p.tmPu, p.status, wbuf, e.nbuf, lane, pk, c0, pu_y0, ty);
+      }
       if (ch + 1 < nch) tmem_ld32_wait(r);
     }
     if (t.last && row < p.N && RL_DCHECK(t.seg < t.aux && t.aux <= p.pcap, p.status)) {
@@ -290,7 +346,12 @@ struct FwdPolicy {
       dst[1] = make_float4(e.w_lo, e.zy, e.found ? 1.f : 0.f, 0.f);
     }
   }
-  __device__ static void epilogue_finish(const Params&, int) {}
+  __device__ static void epilogue_finish(const Params&, int lane) {
+    if constexpr (ST) {
+      if (lane == 0) tma_store_wait_all<0>();
+      __syncwarp();
+    }
+  }
 };
 
 // kMergeLanes lanes per row: see merge_row.cuh.
@@ -355,7 +416,7 @@ struct DlPolicy {
   static constexpr int kBox = 128 * 128;                    // one 128-row x 128-byte operand box
   static constexpr int kABytes = kBox * KBX;
   static constexpr int kBBytes = (256 / PAIR) * 128 * KBX;
-  static constexpr int kStageBuf = 32 * 64;        // one 32-row x 32-column bf16 box, 64-byte swizzle
+  static constexpr int kStageBuf = kBf16BoxBytes;  // one 32-row x 32-column bf16 box, 64-byte swizzle
   static constexpr int kExtraSmem = kEpiWarps * 2 * kStageBuf;
   static constexpr uint32_t kIdesc = idesc_bf16(kRows, 256, 0, 0);
   using Params = DlParams;
@@ -422,20 +483,7 @@ struct DlPolicy {
   // with a TMA store; two staging buffers per warp alternate.
   __device__ static void store_box(const Params& p, EpiState& e, uint8_t* wbuf, int lane, const uint32_t (&w)[16],
                                    int x, int y) {
-    uint8_t* buf = wbuf + (e.nbuf & 1) * kStageBuf;
-    if (lane == 0) tma_store_wait_read<1>();
-    __syncwarp();
-    const int sw = (lane >> 1) & 3;
-    uint4* row = reinterpret_cast<uint4*>(buf + lane * 64);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) row[c ^ sw] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-    fence_proxy_async();
-    __syncwarp();
-    if (lane == 0) {
-      if (tma_x_ok<2>(x, p.status)) tma_store_2d(&p.tmG, buf, x, y);
-      tma_store_commit();
-    }
-    ++e.nbuf;
+    store_bf16_box(&p.tmG, p.status, wbuf, e.nbuf, lane, w, x, y);
   }
 
   __device__ static void epilogue(const Params& p, EpiState& e, const TileInfo& t, uint32_t taddr, int q, int half,
@@ -706,6 +754,7 @@ struct HPolicy {
       const int drow = (y < nc && !no_k) ? p.dx_idx[p.n0 + y] : -1;
       float* dst = (drow >= 0 && RL_DCHECK(drow < p.dx_nrows, p.status)) ? p.dx_out + size_t(drow) * p.dx_ld
                                                                           : nullptr;
+      const float ks = (p.dx_scale && dst) ? p.dx_scale[p.n0 + y] : 1.f;
 #pragma unroll 1
       for (int c = c_begin; c < c_end; ++c) {
         const int x0 = t.n0 + sub * kNS + c * 32;
@@ -713,6 +762,10 @@ struct HPolicy {
         float v[32];
         tmem_ld32(taddr + uint32_t(c * 32), v);   // warp-collective: every lane loads
         if (!dst) continue;
+        if (p.dx_scale) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= ks;
+        }
         if (wrow) add_target_row(v, wrow, ferr, x0, pr.Hout);
         if (p.dx_vec && x0 + 32 <= pr.Hout) {
 #pragma unroll
@@ -900,6 +953,10 @@ int gemmH_resident_clusters() {
 }
 cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, int kbx, cudaStream_t st) {
   if (p.xs) return launch_engine<FwdPolicy<2, true, 2>>(p, units, st);   // e4m3 operands: CTA pairs only
+  if (p.pu_tiles > 0) {
+    if (cluster != 2 || kbx != 2 || p.bias2 || p.nseg != 1) return cudaErrorInvalidValue;
+    return launch_engine<FwdPolicy<2, false, 2, true>>(p, units, st);
+  }
   if (cluster == 1) return launch_engine<FwdPolicy<1>>(p, units, st);
   return kbx == 2 ? launch_engine<FwdPolicy<2, false, 2>>(p, units, st) : launch_engine<FwdPolicy<2>>(p, units, st);
 }

@@ -47,6 +47,14 @@ struct FwdParams {
   const int64_t* targets;
   long long v_begin;          // vocabulary id of column 0 (a shard of a larger vocabulary), else 0
   float4* partial;            // [N][2P][2]
+  // Optional stored probabilities (pu_tiles > 0, bf16 CTA-pair forward only):
+  // for the row tiles in the first pu_tiles slots of the launch's tile order
+  // (slot i = the i-th listed tile, or tile i without a list), every
+  // computed logit's unnormalised probability 2^t (t = logit log2(e) / tau,
+  // so p = 2^(t - lse2)) is written as bf16 to row (slot * 256 + row in
+  // tile) of the buffer tmPu maps; the target column is written as 0.
+  CUtensorMap tmPu;           // inner V columns, outer pu_tiles * 256 rows; box 32 x 32, 64-byte swizzle
+  int pu_tiles;
   int* status;
   unsigned long long limit_ns;
 };
@@ -136,6 +144,9 @@ struct HParams {
   // as err * W[target - w_begin] on the first k part, so the dominant
   // c (onehot - p) W term of each dX row carries no bf16 rounding.
   const float* dx_err;
+  // Optional (problem 0 with dx_idx): each row's accumulator is first scaled
+  // by dx_scale[n0 + row] (the stored-probability backward's -c 2^-lse2 / tau).
+  const float* dx_scale;
   const int64_t* dx_tgt;
   const __nv_bfloat16* dx_w;  // bf16 W [dx_wrows, dx_wld]
   long long dx_wbegin;
@@ -217,7 +228,41 @@ struct CompactParams {
   float* dx_zero;             // optional: [N, H] gradient buffer the gather sets to zero
   int H;
   int dx_vec;                 // dx_zero is 16-byte aligned and H % 4 == 0
+  const uint8_t* done;        // optional: [N] rows already handled (1): not kept here
 };
+
+// Backward rows of the stored-probability path: buffer row j holds row n of
+// the forward's slot j / 256 (see FwdParams::tmPu).  For a row with c != 0
+// whose lse2 lies in [kStoredLse2Min, kStoredLse2Max]:
+//   k2 = -(c/tau) 2^-lse2 (so G = k2 pu off the target, as pu = 2^t),
+//   k1 = (c/tau)(1 - p_y), the target entry of G,
+//   the target entry of pu is set to bf16(k1 / k2) and err = k1 - k2 bf16(k1 / k2),
+//   xs[j] = bf16(k2 X[n]), idx[j] = n, done[n] = 1.
+// Other rows get xs = 0, idx = -1, k2 = err = 0 (they go to the recompute).
+constexpr float kStoredLse2Min = -80.f;
+constexpr float kStoredLse2Max = 96.f;
+struct StoredParams {
+  int N, H, V, rows_cap;      // rows_cap = stored tiles * 256 (host upper bound)
+  int R;                      // row tiles of the forward without a tile list
+  const int* tiles;           // the forward's tile list, or null (slot = tile)
+  const int* ntiles;
+  int pu_tiles;
+  const float* coef;          // [N] c / tau
+  const float* lse2;          // [N]
+  const double* logp64;       // [N]
+  const int64_t* targets;     // [N]
+  const __nv_bfloat16* x;     // [N, H]
+  __nv_bfloat16* pu;          // [rows_cap, pu_ld]
+  int pu_ld;
+  __nv_bfloat16* xs;          // [rows_cap, H]
+  int* idx;                   // [rows_cap]
+  float* k2;                  // [rows_cap]
+  float* err;                 // [rows_cap]
+  int64_t* tgt;               // [rows_cap]
+  uint8_t* done;              // [N], zeroed before the launch
+  int* rows_total;            // out: stored rows (stored tiles * 256)
+};
+cudaError_t launch_stored_rows(const StoredParams& p, cudaStream_t st);
 int compact_groups(int N);   // 32-row groups
 // Row tiles of tile_rows rows holding a row with mask != 0: flags[R], their
 // ascending list and count (ticket zeroed before the launch).

@@ -53,16 +53,28 @@ __global__ void k3_hist_kernel(const float* __restrict__ H, const uint8_t* __res
     p0 = st->prefix[0];
     p1 = st->prefix[1];
   }
-  for (long long n = blockIdx.x * (long long)blockDim.x + threadIdx.x; n < N; n += (long long)gridDim.x * blockDim.x) {
-    if (!m[n]) continue;
-    const uint32_t key = f2key(H[n]);
-    const uint32_t d = (key >> shift) & 255u;
-    if (pass == 0) {
-      atomicAdd(&sh[d], 1u);
-    } else {
-      const uint32_t hp = key >> (shift + 8);
-      if (hp == p0) atomicAdd(&sh[d], 1u);
-      if (hp == p1) atomicAdd(&sh[256 + d], 1u);
+  // Warp-aggregated counts: the lanes of a warp that fall in the same bin add
+  // once (entropies cluster, so early passes put most tokens in a few bins).
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long n = blockIdx.x * (long long)blockDim.x + threadIdx.x; n - lane < N; n += stride) {
+    int b0 = -1, b1 = -1;
+    if (n < N && m[n]) {
+      const uint32_t key = f2key(H[n]);
+      const int d = int((key >> shift) & 255u);
+      if (pass == 0) {
+        b0 = d;
+      } else {
+        const uint32_t hp = key >> (shift + 8);
+        if (hp == p0) b0 = d;
+        if (hp == p1) b1 = 256 + d;
+      }
+    }
+    const unsigned g0 = __match_any_sync(0xffffffffu, b0);
+    if (b0 >= 0 && lane == __ffs(g0) - 1) atomicAdd(&sh[b0], unsigned(__popc(g0)));
+    if (pass > 0) {
+      const unsigned g1 = __match_any_sync(0xffffffffu, b1);
+      if (b1 >= 0 && lane == __ffs(g1) - 1) atomicAdd(&sh[b1], unsigned(__popc(g1)));
     }
   }
   __syncthreads();

@@ -28,6 +28,7 @@ FLAG_SINGLE_CTA_TILES = 0x2
 FLAG_ADV_PER_TOKEN = 0x4
 FLAG_ALL_ROWS = 0x8
 FLAG_ACCUMULATE = 0x10
+FLAG_RECOMPUTE = 0x20
 NMETRICS = 8
 STATE_FLOATS = 8        # floats per token of a vocabulary shard's row state
 MAX_SHARDS = 4096
@@ -104,6 +105,8 @@ def _load():
     lib.rlloss_get_device_status.restype = c_int
     lib.rlloss_get_backward_rows.argtypes = [P, ctypes.POINTER(c_int32)]
     lib.rlloss_get_backward_rows.restype = c_int
+    lib.rlloss_get_stored_rows.argtypes = [P, ctypes.POINTER(c_int32)]
+    lib.rlloss_get_stored_rows.restype = c_int
     lib.rlloss_get_forward_tiles.argtypes = [P, ctypes.POINTER(c_int32)]
     lib.rlloss_get_forward_tiles.restype = c_int
     lib.rlloss_selftest_bounded_wait.argtypes = [P, c_uint64, P]
@@ -281,6 +284,14 @@ def rlloss_get_backward_rows(workspace) -> int:
     rc = lib.rlloss_get_backward_rows(_p(workspace), ctypes.byref(rows))
     if rc != OK:
         raise RllossError(rc, "rlloss_get_backward_rows")
+    return int(rows.value)
+
+
+def rlloss_get_stored_rows(workspace) -> int:
+    rows = c_int32(0)
+    rc = lib.rlloss_get_stored_rows(_p(workspace), ctypes.byref(rows))
+    if rc != OK:
+        raise RllossError(rc, "rlloss_get_stored_rows")
     return int(rows.value)
 
 

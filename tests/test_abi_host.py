@@ -43,9 +43,18 @@ def test_workspace_bytes_positive_and_zero_for_invalid():
 
 
 def test_workspace_grows_with_fp32_split_and_bias():
-    a = R.rlloss_workspace_bytes(_cfg())
+    # against the recompute backward, which the fp32 and bias forms use too
+    a = R.rlloss_workspace_bytes(_cfg(flags=R.FLAG_RECOMPUTE))
     assert R.rlloss_workspace_bytes(_cfg(dtype=R.FP32)) > a
     assert R.rlloss_workspace_bytes(_cfg(has_bias=True)) > a
+
+
+def test_stored_probabilities_need_at_most_one_tile_more_and_a_flag_byte_per_row():
+    # the chunk buffer holds whole 256-row tiles when the forward stores into it
+    for T in (16, 2048):
+        st = R.rlloss_workspace_bytes(_cfg(T=T))
+        rc = R.rlloss_workspace_bytes(_cfg(T=T, flags=R.FLAG_RECOMPUTE))
+        assert rc <= st <= rc + 256 * 576 * 2 + 2 * T + 512
 
 
 class _Null:
@@ -83,9 +92,11 @@ def test_invalid_requests_rejected_synchronously(kw, code):
 
 
 def test_accumulate_flag_is_accepted_and_needs_no_extra_workspace():
-    assert R.rlloss_workspace_bytes(_cfg(flags=R.FLAG_ACCUMULATE)) == R.rlloss_workspace_bytes(_cfg())
+    # accumulation runs the recompute backward
+    assert R.rlloss_workspace_bytes(_cfg(flags=R.FLAG_ACCUMULATE)) == \
+        R.rlloss_workspace_bytes(_cfg(flags=R.FLAG_RECOMPUTE))
     assert R.rlloss_workspace_bytes(_cfg(flags=R.FLAG_ACCUMULATE | R.FLAG_ALL_ROWS)) > 0
-    assert R.rlloss_workspace_bytes(_cfg(flags=0x20)) == 0
+    assert R.rlloss_workspace_bytes(_cfg(flags=0x40)) == 0
 
 
 def test_vocab_shard_entries_validate_before_any_launch():

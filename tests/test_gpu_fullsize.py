@@ -58,7 +58,8 @@ def test_full_size_workload(R, idx):
     stats2 = check_grads(step, case, res2, dx_rows=rows, dw_rows=vs)
     print(f"  training-step call: loss {step['loss'].item():.9g}; forward tiles "
           f"{R.rlloss_get_forward_tiles(step['workspace'])}, backward rows "
-          f"{R.rlloss_get_backward_rows(step['workspace'])}; grads {stats2}")
+          f"{R.rlloss_get_backward_rows(step['workspace'])}, stored rows "
+          f"{R.rlloss_get_stored_rows(step['workspace'])}; grads {stats2}")
 
 
 def test_one_sequence_workload_every_gradient_row(R):

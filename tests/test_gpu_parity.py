@@ -110,10 +110,13 @@ def test_entropy_mask_non_vacuous_and_forced_path_bit_identical(R):
 
 @pytest.mark.parametrize("spec", [MID[1], MID[4], MID[5]], ids=["bf16_bias_k3kl", "fp32_bias_odd", "wide"])
 def test_tile_shapes_agree(R, spec):
-    """256-row CTA-pair tiles (default) and 128-row single-CTA tiles give the
-    same results."""
+    """256-row CTA-pair tiles and 128-row single-CTA tiles give the same
+    results (both with the recomputing backward, which single-CTA tiles use;
+    the default call, which may take the stored-probability backward, passes
+    the oracle as well)."""
     case = Case(spec)
-    a, _, _ = _full_check(R, case)
+    _full_check(R, case)
+    a, _, _ = _full_check(R, case, flags=R.FLAG_RECOMPUTE)
     b, _, _ = _full_check(R, case, flags=R.FLAG_SINGLE_CTA_TILES)
     for k in ("loss", "logp", "entropy"):
         assert torch.allclose(a[k], b[k], rtol=1e-6, atol=1e-7), k
@@ -299,7 +302,8 @@ def test_compacted_backward_matches_dense(R, spec):
     backward over every row gives the same gradients up to fp32 summation
     order, the same forward and loss bits, and both pass the oracle."""
     case = Case(spec)
-    a, res, _ = _full_check(R, case)
+    _full_check(R, case)   # default call (stored probabilities where they apply)
+    a, res, _ = _full_check(R, case, flags=R.FLAG_RECOMPUTE)
     b, _, _ = _full_check(R, case, flags=R.FLAG_ALL_ROWS)
     keep = res.c != 0
     assert 0 < keep.sum() < spec.N, "the workload must both keep and drop rows"
@@ -355,7 +359,8 @@ def test_compaction_with_empty_later_chunks(R):
     the later chunks have none.  Matches the dense backward and the oracle."""
     spec = Workload("mostly_prompt", B=2, T=640, H=128, V=900, dtype="bf16", prompt_len=560, seed=109)
     case = Case(spec)
-    a, res, _ = _full_check(R, case, chunk_rows=256)
+    _full_check(R, case, chunk_rows=256)   # default call (stored probabilities where they apply)
+    a, res, _ = _full_check(R, case, chunk_rows=256, flags=R.FLAG_RECOMPUTE)
     assert 0 < (res.c != 0).sum() <= 160
     b, _, _ = _full_check(R, case, chunk_rows=256, flags=R.FLAG_ALL_ROWS)
     _grads_close(a, b)
@@ -384,7 +389,9 @@ def test_accumulate_adds_gradients(R, spec, all_rows, chunk):
     otherwise.  Rows without gradient keep their initial bits, and the same
     initial values give the same bits on every call."""
     case = Case(spec)
-    base, res, _ = _full_check(R, case, chunk_rows=chunk, flags=R.FLAG_ALL_ROWS if all_rows else 0)
+    # the overwriting call runs the same (recomputing) backward as ACCUMULATE
+    base, res, _ = _full_check(R, case, chunk_rows=chunk,
+                               flags=R.FLAG_ALL_ROWS if all_rows else R.FLAG_RECOMPUTE)
     g = torch.Generator().manual_seed(7)
     init = {k: torch.randn(base[k].shape, generator=g).cuda() for k in ("dX", "dW", "db") if base.get(k) is not None}
     flags = R.FLAG_ACCUMULATE | (R.FLAG_ALL_ROWS if all_rows else 0)
