@@ -174,7 +174,18 @@ size_t rlloss_loss_workspace_bytes(const rlloss_cfg* cfg);
  *   optional (NULL = not written).
  *   workspace: device buffer of at least rlloss_workspace_bytes(cfg) bytes,
  *   256-byte aligned; it also holds the device status word.
- * Pointers must be 16-byte aligned.  Returns RLLOSS_* codes as above. */
+ * Pointers must be 16-byte aligned.  Returns RLLOSS_* codes as above.
+ * The backward needs G = (c/tau)(onehot(y) - softmax) for every row with
+ * c_n != 0 ("Add GMPO ...", Details: the input, weight and bias gradients).
+ * With bf16 operands and without ACCUMULATE it takes the softmax from the
+ * forward, which stores each logit's unnormalised probability 2^t (bf16) in a
+ * buffer of the workspace (cfg.chunk_rows rows, by default one or two waves of
+ * row tiles), for the row tiles that fit; other rows have their logits
+ * recomputed.  Without an entropy mask, with per-sequence advantages and T a
+ * multiple of 256, a batch larger than that buffer runs in groups of whole
+ * sequences that fit it (sequences are coupled only through B and sums), so
+ * every row's probabilities are stored; the results equal the one-pass call
+ * up to fp32 summation order.  RLLOSS_FLAG_RECOMPUTE recomputes every row. */
 int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const void* b,
                    const int64_t* targets, const float* old_logp, const float* ref_logp,
                    const float* adv, const uint8_t* mask, float* out_loss, float* out_metrics,
@@ -235,9 +246,9 @@ int rlloss_loss_from_logp(const rlloss_cfg* cfg, const float* logp, const float*
  *   rlloss_loss_workspace_bytes(cfg) <= RLLOSS_NOALLOC_SCRATCH_BYTES; callers
  *   should size problems with that comparison.  The loss workspace is about
  *   N + B*(84 + 40*S) + 9.5 KB bytes, each region rounded up to 256 bytes,
- *   with N = B*T and S = min(ceil(4*SMs/B), ceil(T/256)) slices per sequence
+ *   with N = B*T and S = min(ceil(16*SMs/B), ceil(T/256)) slices per sequence
  *   (at least 1; SMs of the current device): on a 152-SM GPU, N up to about
- *   4.1e6 tokens when B is small (at most ~25 KB of per-sequence sums), while
+ *   4.08e6 tokens when B is small (at most ~100 KB of per-sequence sums), while
  *   many short sequences fill it sooner (B = 34000 with T = 1 does not fit,
  *   each sequence taking at least 124 + T bytes).  A larger problem is
  *   rejected with RLLOSS_ETOOLARGE before any launch; a configuration the

@@ -26,6 +26,7 @@ constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
 constexpr size_t kBackwardRowsOffset = 12;
 constexpr size_t kTileTicketOffset = 16, kFwdTilesOffset = 20, kFwdSegmentsOffset = 24;
 constexpr size_t kStoredRowsOffset = 28;   // rows the stored-probability backward ran over
+constexpr size_t kStoredValidOffset = 32;  // of those, rows with a nonzero coefficient
 constexpr size_t kPartialCapBytes = size_t(64) << 20;
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
@@ -137,7 +138,10 @@ struct Plan {
   // rows needs no recompute (bf16 CTA pairs, no bias, no ACCUMULATE).
   bool stored;
   int pu_tiles;
+  int xs_ld;                // row stride (elements) of the stored path's scaled X rows
   size_t o_done;
+  int seq_group, ngroups;   // sequences per group of a grouped call (0: one pass), groups
+  size_t o_sums;            // grouped call: [ngroups][8] batch sums, then 4 int row counters
 };
 
 // Largest vocabulary-segment count whose partial states fit the cap (<= 64).
@@ -164,18 +168,7 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
   p.sms = device_sms();
   p.ent = entropy_path(c);
   p.fused_loss = mode == kFull && !p.ent;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    const size_t o = off;
-    off = align256(off + bytes);
-    return o;
-  };
-  p.o_status = take(256);
-  if (loss) {
-    p.o_tickets = take(size_t(p.B) * 4);
-    p.slices = p.fused_loss ? fused_loss_slices(p.T) : loss_slices(p.B, p.T, p.sms);
-    p.o_part = take(size_t(p.B) * p.slices * 5 * 8);
-  }
+  // ---- LM-head parameters
   if (head) {
     p.H = c->H;
     p.V = c->V;
@@ -187,8 +180,6 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.R = int(cdiv(p.N, p.rows_tile));
     p.Vt = int(cdiv(p.V, 256));
     p.fwd_clusters = resident_or(fwd_resident_clusters(p.pair), p.sms / p.pair);
-    p.pcap = segment_cap(p.N);
-    p.P = choose_segments(p.R, p.Vt, p.fwd_clusters, p.pcap);
     p.Hp = int(rup(p.H, 64));
     p.Vp = int(rup(p.V, 64));
     // Stages hold two 128-byte boxes per operand with CTA pairs and one K
@@ -209,28 +200,8 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
       p.Kx = p.H;
     }
     p.kb_dl = p.fp32 ? p.Hp / 64 : int(cdiv(p.H, 64 * p.kbx));
-    if (fwd) {
-      p.o_partial = take(size_t(p.N) * 2 * p.pcap * 32);   // room for a segment count chosen on the device
-      p.o_logp64 = take(size_t(p.N) * 8);
-      p.o_ent = take(size_t(p.N) * 4);
-    }
-    p.o_lse2 = take(size_t(p.N) * 4);
-    p.o_bias2 = take(p.bias ? size_t(p.Vt) * 256 * 4 : 0);
-    p.o_ws2 = take(p.f8 ? size_t(p.Vt) * 256 * 4 : 0);
-    p.o_x3 = take(p.fp32 ? size_t(p.N) * 3 * p.Hp * 2 : 0);
-    p.o_w3 = take(p.fp32 ? size_t(p.V) * 3 * p.Hp * 2 : 0);
   }
-  if (mode == kShardLoss) {
-    p.V = c->V;
-    p.o_lse2 = take(size_t(p.N) * 4);
-    p.o_logp64 = take(size_t(p.N) * 8);
-    p.o_ent = take(size_t(p.N) * 4);
-  }
-  if (loss) {
-    p.o_emask = take(size_t(p.N));
-    p.o_k3 = take(kK3Bytes);
-    p.o_seq = take(size_t(p.B) * 10 * 8);   // sequence records, 10 doubles each
-  }
+  // ---- backward parameters: chunk buffer, stored probabilities, sequence groups
   if (bwd) {
     p.h_pairs = resident_or(gemmH_resident_clusters(), p.sms / 2);
     // Default chunk: a whole number of dX units per pair of SMs (one or two
@@ -243,26 +214,89 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.nchunks = int(cdiv(p.N, p.Nc));
     p.ld_dl = p.fp32 ? 2 * p.Vp : p.Vp;
     p.compact = !(c->flags & RLLOSS_FLAG_ALL_ROWS);
-    p.stored = mode == kFull && !p.fp32 && !p.f8 && !p.bias && p.pair == 2 && p.kbx == 2 && p.compact &&
+    p.stored = mode == kFull && !p.fp32 && !p.f8 && p.pair == 2 && p.kbx == 2 && p.compact &&
                !(c->flags & (RLLOSS_FLAG_ACCUMULATE | RLLOSS_FLAG_RECOMPUTE));
+    // scaled X rows of the stored path: H columns, plus k2 in column H (and
+    // zeros to a 16-byte multiple) with a bias, so dW's GEMM also forms db
+    p.xs_ld = p.stored && p.bias ? p.H + 8 : p.Kx;
     p.pu_tiles = p.stored ? int(cdiv(p.Nc, 256)) : 0;
-    p.o_coef = take(size_t(p.N) * 4);
+    // Whole sequences per group when the batch runs in groups that each fit the
+    // stored-probability buffer (no batch-global entropy threshold couples them;
+    // whole 256-row tiles per sequence); 0: one pass over the batch.
+    p.seq_group = 0;
+    if (p.stored && !p.ent && c->T % 256 == 0 && !(c->flags & RLLOSS_FLAG_ADV_PER_TOKEN)) {
+      const int s = p.pu_tiles * 256 / c->T;
+      if (s >= 1 && s < c->B) p.seq_group = s;
+    }
+    p.ngroups = p.seq_group ? int(cdiv(c->B, p.seq_group)) : 1;
+    if (p.seq_group) {   // the buffer holds exactly one group (and a recompute chunk never needs more)
+      p.Nc = p.seq_group * c->T;
+      p.pu_tiles = p.Nc / 256;
+      p.nchunks = int(cdiv(p.N, p.Nc));
+    }
+  }
+  // ---- regions.  Per-row regions hold one group's rows when the call runs in
+  // groups (the groups reuse them in turn), else the whole batch's.
+  const long long Nr = p.seq_group ? (long long)p.seq_group * p.T : p.N;
+  const int Rr = head ? int(cdiv(Nr, p.rows_tile)) : 0;
+  if (head) {
+    p.pcap = segment_cap(Nr);
+    p.P = choose_segments(p.R, p.Vt, p.fwd_clusters, p.pcap);
+  }
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  p.o_status = take(256);
+  if (loss) {
+    p.o_tickets = take(size_t(p.B) * 4);
+    p.slices = p.fused_loss ? fused_loss_slices(p.T) : loss_slices(p.B, p.T, p.sms);
+    p.o_part = take(size_t(p.B) * p.slices * 5 * 8);
+  }
+  if (head) {
+    if (fwd) {
+      p.o_partial = take(size_t(Nr) * 2 * p.pcap * 32);   // room for a segment count chosen on the device
+      p.o_logp64 = take(size_t(Nr) * 8);
+      p.o_ent = take(size_t(Nr) * 4);
+    }
+    p.o_lse2 = take(size_t(Nr) * 4);
+    p.o_bias2 = take(p.bias ? size_t(p.Vt) * 256 * 4 : 0);
+    p.o_ws2 = take(p.f8 ? size_t(p.Vt) * 256 * 4 : 0);
+    p.o_x3 = take(p.fp32 ? size_t(p.N) * 3 * p.Hp * 2 : 0);
+    p.o_w3 = take(p.fp32 ? size_t(p.V) * 3 * p.Hp * 2 : 0);
+  }
+  if (mode == kShardLoss) {
+    p.V = c->V;
+    p.o_lse2 = take(size_t(p.N) * 4);
+    p.o_logp64 = take(size_t(p.N) * 8);
+    p.o_ent = take(size_t(p.N) * 4);
+  }
+  if (loss) {
+    p.o_emask = take(size_t(Nr));
+    p.o_k3 = take(kK3Bytes);
+    p.o_seq = take(size_t(p.B) * 10 * 8);   // sequence records, 10 doubles each
+  }
+  if (bwd) {
+    p.o_coef = take(size_t(Nr) * 4);
     p.o_dl = take(size_t(std::max(p.Nc, p.pu_tiles * 256)) * p.ld_dl * 2);
     p.o_dbpart = take(p.bias ? size_t(db_part_rows(p.Nc)) * p.V * 4 : 0);
-    p.o_done = take(p.stored ? size_t(p.N) : 0);
+    p.o_done = take(p.stored ? size_t(Nr) : 0);
+    p.o_sums = take(p.seq_group ? size_t(p.ngroups) * 8 * 8 + 64 : 0);
     // bf16 G: each backward row's target-entry rounding error (rows or
     // compacted rows, N rounded up to whole 256-row tiles)
-    p.o_err = take(p.fp32 ? 0 : size_t(rup(p.N, 256)) * 4);
-    p.o_tflags = take(size_t(p.R));
-    p.o_tlist = take(size_t(p.R) * 4);
+    p.o_err = take(p.fp32 ? 0 : size_t(rup(Nr, 256)) * 4);
+    p.o_tflags = take(size_t(Rr));
+    p.o_tlist = take(size_t(Rr) * 4);
     if (p.compact) {
-      p.Ncap = int(rup(p.N, 256));
-      p.o_blk = take(size_t(compact_groups(p.N)) * 2 * 4);
+      p.Ncap = int(rup(Nr, 256));
+      p.o_blk = take(size_t(compact_groups(int(Nr))) * 2 * 4);
       p.o_cidx = take(size_t(p.Ncap) * 4);
       p.o_coefc = take(size_t(p.Ncap) * 4);
       p.o_lse2c = take(size_t(p.Ncap) * 4);
       p.o_tgtc = take(size_t(p.Ncap) * 8);
-      p.o_xc = take(size_t(p.Ncap) * p.Kx * 2);
+      p.o_xc = take(size_t(p.Ncap) * std::max(p.Kx, p.xs_ld) * 2);
       p.o_dxc = take(size_t(p.Nc) * p.H * 4);
     }
   }
@@ -425,6 +459,7 @@ LossParams loss_params(const rlloss_cfg* c, const Plan& p, char* ws) {
   lp.part = reinterpret_cast<double*>(ws + p.o_part);
   lp.seq_ticket = reinterpret_cast<unsigned int*>(ws + p.o_tickets);
   lp.slices = p.slices;
+  lp.coef_slices = coef_slices(c->B, c->T, p.sms > 0 ? p.sms : 1);
   lp.ticket = reinterpret_cast<unsigned int*>(ws + p.o_status + 4);
   lp.status = reinterpret_cast<int*>(ws + p.o_status);
   lp.k3 = p.ent ? reinterpret_cast<const double*>(ws + p.o_k3) : nullptr;
@@ -544,8 +579,8 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
   fp.targets = targets;
   fp.v_begin = v_begin;
   if (p.stored) {
-    if (!tmap_bf16_box(&fp.tmPu, ws + p.o_dl, p.V, (long long)p.pu_tiles * 256, p.ld_dl, 32, 32,
-                       CU_TENSOR_MAP_SWIZZLE_64B))
+    if (!tmap_bf16_box(&fp.tmPu, ws + p.o_dl, p.V, (long long)p.pu_tiles * 256, p.ld_dl, 64, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
       return RLLOSS_ECUDA;
     fp.pu_tiles = p.pu_tiles;
   }
@@ -599,8 +634,11 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
 // The backward from per-row lse (log2 units) and coefficients c_n (G = (c/tau)
 // (onehot(y) - p)): row compaction, then per chunk the G recompute and the
 // grouped dX / dW GEMMs, and db.  hd holds the prepared operands.
+// With add_dw set (a later group of sequences of a grouped call), dW and db
+// are added to instead of stored by the stored-probability launch.
 int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int64_t* targets, long long v_begin,
-                 const float* lse2, const float* coef, float* dX, float* dW, float* db, char* ws, cudaStream_t st) {
+                 const float* lse2, const float* coef, float* dX, float* dW, float* db, char* ws, cudaStream_t st,
+                 bool add_dw = false) {
   int* status = reinterpret_cast<int*>(ws + p.o_status);
   // ---- backward, one chunk of rows at a time:
   //      G = (c/tau)(onehot - p) as bf16, dX = G W, dW += G^T X, db += sum G.
@@ -656,16 +694,19 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     sp.pu = pu;
     sp.pu_ld = p.ld_dl;
     sp.xs = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
+    sp.xs_ld = p.xs_ld;
+    sp.xcol = p.bias ? p.H : -1;
     sp.idx = reinterpret_cast<int*>(ws + p.o_cidx);
     sp.k2 = reinterpret_cast<float*>(ws + p.o_coefc);
     sp.err = err;
     sp.tgt = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
     sp.done = done;
     sp.rows_total = srows;
+    sp.rows_valid = reinterpret_cast<int*>(ws + p.o_status + kStoredValidOffset);
     {
       Phase ph(st, 5);
       RL_TRY(cudaMemsetAsync(dX, 0, size_t(p.N) * p.H * 4, st));
-      RL_TRY(cudaMemsetAsync(done, 0, size_t(p.N), st));
+      RL_TRY(cudaMemsetAsync(done, 0, size_t(p.N), st));   // rows_valid: zeroed with the status block
       RL_TRY(launch_stored_rows(sp, st));
       ph.launched(1);
     }
@@ -675,7 +716,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     if (!tmap_bf16(&hp.tmB[0], hd.Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
     if (!tmap_f32_out(&hp.tmO[0], dX, p.H, p.N)) return RLLOSS_ECUDA;   // unused: rows go through dx_idx
     if (!tmap_bf16(&hp.tmA[1], pu, p.V, pu_rows, p.ld_dl, 64)) return RLLOSS_ECUDA;
-    if (!tmap_bf16(&hp.tmB[1], sp.xs, p.Kx, pu_rows, p.Kx, 64)) return RLLOSS_ECUDA;
+    if (!tmap_bf16(&hp.tmB[1], sp.xs, p.H + (p.bias ? 1 : 0), pu_rows, p.xs_ld, 64)) return RLLOSS_ECUDA;
     if (!tmap_f32_out(&hp.tmO[1], dW, p.H, p.V)) return RLLOSS_ECUDA;
     HProblem& px = hp.pr[0];
     px.kb_per_seg = int(cdiv(p.V, 64));
@@ -693,12 +734,19 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     pw.Hout = p.H;
     pw.order = 1;
     pw.a_mn = 1;
-    pw.reduce = 0;
+    pw.reduce = add_dw ? 1 : 0;
     pw.ksplit = 1;
+    if (p.bias) {   // db = sum over rows of k2 pu (+ the target entries): X~'s column H
+      pw.xcol = p.H;
+      pw.xrows = p.V;
+      pw.xcol_out = db;
+      pw.wide = (p.H % 448 == 0) ? 1 : 0;
+    }
     hp.nprob = 2;
     const int kx = px.kb_per_seg / px.ksplit, kw = pw.kb_per_seg;
     hp.d_tiles = std::max(1, (kx + kw / 2) / kw);
     hp.rows_total = srows;
+    hp.rows_valid = sp.rows_valid;   // all coefficients 0 (e.g. a clipped GSPO sequence): nothing to add
     hp.n0 = 0;
     hp.nc_max = pu_rows;
     hp.status = status;
@@ -791,7 +839,10 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     dp.coef = coef_b;
     dp.dl = dl;
     dp.ld = p.ld_dl;
-    if (!tmap_bf16_box(&dp.tmG, dl, p.fp32 ? 2ll * p.Vp : p.V, nc, p.ld_dl, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    // bf16 G leaves in 64 x 32 boxes (128-byte swizzle); fp32 mode's hi and lo
+    // terms in 32 x 32 boxes (64-byte swizzle)
+    if (!(p.fp32 ? tmap_bf16_box(&dp.tmG, dl, 2ll * p.Vp, nc, p.ld_dl, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)
+                 : tmap_bf16_box(&dp.tmG, dl, p.V, nc, p.ld_dl, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B)))
       return RLLOSS_ECUDA;
     dp.lo_off = lo_off;
     dp.dbp = p.bias ? reinterpret_cast<float*>(ws + p.o_dbpart) : nullptr;
@@ -880,7 +931,8 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     }
     if (p.bias) {
       Phase ph(st, 5);
-      RL_TRY(launch_db_reduce(reinterpret_cast<float*>(ws + p.o_dbpart), rows_total, n0, nc, p.V, db, ch > 0 || acc, st));
+      RL_TRY(launch_db_reduce(reinterpret_cast<float*>(ws + p.o_dbpart), rows_total, n0, nc, p.V, db,
+                              ch > 0 || acc || p.stored, st));
       ph.launched();
     }
   }
@@ -1189,6 +1241,69 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
   // or advantages are per token (tokens outside the mask then count).
   const bool skip_tiles = !(cfg->flags & (RLLOSS_FLAG_ALL_ROWS | RLLOSS_FLAG_ADV_PER_TOKEN)) && !out_logp &&
                           !out_entropy;
+  if (p.seq_group) {
+    // ---- groups of whole sequences that each fit the stored-probability buffer
+    // (no entropy mask: sequences are coupled only by B and by sums): per group
+    // the forward with stores, the loss stage's additive batch sums with the
+    // whole batch's B, and the stored backward (dW, db added after the first
+    // group); then loss and metrics from the groups' sums.
+    double* sums = reinterpret_cast<double*>(ws + p.o_sums);
+    int* counters = reinterpret_cast<int*>(ws + p.o_sums + size_t(p.ngroups) * 64);
+    int* ctr_dev[3] = {reinterpret_cast<int*>(ws + p.o_status + kFwdTilesOffset),
+                       reinterpret_cast<int*>(ws + p.o_status + kStoredRowsOffset),
+                       reinterpret_cast<int*>(ws + p.o_status + kBackwardRowsOffset)};
+    RL_TRY(cudaMemsetAsync(counters, 0, 16, st));
+    const size_t xrow = size_t(cfg->H) * 2;   // bf16 row bytes
+    for (int g = 0; g < p.ngroups; ++g) {
+      const int i0 = g * p.seq_group, i1 = std::min(cfg->B, i0 + p.seq_group);
+      const long long r0 = (long long)i0 * cfg->T;
+      rlloss_cfg cg = *cfg;
+      cg.B = i1 - i0;
+      Plan pg = p;   // the whole batch's regions, used from their start
+      pg.B = cg.B;
+      pg.N = cg.B * cg.T;
+      pg.R = int(cdiv(pg.N, pg.rows_tile));
+      pg.P = choose_segments(pg.R, pg.Vt, pg.fwd_clusters, pg.pcap);
+      pg.nchunks = int(cdiv(pg.N, pg.Nc));
+      pg.Ncap = int(rup(pg.N, 256));
+      // tickets and per-group counters (the status word keeps its bits)
+      RL_TRY(cudaMemsetAsync(ws + p.o_status + 4, 0, p.o_tickets + size_t(pg.B) * 4 - p.o_status - 4, st));
+      Head hg;
+      RL_TRY_RC(run_head(&cg, pg, static_cast<const char*>(X) + size_t(r0) * xrow, W, b, targets + r0,
+                         out_logp ? out_logp + r0 : nullptr, out_entropy ? out_entropy + r0 : nullptr, nullptr, ws,
+                         st, hg, false, skip_tiles ? mask + r0 : nullptr));
+      LossParams lg = loss_params(&cg, pg, ws);
+      lg.Bg = double(cfg->B);
+      lg.logp = hg.mp.logp64;
+      lg.logp_is_f64 = 1;
+      lg.old_logp = old_logp + r0;
+      lg.ref_logp = ref_logp ? ref_logp + r0 : nullptr;
+      lg.adv = adv + i0;
+      lg.mask = mask + r0;
+      lg.coef = reinterpret_cast<float*>(ws + p.o_coef);
+      lg.out_sums = sums + size_t(g) * 8;
+      {
+        Phase ph(st, 1);
+        RL_TRY(launch_merge_loss(hg.mp, lg, st));
+        ph.launched(2);
+      }
+      RL_TRY_RC(run_backward(&cg, pg, hg, targets + r0, 0, hg.mp.lse2, lg.coef, dX + size_t(r0) * cfg->H, dW, db,
+                             ws, st, g > 0));
+      RL_TRY(launch_counters(ctr_dev, counters, false, st));
+      g_launches += 1;
+    }
+    LossParams lf = loss_params(cfg, p, ws);
+    lf.out_loss = out_loss;
+    lf.out_metrics = out_metrics;
+    {
+      Phase ph(st, 1);
+      RL_TRY(launch_fold_sums(sums, p.ngroups, lf, st));
+      RL_TRY(launch_counters(ctr_dev, counters, true, st));
+      ph.launched(2);
+    }
+    if (out_entropy_mask) RL_TRY(cudaMemcpyAsync(out_entropy_mask, mask, size_t(p.N), cudaMemcpyDeviceToDevice, st));
+    return RLLOSS_OK;
+  }
   RL_TRY_RC(run_head(cfg, p, X, W, b, targets, out_logp, out_entropy, nullptr, ws, st, hd, !p.fused_loss,
                      skip_tiles ? mask : nullptr));
   const MergeParams& mp = hd.mp;

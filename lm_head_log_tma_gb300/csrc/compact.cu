@@ -193,72 +193,104 @@ __global__ void scatter_rows_kernel(const float4* src, const int* idx, const int
   }
 }
 
-// One warp per row of the stored-probability buffer (see StoredParams): lane
-// 0 forms the row's factors and writes its target entry into the buffer, the
-// warp writes the scaled X row.
+// Block b handles buffer rows [32 b, 32 b + 32) of the stored-probability
+// buffer (see StoredParams): thread r < 32 forms row 32 b + r's factors and
+// writes its target entry into the buffer; then all threads write the scaled
+// X rows (16-byte words).
 __global__ void __launch_bounds__(kCompactBlock) stored_rows_kernel(StoredParams p) {
-  const int lane = threadIdx.x & 31;
+  __shared__ int src_row[kGroup];
+  __shared__ float scale[kGroup];
   const int nt = p.tiles ? *p.ntiles : p.R;
   const int rows = min(nt, p.pu_tiles) * 256;
   if (blockIdx.x == 0 && threadIdx.x == 0) *p.rows_total = rows;
-  const int wstep = int(gridDim.x) * (kCompactBlock / 32);
-  for (int j = int(blockIdx.x) * (kCompactBlock / 32) + (threadIdx.x >> 5); j < rows; j += wstep) {
-    const int slot = j >> 8;
-    const int n = (p.tiles ? p.tiles[slot] : slot) * 256 + (j & 255);
-    int ok = 0;
-    float k2 = 0.f, er = 0.f;
-    long long y = -1;
-    if (lane == 0 && n < p.N) {
-      const float cf = p.coef[n];
-      const float l2 = p.lse2[n];
-      y = p.targets[n];
-      if (cf != 0.f && l2 >= kStoredLse2Min && l2 <= kStoredLse2Max && y >= 0 && y < p.V) {
-        // G = (c/tau)(onehot - p) with p = pu 2^-lse2: off the target G = k2 pu,
-        // at the target k1 = (c/tau)(1 - p_y), 1 - p_y = -expm1(logp)
-        const double k2d = -double(cf) * exp2(-double(l2));
-        const double k1d = double(cf) * -expm1(p.logp64[n]);
-        const __nv_bfloat16 tv = __float2bfloat16_rn(float(k1d / k2d));
-        k2 = float(k2d);
-        er = float(k1d - k2d * double(__bfloat162float(tv)));
-        p.pu[size_t(j) * p.pu_ld + size_t(y)] = tv;
-        ok = 1;
-      }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    k2 = __shfl_sync(0xffffffffu, k2, 0);
-    const int words = p.H / 8;   // 16-byte words per row
-    uint4* dst = reinterpret_cast<uint4*>(p.xs + size_t(j) * p.H);
-    if (ok) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(n) * p.H);
-      for (int w = lane; w < words; w += 32) {
-        const uint4 u = __ldg(src + w);
-        uint32_t in[4] = {u.x, u.y, u.z, u.w}, out[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&in[k]);
-          const __nv_bfloat162 r2 = __floats2bfloat162_rn(k2 * __low2float(b2), k2 * __high2float(b2));
-          out[k] = *reinterpret_cast<const uint32_t*>(&r2);
+  const int words = p.H / 8;   // 16-byte words per row
+  for (int j0 = int(blockIdx.x) * kGroup; j0 < rows; j0 += int(gridDim.x) * kGroup) {
+    if (threadIdx.x < kGroup) {
+      const int j = j0 + int(threadIdx.x);
+      const int slot = j >> 8;
+      const int n = (p.tiles ? p.tiles[slot] : slot) * 256 + (j & 255);
+      bool ok = false;
+      float k2 = 0.f, er = 0.f;
+      long long y = -1;
+      if (n < p.N) {
+        const float cf = p.coef[n];
+        const float l2 = p.lse2[n];
+        y = p.targets[n];
+        if (cf != 0.f && l2 >= kStoredLse2Min && l2 <= kStoredLse2Max && y >= 0 && y < p.V) {
+          // G = (c/tau)(onehot - p) with p = pu 2^-lse2: off the target G = k2 pu,
+          // at the target k1 = (c/tau)(1 - p_y), 1 - p_y = -expm1(logp)
+          const double k2d = -double(cf) * exp2(-double(l2));
+          const double k1d = double(cf) * -expm1(p.logp64[n]);
+          const __nv_bfloat16 tv = __float2bfloat16_rn(float(k1d / k2d));
+          k2 = float(k2d);
+          er = float(k1d - k2d * double(__bfloat162float(tv)));
+          p.pu[size_t(j) * p.pu_ld + size_t(y)] = tv;
+          ok = true;
         }
-        dst[w] = make_uint4(out[0], out[1], out[2], out[3]);
       }
-    } else {
-      for (int w = lane; w < words; w += 32) dst[w] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (lane == 0) {
       p.idx[j] = ok ? n : -1;
       p.k2[j] = k2;
       p.err[j] = er;
       p.tgt[j] = ok ? y : -1;
       if (ok) p.done[n] = 1;
+      src_row[threadIdx.x] = ok ? n : -1;
+      scale[threadIdx.x] = k2;
+      const unsigned kept = __ballot_sync(0xffffffffu, ok);
+      if (threadIdx.x == 0 && kept) atomicAdd(p.rows_valid, __popc(kept));
     }
+    __syncthreads();
+    const int owords = p.xs_ld / 8;   // words per row of xs (one more with the db column)
+    for (int w = int(threadIdx.x); w < kGroup * owords; w += kCompactBlock) {
+      const int r = w / owords, c = w - r * owords;
+      const int n = src_row[r];
+      uint4 out = make_uint4(0u, 0u, 0u, 0u);
+      if (c >= words) {   // the db column (k2 in its first element), zeros after it
+        if (n >= 0 && c == words && p.xcol >= 0) {
+          const __nv_bfloat162 k2p = __floats2bfloat162_rn(scale[r], 0.f);
+          out.x = *reinterpret_cast<const uint32_t*>(&k2p);
+        }
+      } else if (n >= 0) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.x + size_t(n) * p.H) + c);
+        const float k2 = scale[r];
+        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&in[k]);
+          const __nv_bfloat162 r2 = __floats2bfloat162_rn(k2 * __low2float(b2), k2 * __high2float(b2));
+          o[k] = *reinterpret_cast<const uint32_t*>(&r2);
+        }
+        out = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      reinterpret_cast<uint4*>(p.xs + size_t(j0 + r) * p.xs_ld)[c] = out;
+    }
+    __syncthreads();
   }
 }
 
 cudaError_t launch_stored_rows(const StoredParams& p, cudaStream_t st) {
-  long long blocks = (p.rows_cap + 7) / 8;
+  long long blocks = (p.rows_cap + kGroup - 1) / kGroup;
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
   stored_rows_kernel<<<int(blocks), kCompactBlock, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+// Row counters of a call run in groups: acc[k] += *c[k] after each group, and
+// *c[k] = acc[k] after the last (what the counter queries then report).
+__global__ void counters_kernel(int* c0, int* c1, int* c2, int* acc, int write_back) {
+  if (threadIdx.x != 0) return;
+  int* c[3] = {c0, c1, c2};
+  for (int k = 0; k < 3; ++k) {
+    if (write_back)
+      *c[k] = acc[k];
+    else
+      acc[k] += *c[k];
+  }
+}
+
+cudaError_t launch_counters(int* const (&c)[3], int* acc, bool write_back, cudaStream_t st) {
+  counters_kernel<<<1, 32, 0, st>>>(c[0], c[1], c[2], acc, write_back ? 1 : 0);
   return cudaGetLastError();
 }
 

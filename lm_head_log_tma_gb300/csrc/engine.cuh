@@ -51,6 +51,7 @@ struct TileInfo {
   bool last;     // last tile of its unit
   int aux = 0;   // policy-defined (dX/dW: k-blocks per product term; forward: vocabulary segments)
   int slot = 0;  // forward: slot of the row tile in the launch's tile order
+  int wide = 0;  // dX/dW: 1 when the tile's second sub is widened (set by the schedule)
 };
 
 // Wait that ignores the abort flag; used only to drain in-flight work.
@@ -163,6 +164,9 @@ __global__ void __launch_bounds__(kEngineThreads, 1) tc_engine_kernel(const __gr
   static_assert(P::kSubs == 1 || (P::kSubs == 2 && P::kAccBufs == 1), "a split accumulator is single-buffered");
   static_assert(P::kCluster == 1 || P::kCluster == 2, "single CTAs or CTA pairs");
   constexpr bool kPair = P::kCluster == 2;
+  // Work sizes read on the device (rows left for this launch) are the same for
+  // every CTA: a launch with nothing to do returns before any setup.
+  if (!P::has_work(prm)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

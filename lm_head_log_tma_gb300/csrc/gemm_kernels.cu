@@ -51,6 +51,36 @@ __device__ __forceinline__ void store_bf16_box(const CUtensorMap* m, int* status
   ++nbuf;
 }
 
+// A 32-row x 64-column bf16 box (128-byte rows, 128-byte swizzle: 16-byte
+// chunk k of row r sits at chunk k ^ (r % 8)), filled from two 32-column halves
+// and stored with one TMA store; one such buffer per warp.  stage_half writes
+// this lane's 32 columns as half h; zero_col in [0, 32) writes that column of
+// the half as 0.  Before half 0 the previous box's store must have finished
+// reading the buffer.
+constexpr int kBf16Box64Bytes = 32 * 128;
+__device__ __forceinline__ void stage_half(uint8_t* buf, int lane, const uint32_t (&w)[16], int h,
+                                           unsigned zero_col) {
+  if (h == 0) {
+    if (lane == 0) tma_store_wait_read<0>();
+    __syncwarp();
+  }
+  uint4* row = reinterpret_cast<uint4*>(buf + lane * 128);
+  const int sw = lane & 7;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) row[(4 * h + c) ^ sw] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  if (zero_col < 32u)
+    *reinterpret_cast<uint16_t*>(buf + lane * 128 + (((4 * h + int(zero_col >> 3)) ^ sw) << 4) +
+                                 (zero_col & 7u) * 2) = 0;
+}
+__device__ __forceinline__ void store_box64(const CUtensorMap* m, int* status, uint8_t* buf, int lane, int x, int y) {
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    if (tma_x_ok<2>(x, status)) tma_store_2d(m, buf, x, y);
+    tma_store_commit();
+  }
+}
+
 // =============================================================== forward
 // CL = 1: 128-row tiles on one CTA; CL = 2: 256-row tiles over a CTA pair
 // (cta_group::2).  F8: e4m3 operands (forward-only scoring) with per-row
@@ -75,8 +105,8 @@ struct FwdPolicy {
   static constexpr int kABytes = kBox * KBX;
   static constexpr int kBBytes = (256 / PAIR) * 128 * KBX;   // this CTA's share of the B rows
   static constexpr int kColBytes = 2 * 128 * 4;   // per epilogue warp: its 128 columns' W scales and biases
-  // ST: two staging boxes per epilogue warp instead (no bias, no scales)
-  static constexpr int kExtraSmem = ST ? kEpiWarps * 2 * kBf16BoxBytes : kEpiWarps * kColBytes;
+  // ST: one 32 x 64 staging box per epilogue warp instead (no bias, no scales)
+  static constexpr int kExtraSmem = ST ? kEpiWarps * kBf16Box64Bytes : kEpiWarps * kColBytes;
   static_assert(!ST || (CL == 2 && !F8), "stored probabilities: bf16 CTA-pair forward");
   static constexpr uint32_t kIdesc = F8 ? idesc_e4m3(kRows, 256) : idesc_bf16(kRows, 256, 0, 0);
   static constexpr int kKB = (F8 ? 128 : 64) * KBX;   // K elements per k-block
@@ -91,7 +121,6 @@ struct FwdPolicy {
     float4 pw, pb;
     int pre_n0 = -1;       // tile whose columns pw / pb hold
     int R = -1, P = 0;     // launch shape (for the next tile's columns)
-    int nbuf = 0;          // ST: staging buffer alternation
   };
 
   // Row tiles and vocabulary segments of this launch: all R tiles with the
@@ -105,6 +134,7 @@ struct FwdPolicy {
       P = p.P;
     }
   }
+  __device__ static bool has_work(const Params&) { return true; }   // writes P_out even without tiles
   __device__ static void cta_setup(const Params& p, uint8_t*) {
     if (p.P_out && blockIdx.x == 0 && threadIdx.x == 0) {
       int R, P;
@@ -204,8 +234,8 @@ struct FwdPolicy {
                                   int lane, uint8_t* extra, uint32_t rank) {
     const int row = t.m0 + 128 * int(rank) + q * 32 + lane;
     float* cols = reinterpret_cast<float*>(extra + (q + 4 * half) * kColBytes);   // [128 scales][128 biases]
-    // ST: this warp's staging boxes; the tile's rows go to rows slot * 256 + .. of the buffer
-    uint8_t* wbuf = extra + (q + 4 * half) * 2 * kBf16BoxBytes;
+    // ST: this warp's staging box; the tile's rows go to rows slot * 256 + .. of the buffer
+    uint8_t* wbuf = extra + (q + 4 * half) * kBf16Box64Bytes;
     const bool st_tile = ST && t.slot < p.pu_tiles;
     const int pu_y0 = t.slot * kRows + 128 * int(rank) + q * 32;
     if (!ST && (F8 || p.bias2)) {
@@ -257,11 +287,13 @@ struct FwdPolicy {
           v[4 * i + 2] = fmaf(v[4 * i + 2] * e.xs, w.z, b.z);
           v[4 * i + 3] = fmaf(v[4 * i + 3] * e.xs, w.w, b.w);
         }
-      } else if (!ST && p.bias2) {
-        const float4* b4 = reinterpret_cast<const float4*>(cols + 128 + ch * 32);
+      } else if (p.bias2) {
+        // ST keeps no column vectors in shared memory: the bias comes from L1/L2
+        const float4* b4 = ST ? reinterpret_cast<const float4*>(p.bias2 + c0)
+                              : reinterpret_cast<const float4*>(cols + 128 + ch * 32);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 b = b4[i];
+          const float4 b = ST ? __ldg(b4 + i) : b4[i];
           v[4 * i + 0] = fmaf(v[4 * i + 0], sc, b.x);
           v[4 * i + 1] = fmaf(v[4 * i + 1], sc, b.y);
           v[4 * i + 2] = fmaf(v[4 * i + 2], sc, b.z);
@@ -270,25 +302,61 @@ struct FwdPolicy {
       }
       // Without bias or e4m3 scales v is still the raw logit; its scale to
       // log2 units folds into the FFMA that forms t - m below (mul = sc).
-      const float mul = (F8 || (!ST && p.bias2)) ? 1.f : sc;
+      const float mul = (F8 || p.bias2) ? 1.f : sc;
       const bool tail = c0 + 32 > p.V;   // columns past V: out of the max, weight 0
       if (tail) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           if (c0 + i >= p.V) v[i] = -INFINITY;
       }
-      float mx = v[0];
+      // Reference m: an integer in log2 units, from the first chunk's maximum
+      // of this row's vocabulary range.  Later chunks are exponentiated against
+      // it; only a chunk whose sum leaves the range fp32 keeps exact (2^64, or
+      // not finite) takes its maximum, moves m up by a power of two (an exact
+      // rescale of the sums) and is redone.  Sums of terms up to 2^64 stay
+      // exact to the compensated accumulation, and the segment merge takes
+      // any integer reference.
+      auto chunk_max = [&]() {
+        float mx = v[0];
 #pragma unroll
-      for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
-      mx *= mul;   // mul > 0
-      // Reference max kept on an integer grid in log2 units; move it only
-      // when a logit would exceed it by more than 2^16, so rescaling is rare
-      // and exact (a power of two).
-      if (mx > e.mref + 16.f) {
-        const float nref = ceilf(mx);
-        if (e.mref == -INFINITY) {
-          e.mref = nref;
-        } else {
+        for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
+        return mx * mul;   // mul > 0
+      };
+      if (e.mref == -INFINITY) e.mref = ceilf(chunk_max());
+      // ST: 2^t = 2^(t - m) 2^m exactly (m an integer); m is capped at 100, past
+      // which the backward recomputes the row anyway, and 2^m below 2^-126
+      // is taken as 0 (such a column's p is below 2^-46 in any row the
+      // stored path keeps)
+      uint32_t pk[ST ? 16 : 1];
+      float s0, s1, s2, s3, w0, w1, w2, w3;
+      auto exponentiate = [&]() {
+        float psc = 0.f;
+        if constexpr (ST) {
+          const float mr = fminf(e.mref, 100.f);
+          psc = mr >= -126.f ? __int_as_float((int(mr) + 127) << 23) : 0.f;
+        }
+        s0 = s1 = s2 = s3 = w0 = w1 = w2 = w3 = 0.f;
+        const float nm = -e.mref;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          float d0 = fmaf(v[i], mul, nm), d1 = fmaf(v[i + 1], mul, nm), d2 = fmaf(v[i + 2], mul, nm),
+                d3 = fmaf(v[i + 3], mul, nm);
+          if (tail) {   // -inf -> a finite large negative: 2^d = 0 and 0 * d = 0
+            d0 = fmaxf(d0, -1.0e30f); d1 = fmaxf(d1, -1.0e30f); d2 = fmaxf(d2, -1.0e30f); d3 = fmaxf(d3, -1.0e30f);
+          }
+          const float x0 = ex2_approx(d0), x1 = ex2_approx(d1), x2 = ex2_approx(d2), x3 = ex2_approx(d3);
+          s0 += x0; s1 += x1; s2 += x2; s3 += x3;
+          w0 = fmaf(x0, d0, w0); w1 = fmaf(x1, d1, w1); w2 = fmaf(x2, d2, w2); w3 = fmaf(x3, d3, w3);
+          if constexpr (ST) {
+            pk[i / 2] = pack_bf16x2(x0 * psc, x1 * psc);
+            pk[i / 2 + 1] = pack_bf16x2(x2 * psc, x3 * psc);
+          }
+        }
+      };
+      exponentiate();
+      if (!((s0 + s1) + (s2 + s3) <= 18446744073709551616.f)) {   // 2^64; NaN fails the test too
+        const float nref = ceilf(chunk_max());
+        if (nref > e.mref) {
           const float dd = e.mref - nref;     // negative integer
           const int di = int(dd);
           e.w_hi = ldexpf(e.w_hi + dd * e.s_hi, di);
@@ -296,33 +364,7 @@ struct FwdPolicy {
           e.s_hi = ldexpf(e.s_hi, di);
           e.s_lo = ldexpf(e.s_lo, di);
           e.mref = nref;
-        }
-      }
-      // ST: 2^t = 2^(t - m) 2^m exactly (m an integer); m is capped at 100, past
-      // which the backward recomputes the row anyway, and 2^m below 2^-126
-      // is taken as 0 (such a column's p is below 2^-46 in any row the
-      // stored path keeps)
-      float psc = 0.f;
-      if constexpr (ST) {
-        const float mr = fminf(e.mref, 100.f);
-        psc = mr >= -126.f ? __int_as_float((int(mr) + 127) << 23) : 0.f;
-      }
-      uint32_t pk[ST ? 16 : 1];
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float nm = -e.mref;
-        float d0 = fmaf(v[i], mul, nm), d1 = fmaf(v[i + 1], mul, nm), d2 = fmaf(v[i + 2], mul, nm),
-              d3 = fmaf(v[i + 3], mul, nm);
-        if (tail) {   // -inf -> a finite large negative: 2^d = 0 and 0 * d = 0
-          d0 = fmaxf(d0, -1.0e30f); d1 = fmaxf(d1, -1.0e30f); d2 = fmaxf(d2, -1.0e30f); d3 = fmaxf(d3, -1.0e30f);
-        }
-        const float x0 = ex2_approx(d0), x1 = ex2_approx(d1), x2 = ex2_approx(d2), x3 = ex2_approx(d3);
-        s0 += x0; s1 += x1; s2 += x2; s3 += x3;
-        w0 = fmaf(x0, d0, w0); w1 = fmaf(x1, d1, w1); w2 = fmaf(x2, d2, w2); w3 = fmaf(x3, d3, w3);
-        if constexpr (ST) {
-          pk[i / 2] = pack_bf16x2(x0 * psc, x1 * psc);
-          pk[i / 2 + 1] = pack_bf16x2(x2 * psc, x3 * psc);
+          exponentiate();
         }
       }
       two_sum_acc(e.s_hi, e.s_lo, (s0 + s1) + (s2 + s3));
@@ -335,8 +377,13 @@ struct FwdPolicy {
         e.found = 1;
       }
       if constexpr (ST) {
-        // warp-uniform; the target entry is written as 0 (the backward sets it)
-        if (st_tile) store_bf16_box(&p.tmPu, p.status, wbuf, e.nbuf, lane, pk, c0, pu_y0, ty);
+        // warp-uniform; chunks pair up into 64-column boxes (a lone last chunk's
+        // partner columns lie past V and the store drops them); the target
+        // entry is written as 0 (the backward sets it)
+        if (st_tile) {
+          stage_half(wbuf, lane, pk, ch & 1, ty);
+          if ((ch & 1) || ch + 1 == nch) store_box64(&p.tmPu, p.status, wbuf, lane, c0 - (ch & 1) * 32, pu_y0);
+        }
       }
       if (ch + 1 < nch) tmem_ld32_wait(r);
     }
@@ -425,6 +472,7 @@ struct DlPolicy {
     int nc = -1;   // rows of this chunk (read from the device on the first tile)
   };
   __device__ static int chunk_rows(const Params& p) { return min(max(*p.rows_total - p.n0, 0), p.Nc); }
+  __device__ static bool has_work(const Params& p) { return chunk_rows(p) > 0; }
 
   __device__ static void cta_setup(const Params&, uint8_t*) {}
   __device__ static void prefetch(const Params& p) {
@@ -546,7 +594,14 @@ struct DlPolicy {
 #pragma unroll
       for (int i = 0; i < 16; ++i) hi[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
       const int y0 = r0;
-      store_box(p, e, wbuf, lane, hi, c0, y0);
+      if (!p.lo_off) {
+        // bf16 G: chunks pair up into 64-column boxes (tmG: box 64 x 32, 128-byte
+        // swizzle); a lone last chunk's partner columns lie past V and are dropped
+        stage_half(wbuf, lane, hi, ch & 1, ~0u);
+        if ((ch & 1) || ch == 3 || c0 + 32 >= p.Vp) store_box64(&p.tmG, p.status, wbuf, lane, c0 - (ch & 1) * 32, y0);
+      } else {
+        store_box(p, e, wbuf, lane, hi, c0, y0);
+      }
       if (p.lo_off) {
         uint32_t lo[16];
 #pragma unroll
@@ -609,7 +664,7 @@ struct HPolicy {
   // The chunk's row count is read on the device: problem 0 (dX) gets its
   // row tiles from it, problem 1 (dW) its k-blocks per term.
   __device__ static void chunk_problems(const Params& p, HProblem (&pr)[2]) {
-    const int nc = min(max(*p.rows_total - p.n0, 0), p.nc_max);
+    const int nc = (p.rows_valid && *p.rows_valid == 0) ? 0 : min(max(*p.rows_total - p.n0, 0), p.nc_max);
     pr[0] = p.pr[0];
     pr[1] = p.pr[1];
     pr[0].Mt = (nc + 255) / 256;
@@ -635,9 +690,16 @@ struct HPolicy {
     }
     const int kbt = p.nseg * pr.kb_per_seg;
     const int cut = pr.ksplit == 2 ? kbt / 2 : kbt;
-    return TileInfo{i * 256, j * kNH, part == 0 ? 0 : cut, part == 0 ? cut : kbt, u, q, true, true, pr.kb_per_seg};
+    TileInfo t{i * 256, j * kNH, part == 0 ? 0 : cut, part == 0 ? cut : kbt, u, q, true, true, pr.kb_per_seg};
+    t.wide = (pr.wide && j == pr.Ht - 1) ? 1 : 0;
+    return t;
   }
   __device__ static int units(const HProblem& pr) { return pr.Mt * pr.Ht * pr.ksplit; }
+  __device__ static bool has_work(const Params& p) {
+    HProblem pr[2];
+    chunk_problems(p, pr);
+    return units(pr[0]) > 0 || (p.nprob > 1 && units(pr[1]) > 0);
+  }
   // Pair g of gn: problem 0 units g, g+gn, ...; then problem 1 units.  Pairs
   // that got fewer problem-0 units ("early" pairs) first take problem-1 units
   // [0, F*d) round-robin among themselves, d = problem-0 unit length in
@@ -664,8 +726,10 @@ struct HPolicy {
     for (int u = ph1 + g; u < T1; u += gn)
       if (!f(tile_of(p, pr[1], 1, u))) return;
   }
-  // One k-block: this CTA's 128 A rows and, for each sub, its 112 B rows
-  // (two 64-h runs, rows beyond 112 unused).
+  // Columns of sub `sub` of tile t: 224, or 240 for the widened last sub.
+  __device__ static int sub_n(const TileInfo& t, int sub) { return (t.wide && sub == 1) ? kNS + 16 : kNS; }
+  // One k-block: this CTA's 128 A rows and, for each sub, its half of the B
+  // rows (two 64-h runs; 112 of them used, 120 in a widened sub).
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int q = t.seg;
     const HProblem& pr = p.pr[q];
@@ -682,7 +746,7 @@ struct HPolicy {
     }
 #pragma unroll
     for (int sub = 0; sub < 2; ++sub) {
-      const int h = p.seg_b[s] + t.n0 + kNS * sub + 112 * int(rank);
+      const int h = p.seg_b[s] + t.n0 + kNS * sub + (sub_n(t, sub) / 2) * int(rank);
       uint8_t* b = st + kABytes + sub * kBSub;
       if (tma_x_ok<2>(h, p.status)) tma_load_2d_pair(&p.tmB[q], bar, b, h, pr.b_outer0 + kk);
       if (tma_x_ok<2>(h + 64, p.status)) tma_load_2d_pair(&p.tmB[q], bar, b + 8192, h + 64, pr.b_outer0 + kk);
@@ -694,13 +758,14 @@ struct HPolicy {
   __device__ static uint64_t bdesc(uint32_t sa, int k, int sub) {
     return sdesc_sw128(sa + kABytes + sub * kBSub + k * 2048, 8192, 1024);
   }
-  __device__ static uint32_t idesc(const TileInfo& t) {
-    return t.seg == 1 ? idesc_bf16(256, kNS, 1, 1) : idesc_bf16(256, kNS, 0, 1);
+  __device__ static uint32_t idesc(const TileInfo& t, int sub) {
+    if (sub_n(t, sub) == kNS) return t.seg == 1 ? idesc_bf16(256, kNS, 1, 1) : idesc_bf16(256, kNS, 0, 1);
+    return t.seg == 1 ? idesc_bf16(256, kNS + 16, 1, 1) : idesc_bf16(256, kNS + 16, 0, 1);
   }
   __device__ static uint32_t tx_bytes(const Params&, const TileInfo&) { return kABytes + kBBytes; }
   __device__ static void mma(const Params&, uint32_t d, uint32_t sa, int k, const TileInfo& t, int sub,
                              uint32_t accum) {
-    umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, sub), idesc(t), accum);
+    umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, sub), idesc(t, sub), accum);
   }
 
   // v[i] += err * W[target][x0 + i] for the valid columns (bf16 W row, 16-byte aligned).
@@ -733,7 +798,7 @@ struct HPolicy {
     const CUtensorMap* om = &p.tmO[t.seg];
     uint8_t* buf = extra + (q + 4 * half) * kBoxBytes;
     const int y0 = t.m0 + 128 * int(rank) + q * 32;
-    const int c_begin = half ? 4 : 0, c_end = half ? 7 : 4;
+    const int c_begin = half ? 4 : 0, c_end = half ? (sub_n(t, sub) > kNS ? 8 : 7) : 4;
     const bool no_k = t.kb_end <= t.kb_begin;   // empty sum (a chunk without rows): store zeros
     // dX rows: the target-entry correction err * W[target] on the first k part
     const __nv_bfloat16* wrow = nullptr;
@@ -783,6 +848,13 @@ struct HPolicy {
 #pragma unroll 1
     for (int c = c_begin; c < c_end; ++c) {
       const int x0 = t.n0 + sub * kNS + c * 32;
+      if (pr.xcol_out != nullptr && pr.xcol >= x0 && pr.xcol < x0 + 32) {
+        // the routed column (db through dW's GEMM), one value per output row,
+        // read on its own (warp-uniform column)
+        const float xv = no_k ? 0.f : tmem_ld1(taddr + uint32_t(c * 32 + (pr.xcol - x0)));
+        const int r = y0 + lane;
+        if (r < pr.xrows) pr.xcol_out[r] = pr.reduce ? pr.xcol_out[r] + xv : xv;
+      }
       if (x0 >= pr.Hout) break;
       float v[32];
       if (no_k) {
@@ -954,7 +1026,7 @@ int gemmH_resident_clusters() {
 cudaError_t launch_fwd(const FwdParams& p, int units, int cluster, int kbx, cudaStream_t st) {
   if (p.xs) return launch_engine<FwdPolicy<2, true, 2>>(p, units, st);   // e4m3 operands: CTA pairs only
   if (p.pu_tiles > 0) {
-    if (cluster != 2 || kbx != 2 || p.bias2 || p.nseg != 1) return cudaErrorInvalidValue;
+    if (cluster != 2 || kbx != 2 || p.nseg != 1) return cudaErrorInvalidValue;
     return launch_engine<FwdPolicy<2, false, 2, true>>(p, units, st);
   }
   if (cluster == 1) return launch_engine<FwdPolicy<1>>(p, units, st);

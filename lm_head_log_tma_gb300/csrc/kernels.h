@@ -53,7 +53,7 @@ struct FwdParams {
   // computed logit's unnormalised probability 2^t (t = logit log2(e) / tau,
   // so p = 2^(t - lse2)) is written as bf16 to row (slot * 256 + row in
   // tile) of the buffer tmPu maps; the target column is written as 0.
-  CUtensorMap tmPu;           // inner V columns, outer pu_tiles * 256 rows; box 32 x 32, 64-byte swizzle
+  CUtensorMap tmPu;           // inner V columns, outer pu_tiles * 256 rows; box 64 x 32, 128-byte swizzle
   int pu_tiles;
   int* status;
   unsigned long long limit_ns;
@@ -78,7 +78,8 @@ struct MergeParams {
 
 struct DlParams {
   CUtensorMap tmA, tmB;
-  CUtensorMap tmG;            // G chunk buffer: inner columns, outer chunk rows; box 32 x 32, 64-byte swizzle
+  CUtensorMap tmG;            // G chunk buffer: inner columns, outer chunk rows; bf16 G: box 64 x 32,
+                              // 128-byte swizzle; fp32 mode (hi and lo terms): box 32 x 32, 64-byte swizzle
   int nseg, kb_per_seg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];
   int n0, Nc, Rc, V, Vp, Vt;  // chunk start row, rows in chunk (upper bound), row tiles (128 or 256 rows), vocab, padded vocab, vocab tiles
@@ -115,6 +116,12 @@ struct HProblem {
   int reduce;                 // 0: store, 1: add into the output
   int ksplit;                 // 1, or 2: each tile's k range in two units that both add
                               // into a zeroed output (two addends: the sum is order-free)
+  // Optional output column routed elsewhere (xcol_out set): column xcol (>= Hout
+  // allowed) of output row r < xrows goes to xcol_out[r] (added when reduce;
+  // one tile writes each row).
+  // wide = 1: the last h tile's second sub is 240 columns (xcol = Ht * 448).
+  int xcol, xrows, wide;
+  float* xcol_out;
 };
 struct HParams {
   CUtensorMap tmA[2];         // K-major: inner k, box 64 x 128 | MN-major: inner row, box 64 x 64
@@ -126,6 +133,7 @@ struct HParams {
   // Rows of the chunk, read on the device: nc = clamp(*rows_total - n0, 0, nc_max).
   // Problem 0 (dX) has ceil(nc/256) row tiles; problem 1 (dW) ceil(nc/64) k-blocks per term.
   const int* rows_total;
+  const int* rows_valid;      // optional: when it reads 0 the chunk has no rows (all coefficients 0)
   int n0, nc_max;
   int nseg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];  // inner-coordinate offsets of each product term
@@ -174,6 +182,7 @@ struct LossParams {
   unsigned int* seq_ticket;   // [B], zero on entry
   unsigned int* ticket;       // zero on entry
   int slices;                 // blocks per sequence
+  int coef_slices;            // blocks per sequence of the coefficient kernel (0: by T alone)
   float* coef;                // optional: c / tau
   float* dlogp;               // optional: c
   float* out_loss;            // null: write out_sums only
@@ -254,15 +263,20 @@ struct StoredParams {
   const __nv_bfloat16* x;     // [N, H]
   __nv_bfloat16* pu;          // [rows_cap, pu_ld]
   int pu_ld;
-  __nv_bfloat16* xs;          // [rows_cap, H]
+  __nv_bfloat16* xs;          // [rows_cap, xs_ld]: k2 X; with xcol set also column H = k2
+  int xs_ld, xcol;            // row stride of xs (elements); xcol: H (bias: db through dW's GEMM) or -1
   int* idx;                   // [rows_cap]
   float* k2;                  // [rows_cap]
   float* err;                 // [rows_cap]
   int64_t* tgt;               // [rows_cap]
   uint8_t* done;              // [N], zeroed before the launch
   int* rows_total;            // out: stored rows (stored tiles * 256)
+  int* rows_valid;            // out: rows with c != 0 among them (zeroed before the launch)
 };
 cudaError_t launch_stored_rows(const StoredParams& p, cudaStream_t st);
+// Row counters of a call run in groups of sequences: acc[k] += *c[k] (after a
+// group), or *c[k] = acc[k] (after the last).
+cudaError_t launch_counters(int* const (&c)[3], int* acc, bool write_back, cudaStream_t st);
 int compact_groups(int N);   // 32-row groups
 // Row tiles of tile_rows rows holding a row with mask != 0: flags[R], their
 // ascending list and count (ticket zeroed before the launch).
@@ -301,6 +315,11 @@ cudaError_t launch_entropy_apply(const float* ent, const uint8_t* mask, long lon
                                  uint8_t* emask, cudaStream_t st);
 int loss_slices(int B, int T, int sms);
 int fused_loss_slices(int T);
+int coef_slices(int B, int T, int sms);
 cudaError_t launch_merge_loss(const MergeParams& mp, const LossParams& p, cudaStream_t st);
+// Loss and metrics (p.out_loss, p.out_metrics) from the batch sums of ngroups
+// groups of sequences ([ngroups][8] doubles, as written through out_sums),
+// added in group order; p.Bg is the whole batch's sequence count.
+cudaError_t launch_fold_sums(const double* sums, int ngroups, const LossParams& p, cudaStream_t st);
 
 }  // namespace rl

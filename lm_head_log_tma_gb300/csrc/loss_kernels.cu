@@ -326,6 +326,7 @@ __device__ __forceinline__ void fold_sequence(const LossParams& p, int i, int la
 // (GSPO: clipped sequences), [3] sum of K3 KL, [4] tokens kept by the entropy
 // mask (GSPO: active tokens), [5] sum of sequence log ratios, [6] sum of
 // sequence ratios (both over sequences with tokens), [7] sequences with tokens.
+__device__ __forceinline__ void finish_batch(const LossParams& p, const double (&f)[8], bool gmpo);
 __device__ __forceinline__ void fold_batch(const LossParams& p, int lane, bool gmpo) {
   double f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int j = lane; j < p.B; j += 32) {
@@ -352,6 +353,11 @@ __device__ __forceinline__ void fold_batch(const LossParams& p, int lane, bool g
     if (!isfinite(f[0]) && p.status) atomicOr(p.status, RLLOSS_DEV_ENONFINITE);
     return;
   }
+  finish_batch(p, f, gmpo);
+}
+
+// Loss and metrics from the eight batch sums (the layout of fold_batch).
+__device__ __forceinline__ void finish_batch(const LossParams& p, const double (&f)[8], bool gmpo) {
   double loss = f[0];
   const double n_act = f[1], clip = f[2], kl = f[3], kept = f[4], sx = f[5], sr = f[6], nh = f[7];
   float* m = p.out_metrics;
@@ -418,6 +424,7 @@ __global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p
   const double A = seq_adv(p, i);
   const bool gmpo = p.loss_type == RLLOSS_GMPO;
   double a[5] = {0, 0, 0, 0, 0};
+#pragma unroll 4
   for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
     const long long n = base + t;
     token_terms(p, n, logp_at(p, n), A, gmpo, a);
@@ -429,13 +436,22 @@ __global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p
   if (take_batch_ticket(p, threadIdx.x)) fold_batch(p, threadIdx.x, gmpo);
 }
 
-// Per-token gradient coefficient c_n = dL/dlogp_n from the sequence records.
+// Per-token gradient coefficient c_n = dL/dlogp_n from the sequence records:
+// block (sl, i) takes slice sl of sequence i, with the sequence's record in
+// shared memory.
 __global__ void loss_coef_kernel(LossParams p) {
-  const long long N = (long long)p.B * p.T;
+  __shared__ double rec[kRec];
+  const int i = blockIdx.y;
+  if (threadIdx.x < kRec) rec[threadIdx.x] = __ldcg(p.seqres + size_t(i) * kRec + threadIdx.x);
+  __syncthreads();
   const bool gmpo = p.loss_type == RLLOSS_GMPO;
-  for (long long n = blockIdx.x * (long long)blockDim.x + threadIdx.x; n < N; n += (long long)gridDim.x * blockDim.x) {
-    const int i = int(n / p.T);
-    store_coef(p, n, token_coef(p, n, i, p.seqres + size_t(i) * kRec, gmpo));
+  const long long base = (long long)i * p.T;
+  const int t0 = int((long long)blockIdx.x * p.T / gridDim.x);
+  const int t1 = int((long long)(blockIdx.x + 1) * p.T / gridDim.x);
+#pragma unroll 4
+  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+    const long long n = base + t;
+    store_coef(p, n, token_coef(p, n, i, rec, gmpo));
   }
 }
 
@@ -474,7 +490,7 @@ __global__ void __launch_bounds__(kLossThreads) merge_loss_kernel(MergeParams mp
 }
 
 int loss_slices(int B, int T, int sms) {
-  long long s = (4ll * sms + B - 1) / B;
+  long long s = (16ll * sms + B - 1) / B;
   const long long smax = (T + 255) / 256;
   if (s > smax) s = smax;
   if (s < 1) s = 1;
@@ -483,17 +499,42 @@ int loss_slices(int B, int T, int sms) {
 
 int fused_loss_slices(int T) { return (T + kFusedRows - 1) / kFusedRows; }
 
+// Slices of >= 1024 tokens per sequence for the coefficient kernel, about 16
+// blocks per SM over the batch.
+int coef_slices(int B, int T, int sms) {
+  long long s = (16ll * sms + B - 1) / B;
+  const long long smax = (T + 1023) / 1024;
+  if (s > smax) s = smax;
+  if (s < 1) s = 1;
+  return int(s);
+}
+
 static cudaError_t launch_coef(const LossParams& p, cudaStream_t st) {
-  const long long N = (long long)p.B * p.T;
-  long long nb = (N + 127) / 128;
-  if (nb > 8192) nb = 8192;
-  loss_coef_kernel<<<int(nb), 128, 0, st>>>(p);
+  long long s = p.coef_slices > 0 ? p.coef_slices : (p.T + 1023) / 1024;
+  if (s < 1) s = 1;
+  loss_coef_kernel<<<dim3(unsigned(s), unsigned(p.B)), 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge_loss(const MergeParams& mp, const LossParams& p, cudaStream_t st) {
   merge_loss_kernel<<<dim3(p.slices, p.B), kLossThreads, 0, st>>>(mp, p);
   if (p.coef || p.dlogp) return launch_coef(p, st);
+  return cudaGetLastError();
+}
+
+// Loss and metrics from the batch sums of several groups of sequences
+// ([ngroups][8], each written as LossParams::out_sums), added in group order.
+__global__ void fold_sums_kernel(const double* sums, int ngroups, LossParams p) {
+  if (threadIdx.x != 0) return;
+  double f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int g = 0; g < ngroups; ++g)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) f[k] += __ldcg(sums + size_t(g) * 8 + k);
+  finish_batch(p, f, p.loss_type == RLLOSS_GMPO);
+}
+
+cudaError_t launch_fold_sums(const double* sums, int ngroups, const LossParams& p, cudaStream_t st) {
+  fold_sums_kernel<<<1, 32, 0, st>>>(sums, ngroups, p);
   return cudaGetLastError();
 }
 

@@ -220,6 +220,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// One column of 32 TMEM lanes (lane i of the warp gets lane base+i), waited for.
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r)
+      : "r"(taddr)
+      : "memory");
+  return __uint_as_float(r);
+}
+
 // Split form for software pipelining: tmem_ld32_issue starts the load of 32
 // columns into r; tmem_ld32_wait waits for every load this thread issued and
 // takes r as in/out operands, so no use of r can be scheduled before it.

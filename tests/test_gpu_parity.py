@@ -82,11 +82,14 @@ def test_mid_workloads(R, spec):
 
 
 def test_backward_chunking_is_invariant(R):
-    """Chunks of 128 rows (several dW/db accumulation steps) give the same result."""
+    """Recompute chunks of 128 rows (several dW/db accumulation steps) give the
+    same result as one chunk; with stored probabilities a 128-row buffer stores
+    one row tile and recomputes the rest, which passes the oracle too."""
     spec = MID[1]
     case = Case(spec)
-    a, _, _ = _full_check(R, case)
-    b, _, _ = _full_check(R, case, chunk_rows=128)
+    _full_check(R, case, chunk_rows=128)
+    a, _, _ = _full_check(R, case, flags=R.FLAG_RECOMPUTE)
+    b, _, _ = _full_check(R, case, chunk_rows=128, flags=R.FLAG_RECOMPUTE)
     assert torch.equal(a["loss"], b["loss"])
     assert torch.allclose(a["dX"], b["dX"], rtol=1e-4, atol=1e-9)
     assert torch.allclose(a["dW"], b["dW"], rtol=1e-4, atol=1e-9)
@@ -147,6 +150,23 @@ def test_uniform_logits_closed_form(R):
     assert out["status"] == 0
     assert np.allclose(out["logp"].cpu().numpy(), -np.log(700), atol=2e-6)
     assert np.allclose(out["entropy"].cpu().numpy(), np.log(700), atol=2e-6)
+
+
+def test_rising_logits_move_the_reference(R):
+    """A bias rising along the vocabulary (b_v = 0.048 v: logits climb about 90
+    log2 units across V = 1300) puts every row's largest logits far above the
+    first 32-column chunk the forward takes its reference from, so the
+    reference has to move during the row (the rescale path); per-token logp,
+    entropy, loss and gradients still match the oracle, on the stored path and
+    the recompute."""
+    spec = Workload("rising_logits", B=2, T=300, H=64, V=1300, dtype="bf16", has_bias=True, prompt_len=10,
+                    seed=131)
+    inp = make_inputs(spec)
+    inp.b = (torch.arange(spec.V, dtype=torch.float32) * 0.048).to(torch.bfloat16)
+    case = Case(spec, inp)
+    assert np.all(case.lse * 1.4426950408889634 < 96)   # inside the stored range
+    _full_check(R, case)
+    _full_check(R, case, flags=R.FLAG_RECOMPUTE)
 
 
 def test_bad_target_sets_status(R):

@@ -38,6 +38,17 @@ SPECS = [
              prompt_len=(5, 40), adv_kind="pm1zero", ref_noise_std=0.1, seed=204),
     Workload("stored_wide_h_2048", B=2, T=300, H=2048, V=3000, dtype="bf16", prompt_len=10, seed=205),
     Workload("stored_many_short", B=300, T=3, H=64, V=500, dtype="bf16", prompt_len=1, seed=206),
+    # with a bias, db comes out of dW's GEMM as one more column (k2 in column H of
+    # the scaled X rows): inside the last tile's second half (H=256), in a
+    # widened last half (H=448, a multiple of the 448-column tile), inside the
+    # last tile's first half (H=1040)
+    Workload("stored_bias_k3kl", B=4, T=130, H=256, V=777, dtype="bf16", has_bias=True, bias_std=0.3,
+             eps_low=0.2, eps_high=0.3, beta=0.04, prompt_len=(5, 40), adv_kind="pm1zero", ref_noise_std=0.1,
+             seed=207),
+    Workload("stored_bias_h448", B=2, T=200, H=448, V=1500, dtype="bf16", has_bias=True, bias_std=0.2,
+             prompt_len=16, seed=208),
+    Workload("stored_bias_h1040", B=3, T=100, H=1040, V=1500, dtype="bf16", has_bias=True, bias_std=0.2,
+             temperature=0.7, prompt_len=5, seed=209),
 ]
 
 
@@ -53,7 +64,9 @@ def _check(R, case, **kw):
 
 
 def _close(a, b):
-    for k in ("dX", "dW"):
+    for k in ("dX", "dW", "db"):
+        if a.get(k) is None:
+            continue
         x, y = a[k].double().cpu().numpy(), b[k].double().cpu().numpy()
         assert rel_l2(x, y) <= GRAD_RELL2 and cosine(x, y) >= GRAD_COS, k
 
@@ -127,3 +140,40 @@ def test_stored_calls_are_bit_identical(R):
     b = case.run_gpu(R, per_token=False)
     for k in ("loss", "metrics", "dX", "dW"):
         assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), k
+
+
+GROUPED = [
+    Workload("grouped_gmpo_k3kl_bias", B=6, T=256, H=128, V=1000, dtype="bf16", has_bias=True, bias_std=0.2,
+             eps_low=0.2, eps_high=0.3, beta=0.04, prompt_len=(5, 40), adv_kind="pm1zero", ref_noise_std=0.1,
+             seed=211),
+    Workload("grouped_gspo", B=5, T=512, H=64, V=700, dtype="bf16", loss_type=GSPO_TOKEN, eps_low=3e-4,
+             eps_high=4e-4, prompt_len=16, old_noise_std=0.02, seed=212),
+]
+
+
+@pytest.mark.parametrize("spec", GROUPED, ids=[s.name for s in GROUPED])
+def test_sequence_groups(R, spec):
+    """Without an entropy mask the batch runs in groups of whole sequences that
+    each fit the stored-probability buffer (a buffer of two sequences here:
+    groups of 2, 2 and 1 or 2): per group the forward with stores, the loss
+    stage's additive sums (with the whole batch's B: GMPO's mean over
+    sequences, GSPO's clipped fraction) and the stored backward; dW and db add
+    up over the groups.  Against the oracle, the one-pass call, and the
+    recompute; per-token outputs through the groups; repeated calls bit-identical."""
+    case = Case(spec)
+    chunk = 2 * spec.T
+    a, res = _check(R, case, per_token=False, chunk_rows=chunk)
+    tiles = R.rlloss_get_forward_tiles(a["workspace"])
+    assert tiles == spec.N // 256
+    assert R.rlloss_get_stored_rows(a["workspace"]) == spec.N
+    assert R.rlloss_get_backward_rows(a["workspace"]) == 0
+    b, _ = _check(R, case, per_token=False)   # one pass: the whole batch fits the default buffer
+    c, _ = _check(R, case, per_token=False, chunk_rows=chunk, flags=R.FLAG_RECOMPUTE)
+    for o in (b, c):
+        assert abs(a["loss"].item() - o["loss"].item()) <= 1e-6 * abs(o["loss"].item()) + 1e-9
+        assert torch.allclose(a["metrics"], o["metrics"], rtol=1e-6, atol=1e-7, equal_nan=True)
+        _close(a, o)
+    d, _ = _check(R, case, per_token=True, chunk_rows=chunk)
+    a2 = case.run_gpu(R, per_token=False, chunk_rows=chunk)
+    for k in ("loss", "metrics", "dX", "dW") + (("db",) if spec.has_bias else ()):
+        assert torch.equal(a[k].view(torch.int32), a2[k].view(torch.int32)), k
