@@ -509,6 +509,7 @@ def measure(args, index, dev, world, rank, local):
     status = R.rlloss_get_device_status(ws)
     bwd_rows = R.rlloss_get_backward_rows(ws)   # recomputed rows with c_n != 0
     st_rows = R.rlloss_get_stored_rows(ws)      # rows whose dX, dW came from the stored probabilities
+    st_pos = R.rlloss_get_stored_positions(ws)  # buffer rows those dX, dW ran over (taken 128-row blocks)
     # rows the forward computed: whole row tiles holding an unmasked row
     fwd_rows = min(N, R.rlloss_get_forward_tiles(ws) * (128 if (cfg.flags & R.FLAG_SINGLE_CTA_TILES) else 256))
     if status != 0:
@@ -646,9 +647,9 @@ def measure(args, index, dev, world, rank, local):
     per_step = [m / args.steps for m in phase_ms]
     # tensor-core phases and the flop they execute per step: the forward over
     # its rows, the recompute over the recomputed rows, dX/dW over those and
-    # the stored rows
+    # the stored-probability blocks' rows
     gemm_phases = {0: ("fwd_gemm", 2.0 * fwd_rows), 2: ("bwd_dlogits", 2.0 * bwd_rows),
-                   3: ("bwd_dX_dW", 4.0 * (bwd_rows + st_rows))}
+                   3: ("bwd_dX_dW", 4.0 * (bwd_rows + st_pos))}
     dom = max(gemm_phases, key=lambda k: per_step[k])
     flops_phase = gemm_phases[dom][1] * H * V
     launches_per_step = max(1, phase_n[dom] // args.steps)
@@ -664,7 +665,7 @@ def measure(args, index, dev, world, rank, local):
                 "peak_source": f"{peak_src} bf16 burst", "frac_of_sustained": achieved / peak_sus,
                 "launches_per_step": launches_per_step}
     step_tflops = 6.0 * N * H * V / (ms_step / 1e3) / 1e12
-    executed_tflops = (2.0 * fwd_rows + 4.0 * st_rows + 6.0 * bwd_rows) * H * V / (ms_step / 1e3) / 1e12
+    executed_tflops = (2.0 * fwd_rows + 4.0 * st_pos + 6.0 * bwd_rows) * H * V / (ms_step / 1e3) / 1e12
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -675,6 +676,7 @@ def measure(args, index, dev, world, rank, local):
             "forward_rows": fwd_rows,
             "backward_rows": bwd_rows,
             "stored_rows": st_rows,
+            "stored_block_rows": st_pos,
             "executed_tflops": executed_tflops,
             "executed_peak_frac": executed_tflops / peak,
             "roofline": roofline,

@@ -185,7 +185,9 @@ size_t rlloss_loss_workspace_bytes(const rlloss_cfg* cfg);
  * multiple of 256, a batch larger than that buffer runs in groups of whole
  * sequences that fit it (sequences are coupled only through B and sums), so
  * every row's probabilities are stored; the results equal the one-pass call
- * up to fp32 summation order.  RLLOSS_FLAG_RECOMPUTE recomputes every row. */
+ * up to fp32 summation order.  The stored-probability dX and dW run over the
+ * 128-row blocks of the buffer that hold a row with c_n != 0 (its other rows
+ * with zero factors).  RLLOSS_FLAG_RECOMPUTE recomputes every row. */
 int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const void* b,
                    const int64_t* targets, const float* old_logp, const float* ref_logp,
                    const float* adv, const uint8_t* mask, float* out_loss, float* out_metrics,
@@ -425,14 +427,23 @@ int rlloss_get_device_status(const void* workspace, int32_t* status);
 int rlloss_get_backward_rows(const void* workspace, int32_t* rows);
 
 /* Copy into *rows the number of rows the last rlloss_fwd_bwd on ``workspace``
- * formed dX and dW for from the forward's stored probabilities (whole
- * 256-row tiles, rows with c_n = 0 included; 0 under RLLOSS_FLAG_RECOMPUTE,
- * with a bias, fp32 operands or ACCUMULATE).  The rows counted by
- * rlloss_get_backward_rows are the others, recomputed.  Synchronous; call
+ * formed dX and dW for from the forward's stored probabilities (rows with
+ * c_n != 0; 0 under RLLOSS_FLAG_RECOMPUTE, with fp32 operands or
+ * ACCUMULATE).  The rows counted by rlloss_get_backward_rows are the others
+ * with c_n != 0, recomputed.  Synchronous; call
  * after the stream has finished.  Returns RLLOSS_ECUDA if the copy failed.
  * (Our addition, for reporting executed work; the pages have no
  * counterpart.) */
 int rlloss_get_stored_rows(const void* workspace, int32_t* rows);
+
+/* Copy into *rows the number of buffer rows the stored-probability dX and dW
+ * of the last rlloss_fwd_bwd on ``workspace`` ran over: whole 128-row blocks
+ * of the stored-probability buffer holding a row counted by
+ * rlloss_get_stored_rows (so at least that count, and a multiple of 128 per
+ * sequence group).  Synchronous; call after the stream has finished.  Returns
+ * RLLOSS_ECUDA if the copy failed.  (Our addition, for reporting executed
+ * work; the pages have no counterpart.) */
+int rlloss_get_stored_positions(const void* workspace, int32_t* rows);
 
 /* Copy into *tiles the number of row tiles (256 rows each, 128 with
  * RLLOSS_FLAG_SINGLE_CTA_TILES) the last forward on ``workspace`` computed:

@@ -22,11 +22,13 @@ using namespace rl;
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
 // Status region (first 256 bytes of every workspace): [0] device status word,
 // [4] loss-stage batch ticket, [8] compaction ticket, [12] backward rows,
-// [16] tile-scan ticket, [20] forward row tiles, [24] forward vocabulary segments.
+// [16] tile-scan ticket, [20] forward row tiles, [24] forward vocabulary segments,
+// [28] stored-probability kept rows, [32] its ticket, [36] its positions.
 constexpr size_t kBackwardRowsOffset = 12;
 constexpr size_t kTileTicketOffset = 16, kFwdTilesOffset = 20, kFwdSegmentsOffset = 24;
-constexpr size_t kStoredRowsOffset = 28;   // rows the stored-probability backward ran over
-constexpr size_t kStoredValidOffset = 32;  // of those, rows with a nonzero coefficient
+constexpr size_t kStoredRowsOffset = 28;   // kept rows of the stored-probability backward
+constexpr size_t kStoredTicketOffset = 32;
+constexpr size_t kStoredPositionsOffset = 36;   // rows it ran over (taken 128-row blocks)
 constexpr size_t kPartialCapBytes = size_t(64) << 20;
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
@@ -291,7 +293,7 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
     p.o_tlist = take(size_t(Rr) * 4);
     if (p.compact) {
       p.Ncap = int(rup(Nr, 256));
-      p.o_blk = take(size_t(compact_groups(int(Nr))) * 2 * 4);
+      p.o_blk = take(size_t(compact_groups(int(std::max<long long>(Nr, (long long)p.pu_tiles * 256)))) * 2 * 4);
       p.o_cidx = take(size_t(p.Ncap) * 4);
       p.o_coefc = take(size_t(p.Ncap) * 4);
       p.o_lse2c = take(size_t(p.Ncap) * 4);
@@ -696,22 +698,28 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     sp.xs = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
     sp.xs_ld = p.xs_ld;
     sp.xcol = p.bias ? p.H : -1;
+    sp.rows = reinterpret_cast<int*>(ws + p.o_lse2c);   // buffer row by position
     sp.idx = reinterpret_cast<int*>(ws + p.o_cidx);
     sp.k2 = reinterpret_cast<float*>(ws + p.o_coefc);
     sp.err = err;
     sp.tgt = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
+    sp.blk_cnt = reinterpret_cast<int*>(ws + p.o_blk);
+    sp.blk_off = sp.blk_cnt + compact_groups(pu_rows);
+    sp.ticket = reinterpret_cast<unsigned int*>(ws + p.o_status + kStoredTicketOffset);
     sp.done = done;
-    sp.rows_total = srows;
-    sp.rows_valid = reinterpret_cast<int*>(ws + p.o_status + kStoredValidOffset);
+    sp.kept = srows;
+    sp.positions = reinterpret_cast<int*>(ws + p.o_status + kStoredPositionsOffset);
     {
       Phase ph(st, 5);
       RL_TRY(cudaMemsetAsync(dX, 0, size_t(p.N) * p.H * 4, st));
       RL_TRY(cudaMemsetAsync(done, 0, size_t(p.N), st));   // rows_valid: zeroed with the status block
       RL_TRY(launch_stored_rows(sp, st));
-      ph.launched(1);
+      ph.launched(2);
     }
     HParams hp{};
     set_bwd_segments(hp, p);
+    // both problems read their A rows (the stored probabilities) by position
+    hp.row_map = sp.rows;
     if (!tmap_bf16(&hp.tmA[0], pu, p.V, pu_rows, p.ld_dl, 128)) return RLLOSS_ECUDA;
     if (!tmap_bf16(&hp.tmB[0], hd.Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
     if (!tmap_f32_out(&hp.tmO[0], dX, p.H, p.N)) return RLLOSS_ECUDA;   // unused: rows go through dx_idx
@@ -745,8 +753,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     hp.nprob = 2;
     const int kx = px.kb_per_seg / px.ksplit, kw = pw.kb_per_seg;
     hp.d_tiles = std::max(1, (kx + kw / 2) / kw);
-    hp.rows_total = srows;
-    hp.rows_valid = sp.rows_valid;   // all coefficients 0 (e.g. a clipped GSPO sequence): nothing to add
+    hp.rows_total = sp.positions;   // 0: e.g. a clipped GSPO sequence, nothing to add
     hp.n0 = 0;
     hp.nc_max = pu_rows;
     hp.status = status;
@@ -1027,6 +1034,12 @@ int rlloss_get_stored_rows(const void* workspace, int32_t* rows) {
                             cudaMemcpyDeviceToHost));
 }
 
+int rlloss_get_stored_positions(const void* workspace, int32_t* rows) {
+  if (!workspace || !rows) return RLLOSS_EINVAL;
+  return cuda_rc(cudaMemcpy(rows, static_cast<const char*>(workspace) + kStoredPositionsOffset, sizeof(int32_t),
+                            cudaMemcpyDeviceToHost));
+}
+
 int rlloss_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* stream) {
   if (!workspace || !aligned(workspace, 256)) return RLLOSS_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1249,9 +1262,10 @@ int rlloss_fwd_bwd(const rlloss_cfg* cfg, const void* X, const void* W, const vo
     // group); then loss and metrics from the groups' sums.
     double* sums = reinterpret_cast<double*>(ws + p.o_sums);
     int* counters = reinterpret_cast<int*>(ws + p.o_sums + size_t(p.ngroups) * 64);
-    int* ctr_dev[3] = {reinterpret_cast<int*>(ws + p.o_status + kFwdTilesOffset),
+    int* ctr_dev[4] = {reinterpret_cast<int*>(ws + p.o_status + kFwdTilesOffset),
                        reinterpret_cast<int*>(ws + p.o_status + kStoredRowsOffset),
-                       reinterpret_cast<int*>(ws + p.o_status + kBackwardRowsOffset)};
+                       reinterpret_cast<int*>(ws + p.o_status + kBackwardRowsOffset),
+                       reinterpret_cast<int*>(ws + p.o_status + kStoredPositionsOffset)};
     RL_TRY(cudaMemsetAsync(counters, 0, 16, st));
     const size_t xrow = size_t(cfg->H) * 2;   // bf16 row bytes
     for (int g = 0; g < p.ngroups; ++g) {

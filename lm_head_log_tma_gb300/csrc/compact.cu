@@ -193,95 +193,188 @@ __global__ void scatter_rows_kernel(const float4* src, const int* idx, const int
   }
 }
 
-// Block b handles buffer rows [32 b, 32 b + 32) of the stored-probability
-// buffer (see StoredParams): thread r < 32 forms row 32 b + r's factors and
-// writes its target entry into the buffer; then all threads write the scaled
-// X rows (16-byte words).
-__global__ void __launch_bounds__(kCompactBlock) stored_rows_kernel(StoredParams p) {
+// Stored-probability rows (see StoredParams) in blocks of kStoredBlock buffer
+// rows: a block that holds a kept row is taken whole, in buffer order, its
+// other rows with zero factors; a block without one is left out.  The count
+// kernel marks every 32-row group with its block's decision and its kept rows
+// (packed: marked << 16 | kept); the block that finishes last turns the marks
+// into positions and fills the tail up to a whole 256-row tile; then every
+// marked group writes its rows at their positions.
+constexpr int kStoredBlock = 128;
+static_assert(kCompactBlock % kStoredBlock == 0 && kStoredBlock % kGroup == 0, "block split");
+__device__ __forceinline__ int stored_source(const StoredParams& p, int j) {
+  const int slot = j >> 8;
+  return (p.tiles ? p.tiles[slot] : slot) * 256 + (j & 255);
+}
+__device__ __forceinline__ bool stored_keep(const StoredParams& p, int n) {
+  if (n >= p.N) return false;
+  const float l2 = p.lse2[n];
+  const long long y = p.targets[n];
+  return p.coef[n] != 0.f && l2 >= kStoredLse2Min && l2 <= kStoredLse2Max && y >= 0 && y < p.V;
+}
+__device__ __forceinline__ int stored_rows_of(const StoredParams& p) {
+  const int nt = p.tiles ? *p.ntiles : p.R;
+  return min(nt, p.pu_tiles) * 256;
+}
+
+__global__ void __launch_bounds__(kCompactBlock) stored_count_kernel(StoredParams p) {
+  constexpr int kWarps = kCompactBlock / 32, kWarpsPerBlock = kStoredBlock / 32;
+  __shared__ int is_last, kept_sum, first_mark;
+  __shared__ unsigned any[kWarps];
+  __shared__ int part[kCompactBlock];
+  const int rows = stored_rows_of(p);
+  const int j = blockIdx.x * kCompactBlock + threadIdx.x;   // every block of the launch takes part
+  const bool keep = j < rows && stored_keep(p, stored_source(p, j));
+  const unsigned bal = __ballot_sync(0xffffffffu, keep);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) any[w] = bal;
+  __syncthreads();
+  const int ngroups = rows / kGroup;
+  const int grp = j / kGroup;
+  if ((threadIdx.x & 31) == 0 && grp < ngroups) {
+    unsigned a = 0;
+    for (int k = 0; k < kWarpsPerBlock; ++k) a |= any[(w & ~(kWarpsPerBlock - 1)) + k];
+    p.blk_cnt[grp] = (a ? 1 << 16 : 0) | __popc(bal);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    is_last = atomicAdd(p.ticket, 1u) == gridDim.x - 1;
+    if (is_last) __threadfence();
+    kept_sum = 0;
+    first_mark = ngroups;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  const int per = (ngroups + kCompactBlock - 1) / kCompactBlock;
+  int s = 0, kc = 0;
+  for (int k = 0; k < per; ++k) {
+    const int i = threadIdx.x * per + k;
+    if (i < ngroups) {
+      const int v = __ldcg(p.blk_cnt + i);
+      s += v >> 16;
+      kc += v & 0xffff;
+      if ((v >> 16) && i < first_mark) atomicMin(&first_mark, i);
+    }
+  }
+  part[threadIdx.x] = s;
+  if (kc) atomicAdd(&kept_sum, kc);
+  __syncthreads();
+  for (int o = 1; o < kCompactBlock; o <<= 1) {
+    const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int base = threadIdx.x ? part[threadIdx.x - 1] : 0;   // marked groups before
+  for (int k = 0; k < per; ++k) {
+    const int i = threadIdx.x * per + k;
+    if (i < ngroups) {
+      p.blk_off[i] = base * kGroup;
+      base += __ldcg(p.blk_cnt + i) >> 16;
+    }
+  }
+  const int total = part[kCompactBlock - 1] * kGroup;   // positions: a multiple of kStoredBlock
+  if (threadIdx.x == 0) {
+    *p.kept = kept_sum;
+    *p.positions = total;
+  }
+  // positions past the taken blocks read the first taken block (finite
+  // probabilities) against zero X rows and drop their dX rows
+  const int fill = first_mark < ngroups ? first_mark * kGroup : 0;
+  const int tail_end = min((total + 255) / 256 * 256, p.rows_cap);
+  if (threadIdx.x == 0 && tail_end > total) p.rows[total / kStoredBlock] = fill;
+  for (int r = total + threadIdx.x; r < tail_end; r += kCompactBlock) {
+    p.idx[r] = -1;
+    p.k2[r] = 0.f;
+    p.err[r] = 0.f;
+    p.tgt[r] = -1;
+  }
+  const int words = p.xs_ld / 8;
+  const long long tail_words = (long long)(tail_end - total) * words;
+  for (long long w2 = threadIdx.x; w2 < tail_words; w2 += kCompactBlock) {
+    const long long r = total + w2 / words;
+    reinterpret_cast<uint4*>(p.xs + r * p.xs_ld)[w2 % words] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__global__ void __launch_bounds__(kCompactBlock) stored_gather_kernel(StoredParams p) {
   __shared__ int src_row[kGroup];
   __shared__ float scale[kGroup];
-  const int nt = p.tiles ? *p.ntiles : p.R;
-  const int rows = min(nt, p.pu_tiles) * 256;
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.rows_total = rows;
-  const int words = p.H / 8;   // 16-byte words per row
-  for (int j0 = int(blockIdx.x) * kGroup; j0 < rows; j0 += int(gridDim.x) * kGroup) {
-    if (threadIdx.x < kGroup) {
-      const int j = j0 + int(threadIdx.x);
-      const int slot = j >> 8;
-      const int n = (p.tiles ? p.tiles[slot] : slot) * 256 + (j & 255);
-      bool ok = false;
-      float k2 = 0.f, er = 0.f;
-      long long y = -1;
-      if (n < p.N) {
-        const float cf = p.coef[n];
-        const float l2 = p.lse2[n];
-        y = p.targets[n];
-        if (cf != 0.f && l2 >= kStoredLse2Min && l2 <= kStoredLse2Max && y >= 0 && y < p.V) {
-          // G = (c/tau)(onehot - p) with p = pu 2^-lse2: off the target G = k2 pu,
-          // at the target k1 = (c/tau)(1 - p_y), 1 - p_y = -expm1(logp)
-          const double k2d = -double(cf) * exp2(-double(l2));
-          const double k1d = double(cf) * -expm1(p.logp64[n]);
-          const __nv_bfloat16 tv = __float2bfloat16_rn(float(k1d / k2d));
-          k2 = float(k2d);
-          er = float(k1d - k2d * double(__bfloat162float(tv)));
-          p.pu[size_t(j) * p.pu_ld + size_t(y)] = tv;
-          ok = true;
-        }
-      }
-      p.idx[j] = ok ? n : -1;
-      p.k2[j] = k2;
-      p.err[j] = er;
-      p.tgt[j] = ok ? y : -1;
-      if (ok) p.done[n] = 1;
-      src_row[threadIdx.x] = ok ? n : -1;
-      scale[threadIdx.x] = k2;
-      const unsigned kept = __ballot_sync(0xffffffffu, ok);
-      if (threadIdx.x == 0 && kept) atomicAdd(p.rows_valid, __popc(kept));
+  const int g = blockIdx.x;
+  const int rows = stored_rows_of(p);
+  if (g * kGroup >= rows || !(p.blk_cnt[g] >> 16)) return;   // uniform over the block
+  const int base = p.blk_off[g];
+  if (threadIdx.x < kGroup) {
+    const int j = g * kGroup + int(threadIdx.x);
+    const int n = stored_source(p, j);
+    const bool keep = stored_keep(p, n);
+    const int pos = base + int(threadIdx.x);   // < positions <= stored rows <= rows_cap
+    float k2 = 0.f, er = 0.f;
+    long long y = -1;
+    if (keep) {
+      // G = (c/tau)(onehot - p) with p = pu 2^-lse2: off the target G = k2 pu,
+      // at the target k1 = (c/tau)(1 - p_y), 1 - p_y = -expm1(logp)
+      const float cf = p.coef[n];
+      y = p.targets[n];
+      const double k2d = -double(cf) * exp2(-double(p.lse2[n]));
+      const double k1d = double(cf) * -expm1(p.logp64[n]);
+      const __nv_bfloat16 tv = __float2bfloat16_rn(float(k1d / k2d));
+      k2 = float(k2d);
+      er = float(k1d - k2d * double(__bfloat162float(tv)));
+      p.pu[size_t(j) * p.pu_ld + size_t(y)] = tv;
+      p.done[n] = 1;
     }
-    __syncthreads();
-    const int owords = p.xs_ld / 8;   // words per row of xs (one more with the db column)
-    for (int w = int(threadIdx.x); w < kGroup * owords; w += kCompactBlock) {
-      const int r = w / owords, c = w - r * owords;
-      const int n = src_row[r];
-      uint4 out = make_uint4(0u, 0u, 0u, 0u);
-      if (c >= words) {   // the db column (k2 in its first element), zeros after it
-        if (n >= 0 && c == words && p.xcol >= 0) {
-          const __nv_bfloat162 k2p = __floats2bfloat162_rn(scale[r], 0.f);
-          out.x = *reinterpret_cast<const uint32_t*>(&k2p);
-        }
-      } else if (n >= 0) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.x + size_t(n) * p.H) + c);
-        const float k2 = scale[r];
-        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-        uint32_t o[4];
+    if (threadIdx.x == 0 && pos % kStoredBlock == 0) p.rows[pos / kStoredBlock] = j;
+    p.idx[pos] = keep ? n : -1;
+    p.k2[pos] = k2;
+    p.err[pos] = er;
+    p.tgt[pos] = y;
+    src_row[threadIdx.x] = keep ? n : -1;
+    scale[threadIdx.x] = k2;
+  }
+  __syncthreads();
+  const int words = p.H / 8;          // 16-byte words of an X row
+  const int owords = p.xs_ld / 8;     // of an xs row (one more with the db column)
+  for (int w = int(threadIdx.x); w < kGroup * owords; w += kCompactBlock) {
+    const int r = w / owords, c = w - r * owords;
+    const int n = src_row[r];
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (n < 0) {
+      // a row left out inside a taken block: zero X~ row (and db column)
+    } else if (c < words) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.x + size_t(n) * p.H) + c);
+      const float k2 = scale[r];
+      const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&in[k]);
-          const __nv_bfloat162 r2 = __floats2bfloat162_rn(k2 * __low2float(b2), k2 * __high2float(b2));
-          o[k] = *reinterpret_cast<const uint32_t*>(&r2);
-        }
-        out = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&in[k]);
+        const __nv_bfloat162 r2 = __floats2bfloat162_rn(k2 * __low2float(b2), k2 * __high2float(b2));
+        o[k] = *reinterpret_cast<const uint32_t*>(&r2);
       }
-      reinterpret_cast<uint4*>(p.xs + size_t(j0 + r) * p.xs_ld)[c] = out;
+      out = make_uint4(o[0], o[1], o[2], o[3]);
+    } else if (c == words && p.xcol >= 0) {   // the db column: k2, zeros after it
+      const __nv_bfloat162 k2p = __floats2bfloat162_rn(scale[r], 0.f);
+      out.x = *reinterpret_cast<const uint32_t*>(&k2p);
     }
-    __syncthreads();
+    reinterpret_cast<uint4*>(p.xs + size_t(base + r) * p.xs_ld)[c] = out;
   }
 }
 
 cudaError_t launch_stored_rows(const StoredParams& p, cudaStream_t st) {
-  long long blocks = (p.rows_cap + kGroup - 1) / kGroup;
-  if (blocks > 4096) blocks = 4096;
-  if (blocks < 1) blocks = 1;
-  stored_rows_kernel<<<int(blocks), kCompactBlock, 0, st>>>(p);
+  const int blocks = (p.rows_cap + kCompactBlock - 1) / kCompactBlock;
+  stored_count_kernel<<<blocks > 0 ? blocks : 1, kCompactBlock, 0, st>>>(p);
+  stored_gather_kernel<<<(p.rows_cap + kGroup - 1) / kGroup, kCompactBlock, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 // Row counters of a call run in groups: acc[k] += *c[k] after each group, and
 // *c[k] = acc[k] after the last (what the counter queries then report).
-__global__ void counters_kernel(int* c0, int* c1, int* c2, int* acc, int write_back) {
+__global__ void counters_kernel(int* c0, int* c1, int* c2, int* c3, int* acc, int write_back) {
   if (threadIdx.x != 0) return;
-  int* c[3] = {c0, c1, c2};
-  for (int k = 0; k < 3; ++k) {
+  int* c[4] = {c0, c1, c2, c3};
+  for (int k = 0; k < 4; ++k) {
     if (write_back)
       *c[k] = acc[k];
     else
@@ -289,8 +382,8 @@ __global__ void counters_kernel(int* c0, int* c1, int* c2, int* acc, int write_b
   }
 }
 
-cudaError_t launch_counters(int* const (&c)[3], int* acc, bool write_back, cudaStream_t st) {
-  counters_kernel<<<1, 32, 0, st>>>(c[0], c[1], c[2], acc, write_back ? 1 : 0);
+cudaError_t launch_counters(int* const (&c)[4], int* acc, bool write_back, cudaStream_t st) {
+  counters_kernel<<<1, 32, 0, st>>>(c[0], c[1], c[2], c[3], acc, write_back ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -309,54 +309,19 @@ struct FwdPolicy {
         for (int i = 0; i < 32; ++i)
           if (c0 + i >= p.V) v[i] = -INFINITY;
       }
-      // Reference m: an integer in log2 units, from the first chunk's maximum
-      // of this row's vocabulary range.  Later chunks are exponentiated against
-      // it; only a chunk whose sum leaves the range fp32 keeps exact (2^64, or
-      // not finite) takes its maximum, moves m up by a power of two (an exact
-      // rescale of the sums) and is redone.  Sums of terms up to 2^64 stay
-      // exact to the compensated accumulation, and the segment merge takes
-      // any integer reference.
-      auto chunk_max = [&]() {
-        float mx = v[0];
+      float mx = v[0];
 #pragma unroll
-        for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
-        return mx * mul;   // mul > 0
-      };
-      if (e.mref == -INFINITY) e.mref = ceilf(chunk_max());
-      // ST: 2^t = 2^(t - m) 2^m exactly (m an integer); m is capped at 100, past
-      // which the backward recomputes the row anyway, and 2^m below 2^-126
-      // is taken as 0 (such a column's p is below 2^-46 in any row the
-      // stored path keeps)
-      uint32_t pk[ST ? 16 : 1];
-      float s0, s1, s2, s3, w0, w1, w2, w3;
-      auto exponentiate = [&]() {
-        float psc = 0.f;
-        if constexpr (ST) {
-          const float mr = fminf(e.mref, 100.f);
-          psc = mr >= -126.f ? __int_as_float((int(mr) + 127) << 23) : 0.f;
-        }
-        s0 = s1 = s2 = s3 = w0 = w1 = w2 = w3 = 0.f;
-        const float nm = -e.mref;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          float d0 = fmaf(v[i], mul, nm), d1 = fmaf(v[i + 1], mul, nm), d2 = fmaf(v[i + 2], mul, nm),
-                d3 = fmaf(v[i + 3], mul, nm);
-          if (tail) {   // -inf -> a finite large negative: 2^d = 0 and 0 * d = 0
-            d0 = fmaxf(d0, -1.0e30f); d1 = fmaxf(d1, -1.0e30f); d2 = fmaxf(d2, -1.0e30f); d3 = fmaxf(d3, -1.0e30f);
-          }
-          const float x0 = ex2_approx(d0), x1 = ex2_approx(d1), x2 = ex2_approx(d2), x3 = ex2_approx(d3);
-          s0 += x0; s1 += x1; s2 += x2; s3 += x3;
-          w0 = fmaf(x0, d0, w0); w1 = fmaf(x1, d1, w1); w2 = fmaf(x2, d2, w2); w3 = fmaf(x3, d3, w3);
-          if constexpr (ST) {
-            pk[i / 2] = pack_bf16x2(x0 * psc, x1 * psc);
-            pk[i / 2 + 1] = pack_bf16x2(x2 * psc, x3 * psc);
-          }
-        }
-      };
-      exponentiate();
-      if (!((s0 + s1) + (s2 + s3) <= 18446744073709551616.f)) {   // 2^64; NaN fails the test too
-        const float nref = ceilf(chunk_max());
-        if (nref > e.mref) {
+      for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
+      mx *= mul;   // mul > 0
+      // Reference max kept on an integer grid in log2 units; move it only
+      // when a logit would exceed it by more than 2^16, so rescaling is rare
+      // and exact (a power of two).  (Every 2^(t - m) then stays <= 2^16, which
+      // also bounds the stored 2^t below, 2^(16 + 100), for any row.)
+      if (mx > e.mref + 16.f) {
+        const float nref = ceilf(mx);
+        if (e.mref == -INFINITY) {
+          e.mref = nref;
+        } else {
           const float dd = e.mref - nref;     // negative integer
           const int di = int(dd);
           e.w_hi = ldexpf(e.w_hi + dd * e.s_hi, di);
@@ -364,7 +329,33 @@ struct FwdPolicy {
           e.s_hi = ldexpf(e.s_hi, di);
           e.s_lo = ldexpf(e.s_lo, di);
           e.mref = nref;
-          exponentiate();
+        }
+      }
+      // ST: 2^t = 2^(t - m) 2^m exactly (m an integer); m is capped at 100, past
+      // which the backward recomputes the row anyway (its stored values stay
+      // finite, below 2^116), and 2^m below 2^-126 is taken as 0 (such a
+      // column's p is below 2^-46 in any row the stored path keeps)
+      float psc = 0.f;
+      if constexpr (ST) {
+        const float mr = fminf(e.mref, 100.f);
+        psc = mr >= -126.f ? __int_as_float((int(mr) + 127) << 23) : 0.f;
+      }
+      uint32_t pk[ST ? 16 : 1];
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float nm = -e.mref;
+        float d0 = fmaf(v[i], mul, nm), d1 = fmaf(v[i + 1], mul, nm), d2 = fmaf(v[i + 2], mul, nm),
+              d3 = fmaf(v[i + 3], mul, nm);
+        if (tail) {   // -inf -> a finite large negative: 2^d = 0 and 0 * d = 0
+          d0 = fmaxf(d0, -1.0e30f); d1 = fmaxf(d1, -1.0e30f); d2 = fmaxf(d2, -1.0e30f); d3 = fmaxf(d3, -1.0e30f);
+        }
+        const float x0 = ex2_approx(d0), x1 = ex2_approx(d1), x2 = ex2_approx(d2), x3 = ex2_approx(d3);
+        s0 += x0; s1 += x1; s2 += x2; s3 += x3;
+        w0 = fmaf(x0, d0, w0); w1 = fmaf(x1, d1, w1); w2 = fmaf(x2, d2, w2); w3 = fmaf(x3, d3, w3);
+        if constexpr (ST) {
+          pk[i / 2] = pack_bf16x2(x0 * psc, x1 * psc);
+          pk[i / 2 + 1] = pack_bf16x2(x2 * psc, x3 * psc);
         }
       }
       two_sum_acc(e.s_hi, e.s_lo, (s0 + s1) + (s2 + s3));
@@ -664,7 +655,7 @@ struct HPolicy {
   // The chunk's row count is read on the device: problem 0 (dX) gets its
   // row tiles from it, problem 1 (dW) its k-blocks per term.
   __device__ static void chunk_problems(const Params& p, HProblem (&pr)[2]) {
-    const int nc = (p.rows_valid && *p.rows_valid == 0) ? 0 : min(max(*p.rows_total - p.n0, 0), p.nc_max);
+    const int nc = min(max(*p.rows_total - p.n0, 0), p.nc_max);
     pr[0] = p.pr[0];
     pr[1] = p.pr[1];
     pr[0].Mt = (nc + 255) / 256;
@@ -736,13 +727,15 @@ struct HPolicy {
     const int s = kb / t.aux;
     const int kk = (kb - s * t.aux) * 64;
     const int r = t.m0 + 128 * int(rank);
-    if (pr.a_mn) {
-      if (tma_x_ok<2>(p.seg_a[s] + r, p.status))
-        tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + r, pr.a_outer0 + kk);
+    if (pr.a_mn) {   // dW: k = A rows (positions) kk..kk+63, this CTA's 128 columns
+      const int pk = pr.a_outer0 + kk;
+      const int y = p.row_map ? __ldg(p.row_map + (pk >> 7)) + (pk & 127) : pk;
+      if (tma_x_ok<2>(p.seg_a[s] + r, p.status)) tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + r, y);
       if (tma_x_ok<2>(p.seg_a[s] + r + 64, p.status))
-        tma_load_2d_pair(&p.tmA[q], bar, st + 8192, p.seg_a[s] + r + 64, pr.a_outer0 + kk);
-    } else {
-      if (tma_x_ok<2>(p.seg_a[s] + kk, p.status)) tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + kk, r);
+        tma_load_2d_pair(&p.tmA[q], bar, st + 8192, p.seg_a[s] + r + 64, y);
+    } else {         // dX: this CTA's 128 A rows (positions r..r+127), k = columns kk..kk+63
+      const int y = p.row_map ? __ldg(p.row_map + (r >> 7)) : r;
+      if (tma_x_ok<2>(p.seg_a[s] + kk, p.status)) tma_load_2d_pair(&p.tmA[q], bar, st, p.seg_a[s] + kk, y);
     }
 #pragma unroll
     for (int sub = 0; sub < 2; ++sub) {

@@ -125,6 +125,11 @@ struct HProblem {
 };
 struct HParams {
   CUtensorMap tmA[2];         // K-major: inner k, box 64 x 128 | MN-major: inner row, box 64 x 64
+  // Optional (both problems' A operand rows by position): position p is A row
+  // row_map[p / 128] + p % 128 (blocks of 128 positions map to 128 consecutive
+  // rows), so one box of 128 (dX) or 64 (dW k-block) positions is one plain
+  // tile.  row_map covers every block a tile can reach.
+  const int* row_map;
   CUtensorMap tmB[2];         // inner h, outer k, box 64 x 64
   CUtensorMap tmO[2];         // fp32 output: inner h, outer rows, box 32 x 32, 128-byte swizzle
   HProblem pr[2];             // problem 0 must be the K-major one (a_mn = 0) when both run
@@ -133,7 +138,6 @@ struct HParams {
   // Rows of the chunk, read on the device: nc = clamp(*rows_total - n0, 0, nc_max).
   // Problem 0 (dX) has ceil(nc/256) row tiles; problem 1 (dW) ceil(nc/64) k-blocks per term.
   const int* rows_total;
-  const int* rows_valid;      // optional: when it reads 0 the chunk has no rows (all coefficients 0)
   int n0, nc_max;
   int nseg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];  // inner-coordinate offsets of each product term
@@ -241,13 +245,16 @@ struct CompactParams {
 };
 
 // Backward rows of the stored-probability path: buffer row j holds row n of
-// the forward's slot j / 256 (see FwdParams::tmPu).  For a row with c != 0
-// whose lse2 lies in [kStoredLse2Min, kStoredLse2Max]:
+// the forward's slot j / 256 (see FwdParams::tmPu).  A row with c != 0 whose
+// lse2 lies in [kStoredLse2Min, kStoredLse2Max] is kept; kept rows are numbered
+// in buffer order (position p) and get
 //   k2 = -(c/tau) 2^-lse2 (so G = k2 pu off the target, as pu = 2^t),
 //   k1 = (c/tau)(1 - p_y), the target entry of G,
-//   the target entry of pu is set to bf16(k1 / k2) and err = k1 - k2 bf16(k1 / k2),
-//   xs[j] = bf16(k2 X[n]), idx[j] = n, done[n] = 1.
-// Other rows get xs = 0, idx = -1, k2 = err = 0 (they go to the recompute).
+//   the target entry of pu set to bf16(k1 / k2) and err = k1 - k2 bf16(k1 / k2),
+//   rows[p] = j, idx[p] = n, xs[p] = bf16(k2 X[n]) (with xcol set, also k2 in
+//   column H), done[n] = 1.
+// Positions from the kept count up to the next multiple of 256 get rows = 0,
+// idx = -1 and zeros.  Other rows go to the recompute.
 constexpr float kStoredLse2Min = -80.f;
 constexpr float kStoredLse2Max = 96.f;
 struct StoredParams {
@@ -263,20 +270,24 @@ struct StoredParams {
   const __nv_bfloat16* x;     // [N, H]
   __nv_bfloat16* pu;          // [rows_cap, pu_ld]
   int pu_ld;
-  __nv_bfloat16* xs;          // [rows_cap, xs_ld]: k2 X; with xcol set also column H = k2
+  __nv_bfloat16* xs;          // [rows_cap, xs_ld] by position
   int xs_ld, xcol;            // row stride of xs (elements); xcol: H (bias: db through dW's GEMM) or -1
-  int* idx;                   // [rows_cap]
+  int* rows;                  // [rows_cap / 128 + 1] buffer row of each block of 128 positions
+  int* idx;                   // [rows_cap] original row by position, -1 where not kept
   float* k2;                  // [rows_cap]
   float* err;                 // [rows_cap]
   int64_t* tgt;               // [rows_cap]
+  int* blk_cnt;               // [rows_cap / 32] scratch
+  int* blk_off;               // [rows_cap / 32] scratch
+  unsigned int* ticket;       // zeroed before the launch
   uint8_t* done;              // [N], zeroed before the launch
-  int* rows_total;            // out: stored rows (stored tiles * 256)
-  int* rows_valid;            // out: rows with c != 0 among them (zeroed before the launch)
+  int* kept;                  // out: kept rows
+  int* positions;             // out: positions (rows of the taken 128-row blocks)
 };
 cudaError_t launch_stored_rows(const StoredParams& p, cudaStream_t st);
 // Row counters of a call run in groups of sequences: acc[k] += *c[k] (after a
 // group), or *c[k] = acc[k] (after the last).
-cudaError_t launch_counters(int* const (&c)[3], int* acc, bool write_back, cudaStream_t st);
+cudaError_t launch_counters(int* const (&c)[4], int* acc, bool write_back, cudaStream_t st);
 int compact_groups(int N);   // 32-row groups
 // Row tiles of tile_rows rows holding a row with mask != 0: flags[R], their
 // ascending list and count (ticket zeroed before the launch).

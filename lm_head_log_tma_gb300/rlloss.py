@@ -107,6 +107,8 @@ def _load():
     lib.rlloss_get_backward_rows.restype = c_int
     lib.rlloss_get_stored_rows.argtypes = [P, ctypes.POINTER(c_int32)]
     lib.rlloss_get_stored_rows.restype = c_int
+    lib.rlloss_get_stored_positions.argtypes = [P, ctypes.POINTER(c_int32)]
+    lib.rlloss_get_stored_positions.restype = c_int
     lib.rlloss_get_forward_tiles.argtypes = [P, ctypes.POINTER(c_int32)]
     lib.rlloss_get_forward_tiles.restype = c_int
     lib.rlloss_selftest_bounded_wait.argtypes = [P, c_uint64, P]
@@ -292,6 +294,14 @@ def rlloss_get_stored_rows(workspace) -> int:
     rc = lib.rlloss_get_stored_rows(_p(workspace), ctypes.byref(rows))
     if rc != OK:
         raise RllossError(rc, "rlloss_get_stored_rows")
+    return int(rows.value)
+
+
+def rlloss_get_stored_positions(workspace) -> int:
+    rows = c_int32(0)
+    rc = lib.rlloss_get_stored_positions(_p(workspace), ctypes.byref(rows))
+    if rc != OK:
+        raise RllossError(rc, "rlloss_get_stored_positions")
     return int(rows.value)
 
 

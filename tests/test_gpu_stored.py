@@ -63,6 +63,16 @@ def _check(R, case, **kw):
     return out, res
 
 
+def _taken_rows(c, block=128):
+    """Rows the stored-probability dX, dW run over: the 128-row blocks (of the
+    forward's 256-row tiles, so 128-aligned in row order) holding a row with
+    c_n != 0, taken whole."""
+    nz = np.asarray(c) != 0
+    pad = (-len(nz)) % block
+    nz = np.concatenate([nz, np.zeros(pad, bool)])
+    return int(nz.reshape(-1, block).any(axis=1).sum()) * block
+
+
 def _close(a, b):
     for k in ("dX", "dW", "db"):
         if a.get(k) is None:
@@ -82,8 +92,8 @@ def test_stored_backward_matches_recompute_and_oracle(R, spec):
     for k in ("loss", "metrics"):
         assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), k
     kept = int((res.c != 0).sum())
-    tiles = R.rlloss_get_forward_tiles(a["workspace"])
-    assert R.rlloss_get_stored_rows(a["workspace"]) == 256 * tiles
+    assert R.rlloss_get_stored_rows(a["workspace"]) == kept
+    assert R.rlloss_get_stored_positions(a["workspace"]) == _taken_rows(res.c)
     assert R.rlloss_get_backward_rows(a["workspace"]) == 0
     assert R.rlloss_get_stored_rows(b["workspace"]) == 0
     assert R.rlloss_get_backward_rows(b["workspace"]) == kept
@@ -96,7 +106,8 @@ def test_stored_with_per_token_outputs_runs_every_tile(R):
     the stored rows are then every tile's, and the result still matches."""
     case = Case(SPECS[0])
     a, res = _check(R, case, per_token=True)
-    assert R.rlloss_get_stored_rows(a["workspace"]) == 256 * ((SPECS[0].N + 255) // 256)
+    assert R.rlloss_get_stored_rows(a["workspace"]) == int((res.c != 0).sum())
+    assert R.rlloss_get_stored_positions(a["workspace"]) == _taken_rows(res.c)
 
 
 def test_stored_and_recomputed_rows_in_one_call(R):
@@ -106,8 +117,8 @@ def test_stored_and_recomputed_rows_in_one_call(R):
     spec = SPECS[0]
     case = Case(spec)
     a, res = _check(R, case, per_token=False, chunk_rows=256)
-    assert R.rlloss_get_stored_rows(a["workspace"]) == 256
     c = res.c != 0
+    assert R.rlloss_get_stored_rows(a["workspace"]) == int(c[:256].sum())
     assert R.rlloss_get_backward_rows(a["workspace"]) == int(c[256:].sum()) > 0
     b, _ = _check(R, case, per_token=False, chunk_rows=256, flags=R.FLAG_RECOMPUTE)
     _close(a, b)
@@ -130,6 +141,38 @@ def test_rows_outside_the_stored_range_are_recomputed(R):
     assert R.rlloss_get_backward_rows(a["workspace"]) == kept_big
     rows = torch.from_numpy(big[res.c[big] != 0]).cuda()
     assert torch.count_nonzero(a["dX"][rows]) > 0
+
+
+BLOCKS = [
+    # prompt of 200 rows: in the first 256-row tile the first 128-row block has
+    # no kept row (left out), the second has some; three blocks taken, so the
+    # last dX tile is half tail
+    Workload("blocks_prompt200", B=1, T=512, H=192, V=900, dtype="bf16", prompt_len=200, seed=221),
+    # whole sequences clipped (GSPO, tight bounds): their blocks are left out
+    Workload("blocks_gspo_clipped", B=4, T=256, H=128, V=700, dtype="bf16", loss_type=GSPO_TOKEN,
+             eps_low=3e-4, eps_high=4e-4, prompt_len=130, old_noise_std=0.02, seed=222),
+    # with a bias (db through dW's GEMM): one taken block per sequence, three in all
+    Workload("blocks_bias_prompt330", B=3, T=384, H=256, V=800, dtype="bf16", has_bias=True, bias_std=0.2,
+             prompt_len=330, seed=223),
+]
+
+
+@pytest.mark.parametrize("spec", BLOCKS, ids=[s.name for s in BLOCKS])
+def test_blocks_without_kept_rows_are_left_out(R, spec):
+    """The stored-probability dX and dW skip 128-row blocks whose rows all have
+    c_n = 0 and run a taken block whole, its other rows with zero factors
+    (positions past the last taken block read the first one against zero X
+    rows); the result passes the oracle and matches the recompute, and the
+    rows run over are exactly the taken blocks'."""
+    case = Case(spec)
+    a, res = _check(R, case, per_token=False)
+    b, _ = _check(R, case, per_token=False, flags=R.FLAG_RECOMPUTE)
+    taken = _taken_rows(res.c)
+    assert taken < spec.N
+    assert R.rlloss_get_stored_positions(a["workspace"]) == taken
+    assert R.rlloss_get_stored_rows(a["workspace"]) == int((res.c != 0).sum())
+    assert torch.count_nonzero(a["dX"][torch.from_numpy(res.c == 0).cuda()]) == 0
+    _close(a, b)
 
 
 def test_stored_calls_are_bit_identical(R):
@@ -165,7 +208,8 @@ def test_sequence_groups(R, spec):
     a, res = _check(R, case, per_token=False, chunk_rows=chunk)
     tiles = R.rlloss_get_forward_tiles(a["workspace"])
     assert tiles == spec.N // 256
-    assert R.rlloss_get_stored_rows(a["workspace"]) == spec.N
+    assert R.rlloss_get_stored_rows(a["workspace"]) == int((res.c != 0).sum())
+    assert R.rlloss_get_stored_positions(a["workspace"]) == _taken_rows(res.c)   # groups start 128-aligned
     assert R.rlloss_get_backward_rows(a["workspace"]) == 0
     b, _ = _check(R, case, per_token=False)   # one pass: the whole batch fits the default buffer
     c, _ = _check(R, case, per_token=False, chunk_rows=chunk, flags=R.FLAG_RECOMPUTE)
