@@ -581,8 +581,8 @@ int run_head(const rlloss_cfg* cfg, const Plan& p, const void* X, const void* W,
   fp.targets = targets;
   fp.v_begin = v_begin;
   if (p.stored) {
-    if (!tmap_bf16_box(&fp.tmPu, ws + p.o_dl, p.V, (long long)p.pu_tiles * 256, p.ld_dl, 64, 32,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!tmap_bf16_box(&fp.tmPu, ws + p.o_dl, p.V, (long long)p.pu_tiles * 256, p.ld_dl, 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B))
       return RLLOSS_ECUDA;
     fp.pu_tiles = p.pu_tiles;
   }

@@ -106,7 +106,7 @@ struct FwdPolicy {
   static constexpr int kBBytes = (256 / PAIR) * 128 * KBX;   // this CTA's share of the B rows
   static constexpr int kColBytes = 2 * 128 * 4;   // per epilogue warp: its 128 columns' W scales and biases
   // ST: one 32 x 64 staging box per epilogue warp instead (no bias, no scales)
-  static constexpr int kExtraSmem = ST ? kEpiWarps * kBf16Box64Bytes : kEpiWarps * kColBytes;
+  static constexpr int kExtraSmem = ST ? kEpiWarps * 2 * kBf16BoxBytes : kEpiWarps * kColBytes;
   static_assert(!ST || (CL == 2 && !F8), "stored probabilities: bf16 CTA-pair forward");
   static constexpr uint32_t kIdesc = F8 ? idesc_e4m3(kRows, 256) : idesc_bf16(kRows, 256, 0, 0);
   static constexpr int kKB = (F8 ? 128 : 64) * KBX;   // K elements per k-block
@@ -121,6 +121,7 @@ struct FwdPolicy {
     float4 pw, pb;
     int pre_n0 = -1;       // tile whose columns pw / pb hold
     int R = -1, P = 0;     // launch shape (for the next tile's columns)
+    int nbuf = 0;          // ST: staging boxes used so far (two alternate)
   };
 
   // Row tiles and vocabulary segments of this launch: all R tiles with the
@@ -234,8 +235,8 @@ struct FwdPolicy {
                                   int lane, uint8_t* extra, uint32_t rank) {
     const int row = t.m0 + 128 * int(rank) + q * 32 + lane;
     float* cols = reinterpret_cast<float*>(extra + (q + 4 * half) * kColBytes);   // [128 scales][128 biases]
-    // ST: this warp's staging box; the tile's rows go to rows slot * 256 + .. of the buffer
-    uint8_t* wbuf = extra + (q + 4 * half) * kBf16Box64Bytes;
+    // ST: this warp's two staging boxes; the tile's rows go to rows slot * 256 + .. of the buffer
+    uint8_t* wbuf = extra + (q + 4 * half) * 2 * kBf16BoxBytes;
     const bool st_tile = ST && t.slot < p.pu_tiles;
     const int pu_y0 = t.slot * kRows + 128 * int(rank) + q * 32;
     if (!ST && (F8 || p.bias2)) {
@@ -368,13 +369,10 @@ struct FwdPolicy {
         e.found = 1;
       }
       if constexpr (ST) {
-        // warp-uniform; chunks pair up into 64-column boxes (a lone last chunk's
-        // partner columns lie past V and the store drops them); the target
-        // entry is written as 0 (the backward sets it)
-        if (st_tile) {
-          stage_half(wbuf, lane, pk, ch & 1, ty);
-          if ((ch & 1) || ch + 1 == nch) store_box64(&p.tmPu, p.status, wbuf, lane, c0 - (ch & 1) * 32, pu_y0);
-        }
+        // warp-uniform; one 32 x 32 box per chunk through two alternate staging
+        // buffers (columns past V are dropped by the store); the target entry
+        // is written as 0 (the backward sets it)
+        if (st_tile) store_bf16_box(&p.tmPu, p.status, wbuf, e.nbuf, lane, pk, c0, pu_y0, ty);
       }
       if (ch + 1 < nch) tmem_ld32_wait(r);
     }

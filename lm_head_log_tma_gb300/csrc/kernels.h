@@ -53,7 +53,7 @@ struct FwdParams {
   // computed logit's unnormalised probability 2^t (t = logit log2(e) / tau,
   // so p = 2^(t - lse2)) is written as bf16 to row (slot * 256 + row in
   // tile) of the buffer tmPu maps; the target column is written as 0.
-  CUtensorMap tmPu;           // inner V columns, outer pu_tiles * 256 rows; box 64 x 32, 128-byte swizzle
+  CUtensorMap tmPu;           // inner V columns, outer pu_tiles * 256 rows; box 32 x 32, 64-byte swizzle
   int pu_tiles;
   int* status;
   unsigned long long limit_ns;

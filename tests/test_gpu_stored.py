@@ -41,7 +41,7 @@ SPECS = [
     # with a bias, db comes out of dW's GEMM as one more column (k2 in column H of
     # the scaled X rows): inside the last tile's second half (H=256), in a
     # widened last half (H=448, a multiple of the 448-column tile), inside the
-    # last tile's first half (H=1040)
+    # last tile's first half (H=1040, H=512)
     Workload("stored_bias_k3kl", B=4, T=130, H=256, V=777, dtype="bf16", has_bias=True, bias_std=0.3,
              eps_low=0.2, eps_high=0.3, beta=0.04, prompt_len=(5, 40), adv_kind="pm1zero", ref_noise_std=0.1,
              seed=207),
@@ -49,6 +49,8 @@ SPECS = [
              prompt_len=16, seed=208),
     Workload("stored_bias_h1040", B=3, T=100, H=1040, V=1500, dtype="bf16", has_bias=True, bias_std=0.2,
              temperature=0.7, prompt_len=5, seed=209),
+    Workload("stored_bias_h512", B=2, T=160, H=512, V=1100, dtype="bf16", has_bias=True, bias_std=0.2,
+             prompt_len=12, seed=210),
 ]
 
 
