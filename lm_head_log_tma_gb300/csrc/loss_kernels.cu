@@ -56,11 +56,10 @@ __global__ void k3_hist_kernel(const float* __restrict__ H, const uint8_t* __res
   // Warp-aggregated counts: the lanes of a warp that fall in the same bin add
   // once (entropies cluster, so early passes put most tokens in a few bins).
   const int lane = threadIdx.x & 31;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long n = blockIdx.x * (long long)blockDim.x + threadIdx.x; n - lane < N; n += stride) {
+  auto count = [&](bool act, float h) {
     int b0 = -1, b1 = -1;
-    if (n < N && m[n]) {
-      const uint32_t key = f2key(H[n]);
+    if (act) {
+      const uint32_t key = f2key(h);
       const int d = int((key >> shift) & 255u);
       if (pass == 0) {
         b0 = d;
@@ -75,6 +74,39 @@ __global__ void k3_hist_kernel(const float* __restrict__ H, const uint8_t* __res
     if (pass > 0) {
       const unsigned g1 = __match_any_sync(0xffffffffu, b1);
       if (b1 >= 0 && lane == __ffs(g1) - 1) atomicAdd(&sh[b1], unsigned(__popc(g1)));
+    }
+  };
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (((reinterpret_cast<uintptr_t>(H) & 15u) | (reinterpret_cast<uintptr_t>(m) & 3u)) == 0) {
+    // four tokens a thread: one 4-byte mask word and, when any is active, one
+    // 16-byte entropy load (the last, partial group element by element)
+    const long long NG = (N + 3) / 4;
+    for (long long g = tid; g - lane < NG; g += stride) {
+      uint32_t mw = 0;
+      float hv[4] = {0.f, 0.f, 0.f, 0.f};
+      if (g < NG) {
+        if (4 * g + 3 < N) {
+          mw = __ldg(reinterpret_cast<const uint32_t*>(m) + g);
+          if (mw) {
+            const float4 h4 = __ldg(reinterpret_cast<const float4*>(H) + g);
+            hv[0] = h4.x; hv[1] = h4.y; hv[2] = h4.z; hv[3] = h4.w;
+          }
+        } else {
+          for (int k = 0; k < 4; ++k)
+            if (4 * g + k < N && m[4 * g + k]) {
+              mw |= 1u << (8 * k);
+              hv[k] = H[4 * g + k];
+            }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) count(((mw >> (8 * k)) & 255u) != 0u, hv[k]);
+    }
+  } else {
+    for (long long n = tid; n - lane < N; n += stride) {
+      const bool act = n < N && m[n];
+      count(act, act ? H[n] : 0.f);
     }
   }
   __syncthreads();
@@ -124,9 +156,28 @@ __global__ void k3_select_kernel(int pass, K3State* st, const uint32_t* hist, do
 
 __global__ void k3_mask_kernel(const float* __restrict__ H, const uint8_t* __restrict__ m, long long N,
                                const K3State* st, uint8_t* e) {
-  const double thr = st->thr;
-  for (long long n = blockIdx.x * (long long)blockDim.x + threadIdx.x; n < N; n += (long long)gridDim.x * blockDim.x)
-    e[n] = (m[n] && double(H[n]) >= thr) ? 1 : 0;
+  // For a float h, h >= thr exactly when h >= the smallest float >= thr (a
+  // NaN threshold keeps nothing either way), so the test runs in fp32.
+  const float thr = __double2float_ru(st->thr);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (((reinterpret_cast<uintptr_t>(H) & 15u) | (reinterpret_cast<uintptr_t>(m) & 3u) |
+       (reinterpret_cast<uintptr_t>(e) & 3u)) == 0) {
+    const long long NG = N / 4;   // whole groups of four tokens; the rest below
+    for (long long g = tid; g < NG; g += stride) {
+      const uint32_t mw = __ldg(reinterpret_cast<const uint32_t*>(m) + g);
+      uint32_t ew = 0;
+      if (mw) {
+        const float4 h4 = __ldg(reinterpret_cast<const float4*>(H) + g);
+        ew = ((mw & 0xffu) && h4.x >= thr ? 1u : 0u) | ((mw & 0xff00u) && h4.y >= thr ? 1u << 8 : 0u) |
+             ((mw & 0xff0000u) && h4.z >= thr ? 1u << 16 : 0u) | ((mw & 0xff000000u) && h4.w >= thr ? 1u << 24 : 0u);
+      }
+      reinterpret_cast<uint32_t*>(e)[g] = ew;
+    }
+    for (long long n = 4 * NG + tid; n < N; n += stride) e[n] = (m[n] && H[n] >= thr) ? 1 : 0;
+  } else {
+    for (long long n = tid; n < N; n += stride) e[n] = (m[n] && H[n] >= thr) ? 1 : 0;
+  }
 }
 
 cudaError_t launch_entropy_mask(const float* ent, const uint8_t* mask, long long N, double q, void* k3_ws,
