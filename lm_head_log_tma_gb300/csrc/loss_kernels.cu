@@ -53,9 +53,23 @@ __global__ void k3_hist_kernel(const float* __restrict__ H, const uint8_t* __res
     p0 = st->prefix[0];
     p1 = st->prefix[1];
   }
-  // Warp-aggregated counts: the lanes of a warp that fall in the same bin add
-  // once (entropies cluster, so early passes put most tokens in a few bins).
+  // The two order statistics usually share their prefix (adjacent ranks):
+  // then one count serves both halves of the histogram.
+  const bool two = pass > 0 && p0 != p1;
+  // Passes 0 and 1 (sign, exponent, top mantissa bits) put most tokens of a
+  // narrow distribution in a few bins: the lanes of a warp that share a bin
+  // add once.  The low key bytes of passes 2 and 3 are spread over the bins,
+  // where plain shared-memory atomics are cheaper than the grouping.
+  const bool group = pass < 2;
   const int lane = threadIdx.x & 31;
+  auto add = [&](int b) {
+    if (group) {
+      const unsigned g = __match_any_sync(0xffffffffu, b);
+      if (b >= 0 && lane == __ffs(g) - 1) atomicAdd(&sh[b], unsigned(__popc(g)));
+    } else if (b >= 0) {
+      atomicAdd(&sh[b], 1u);
+    }
+  };
   auto count = [&](bool act, float h) {
     int b0 = -1, b1 = -1;
     if (act) {
@@ -66,15 +80,11 @@ __global__ void k3_hist_kernel(const float* __restrict__ H, const uint8_t* __res
       } else {
         const uint32_t hp = key >> (shift + 8);
         if (hp == p0) b0 = d;
-        if (hp == p1) b1 = 256 + d;
+        if (two && hp == p1) b1 = 256 + d;
       }
     }
-    const unsigned g0 = __match_any_sync(0xffffffffu, b0);
-    if (b0 >= 0 && lane == __ffs(g0) - 1) atomicAdd(&sh[b0], unsigned(__popc(g0)));
-    if (pass > 0) {
-      const unsigned g1 = __match_any_sync(0xffffffffu, b1);
-      if (b1 >= 0 && lane == __ffs(g1) - 1) atomicAdd(&sh[b1], unsigned(__popc(g1)));
-    }
+    add(b0);
+    if (two) add(b1);
   };
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -110,8 +120,16 @@ __global__ void k3_hist_kernel(const float* __restrict__ H, const uint8_t* __res
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 512; i += blockDim.x)
-    if (sh[i]) atomicAdd(&hist[i], sh[i]);
+  if (pass > 0 && !two) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+      if (sh[i]) {
+        atomicAdd(&hist[i], sh[i]);
+        atomicAdd(&hist[256 + i], sh[i]);
+      }
+  } else {
+    for (int i = threadIdx.x; i < 512; i += blockDim.x)
+      if (sh[i]) atomicAdd(&hist[i], sh[i]);
+  }
 }
 
 __global__ void k3_select_kernel(int pass, K3State* st, const uint32_t* hist, double q) {
