@@ -277,6 +277,23 @@ __device__ __forceinline__ void block_sum_k(double (&v)[K], double (*sh)[32]) {
   }
 }
 
+// lr = lp - old of two floats, held exactly as hi + lo (two-sum), and the
+// clip test of GMPO decided on it exactly: lr > e holds iff hi > e, or
+// hi == e and lo > 0 (|lo| is at most half an ulp of hi), for a float bound e.
+struct ExactDiff {
+  float hi, lo;
+};
+__device__ __forceinline__ ExactDiff exact_diff(float lp, float old) {
+  const float hi = lp - old;
+  const float bb = hi - lp;
+  return {hi, (lp - (hi - bb)) + (-old - bb)};
+}
+__device__ __forceinline__ bool gmpo_clipped(const ExactDiff& d, double A, float eh, float el) {
+  if (A > 0.0) return d.hi > eh || (d.hi == eh && d.lo > 0.f);
+  if (A < 0.0) return d.hi < el || (d.hi == el && d.lo < 0.f);
+  return false;
+}
+
 __device__ __forceinline__ double logp_at(const LossParams& p, long long n) {
   return p.logp_is_f64 ? __ldcg(static_cast<const double*>(p.logp) + n)
                        : double(static_cast<const float*>(p.logp)[n]);
@@ -493,10 +510,78 @@ __global__ void __launch_bounds__(kLossThreads) loss_partial_kernel(LossParams p
   const double A = seq_adv(p, i);
   const bool gmpo = p.loss_type == RLLOSS_GMPO;
   double a[5] = {0, 0, 0, 0, 0};
+  if (gmpo && !p.logp_is_f64) {
+    // fp32 log-probs: the same terms with the clip test exact in fp32 (two-sum),
+    // integer counts, and the clipped log ratios summed in compensated fp32
+    // (one thread's few hundred tokens) before the fp64 block sums
+    const float* lpf = static_cast<const float*>(p.logp);
+    const float eh = float(p.eps_high), el = float(-p.eps_low);   // the fp32 bounds, exactly
+    int cnt = 0, clips = 0, kept = 0;
+    float sum = 0.f, comp = 0.f, slo = 0.f, nonfin = 0.f;   // nonfin: infinite or NaN terms, as fp64 adds them
+    double kl = 0.0;
+    auto term = [&](long long n, float lp, float old, bool kept_bit) {
+      const ExactDiff d = exact_diff(lp, old);
+      const bool clip = gmpo_clipped(d, A, eh, el);
+      const float x = clip ? (A > 0.0 ? eh : el) : d.hi;
+      if (!isfinite(x)) {
+        nonfin += x;
+      } else {
+        if (!clip) slo += d.lo;
+        const float y = x - comp;   // Kahan
+        const float tt = sum + y;
+        comp = (tt - sum) - y;
+        sum = tt;
+      }
+      ++cnt;
+      clips += clip ? 1 : 0;
+      kept += kept_bit ? 1 : 0;
+      if (p.beta != 0.0) {
+        const double dk = double(p.ref_logp[n]) - double(lp);
+        kl += exp(dk) - dk - 1.0;
+      }
+    };
+    auto scalar = [&](long long n) {
+      if (p.mask[n]) term(n, lpf[n], p.old_logp[n], p.emask ? p.emask[n] != 0 : true);
+    };
+    const long long n0 = base + t0, n1 = base + t1;
+    const bool vec = ((reinterpret_cast<uintptr_t>(lpf) | reinterpret_cast<uintptr_t>(p.old_logp)) & 15u) == 0 &&
+                     ((reinterpret_cast<uintptr_t>(p.mask) | reinterpret_cast<uintptr_t>(p.emask)) & 3u) == 0;
+    if (vec) {
+      // four tokens a thread over the slice's aligned groups; the ends one by one
+      const long long g0 = (n0 + 3) / 4, g1 = n1 / 4;
+      if (g0 < g1) {
+        for (long long n = n0 + threadIdx.x; n < 4 * g0; n += blockDim.x) scalar(n);
+        for (long long n = 4 * g1 + threadIdx.x; n < n1; n += blockDim.x) scalar(n);
+#pragma unroll 2
+        for (long long g = g0 + threadIdx.x; g < g1; g += blockDim.x) {
+          const uint32_t mw = __ldg(reinterpret_cast<const uint32_t*>(p.mask) + g);
+          if (!mw) continue;
+          const uint32_t ew = p.emask ? __ldg(reinterpret_cast<const uint32_t*>(p.emask) + g) : 0x01010101u;
+          const float4 l4 = __ldg(reinterpret_cast<const float4*>(lpf) + g);
+          const float4 o4 = __ldg(reinterpret_cast<const float4*>(p.old_logp) + g);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, ov[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if ((mw >> (8 * k)) & 255u) term(4 * g + k, lv[k], ov[k], ((ew >> (8 * k)) & 255u) != 0u);
+        }
+      } else {
+        for (long long n = n0 + threadIdx.x; n < n1; n += blockDim.x) scalar(n);
+      }
+    } else {
 #pragma unroll 4
-  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
-    const long long n = base + t;
-    token_terms(p, n, logp_at(p, n), A, gmpo, a);
+      for (long long n = n0 + threadIdx.x; n < n1; n += blockDim.x) scalar(n);
+    }
+    a[0] = double(cnt);
+    a[1] = ((double(sum) - double(comp)) + double(slo)) + double(nonfin);
+    a[2] = double(kept);
+    a[3] = kl;
+    a[4] = double(clips);
+  } else {
+#pragma unroll 4
+    for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+      const long long n = base + t;
+      token_terms(p, n, logp_at(p, n), A, gmpo, a);
+    }
   }
   block_sum_k(a, sh);
   if (!publish_slice(p, i, sl, a, &is_last) || threadIdx.x >= 32) return;
@@ -517,6 +602,51 @@ __global__ void loss_coef_kernel(LossParams p) {
   const long long base = (long long)i * p.T;
   const int t0 = int((long long)blockIdx.x * p.T / gridDim.x);
   const int t1 = int((long long)(blockIdx.x + 1) * p.T / gridDim.x);
+  if (gmpo && !p.logp_is_f64 && p.beta == 0.0) {
+    // fp32 log-probs without KL: c_n is the sequence's factor for unclipped
+    // active tokens and 0 otherwise, the clip test exact in fp32 (two-sum)
+    const float* lpf = static_cast<const float*>(p.logp);
+    const float eh = float(p.eps_high), el = float(-p.eps_low);
+    const double A = double(p.adv[i]);
+    const bool live = rec[1] > 0;
+    const float cf = float(rec[9] * p.inv_tau), cd = float(rec[9]);
+    auto one = [&](long long n, bool m, float lp, float old) {
+      return live && m && !gmpo_clipped(exact_diff(lp, old), A, eh, el);
+    };
+    auto scalar = [&](long long n) {
+      const bool on = one(n, p.mask[n] != 0, lpf[n], p.old_logp[n]);
+      if (p.coef) p.coef[n] = on ? cf : 0.f;
+      if (p.dlogp) p.dlogp[n] = on ? cd : 0.f;
+    };
+    const long long n0 = base + t0, n1 = base + t1;
+    const bool vec = ((reinterpret_cast<uintptr_t>(lpf) | reinterpret_cast<uintptr_t>(p.old_logp) |
+                       reinterpret_cast<uintptr_t>(p.coef) | reinterpret_cast<uintptr_t>(p.dlogp)) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(p.mask) & 3u) == 0;
+    const long long g0 = (n0 + 3) / 4, g1 = n1 / 4;
+    if (vec && g0 < g1) {
+      // four tokens a thread over the slice's aligned groups; the ends one by one
+      for (long long n = n0 + threadIdx.x; n < 4 * g0; n += blockDim.x) scalar(n);
+      for (long long n = 4 * g1 + threadIdx.x; n < n1; n += blockDim.x) scalar(n);
+#pragma unroll 2
+      for (long long g = g0 + threadIdx.x; g < g1; g += blockDim.x) {
+        const uint32_t mw = __ldg(reinterpret_cast<const uint32_t*>(p.mask) + g);
+        float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = c4;
+        if (mw && live) {
+          const float4 l4 = __ldg(reinterpret_cast<const float4*>(lpf) + g);
+          const float4 o4 = __ldg(reinterpret_cast<const float4*>(p.old_logp) + g);
+          const bool b0 = one(4 * g, mw & 0xffu, l4.x, o4.x), b1 = one(4 * g + 1, mw & 0xff00u, l4.y, o4.y),
+                     b2 = one(4 * g + 2, mw & 0xff0000u, l4.z, o4.z), b3 = one(4 * g + 3, mw & 0xff000000u, l4.w, o4.w);
+          c4 = make_float4(b0 ? cf : 0.f, b1 ? cf : 0.f, b2 ? cf : 0.f, b3 ? cf : 0.f);
+          d4 = make_float4(b0 ? cd : 0.f, b1 ? cd : 0.f, b2 ? cd : 0.f, b3 ? cd : 0.f);
+        }
+        if (p.coef) reinterpret_cast<float4*>(p.coef)[g] = c4;
+        if (p.dlogp) reinterpret_cast<float4*>(p.dlogp)[g] = d4;
+      }
+    } else {
+      for (long long n = n0 + threadIdx.x; n < n1; n += blockDim.x) scalar(n);
+    }
+    return;
+  }
 #pragma unroll 4
   for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
     const long long n = base + t;
