@@ -698,18 +698,18 @@ int loss_slices(int B, int T, int sms) {
 
 int fused_loss_slices(int T) { return (T + kFusedRows - 1) / kFusedRows; }
 
-// Slices of >= 1024 tokens per sequence for the coefficient kernel, about 16
+// Slices of >= 256 tokens per sequence for the coefficient kernel, about 16
 // blocks per SM over the batch.
 int coef_slices(int B, int T, int sms) {
   long long s = (16ll * sms + B - 1) / B;
-  const long long smax = (T + 1023) / 1024;
+  const long long smax = (T + 255) / 256;
   if (s > smax) s = smax;
   if (s < 1) s = 1;
   return int(s);
 }
 
 static cudaError_t launch_coef(const LossParams& p, cudaStream_t st) {
-  long long s = p.coef_slices > 0 ? p.coef_slices : (p.T + 1023) / 1024;
+  long long s = p.coef_slices > 0 ? p.coef_slices : (p.T + 255) / 256;
   if (s < 1) s = 1;
   loss_coef_kernel<<<dim3(unsigned(s), unsigned(p.B)), 256, 0, st>>>(p);
   return cudaGetLastError();
