@@ -298,7 +298,9 @@ Plan make_plan(const rlloss_cfg* c, PlanMode mode) {
       p.o_coefc = take(size_t(p.Ncap) * 4);
       p.o_lse2c = take(size_t(p.Ncap) * 4);
       p.o_tgtc = take(size_t(p.Ncap) * 8);
-      p.o_xc = take(size_t(p.Ncap) * std::max(p.Kx, p.xs_ld) * 2);
+      // X operand rows of one backward chunk (the recompute gathers each chunk's
+      // kept rows before its launch), or the stored path's scaled rows
+      p.o_xc = take(size_t(rup(std::max(p.Nc, p.pu_tiles * 256), 256)) * std::max(p.Kx, p.xs_ld) * 2);
       p.o_dxc = take(size_t(p.Nc) * p.H * 4);
     }
   }
@@ -793,7 +795,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       cp.coefc = reinterpret_cast<float*>(ws + p.o_coefc);
       cp.lse2c = reinterpret_cast<float*>(ws + p.o_lse2c);
       cp.tgtc = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
-      cp.xc = reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc);
+      cp.xc = nullptr;   // each chunk gathers its own X rows (below)
       cp.errc = err;
       cp.status = status;
       cp.done = done;
@@ -804,13 +806,13 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       }
       RL_TRY(launch_compact(cp, st));
       ph.launched(2);
-      Xb = cp.xc;
+      Xb = ws + p.o_xc;
       tg_b = cp.tgtc;
       lse2_b = cp.lse2c;
       coef_b = cp.coefc;
       cidx = cp.idx;
       dxc = reinterpret_cast<float*>(ws + p.o_dxc);
-      xb_rows = p.Ncap;
+      xb_rows = rup(p.Nc, 256);
     } else {
       RL_TRY(launch_set_total(rows_total, p.N, st));
       ph.launched();
@@ -824,8 +826,15 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     const int nc = std::min(p.Nc, p.N - n0);   // upper bound; the kernels clamp to the kept rows
     const int Rc = int(cdiv(nc, p.rows_tile));
 
+    if (p.compact) {   // this chunk's kept X rows, zeros after them
+      Phase ph(st, 2);
+      RL_TRY(launch_gather_chunk_rows(static_cast<const __nv_bfloat16*>(hd.Xop), p.Kx, cidx, rows_total, n0, nc,
+                                      int(xb_rows), static_cast<__nv_bfloat16*>(const_cast<void*>(Xb)), st));
+      ph.launched();
+    }
     DlParams dp{};
     dp.tmA = tm_xb;
+    dp.a_row0 = p.compact ? 0 : n0;
     dp.tmB = hd.fp.tmB;
     dp.nseg = hd.fp.nseg;
     dp.kb_per_seg = p.kb_dl;
@@ -895,7 +904,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       HProblem& pw = hp.pr[1];
       pw.kb_per_seg = int(cdiv(nc, 64));
       pw.a_outer0 = 0;
-      pw.b_outer0 = n0;
+      pw.b_outer0 = p.compact ? 0 : n0;
       pw.Mt = int(cdiv(p.V, 256));
       pw.Ht = int(cdiv(p.H, 448));
       pw.Hout = p.H;

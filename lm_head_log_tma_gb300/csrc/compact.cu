@@ -71,11 +71,13 @@ __global__ void __launch_bounds__(kCompactBlock) compact_count_kernel(CompactPar
     p.tgtc[r] = -1;
     if (p.errc) p.errc[r] = 0.f;
   }
-  const int words = p.Kx / 8;   // 16-byte words per row
-  const long long tail_words = (long long)(tail_end - total) * words;
-  for (long long w = threadIdx.x; w < tail_words; w += kCompactBlock) {
-    const long long r = total + w / words;
-    reinterpret_cast<uint4*>(p.xc + r * p.Kx)[w % words] = make_uint4(0u, 0u, 0u, 0u);
+  if (p.xc) {
+    const int words = p.Kx / 8;   // 16-byte words per row
+    const long long tail_words = (long long)(tail_end - total) * words;
+    for (long long w = threadIdx.x; w < tail_words; w += kCompactBlock) {
+      const long long r = total + w / words;
+      reinterpret_cast<uint4*>(p.xc + r * p.Kx)[w % words] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 }
 
@@ -104,13 +106,15 @@ __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactPa
     if (threadIdx.x == 0) cnt = __popc(bal);
   }
   __syncthreads();
-  const int base = p.blk_off[g];
-  const int words = p.Kx / 8;
-  const int total_words = cnt * words;
-  for (int w = threadIdx.x; w < total_words; w += kCompactBlock) {
-    const int r = w / words, c = w - r * words;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + size_t(rows[r]) * p.Kx) + c);
-    reinterpret_cast<uint4*>(p.xc + size_t(base + r) * p.Kx)[c] = v;
+  if (p.xc) {
+    const int base = p.blk_off[g];
+    const int words = p.Kx / 8;
+    const int total_words = cnt * words;
+    for (int w = threadIdx.x; w < total_words; w += kCompactBlock) {
+      const int r = w / words, c = w - r * words;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + size_t(rows[r]) * p.Kx) + c);
+      reinterpret_cast<uint4*>(p.xc + size_t(base + r) * p.Kx)[c] = v;
+    }
   }
   if (p.dx_zero) {
     const int r0 = g * kGroup;
@@ -392,6 +396,32 @@ int compact_groups(int N) { return (N + kGroup - 1) / kGroup; }
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t st) {
   compact_count_kernel<<<(p.N + kCompactBlock - 1) / kCompactBlock, kCompactBlock, 0, st>>>(p);
   compact_gather_kernel<<<compact_groups(p.N), kCompactBlock, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+// Rows j < rows of a chunk's X buffer: X row idx[n0 + j] for the chunk's
+// compacted rows (j < clamp(*total - n0, 0, nc)), zeros after them.
+__global__ void __launch_bounds__(kCompactBlock) gather_chunk_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                         int Kx, const int* __restrict__ idx,
+                                                                         const int* total, int n0, int nc, int rows,
+                                                                         __nv_bfloat16* out) {
+  const int kept = min(max(*total - n0, 0), nc);
+  const int words = Kx / 8;   // 16-byte words per row
+  const long long n = (long long)rows * words;
+  for (long long w = blockIdx.x * (long long)blockDim.x + threadIdx.x; w < n; w += (long long)gridDim.x * blockDim.x) {
+    const int j = int(w / words), c = int(w - (long long)j * words);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (j < kept) v = __ldg(reinterpret_cast<const uint4*>(x + size_t(idx[n0 + j]) * Kx) + c);
+    reinterpret_cast<uint4*>(out + size_t(j) * Kx)[c] = v;
+  }
+}
+
+cudaError_t launch_gather_chunk_rows(const __nv_bfloat16* x, int Kx, const int* idx, const int* total, int n0, int nc,
+                                     int rows, __nv_bfloat16* out, cudaStream_t st) {
+  long long blocks = ((long long)rows * (Kx / 8) + kCompactBlock - 1) / kCompactBlock;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  gather_chunk_rows_kernel<<<int(blocks), kCompactBlock, 0, st>>>(x, Kx, idx, total, n0, nc, rows, out);
   return cudaGetLastError();
 }
 

@@ -490,13 +490,13 @@ struct DlPolicy {
 #pragma unroll
       for (int x = 0; x < KBX; ++x) {
         if (tma_x_ok<2>(p.seg_a[s] + kk + 64 * x, p.status))
-          tma_load_2d_pair(&p.tmA, bar, st + x * kBox, p.seg_a[s] + kk + 64 * x, p.n0 + t.m0 + 128 * int(rank));
+          tma_load_2d_pair(&p.tmA, bar, st + x * kBox, p.seg_a[s] + kk + 64 * x, p.a_row0 + t.m0 + 128 * int(rank));
         if (tma_x_ok<2>(p.seg_b[s] + kk + 64 * x, p.status))
           tma_load_2d_pair(&p.tmB, bar, st + kABytes + x * kBox, p.seg_b[s] + kk + 64 * x, t.n0 + 128 * int(rank));
       }
     } else {
       static_assert(KBX == 1, "single-CTA tiles keep one box per operand");
-      if (tma_x_ok<2>(p.seg_a[s] + kk, p.status)) tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, p.n0 + t.m0);
+      if (tma_x_ok<2>(p.seg_a[s] + kk, p.status)) tma_load_2d(&p.tmA, bar, st, p.seg_a[s] + kk, p.a_row0 + t.m0);
       if (tma_x_ok<2>(p.seg_b[s] + kk, p.status)) tma_load_2d(&p.tmB, bar, st + kABytes, p.seg_b[s] + kk, t.n0);
     }
   }

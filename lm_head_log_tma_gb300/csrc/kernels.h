@@ -83,6 +83,7 @@ struct DlParams {
   int nseg, kb_per_seg;
   int seg_a[kMaxSeg], seg_b[kMaxSeg];
   int n0, Nc, Rc, V, Vp, Vt;  // chunk start row, rows in chunk (upper bound), row tiles (128 or 256 rows), vocab, padded vocab, vocab tiles
+  int a_row0;                 // row of tmA holding the chunk's first row (n0, or 0 for a chunk-sized X buffer)
   const int* rows_total;      // device: rows of the backward operands (chunk rows = clamp(*rows_total - n0, 0, Nc))
   float scale2;
   const float* bias2;
@@ -235,7 +236,7 @@ struct CompactParams {
   float* coefc;               // [Ncap]
   float* lse2c;               // [Ncap]
   int64_t* tgtc;              // [Ncap]
-  __nv_bfloat16* xc;          // [Ncap, Kx]
+  __nv_bfloat16* xc;          // optional: [Ncap, Kx] the kept X rows by position (null: not copied)
   float* errc;                // optional: [Ncap] zeroed for kept rows and the tile tail
   int* status;                // device status word (index checks of debug builds)
   float* dx_zero;             // optional: [N, H] gradient buffer the gather sets to zero
@@ -295,6 +296,10 @@ cudaError_t launch_tile_scan(const uint8_t* mask, int N, int tile_rows, uint8_t*
                              unsigned int* ticket, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t st);
 cudaError_t launch_set_total(int* total, int N, cudaStream_t st);
+// out[j] = X row idx[n0 + j] for j < clamp(*total - n0, 0, nc), zero rows after
+// them up to `rows` (a chunk's X operand rows of the recompute).
+cudaError_t launch_gather_chunk_rows(const __nv_bfloat16* x, int Kx, const int* idx, const int* total, int n0, int nc,
+                                     int rows, __nv_bfloat16* out, cudaStream_t st);
 // dst[idx[n0 + j]][:] (+)= src[j][:] for j < clamp(*total - n0, 0, nc_max); H % 4 == 0.
 cudaError_t launch_scatter_rows(const float* src, const int* idx, const int* total, int n0, int nc_max, int H,
                                 float* dst, bool accumulate, cudaStream_t st);
