@@ -795,7 +795,9 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       cp.coefc = reinterpret_cast<float*>(ws + p.o_coefc);
       cp.lse2c = reinterpret_cast<float*>(ws + p.o_lse2c);
       cp.tgtc = reinterpret_cast<int64_t*>(ws + p.o_tgtc);
-      cp.xc = nullptr;   // each chunk gathers its own X rows (below)
+      // one chunk: the compaction copies the kept X rows into the chunk's X
+      // buffer (every position fits it); several: each chunk gathers its own
+      cp.xc = p.nchunks == 1 ? reinterpret_cast<__nv_bfloat16*>(ws + p.o_xc) : nullptr;
       cp.errc = err;
       cp.status = status;
       cp.done = done;
@@ -826,7 +828,7 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     const int nc = std::min(p.Nc, p.N - n0);   // upper bound; the kernels clamp to the kept rows
     const int Rc = int(cdiv(nc, p.rows_tile));
 
-    if (p.compact) {   // this chunk's kept X rows, zeros after them
+    if (p.compact && p.nchunks > 1) {   // this chunk's kept X rows, zeros after them
       Phase ph(st, 2);
       RL_TRY(launch_gather_chunk_rows(static_cast<const __nv_bfloat16*>(hd.Xop), p.Kx, cidx, rows_total, n0, nc,
                                       int(xb_rows), static_cast<__nv_bfloat16*>(const_cast<void*>(Xb)), st));

@@ -318,14 +318,15 @@ __global__ void __launch_bounds__(kCompactBlock) stored_gather_kernel(StoredPara
     long long y = -1;
     if (keep) {
       // G = (c/tau)(onehot - p) with p = pu 2^-lse2: off the target G = k2 pu,
-      // at the target k1 = (c/tau)(1 - p_y), 1 - p_y = -expm1(logp)
+      // at the target k1 = (c/tau)(1 - p_y), 1 - p_y = -expm1(logp).  fp32 (the
+      // values feed bf16 entries and fp32 scales); err = k1 - k2 tv from one
+      // fused multiply-add, exact but for its final rounding
       const float cf = p.coef[n];
       y = p.targets[n];
-      const double k2d = -double(cf) * exp2(-double(p.lse2[n]));
-      const double k1d = double(cf) * -expm1(p.logp64[n]);
-      const __nv_bfloat16 tv = __float2bfloat16_rn(float(k1d / k2d));
-      k2 = float(k2d);
-      er = float(k1d - k2d * double(__bfloat162float(tv)));
+      k2 = -cf * exp2f(-p.lse2[n]);
+      const float k1 = cf * -expm1f(float(p.logp64[n]));
+      const __nv_bfloat16 tv = __float2bfloat16_rn(k1 / k2);
+      er = fmaf(-k2, __bfloat162float(tv), k1);
       p.pu[size_t(j) * p.pu_ld + size_t(y)] = tv;
       p.done[n] = 1;
     }
@@ -399,15 +400,17 @@ cudaError_t launch_compact(const CompactParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Rows j < rows of a chunk's X buffer: X row idx[n0 + j] for the chunk's
-// compacted rows (j < clamp(*total - n0, 0, nc)), zeros after them.
+// A chunk's X buffer: row j = X row idx[n0 + j] for the chunk's compacted rows
+// (j < kept = clamp(*total - n0, 0, nc)), zero rows after them up to a whole
+// 256-row tile (at most `rows`); nothing when the chunk keeps no row.
 __global__ void __launch_bounds__(kCompactBlock) gather_chunk_rows_kernel(const __nv_bfloat16* __restrict__ x,
                                                                          int Kx, const int* __restrict__ idx,
                                                                          const int* total, int n0, int nc, int rows,
                                                                          __nv_bfloat16* out) {
   const int kept = min(max(*total - n0, 0), nc);
+  const int lim = min(rows, (kept + 255) / 256 * 256);   // the recompute reads whole 256-row tiles
   const int words = Kx / 8;   // 16-byte words per row
-  const long long n = (long long)rows * words;
+  const long long n = (long long)lim * words;
   for (long long w = blockIdx.x * (long long)blockDim.x + threadIdx.x; w < n; w += (long long)gridDim.x * blockDim.x) {
     const int j = int(w / words), c = int(w - (long long)j * words);
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -418,8 +421,10 @@ __global__ void __launch_bounds__(kCompactBlock) gather_chunk_rows_kernel(const 
 
 cudaError_t launch_gather_chunk_rows(const __nv_bfloat16* x, int Kx, const int* idx, const int* total, int n0, int nc,
                                      int rows, __nv_bfloat16* out, cudaStream_t st) {
+  // grid-stride over at most 512 blocks: the kept count is known only on the
+  // device, and a chunk without kept rows then costs one short wave
   long long blocks = ((long long)rows * (Kx / 8) + kCompactBlock - 1) / kCompactBlock;
-  if (blocks > 4096) blocks = 4096;
+  if (blocks > 512) blocks = 512;
   if (blocks < 1) blocks = 1;
   gather_chunk_rows_kernel<<<int(blocks), kCompactBlock, 0, st>>>(x, Kx, idx, total, n0, nc, rows, out);
   return cudaGetLastError();

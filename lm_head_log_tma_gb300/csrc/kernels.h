@@ -296,8 +296,9 @@ cudaError_t launch_tile_scan(const uint8_t* mask, int N, int tile_rows, uint8_t*
                              unsigned int* ticket, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t st);
 cudaError_t launch_set_total(int* total, int N, cudaStream_t st);
-// out[j] = X row idx[n0 + j] for j < clamp(*total - n0, 0, nc), zero rows after
-// them up to `rows` (a chunk's X operand rows of the recompute).
+// out[j] = X row idx[n0 + j] for j < kept = clamp(*total - n0, 0, nc), zero rows
+// after them up to a whole 256-row tile, at most `rows` (a chunk's X operand rows
+// of the recompute, which reads whole tiles of its kept rows).
 cudaError_t launch_gather_chunk_rows(const __nv_bfloat16* x, int Kx, const int* idx, const int* total, int n0, int nc,
                                      int rows, __nv_bfloat16* out, cudaStream_t st);
 // dst[idx[n0 + j]][:] (+)= src[j][:] for j < clamp(*total - n0, 0, nc_max); H % 4 == 0.
