@@ -541,10 +541,12 @@ def measure(args, index, dev, world, rank, local):
     ms_step = ms / args.steps
     value = whole_job_rate(N, world, args.steps, ms / 1e3)
 
-    # ---- host time to enqueue one call (plan, tensor maps, launches)
-    torch.cuda.synchronize()
+    # ---- host time to enqueue one call (plan, tensor maps, launches), each
+    # call from an empty queue (back to back, a call of many launches would
+    # fill the launch queue and wait for the GPU instead)
     th = []
     for _ in range(20):
+        torch.cuda.synchronize()
         t0h = time.perf_counter()
         step()
         th.append(time.perf_counter() - t0h)
