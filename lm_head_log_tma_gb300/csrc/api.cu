@@ -753,8 +753,6 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       pw.wide = (p.H % 448 == 0) ? 1 : 0;
     }
     hp.nprob = 2;
-    const int kx = px.kb_per_seg / px.ksplit, kw = pw.kb_per_seg;
-    hp.d_tiles = std::max(1, (kx + kw / 2) / kw);
     hp.rows_total = sp.positions;   // 0: e.g. a clipped GSPO sequence, nothing to add
     hp.n0 = 0;
     hp.nc_max = pu_rows;
@@ -915,8 +913,6 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       pw.reduce = (ch > 0 || acc || p.stored) ? 1 : 0;
       pw.ksplit = 1;
       hp.nprob = 2;
-      const int kx = hp.nseg * px.kb_per_seg / px.ksplit, kw = hp.nseg * pw.kb_per_seg;
-      hp.d_tiles = std::max(1, (kx + kw / 2) / kw);
       hp.rows_total = rows_total;
       hp.n0 = n0;
       hp.nc_max = nc;

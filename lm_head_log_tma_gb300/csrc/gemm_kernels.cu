@@ -692,7 +692,7 @@ struct HPolicy {
   // Pair g of gn: problem 0 units g, g+gn, ...; then problem 1 units.  Pairs
   // that got fewer problem-0 units ("early" pairs) first take problem-1 units
   // [0, F*d) round-robin among themselves, d = problem-0 unit length in
-  // problem-1 units; the rest go round-robin over all pairs.  Consecutive
+  // problem-1 units (by cost); the rest go round-robin over all pairs.  Consecutive
   // units run at the same time, so operand tiles they share stay in L2.
   template <class F>
   __device__ static void for_each_tile(const Params& p, F&& f) {
@@ -704,8 +704,14 @@ struct HPolicy {
       if (!f(tile_of(p, pr[0], 0, u))) return;
     if (p.nprob < 2) return;
     const int T1 = units(pr[1]);
+    // A problem-1 (dW) unit costs its k-blocks plus the drain of its accumulator
+    // (two 224-column subs stored from TMEM with no next k-loop to hide behind),
+    // measured as about kDrainKb k-blocks: d problem-1 units match one problem-0
+    // unit (kDrainKb = 6 against 0: the B=1, T=4096 dX/dW launch 1.095 -> 1.055 ms;
+    // 4 and 8 bracket it).
+    constexpr int kDrainKb = 6;
     const int kx = p.nseg * pr[0].kb_per_seg / pr[0].ksplit, kw = p.nseg * pr[1].kb_per_seg;
-    const int d_tiles = kw > 0 ? max(1, (kx + kw / 2) / kw) : 1;
+    const int d_tiles = kw > 0 ? max(1, (kx + (kw + kDrainKb) / 2) / (kw + kDrainKb)) : 1;
     const int r = T0 % gn;
     const int early = (r == 0) ? 0 : gn - r;
     const int ph1 = min(T1, early * d_tiles);

@@ -135,7 +135,6 @@ struct HParams {
   CUtensorMap tmO[2];         // fp32 output: inner h, outer rows, box 32 x 32, 128-byte swizzle
   HProblem pr[2];             // problem 0 must be the K-major one (a_mn = 0) when both run
   int nprob;                  // 1 or 2
-  int d_tiles;                // problem-0 tile length in problem-1 tiles (host estimate; the kernel recomputes it)
   // Rows of the chunk, read on the device: nc = clamp(*rows_total - n0, 0, nc_max).
   // Problem 0 (dX) has ceil(nc/256) row tiles; problem 1 (dW) ceil(nc/64) k-blocks per term.
   const int* rows_total;
