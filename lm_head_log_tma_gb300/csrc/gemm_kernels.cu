@@ -454,6 +454,7 @@ struct DlPolicy {
   static constexpr int kBBytes = (256 / PAIR) * 128 * KBX;
   static constexpr int kStageBuf = kBf16BoxBytes;  // one 32-row x 32-column bf16 box, 64-byte swizzle
   static constexpr int kExtraSmem = kEpiWarps * 2 * kStageBuf;
+  static_assert(2 * kStageBuf == kBf16Box64Bytes, "a warp's two boxes hold one 32 x 64 bf16 box (bf16 G)");
   static constexpr uint32_t kIdesc = idesc_bf16(kRows, 256, 0, 0);
   using Params = DlParams;
   struct EpiState {
