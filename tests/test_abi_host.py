@@ -57,6 +57,31 @@ def test_stored_probabilities_need_at_most_one_tile_more_and_a_flag_byte_per_row
         assert rc <= st <= rc + 256 * 576 * 2 + 2 * T + 512
 
 
+def test_workspace_grows_only_by_row_state_beyond_the_chunk():
+    """Past the chunk buffer the workspace grows by O(N) row state only, not by
+    O(N*H): doubling a batch whose sequences do not fit a group (T = 32768, one
+    pass) adds at most about 128 bytes per added token, whether the backward
+    stores probabilities or recomputes (each chunk gathers its own X rows)."""
+    for flags in (0, R.FLAG_RECOMPUTE):
+        for H in (896, 4096):
+            small = R.rlloss_workspace_bytes(R.make_cfg(64, 32768, H, 151936, flags=flags))
+            big = R.rlloss_workspace_bytes(R.make_cfg(128, 32768, H, 151936, flags=flags))
+            added = 64 * 32768
+            assert 0 < big - small <= 128 * added, (flags, H, (big - small) / added)
+
+
+def test_small_chunks_bound_the_workspace():
+    """RLLOSS_FLAG_RECOMPUTE with 256-row chunks keeps the workspace below the
+    pages' fused-path peaks at every shape of the GMPO page's H100 memory
+    comparison (1.34-29.44 GiB), and the default stays within a few GiB."""
+    gib = 2 ** 30
+    for B, T in ((1, 512), (8, 2048), (16, 4096), (2, 32768), (128, 32768)):
+        cfg = R.make_cfg(B, T, 896, 151936, flags=R.FLAG_RECOMPUTE)
+        cfg.chunk_rows = 256
+        assert R.rlloss_workspace_bytes(cfg) < 0.6 * gib, (B, T)
+        assert R.rlloss_workspace_bytes(R.make_cfg(B, T, 896, 151936)) < 3.5 * gib, (B, T)
+
+
 class _Null:
     def data_ptr(self):
         return 0
