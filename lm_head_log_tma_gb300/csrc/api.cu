@@ -724,9 +724,13 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
     hp.row_map = sp.rows;
     if (!tmap_bf16(&hp.tmA[0], pu, p.V, pu_rows, p.ld_dl, 128)) return RLLOSS_ECUDA;
     if (!tmap_bf16(&hp.tmB[0], hd.Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
+    if (!tmap_bf16_box(&hp.tmB48[0], hd.Wop, p.Kx, p.V, p.Kx, 48, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      return RLLOSS_ECUDA;
     if (!tmap_f32_out(&hp.tmO[0], dX, p.H, p.N)) return RLLOSS_ECUDA;   // unused: rows go through dx_idx
     if (!tmap_bf16(&hp.tmA[1], pu, p.V, pu_rows, p.ld_dl, 64)) return RLLOSS_ECUDA;
     if (!tmap_bf16(&hp.tmB[1], sp.xs, p.H + (p.bias ? 1 : 0), pu_rows, p.xs_ld, 64)) return RLLOSS_ECUDA;
+    if (!tmap_bf16_box(&hp.tmB48[1], sp.xs, p.H + (p.bias ? 1 : 0), pu_rows, p.xs_ld, 48, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      return RLLOSS_ECUDA;
     if (!tmap_f32_out(&hp.tmO[1], dW, p.H, p.V)) return RLLOSS_ECUDA;
     HProblem& px = hp.pr[0];
     px.kb_per_seg = int(cdiv(p.V, 64));
@@ -881,9 +885,13 @@ int run_backward(const rlloss_cfg* cfg, const Plan& p, const Head& hd, const int
       const long long g_inner = p.fp32 ? 2ll * p.Vp : p.V;
       if (!tmap_bf16(&hp.tmA[0], dl, g_inner, nc, p.ld_dl, 128)) return RLLOSS_ECUDA;
       if (!tmap_bf16(&hp.tmB[0], hd.Wop, p.Kx, p.V, p.Kx, 64)) return RLLOSS_ECUDA;
+      if (!tmap_bf16_box(&hp.tmB48[0], hd.Wop, p.Kx, p.V, p.Kx, 48, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return RLLOSS_ECUDA;
       if (!tmap_f32_out(&hp.tmO[0], dx_out, p.H, nc)) return RLLOSS_ECUDA;
       if (!tmap_bf16(&hp.tmA[1], dl, g_inner, nc, p.ld_dl, 64)) return RLLOSS_ECUDA;
       if (!tmap_bf16(&hp.tmB[1], Xb, p.Kx, xb_rows, p.Kx, 64)) return RLLOSS_ECUDA;
+      if (!tmap_bf16_box(&hp.tmB48[1], Xb, p.Kx, xb_rows, p.Kx, 48, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return RLLOSS_ECUDA;
       if (!tmap_f32_out(&hp.tmO[1], dW, p.H, p.V)) return RLLOSS_ECUDA;
       HProblem& px = hp.pr[0];
       px.kb_per_seg = int(cdiv(p.V, 64));

@@ -648,6 +648,7 @@ struct HPolicy {
     for (int q = 0; q < p.nprob; ++q) {
       tma_prefetch_desc(&p.tmA[q]);
       tma_prefetch_desc(&p.tmB[q]);
+      tma_prefetch_desc(&p.tmB48[q]);
       tma_prefetch_desc(&p.tmO[q]);
     }
   }
@@ -725,7 +726,9 @@ struct HPolicy {
   // Columns of sub `sub` of tile t: 224, or 240 for the widened last sub.
   __device__ static int sub_n(const TileInfo& t, int sub) { return (t.wide && sub == 1) ? kNS + 16 : kNS; }
   // One k-block: this CTA's 128 A rows and, for each sub, its half of the B
-  // rows (two 64-h runs; 112 of them used, 120 in a widened sub).
+  // rows: a 64-h run and the next 48 (a 48-wide box lands where the first 48
+  // columns of a 64-wide one would, the rest of that run untouched and unread),
+  // or two 64-h runs for the 120 of a widened sub.
   __device__ static void load(const Params& p, uint8_t* st, uint32_t bar, const TileInfo& t, int kb, uint32_t rank) {
     const int q = t.seg;
     const HProblem& pr = p.pr[q];
@@ -747,8 +750,14 @@ struct HPolicy {
       const int h = p.seg_b[s] + t.n0 + kNS * sub + (sub_n(t, sub) / 2) * int(rank);
       uint8_t* b = st + kABytes + sub * kBSub;
       if (tma_x_ok<2>(h, p.status)) tma_load_2d_pair(&p.tmB[q], bar, b, h, pr.b_outer0 + kk);
-      if (tma_x_ok<2>(h + 64, p.status)) tma_load_2d_pair(&p.tmB[q], bar, b + 8192, h + 64, pr.b_outer0 + kk);
+      const CUtensorMap* m2 = sub_n(t, sub) == kNS ? &p.tmB48[q] : &p.tmB[q];
+      if (tma_x_ok<2>(h + 64, p.status)) tma_load_2d_pair(m2, bar, b + 8192, h + 64, pr.b_outer0 + kk);
     }
+  }
+  // Bytes one CTA's copies of a sub's B rows bring: 64 + 48 columns, or 64 + 64
+  // in a widened sub.
+  __device__ static uint32_t b_sub_bytes(const TileInfo& t, int sub) {
+    return sub_n(t, sub) == kNS ? 8192u + 6144u : 16384u;
   }
   __device__ static uint64_t adesc(uint32_t sa, int k, const TileInfo& t) {
     return t.seg == 1 ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
@@ -760,7 +769,9 @@ struct HPolicy {
     if (sub_n(t, sub) == kNS) return t.seg == 1 ? idesc_bf16(256, kNS, 1, 1) : idesc_bf16(256, kNS, 0, 1);
     return t.seg == 1 ? idesc_bf16(256, kNS + 16, 1, 1) : idesc_bf16(256, kNS + 16, 0, 1);
   }
-  __device__ static uint32_t tx_bytes(const Params&, const TileInfo&) { return kABytes + kBBytes; }
+  __device__ static uint32_t tx_bytes(const Params&, const TileInfo& t) {
+    return kABytes + b_sub_bytes(t, 0) + b_sub_bytes(t, 1);
+  }
   __device__ static void mma(const Params&, uint32_t d, uint32_t sa, int k, const TileInfo& t, int sub,
                              uint32_t accum) {
     umma_bf16_pair(d, adesc(sa, k, t), bdesc(sa, k, sub), idesc(t, sub), accum);

@@ -132,6 +132,8 @@ struct HParams {
   // tile.  row_map covers every block a tile can reach.
   const int* row_map;
   CUtensorMap tmB[2];         // inner h, outer k, box 64 x 64
+  CUtensorMap tmB48[2];       // the same maps with box 48 x 64: the last 48 columns of a CTA's
+                              // 112 of a sub, placed as in a 64-column box (the rest untouched)
   CUtensorMap tmO[2];         // fp32 output: inner h, outer rows, box 32 x 32, 128-byte swizzle
   HProblem pr[2];             // problem 0 must be the K-major one (a_mn = 0) when both run
   int nprob;                  // 1 or 2
